@@ -1,0 +1,126 @@
+"""Plain fp64 CPU oracle for causal log-linear Mamba-2 attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the product path
+(the ``log_linear_attention_gb300`` package and its CUDA library) never does.
+
+The arithmetic lives in ``lla_oracle.c`` (single-threaded, fp64, written as
+the definition reads); this module only compiles it with gcc and marshals
+numpy arrays through ctypes. Sources: "Log-Linear Attention" (gist.science
+summaries of arXiv 2506.04761), §2 of the Portuguese and French pages
+(Fenwick partition, hierarchical mask M_H, recurrent and chunkwise forms).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lla_oracle.c")
+_LIB = os.path.join(_HERE, "liblla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``lla_oracle.c`` into ``liblla_oracle.so`` next to it."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            lib.lla_oracle_level.argtypes = [ctypes.c_int64, ctypes.c_int64]
+            lib.lla_oracle_level.restype = ctypes.c_int
+            lib.lla_oracle_num_levels.argtypes = [ctypes.c_int64]
+            lib.lla_oracle_num_levels.restype = ctypes.c_int
+            lib.lla_oracle_explicit.argtypes = [dp] * 6 + [ctypes.c_int] * 6
+            lib.lla_oracle_explicit.restype = None
+            lib.lla_oracle_recurrent.argtypes = [dp] * 6 + [ctypes.c_int] * 6
+            lib.lla_oracle_recurrent.restype = ctypes.c_int
+            lib.lla_oracle_decode_step.argtypes = [dp] * 6 + [i64p, dp] + [ctypes.c_int] * 5
+            lib.lla_oracle_decode_step.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def level(t: int, s: int) -> int:
+    """Fenwick level of key ``s`` for query ``t`` (-1 if ``s > t``)."""
+    return int(_load().lla_oracle_level(int(t), int(s)))
+
+
+def num_levels(T: int) -> int:
+    """Number of Fenwick levels reached by a length-``T`` sequence (enumerated)."""
+    return int(_load().lla_oracle_num_levels(int(T)))
+
+
+def _check_forward(q, k, v, log_a, lam):
+    q, k, v, log_a, lam = (_f64(x) for x in (q, k, v, log_a, lam))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    L = lam.shape[-1]
+    assert k.shape == (B, H, T, dk) and v.shape == (B, H, T, dv)
+    assert log_a.shape == (B, H, T) and lam.shape == (B, H, T, L)
+    return q, k, v, log_a, lam, (B, H, T, dk, dv, L)
+
+
+def explicit(q, k, v, log_a, lam) -> np.ndarray:
+    """O(T^2) explicit-mask form: (Q K^T (.) M^S (.) M^H) V, fp64."""
+    q, k, v, log_a, lam, (B, H, T, dk, dv, L) = _check_forward(q, k, v, log_a, lam)
+    out = np.zeros((B, H, T, dv), dtype=np.float64)
+    _load().lla_oracle_explicit(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
+                                B, H, T, dk, dv, L)
+    return out
+
+
+def recurrent(q, k, v, log_a, lam) -> np.ndarray:
+    """Token-by-token Fenwick recurrence with lowbit-carry merges, fp64."""
+    q, k, v, log_a, lam, (B, H, T, dk, dv, L) = _check_forward(q, k, v, log_a, lam)
+    out = np.zeros((B, H, T, dv), dtype=np.float64)
+    rc = _load().lla_oracle_recurrent(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
+                                      B, H, T, dk, dv, L)
+    if rc != 0:
+        raise MemoryError("oracle state allocation failed")
+    return out
+
+
+def decode_step(q, k, v, log_a, lam, states, t):
+    """One recurrent decode step for a batch, fp64.
+
+    ``states`` [B,H,Lmax,dk,dv] is updated in place (it must be a C-contiguous
+    float64 array); returns ``out`` [B,H,dv]."""
+    q, k, v, log_a, lam = (_f64(x) for x in (q, k, v, log_a, lam))
+    assert isinstance(states, np.ndarray) and states.dtype == np.float64 and states.flags.c_contiguous
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.int64))
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    Lmax = states.shape[2]
+    assert states.shape == (B, H, Lmax, dk, dv) and lam.shape == (B, H, Lmax) and t.shape == (B,)
+    out = np.zeros((B, H, dv), dtype=np.float64)
+    rc = _load().lla_oracle_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(states),
+                                        t.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _ptr(out),
+                                        B, H, dk, dv, Lmax)
+    if rc != 0:
+        raise ValueError("decode position needs more levels than the state set holds")
+    return out

@@ -1,0 +1,215 @@
+/*
+ * Plain CPU oracle for the causal log-linear Mamba-2 attention operator.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it. It shares no code with the CUDA library.
+ *
+ * Everything is fp64, single-threaded, and written as the definition reads,
+ * without blocking, fusion or reordering.
+ *
+ * Sources ("Log-Linear Attention", gist.science summaries of arXiv 2506.04761,
+ * pages in Portuguese (pt) and French (fr)):
+ *   - pt §2 "Particionamento Hierarquico (Arvore Fenwick)" and fr §2
+ *     "Partitionnement par Arbre de Fenwick": the prefix of each query is cut
+ *     into Fenwick-tree buckets of sizes 1, 2, 4, 8, ...; O(log T) of them are
+ *     active at any time t.
+ *   - pt §2 "Mascara Hierarquica (M_H)" and fr §2 "Matrice de Masque
+ *     Hierarchique": O = (Q K^T (.) M_H) V, with one data-dependent weight
+ *     lambda_t^(l) per level l of query t.
+ *   - pt §2 "Generalizacao" and fr §3 "Cadre General": the hierarchical mask
+ *     is applied on top of a linear-attention variant's own mask; for Mamba-2
+ *     that is the semiseparable scalar-decay mask M^S.
+ *   - pt §2 "Forma Recorrente e Paralela" and fr §2 "Algorithmes Efficaces"
+ *     (Inference): the decode keeps O(log T) states S_t^(l); each new token
+ *     updates the finest level and the levels are merged along the Fenwick
+ *     structure.
+ *
+ * Readings taken where the pages are silent:
+ *   - positions are 0-indexed; the query token itself is its own level 0;
+ *   - M^S[t,s] = prod_{r=s+1..t} a_r (exclusive of s, so the diagonal is 1);
+ *   - lambda is indexed by the query: lambda[b,h,t,l];
+ *   - no 1/sqrt(d) scale, no normalisation, no gating beyond M^S.
+ *
+ * Layouts are row-major: q,k [B,H,T,dk]; v,out [B,H,T,dv]; log_a [B,H,T];
+ * lambda [B,H,T,L]. Decode: q,k [B,H,dk]; v,out [B,H,dv]; log_a [B,H];
+ * lambda [B,H,Lmax]; states [B,H,Lmax,dk,dv]; t [B].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Fenwick bucket of key s for query t (s <= t), found by walking the Fenwick
+ * decomposition of t's prefix: the query token alone is level 0; then, from
+ * b = t, the bucket [b - lowbit(b), b) holds 2^(l-1) keys and has level
+ * l = log2(lowbit(b)) + 1, and b steps down to b - lowbit(b). Returns -1 when
+ * s > t (the key is in the future). */
+int lla_oracle_level(int64_t t, int64_t s)
+{
+    if (s > t || s < 0) return -1;
+    if (s == t) return 0;
+    int64_t b = t;
+    while (b > 0) {
+        int64_t low = b & (-b);
+        int level = 1;
+        for (int64_t w = low; w > 1; w >>= 1) level++;
+        if (s >= b - low && s < b) return level;
+        b -= low;
+    }
+    return -1; /* unreachable for 0 <= s < t */
+}
+
+/* Number of Fenwick levels for a sequence of length T: the largest level any
+ * (t, s) pair reaches, plus one, found by enumeration. */
+int lla_oracle_num_levels(int64_t T)
+{
+    int best = 0;
+    for (int64_t t = 0; t < T; t++)
+        for (int64_t s = 0; s <= t; s++) {
+            int l = lla_oracle_level(t, s);
+            if (l > best) best = l;
+        }
+    return T > 0 ? best + 1 : 0;
+}
+
+/* Explicit O(T^2) form: for every query t,
+ *   o_t = sum_{s<=t} lambda_t^(l(t,s)) * exp(sum_{r=s+1..t} log_a_r) * (q_t . k_s) * v_s,
+ * i.e. row t of (Q K^T (.) M^S (.) M^H) V. The decay exponent is accumulated
+ * while s walks down from t, so it is the plain sum over r in (s, t]. */
+void lla_oracle_explicit(const double* q, const double* k, const double* v,
+                         const double* log_a, const double* lambda, double* out,
+                         int B, int H, int T, int dk, int dv, int L)
+{
+    for (int bh = 0; bh < B * H; bh++) {
+        const double* qh = q + (size_t)bh * T * dk;
+        const double* kh = k + (size_t)bh * T * dk;
+        const double* vh = v + (size_t)bh * T * dv;
+        const double* ah = log_a + (size_t)bh * T;
+        const double* lh = lambda + (size_t)bh * T * L;
+        double* oh = out + (size_t)bh * T * dv;
+        for (int t = 0; t < T; t++) {
+            double* o = oh + (size_t)t * dv;
+            for (int j = 0; j < dv; j++) o[j] = 0.0;
+            double decay_exp = 0.0; /* sum of log_a over (s, t] */
+            for (int s = t; s >= 0; s--) {
+                int l = lla_oracle_level(t, s);
+                double qk = 0.0;
+                for (int i = 0; i < dk; i++) qk += qh[(size_t)t * dk + i] * kh[(size_t)s * dk + i];
+                double w = lh[(size_t)t * L + l] * exp(decay_exp) * qk;
+                for (int j = 0; j < dv; j++) o[j] += w * vh[(size_t)s * dv + j];
+                decay_exp += ah[s];
+            }
+        }
+    }
+}
+
+/* Lowest set bit position of t > 0. */
+static int trailing_zeros(int64_t t)
+{
+    int c = 0;
+    while (((t >> c) & 1) == 0) c++;
+    return c;
+}
+
+/* Is level l of the state set held after token u nonempty? Level 0 is the
+ * token u itself; level l >= 1 is nonempty exactly when bit l-1 of u is set
+ * (the Fenwick bucket of that size exists in u's prefix). */
+static int level_nonempty(int64_t u, int l)
+{
+    if (l == 0) return 1;
+    return (int)((u >> (l - 1)) & 1);
+}
+
+/* One recurrent step on one head's state set, in place.
+ * On entry `S` (Lmax matrices dk x dv) holds, for query t-1, each Fenwick
+ * bucket's keys summed as exp(decay to t-1) k_s v_s^T; levels empty for t-1
+ * are not read. On exit it holds the same for query t, and o = sum_l
+ * lambda^(l) S^(l)^T q. For t > 0 with c = ctz(t): every held bucket is
+ * decayed by a_t; buckets 0..c (together the 2^c keys t-2^c .. t-1) merge
+ * into level c+1 and levels 1..c become empty (set to zero here); the new
+ * token's k v^T becomes level 0. */
+static void recurrent_step(double* S, const double* qt, const double* kt, const double* vt,
+                           double log_a_t, const double* lam, int64_t t,
+                           int dk, int dv, int Lmax, double* o)
+{
+    size_t msz = (size_t)dk * dv;
+    if (t > 0) {
+        int c = trailing_zeros(t);
+        double a = exp(log_a_t);
+        /* decay every bucket held for query t-1 */
+        for (int l = 0; l < Lmax; l++) {
+            if (!level_nonempty(t - 1, l)) continue;
+            for (size_t e = 0; e < msz; e++) S[l * msz + e] *= a;
+        }
+        /* merge levels 0..c into level c+1 (level c+1 is empty for t-1) */
+        double* dst = S + (size_t)(c + 1) * msz;
+        for (size_t e = 0; e < msz; e++) dst[e] = 0.0;
+        for (int l = 0; l <= c; l++) {
+            for (size_t e = 0; e < msz; e++) dst[e] += S[l * msz + e];
+            if (l > 0)
+                for (size_t e = 0; e < msz; e++) S[l * msz + e] = 0.0;
+        }
+    }
+    /* the new token is level 0 */
+    for (int i = 0; i < dk; i++)
+        for (int j = 0; j < dv; j++) S[(size_t)i * dv + j] = kt[i] * vt[j];
+    /* read every nonempty level with its lambda */
+    for (int j = 0; j < dv; j++) o[j] = 0.0;
+    for (int l = 0; l < Lmax; l++) {
+        if (!level_nonempty(t, l)) continue;
+        const double* Sl = S + (size_t)l * msz;
+        for (int j = 0; j < dv; j++) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; i++) acc += qt[i] * Sl[(size_t)i * dv + j];
+            o[j] += lam[l] * acc;
+        }
+    }
+}
+
+/* Recurrent form over whole sequences: one state set per head, stepped token
+ * by token with the lowbit-carry merge of recurrent_step. Independent of the
+ * explicit form: it never evaluates l(t,s) or a pairwise decay. */
+int lla_oracle_recurrent(const double* q, const double* k, const double* v,
+                         const double* log_a, const double* lambda, double* out,
+                         int B, int H, int T, int dk, int dv, int L)
+{
+    int Lmax = L; /* for t < T every merge target and every read level is < L */
+    size_t msz = (size_t)dk * dv;
+    double* S = (double*)calloc((size_t)Lmax * msz, sizeof(double));
+    if (!S) return -1;
+    for (int bh = 0; bh < B * H; bh++) {
+        memset(S, 0, (size_t)Lmax * msz * sizeof(double));
+        for (int t = 0; t < T; t++) {
+            size_t r = (size_t)bh * T + t;
+            recurrent_step(S, q + r * dk, k + r * dk, v + r * dv, log_a[r],
+                           lambda + r * L, t, dk, dv, Lmax, out + r * dv);
+        }
+    }
+    free(S);
+    return 0;
+}
+
+/* One decode step for a batch: the same recurrent step applied to each
+ * (b, h) state set at its sequence position t[b]. Returns -1 if a position
+ * needs more levels than Lmax holds. */
+int lla_oracle_decode_step(const double* q, const double* k, const double* v,
+                           const double* log_a, const double* lambda, double* states,
+                           const int64_t* t, double* out,
+                           int B, int H, int dk, int dv, int Lmax)
+{
+    size_t msz = (size_t)dk * dv;
+    for (int b = 0; b < B; b++) {
+        int64_t tb = t[b];
+        if (tb < 0) return -1;
+        int need = 1;
+        for (int64_t x = tb; x > 0; x >>= 1) need++;
+        if (need > Lmax) return -1;
+        for (int h = 0; h < H; h++) {
+            size_t bh = (size_t)b * H + h;
+            recurrent_step(states + bh * Lmax * msz, q + bh * dk, k + bh * dk, v + bh * dv,
+                           log_a[bh], lambda + bh * Lmax, tb, dk, dv, Lmax, out + bh * dv);
+        }
+    }
+    return 0;
+}
