@@ -1,0 +1,486 @@
+#!/usr/bin/env python
+"""Benchmark of causal log-linear Mamba-2 attention on one GB300 per rank.
+
+One step = one lla_forward over the mid-size prefill workload (B=4, H=16,
+T=8192, dk=128, dv=64, bf16 q/k/v, chunk 64), inputs resident in HBM (434 MB,
+larger than L2, so no flush between steps). The same run also times the
+recurrent decode workload (64 sequences x 16 heads, t ~ U[1, 65536), 1000
+one-token steps) and reports its HBM bandwidth. Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lla|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from log_linear_attention_gb300 import inputs  # noqa: E402
+
+METRIC = "log-linear attn fwd tokens/s & TFLOP/s vs bf16 peak @T=8192; decode GB/s vs HBM"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (maximum SM clock)
+ALU_F32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+# ----------------------------------------------------------------------------- work model
+
+def popcount_sum(n: int) -> int:
+    return sum(bin(j).count("1") for j in range(n))
+
+
+def prefill_work(cfg: inputs.PrefillConfig) -> dict:
+    """Algorithmic flops and minimum bytes of one prefill call: causal pairs only,
+    nonempty Fenwick levels only, each input read once and the output written once."""
+    BH = cfg.B * cfg.H
+    C, dk, dv, T = cfg.chunk, cfg.dk, cfg.dv, cfg.T
+    N = T // C
+    esz = 2 if cfg.dtype == "bf16" else 4
+    intra = BH * N * C * (C + 1) // 2 * 2 * (dk + dv)
+    state = BH * N * 2 * C * dk * dv
+    level = BH * popcount_sum(N) * 2 * C * dk * dv
+    in_bytes = BH * T * (2 * dk + dv) * esz + BH * T * 4 + BH * T * cfg.L * 4
+    out_bytes = BH * T * dv * esz
+    return dict(intra=intra, state=state, level=level, flops=intra + state + level,
+                in_bytes=in_bytes, out_bytes=out_bytes, bytes=in_bytes + out_bytes)
+
+
+def kernel_work(name: str, cfg: inputs.PrefillConfig) -> dict:
+    """Per-launch algorithmic work of each kernel the forward launches, and its bound."""
+    w = prefill_work(cfg)
+    BH = cfg.B * cfg.H
+    T, dk, dv = cfg.T, cfg.dk, cfg.dv
+    esz = 2 if cfg.dtype == "bf16" else 4
+    q_b = BH * T * dk * esz
+    k_b = BH * T * dk * esz
+    v_b = BH * T * dv * esz
+    a_b = BH * T * 4
+    lam_b = BH * T * cfg.L * 4
+    if name == "simt_output":
+        return dict(bound="alu", flops=w["intra"] + w["level"],
+                    bytes=q_b + k_b + v_b + a_b + lam_b + w["out_bytes"])
+    if name == "simt_chunk_state":
+        return dict(bound="alu", flops=w["state"], bytes=k_b + v_b + a_b + BH * (T // cfg.chunk) * dk * dv * 4)
+    if name == "tc_output":
+        return dict(bound="hbm", flops=w["intra"] + w["level"],
+                    bytes=q_b + k_b + v_b + a_b + lam_b + w["out_bytes"])
+    if name == "tc_nodes":
+        return dict(bound="hbm", flops=w["state"], bytes=k_b + v_b + a_b)
+    return dict(bound="hbm", flops=0, bytes=a_b)
+
+
+def decode_bytes(t: np.ndarray, H: int, dk: int, dv: int, Lmax: int, esz: int = 2) -> int:
+    """Bytes one decode step must move: every nonempty state level read once
+    (popcount(t-1) + 1 of them) and every level held after the step written once
+    (popcount(t) + 1), fp32; plus the token vectors, lambda, log_a and the output."""
+    total = 0
+    for x in t.tolist():
+        reads = (bin(x - 1).count("1") + 1) if x > 0 else 0
+        writes = bin(x).count("1") + 1
+        total += H * 4 * dk * dv * (reads + writes)
+    total += len(t) * H * ((2 * dk + dv) * esz + 4 + Lmax * 4 + dv * esz) + len(t) * 8
+    return total
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS,
+                 bf16_tflops_sustained=1700.0, source="fallback")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k_, v_ in x.items():
+                        walk(v_, f"{pre}{k_}.")
+                else:
+                    flat[pre[:-1]] = x
+            walk(d)
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                for fk, fv in flat.items():
+                    if fk.split(".")[-1] == key and isinstance(fv, (int, float)):
+                        peaks[key] = float(fv)
+            peaks["source"] = "measured"
+        except Exception:
+            pass
+    return peaks
+
+
+def traffic_record(name: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's source
+    has not changed since the counters were taken; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(name)
+        if not rec:
+            return None
+        src = os.path.join(ROOT, rec["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if sha != rec["source_sha256"]:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        time.sleep(0.15)
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [l for (ts, l) in self.lines if self.t0 is not None and self.t0 <= ts <= (self.t1 or ts)]
+        adjacent = False
+        if not inside and self.lines:
+            # region shorter than the sampling period: take the samples nearest to it
+            mid = ((self.t0 or 0) + (self.t1 or 0)) / 2
+            inside = [l for _, l in sorted(self.lines, key=lambda x: abs(x[0] - mid))[:3]]
+            adjacent = True
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in inside:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[5:9]):
+                if p.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "adjacent_samples": adjacent}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle (CPU baseline)
+
+def oracle_tokens_per_s(cfg: inputs.PrefillConfig, inp: inputs.PrefillInputs, budget_s: float, T_sample=None):
+    """Time the fp64 oracle (recurrent form, one core) on whole heads of the workload
+    until ``budget_s`` elapses; returns (tokens/s in whole-token units, sample text)."""
+    import oracle
+    T = cfg.T if T_sample is None else T_sample
+    heads = 0
+    t0 = time.perf_counter()
+    for bh in range(cfg.B * cfg.H):
+        b, h = divmod(bh, cfg.H)
+        sl = (slice(b, b + 1), slice(h, h + 1), slice(0, T))
+        lam = inp.lam[sl][..., :inputs.num_levels(T)]
+        oracle.recurrent(inp.q[sl], inp.k[sl], inp.v[sl], inp.log_a[sl], lam)
+        heads += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    tokens = heads * T / cfg.H  # a token of the workload carries all H heads
+    return tokens / dt, f"{heads} of {cfg.B * cfg.H} heads x {T} tokens (recurrent form), scaled by 1/H", dt
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = inputs.make_prefill(cfg, seed=0, B=1, H=1)
+    one = inputs.PrefillConfig(**{**cfg.__dict__, "B": 1, "H": 1})
+    # size each step so that warmup + steps end within about two minutes
+    est_per_token = 2.5e-4
+    T_sample = cfg.T
+    while T_sample > 1024 and (args.steps + args.warmup) * T_sample * est_per_token > 120:
+        T_sample //= 2
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(one, inp, 0.0, T_sample)
+    times = []
+    for _ in range(args.steps):
+        _, sample, dt = oracle_tokens_per_s(one, inp, 0.0, T_sample)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = (T_sample / cfg.H) / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "T": cfg.T, "dk": cfg.dk, "dv": cfg.dv,
+                   "chunk": cfg.chunk},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: 1 head x {T_sample} tokens of the workload (recurrent form, fp64), "
+                                   f"scaled by 1/H"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def cuda_time(fn, steps, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def run_lla(args, cfg):
+    import torch
+    from log_linear_attention_gb300 import binding
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    # ---- inputs (per-rank seed: every rank runs the full workload: weak scaling)
+    inp = inputs.make_prefill(cfg, seed=rank)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    host = [bf16(inp.bits["q"]), bf16(inp.bits["k"]), bf16(inp.bits["v"]),
+            torch.from_numpy(inp.log_a), torch.from_numpy(inp.lam)]
+    host = [h.pin_memory() for h in host]
+    dq, dk_, dv_, da, dl = (h.to(dev) for h in host)
+    out = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.bfloat16, device=dev)
+    work = prefill_work(cfg)
+
+    def step():
+        binding.forward(dq, dk_, dv_, da, dl, cfg.chunk, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    assert binding.device_error() == 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.mark("start")
+    ms_total = cuda_time(step, args.steps, stream)
+    clocks.mark("end")
+    clk = clocks.stop()
+    ms_total = max_over_ranks(ms_total, ws)
+    ms = ms_total / args.steps
+    tokens_per_s = ws * cfg.tokens / (ms / 1e3)
+    tflops = work["flops"] / (ms / 1e3) / 1e12
+
+    # ---- per-kernel device times (CUDA events recorded by the library between its launches)
+    per_kernel = {}
+    nprof = max(3, min(args.steps, 20))
+    launches_per_step = 0
+    for _ in range(nprof):
+        rec = binding.forward_profile(dq, dk_, dv_, da, dl, cfg.chunk, out)
+        launches_per_step = len(rec)
+        for name, kms in rec:
+            per_kernel.setdefault(name, []).append(kms)
+    kavg = {n: sum(v) / len(v) for n, v in per_kernel.items()}
+    top = max(kavg, key=kavg.get)
+    kw = kernel_work(top, cfg)
+    t_top = kavg[top] / 1e3
+    if kw["bound"] == "hbm":
+        achieved, peak, unit = kw["bytes"] / t_top / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif kw["bound"] == "tensor":
+        achieved, peak, unit = kw["flops"] / t_top / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = kw["flops"] / t_top / 1e12, ALU_F32_TFLOPS, "TFLOP/s"
+    roofline = {"bound": kw["bound"], "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": traffic_record(top), "kernel": top, "kernel_ms": kavg[top],
+                "algorithmic_bytes": kw["bytes"], "algorithmic_flops": kw["flops"],
+                "peak_source": peaks["source"] if kw["bound"] != "alu" else "derived: 152 SM x 128 FMA x 2.07 GHz",
+                "kernel_share": kavg[top] / sum(kavg.values()),
+                "kernels_ms": kavg}
+
+    # ---- end to end: pinned host buffers -> device -> lla_forward -> host, every step
+    def e2e_step():
+        r = binding.forward(*host, cfg.chunk)
+        return r
+
+    e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    ms_e2e = cuda_time(e2e_step, n_e2e, stream) / n_e2e
+    wall_e2e = (time.perf_counter() - t0) / n_e2e * 1e3
+    ms_e2e = max(ms_e2e, wall_e2e)
+    ms_e2e = max_over_ranks(ms_e2e, ws)
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = out.numel() * out.element_size()
+
+    # ---- decode: 64 sequences x 16 heads, t ~ U[1, 65536), one-token steps
+    dcfg = inputs.DECODE_CONFIG
+    dsteps = args.decode_steps
+    t0v = inputs.make_positions(dcfg, rank)
+    t_all_np = t0v[None, :] + np.arange(dsteps + max(args.warmup, 3), dtype=np.int64)[:, None]
+    t_all = torch.from_numpy(t_all_np).to(dev)
+    n_tok = 32
+    toks = [inputs.make_decode_token(dcfg, rank * 1000 + i) for i in range(n_tok)]
+    dq_s = [(bf16(tk.bits["q"]).to(dev), bf16(tk.bits["k"]).to(dev), bf16(tk.bits["v"]).to(dev),
+             torch.from_numpy(tk.log_a).to(dev), torch.from_numpy(tk.lam).to(dev)) for tk in toks]
+    states = torch.randn((dcfg.batch, dcfg.H, dcfg.Lmax, dcfg.dk, dcfg.dv), device=dev,
+                         generator=torch.Generator(device=dev).manual_seed(rank)) * (dcfg.dk ** -0.5)
+    dout = torch.empty((dcfg.batch, dcfg.H, dcfg.dv), dtype=torch.bfloat16, device=dev)
+    counter = [0]
+
+    def dstep():
+        i = counter[0]
+        x = dq_s[i % n_tok]
+        binding.decode_step(*x, states, t_all[i], out=dout)
+        counter[0] += 1
+
+    for _ in range(max(args.warmup, 3)):
+        dstep()
+    first = counter[0]
+    d_ms_total = cuda_time(dstep, dsteps, stream)
+    d_ms_total = max_over_ranks(d_ms_total, ws)
+    assert binding.device_error() == 0
+    dbytes = sum(decode_bytes(t_all_np[i], dcfg.H, dcfg.dk, dcfg.dv, dcfg.Lmax) for i in range(first, first + dsteps))
+    d_gbs = ws * dbytes / (d_ms_total / 1e3) / 1e9
+
+    line = None
+    if rank == 0:
+        # CPU baseline: the oracle as it stands, on the host cores, bounded sample
+        cpu_val, cpu_sample, _ = oracle_tokens_per_s(cfg, inp, args.cpu_budget)
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{cfg.name} prefill: B={cfg.B} H={cfg.H} T={cfg.T} dk={cfg.dk} dv={cfg.dv} "
+                                   f"chunk={cfg.chunk}, bf16 q/k/v, fp32 log_a/lambda ({cfg.L} levels)",
+                       "global_batch": cfg.B * ws, "seq_len": cfg.T, "parallelism": f"heads-replicated x{ws}",
+                       "l2": "inputs (434 MB) exceed L2; no flush"},
+            "tflops": {"value": tflops, "algorithmic_gflop_per_step": work["flops"] / 1e9,
+                       "frac_of_bf16_peak": tflops / peaks["bf16_tflops"], "peak_source": peaks["source"]},
+            "hbm": {"min_bytes_per_step": work["bytes"], "gbs_at_min_bytes": work["bytes"] / (ms / 1e3) / 1e9,
+                    "frac": work["bytes"] / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+            "roofline": roofline,
+            "decode": {"workload": "64 sequences x 16 heads, dk=128 dv=64, t ~ U[1,65536), fp32 states (18 slots), "
+                                   "bf16 q/k/v", "steps": dsteps, "us_per_step": 1e3 * d_ms_total / dsteps,
+                       "gbs": d_gbs, "frac_of_hbm": d_gbs / peaks["hbm_gbs"],
+                       "bytes_per_step": dbytes / dsteps, "convention": "eager: nonempty levels read once, "
+                                                                         "held levels written once"},
+            "e2e": {"value": ws * cfg.tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "cpu_baseline": {"value": cpu_val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": cpu_sample},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "peaks": {k_: peaks[k_] for k_ in ("hbm_gbs", "bf16_tflops", "source")},
+        }
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["lla", "reference"], default="lla")
+    ap.add_argument("--config", default="headline", choices=sorted(inputs.PREFILL_CONFIGS))
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    cfg = inputs.PREFILL_CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_lla(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

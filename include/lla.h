@@ -1,0 +1,150 @@
+/*
+ * lla.h — C ABI of liblla.so: causal log-linear Mamba-2 attention on GB300 (sm_103a).
+ *
+ * The operator ("Log-Linear Attention", arXiv 2506.04761; gist.science pages in
+ * Portuguese and French, §2 "Particionamento Hierarquico / Mascara Hierarquica"
+ * and "Partitionnement par Arbre de Fenwick / Matrice de Masque Hierarchique"):
+ *
+ *     O = (Q K^T (.) M^S (.) M^H) V
+ *     o_t = sum_{s<=t} lambda_t^(l(t,s)) * prod_{r=s+1..t} a_r * (q_t . k_s) * v_s
+ *
+ * M^S is the Mamba-2 semiseparable scalar-decay mask (a_r = exp(log_a_r) in
+ * (0,1], exclusive of s so the diagonal is 1). M^H weights key s for query t
+ * by lambda_t at the Fenwick level l(t,s) of s in t's prefix: l = 0 for s = t,
+ * otherwise the bucket of size 2^(l-1) in the Fenwick decomposition of [0,t),
+ * which equals 1 + floor(log2(t xor s)) with 0-indexed positions. A length-T
+ * sequence uses L = bitlength(T-1) + 1 levels (7, 12, 14, 17 for T = 64, 2048,
+ * 8192, 65536). There is no 1/sqrt(d) scale and no normalisation.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are dense, row-major (C-contiguous), batch-major: [B, H, ...].
+ *  - q/k/v/out are bf16 (LLA_BF16) or fp32 (LLA_F32); log_a, lambda and decode
+ *    states are always fp32; decode positions are int64.
+ *  - Device pointers are caller-owned CUDA device memory on the current device.
+ *    The library keeps no pointer after the call returns. Every pointer must be
+ *    16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). All work is
+ *    enqueued asynchronously on it; outputs are valid once the stream reaches
+ *    that point.
+ *  - Return value: LLA_OK, or a negative lla_status. Argument errors are found
+ *    on the host before anything is enqueued and leave all buffers untouched.
+ *    Faults found by a kernel (an out-of-range decode position, a bounded wait
+ *    that ran out) are recorded in a per-device error word and reported by
+ *    lla_device_error(). No kernel traps and the library never exits.
+ */
+#ifndef LLA_H
+#define LLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LLA_OK = 0,
+    LLA_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer */
+    LLA_ERR_UNSUPPORTED = -2, /* valid operator, but a shape this build has no kernel for */
+    LLA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+    LLA_ERR_TIMEOUT = -4,     /* a kernel's bounded wait ran out (device error word) */
+    LLA_ERR_NOMEM = -5,       /* workspace allocation failed, or workspace too small */
+    LLA_ERR_DEVICE = -6       /* a kernel rejected its device-side input (device error word) */
+} lla_status;
+
+typedef enum { LLA_BF16 = 0, LLA_F32 = 1 } lla_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* lla_status_string(int status);
+
+/* Number of Fenwick levels used by a length-T sequence: bitlength(T-1) + 1
+ * (1 for T = 1, 0 for T <= 0). lambda's last dimension must equal this. */
+int lla_num_levels(int64_t T);
+
+/*
+ * Chunk-parallel prefill (pages' "Chunk-scan" / "balayage par blocs": dense
+ * intra-chunk work, hierarchical inter-chunk state passing, O(T log T)).
+ *
+ *   q      [B,H,T,dk]  dtype        queries
+ *   k      [B,H,T,dk]  dtype        keys
+ *   v      [B,H,T,dv]  dtype        values
+ *   log_a  [B,H,T]     fp32         log of the Mamba-2 decay a_t (<= 0 expected;
+ *                                   positive values are computed as given)
+ *   lambda [B,H,T,L]   fp32         per-query, per-level weights, L = lla_num_levels(T)
+ *   out    [B,H,T,dv]  dtype        written; must not overlap any input
+ *   chunk  chunk length of the scan: 16, 32, 64 or 128, with T % chunk == 0.
+ *          It sets how keys are grouped into inter-chunk states; the result is
+ *          the same operator for every valid chunk (up to rounding order).
+ *   dk, dv 1..128; the bf16 tensor-core path runs for dk == 128, dv in {64,128},
+ *          T % 128 == 0; other shapes run the fp32 SIMT path.
+ *
+ * Scratch: the call takes its workspace (inter-chunk states) from a
+ * library-owned, stream-ordered memory pool on `stream` and returns it there.
+ * Use lla_forward_ws to pass caller-owned workspace instead.
+ */
+int lla_forward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype);
+
+/* Workspace bytes lla_forward_ws needs for these sizes (0 on invalid sizes). */
+size_t lla_forward_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype);
+
+/* lla_forward with caller-owned device workspace of at least
+ * lla_forward_workspace_size(...) bytes, 256-byte aligned. The workspace holds
+ * no state between calls; calls that share it must not overlap on the GPU.
+ * Returns LLA_ERR_NOMEM if workspace_bytes is too small. */
+int lla_forward_ws(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                   void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype,
+                   void* workspace, size_t workspace_bytes);
+
+/*
+ * Measurement aid: runs lla_forward once with a CUDA event recorded on `stream`
+ * before the first kernel and after each kernel launch, waits for the last
+ * event, and writes, in launch order, each kernel's elapsed device time in
+ * milliseconds to kernel_ms[i] and its static name to kernel_names[i], for
+ * i < cap. Returns the number of kernels the call launched (which may exceed
+ * cap), or a negative lla_status. Synchronous; not meant for hot loops.
+ */
+int lla_forward_profile(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                        void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype,
+                        float* kernel_ms, const char** kernel_names, int cap);
+
+/*
+ * One recurrent decode step (pages' "Decodificacao" / "Inference": O(log T)
+ * states S_t^(l), the new token updates the finest level and levels merge
+ * along the Fenwick tree; O(log T) time and memory per step).
+ *
+ *   q, k   [B,H,dk]          dtype   the new token's query and key
+ *   v      [B,H,dv]          dtype   its value
+ *   log_a  [B,H]             fp32    log a_t of the new token
+ *   lambda [B,H,Lmax]        fp32    lambda_t^(l) of the new token, l < Lmax
+ *   fenwick_states [B,H,Lmax,dk,dv] fp32, read and written in place.
+ *          Slot l holds bucket l of the Fenwick partition as
+ *          sum_s prod_{r=s+1..pos} a_r k_s v_s^T, decayed to the last token
+ *          `pos` already absorbed. On entry pos = t[b]-1 (nothing for t[b] = 0);
+ *          on return pos = t[b]. Slots empty at `pos` (level l >= 1 with bit
+ *          l-1 of pos clear) are never read and may hold anything.
+ *   t      [B]               int64   device array: position of the new token per
+ *          sequence (tokens 0..t-1 are in the states). Not modified: the caller
+ *          advances it. Needs 0 <= t < 2^(Lmax-1); a sequence outside that range
+ *          is skipped (its state and output untouched) and LLA_ERR_DEVICE is
+ *          recorded in the device error word.
+ *   out    [B,H,dv]          dtype   o_t = sum_l lambda_t^(l) S^(l)^T q_t (after the update)
+ *   dk     1..256; dv in {16, 32, 64, 128}; Lmax in 1..40.
+ */
+int lla_decode_step(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                    float* fenwick_states, const int64_t* t, void* out, void* stream,
+                    int B, int H, int dk, int dv, int Lmax, int dtype);
+
+/*
+ * Reads and clears the device error word of the current device after
+ * synchronising `stream`: LLA_OK if no kernel recorded a fault since the last
+ * read, LLA_ERR_DEVICE for rejected device-side input, LLA_ERR_TIMEOUT for a
+ * bounded wait that ran out, LLA_ERR_CUDA if the synchronisation itself failed.
+ */
+int lla_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLA_H */

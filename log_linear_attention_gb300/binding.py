@@ -1,0 +1,205 @@
+"""Thin ctypes binding of liblla.so (include/lla.h) for torch tensors.
+
+Argument marshalling only: every step of the operator runs in the library's
+CUDA kernels. torch supplies device memory and the current stream. The
+library must exist (built by ``log_linear_attention_gb300.build``); there is
+no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblla.so")
+
+LLA_OK = 0
+LLA_ERR_INVALID_ARG = -1
+LLA_ERR_UNSUPPORTED = -2
+LLA_ERR_CUDA = -3
+LLA_ERR_TIMEOUT = -4
+LLA_ERR_NOMEM = -5
+LLA_ERR_DEVICE = -6
+LLA_BF16 = 0
+LLA_F32 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LLAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def load() -> ctypes.CDLL:
+    """Load liblla.so (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with log_linear_attention_gb300.build.build()")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, fp, i, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            lib.lla_status_string.argtypes = [i]
+            lib.lla_status_string.restype = ctypes.c_char_p
+            lib.lla_num_levels.argtypes = [ctypes.c_int64]
+            lib.lla_num_levels.restype = i
+            lib.lla_forward.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i]
+            lib.lla_forward.restype = i
+            lib.lla_forward_workspace_size.argtypes = [i] * 7
+            lib.lla_forward_workspace_size.restype = sz
+            lib.lla_forward_ws.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i, vp, sz]
+            lib.lla_forward_ws.restype = i
+            lib.lla_forward_profile.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i, vp, vp, i]
+            lib.lla_forward_profile.restype = i
+            lib.lla_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, vp] + [i] * 6
+            lib.lla_decode_step.restype = i
+            lib.lla_device_error.argtypes = [vp]
+            lib.lla_device_error.restype = i
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().lla_status_string(int(status)).decode()
+
+
+def num_levels(T: int) -> int:
+    return int(load().lla_num_levels(int(T)))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return LLA_BF16
+    if t.dtype == torch.float32:
+        return LLA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check(t, name, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _call(status: int, where: str):
+    if status != LLA_OK:
+        raise LLAError(status, where)
+
+
+def forward(q, k, v, log_a, lam, chunk: int, out=None, stream=None, workspace=None):
+    """Chunk-parallel prefill, lla_forward / lla_forward_ws.
+
+    q, k [B,H,T,dk]; v [B,H,T,dv] (bf16 or fp32, same dtype); log_a [B,H,T] fp32;
+    lam [B,H,T,L] fp32 with L = num_levels(T). Host (CPU) inputs are copied to the
+    current device first and the result is copied back (the end-to-end path).
+    ``workspace``: optional uint8 CUDA tensor of at least workspace_size(...) bytes.
+    """
+    torch = _torch()
+    host = not q.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        q, k, v, log_a, lam = (x.to(dev, non_blocking=True) for x in (q, k, v, log_a, lam))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda")):
+        _check(t_, n, q.device)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if log_a.dtype != torch.float32 or lam.dtype != torch.float32:
+        raise TypeError("log_a and lambda must be float32")
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or log_a.shape != (B, H, T) or lam.shape[:3] != (B, H, T):
+        raise ValueError("shape mismatch between q, k, v, log_a and lambda")
+    if lam.shape[3] != num_levels(T):
+        raise ValueError(f"lambda needs {num_levels(T)} levels for T={T}, got {lam.shape[3]}")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", q.device)
+    code = _dtype_code(q)
+    lib = load()
+    sh = _stream_handle(stream)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(), out.data_ptr(),
+            B, H, T, dk, dv, int(chunk), sh, code)
+    if workspace is None:
+        _call(lib.lla_forward(*args), "lla_forward")
+    else:
+        _check(workspace, "workspace", q.device)
+        _call(lib.lla_forward_ws(*args, workspace.data_ptr(), workspace.numel() * workspace.element_size()),
+              "lla_forward_ws")
+    if host:
+        return out.to("cpu")
+    return out
+
+
+def forward_profile(q, k, v, log_a, lam, chunk: int, out, stream=None):
+    """lla_forward_profile: one synchronous forward call; returns [(kernel_name, ms), ...]
+    in launch order, timed with CUDA events on the launch stream."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    cap = 16
+    ms = (ctypes.c_float * cap)()
+    names = (ctypes.c_char_p * cap)()
+    n = load().lla_forward_profile(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(),
+                                   out.data_ptr(), B, H, T, dk, dv, int(chunk), _stream_handle(stream),
+                                   _dtype_code(q), ctypes.cast(ms, ctypes.c_void_p),
+                                   ctypes.cast(names, ctypes.c_void_p), cap)
+    if n < 0:
+        raise LLAError(n, "lla_forward_profile")
+    return [(names[i].decode(), float(ms[i])) for i in range(min(n, cap))]
+
+
+def workspace_size(B: int, H: int, T: int, dk: int, dv: int, chunk: int, dtype) -> int:
+    """Bytes of caller-owned workspace lla_forward_ws needs (0 for invalid sizes)."""
+    torch = _torch()
+    code = LLA_BF16 if dtype == torch.bfloat16 else LLA_F32
+    return int(load().lla_forward_workspace_size(B, H, T, dk, dv, int(chunk), code))
+
+
+def decode_step(q, k, v, log_a, lam, states, t, out=None, stream=None):
+    """One recurrent decode step, lla_decode_step. ``states`` [B,H,Lmax,dk,dv] fp32 is
+    updated in place; ``t`` int64 [B] on the device. Returns out [B,H,dv]."""
+    torch = _torch()
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    Lmax = states.shape[2]
+    for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda"), (states, "states"), (t, "t")):
+        _check(t_, n, q.device)
+    if states.dtype != torch.float32 or states.shape != (B, H, Lmax, dk, dv):
+        raise ValueError("states must be float32 [B,H,Lmax,dk,dv]")
+    if t.dtype != torch.int64 or t.shape != (B,):
+        raise ValueError("t must be int64 [B]")
+    if lam.shape != (B, H, Lmax) or log_a.shape != (B, H) or k.shape != q.shape or v.shape[:2] != (B, H):
+        raise ValueError("shape mismatch in decode inputs")
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", q.device)
+    _call(load().lla_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(),
+                                 states.data_ptr(), t.data_ptr(), out.data_ptr(), _stream_handle(stream),
+                                 B, H, dk, dv, Lmax, _dtype_code(q)), "lla_decode_step")
+    return out
+
+
+def device_error(stream=None) -> int:
+    """Synchronise ``stream``, then read and clear the device error word (an lla status)."""
+    return int(load().lla_device_error(_stream_handle(stream)))

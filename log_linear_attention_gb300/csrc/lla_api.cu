@@ -1,0 +1,253 @@
+// Host side of the C ABI declared in include/lla.h: argument validation,
+// path selection (tcgen05 tensor-core path or SIMT path), workspace handling
+// and the per-device error word.
+#include <mutex>
+
+#include "../../include/lla.h"
+#include "lla_internal.cuh"
+
+// One error word per device (each device holds its own copy of this variable).
+__device__ int lla_device_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+int* g_err_ptr[kMaxDevices];
+cudaMemPool_t g_pool[kMaxDevices];
+bool g_pool_ready[kMaxDevices];
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+// Device address of this device's error word (looked up once per device).
+int* error_word(int dev) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, lla_device_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+// Library-private stream-ordered pool: freed workspace stays reserved for the
+// next call instead of going back to the driver.
+cudaMemPool_t workspace_pool(int dev) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_pool_ready[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pool[dev] = pool;
+        g_pool_ready[dev] = true;
+    }
+    return g_pool[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct ForwardPlan {
+    bool tc;
+    lla::TcPlan tcp;
+    lla::SimtPlan sp;
+    size_t bytes;
+};
+
+int validate_forward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                     const void* out, int B, int H, int T, int dk, int dv, int chunk, int dtype) {
+    if (!q || !k || !v || !log_a || !lambda || !out) return LLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_a) || !aligned16(lambda) || !aligned16(out))
+        return LLA_ERR_INVALID_ARG;
+    if (dtype != LLA_BF16 && dtype != LLA_F32) return LLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 1 || dk < 1 || dv < 1) return LLA_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return LLA_ERR_INVALID_ARG;
+    if (T % chunk != 0) return LLA_ERR_INVALID_ARG;
+    if (dk > 128 || dv > 128) return LLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 65535) return LLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H * T * (dk > dv ? dk : dv) > ((int64_t)1 << 40)) return LLA_ERR_UNSUPPORTED;
+    return LLA_OK;
+}
+
+bool plan_forward(int B, int H, int T, int dk, int dv, int chunk, int dtype, ForwardPlan* fp) {
+    fp->tc = lla::tc_supported(dtype, dk, dv, T);
+    if (fp->tc) {
+        if (!lla::make_tc_plan(B, H, T, dk, dv, &fp->tcp)) return false;
+        fp->bytes = fp->tcp.total_bytes;
+    } else {
+        if (!lla::make_simt_plan(B, H, T, dk, dv, chunk, &fp->sp)) return false;
+        fp->bytes = fp->sp.total_bytes;
+    }
+    return true;
+}
+
+int run_forward(const ForwardPlan& fp, const void* q, const void* k, const void* v, const float* log_a,
+                const float* lambda, void* out, int dtype, void* ws, int* err, cudaStream_t stream) {
+    cudaError_t e = fp.tc ? lla::tc_forward(fp.tcp, q, k, v, log_a, lambda, out, ws, err, stream)
+                          : lla::simt_forward(fp.sp, dtype, q, k, v, log_a, lambda, out, ws, err, stream);
+    return e == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace lla {
+LaunchLog*& active_launch_log() {
+    static thread_local LaunchLog* log = nullptr;
+    return log;
+}
+}  // namespace lla
+
+extern "C" {
+
+const char* lla_status_string(int status) {
+    switch (status) {
+        case LLA_OK: return "LLA_OK";
+        case LLA_ERR_INVALID_ARG: return "LLA_ERR_INVALID_ARG: null, misaligned or out-of-range argument";
+        case LLA_ERR_UNSUPPORTED: return "LLA_ERR_UNSUPPORTED: shape outside the kernels of this build";
+        case LLA_ERR_CUDA: return "LLA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case LLA_ERR_TIMEOUT: return "LLA_ERR_TIMEOUT: a kernel's bounded wait ran out";
+        case LLA_ERR_NOMEM: return "LLA_ERR_NOMEM: workspace missing or too small";
+        case LLA_ERR_DEVICE: return "LLA_ERR_DEVICE: a kernel rejected its device-side input";
+        default: return "unknown lla status";
+    }
+}
+
+int lla_num_levels(int64_t T) {
+    if (T <= 0) return 0;
+    return lla::bitlength(T - 1) + 1;
+}
+
+size_t lla_forward_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype) {
+    // Pointers are not inspected here; validate sizes with dummy aligned non-null pointers.
+    const void* dummy = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+    if (validate_forward(dummy, dummy, dummy, static_cast<const float*>(dummy), static_cast<const float*>(dummy),
+                         dummy, B, H, T, dk, dv, chunk, dtype) != LLA_OK)
+        return 0;
+    ForwardPlan fp;
+    if (!plan_forward(B, H, T, dk, dv, chunk, dtype, &fp)) return 0;
+    return fp.bytes;
+}
+
+int lla_forward_ws(const void* q, const void* k, const void* v, const float* log_a, const float* lambda, void* out,
+                   int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype, void* workspace,
+                   size_t workspace_bytes) {
+    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    ForwardPlan fp;
+    if (!plan_forward(B, H, T, dk, dv, chunk, dtype, &fp)) return LLA_ERR_UNSUPPORTED;
+    if (fp.bytes > 0 && (!workspace || workspace_bytes < fp.bytes)) return LLA_ERR_NOMEM;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LLA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
+    return run_forward(fp, q, k, v, log_a, lambda, out, dtype, workspace, err, static_cast<cudaStream_t>(stream));
+}
+
+int lla_forward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda, void* out,
+                int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype) {
+    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    ForwardPlan fp;
+    if (!plan_forward(B, H, T, dk, dv, chunk, dtype, &fp)) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    if (fp.bytes > 0) {
+        cudaMemPool_t pool = workspace_pool(dev);
+        if (!pool) return LLA_ERR_CUDA;
+        if (cudaMallocFromPoolAsync(&ws, fp.bytes, pool, s) != cudaSuccess) {
+            cudaGetLastError();
+            return LLA_ERR_NOMEM;
+        }
+    }
+    st = run_forward(fp, q, k, v, log_a, lambda, out, dtype, ws, err, s);
+    if (ws && cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
+    return st;
+}
+
+int lla_forward_profile(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                        void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype,
+                        float* kernel_ms, const char** kernel_names, int cap) {
+    if (cap < 0 || (cap > 0 && (!kernel_ms || !kernel_names))) return LLA_ERR_INVALID_ARG;
+    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    lla::LaunchLog log;
+    log.count = 0;
+    cudaEvent_t start;
+    if (cudaEventCreate(&start) != cudaSuccess) return LLA_ERR_CUDA;
+    int made = 0;
+    for (; made < lla::LaunchLog::kMax; made++)
+        if (cudaEventCreate(&log.events[made]) != cudaSuccess) break;
+    if (made < lla::LaunchLog::kMax) {
+        for (int i = 0; i < made; i++) cudaEventDestroy(log.events[i]);
+        cudaEventDestroy(start);
+        return LLA_ERR_CUDA;
+    }
+    cudaEventRecord(start, s);
+    lla::active_launch_log() = &log;
+    st = lla_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, stream, dtype);
+    lla::active_launch_log() = nullptr;
+    int n = log.count < lla::LaunchLog::kMax ? log.count : lla::LaunchLog::kMax;
+    if (st == LLA_OK && n > 0 && cudaEventSynchronize(log.events[n - 1]) != cudaSuccess) st = LLA_ERR_CUDA;
+    if (st == LLA_OK) {
+        cudaEvent_t prev = start;
+        for (int i = 0; i < n && i < cap; i++) {
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, prev, log.events[i]);
+            kernel_ms[i] = ms;
+            kernel_names[i] = log.names[i];
+            prev = log.events[i];
+        }
+    }
+    for (int i = 0; i < lla::LaunchLog::kMax; i++) cudaEventDestroy(log.events[i]);
+    cudaEventDestroy(start);
+    return st == LLA_OK ? log.count : st;
+}
+
+int lla_decode_step(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                    float* fenwick_states, const int64_t* t, void* out, void* stream, int B, int H, int dk, int dv,
+                    int Lmax, int dtype) {
+    if (!q || !k || !v || !log_a || !lambda || !fenwick_states || !t || !out) return LLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_a) || !aligned16(lambda) ||
+        !aligned16(fenwick_states) || !aligned16(t) || !aligned16(out))
+        return LLA_ERR_INVALID_ARG;
+    if (dtype != LLA_BF16 && dtype != LLA_F32) return LLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || dk < 1 || dv < 1 || Lmax < 1 || Lmax > 40) return LLA_ERR_INVALID_ARG;
+    if (dk > 256 || (dv != 16 && dv != 32 && dv != 64 && dv != 128)) return LLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 0x7fffffff) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
+    cudaError_t e = lla::decode_step(dtype, q, k, v, log_a, lambda, fenwick_states, t, out, B, H, dk, dv, Lmax, err,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
+int lla_device_error(void* stream) {
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LLA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, lla_device_error_word, sizeof(int)) != cudaSuccess) return LLA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(lla_device_error_word, &zero, sizeof(int)) != cudaSuccess) return LLA_ERR_CUDA;
+    if (word == lla::kDevBadInput) return LLA_ERR_DEVICE;
+    if (word == lla::kDevTimeout) return LLA_ERR_TIMEOUT;
+    return word == 0 ? LLA_OK : LLA_ERR_DEVICE;
+}
+
+}  // extern "C"

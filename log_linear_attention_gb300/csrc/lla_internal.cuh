@@ -1,0 +1,93 @@
+// Internal declarations shared by the host API (lla_api.cu) and the kernel
+// translation units. Not part of the public ABI (see include/lla.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace lla {
+
+// Device error word values (a kernel writes the first fault it sees with atomicCAS).
+enum DeviceError : int { kDevOk = 0, kDevBadInput = 1, kDevTimeout = 2 };
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ float load_f(const float* p) { return *p; }
+__device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void store_f(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Fenwick level of key s for query t (s <= t), 0-indexed positions:
+// 0 for s == t, else 1 + floor(log2(t xor s)). Valid for positions < 2^31.
+__device__ __forceinline__ int fenwick_level(int t, int s) { return 32 - __clz(t ^ s); }
+
+// Optional per-launch event log for lla_forward_profile: when a log is active on
+// this host thread, every launcher calls note_launch() right after enqueueing a
+// kernel, which records a CUDA event on the launch stream.
+struct LaunchLog {
+    static constexpr int kMax = 16;
+    cudaEvent_t events[kMax];
+    const char* names[kMax];
+    int count;
+};
+LaunchLog*& active_launch_log();
+inline void note_launch(cudaStream_t stream, const char* name) {
+    LaunchLog* log = active_launch_log();
+    if (!log) return;
+    if (log->count < LaunchLog::kMax) {
+        log->names[log->count] = name;
+        cudaEventRecord(log->events[log->count], stream);
+    }
+    log->count++;
+}
+
+inline int bitlength(int64_t x) {
+    int n = 0;
+    while (x > 0) { n++; x >>= 1; }
+    return n;
+}
+
+// Layout of the SIMT path's workspace for one lla_forward call.
+//   g      fp32 [BH][N]                        per-chunk total log-decay
+//   nodes  fp32 [BH][node_count][dk][dv]      Fenwick pyramid: level p holds
+//          N >> p nodes; node (p, m) is the decayed state sum of chunks
+//          [m 2^p, (m+1) 2^p), decayed to the last token of the block.
+struct SimtPlan {
+    int B, H, T, dk, dv, chunk, c;  // c = log2(chunk)
+    int N;                          // chunks per sequence
+    int P;                          // pyramid levels read: bitlength(N - 1)
+    int node_count;                 // sum_{p<P} N >> p
+    int level_off[32];              // first node of level p
+    size_t g_bytes, nodes_bytes, total_bytes;
+};
+
+bool make_simt_plan(int B, int H, int T, int dk, int dv, int chunk, SimtPlan* plan);
+
+// Tensor-core (tcgen05) path for bf16, dk = 128. Plan and launcher live in lla_tc.cu.
+struct TcPlan {
+    int B, H, T, dk, dv;
+    int NT;                  // 128-token tiles per sequence
+    int P;                   // node levels read: bitlength(NT - 1)
+    int node_count;          // even-indexed nodes actually read, all levels
+    int level_off[32];       // node index of (p, m = 0); node (p, m even) at level_off[p] + m / 2
+    size_t g_bytes, nodes_bytes, total_bytes;
+};
+
+bool tc_supported(int dtype, int dk, int dv, int T);
+bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* plan);
+cudaError_t tc_forward(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
+                       const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream);
+
+// SIMT launchers (lla_simt.cu).
+cudaError_t simt_forward(const SimtPlan& plan, int dtype, const void* q, const void* k, const void* v,
+                         const float* log_a, const float* lambda, void* out, void* workspace, int* err,
+                         cudaStream_t stream);
+cudaError_t decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
+                        const float* lambda, float* states, const int64_t* t, void* out, int B, int H,
+                        int dk, int dv, int Lmax, int* err, cudaStream_t stream);
+
+}  // namespace lla

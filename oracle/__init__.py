@@ -51,6 +51,8 @@ def _load():
             lib.lla_oracle_explicit.restype = None
             lib.lla_oracle_recurrent.argtypes = [dp] * 6 + [ctypes.c_int] * 6
             lib.lla_oracle_recurrent.restype = ctypes.c_int
+            lib.lla_oracle_explicit_rows.argtypes = [dp] * 6 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int]
+            lib.lla_oracle_explicit_rows.restype = None
             lib.lla_oracle_decode_step.argtypes = [dp] * 6 + [i64p, dp] + [ctypes.c_int] * 5
             lib.lla_oracle_decode_step.restype = ctypes.c_int
             _lib = lib
@@ -91,6 +93,19 @@ def explicit(q, k, v, log_a, lam) -> np.ndarray:
     out = np.zeros((B, H, T, dv), dtype=np.float64)
     _load().lla_oracle_explicit(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
                                 B, H, T, dk, dv, L)
+    return out
+
+
+def explicit_rows(q, k, v, log_a, lam, b: int, h: int, rows) -> np.ndarray:
+    """Explicit form for chosen query rows of head (b, h) only: returns [len(rows), dv]."""
+    sl = (slice(b, b + 1), slice(h, h + 1))
+    q, k, v, log_a, lam, (_, _, T, dk, dv, L) = _check_forward(q[sl], k[sl], v[sl], log_a[sl], lam[sl])
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    assert rows.ndim == 1 and (rows >= 0).all() and (rows < T).all()
+    out = np.zeros((rows.size, dv), dtype=np.float64)
+    _load().lla_oracle_explicit_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(out),
+                                     0, T, dk, dv, L,
+                                     rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), int(rows.size))
     return out
 
 

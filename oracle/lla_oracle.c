@@ -104,6 +104,35 @@ void lla_oracle_explicit(const double* q, const double* k, const double* v,
     }
 }
 
+/* The explicit form restricted to chosen query rows of one head (bh), for
+ * spot checks of long sequences: o_t for each t in rows[0..nrows), written to
+ * out[r * dv ...]. Same definition and summation order as lla_oracle_explicit. */
+void lla_oracle_explicit_rows(const double* q, const double* k, const double* v,
+                              const double* log_a, const double* lambda, double* out,
+                              int bh, int T, int dk, int dv, int L,
+                              const int64_t* rows, int nrows)
+{
+    const double* qh = q + (size_t)bh * T * dk;
+    const double* kh = k + (size_t)bh * T * dk;
+    const double* vh = v + (size_t)bh * T * dv;
+    const double* ah = log_a + (size_t)bh * T;
+    const double* lh = lambda + (size_t)bh * T * L;
+    for (int r = 0; r < nrows; r++) {
+        int64_t t = rows[r];
+        double* o = out + (size_t)r * dv;
+        for (int j = 0; j < dv; j++) o[j] = 0.0;
+        double decay_exp = 0.0;
+        for (int64_t s = t; s >= 0; s--) {
+            int l = lla_oracle_level(t, s);
+            double qk = 0.0;
+            for (int i = 0; i < dk; i++) qk += qh[(size_t)t * dk + i] * kh[(size_t)s * dk + i];
+            double w = lh[(size_t)t * L + l] * exp(decay_exp) * qk;
+            for (int j = 0; j < dv; j++) o[j] += w * vh[(size_t)s * dv + j];
+            decay_exp += ah[s];
+        }
+    }
+}
+
 /* Lowest set bit position of t > 0. */
 static int trailing_zeros(int64_t t)
 {

@@ -215,3 +215,12 @@ def test_decode_rejects_too_few_levels():
     with pytest.raises(ValueError):
         oracle.decode_step(z((B, H, dk)), z((B, H, dk)), z((B, H, dv)), z((B, H)), z((B, H, Lmax)),
                            z((B, H, Lmax, dk, dv)), np.array([4]))
+
+
+def test_explicit_rows_matches_full_explicit():
+    rng = np.random.default_rng(11)
+    q, k, v, log_a, lam = _rand_problem(rng, 2, 2, 70, 5, 3)
+    full = oracle.explicit(q, k, v, log_a, lam)
+    rows = [0, 1, 31, 32, 69]
+    got = oracle.explicit_rows(q, k, v, log_a, lam, 1, 0, rows)
+    assert np.array_equal(got, full[1, 0, rows])
