@@ -78,9 +78,8 @@ int validate_forward(const void* q, const void* k, const void* v, const float* l
 }
 
 bool plan_forward(int B, int H, int T, int dk, int dv, int chunk, int dtype, ForwardPlan* fp) {
-    fp->tc = lla::tc_supported(dtype, dk, dv, T);
+    fp->tc = lla::tc_supported(dtype, dk, dv, T) && lla::make_tc_plan(B, H, T, dk, dv, &fp->tcp);
     if (fp->tc) {
-        if (!lla::make_tc_plan(B, H, T, dk, dv, &fp->tcp)) return false;
         fp->bytes = fp->tcp.total_bytes;
     } else {
         if (!lla::make_simt_plan(B, H, T, dk, dv, chunk, &fp->sp)) return false;

@@ -1,13 +1,848 @@
-// Tensor-core (tcgen05) path for bf16 prefill. Placeholder until the kernels land.
+// Tensor-core (tcgen05 / TMEM / TMA) path of log-linear Mamba-2 attention
+// prefill, bf16 q/k/v with fp32 accumulation, dk = 128, dv in {64, 128},
+// T % 128 == 0.
+//
+// Chunkwise algorithm ("Log-Linear Attention", pt §2 "Forma Recorrente e
+// Paralela" / fr §2 "Algorithmes Efficaces": dense intra-block work,
+// hierarchical inter-block state passing, O(T log T), matmul-rich) laid out
+// on 128-token tiles (the M = 128 tcgen05 shape). Tile j covers tokens
+// [128 j, 128 j + 128). Within a tile, every key s <= t is handled densely
+// with its exact Fenwick level 1 + floor(log2(t xor s)) <= 7. A key in an
+// earlier tile i sits at level 8 + floor(log2(j xor i)), and the keys of level
+// 8 + p are exactly the tiles of the aligned block ((j >> p) - 1) << p ..
+// ((j >> p) << p) - 1, present when bit p of j is set. That block's decayed
+// state sum is the Fenwick node (p, m = (j >> p) - 1): a dk x dv matrix.
+//
+// Kernels (one stream, in order):
+//   tc_nodes  : per (head, segment of 2^q tiles): S_u = K_u^T diag(w) V_u on
+//               tcgen05 (w_s = decay from s to the tile end), then the level
+//               accumulators A_l <- e^{g_u} A_l + S_u kept in TMEM; a node is
+//               written (bf16) when its block closes. Also writes the tile
+//               log-decay totals g_u and each full segment's fp32 total.
+//   tc_merge  : levels above a segment: fp32 pyramid over segment totals
+//               (SIMT, small), writing the nodes that are read (bf16).
+//   tc_output : per (head, tile): S = Q K^T (tcgen05, TMEM), masked with
+//               decay and lambda into bf16 P (smem), O = P V plus, per set
+//               bit p of j, L_p = Q B_p (tcgen05, TMEM); epilogue
+//               O + sum_p lambda_t^(8+p) exp(decay) L_p -> bf16.
+// Only even-indexed nodes are ever read (node (p, m) is read by tile j iff
+// j >> p == m + 1, and bit p of j is set), so only those are stored.
+//
+// Every mbarrier wait is bounded: on overrun a kernel records
+// LLA_ERR_TIMEOUT in the device error word, waits (bounded) for its own
+// in-flight work, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "lla_internal.cuh"
 
 namespace lla {
+namespace {
 
-bool tc_supported(int, int, int, int) { return false; }
-bool make_tc_plan(int, int, int, int, int, TcPlan*) { return false; }
-cudaError_t tc_forward(const TcPlan&, const void*, const void*, const void*, const float*, const float*, void*, void*,
-                       int*, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int kTile = 128;        // tokens per tile (MMA M)
+constexpr int kDk = 128;          // head dim of q/k on this path
+constexpr int kPanelBytes = 16384;  // 128 rows x 128 B (64 bf16), one SWIZZLE_128B panel
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr float kLog2e = 1.4426950408889634f;
+// Spare shared memory past the last operand: a descriptor-addressed read of an
+// MN-major operand spans at most one 16 KB panel stride plus 2 KB past its
+// start, and this keeps every such read inside the CTA's allocation.
+constexpr int kGuardBytes = 20480;
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const long long start = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - start > kWaitCycles) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulate, issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every previously issued tcgen05.mma of this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes: v[i] = column (col + i) of lane (warp lane).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) r[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, SWIZZLE_128B canonical layout.
+//  K-major operand (rows of 64 K-elements, 128 B, 8-row atoms 1024 B apart):
+//      lbo unused, sbo = 1024; a K step of 16 elements adds 32 B inside the atom.
+//  MN-major operand (rows of 64 MN-elements, 128 B, one row per K index):
+//      lbo = byte stride between 64-element MN atoms, sbo = 1024 (8 K rows);
+//      a K step of 16 adds 16 rows = 2048 B.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;  // swizzle: 128 B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, dense.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4)                                 // D format: f32
+           | (1u << 7)                               // A format: bf16
+           | (1u << 10)                              // B format: bf16
+           | (static_cast<uint32_t>(a_mn_major) << 15)  // A major: 0 = K, 1 = MN
+           | (static_cast<uint32_t>(b_mn_major) << 16)  // B major
+           | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// Byte offset of element (row r, col c) of a 128-row x 64-col bf16 panel in SWIZZLE_128B layout.
+__device__ __forceinline__ uint32_t sw128_off(int r, int chunk16) {
+    return static_cast<uint32_t>(r * 128 + ((chunk16 ^ (r & 7)) << 4));
+}
+
+// Inclusive prefix sum over the 128 threads of the block (one value each).
+__device__ __forceinline__ float block_scan128(float x, float* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float incl = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        float y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    float base = 0.f;
+    for (int w = 0; w < warp; w++) base += warp_tot[w];
+    __syncthreads();
+    return incl + base;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(h);
+}
+
+struct LevelOffsets { int off[32]; };
+
+// ------------------------------------------------------------------ tc_nodes
+
+template <int DV>
+struct NodesSmem {
+    static constexpr int kKBytes = 2 * kPanelBytes;             // K tile: 128 tokens x 128 dk
+    static constexpr int kVBytes = (DV / 64) * kPanelBytes;     // V tile: 128 tokens x DV
+    static constexpr int kStageBytes = kKBytes + kVBytes;
+    static constexpr int kStages = 2;
+    static constexpr int kBytes = kStages * kStageBytes + 1024 + kGuardBytes;  // + alignment slack
+};
+
+// grid (num_segments, B*H), 128 threads. Segment s covers tiles [s 2^q, (s+1) 2^q).
+template <int DV>
+__global__ void __launch_bounds__(128, 1)
+    tc_nodes_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const float* __restrict__ log_a, float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
+                    float* __restrict__ seg_tot, int T, int NT, int q, int node_count, LevelOffsets lo,
+                    uint32_t tmem_cols, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar_full[2];
+    __shared__ uint64_t bar_mma;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ float warp_tot[4];
+    __shared__ float g_sh;
+    __shared__ int fail_sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int seg = blockIdx.x, bh = blockIdx.y;
+    const int seg_tiles = 1 << q;
+    const int tile0 = seg * seg_tiles;
+    const int ntiles = min(seg_tiles, NT - tile0);
+    constexpr uint32_t kTxBytes = NodesSmem<DV>::kStageBytes;
+
+    if (tid == 0) {
+        mbar_init(&bar_full[0], 1);
+        mbar_init(&bar_full[1], 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        fail_sh = 0;
+    }
+    if (warp == 0) tmem_alloc(&tmem_base_sh, tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    auto stage_ptr = [&](int s) { return smem + s * NodesSmem<DV>::kStageBytes; };
+    auto issue_tile = [&](int u) {
+        const int s = u & 1;
+        uint8_t* st = stage_ptr(s);
+        const int row = bh * T + (tile0 + u) * kTile;
+        mbar_expect_tx(&bar_full[s], kTxBytes);
+        tma_load_2d(st, &tm_k, &bar_full[s], 0, row);
+        tma_load_2d(st + kPanelBytes, &tm_k, &bar_full[s], 64, row);
+#pragma unroll
+        for (int p = 0; p < DV / 64; p++)
+            tma_load_2d(st + NodesSmem<DV>::kKBytes + p * kPanelBytes, &tm_v, &bar_full[s], 64 * p, row);
+    };
+    if (tid == 0) {
+        issue_tile(0);
+        if (ntiles > 1) issue_tile(1);
+    }
+
+    constexpr uint32_t kIdesc = idesc_bf16(kDk, DV, 1, 1);  // A = K^T (MN-major), B = V (MN-major)
+    const size_t msz = static_cast<size_t>(kDk) * DV;
+    const int i_row = tid;  // TMEM lane = dk row
+    int issued = ntiles > 1 ? 2 : 1;
+    int mma_phase = 0;
+    bool ok = true;
+
+    for (int u = 0; u < ntiles; u++) {
+        const int s = u & 1;
+        const int tile = tile0 + u;
+        // tile-local decays
+        const float a = log_a[static_cast<size_t>(bh) * T + static_cast<size_t>(tile) * kTile + tid];
+        const float cl = block_scan128(a, warp_tot);
+        if (tid == kTile - 1) g_sh = cl;
+        __syncthreads();
+        const float g = g_sh;
+        if (tid == 0) g_tiles[static_cast<size_t>(bh) * NT + tile] = g;
+        const float w = exp2f((g - cl) * kLog2e);
+
+        if (!mbar_wait(&bar_full[s], (u >> 1) & 1)) {
+            ok = false;
+            atomicExch(&fail_sh, 1);
+        }
+        __syncthreads();
+        if (fail_sh) break;
+        // scale V row `tid` (one token) by its decay to the tile end
+        uint8_t* vbase = stage_ptr(s) + NodesSmem<DV>::kKBytes;
+#pragma unroll
+        for (int p = 0; p < DV / 64; p++) {
+            uint4* rowp = reinterpret_cast<uint4*>(vbase + p * kPanelBytes + tid * 128);
+#pragma unroll
+            for (int c = 0; c < 8; c++) {
+                uint4 x = rowp[c];
+                float2 f0 = unpack_bf16(x.x), f1 = unpack_bf16(x.y), f2 = unpack_bf16(x.z), f3 = unpack_bf16(x.w);
+                x.x = pack_bf16(f0.x * w, f0.y * w);
+                x.y = pack_bf16(f1.x * w, f1.y * w);
+                x.z = pack_bf16(f2.x * w, f2.y * w);
+                x.w = pack_bf16(f3.x * w, f3.y * w);
+                rowp[c] = x;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t kb = smem_u32(stage_ptr(s));
+            const uint32_t vb = kb + NodesSmem<DV>::kKBytes;
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; kk++) {
+                const uint64_t ad = sdesc(kb + kk * 2048, kPanelBytes, 1024);
+                const uint64_t bd = sdesc(vb + kk * 2048, kPanelBytes, 1024);
+                mma_bf16(tmem, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mbar_wait(&bar_mma, mma_phase)) {
+            ok = false;
+            atomicExch(&fail_sh, 1);
+        }
+        mma_phase ^= 1;
+        tc_fence_after();
+        __syncthreads();
+        if (fail_sh) break;
+        // stage s is free again: prefetch tile u + 2 into it
+        if (tid == 0 && issued < ntiles) {
+            issue_tile(issued);
+            issued++;
+        }
+
+        // epilogue: level accumulators l = 0..q (level 0 is S_u itself)
+        const float ge = exp2f(g * kLog2e);
+#pragma unroll 1
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+            float sv[32], av[32];
+            tmem_ld32(tmem + lane_base + c0, sv);
+#pragma unroll 1
+            for (int l = 0; l <= q; l++) {
+                const int span = 1 << l;
+                const bool first = (tile & (span - 1)) == 0;
+                const bool closes = ((tile + 1) & (span - 1)) == 0;
+                if (l == 0) {
+#pragma unroll
+                    for (int e = 0; e < 32; e++) av[e] = sv[e];
+                } else {
+                    if (first) {
+#pragma unroll
+                        for (int e = 0; e < 32; e++) av[e] = sv[e];
+                    } else {
+                        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(l * DV + c0), av);
+#pragma unroll
+                        for (int e = 0; e < 32; e++) av[e] = fmaf(av[e], ge, sv[e]);
+                    }
+                    if (!closes) tmem_st32(tmem + lane_base + static_cast<uint32_t>(l * DV + c0), av);
+                }
+                if (closes) {
+                    const int m = tile >> l;
+                    if ((m & 1) == 0 && ((m + 1) << l) < NT) {
+                        __nv_bfloat16* dst = nodes + (static_cast<size_t>(bh) * node_count + lo.off[l] + (m >> 1)) * msz +
+                                             static_cast<size_t>(i_row) * DV + c0;
+                        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                        for (int c = 0; c < 4; c++)
+                            d4[c] = make_uint4(pack_bf16(av[8 * c], av[8 * c + 1]), pack_bf16(av[8 * c + 2], av[8 * c + 3]),
+                                               pack_bf16(av[8 * c + 4], av[8 * c + 5]),
+                                               pack_bf16(av[8 * c + 6], av[8 * c + 7]));
+                    }
+                    if (l == q && ntiles == seg_tiles) {
+                        float* dst = seg_tot + (static_cast<size_t>(bh) * ((NT + seg_tiles - 1) / seg_tiles) + seg) * msz +
+                                     static_cast<size_t>(i_row) * DV + c0;
+                        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+                        for (int c = 0; c < 8; c++) d4[c] = make_float4(av[4 * c], av[4 * c + 1], av[4 * c + 2], av[4 * c + 3]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    if (!ok || fail_sh) {
+        if (tid == 0) record_error(err, kDevTimeout);
+        // let in-flight copies and MMAs land before the shared memory and TMEM go away
+        mbar_wait(&bar_mma, mma_phase);
+        for (int s = 0; s < 2; s++) mbar_try_wait(&bar_full[s], 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, tmem_cols);
+}
+
+// ------------------------------------------------------------------ tc_merge
+
+// Levels p = q+1 .. P-1 from full-segment totals (fp32 [BH][nseg][dk][DV], decayed to
+// each segment's end). In place: pyramid node (r, m) over segments overwrites segment
+// slot m 2^r. grid (dk*DV/256, BH), 256 threads, one matrix element per thread.
+__global__ void __launch_bounds__(256)
+    tc_merge_kernel(float* __restrict__ seg_tot, const float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
+                    int NT, int q, int P, int nseg, int node_count, int msz, LevelOffsets lo) {
+    extern __shared__ float Gs[];  // nseg segment log-decay totals (updated in place per level)
+    const int bh = blockIdx.y;
+    const int seg_tiles = 1 << q;
+    for (int sgi = threadIdx.x; sgi < nseg; sgi += blockDim.x) {
+        float acc = 0.f;
+        for (int u = 0; u < seg_tiles; u++) {
+            const int tile = sgi * seg_tiles + u;
+            if (tile < NT) acc += g_tiles[static_cast<size_t>(bh) * NT + tile];
+        }
+        Gs[sgi] = acc;
+    }
+    __syncthreads();
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    float* base = seg_tot + static_cast<size_t>(bh) * nseg * msz;
+    for (int r = 1; q + r < P; r++) {
+        const int p = q + r;
+        const int span = 1 << r;       // segments per node at this level
+        const int half = span >> 1;
+        const int nnodes = (NT >> p);  // full blocks of 2^p tiles
+        if (e < msz) {
+            for (int m = 0; m < nnodes; m++) {
+                const int s_lo = m * span, s_hi = m * span + half;
+                const float v = expf(Gs[s_hi]) * base[static_cast<size_t>(s_lo) * msz + e] +
+                                base[static_cast<size_t>(s_hi) * msz + e];
+                base[static_cast<size_t>(s_lo) * msz + e] = v;
+                if ((m & 1) == 0 && ((m + 1) << p) < NT)
+                    nodes[(static_cast<size_t>(bh) * node_count + lo.off[p] + (m >> 1)) * msz + e] = __float2bfloat16_rn(v);
+            }
+        }
+        __syncthreads();
+        for (int m = threadIdx.x; m < nnodes; m += blockDim.x) Gs[m * span] = Gs[m * span] + Gs[m * span + half];
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ tc_output
+
+template <int DV>
+struct OutSmem {
+    static constexpr int kQ = 0;                                  // Q tile: 2 panels (K-major over dk)
+    static constexpr int kK = kQ + 2 * kPanelBytes;               // K tile: 2 panels
+    static constexpr int kV = kK + 2 * kPanelBytes;               // V tile: DV/64 panels (MN-major over dv)
+    static constexpr int kP = kV + (DV / 64) * kPanelBytes;       // P: 2 panels (K-major over keys)
+    static constexpr int kNode = kP + 2 * kPanelBytes;            // node slots
+    static constexpr int kSlots = 256 / DV;                       // TMEM level slots [256, 512)
+    static constexpr int kNodeBytes = (DV / 64) * kPanelBytes;
+    static constexpr int kBytes = kNode + kSlots * kNodeBytes + 1024 + kGuardBytes;
+};
+
+// grid (NT, B*H), 128 threads (thread t = query row t of the tile = TMEM lane t).
+template <int DV>
+__global__ void __launch_bounds__(128, 1)
+    tc_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_nodes,
+                     const float* __restrict__ log_a, const float* __restrict__ lambda,
+                     const float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ out, int T, int NT, int L,
+                     int P, int node_count, LevelOffsets lo, int* err) {
+    using S = OutSmem<DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar_qkv;
+    __shared__ uint64_t bar_node[S::kSlots];
+    __shared__ uint64_t bar_mma;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ float warp_tot[4];
+    __shared__ float cl2_sh[kTile];
+    __shared__ float dsum2_sh[32];
+    __shared__ int fail_sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j = blockIdx.x, bh = blockIdx.y;
+    const int row0 = bh * T + j * kTile;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    constexpr uint32_t kTmemCols = 512;
+    constexpr uint32_t kColO = 128;
+    constexpr uint32_t kColLv = 256;
+
+    // levels read by this tile: set bits of j
+    int lv[16];
+    int n_lv = 0;
+    for (int p = 0; p < P; p++)
+        if ((j >> p) & 1) lv[n_lv++] = p;
+
+    if (tid == 0) {
+        mbar_init(&bar_qkv, 1);
+        for (int s = 0; s < S::kSlots; s++) mbar_init(&bar_node[s], 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        fail_sh = 0;
+    }
+    if (warp == 0) tmem_alloc(&tmem_base_sh, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    auto issue_node = [&](int slot, int p) {
+        const int m = (j >> p) - 1;
+        const int nrow = (bh * node_count + lo.off[p] + (m >> 1)) * kDk;
+        mbar_expect_tx(&bar_node[slot], S::kNodeBytes);
+#pragma unroll
+        for (int c = 0; c < DV / 64; c++)
+            tma_load_2d(smem + S::kNode + slot * S::kNodeBytes + c * kPanelBytes, &tm_nodes, &bar_node[slot], 64 * c,
+                        nrow);
+    };
+    if (tid == 0) {
+        mbar_expect_tx(&bar_qkv, (4 + DV / 64) * kPanelBytes);
+        tma_load_2d(smem + S::kQ, &tm_q, &bar_qkv, 0, row0);
+        tma_load_2d(smem + S::kQ + kPanelBytes, &tm_q, &bar_qkv, 64, row0);
+        tma_load_2d(smem + S::kK, &tm_k, &bar_qkv, 0, row0);
+        tma_load_2d(smem + S::kK + kPanelBytes, &tm_k, &bar_qkv, 64, row0);
+#pragma unroll
+        for (int c = 0; c < DV / 64; c++) tma_load_2d(smem + S::kV + c * kPanelBytes, &tm_v, &bar_qkv, 64 * c, row0);
+        for (int s = 0; s < S::kSlots && s < n_lv; s++) issue_node(s, lv[s]);
+    }
+
+    // decays: chunk-local inclusive cumsum (in log2 units) and, per set bit p of j,
+    // the summed log-decay of the tiles between the node's block end and this tile
+    const float a = log_a[static_cast<size_t>(row0) + tid];
+    const float cl = block_scan128(a, warp_tot);
+    cl2_sh[tid] = cl * kLog2e;
+    if (warp == 0) {
+        for (int x = 0; x < n_lv; x++) {
+            const int p = lv[x];
+            float d = 0.f;
+            for (int i = ((j >> p) << p) + lane; i < j; i += 32) d += g_tiles[static_cast<size_t>(bh) * NT + i];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+            if (lane == 0) dsum2_sh[x] = d * kLog2e;
+        }
+    }
+    __syncthreads();
+
+    const int t = tid;
+    const float cl2_t = cl2_sh[t];
+    const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
+    float lam_in[8];
+#pragma unroll
+    for (int l = 0; l < 8; l++) lam_in[l] = (l < L) ? lam_row[l] : 0.f;
+
+    bool ok = mbar_wait(&bar_qkv, 0);
+    if (!ok) atomicExch(&fail_sh, 1);
+    __syncthreads();
+    int mma_phase = 0;
+    float acc[DV];
+#pragma unroll
+    for (int c = 0; c < DV; c++) acc[c] = 0.f;
+
+    if (!fail_sh) {
+        // S = Q K^T: M = 128 queries, N = 128 keys, K = dk (both operands K-major)
+        if (tid == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kTile, kTile, 0, 0);
+            const uint32_t qb = smem_u32(smem + S::kQ), kb = smem_u32(smem + S::kK);
+#pragma unroll
+            for (int kk = 0; kk < kDk / 16; kk++) {
+                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                mma_bf16(tmem, sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mbar_wait(&bar_mma, mma_phase)) atomicExch(&fail_sh, 1);
+        mma_phase ^= 1;
+        tc_fence_after();
+
+        // P[t][s] = S[t][s] * exp(cl_t - cl_s) * lambda_t^(level(t,s)) for s <= t, as bf16, K-major SW128
+        uint8_t* pbase = smem + S::kP;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+            float sv[32];
+            tmem_ld32(tmem + lane_base + c0, sv);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float v2[2];
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int s = c0 + e + h;
+                    float val = 0.f;
+                    if (s <= t) {
+                        const int lvl = 32 - __clz(t ^ s);
+                        val = sv[e + h] * exp2f(cl2_t - cl2_sh[s]) * lam_in[lvl];
+                    }
+                    v2[h] = val;
+                }
+                pk[e >> 1] = pack_bf16(v2[0], v2[1]);
+            }
+            uint8_t* panel = pbase + (c0 >> 6) * kPanelBytes;
+            const int chunk0 = (c0 & 63) >> 3;
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0 + c)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    // O = P V (+ level reads), in rounds of up to kSlots levels
+    int node_phase[S::kSlots];
+#pragma unroll
+    for (int s = 0; s < S::kSlots; s++) node_phase[s] = 0;
+    const int rounds = n_lv == 0 ? 1 : (n_lv + S::kSlots - 1) / S::kSlots;
+    for (int rd = 0; rd < rounds && !fail_sh; rd++) {
+        const int first = rd * S::kSlots;
+        const int cnt = min(S::kSlots, n_lv - first);
+        if (tid == 0) {
+            if (rd > 0)
+                for (int s = 0; s < cnt; s++) issue_node(s, lv[first + s]);
+            const uint32_t qb = smem_u32(smem + S::kQ);
+            if (rd == 0) {
+                constexpr uint32_t idesc = idesc_bf16(kTile, DV, 0, 1);
+                const uint32_t pb = smem_u32(smem + S::kP), vb = smem_u32(smem + S::kV);
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; kk++) {
+                    const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                    mma_bf16(tmem + kColO, sdesc(pb + aoff, 16, 1024), sdesc(vb + kk * 2048, kPanelBytes, 1024), idesc,
+                             kk > 0 ? 1u : 0u);
+                }
+            }
+            for (int s = 0; s < cnt; s++) {
+                if (!mbar_wait(&bar_node[s], node_phase[s])) {
+                    atomicExch(&fail_sh, 1);
+                    break;
+                }
+                tc_fence_after();
+                constexpr uint32_t idesc = idesc_bf16(kTile, DV, 0, 1);
+                const uint32_t nb = smem_u32(smem + S::kNode + s * S::kNodeBytes);
+#pragma unroll
+                for (int kk = 0; kk < kDk / 16; kk++) {
+                    const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                    mma_bf16(tmem + kColLv + s * DV, sdesc(qb + aoff, 16, 1024),
+                             sdesc(nb + kk * 2048, kPanelBytes, 1024), idesc, kk > 0 ? 1u : 0u);
+                }
+            }
+            mma_commit(&bar_mma);
+        }
+#pragma unroll
+        for (int s = 0; s < S::kSlots; s++)
+            if (s < cnt) node_phase[s] ^= 1;
+        if (!mbar_wait(&bar_mma, mma_phase)) atomicExch(&fail_sh, 1);
+        mma_phase ^= 1;
+        tc_fence_after();
+        __syncthreads();
+        if (fail_sh) break;
+        if (rd == 0) {
+#pragma unroll
+            for (int c0 = 0; c0 < DV; c0 += 32) tmem_ld32(tmem + lane_base + kColO + c0, acc + c0);
+        }
+        for (int s = 0; s < cnt; s++) {
+            const int x = first + s;
+            const int p = lv[x];
+            const float r = lam_row[8 + p] * exp2f(cl2_t + dsum2_sh[x]);
+#pragma unroll
+            for (int c0 = 0; c0 < DV; c0 += 32) {
+                float lvv[32];
+                tmem_ld32(tmem + lane_base + kColLv + s * DV + c0, lvv);
+#pragma unroll
+                for (int e = 0; e < 32; e++) acc[c0 + e] = fmaf(r, lvv[e], acc[c0 + e]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+
+    if (!fail_sh) {
+        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV);
+#pragma unroll
+        for (int c = 0; c < DV / 8; c++)
+            dst[c] = make_uint4(pack_bf16(acc[8 * c], acc[8 * c + 1]), pack_bf16(acc[8 * c + 2], acc[8 * c + 3]),
+                                pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
+    } else {
+        if (tid == 0) record_error(err, kDevTimeout);
+        mbar_wait(&bar_mma, mma_phase ^ 1);
+        mbar_try_wait(&bar_qkv, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qres) ==
+                cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D bf16 row-major [rows, cols] tensor, box = 64 cols x 128 rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Segment size 2^q: level accumulators need (1 + q) * dv TMEM columns (<= 256 so two
+// CTAs fit an SM); prefer at least two CTAs per SM worth of segments.
+int choose_q(int BH, int NT, int dv) {
+    const int qmax = dv == 64 ? 3 : 1;
+    int q = 0;
+    while (q < qmax && static_cast<int64_t>(BH) * ((NT + (2 << q) - 1) / (2 << q)) >= 2 * 152) q++;
+    return q;
+}
+
+uint32_t pow2_cols(int cols) {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(cols)) c <<= 1;
+    return c;
+}
+
+template <int DV>
+cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
+                          const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream) {
+    const int BH = pl.B * pl.H;
+    const int qlog = pl.q;
+    const int seg_tiles = 1 << qlog;
+    const int nseg = (pl.NT + seg_tiles - 1) / seg_tiles;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* g_tiles = reinterpret_cast<float*>(ws);
+    __nv_bfloat16* nodes = reinterpret_cast<__nv_bfloat16*>(ws + pl.g_bytes);
+    float* seg_tot = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes);
+    LevelOffsets lo;
+    for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
+    const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
+
+    CUtensorMap tq, tk, tv, tn;
+    if (!make_map(&tq, q, rows, kDk) || !make_map(&tk, k, rows, kDk) || !make_map(&tv, v, rows, DV))
+        return cudaErrorInvalidValue;
+    const bool have_nodes = pl.node_count > 0;
+    if (have_nodes && !make_map(&tn, nodes, static_cast<uint64_t>(BH) * pl.node_count * kDk, DV))
+        return cudaErrorInvalidValue;
+    if (!have_nodes) tn = tv;  // never read when no tile has an earlier tile
+
+    // nodes and tile decays
+    {
+        const int smem = NodesSmem<DV>::kBytes;
+        cudaError_t e = cudaFuncSetAttribute(tc_nodes_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const uint32_t cols = pow2_cols((1 + qlog) * DV);
+        tc_nodes_kernel<DV><<<dim3(nseg, BH), 128, smem, stream>>>(tk, tv, log_a, g_tiles, nodes, seg_tot, pl.T, pl.NT,
+                                                                   qlog, pl.node_count, lo, cols, err);
+        note_launch(stream, "tc_nodes");
+    }
+    if (pl.P > qlog + 1) {
+        const int msz = kDk * DV;
+        tc_merge_kernel<<<dim3(msz / 256, BH), 256, nseg * sizeof(float), stream>>>(
+            seg_tot, g_tiles, nodes, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
+        note_launch(stream, "tc_merge");
+    }
+    {
+        const int smem = OutSmem<DV>::kBytes;
+        cudaError_t e = cudaFuncSetAttribute(tc_output_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int L = bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
+        tc_output_kernel<DV><<<dim3(pl.NT, BH), 128, smem, stream>>>(tq, tk, tv, tn, log_a, lambda, g_tiles,
+                                                                     static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L,
+                                                                     pl.P, pl.node_count, lo, err);
+        note_launch(stream, "tc_output");
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(int dtype, int dk, int dv, int T) {
+    return dtype == 0 && dk == kDk && (dv == 64 || dv == 128) && T % kTile == 0;
+}
+
+bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* pl) {
+    pl->B = B; pl->H = H; pl->T = T; pl->dk = dk; pl->dv = dv;
+    pl->NT = T / kTile;
+    pl->P = bitlength(static_cast<int64_t>(pl->NT) - 1);
+    const int BH = B * H;
+    pl->q = choose_q(BH, pl->NT, dv);
+    int off = 0;
+    for (int p = 0; p < 32; p++) {
+        pl->level_off[p] = off;
+        if (p < pl->P) off += (((pl->NT - 1) >> p) + 1) / 2;  // even m with (m + 1) 2^p < NT
+    }
+    pl->node_count = off;
+    const int seg_tiles = 1 << pl->q;
+    const int nseg = (pl->NT + seg_tiles - 1) / seg_tiles;
+    // 32-bit TMA row coordinates, a 16-entry level list per tile, merge totals in shared memory
+    if (static_cast<int64_t>(BH) * T >= (int64_t(1) << 31) || pl->P > 16 || nseg > 12288) return false;
+    if (static_cast<int64_t>(BH) * pl->node_count * kDk >= (int64_t(1) << 31)) return false;
+    const size_t msz = static_cast<size_t>(dk) * dv;
+    pl->g_bytes = (static_cast<size_t>(BH) * pl->NT * sizeof(float) + 1023) / 1024 * 1024;
+    pl->nodes_bytes = (static_cast<size_t>(BH) * pl->node_count * msz * 2 + 1023) / 1024 * 1024;
+    pl->seg_bytes = static_cast<size_t>(BH) * nseg * msz * sizeof(float);
+    pl->total_bytes = pl->g_bytes + pl->nodes_bytes + pl->seg_bytes;
+    return true;
+}
+
+cudaError_t tc_forward(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
+                       const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream) {
+    if (pl.dv == 64) return tc_forward_dv<64>(pl, q, k, v, log_a, lambda, out, workspace, err, stream);
+    return tc_forward_dv<128>(pl, q, k, v, log_a, lambda, out, workspace, err, stream);
 }
 
 }  // namespace lla
