@@ -309,6 +309,46 @@ def cuda_time(fn, steps, stream):
     return start.elapsed_time(end)
 
 
+def bench_decode(args, dev, stream, rank, ws):
+    """Time args.decode_steps one-token decode steps of the decode workload; returns
+    (total ms, algorithmic bytes moved, steps)."""
+    import torch
+    from log_linear_attention_gb300 import binding
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    dcfg = inputs.DECODE_CONFIG
+    dsteps = args.decode_steps
+    t0v = inputs.make_positions(dcfg, rank)
+    t_all_np = t0v[None, :] + np.arange(dsteps + max(args.warmup, 3), dtype=np.int64)[:, None]
+    t_all = torch.from_numpy(t_all_np).to(dev)
+    n_tok = 32
+    toks = [inputs.make_decode_token(dcfg, rank * 1000 + i) for i in range(n_tok)]
+    dq_s = [(bf16(tk.bits["q"]).to(dev), bf16(tk.bits["k"]).to(dev), bf16(tk.bits["v"]).to(dev),
+             torch.from_numpy(tk.log_a).to(dev), torch.from_numpy(tk.lam).to(dev)) for tk in toks]
+    states = torch.randn((dcfg.batch, dcfg.H, dcfg.Lmax, dcfg.dk, dcfg.dv), device=dev,
+                         generator=torch.Generator(device=dev).manual_seed(rank)) * (dcfg.dk ** -0.5)
+    dout = torch.empty((dcfg.batch, dcfg.H, dcfg.dv), dtype=torch.bfloat16, device=dev)
+    counter = [0]
+
+    def dstep():
+        i = counter[0]
+        x = dq_s[i % n_tok]
+        binding.decode_step(*x, states, t_all[i], out=dout)
+        counter[0] += 1
+
+    for _ in range(max(args.warmup, 3)):
+        dstep()
+    first = counter[0]
+    d_ms_total = cuda_time(dstep, dsteps, stream)
+    d_ms_total = max_over_ranks(d_ms_total, ws)
+    assert binding.device_error() == 0
+    dbytes = sum(decode_bytes(t_all_np[i], dcfg.H, dcfg.dk, dcfg.dv, dcfg.Lmax) for i in range(first, first + dsteps))
+
+    return d_ms_total, dbytes, dsteps
+
+
 def run_lla(args, cfg):
     import torch
     from log_linear_attention_gb300 import binding
@@ -321,6 +361,14 @@ def run_lla(args, cfg):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     peaks = load_peaks()
+
+    if args.mode == "decode":
+        # decode launches only (a short target for profilers); not the benchmark line
+        d_ms_total, dbytes, dsteps = bench_decode(args, dev, stream, rank, ws)
+        if rank == 0:
+            print(json.dumps({"mode": "decode", "us_per_step": 1e3 * d_ms_total / dsteps,
+                              "gbs": dbytes / (d_ms_total / 1e3) / 1e9, "steps": dsteps}))
+        return 0
 
     # ---- inputs (per-rank seed: every rank runs the full workload: weak scaling)
     inp = inputs.make_prefill(cfg, seed=rank)
@@ -341,6 +389,13 @@ def run_lla(args, cfg):
     for _ in range(max(args.warmup, 3)):
         step()
     assert binding.device_error() == 0
+    if args.mode == "prefill":
+        # prefill launches only (a short target for profilers); not the benchmark line
+        ms = cuda_time(step, args.steps, stream) / args.steps
+        assert binding.device_error() == 0
+        if rank == 0:
+            print(json.dumps({"mode": "prefill", "config": cfg.name, "ms_per_step": ms, "steps": args.steps}))
+        return 0
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -397,34 +452,7 @@ def run_lla(args, cfg):
     h2d = sum(h.numel() * h.element_size() for h in host)
     d2h = out.numel() * out.element_size()
 
-    # ---- decode: 64 sequences x 16 heads, t ~ U[1, 65536), one-token steps
-    dcfg = inputs.DECODE_CONFIG
-    dsteps = args.decode_steps
-    t0v = inputs.make_positions(dcfg, rank)
-    t_all_np = t0v[None, :] + np.arange(dsteps + max(args.warmup, 3), dtype=np.int64)[:, None]
-    t_all = torch.from_numpy(t_all_np).to(dev)
-    n_tok = 32
-    toks = [inputs.make_decode_token(dcfg, rank * 1000 + i) for i in range(n_tok)]
-    dq_s = [(bf16(tk.bits["q"]).to(dev), bf16(tk.bits["k"]).to(dev), bf16(tk.bits["v"]).to(dev),
-             torch.from_numpy(tk.log_a).to(dev), torch.from_numpy(tk.lam).to(dev)) for tk in toks]
-    states = torch.randn((dcfg.batch, dcfg.H, dcfg.Lmax, dcfg.dk, dcfg.dv), device=dev,
-                         generator=torch.Generator(device=dev).manual_seed(rank)) * (dcfg.dk ** -0.5)
-    dout = torch.empty((dcfg.batch, dcfg.H, dcfg.dv), dtype=torch.bfloat16, device=dev)
-    counter = [0]
-
-    def dstep():
-        i = counter[0]
-        x = dq_s[i % n_tok]
-        binding.decode_step(*x, states, t_all[i], out=dout)
-        counter[0] += 1
-
-    for _ in range(max(args.warmup, 3)):
-        dstep()
-    first = counter[0]
-    d_ms_total = cuda_time(dstep, dsteps, stream)
-    d_ms_total = max_over_ranks(d_ms_total, ws)
-    assert binding.device_error() == 0
-    dbytes = sum(decode_bytes(t_all_np[i], dcfg.H, dcfg.dk, dcfg.dv, dcfg.Lmax) for i in range(first, first + dsteps))
+    d_ms_total, dbytes, dsteps = bench_decode(args, dev, stream, rank, ws)
     d_gbs = ws * dbytes / (d_ms_total / 1e3) / 1e9
 
     line = None
@@ -475,6 +503,8 @@ def main():
     ap.add_argument("--config", default="headline", choices=sorted(inputs.PREFILL_CONFIGS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--mode", choices=["all", "prefill", "decode"], default="all",
+                    help="prefill / decode: run only that workload's launches (profiling targets)")
     args = ap.parse_args()
     cfg = inputs.PREFILL_CONFIGS[args.config]
     if args.impl == "reference":

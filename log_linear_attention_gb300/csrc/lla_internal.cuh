@@ -73,9 +73,10 @@ struct TcPlan {
     int NT;                  // 128-token tiles per sequence
     int P;                   // node levels read: bitlength(NT - 1)
     int q;                   // log2 of the tiles per segment of the node kernel
+    int num_sms;             // persistent grid size of the output kernel
     int node_count;          // even-indexed nodes actually read, all levels
     int level_off[32];       // node index of (p, m = 0); node (p, m even) at level_off[p] + m / 2
-    size_t g_bytes, nodes_bytes, seg_bytes, total_bytes;
+    size_t g_bytes, nodes_bytes, seg_bytes, dtab_bytes, total_bytes;
 };
 
 bool tc_supported(int dtype, int dk, int dv, int T);

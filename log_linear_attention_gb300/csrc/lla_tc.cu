@@ -46,10 +46,6 @@ constexpr int kDk = 128;          // head dim of q/k on this path
 constexpr int kPanelBytes = 16384;  // 128 rows x 128 B (64 bf16), one SWIZZLE_128B panel
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kLog2e = 1.4426950408889634f;
-// Spare shared memory past the last operand: a descriptor-addressed read of an
-// MN-major operand spans at most one 16 KB panel stride plus 2 KB past its
-// start, and this keeps every such read inside the CTA's allocation.
-constexpr int kGuardBytes = 20480;
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -230,7 +226,7 @@ struct NodesSmem {
     static constexpr int kVBytes = (DV / 64) * kPanelBytes;     // V tile: 128 tokens x DV
     static constexpr int kStageBytes = kKBytes + kVBytes;
     static constexpr int kStages = 2;
-    static constexpr int kBytes = kStages * kStageBytes + 1024 + kGuardBytes;  // + alignment slack
+    static constexpr int kBytes = kStages * kStageBytes + 1024;  // + alignment slack
 };
 
 // grid (num_segments, B*H), 128 threads. Segment s covers tiles [s 2^q, (s+1) 2^q).
@@ -422,20 +418,50 @@ __global__ void __launch_bounds__(128, 1)
 
 // ------------------------------------------------------------------ tc_merge
 
-// Levels p = q+1 .. P-1 from full-segment totals (fp32 [BH][nseg][dk][DV], decayed to
-// each segment's end). In place: pyramid node (r, m) over segments overwrites segment
-// slot m 2^r. grid (dk*DV/256, BH), 256 threads, one matrix element per thread.
+// Two jobs, one launch, grid (dk*DV/256 + 1, BH), 256 threads:
+//  * blocks x < dk*DV/256 (only when P > q + 1): levels p = q+1 .. P-1 from the
+//    full-segment totals (fp32 [BH][nseg][dk][DV], decayed to each segment's
+//    end). In place: pyramid node (r, m) over segments overwrites segment slot
+//    m 2^r. One matrix element per thread.
+//  * block x = dk*DV/256: the per-tile decay table dtab[bh][j][p] (log2 units):
+//    sum of g over tiles [(j >> p) << p, j), the log-decay from the end of the
+//    block node (p, (j >> p) - 1) to the start of tile j, for each set bit p of j.
 __global__ void __launch_bounds__(256)
     tc_merge_kernel(float* __restrict__ seg_tot, const float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
-                    int NT, int q, int P, int nseg, int node_count, int msz, LevelOffsets lo) {
+                    float* __restrict__ dtab, int NT, int q, int P, int nseg, int node_count, int msz,
+                    LevelOffsets lo) {
     extern __shared__ float Gs[];  // nseg segment log-decay totals (updated in place per level)
     const int bh = blockIdx.y;
+    const float* gh = g_tiles + static_cast<size_t>(bh) * NT;
+    if (static_cast<int>(blockIdx.x) == msz / 256) {
+        for (int j = threadIdx.x; j < NT; j += blockDim.x) {
+            float d[16];
+#pragma unroll
+            for (int p = 0; p < 16; p++) d[p] = 0.f;
+            // walk down from tile j-1, closing the sum at each level's block boundary
+            float acc = 0.f;
+            int i = j - 1;
+#pragma unroll
+            for (int p = 0; p < 16; p++) {
+                if (p < P && ((j >> p) & 1)) {
+                    const int start = (j >> p) << p;
+                    for (; i >= start; i--) acc += gh[i];
+                    d[p] = acc * kLog2e;
+                }
+            }
+            float4* dst = reinterpret_cast<float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
+#pragma unroll
+            for (int c = 0; c < 4; c++) dst[c] = make_float4(d[4 * c], d[4 * c + 1], d[4 * c + 2], d[4 * c + 3]);
+        }
+        return;
+    }
+    if (q + 1 >= P) return;
     const int seg_tiles = 1 << q;
     for (int sgi = threadIdx.x; sgi < nseg; sgi += blockDim.x) {
         float acc = 0.f;
         for (int u = 0; u < seg_tiles; u++) {
             const int tile = sgi * seg_tiles + u;
-            if (tile < NT) acc += g_tiles[static_cast<size_t>(bh) * NT + tile];
+            if (tile < NT) acc += gh[tile];
         }
         Gs[sgi] = acc;
     }
@@ -465,250 +491,467 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------ tc_output
 
+// Persistent, warp-specialised output kernel. Each CTA walks tiles
+// idx = blockIdx.x + k * gridDim.x (head-major order, so the CTAs running at
+// one time share a few heads' nodes in L2). Roles (11 warps):
+//   warp 0        input producer: TMA of Q, K, V and a bulk copy of the tile's
+//                 log_a into input stage k % kStages; its 32 lanes copy the
+//                 tile's intra-tile lambda weights (levels 0..7) beside them.
+//   warp 1        MMA issuer (one lane): S_k = Q K^T into TMEM buffer k % 2;
+//                 then O = P V and L_p = Q B_p into the O and level slots of
+//                 TMEM, kLvSlots levels per round.
+//   warp 2        node producer (one lane): the Fenwick nodes each tile reads,
+//                 in order, into a ring of shared-memory slots.
+//   warps 3-10    epilogue, two warps per TMEM lane quadrant (thread = query
+//                 row), each owning half of the columns. Phase 1 builds P_k
+//                 (bf16, into the K buffer of the tile's stage) from S_k;
+//                 phase 2 writes O + sum_p r_p L_p with
+//                 r_p = lambda_t^(8+p) exp(cl_t + D_p).
+// With two input stages the input producer and the MMA warp run one tile
+// ahead (phase 1 of tile k+1 before phase 2 of tile k) and the epilogue
+// builds P of tile k+1 before finishing tile k. All hand-offs are mbarriers;
+// every wait is bounded.
 template <int DV>
-struct OutSmem {
-    static constexpr int kQ = 0;                                  // Q tile: 2 panels (K-major over dk)
-    static constexpr int kK = kQ + 2 * kPanelBytes;               // K tile: 2 panels
-    static constexpr int kV = kK + 2 * kPanelBytes;               // V tile: DV/64 panels (MN-major over dv)
-    static constexpr int kP = kV + (DV / 64) * kPanelBytes;       // P: 2 panels (K-major over keys)
-    static constexpr int kNode = kP + 2 * kPanelBytes;            // node slots
-    static constexpr int kSlots = 256 / DV;                       // TMEM level slots [256, 512)
+struct OutCfg {
+    static constexpr int kStages = DV == 64 ? 2 : 1;
+    static constexpr int kAhead = kStages - 1;
+    static constexpr int kQ = 0;
+    static constexpr int kK = 2 * kPanelBytes;  // K tile, then P of the same tile
+    static constexpr int kV = 4 * kPanelBytes;
+    static constexpr int kLogA = kV + (DV / 64) * kPanelBytes;  // 128 floats
+    static constexpr int kLam8 = kLogA + 512;                    // 128 x 8 floats
+    static constexpr int kStageBytes = (kLam8 + kTile * 8 * 4 + 1023) / 1024 * 1024;
+    static constexpr int kQkvBytes = (4 + DV / 64) * kPanelBytes;
     static constexpr int kNodeBytes = (DV / 64) * kPanelBytes;
-    static constexpr int kBytes = kNode + kSlots * kNodeBytes + 1024 + kGuardBytes;
+    static constexpr int kLvSlots = DV == 64 ? 3 : 1;  // TMEM level slots after O
+    static constexpr int kNodeSlots = DV == 64 ? 3 : 2;
+    static constexpr int kNodeBase = kStages * kStageBytes;
+    static constexpr int kBytes = kNodeBase + kNodeSlots * kNodeBytes + 1024;
+    static constexpr uint32_t kColO = 256;
+    static constexpr uint32_t kColLv = 256 + DV;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kThreads = (3 + kEpiWarps) * 32;
 };
 
-// grid (NT, B*H), 128 threads (thread t = query row t of the tile = TMEM lane t).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Contiguous global -> shared copy through the async proxy (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Bounded wait taken by a whole warp: every lane polls, the warp leaves together.
+__device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    const long long start = clock64();
+    while (true) {
+        const bool done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        const bool late = clock64() - start > kWaitCycles;
+        if (__any_sync(0xffffffffu, late)) return false;
+    }
+}
+
 template <int DV>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     tc_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_nodes,
                      const float* __restrict__ log_a, const float* __restrict__ lambda,
-                     const float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ out, int T, int NT, int L,
-                     int P, int node_count, LevelOffsets lo, int* err) {
-    using S = OutSmem<DV>;
+                     const float* __restrict__ dtab, __nv_bfloat16* __restrict__ out, int T, int NT, int L, int P,
+                     int node_count, LevelOffsets lo, int total_tiles, int* err) {
+    using C = OutCfg<DV>;
+    constexpr int NS = C::kStages;
+    constexpr int DH = DV / 2;  // columns of O per epilogue warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_qkv;
-    __shared__ uint64_t bar_node[S::kSlots];
-    __shared__ uint64_t bar_mma;
+    __shared__ uint64_t in_full[NS], in_empty[NS], s_full[2], s_free[2], p_ready[2];
+    __shared__ uint64_t node_full[C::kNodeSlots], node_empty[C::kNodeSlots];
+    __shared__ uint64_t lv_full, lv_free, drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ float warp_tot[4];
-    __shared__ float cl2_sh[kTile];
-    __shared__ float dsum2_sh[32];
-    __shared__ int fail_sh;
+    __shared__ float cl2_sh[2][kTile];
+    __shared__ float colw_sh[kTile];
+    __shared__ volatile int fail_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = blockIdx.x, bh = blockIdx.y;
-    const int row0 = bh * T + j * kTile;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kColO = 128;
-    constexpr uint32_t kColLv = 256;
-
-    // levels read by this tile: set bits of j
-    int lv[16];
-    int n_lv = 0;
-    for (int p = 0; p < P; p++)
-        if ((j >> p) & 1) lv[n_lv++] = p;
+    const int G = gridDim.x;
+    const int n_my = (total_tiles - static_cast<int>(blockIdx.x) + G - 1) / G;
 
     if (tid == 0) {
-        mbar_init(&bar_qkv, 1);
-        for (int s = 0; s < S::kSlots; s++) mbar_init(&bar_node[s], 1);
-        mbar_init(&bar_mma, 1);
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&in_full[s], 2);  // TMA/bulk bytes + the lambda copy
+            mbar_init(&in_empty[s], 1);
+        }
+        for (int s = 0; s < 2; s++) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_free[s], C::kEpiWarps);
+            mbar_init(&p_ready[s], C::kEpiWarps);
+        }
+        for (int s = 0; s < C::kNodeSlots; s++) {
+            mbar_init(&node_full[s], 1);
+            mbar_init(&node_empty[s], 1);
+        }
+        mbar_init(&lv_full, 1);
+        mbar_init(&lv_free, C::kEpiWarps);
+        mbar_init(&drain, 1);
         fence_mbar_init();
         fail_sh = 0;
     }
-    if (warp == 0) tmem_alloc(&tmem_base_sh, kTmemCols);
+    if (warp == 1) tmem_alloc(&tmem_base_sh, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    auto issue_node = [&](int slot, int p) {
-        const int m = (j >> p) - 1;
-        const int nrow = (bh * node_count + lo.off[p] + (m >> 1)) * kDk;
-        mbar_expect_tx(&bar_node[slot], S::kNodeBytes);
-#pragma unroll
-        for (int c = 0; c < DV / 64; c++)
-            tma_load_2d(smem + S::kNode + slot * S::kNodeBytes + c * kPanelBytes, &tm_nodes, &bar_node[slot], 64 * c,
-                        nrow);
+    auto tile_of = [&](int k, int& bh, int& j) {
+        const int idx = static_cast<int>(blockIdx.x) + k * G;
+        bh = idx / NT;
+        j = idx - bh * NT;
     };
-    if (tid == 0) {
-        mbar_expect_tx(&bar_qkv, (4 + DV / 64) * kPanelBytes);
-        tma_load_2d(smem + S::kQ, &tm_q, &bar_qkv, 0, row0);
-        tma_load_2d(smem + S::kQ + kPanelBytes, &tm_q, &bar_qkv, 64, row0);
-        tma_load_2d(smem + S::kK, &tm_k, &bar_qkv, 0, row0);
-        tma_load_2d(smem + S::kK + kPanelBytes, &tm_k, &bar_qkv, 64, row0);
-#pragma unroll
-        for (int c = 0; c < DV / 64; c++) tma_load_2d(smem + S::kV + c * kPanelBytes, &tm_v, &bar_qkv, 64 * c, row0);
-        for (int s = 0; s < S::kSlots && s < n_lv; s++) issue_node(s, lv[s]);
-    }
+    // single-thread bounded wait; after a failure anywhere it returns false at once
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (fail_sh) return false;
+        if (mbar_wait(bar, parity)) return true;
+        fail_sh = 1;
+        record_error(err, kDevTimeout);
+        return false;
+    };
+    // warp-uniform bounded wait with the same failure short-cut
+    auto ewait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (__any_sync(0xffffffffu, fail_sh != 0)) return false;
+        if (warp_wait(bar, parity)) return true;
+        if (lane == 0) {
+            fail_sh = 1;
+            record_error(err, kDevTimeout);
+        }
+        return false;
+    };
 
-    // decays: chunk-local inclusive cumsum (in log2 units) and, per set bit p of j,
-    // the summed log-decay of the tiles between the node's block end and this tile
-    const float a = log_a[static_cast<size_t>(row0) + tid];
-    const float cl = block_scan128(a, warp_tot);
-    cl2_sh[tid] = cl * kLog2e;
     if (warp == 0) {
-        for (int x = 0; x < n_lv; x++) {
-            const int p = lv[x];
-            float d = 0.f;
-            for (int i = ((j >> p) << p) + lane; i < j; i += 32) d += g_tiles[static_cast<size_t>(bh) * NT + i];
+        // ---------------------------------------------------------------- input producer
+        int n_in = 0;
+        for (int k = 0; k < n_my; k++) {
+            int bh, j;
+            tile_of(k, bh, j);
+            const int row0 = bh * T + j * kTile;
+            const int s = k % NS;
+            if (k >= NS && !ewait(&in_empty[s], ((k / NS) - 1) & 1)) break;
+            uint8_t* st = smem + s * C::kStageBytes;
+            if (lane == 0) {
+                mbar_expect_tx(&in_full[s], C::kQkvBytes + 512);
+                tma_load_2d(st + C::kQ, &tm_q, &in_full[s], 0, row0);
+                tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[s], 64, row0);
+                tma_load_2d(st + C::kK, &tm_k, &in_full[s], 0, row0);
+                tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &in_full[s], 64, row0);
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-            if (lane == 0) dsum2_sh[x] = d * kLog2e;
-        }
-    }
-    __syncthreads();
-
-    const int t = tid;
-    const float cl2_t = cl2_sh[t];
-    const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
-    float lam_in[8];
-#pragma unroll
-    for (int l = 0; l < 8; l++) lam_in[l] = (l < L) ? lam_row[l] : 0.f;
-
-    bool ok = mbar_wait(&bar_qkv, 0);
-    if (!ok) atomicExch(&fail_sh, 1);
-    __syncthreads();
-    int mma_phase = 0;
-    float acc[DV];
-#pragma unroll
-    for (int c = 0; c < DV; c++) acc[c] = 0.f;
-
-    if (!fail_sh) {
-        // S = Q K^T: M = 128 queries, N = 128 keys, K = dk (both operands K-major)
-        if (tid == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kTile, kTile, 0, 0);
-            const uint32_t qb = smem_u32(smem + S::kQ), kb = smem_u32(smem + S::kK);
-#pragma unroll
-            for (int kk = 0; kk < kDk / 16; kk++) {
-                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                mma_bf16(tmem, sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+                for (int c = 0; c < DV / 64; c++)
+                    tma_load_2d(st + C::kV + c * kPanelBytes, &tm_v, &in_full[s], 64 * c, row0);
+                bulk_load(st + C::kLogA, log_a + row0, 512, &in_full[s]);
             }
-            mma_commit(&bar_mma);
+            // lambda_t^(0..7) of the tile's 128 rows (rows are L floats apart, not 16-byte aligned)
+            float* lam8 = reinterpret_cast<float*>(st + C::kLam8);
+#pragma unroll
+            for (int rr = 0; rr < 4; rr++) {
+                const int t = lane * 4 + rr;
+                const float* src = lambda + static_cast<size_t>(row0 + t) * L;
+#pragma unroll
+                for (int l = 0; l < 8; l++) lam8[t * 8 + l] = src[l];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&in_full[s]);
+            n_in = k + 1;
         }
-        if (!mbar_wait(&bar_mma, mma_phase)) atomicExch(&fail_sh, 1);
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // P[t][s] = S[t][s] * exp(cl_t - cl_s) * lambda_t^(level(t,s)) for s <= t, as bf16, K-major SW128
-        uint8_t* pbase = smem + S::kP;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-            float sv[32];
-            tmem_ld32(tmem + lane_base + c0, sv);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                float v2[2];
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int s = c0 + e + h;
-                    float val = 0.f;
-                    if (s <= t) {
-                        const int lvl = 32 - __clz(t ^ s);
-                        val = sv[e + h] * exp2f(cl2_t - cl2_sh[s]) * lam_in[lvl];
+        if (fail_sh && lane == 0) {
+            // let this CTA's copies land before its shared memory is released
+            for (int k = n_in - NS; k < n_in; k++)
+                if (k >= 0) mbar_wait(&in_full[k % NS], (k / NS) & 1);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- node producer
+        if (lane == 0) {
+            int gn = 0;
+            bool ok = true;
+            for (int k = 0; k < n_my && ok; k++) {
+                int bh, j;
+                tile_of(k, bh, j);
+                for (int p = 0; p < P; p++) {
+                    if (((j >> p) & 1) == 0) continue;
+                    const int slot = gn % C::kNodeSlots;
+                    if (gn >= C::kNodeSlots && !wait(&node_empty[slot], ((gn / C::kNodeSlots) - 1) & 1)) {
+                        ok = false;
+                        break;
                     }
-                    v2[h] = val;
-                }
-                pk[e >> 1] = pack_bf16(v2[0], v2[1]);
-            }
-            uint8_t* panel = pbase + (c0 >> 6) * kPanelBytes;
-            const int chunk0 = (c0 & 63) >> 3;
+                    const int m = (j >> p) - 1;
+                    const int nrow = (bh * node_count + lo.off[p] + (m >> 1)) * kDk;
+                    mbar_expect_tx(&node_full[slot], C::kNodeBytes);
 #pragma unroll
-            for (int c = 0; c < 4; c++)
-                *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0 + c)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    for (int c = 0; c < DV / 64; c++)
+                        tma_load_2d(smem + C::kNodeBase + slot * C::kNodeBytes + c * kPanelBytes, &tm_nodes,
+                                    &node_full[slot], 64 * c, nrow);
+                    gn++;
+                }
+            }
+            if (fail_sh) {
+                for (int g = gn - C::kNodeSlots; g < gn; g++)
+                    if (g >= 0) mbar_wait(&node_full[g % C::kNodeSlots], (g / C::kNodeSlots) & 1);
+            }
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    }
-
-    // O = P V (+ level reads), in rounds of up to kSlots levels
-    int node_phase[S::kSlots];
-#pragma unroll
-    for (int s = 0; s < S::kSlots; s++) node_phase[s] = 0;
-    const int rounds = n_lv == 0 ? 1 : (n_lv + S::kSlots - 1) / S::kSlots;
-    for (int rd = 0; rd < rounds && !fail_sh; rd++) {
-        const int first = rd * S::kSlots;
-        const int cnt = min(S::kSlots, n_lv - first);
-        if (tid == 0) {
-            if (rd > 0)
-                for (int s = 0; s < cnt; s++) issue_node(s, lv[first + s]);
-            const uint32_t qb = smem_u32(smem + S::kQ);
-            if (rd == 0) {
-                constexpr uint32_t idesc = idesc_bf16(kTile, DV, 0, 1);
-                const uint32_t pb = smem_u32(smem + S::kP), vb = smem_u32(smem + S::kV);
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; kk++) {
-                    const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                    mma_bf16(tmem + kColO, sdesc(pb + aoff, 16, 1024), sdesc(vb + kk * 2048, kPanelBytes, 1024), idesc,
-                             kk > 0 ? 1u : 0u);
-                }
-            }
-            for (int s = 0; s < cnt; s++) {
-                if (!mbar_wait(&bar_node[s], node_phase[s])) {
-                    atomicExch(&fail_sh, 1);
-                    break;
-                }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int gn = 0, round = 0;
+            constexpr uint32_t kIdS = idesc_bf16(kTile, kTile, 0, 0);
+            constexpr uint32_t kIdO = idesc_bf16(kTile, DV, 0, 1);
+            auto phase1 = [&](int k) -> bool {
+                const int s = k % NS, b = k & 1;
+                if (!wait(&in_full[s], (k / NS) & 1)) return false;
+                if (k >= 2 && !wait(&s_free[b], ((k >> 1) - 1) & 1)) return false;
                 tc_fence_after();
-                constexpr uint32_t idesc = idesc_bf16(kTile, DV, 0, 1);
-                const uint32_t nb = smem_u32(smem + S::kNode + s * S::kNodeBytes);
+                const uint32_t qb = smem_u32(smem + s * C::kStageBytes + C::kQ);
+                const uint32_t kb = smem_u32(smem + s * C::kStageBytes + C::kK);
 #pragma unroll
                 for (int kk = 0; kk < kDk / 16; kk++) {
-                    const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                    mma_bf16(tmem + kColLv + s * DV, sdesc(qb + aoff, 16, 1024),
-                             sdesc(nb + kk * 2048, kPanelBytes, 1024), idesc, kk > 0 ? 1u : 0u);
+                    const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                    mma_bf16(tmem + b * kTile, sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024), kIdS,
+                             kk > 0 ? 1u : 0u);
                 }
+                mma_commit(&s_full[b]);
+                return true;
+            };
+            auto phase2 = [&](int k) -> bool {
+                int bh, j;
+                tile_of(k, bh, j);
+                const int s = k % NS, b = k & 1;
+                if (!wait(&p_ready[b], (k >> 1) & 1)) return false;
+                tc_fence_after();
+                const uint32_t qb = smem_u32(smem + s * C::kStageBytes + C::kQ);
+                const uint32_t pb = smem_u32(smem + s * C::kStageBytes + C::kK);
+                const uint32_t vb = smem_u32(smem + s * C::kStageBytes + C::kV);
+                const int n_lv = __popc(static_cast<unsigned>(j) & ((1u << P) - 1u));
+                const int rounds = n_lv == 0 ? 1 : (n_lv + C::kLvSlots - 1) / C::kLvSlots;
+                int p = 0;
+                for (int r = 0; r < rounds; r++, round++) {
+                    if (round > 0 && !wait(&lv_free, (round - 1) & 1)) return false;
+                    tc_fence_after();
+                    if (r == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; kk++) {
+                            const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                            mma_bf16(tmem + C::kColO, sdesc(pb + aoff, 16, 1024),
+                                     sdesc(vb + kk * 2048, kPanelBytes, 1024), kIdO, kk > 0 ? 1u : 0u);
+                        }
+                    }
+                    for (int sl = 0; sl < C::kLvSlots; sl++) {
+                        while (p < P && ((j >> p) & 1) == 0) p++;
+                        if (p >= P) break;
+                        p++;
+                        const int slot = gn % C::kNodeSlots;
+                        if (!wait(&node_full[slot], (gn / C::kNodeSlots) & 1)) return false;
+                        tc_fence_after();
+                        const uint32_t nb = smem_u32(smem + C::kNodeBase + slot * C::kNodeBytes);
+                        const uint32_t dcol = C::kColLv + sl * DV;
+#pragma unroll
+                        for (int kk = 0; kk < kDk / 16; kk++) {
+                            const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                            mma_bf16(tmem + dcol, sdesc(qb + aoff, 16, 1024), sdesc(nb + kk * 2048, kPanelBytes, 1024),
+                                     kIdO, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&node_empty[slot]);
+                        gn++;
+                    }
+                    mma_commit(&lv_full);
+                }
+                mma_commit(&in_empty[s]);
+                return true;
+            };
+            bool ok = true;
+            for (int k = 0; k < C::kAhead && k < n_my && ok; k++) ok = phase1(k);
+            for (int k = 0; k < n_my && ok; k++) {
+                if (k + C::kAhead < n_my && !phase1(k + C::kAhead)) break;
+                if (!phase2(k)) break;
             }
-            mma_commit(&bar_mma);
+            // every MMA issued by this CTA has completed before TMEM is released
+            mma_commit(&drain);
+            mbar_wait(&drain, 0);
         }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int ew = warp - 3;
+        const int quad = warp & 3;
+        const int half = ew >> 2;
+        const int t = quad * 32 + lane;  // query row of the tile = TMEM lane
+        const int q32 = quad * 32;
+        const uint32_t lane_base = static_cast<uint32_t>(q32) << 16;
+        int round = 0;
+
+        // Phase 1: P_k. The epilogue warps never leave their tile loop early, so
+        // every named barrier is reached by all eight of them.
+        auto epi1 = [&](int k) {
+            const int s = k % NS, b = k & 1;
+            const uint8_t* st = smem + s * C::kStageBytes;
+            const bool have = ewait(&in_full[s], (k / NS) & 1);
+            float incl = 0.f;
+            if (half == 0) {
+                incl = have ? reinterpret_cast<const float*>(st + C::kLogA)[t] : 0.f;
 #pragma unroll
-        for (int s = 0; s < S::kSlots; s++)
-            if (s < cnt) node_phase[s] ^= 1;
-        if (!mbar_wait(&bar_mma, mma_phase)) atomicExch(&fail_sh, 1);
-        mma_phase ^= 1;
-        tc_fence_after();
-        __syncthreads();
-        if (fail_sh) break;
-        if (rd == 0) {
-#pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 32) tmem_ld32(tmem + lane_base + kColO + c0, acc + c0);
-        }
-        for (int s = 0; s < cnt; s++) {
-            const int x = first + s;
-            const int p = lv[x];
-            const float r = lam_row[8 + p] * exp2f(cl2_t + dsum2_sh[x]);
-#pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 32) {
-                float lvv[32];
-                tmem_ld32(tmem + lane_base + kColLv + s * DV + c0, lvv);
-#pragma unroll
-                for (int e = 0; e < 32; e++) acc[c0 + e] = fmaf(r, lvv[e], acc[c0 + e]);
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += y;
+                }
+                if (lane == 31) warp_tot[quad] = incl;
             }
+            epi_sync();
+            if (half == 0) {
+                float base = 0.f;
+                for (int w = 0; w < quad; w++) base += warp_tot[w];
+                cl2_sh[b][t] = (incl + base) * kLog2e;
+            }
+            epi_sync();
+            const float cl2_t = cl2_sh[b][t];
+            // column weights exp(decay from s to the end of its 32-column chunk), <= 1
+            if (half == 0) colw_sh[t] = exp2f(cl2_sh[b][t | 31] - cl2_t);
+            float lam_in[8];
+            const float* lam8 = reinterpret_cast<const float*>(st + C::kLam8) + t * 8;
+#pragma unroll
+            for (int l = 0; l < 8; l++) lam_in[l] = lam8[l];
+            epi_sync();  // colw visible
+            if (!have || !ewait(&s_full[b], (k >> 1) & 1)) return;
+            tc_fence_after();
+            uint8_t* pbase = smem + s * C::kStageBytes + C::kK;
+#pragma unroll 1
+            for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
+                uint32_t pk[16];
+                if (c0 > q32) {
+                    // keys after every query row of this warp
+#pragma unroll
+                    for (int e = 0; e < 16; e++) pk[e] = 0u;
+                } else {
+                    float sv[32];
+                    tmem_ld32(tmem + lane_base + b * kTile + c0, sv);
+                    if (c0 < q32) {
+                        // keys before every row of this warp: one level per row, factorised decay
+                        const int lvl = 32 - __clz(t ^ c0);
+                        float lw = lam_in[0];
+#pragma unroll
+                        for (int l = 1; l < 8; l++) lw = (lvl == l) ? lam_in[l] : lw;
+                        const float rowf = exp2f(cl2_t - cl2_sh[b][c0 + 31]) * lw;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2)
+                            pk[e >> 1] = pack_bf16(sv[e] * rowf * colw_sh[c0 + e], sv[e + 1] * rowf * colw_sh[c0 + e + 1]);
+                    } else {
+                        // diagonal chunk: causal mask and per-key levels 0..5
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float v2[2];
+#pragma unroll
+                            for (int h = 0; h < 2; h++) {
+                                const int sidx = c0 + e + h;
+                                float val = 0.f;
+                                if (sidx <= t) {
+                                    const int lvl = 32 - __clz(t ^ sidx);
+                                    float lw = lam_in[0];
+#pragma unroll
+                                    for (int l = 1; l < 6; l++) lw = (lvl == l) ? lam_in[l] : lw;
+                                    val = sv[e + h] * exp2f(cl2_t - cl2_sh[b][sidx]) * lw;
+                                }
+                                v2[h] = val;
+                            }
+                            pk[e >> 1] = pack_bf16(v2[0], v2[1]);
+                        }
+                    }
+                }
+                uint8_t* panel = pbase + (c0 >> 6) * kPanelBytes;
+                const int chunk0 = (c0 & 63) >> 3;
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+                    *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0 + c)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&p_ready[b]);
+                mbar_arrive(&s_free[b]);
+            }
+        };
+
+        // Phase 2: O + sum_p r_p L_p for this warp's half of the columns.
+        auto epi2 = [&](int k) {
+            int bh, j;
+            tile_of(k, bh, j);
+            const int b = k & 1;
+            const int row0 = bh * T + j * kTile;
+            // per-row level weights (issued before waiting on the MMAs)
+            const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
+            const float4* drow = reinterpret_cast<const float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
+            float d2[16];
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const float4 x = drow[c];
+                d2[4 * c] = x.x; d2[4 * c + 1] = x.y; d2[4 * c + 2] = x.z; d2[4 * c + 3] = x.w;
+            }
+            const float cl2_t = cl2_sh[b][t];
+            float rr[16];
+#pragma unroll
+            for (int p = 0; p < 16; p++) {
+                const bool on = p < P && ((j >> p) & 1);
+                rr[p] = on ? lam_row[8 + p] * exp2f(cl2_t + d2[p]) : 0.f;
+            }
+            float acc[DH];
+            const int n_lv = __popc(static_cast<unsigned>(j) & ((1u << P) - 1u));
+            const int rounds = n_lv == 0 ? 1 : (n_lv + C::kLvSlots - 1) / C::kLvSlots;
+            for (int r = 0; r < rounds; r++, round++) {
+                if (!ewait(&lv_full, round & 1)) return;
+                tc_fence_after();
+                if (r == 0) {
+#pragma unroll
+                    for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tmem + lane_base + C::kColO + half * DH + c0, acc + c0);
+                }
+#pragma unroll
+                for (int p = 0; p < 16; p++) {
+                    if (p < P && ((j >> p) & 1)) {
+                        const int x = __popc(static_cast<unsigned>(j) & ((1u << p) - 1u));
+                        if (x / C::kLvSlots == r) {
+                            const uint32_t col = C::kColLv + (x % C::kLvSlots) * DV + half * DH;
+#pragma unroll
+                            for (int c0 = 0; c0 < DH; c0 += 32) {
+                                float lvv[32];
+                                tmem_ld32(tmem + lane_base + col + c0, lvv);
+#pragma unroll
+                                for (int e = 0; e < 32; e++) acc[c0 + e] = fmaf(rr[p], lvv[e], acc[c0 + e]);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&lv_free);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV + half * DH);
+#pragma unroll
+            for (int c = 0; c < DH / 8; c++)
+                dst[c] = make_uint4(pack_bf16(acc[8 * c], acc[8 * c + 1]), pack_bf16(acc[8 * c + 2], acc[8 * c + 3]),
+                                    pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
+        };
+
+        for (int k = 0; k < C::kAhead && k < n_my; k++) epi1(k);
+        for (int k = 0; k < n_my; k++) {
+            if (k + C::kAhead < n_my) epi1(k + C::kAhead);
+            epi2(k);
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
 
-    if (!fail_sh) {
-        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV);
-#pragma unroll
-        for (int c = 0; c < DV / 8; c++)
-            dst[c] = make_uint4(pack_bf16(acc[8 * c], acc[8 * c + 1]), pack_bf16(acc[8 * c + 2], acc[8 * c + 3]),
-                                pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
-    } else {
-        if (tid == 0) record_error(err, kDevTimeout);
-        mbar_wait(&bar_mma, mma_phase ^ 1);
-        mbar_try_wait(&bar_qkv, 0);
-    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -767,6 +1010,7 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
     float* g_tiles = reinterpret_cast<float*>(ws);
     __nv_bfloat16* nodes = reinterpret_cast<__nv_bfloat16*>(ws + pl.g_bytes);
     float* seg_tot = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes);
+    float* dtab = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes + pl.seg_bytes);
     LevelOffsets lo;
     for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
     const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
@@ -789,20 +1033,23 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
                                                                    qlog, pl.node_count, lo, cols, err);
         note_launch(stream, "tc_nodes");
     }
-    if (pl.P > qlog + 1) {
+    {
         const int msz = kDk * DV;
-        tc_merge_kernel<<<dim3(msz / 256, BH), 256, nseg * sizeof(float), stream>>>(
-            seg_tot, g_tiles, nodes, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
+        tc_merge_kernel<<<dim3(msz / 256 + 1, BH), 256, nseg * sizeof(float), stream>>>(
+            seg_tot, g_tiles, nodes, dtab, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
         note_launch(stream, "tc_merge");
     }
     {
-        const int smem = OutSmem<DV>::kBytes;
+        const int smem = OutCfg<DV>::kBytes;
         cudaError_t e = cudaFuncSetAttribute(tc_output_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const int L = bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
-        tc_output_kernel<DV><<<dim3(pl.NT, BH), 128, smem, stream>>>(tq, tk, tv, tn, log_a, lambda, g_tiles,
-                                                                     static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L,
-                                                                     pl.P, pl.node_count, lo, err);
+        const int total = BH * pl.NT;
+        const int grid = total < pl.num_sms ? total : pl.num_sms;
+        tc_output_kernel<DV><<<grid, OutCfg<DV>::kThreads, smem, stream>>>(tq, tk, tv, tn, log_a, lambda, dtab,
+                                                                            static_cast<__nv_bfloat16*>(out), pl.T,
+                                                                            pl.NT, L, pl.P, pl.node_count, lo, total,
+                                                                            err);
         note_launch(stream, "tc_output");
     }
     return cudaGetLastError();
@@ -817,6 +1064,14 @@ bool tc_supported(int dtype, int dk, int dv, int T) {
 bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* pl) {
     pl->B = B; pl->H = H; pl->T = T; pl->dk = dk; pl->dv = dv;
     pl->NT = T / kTile;
+    {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+            cudaGetLastError();
+            sms = 152;
+        }
+        pl->num_sms = sms;
+    }
     pl->P = bitlength(static_cast<int64_t>(pl->NT) - 1);
     const int BH = B * H;
     pl->q = choose_q(BH, pl->NT, dv);
@@ -834,8 +1089,9 @@ bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* pl) {
     const size_t msz = static_cast<size_t>(dk) * dv;
     pl->g_bytes = (static_cast<size_t>(BH) * pl->NT * sizeof(float) + 1023) / 1024 * 1024;
     pl->nodes_bytes = (static_cast<size_t>(BH) * pl->node_count * msz * 2 + 1023) / 1024 * 1024;
-    pl->seg_bytes = static_cast<size_t>(BH) * nseg * msz * sizeof(float);
-    pl->total_bytes = pl->g_bytes + pl->nodes_bytes + pl->seg_bytes;
+    pl->seg_bytes = (static_cast<size_t>(BH) * nseg * msz * sizeof(float) + 1023) / 1024 * 1024;
+    pl->dtab_bytes = static_cast<size_t>(BH) * pl->NT * 16 * sizeof(float);
+    pl->total_bytes = pl->g_bytes + pl->nodes_bytes + pl->seg_bytes + pl->dtab_bytes;
     return true;
 }
 
