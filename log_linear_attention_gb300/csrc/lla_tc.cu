@@ -141,6 +141,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
     uint32_t r[32];
 #pragma unroll
@@ -494,19 +508,21 @@ __global__ void __launch_bounds__(256)
 // Persistent, warp-specialised output kernel. Each CTA walks tiles
 // idx = blockIdx.x + k * gridDim.x (head-major order, so the CTAs running at
 // one time share a few heads' nodes in L2). Roles (11 warps):
-//   warp 0        input producer: TMA of Q, K, V and a bulk copy of the tile's
-//                 log_a into input stage k % kStages; its 32 lanes copy the
-//                 tile's intra-tile lambda weights (levels 0..7) beside them.
+//   warp 0        input producer: TMA of Q, K, V into input stage k % kStages;
+//                 its 32 lanes also stage the tile's in-tile decay prefix
+//                 cl_t (log2 units), the column weights exp(cl_{s|31} - cl_s)
+//                 and lambda levels 0..7 of every row beside them.
 //   warp 1        MMA issuer (one lane): S_k = Q K^T into TMEM buffer k % 2;
 //                 then O = P V and L_p = Q B_p into the O and level slots of
 //                 TMEM, kLvSlots levels per round.
 //   warp 2        node producer (one lane): the Fenwick nodes each tile reads,
 //                 in order, into a ring of shared-memory slots.
 //   warps 3-10    epilogue, two warps per TMEM lane quadrant (thread = query
-//                 row), each owning half of the columns. Phase 1 builds P_k
-//                 (bf16, into the K buffer of the tile's stage) from S_k;
-//                 phase 2 writes O + sum_p r_p L_p with
-//                 r_p = lambda_t^(8+p) exp(cl_t + D_p).
+//                 row), each owning half of the columns, with no barrier among
+//                 them. Phase 1 builds P_k (bf16, into the K buffer of the
+//                 tile's stage) from S_k; phase 2 writes O + sum_p r_p L_p with
+//                 r_p = lambda_t^(8+p) exp(cl_t + D_p), whose inputs are fetched
+//                 while phase 1 of the next tile runs.
 // With two input stages the input producer and the MMA warp run one tile
 // ahead (phase 1 of tile k+1 before phase 2 of tile k) and the epilogue
 // builds P of tile k+1 before finishing tile k. All hand-offs are mbarriers;
@@ -518,8 +534,9 @@ struct OutCfg {
     static constexpr int kQ = 0;
     static constexpr int kK = 2 * kPanelBytes;  // K tile, then P of the same tile
     static constexpr int kV = 4 * kPanelBytes;
-    static constexpr int kLogA = kV + (DV / 64) * kPanelBytes;  // 128 floats
-    static constexpr int kLam8 = kLogA + 512;                    // 128 x 8 floats
+    static constexpr int kCl2 = kV + (DV / 64) * kPanelBytes;  // 128 floats: in-tile log2 decay prefix
+    static constexpr int kColw = kCl2 + 512;                     // 128 floats: column weights
+    static constexpr int kLam8 = kColw + 512;                    // 128 x 8 floats: lambda levels 0..7
     static constexpr int kStageBytes = (kLam8 + kTile * 8 * 4 + 1023) / 1024 * 1024;
     static constexpr int kQkvBytes = (4 + DV / 64) * kPanelBytes;
     static constexpr int kNodeBytes = (DV / 64) * kPanelBytes;
@@ -537,16 +554,6 @@ struct OutCfg {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-
-// Contiguous global -> shared copy through the async proxy (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Bounded wait taken by a whole warp: every lane polls, the warp leaves together.
 __device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
@@ -575,9 +582,6 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     __shared__ uint64_t node_full[C::kNodeSlots], node_empty[C::kNodeSlots];
     __shared__ uint64_t lv_full, lv_free, drain;
     __shared__ uint32_t tmem_base_sh;
-    __shared__ float warp_tot[4];
-    __shared__ float cl2_sh[2][kTile];
-    __shared__ float colw_sh[kTile];
     __shared__ volatile int fail_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < NS; s++) {
-            mbar_init(&in_full[s], 2);  // TMA/bulk bytes + the lambda copy
+            mbar_init(&in_full[s], 2);  // TMA bytes + the staged per-row scalars
             mbar_init(&in_empty[s], 1);
         }
         for (int s = 0; s < 2; s++) {
@@ -645,7 +649,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
             if (k >= NS && !ewait(&in_empty[s], ((k / NS) - 1) & 1)) break;
             uint8_t* st = smem + s * C::kStageBytes;
             if (lane == 0) {
-                mbar_expect_tx(&in_full[s], C::kQkvBytes + 512);
+                mbar_expect_tx(&in_full[s], C::kQkvBytes);
                 tma_load_2d(st + C::kQ, &tm_q, &in_full[s], 0, row0);
                 tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[s], 64, row0);
                 tma_load_2d(st + C::kK, &tm_k, &in_full[s], 0, row0);
@@ -653,7 +657,28 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < DV / 64; c++)
                     tma_load_2d(st + C::kV + c * kPanelBytes, &tm_v, &in_full[s], 64 * c, row0);
-                bulk_load(st + C::kLogA, log_a + row0, 512, &in_full[s]);
+            }
+            // in-tile inclusive decay prefix: lane owns rows 4 lane .. 4 lane + 3
+            const float4 a4 = *reinterpret_cast<const float4*>(log_a + row0 + lane * 4);
+            float c4[4] = {a4.x, a4.x + a4.y, a4.x + a4.y + a4.z, a4.x + a4.y + a4.z + a4.w};
+            float incl = c4[3];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const float excl = incl - c4[3];
+            float* cl2 = reinterpret_cast<float*>(st + C::kCl2);
+            float* colw = reinterpret_cast<float*>(st + C::kColw);
+            float c2[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) c2[e] = (c4[e] + excl) * kLog2e;
+            // decay prefix at the last row of this lane's 32-row chunk (row t | 31 is lane | 7, element 3)
+            const float chunk_end = __shfl_sync(0xffffffffu, c2[3], lane | 7);
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                cl2[lane * 4 + e] = c2[e];
+                colw[lane * 4 + e] = exp2f(chunk_end - c2[e]);
             }
             // lambda_t^(0..7) of the tile's 128 rows (rows are L floats apart, not 16-byte aligned)
             float* lam8 = reinterpret_cast<float*>(st + C::kLam8);
@@ -786,93 +811,93 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
         const int ew = warp - 3;
         const int quad = warp & 3;
         const int half = ew >> 2;
+        (void)quad;
         const int t = quad * 32 + lane;  // query row of the tile = TMEM lane
         const int q32 = quad * 32;
         const uint32_t lane_base = static_cast<uint32_t>(q32) << 16;
         int round = 0;
 
-        // Phase 1: P_k. The epilogue warps never leave their tile loop early, so
-        // every named barrier is reached by all eight of them.
+        // Inputs of phase 2 of a tile, fetched one phase early: lambda_t^(8+p) and the
+        // decay-table row of the tile, plus the row's decay prefix.
+        float pre_lam[16], pre_d[16];
+        float cl2_even = 0.f, cl2_odd = 0.f;
+        auto prefetch2 = [&](int k) {
+            int bh, j;
+            tile_of(k, bh, j);
+            const int row0 = bh * T + j * kTile;
+            const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
+            const float4* drow = reinterpret_cast<const float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const float4 x = drow[c];
+                pre_d[4 * c] = x.x; pre_d[4 * c + 1] = x.y; pre_d[4 * c + 2] = x.z; pre_d[4 * c + 3] = x.w;
+            }
+#pragma unroll
+            for (int p = 0; p < 16; p++) pre_lam[p] = (p < P && ((j >> p) & 1)) ? lam_row[8 + p] : 0.f;
+        };
+
+        // Phase 1: P_k. The two warps of a lane quadrant split every 32-key chunk,
+        // 16 keys each, so the masked diagonal chunk is shared evenly.
         auto epi1 = [&](int k) {
             const int s = k % NS, b = k & 1;
             const uint8_t* st = smem + s * C::kStageBytes;
-            const bool have = ewait(&in_full[s], (k / NS) & 1);
-            float incl = 0.f;
-            if (half == 0) {
-                incl = have ? reinterpret_cast<const float*>(st + C::kLogA)[t] : 0.f;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += y;
-                }
-                if (lane == 31) warp_tot[quad] = incl;
-            }
-            epi_sync();
-            if (half == 0) {
-                float base = 0.f;
-                for (int w = 0; w < quad; w++) base += warp_tot[w];
-                cl2_sh[b][t] = (incl + base) * kLog2e;
-            }
-            epi_sync();
-            const float cl2_t = cl2_sh[b][t];
-            // column weights exp(decay from s to the end of its 32-column chunk), <= 1
-            if (half == 0) colw_sh[t] = exp2f(cl2_sh[b][t | 31] - cl2_t);
+            if (!ewait(&in_full[s], (k / NS) & 1)) return;
+            const float* cl2 = reinterpret_cast<const float*>(st + C::kCl2);
+            const float* colw = reinterpret_cast<const float*>(st + C::kColw);
+            const float cl2_t = cl2[t];
+            if (b) cl2_odd = cl2_t; else cl2_even = cl2_t;
             float lam_in[8];
-            const float* lam8 = reinterpret_cast<const float*>(st + C::kLam8) + t * 8;
-#pragma unroll
-            for (int l = 0; l < 8; l++) lam_in[l] = lam8[l];
-            epi_sync();  // colw visible
-            if (!have || !ewait(&s_full[b], (k >> 1) & 1)) return;
+            const float4* lam8 = reinterpret_cast<const float4*>(st + C::kLam8) + t * 2;
+            {
+                const float4 x0 = lam8[0], x1 = lam8[1];
+                lam_in[0] = x0.x; lam_in[1] = x0.y; lam_in[2] = x0.z; lam_in[3] = x0.w;
+                lam_in[4] = x1.x; lam_in[5] = x1.y; lam_in[6] = x1.z; lam_in[7] = x1.w;
+            }
+            if (!ewait(&s_full[b], (k >> 1) & 1)) return;
             tc_fence_after();
             uint8_t* pbase = smem + s * C::kStageBytes + C::kK;
 #pragma unroll 1
-            for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
-                uint32_t pk[16];
+            for (int c0 = 0; c0 < kTile; c0 += 32) {
+                const int cb = c0 + half * 16;  // first key of this warp's 16
+                uint32_t pk[8];
                 if (c0 > q32) {
                     // keys after every query row of this warp
 #pragma unroll
-                    for (int e = 0; e < 16; e++) pk[e] = 0u;
+                    for (int e = 0; e < 8; e++) pk[e] = 0u;
                 } else {
-                    float sv[32];
-                    tmem_ld32(tmem + lane_base + b * kTile + c0, sv);
+                    float sv[16];
+                    tmem_ld16(tmem + lane_base + b * kTile + cb, sv);
                     if (c0 < q32) {
                         // keys before every row of this warp: one level per row, factorised decay
                         const int lvl = 32 - __clz(t ^ c0);
                         float lw = lam_in[0];
 #pragma unroll
                         for (int l = 1; l < 8; l++) lw = (lvl == l) ? lam_in[l] : lw;
-                        const float rowf = exp2f(cl2_t - cl2_sh[b][c0 + 31]) * lw;
+                        const float rowf = exp2f(cl2_t - cl2[c0 + 31]) * lw;
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2)
-                            pk[e >> 1] = pack_bf16(sv[e] * rowf * colw_sh[c0 + e], sv[e + 1] * rowf * colw_sh[c0 + e + 1]);
+                        for (int e = 0; e < 16; e += 2)
+                            pk[e >> 1] = pack_bf16(sv[e] * rowf * colw[cb + e], sv[e + 1] * rowf * colw[cb + e + 1]);
                     } else {
-                        // diagonal chunk: causal mask and per-key levels 0..5
+                        // diagonal chunk: causal mask and per-key levels 0..5, branch-free
+                        float v[16];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float v2[2];
+                        for (int e = 0; e < 16; e++) {
+                            const int sidx = cb + e;
+                            const int lvl = 32 - __clz(t ^ sidx);
+                            float lw = lam_in[0];
 #pragma unroll
-                            for (int h = 0; h < 2; h++) {
-                                const int sidx = c0 + e + h;
-                                float val = 0.f;
-                                if (sidx <= t) {
-                                    const int lvl = 32 - __clz(t ^ sidx);
-                                    float lw = lam_in[0];
-#pragma unroll
-                                    for (int l = 1; l < 6; l++) lw = (lvl == l) ? lam_in[l] : lw;
-                                    val = sv[e + h] * exp2f(cl2_t - cl2_sh[b][sidx]) * lw;
-                                }
-                                v2[h] = val;
-                            }
-                            pk[e >> 1] = pack_bf16(v2[0], v2[1]);
+                            for (int l = 1; l < 6; l++) lw = (lvl == l) ? lam_in[l] : lw;
+                            const float x = sv[e] * exp2f(fminf(cl2_t - cl2[sidx], 0.f)) * lw;
+                            v[e] = sidx <= t ? x : 0.f;
                         }
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) pk[e >> 1] = pack_bf16(v[e], v[e + 1]);
                     }
                 }
                 uint8_t* panel = pbase + (c0 >> 6) * kPanelBytes;
-                const int chunk0 = (c0 & 63) >> 3;
-#pragma unroll
-                for (int c = 0; c < 4; c++)
-                    *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0 + c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                const int chunk0 = (cb & 63) >> 3;
+                *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0 + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
             fence_async_smem();
             tc_fence_before();
@@ -889,25 +914,17 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
             tile_of(k, bh, j);
             const int b = k & 1;
             const int row0 = bh * T + j * kTile;
-            // per-row level weights (issued before waiting on the MMAs)
-            const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
-            const float4* drow = reinterpret_cast<const float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
-            float d2[16];
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                const float4 x = drow[c];
-                d2[4 * c] = x.x; d2[4 * c + 1] = x.y; d2[4 * c + 2] = x.z; d2[4 * c + 3] = x.w;
-            }
-            const float cl2_t = cl2_sh[b][t];
+            const float cl2_t = b ? cl2_odd : cl2_even;
+            // level weights of the tile's set bits, in level order
             float rr[16];
+            int nl = 0;
 #pragma unroll
             for (int p = 0; p < 16; p++) {
-                const bool on = p < P && ((j >> p) & 1);
-                rr[p] = on ? lam_row[8 + p] * exp2f(cl2_t + d2[p]) : 0.f;
+                const float w = pre_lam[p] * exp2f(cl2_t + pre_d[p]);
+                if (p < P && ((j >> p) & 1)) rr[nl++] = w;
             }
             float acc[DH];
-            const int n_lv = __popc(static_cast<unsigned>(j) & ((1u << P) - 1u));
-            const int rounds = n_lv == 0 ? 1 : (n_lv + C::kLvSlots - 1) / C::kLvSlots;
+            const int rounds = nl == 0 ? 1 : (nl + C::kLvSlots - 1) / C::kLvSlots;
             for (int r = 0; r < rounds; r++, round++) {
                 if (!ewait(&lv_full, round & 1)) return;
                 tc_fence_after();
@@ -915,20 +932,17 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 #pragma unroll
                     for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tmem + lane_base + C::kColO + half * DH + c0, acc + c0);
                 }
+                const int x_end = min(nl, (r + 1) * C::kLvSlots);
+#pragma unroll 1
+                for (int x = r * C::kLvSlots; x < x_end; x++) {
+                    const float w = rr[x];
+                    const uint32_t col = C::kColLv + (x - r * C::kLvSlots) * DV + half * DH;
 #pragma unroll
-                for (int p = 0; p < 16; p++) {
-                    if (p < P && ((j >> p) & 1)) {
-                        const int x = __popc(static_cast<unsigned>(j) & ((1u << p) - 1u));
-                        if (x / C::kLvSlots == r) {
-                            const uint32_t col = C::kColLv + (x % C::kLvSlots) * DV + half * DH;
+                    for (int c0 = 0; c0 < DH; c0 += 32) {
+                        float lvv[32];
+                        tmem_ld32(tmem + lane_base + col + c0, lvv);
 #pragma unroll
-                            for (int c0 = 0; c0 < DH; c0 += 32) {
-                                float lvv[32];
-                                tmem_ld32(tmem + lane_base + col + c0, lvv);
-#pragma unroll
-                                for (int e = 0; e < 32; e++) acc[c0 + e] = fmaf(rr[p], lvv[e], acc[c0 + e]);
-                            }
-                        }
+                        for (int e = 0; e < 32; e++) acc[c0 + e] = fmaf(w, lvv[e], acc[c0 + e]);
                     }
                 }
                 tc_fence_before();
@@ -944,6 +958,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 
         for (int k = 0; k < C::kAhead && k < n_my; k++) epi1(k);
         for (int k = 0; k < n_my; k++) {
+            prefetch2(k);
             if (k + C::kAhead < n_my) epi1(k + C::kAhead);
             epi2(k);
         }
