@@ -97,6 +97,30 @@ int lla_forward_ws(const void* q, const void* k, const void* v, const float* log
                    void* workspace, size_t workspace_bytes);
 
 /*
+ * lla_forward without any allocation, for callers that cannot call cudaMalloc
+ * (a host that pre-sizes and owns every device allocation, or code that must
+ * not grow the process's GPU footprint after start-up). The paper has no
+ * counterpart: this is a deployment variant of lla_forward with identical
+ * arguments, results and kernels.
+ *
+ * Its scratch is a fixed, file-scope device array of LLA_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) that every GPU loading this library holds until the process exits.
+ * Sizes whose workspace (lla_forward_workspace_size) exceeds it are rejected
+ * with LLA_ERR_NOMEM before anything is enqueued. No cudaMalloc, cudaFree or
+ * allocating library routine is called.
+ *  - The first call on a device looks up that device's copy of the array; make
+ *    that first call before capturing a stream into a CUDA graph.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; no part of it needs to start at zero (each call writes every
+ *    scratch value before reading it). Calls whose work overlaps on the GPU
+ *    (different streams, or graphs replayed concurrently) race on the array:
+ *    serialise them.
+ */
+#define LLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int lla_forward_noalloc(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                        void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype);
+
+/*
  * Measurement aid: runs lla_forward once with a CUDA event recorded on `stream`
  * before the first kernel and after each kernel launch, waits for the last
  * event, and writes, in launch order, each kernel's elapsed device time in

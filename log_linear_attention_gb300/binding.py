@@ -53,6 +53,8 @@ def load() -> ctypes.CDLL:
             lib.lla_forward_workspace_size.restype = sz
             lib.lla_forward_ws.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i, vp, sz]
             lib.lla_forward_ws.restype = i
+            lib.lla_forward_noalloc.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i]
+            lib.lla_forward_noalloc.restype = i
             lib.lla_forward_profile.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i, vp, vp, i]
             lib.lla_forward_profile.restype = i
             lib.lla_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, vp] + [i] * 6
@@ -149,6 +151,23 @@ def forward(q, k, v, log_a, lam, chunk: int, out=None, stream=None, workspace=No
               "lla_forward_ws")
     if host:
         return out.to("cpu")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def forward_noalloc(q, k, v, log_a, lam, chunk: int, out, stream=None):
+    """lla_forward_noalloc: the prefill with its scratch in the library's fixed device
+    array (no allocation at all). ``out`` must be preallocated by the caller. Raises
+    LLAError(LLA_ERR_NOMEM) when the sizes need more than NOALLOC_SCRATCH_BYTES."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda"), (out, "out")):
+        _check(t_, n, q.device)
+    _call(load().lla_forward_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(),
+                                     out.data_ptr(), B, H, T, dk, dv, int(chunk), _stream_handle(stream),
+                                     _dtype_code(q)), "lla_forward_noalloc")
     return out
 
 
