@@ -125,22 +125,23 @@ def load_peaks() -> dict:
 
 
 def traffic_record(name: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel's source
-    has not changed since the counters were taken; else None."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    """DRAM bytes per launch from the committed ncu summary (profiles/ncu_traffic.txt), if the
+    kernel's source still has the hash recorded at capture time; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
     try:
-        rec = json.load(open(path)).get(name)
-        if not rec:
-            return None
-        src = os.path.join(ROOT, rec["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if sha != rec["source_sha256"]:
-            return None
-        return float(rec["dram_bytes_per_launch"])
-    except Exception:
+        for line in open(path):
+            parts = line.split()
+            if not parts or parts[0].startswith("#") or parts[0] != name or len(parts) != 4:
+                continue
+            src = os.path.join(ROOT, parts[1])
+            if hashlib.sha256(open(src, "rb").read()).hexdigest() != parts[2]:
+                return None
+            return float(parts[3])
+    except OSError:
         return None
+    return None
 
 
 # ----------------------------------------------------------------------------- clocks
