@@ -76,7 +76,7 @@ struct TcPlan {
     int num_sms;             // persistent grid size of the output kernel
     int node_count;          // even-indexed nodes actually read, all levels
     int level_off[32];       // node index of (p, m = 0); node (p, m even) at level_off[p] + m / 2
-    size_t g_bytes, nodes_bytes, seg_bytes, dtab_bytes, total_bytes;
+    size_t g_bytes, nodes_bytes, seg_bytes, dtab_bytes, tok_bytes, ctr_bytes, total_bytes;
 };
 
 bool tc_supported(int dtype, int dk, int dv, int T);

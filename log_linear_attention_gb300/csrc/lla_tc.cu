@@ -248,8 +248,8 @@ template <int DV>
 __global__ void __launch_bounds__(128, 1)
     tc_nodes_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
-                    float* __restrict__ seg_tot, int T, int NT, int q, int node_count, LevelOffsets lo,
-                    uint32_t tmem_cols, int* err) {
+                    float* __restrict__ seg_tot, float* __restrict__ tok_cl2, float* __restrict__ tok_colw, int T,
+                    int NT, int q, int node_count, LevelOffsets lo, uint32_t tmem_cols, int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t bar_full[2];
@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ float warp_tot[4];
     __shared__ float g_sh;
+    __shared__ float cl2_sh[kTile];
     __shared__ int fail_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -308,12 +309,17 @@ __global__ void __launch_bounds__(128, 1)
         const int s = u & 1;
         const int tile = tile0 + u;
         // tile-local decays
-        const float a = log_a[static_cast<size_t>(bh) * T + static_cast<size_t>(tile) * kTile + tid];
+        const size_t tok = static_cast<size_t>(bh) * T + static_cast<size_t>(tile) * kTile + tid;
+        const float a = log_a[tok];
         const float cl = block_scan128(a, warp_tot);
         if (tid == kTile - 1) g_sh = cl;
+        cl2_sh[tid] = cl * kLog2e;
         __syncthreads();
         const float g = g_sh;
         if (tid == 0) g_tiles[static_cast<size_t>(bh) * NT + tile] = g;
+        // per-token decay prefix (log2 units) and column weights for the output kernel
+        tok_cl2[tok] = cl2_sh[tid];
+        tok_colw[tok] = exp2f(cl2_sh[tid | 31] - cl2_sh[tid]);
         const float w = exp2f((g - cl) * kLog2e);
 
         if (!mbar_wait(&bar_full[s], (u >> 1) & 1)) {
@@ -440,12 +446,14 @@ __global__ void __launch_bounds__(128, 1)
 //  * block x = dk*DV/256: the per-tile decay table dtab[bh][j][p] (log2 units):
 //    sum of g over tiles [(j >> p) << p, j), the log-decay from the end of the
 //    block node (p, (j >> p) - 1) to the start of tile j, for each set bit p of j.
+// Block (0, 0) also resets the tile counter tc_output's CTAs take tiles from.
 __global__ void __launch_bounds__(256)
     tc_merge_kernel(float* __restrict__ seg_tot, const float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
-                    float* __restrict__ dtab, int NT, int q, int P, int nseg, int node_count, int msz,
-                    LevelOffsets lo) {
+                    float* __restrict__ dtab, int* __restrict__ tile_counter, int NT, int q, int P, int nseg,
+                    int node_count, int msz, LevelOffsets lo) {
     extern __shared__ float Gs[];  // nseg segment log-decay totals (updated in place per level)
     const int bh = blockIdx.y;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *tile_counter = 0;  // tile scheduler of tc_output
     const float* gh = g_tiles + static_cast<size_t>(bh) * NT;
     if (static_cast<int>(blockIdx.x) == msz / 256) {
         for (int j = threadIdx.x; j < NT; j += blockDim.x) {
@@ -508,10 +516,11 @@ __global__ void __launch_bounds__(256)
 // Persistent, warp-specialised output kernel. Each CTA walks tiles
 // idx = blockIdx.x + k * gridDim.x (head-major order, so the CTAs running at
 // one time share a few heads' nodes in L2). Roles (11 warps):
-//   warp 0        input producer: TMA of Q, K, V into input stage k % kStages;
-//                 its 32 lanes also stage the tile's in-tile decay prefix
-//                 cl_t (log2 units), the column weights exp(cl_{s|31} - cl_s)
-//                 and lambda levels 0..7 of every row beside them.
+//   warp 0        input producer: TMA of Q, K, V and bulk copies of the
+//                 tile's in-tile decay prefix cl_t (log2 units) and column
+//                 weights exp(cl_{s|31} - cl_s) (both written by tc_nodes)
+//                 into input stage k % kStages; its 32 lanes add lambda
+//                 levels 0..7 of every row with 4-byte cp.async copies.
 //   warp 1        MMA issuer (one lane): S_k = Q K^T into TMEM buffer k % 2;
 //                 then O = P V and L_p = Q B_p into the O and level slots of
 //                 TMEM, kLvSlots levels per round.
@@ -535,6 +544,7 @@ struct OutCfg {
     static constexpr int kK = 2 * kPanelBytes;  // K tile, then P of the same tile
     static constexpr int kV = 4 * kPanelBytes;
     static constexpr int kCl2 = kV + (DV / 64) * kPanelBytes;  // 128 floats: in-tile log2 decay prefix
+    static constexpr int kScalarTx = 2 * 512;                    // cl2 + colw bulk copies
     static constexpr int kColw = kCl2 + 512;                     // 128 floats: column weights
     static constexpr int kLam8 = kColw + 512;                    // 128 x 8 floats: lambda levels 0..7
     static constexpr int kStageBytes = (kLam8 + kTile * 8 * 4 + 1023) / 1024 * 1024;
@@ -566,13 +576,32 @@ __device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// Contiguous global -> shared copy through the async proxy (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy (no alignment beyond 4 bytes needed).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 template <int DV>
 __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     tc_output_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_nodes,
-                     const float* __restrict__ log_a, const float* __restrict__ lambda,
-                     const float* __restrict__ dtab, __nv_bfloat16* __restrict__ out, int T, int NT, int L, int P,
-                     int node_count, LevelOffsets lo, int total_tiles, int* err) {
+                     const float* __restrict__ tok_cl2, const float* __restrict__ tok_colw,
+                     const float* __restrict__ lambda, const float* __restrict__ dtab,
+                     __nv_bfloat16* __restrict__ out, int T, int NT, int L, int P, int node_count, LevelOffsets lo,
+                     int total_tiles, int* __restrict__ tile_counter, int* err) {
     using C = OutCfg<DV>;
     constexpr int NS = C::kStages;
     constexpr int DH = DV / 2;  // columns of O per epilogue warp
@@ -580,18 +609,18 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t in_full[NS], in_empty[NS], s_full[2], s_free[2], p_ready[2];
     __shared__ uint64_t node_full[C::kNodeSlots], node_empty[C::kNodeSlots];
-    __shared__ uint64_t lv_full, lv_free, drain;
+    __shared__ uint64_t lv_full, lv_free, drain, id_ready[NS];
     __shared__ uint32_t tmem_base_sh;
+    __shared__ int tile_id_sh[NS];  // tile of the job in each input stage, -1 = no more tiles
     __shared__ volatile int fail_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = gridDim.x;
-    const int n_my = (total_tiles - static_cast<int>(blockIdx.x) + G - 1) / G;
 
     if (tid == 0) {
         for (int s = 0; s < NS; s++) {
-            mbar_init(&in_full[s], 2);  // TMA bytes + the staged per-row scalars
+            mbar_init(&in_full[s], 2);  // TMA/bulk bytes + lane 0's arrive; the lambda cp.asyncs add their own
             mbar_init(&in_empty[s], 1);
+            mbar_init(&id_ready[s], 1);
         }
         for (int s = 0; s < 2; s++) {
             mbar_init(&s_full[s], 1);
@@ -614,10 +643,12 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    auto tile_of = [&](int k, int& bh, int& j) {
-        const int idx = static_cast<int>(blockIdx.x) + k * G;
+    // Tiles are handed out by a global counter (zeroed by tc_merge), head by head and,
+    // within a head, from the last tile down: the tiles with the most Fenwick levels
+    // start first and the cheap ones fill the tail.
+    auto tile_of = [&](int idx, int& bh, int& j) {
         bh = idx / NT;
-        j = idx - bh * NT;
+        j = NT - 1 - (idx - bh * NT);
     };
     // single-thread bounded wait; after a failure anywhere it returns false at once
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -641,15 +672,30 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------------- input producer
         int n_in = 0;
-        for (int k = 0; k < n_my; k++) {
-            int bh, j;
-            tile_of(k, bh, j);
-            const int row0 = bh * T + j * kTile;
+        for (int k = 0;; k++) {
             const int s = k % NS;
             if (k >= NS && !ewait(&in_empty[s], ((k / NS) - 1) & 1)) break;
+            int idx = 0;
+            if (lane == 0) idx = atomicAdd(tile_counter, 1);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            const bool done = idx >= total_tiles;
+            if (lane == 0) {
+                tile_id_sh[s] = done ? -1 : idx;
+                mbar_arrive(&id_ready[s]);
+            }
+            if (done) {
+                if (lane == 0) {
+                    mbar_arrive(&in_full[s]);
+                    mbar_arrive(&in_full[s]);
+                }
+                break;
+            }
+            int bh, j;
+            tile_of(idx, bh, j);
+            const int row0 = bh * T + j * kTile;
             uint8_t* st = smem + s * C::kStageBytes;
             if (lane == 0) {
-                mbar_expect_tx(&in_full[s], C::kQkvBytes);
+                mbar_expect_tx(&in_full[s], C::kQkvBytes + C::kScalarTx);
                 tma_load_2d(st + C::kQ, &tm_q, &in_full[s], 0, row0);
                 tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[s], 64, row0);
                 tma_load_2d(st + C::kK, &tm_k, &in_full[s], 0, row0);
@@ -657,28 +703,8 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < DV / 64; c++)
                     tma_load_2d(st + C::kV + c * kPanelBytes, &tm_v, &in_full[s], 64 * c, row0);
-            }
-            // in-tile inclusive decay prefix: lane owns rows 4 lane .. 4 lane + 3
-            const float4 a4 = *reinterpret_cast<const float4*>(log_a + row0 + lane * 4);
-            float c4[4] = {a4.x, a4.x + a4.y, a4.x + a4.y + a4.z, a4.x + a4.y + a4.z + a4.w};
-            float incl = c4[3];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += y;
-            }
-            const float excl = incl - c4[3];
-            float* cl2 = reinterpret_cast<float*>(st + C::kCl2);
-            float* colw = reinterpret_cast<float*>(st + C::kColw);
-            float c2[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) c2[e] = (c4[e] + excl) * kLog2e;
-            // decay prefix at the last row of this lane's 32-row chunk (row t | 31 is lane | 7, element 3)
-            const float chunk_end = __shfl_sync(0xffffffffu, c2[3], lane | 7);
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                cl2[lane * 4 + e] = c2[e];
-                colw[lane * 4 + e] = exp2f(chunk_end - c2[e]);
+                bulk_load(st + C::kCl2, tok_cl2 + row0, 512, &in_full[s]);
+                bulk_load(st + C::kColw, tok_colw + row0, 512, &in_full[s]);
             }
             // lambda_t^(0..7) of the tile's 128 rows (rows are L floats apart, not 16-byte aligned)
             float* lam8 = reinterpret_cast<float*>(st + C::kLam8);
@@ -687,8 +713,9 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 const int t = lane * 4 + rr;
                 const float* src = lambda + static_cast<size_t>(row0 + t) * L;
 #pragma unroll
-                for (int l = 0; l < 8; l++) lam8[t * 8 + l] = src[l];
+                for (int l = 0; l < 8; l++) cp_async4(lam8 + t * 8 + l, src + l);
             }
+            cp_async_arrive(&in_full[s]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&in_full[s]);
             n_in = k + 1;
@@ -703,9 +730,12 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
         if (lane == 0) {
             int gn = 0;
             bool ok = true;
-            for (int k = 0; k < n_my && ok; k++) {
+            for (int k = 0; ok; k++) {
+                if (!wait(&id_ready[k % NS], (k / NS) & 1)) break;
+                const int idx = tile_id_sh[k % NS];
+                if (idx < 0) break;
                 int bh, j;
-                tile_of(k, bh, j);
+                tile_of(idx, bh, j);
                 for (int p = 0; p < P; p++) {
                     if (((j >> p) & 1) == 0) continue;
                     const int slot = gn % C::kNodeSlots;
@@ -734,10 +764,13 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
             int gn = 0, round = 0;
             constexpr uint32_t kIdS = idesc_bf16(kTile, kTile, 0, 0);
             constexpr uint32_t kIdO = idesc_bf16(kTile, DV, 0, 1);
-            auto phase1 = [&](int k) -> bool {
+            // phase 1 of the k-th job: returns its tile, -1 when the tiles are exhausted, -2 on failure
+            auto phase1 = [&](int k) -> int {
                 const int s = k % NS, b = k & 1;
-                if (!wait(&in_full[s], (k / NS) & 1)) return false;
-                if (k >= 2 && !wait(&s_free[b], ((k >> 1) - 1) & 1)) return false;
+                if (!wait(&in_full[s], (k / NS) & 1)) return -2;
+                const int idx = tile_id_sh[s];
+                if (idx < 0) return -1;
+                if (k >= 2 && !wait(&s_free[b], ((k >> 1) - 1) & 1)) return -2;
                 tc_fence_after();
                 const uint32_t qb = smem_u32(smem + s * C::kStageBytes + C::kQ);
                 const uint32_t kb = smem_u32(smem + s * C::kStageBytes + C::kK);
@@ -748,21 +781,29 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                              kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&s_full[b]);
-                return true;
+                return idx;
             };
-            auto phase2 = [&](int k) -> bool {
+            // Phase 2 of tile k (O = P V and the level reads, kLvSlots per round) is issued
+            // after phase 1 of tile k+1, so S of the next tile is computed while this
+            // tile waits for its P; the inputs are staged well ahead by the producer.
+            int p2_p = 0, p2_rounds = 0;
+            auto phase2 = [&](int k, int idx, bool first_round) -> bool {
                 int bh, j;
-                tile_of(k, bh, j);
+                tile_of(idx, bh, j);
                 const int s = k % NS, b = k & 1;
-                if (!wait(&p_ready[b], (k >> 1) & 1)) return false;
-                tc_fence_after();
+                if (first_round) {
+                    if (!wait(&p_ready[b], (k >> 1) & 1)) return false;
+                    tc_fence_after();
+                    const int n_lv = __popc(static_cast<unsigned>(j) & ((1u << P) - 1u));
+                    p2_rounds = n_lv == 0 ? 1 : (n_lv + C::kLvSlots - 1) / C::kLvSlots;
+                    p2_p = 0;
+                }
                 const uint32_t qb = smem_u32(smem + s * C::kStageBytes + C::kQ);
                 const uint32_t pb = smem_u32(smem + s * C::kStageBytes + C::kK);
                 const uint32_t vb = smem_u32(smem + s * C::kStageBytes + C::kV);
-                const int n_lv = __popc(static_cast<unsigned>(j) & ((1u << P) - 1u));
-                const int rounds = n_lv == 0 ? 1 : (n_lv + C::kLvSlots - 1) / C::kLvSlots;
-                int p = 0;
-                for (int r = 0; r < rounds; r++, round++) {
+                const int r_begin = first_round ? 0 : 1;
+                const int r_end = first_round ? 1 : p2_rounds;
+                for (int r = r_begin; r < r_end; r++, round++) {
                     if (round > 0 && !wait(&lv_free, (round - 1) & 1)) return false;
                     tc_fence_after();
                     if (r == 0) {
@@ -774,9 +815,9 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                         }
                     }
                     for (int sl = 0; sl < C::kLvSlots; sl++) {
-                        while (p < P && ((j >> p) & 1) == 0) p++;
-                        if (p >= P) break;
-                        p++;
+                        while (p2_p < P && ((j >> p2_p) & 1) == 0) p2_p++;
+                        if (p2_p >= P) break;
+                        p2_p++;
                         const int slot = gn % C::kNodeSlots;
                         if (!wait(&node_full[slot], (gn / C::kNodeSlots) & 1)) return false;
                         tc_fence_after();
@@ -793,14 +834,34 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                     }
                     mma_commit(&lv_full);
                 }
-                mma_commit(&in_empty[s]);
+                if (r_end == p2_rounds) mma_commit(&in_empty[s]);  // every MMA of the tile is issued
                 return true;
             };
+            int ids[2] = {-1, -1};
+            int count = 1 << 30;  // jobs of this CTA, known once phase 1 meets the end marker
             bool ok = true;
-            for (int k = 0; k < C::kAhead && k < n_my && ok; k++) ok = phase1(k);
-            for (int k = 0; k < n_my && ok; k++) {
-                if (k + C::kAhead < n_my && !phase1(k + C::kAhead)) break;
-                if (!phase2(k)) break;
+            for (int k = 0; k < C::kAhead && ok; k++) {
+                const int id = phase1(k);
+                if (id == -2) ok = false;
+                else if (id < 0) { count = k; break; }
+                else ids[k & 1] = id;
+            }
+            for (int k = 0; ok; k++) {
+                if (C::kAhead == 0) {
+                    const int id = phase1(k);
+                    if (id < 0) break;
+                    ids[k & 1] = id;
+                } else if (k >= count) {
+                    break;
+                }
+                if (C::kAhead > 0 && k + C::kAhead < count) {
+                    const int id = phase1(k + C::kAhead);
+                    if (id == -2) break;
+                    if (id < 0) count = k + C::kAhead;
+                    else ids[(k + C::kAhead) & 1] = id;
+                }
+                if (!phase2(k, ids[k & 1], true)) break;
+                if (p2_rounds > 1 && !phase2(k, ids[k & 1], false)) break;
             }
             // every MMA issued by this CTA has completed before TMEM is released
             mma_commit(&drain);
@@ -821,9 +882,9 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
         // decay-table row of the tile, plus the row's decay prefix.
         float pre_lam[16], pre_d[16];
         float cl2_even = 0.f, cl2_odd = 0.f;
-        auto prefetch2 = [&](int k) {
+        auto prefetch2 = [&](int idx) {
             int bh, j;
-            tile_of(k, bh, j);
+            tile_of(idx, bh, j);
             const int row0 = bh * T + j * kTile;
             const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
             const float4* drow = reinterpret_cast<const float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
@@ -838,10 +899,13 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 
         // Phase 1: P_k. The two warps of a lane quadrant split every 32-key chunk,
         // 16 keys each, so the masked diagonal chunk is shared evenly.
-        auto epi1 = [&](int k) {
+        // returns the job's tile, -1 at the end marker or on failure
+        auto epi1 = [&](int k) -> int {
             const int s = k % NS, b = k & 1;
             const uint8_t* st = smem + s * C::kStageBytes;
-            if (!ewait(&in_full[s], (k / NS) & 1)) return;
+            if (!ewait(&in_full[s], (k / NS) & 1)) return -1;
+            const int idx = tile_id_sh[s];
+            if (idx < 0) return -1;
             const float* cl2 = reinterpret_cast<const float*>(st + C::kCl2);
             const float* colw = reinterpret_cast<const float*>(st + C::kColw);
             const float cl2_t = cl2[t];
@@ -853,7 +917,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 lam_in[0] = x0.x; lam_in[1] = x0.y; lam_in[2] = x0.z; lam_in[3] = x0.w;
                 lam_in[4] = x1.x; lam_in[5] = x1.y; lam_in[6] = x1.z; lam_in[7] = x1.w;
             }
-            if (!ewait(&s_full[b], (k >> 1) & 1)) return;
+            if (!ewait(&s_full[b], (k >> 1) & 1)) return -1;
             tc_fence_after();
             uint8_t* pbase = smem + s * C::kStageBytes + C::kK;
 #pragma unroll 1
@@ -906,12 +970,13 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 mbar_arrive(&p_ready[b]);
                 mbar_arrive(&s_free[b]);
             }
+            return idx;
         };
 
         // Phase 2: O + sum_p r_p L_p for this warp's half of the columns.
-        auto epi2 = [&](int k) {
+        auto epi2 = [&](int k, int idx) {
             int bh, j;
-            tile_of(k, bh, j);
+            tile_of(idx, bh, j);
             const int b = k & 1;
             const int row0 = bh * T + j * kTile;
             const float cl2_t = b ? cl2_odd : cl2_even;
@@ -956,11 +1021,28 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                                     pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
         };
 
-        for (int k = 0; k < C::kAhead && k < n_my; k++) epi1(k);
-        for (int k = 0; k < n_my; k++) {
-            prefetch2(k);
-            if (k + C::kAhead < n_my) epi1(k + C::kAhead);
-            epi2(k);
+        int ids[2] = {-1, -1};
+        int count = 1 << 30;
+        for (int k = 0; k < C::kAhead; k++) {
+            const int id = epi1(k);
+            if (id < 0) { count = k; break; }
+            ids[k & 1] = id;
+        }
+        for (int k = 0;; k++) {
+            if (C::kAhead == 0) {
+                const int id = epi1(k);
+                if (id < 0) break;
+                ids[k & 1] = id;
+            } else if (k >= count) {
+                break;
+            }
+            prefetch2(ids[k & 1]);
+            if (C::kAhead > 0 && k + C::kAhead < count) {
+                const int id = epi1(k + C::kAhead);
+                if (id < 0) count = k + C::kAhead;
+                else ids[(k + C::kAhead) & 1] = id;
+            }
+            epi2(k, ids[k & 1]);
         }
     }
 
@@ -1026,6 +1108,9 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
     __nv_bfloat16* nodes = reinterpret_cast<__nv_bfloat16*>(ws + pl.g_bytes);
     float* seg_tot = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes);
     float* dtab = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes + pl.seg_bytes);
+    float* tok_cl2 = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes + pl.seg_bytes + pl.dtab_bytes);
+    float* tok_colw = tok_cl2 + static_cast<size_t>(BH) * pl.T;
+    int* tile_counter = reinterpret_cast<int*>(ws + pl.total_bytes - pl.ctr_bytes);
     LevelOffsets lo;
     for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
     const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
@@ -1044,14 +1129,15 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
         cudaError_t e = cudaFuncSetAttribute(tc_nodes_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const uint32_t cols = pow2_cols((1 + qlog) * DV);
-        tc_nodes_kernel<DV><<<dim3(nseg, BH), 128, smem, stream>>>(tk, tv, log_a, g_tiles, nodes, seg_tot, pl.T, pl.NT,
-                                                                   qlog, pl.node_count, lo, cols, err);
+        tc_nodes_kernel<DV><<<dim3(nseg, BH), 128, smem, stream>>>(tk, tv, log_a, g_tiles, nodes, seg_tot, tok_cl2,
+                                                                   tok_colw, pl.T, pl.NT, qlog, pl.node_count, lo,
+                                                                   cols, err);
         note_launch(stream, "tc_nodes");
     }
     {
         const int msz = kDk * DV;
         tc_merge_kernel<<<dim3(msz / 256 + 1, BH), 256, nseg * sizeof(float), stream>>>(
-            seg_tot, g_tiles, nodes, dtab, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
+            seg_tot, g_tiles, nodes, dtab, tile_counter, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
         note_launch(stream, "tc_merge");
     }
     {
@@ -1061,10 +1147,10 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
         const int L = bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
         const int total = BH * pl.NT;
         const int grid = total < pl.num_sms ? total : pl.num_sms;
-        tc_output_kernel<DV><<<grid, OutCfg<DV>::kThreads, smem, stream>>>(tq, tk, tv, tn, log_a, lambda, dtab,
+        tc_output_kernel<DV><<<grid, OutCfg<DV>::kThreads, smem, stream>>>(tq, tk, tv, tn, tok_cl2, tok_colw, lambda, dtab,
                                                                             static_cast<__nv_bfloat16*>(out), pl.T,
                                                                             pl.NT, L, pl.P, pl.node_count, lo, total,
-                                                                            err);
+                                                                            tile_counter, err);
         note_launch(stream, "tc_output");
     }
     return cudaGetLastError();
@@ -1106,7 +1192,9 @@ bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* pl) {
     pl->nodes_bytes = (static_cast<size_t>(BH) * pl->node_count * msz * 2 + 1023) / 1024 * 1024;
     pl->seg_bytes = (static_cast<size_t>(BH) * nseg * msz * sizeof(float) + 1023) / 1024 * 1024;
     pl->dtab_bytes = static_cast<size_t>(BH) * pl->NT * 16 * sizeof(float);
-    pl->total_bytes = pl->g_bytes + pl->nodes_bytes + pl->seg_bytes + pl->dtab_bytes;
+    pl->tok_bytes = (2 * static_cast<size_t>(BH) * T * sizeof(float) + 255) / 256 * 256;
+    pl->ctr_bytes = 256;
+    pl->total_bytes = pl->g_bytes + pl->nodes_bytes + pl->seg_bytes + pl->dtab_bytes + pl->tok_bytes + pl->ctr_bytes;
     return true;
 }
 
