@@ -243,105 +243,141 @@ struct NodesSmem {
     static constexpr int kBytes = kStages * kStageBytes + 1024;  // + alignment slack
 };
 
-// grid (num_segments, B*H), 128 threads. Segment s covers tiles [s 2^q, (s+1) 2^q).
-template <int DV>
-__global__ void __launch_bounds__(128, 1)
+// grid (num_segments, B*H), 256 threads: two threads per dk row (= TMEM lane), each
+// owning half of the dv columns. Segment s covers tiles [s 2^Q, (s+1) 2^Q).
+// Per tile u: S_u = K_u^T diag(w) V_u on tcgen05 into TMEM buffer u % 2 (the MMA of
+// tile u+1 runs while tile u's epilogue reads its buffer); then, in registers,
+// A_l <- e^{g_u} A_l + S_u for the levels l = 1..Q whose blocks contain u. A block
+// that closes at u is written out as a node (bf16) when it is read by a later tile,
+// and the level-Q block (the whole segment) as the segment's fp32 total.
+template <int DV, int Q>
+__global__ void __launch_bounds__(256, 2)
     tc_nodes_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
                     float* __restrict__ seg_tot, float* __restrict__ tok_cl2, float* __restrict__ tok_colw, int T,
-                    int NT, int q, int node_count, LevelOffsets lo, uint32_t tmem_cols, int* err) {
+                    int NT, int node_count, LevelOffsets lo, int* err) {
+    constexpr int DH = DV / 2;  // columns per thread
+    constexpr int kSegTiles = 1 << Q;
+    using S = NodesSmem<DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[2];
-    __shared__ uint64_t bar_mma;
+    __shared__ uint64_t bar_full[2], bar_mma[2];
     __shared__ uint32_t tmem_base_sh;
-    __shared__ float warp_tot[4];
-    __shared__ float g_sh;
-    __shared__ float cl2_sh[kTile];
+    __shared__ float warp_tot[8];
+    __shared__ float cl2_sh[kSegTiles][kTile];  // in-tile decay prefix, log2 units
+    __shared__ float g2_sh[kSegTiles];          // tile totals, log2 units
     __shared__ int fail_sh;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, bh = blockIdx.y;
-    const int seg_tiles = 1 << q;
-    const int tile0 = seg * seg_tiles;
-    const int ntiles = min(seg_tiles, NT - tile0);
-    constexpr uint32_t kTxBytes = NodesSmem<DV>::kStageBytes;
+    const int tile0 = seg * kSegTiles;
+    const int ntiles = min(kSegTiles, NT - tile0);
+    const int row = tid & 127;         // dk row in the epilogue, token row while scaling V
+    const int half = tid >> 7;         // which half of the dv columns / of the V row
+    const int quad = warp & 3;         // TMEM lane quadrant of this warp
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    constexpr uint32_t kTxBytes = S::kStageBytes;
+    constexpr uint32_t kCols = 2 * DV <= 32 ? 32 : 2 * DV;
 
     if (tid == 0) {
-        mbar_init(&bar_full[0], 1);
-        mbar_init(&bar_full[1], 1);
-        mbar_init(&bar_mma, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&bar_full[b], 1);
+            mbar_init(&bar_mma[b], 1);
+        }
         fence_mbar_init();
         fail_sh = 0;
     }
-    if (warp == 0) tmem_alloc(&tmem_base_sh, tmem_cols);
+    if (warp == 0) tmem_alloc(&tmem_base_sh, kCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 
-    auto stage_ptr = [&](int s) { return smem + s * NodesSmem<DV>::kStageBytes; };
+    auto stage_ptr = [&](int s) { return smem + s * S::kStageBytes; };
     auto issue_tile = [&](int u) {
         const int s = u & 1;
         uint8_t* st = stage_ptr(s);
-        const int row = bh * T + (tile0 + u) * kTile;
+        const int r0 = bh * T + (tile0 + u) * kTile;
         mbar_expect_tx(&bar_full[s], kTxBytes);
-        tma_load_2d(st, &tm_k, &bar_full[s], 0, row);
-        tma_load_2d(st + kPanelBytes, &tm_k, &bar_full[s], 64, row);
+        tma_load_2d(st, &tm_k, &bar_full[s], 0, r0);
+        tma_load_2d(st + kPanelBytes, &tm_k, &bar_full[s], 64, r0);
 #pragma unroll
         for (int p = 0; p < DV / 64; p++)
-            tma_load_2d(st + NodesSmem<DV>::kKBytes + p * kPanelBytes, &tm_v, &bar_full[s], 64 * p, row);
+            tma_load_2d(st + S::kKBytes + p * kPanelBytes, &tm_v, &bar_full[s], 64 * p, r0);
     };
     if (tid == 0) {
         issue_tile(0);
         if (ntiles > 1) issue_tile(1);
     }
 
+    // decays of the whole segment: per tile an inclusive prefix over its 128 tokens
+    // (threads 0..127, one token each), stored for the output kernel as well; every
+    // tile's log_a is loaded before the first scan
+    float la[kSegTiles];
+#pragma unroll
+    for (int u = 0; u < kSegTiles; u++) {
+        const size_t tok = static_cast<size_t>(bh) * T + static_cast<size_t>(tile0 + u) * kTile + row;
+        la[u] = (half == 0 && u < ntiles) ? log_a[tok] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kSegTiles; u++) {
+        if (u >= ntiles) break;
+        const size_t tok = static_cast<size_t>(bh) * T + static_cast<size_t>(tile0 + u) * kTile + row;
+        float x = la[u];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (half == 0) {
+            float base = 0.f;
+            for (int w = 0; w < quad; w++) base += warp_tot[w];
+            cl2_sh[u][row] = (x + base) * kLog2e;
+            if (row == kTile - 1) {
+                g2_sh[u] = (x + base) * kLog2e;
+                g_tiles[static_cast<size_t>(bh) * NT + tile0 + u] = x + base;
+            }
+        }
+        __syncthreads();
+        if (half == 0) {
+            tok_cl2[tok] = cl2_sh[u][row];
+            tok_colw[tok] = exp2f(cl2_sh[u][row | 31] - cl2_sh[u][row]);
+        }
+    }
+
     constexpr uint32_t kIdesc = idesc_bf16(kDk, DV, 1, 1);  // A = K^T (MN-major), B = V (MN-major)
     const size_t msz = static_cast<size_t>(kDk) * DV;
-    const int i_row = tid;  // TMEM lane = dk row
-    int issued = ntiles > 1 ? 2 : 1;
-    int mma_phase = 0;
     bool ok = true;
 
-    for (int u = 0; u < ntiles; u++) {
+    // scale V rows of tile u by their decay to the tile end, then issue its MMA
+    auto scale_and_mma = [&](int u) {
         const int s = u & 1;
-        const int tile = tile0 + u;
-        // tile-local decays
-        const size_t tok = static_cast<size_t>(bh) * T + static_cast<size_t>(tile) * kTile + tid;
-        const float a = log_a[tok];
-        const float cl = block_scan128(a, warp_tot);
-        if (tid == kTile - 1) g_sh = cl;
-        cl2_sh[tid] = cl * kLog2e;
-        __syncthreads();
-        const float g = g_sh;
-        if (tid == 0) g_tiles[static_cast<size_t>(bh) * NT + tile] = g;
-        // per-token decay prefix (log2 units) and column weights for the output kernel
-        tok_cl2[tok] = cl2_sh[tid];
-        tok_colw[tok] = exp2f(cl2_sh[tid | 31] - cl2_sh[tid]);
-        const float w = exp2f((g - cl) * kLog2e);
-
         if (!mbar_wait(&bar_full[s], (u >> 1) & 1)) {
             ok = false;
             atomicExch(&fail_sh, 1);
         }
         __syncthreads();
-        if (fail_sh) break;
-        // scale V row `tid` (one token) by its decay to the tile end
-        uint8_t* vbase = stage_ptr(s) + NodesSmem<DV>::kKBytes;
+        if (fail_sh) return;
+        const float w = exp2f(g2_sh[u] - cl2_sh[u][row]);
+        uint8_t* vbase = stage_ptr(s) + S::kKBytes;
+        // this thread scales four of the eight 16-byte chunks of its token's 128-byte panel
+        // row; the chunks sit in swizzled order (chunk c at c ^ (row & 7)), which also
+        // spreads the lanes of a warp over all banks
 #pragma unroll
         for (int p = 0; p < DV / 64; p++) {
-            uint4* rowp = reinterpret_cast<uint4*>(vbase + p * kPanelBytes + tid * 128);
+            uint8_t* rowp = vbase + p * kPanelBytes + row * 128;
 #pragma unroll
-            for (int c = 0; c < 8; c++) {
-                uint4 x = rowp[c];
+            for (int c = 0; c < 4; c++) {
+                uint4* cp = reinterpret_cast<uint4*>(rowp + (((half * 4 + c) ^ (row & 7)) << 4));
+                uint4 x = *cp;
                 float2 f0 = unpack_bf16(x.x), f1 = unpack_bf16(x.y), f2 = unpack_bf16(x.z), f3 = unpack_bf16(x.w);
                 x.x = pack_bf16(f0.x * w, f0.y * w);
                 x.y = pack_bf16(f1.x * w, f1.y * w);
                 x.z = pack_bf16(f2.x * w, f2.y * w);
                 x.w = pack_bf16(f3.x * w, f3.y * w);
-                rowp[c] = x;
+                *cp = x;
             }
         }
         fence_async_smem();
@@ -350,74 +386,67 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_after();
         if (tid == 0) {
             const uint32_t kb = smem_u32(stage_ptr(s));
-            const uint32_t vb = kb + NodesSmem<DV>::kKBytes;
+            const uint32_t vb = kb + S::kKBytes;
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; kk++) {
                 const uint64_t ad = sdesc(kb + kk * 2048, kPanelBytes, 1024);
                 const uint64_t bd = sdesc(vb + kk * 2048, kPanelBytes, 1024);
-                mma_bf16(tmem, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+                mma_bf16(tmem + s * DV, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&bar_mma);
+            mma_commit(&bar_mma[s]);
         }
-        if (!mbar_wait(&bar_mma, mma_phase)) {
+    };
+
+    float acc[Q > 0 ? Q : 1][DH];
+    scale_and_mma(0);
+    int u = 0;
+    for (; u < ntiles && !fail_sh; u++) {
+        const int s = u & 1;
+        const int tile = tile0 + u;
+        if (u + 1 < ntiles) scale_and_mma(u + 1);
+        if (fail_sh) break;
+        if (!mbar_wait(&bar_mma[s], (u >> 1) & 1)) {
             ok = false;
             atomicExch(&fail_sh, 1);
         }
-        mma_phase ^= 1;
         tc_fence_after();
-        __syncthreads();
-        if (fail_sh) break;
         // stage s is free again: prefetch tile u + 2 into it
-        if (tid == 0 && issued < ntiles) {
-            issue_tile(issued);
-            issued++;
-        }
+        if (tid == 0 && u + 2 < ntiles && ok) issue_tile(u + 2);
 
-        // epilogue: level accumulators l = 0..q (level 0 is S_u itself)
-        const float ge = exp2f(g * kLog2e);
-#pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
-            float sv[32], av[32];
-            tmem_ld32(tmem + lane_base + c0, sv);
-#pragma unroll 1
-            for (int l = 0; l <= q; l++) {
-                const int span = 1 << l;
-                const bool first = (tile & (span - 1)) == 0;
-                const bool closes = ((tile + 1) & (span - 1)) == 0;
-                if (l == 0) {
+        float sv[DH];
 #pragma unroll
-                    for (int e = 0; e < 32; e++) av[e] = sv[e];
-                } else {
-                    if (first) {
+        for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tmem + lane_base + s * DV + half * DH + c0, sv + c0);
+        const float ge = exp2f(g2_sh[u]);
+        auto store_node = [&](int l, int m, const float* v) {
+            __nv_bfloat16* dst = nodes + (static_cast<size_t>(bh) * node_count + lo.off[l] + (m >> 1)) * msz +
+                                 static_cast<size_t>(row) * DV + half * DH;
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                        for (int e = 0; e < 32; e++) av[e] = sv[e];
-                    } else {
-                        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(l * DV + c0), av);
+            for (int c = 0; c < DH / 8; c++)
+                d4[c] = make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                                   pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+        };
+        auto store_seg = [&](const float* v) {
+            float* dst = seg_tot + (static_cast<size_t>(bh) * ((NT + kSegTiles - 1) / kSegTiles) + seg) * msz +
+                         static_cast<size_t>(row) * DV + half * DH;
+            float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-                        for (int e = 0; e < 32; e++) av[e] = fmaf(av[e], ge, sv[e]);
-                    }
-                    if (!closes) tmem_st32(tmem + lane_base + static_cast<uint32_t>(l * DV + c0), av);
-                }
-                if (closes) {
-                    const int m = tile >> l;
-                    if ((m & 1) == 0 && ((m + 1) << l) < NT) {
-                        __nv_bfloat16* dst = nodes + (static_cast<size_t>(bh) * node_count + lo.off[l] + (m >> 1)) * msz +
-                                             static_cast<size_t>(i_row) * DV + c0;
-                        uint4* d4 = reinterpret_cast<uint4*>(dst);
+            for (int c = 0; c < DH / 4; c++) d4[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        };
+        // level 0: the tile itself
+        if ((tile & 1) == 0 && tile + 1 < NT) store_node(0, tile, sv);
+        if (Q == 0 && ntiles == kSegTiles) store_seg(sv);
 #pragma unroll
-                        for (int c = 0; c < 4; c++)
-                            d4[c] = make_uint4(pack_bf16(av[8 * c], av[8 * c + 1]), pack_bf16(av[8 * c + 2], av[8 * c + 3]),
-                                               pack_bf16(av[8 * c + 4], av[8 * c + 5]),
-                                               pack_bf16(av[8 * c + 6], av[8 * c + 7]));
-                    }
-                    if (l == q && ntiles == seg_tiles) {
-                        float* dst = seg_tot + (static_cast<size_t>(bh) * ((NT + seg_tiles - 1) / seg_tiles) + seg) * msz +
-                                     static_cast<size_t>(i_row) * DV + c0;
-                        float4* d4 = reinterpret_cast<float4*>(dst);
+        for (int l = 1; l <= Q; l++) {
+            const int span = 1 << l;
+            const bool first = (tile & (span - 1)) == 0;
+            const bool closes = ((tile + 1) & (span - 1)) == 0;
 #pragma unroll
-                        for (int c = 0; c < 8; c++) d4[c] = make_float4(av[4 * c], av[4 * c + 1], av[4 * c + 2], av[4 * c + 3]);
-                    }
-                }
+            for (int e = 0; e < DH; e++) acc[l - 1][e] = first ? sv[e] : fmaf(acc[l - 1][e], ge, sv[e]);
+            if (closes) {
+                const int m = tile >> l;
+                if ((m & 1) == 0 && ((m + 1) << l) < NT) store_node(l, m, acc[l - 1]);
+                if (l == Q && ntiles == kSegTiles) store_seg(acc[l - 1]);
             }
         }
         tc_fence_before();
@@ -428,34 +457,39 @@ __global__ void __launch_bounds__(128, 1)
     if (!ok || fail_sh) {
         if (tid == 0) record_error(err, kDevTimeout);
         // let in-flight copies and MMAs land before the shared memory and TMEM go away
-        mbar_wait(&bar_mma, mma_phase);
-        for (int s = 0; s < 2; s++) mbar_try_wait(&bar_full[s], 0);
+        for (int b = 0; b < 2; b++) mbar_wait(&bar_mma[b], 0), mbar_wait(&bar_full[b], 0);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, tmem_cols);
+    if (warp == 0) tmem_dealloc(tmem, kCols);
 }
 
 // ------------------------------------------------------------------ tc_merge
 
-// Two jobs, one launch, grid (dk*DV/256 + 1, BH), 256 threads:
-//  * blocks x < dk*DV/256 (only when P > q + 1): levels p = q+1 .. P-1 from the
-//    full-segment totals (fp32 [BH][nseg][dk][DV], decayed to each segment's
-//    end). In place: pyramid node (r, m) over segments overwrites segment slot
-//    m 2^r. One matrix element per thread.
-//  * block x = dk*DV/256: the per-tile decay table dtab[bh][j][p] (log2 units):
-//    sum of g over tiles [(j >> p) << p, j), the log-decay from the end of the
-//    block node (p, (j >> p) - 1) to the start of tile j, for each set bit p of j.
+// Nodes above the segment level and the per-tile decay table, one launch,
+// grid (dk*DV/1024 + 1, max(1, nodes above level q), BH), 256 threads:
+//  * block (x >= 1, y): elements [1024 (x-1), 1024 x) of the y-th node (p, m) with
+//    p > q that a tile reads (m even, (m+1) 2^p < NT): the decayed sum of its block's
+//    full-segment totals (fp32, each decayed to its segment's end),
+//    node = sum_sigma exp(log-decay from sigma's end to the block end) Z_sigma.
+//    Every input is read independently; no level depends on another.
+//  * block (0, 0): the per-tile decay table dtab[bh][j][p] (log2 units): sum of g over
+//    tiles [(j >> p) << p, j), the log-decay from the end of node (p, (j >> p) - 1) to
+//    the start of tile j, for each set bit p of j.
 // Block (0, 0) also resets the tile counter tc_output's CTAs take tiles from.
 __global__ void __launch_bounds__(256)
-    tc_merge_kernel(float* __restrict__ seg_tot, const float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
-                    float* __restrict__ dtab, int* __restrict__ tile_counter, int NT, int q, int P, int nseg,
-                    int node_count, int msz, LevelOffsets lo) {
-    extern __shared__ float Gs[];  // nseg segment log-decay totals (updated in place per level)
-    const int bh = blockIdx.y;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *tile_counter = 0;  // tile scheduler of tc_output
+    tc_merge_kernel(const float* __restrict__ seg_tot, const float* __restrict__ g_tiles,
+                    __nv_bfloat16* __restrict__ nodes, float* __restrict__ dtab, int* __restrict__ tile_counter,
+                    int NT, int q, int P, int nseg, int node_count, int msz, LevelOffsets lo) {
+    __shared__ float wsg[1024];      // per-segment totals, then weights, of this block's node
+    extern __shared__ float g_sh[];  // the head's tile totals (decay-table block only)
+    const int bh = blockIdx.z;
     const float* gh = g_tiles + static_cast<size_t>(bh) * NT;
-    if (static_cast<int>(blockIdx.x) == msz / 256) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *tile_counter = 0;
+    if (blockIdx.x == 0) {
+        if (blockIdx.y != 0) return;
+        for (int i = threadIdx.x; i < NT; i += blockDim.x) g_sh[i] = gh[i];
+        __syncthreads();
         for (int j = threadIdx.x; j < NT; j += blockDim.x) {
             float d[16];
 #pragma unroll
@@ -467,7 +501,7 @@ __global__ void __launch_bounds__(256)
             for (int p = 0; p < 16; p++) {
                 if (p < P && ((j >> p) & 1)) {
                     const int start = (j >> p) << p;
-                    for (; i >= start; i--) acc += gh[i];
+                    for (; i >= start; i--) acc += g_sh[i];
                     d[p] = acc * kLog2e;
                 }
             }
@@ -477,38 +511,44 @@ __global__ void __launch_bounds__(256)
         }
         return;
     }
-    if (q + 1 >= P) return;
+    // which node (p, m) is block y
+    int y = blockIdx.y, p = q + 1, m = -1;
+    for (; p < P; p++) {
+        const int cnt = (((NT - 1) >> p) + 1) / 2;
+        if (y < cnt) { m = 2 * y; break; }
+        y -= cnt;
+    }
+    if (m < 0) return;
+    const int nsg = 1 << (p - q);      // segments in the block
+    const int sg0 = m * nsg;           // its first segment
     const int seg_tiles = 1 << q;
-    for (int sgi = threadIdx.x; sgi < nseg; sgi += blockDim.x) {
-        float acc = 0.f;
-        for (int u = 0; u < seg_tiles; u++) {
-            const int tile = sgi * seg_tiles + u;
-            if (tile < NT) acc += gh[tile];
-        }
-        Gs[sgi] = acc;
+    // segment log-decay totals, then each segment's weight exp(sum of the totals after it)
+    for (int sg = threadIdx.x; sg < nsg; sg += blockDim.x) {
+        float tot = 0.f;
+        for (int u = 0; u < seg_tiles; u++) tot += gh[(sg0 + sg) * seg_tiles + u];
+        wsg[sg] = tot;
     }
     __syncthreads();
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    float* base = seg_tot + static_cast<size_t>(bh) * nseg * msz;
-    for (int r = 1; q + r < P; r++) {
-        const int p = q + r;
-        const int span = 1 << r;       // segments per node at this level
-        const int half = span >> 1;
-        const int nnodes = (NT >> p);  // full blocks of 2^p tiles
-        if (e < msz) {
-            for (int m = 0; m < nnodes; m++) {
-                const int s_lo = m * span, s_hi = m * span + half;
-                const float v = expf(Gs[s_hi]) * base[static_cast<size_t>(s_lo) * msz + e] +
-                                base[static_cast<size_t>(s_hi) * msz + e];
-                base[static_cast<size_t>(s_lo) * msz + e] = v;
-                if ((m & 1) == 0 && ((m + 1) << p) < NT)
-                    nodes[(static_cast<size_t>(bh) * node_count + lo.off[p] + (m >> 1)) * msz + e] = __float2bfloat16_rn(v);
-            }
+    if (threadIdx.x == 0) {
+        float after = 0.f;
+        for (int sg = nsg - 1; sg >= 0; sg--) {
+            const float tot = wsg[sg];
+            wsg[sg] = expf(after);
+            after += tot;
         }
-        __syncthreads();
-        for (int m = threadIdx.x; m < nnodes; m += blockDim.x) Gs[m * span] = Gs[m * span] + Gs[m * span + half];
-        __syncthreads();
     }
+    __syncthreads();
+    const int e = (blockIdx.x - 1) * 1024 + threadIdx.x;
+    const float* z = seg_tot + (static_cast<size_t>(bh) * nseg + sg0) * msz + e;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int sg = 0; sg < nsg; sg++) {
+        const float w = wsg[sg];
+#pragma unroll
+        for (int i = 0; i < 4; i++) acc[i] = fmaf(w, z[static_cast<size_t>(sg) * msz + 256 * i], acc[i]);
+    }
+    __nv_bfloat16* dst = nodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + (m >> 1)) * msz + e;
+#pragma unroll
+    for (int i = 0; i < 4; i++) dst[256 * i] = __float2bfloat16_rn(acc[i]);
 }
 
 // ------------------------------------------------------------------ tc_output
@@ -1081,20 +1121,17 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
     return r == CUDA_SUCCESS;
 }
 
-// Segment size 2^q: level accumulators need (1 + q) * dv TMEM columns (<= 256 so two
-// CTAs fit an SM); prefer at least two CTAs per SM worth of segments.
+// Segment size 2^q: the node kernel keeps q level accumulators of dv/2 floats per
+// thread in registers, within the 128 registers that let two CTAs share an SM
+// (q <= 2 for dv = 64, q <= 1 for dv = 128); prefer at least two CTAs per SM worth
+// of segments.
 int choose_q(int BH, int NT, int dv) {
-    const int qmax = dv == 64 ? 3 : 1;
+    const int qmax = dv == 64 ? 2 : 1;
     int q = 0;
     while (q < qmax && static_cast<int64_t>(BH) * ((NT + (2 << q) - 1) / (2 << q)) >= 2 * 152) q++;
     return q;
 }
 
-uint32_t pow2_cols(int cols) {
-    uint32_t c = 32;
-    while (c < static_cast<uint32_t>(cols)) c <<= 1;
-    return c;
-}
 
 template <int DV>
 cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
@@ -1126,17 +1163,27 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
     // nodes and tile decays
     {
         const int smem = NodesSmem<DV>::kBytes;
-        cudaError_t e = cudaFuncSetAttribute(tc_nodes_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        auto launch = [&](auto kern) -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            kern<<<dim3(nseg, BH), 256, smem, stream>>>(tk, tv, log_a, g_tiles, nodes, seg_tot, tok_cl2, tok_colw, pl.T,
+                                                        pl.NT, pl.node_count, lo, err);
+            return cudaSuccess;
+        };
+        cudaError_t e;
+        switch (qlog) {
+            case 0: e = launch(tc_nodes_kernel<DV, 0>); break;
+            case 1: e = launch(tc_nodes_kernel<DV, 1>); break;
+            default: e = launch(tc_nodes_kernel<DV, DV == 64 ? 2 : 1>); break;
+        }
         if (e != cudaSuccess) return e;
-        const uint32_t cols = pow2_cols((1 + qlog) * DV);
-        tc_nodes_kernel<DV><<<dim3(nseg, BH), 128, smem, stream>>>(tk, tv, log_a, g_tiles, nodes, seg_tot, tok_cl2,
-                                                                   tok_colw, pl.T, pl.NT, qlog, pl.node_count, lo,
-                                                                   cols, err);
         note_launch(stream, "tc_nodes");
     }
     {
         const int msz = kDk * DV;
-        tc_merge_kernel<<<dim3(msz / 256 + 1, BH), 256, nseg * sizeof(float), stream>>>(
+        int n_above = 0;
+        for (int p = qlog + 1; p < pl.P; p++) n_above += (((pl.NT - 1) >> p) + 1) / 2;
+        tc_merge_kernel<<<dim3(msz / 1024 + 1, n_above > 0 ? n_above : 1, BH), 256, pl.NT * sizeof(float), stream>>>(
             seg_tot, g_tiles, nodes, dtab, tile_counter, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
         note_launch(stream, "tc_merge");
     }
@@ -1186,6 +1233,8 @@ bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* pl) {
     const int nseg = (pl->NT + seg_tiles - 1) / seg_tiles;
     // 32-bit TMA row coordinates, a 16-entry level list per tile, merge totals in shared memory
     if (static_cast<int64_t>(BH) * T >= (int64_t(1) << 31) || pl->P > 16 || nseg > 12288) return false;
+    if (pl->P - 1 - pl->q > 10) return false;  // the merge kernel weighs at most 1024 segments per node
+    if (pl->NT > 8192) return false;            // and holds a head's tile totals in shared memory
     if (static_cast<int64_t>(BH) * pl->node_count * kDk >= (int64_t(1) << 31)) return false;
     const size_t msz = static_cast<size_t>(dk) * dv;
     pl->g_bytes = (static_cast<size_t>(BH) * pl->NT * sizeof(float) + 1023) / 1024 * 1024;
