@@ -590,13 +590,18 @@ struct OutCfg {
     static constexpr int kStageBytes = (kLam8 + kTile * 8 * 4 + 1023) / 1024 * 1024;
     static constexpr int kQkvBytes = (4 + DV / 64) * kPanelBytes;
     static constexpr int kNodeBytes = (DV / 64) * kPanelBytes;
-    static constexpr int kLvSlots = DV == 64 ? 3 : 1;  // TMEM level slots after O
+    // TMEM: S of the two tiles in flight at columns [128 b, 128 b + 128). Once a tile's
+    // S is consumed its buffer takes the tile's O (first DV columns) and, for DV = 64,
+    // level slot 0; the other level slots sit at [256, 512).
+    static constexpr int kLvSlots = DV == 64 ? 5 : 2;
     static constexpr int kNodeSlots = DV == 64 ? 3 : 2;
     static constexpr int kNodeBase = kStages * kStageBytes;
     static constexpr int kBytes = kNodeBase + kNodeSlots * kNodeBytes + 1024;
-    static constexpr uint32_t kColO = 256;
-    static constexpr uint32_t kColLv = 256 + DV;
     static constexpr uint32_t kTmemCols = 512;
+    __device__ static constexpr uint32_t col_o(int b) { return 128u * b; }
+    __device__ static constexpr uint32_t col_lv(int b, int slot) {
+        return DV == 64 ? (slot == 0 ? 128u * b + 64u : 256u + 64u * (slot - 1)) : 256u + 128u * slot;
+    }
     static constexpr int kEpiWarps = 8;
     static constexpr int kThreads = (3 + kEpiWarps) * 32;
 };
@@ -622,6 +627,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                      smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
+}
+
+// Pull a 128-row x 64-column box of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Pull a contiguous range (16-byte aligned, size % 16 == 0) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 4-byte asynchronous global -> shared copy (no alignment beyond 4 bytes needed).
@@ -711,14 +729,45 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- input producer
+        // Tiles are claimed kClaimAhead jobs before their stage frees up; a claimed
+        // tile's Q, K, V, decay rows and lambda rows are pulled into L2 at once, so the
+        // stage's own copies later come from L2.
+        constexpr int kClaimAhead = 2;
+        int claimed[kClaimAhead + 1];
         int n_in = 0;
-        for (int k = 0;; k++) {
-            const int s = k % NS;
-            if (k >= NS && !ewait(&in_empty[s], ((k / NS) - 1) & 1)) break;
+        auto claim = [&]() -> int {
             int idx = 0;
             if (lane == 0) idx = atomicAdd(tile_counter, 1);
             idx = __shfl_sync(0xffffffffu, idx, 0);
-            const bool done = idx >= total_tiles;
+            if (idx >= total_tiles) return -1;
+            if (lane == 0) {
+                int pbh, pj;
+                tile_of(idx, pbh, pj);
+                const int r0 = pbh * T + pj * kTile;
+                tma_prefetch_l2(&tm_q, 0, r0);
+                tma_prefetch_l2(&tm_q, 64, r0);
+                tma_prefetch_l2(&tm_k, 0, r0);
+                tma_prefetch_l2(&tm_k, 64, r0);
+#pragma unroll
+                for (int c = 0; c < DV / 64; c++) tma_prefetch_l2(&tm_v, 64 * c, r0);
+                prefetch_l2(tok_cl2 + r0, 512);
+                prefetch_l2(tok_colw + r0, 512);
+                const uintptr_t lb = reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r0) * L) & ~uintptr_t(15);
+                const uintptr_t le = (reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r0 + kTile) * L) + 15) &
+                                     ~uintptr_t(15);
+                prefetch_l2(reinterpret_cast<const void*>(lb), static_cast<uint32_t>(le - lb));
+            }
+            return idx;
+        };
+        for (int a = 0; a < kClaimAhead; a++) claimed[a] = claim();
+        for (int k = 0;; k++) {
+            const int s = k % NS;
+            if (k >= NS && !ewait(&in_empty[s], ((k / NS) - 1) & 1)) break;
+            const int idx = claimed[0];
+#pragma unroll
+            for (int a = 0; a + 1 < kClaimAhead; a++) claimed[a] = claimed[a + 1];
+            claimed[kClaimAhead - 1] = idx < 0 ? -1 : claim();
+            const bool done = idx < 0;
             if (lane == 0) {
                 tile_id_sh[s] = done ? -1 : idx;
                 mbar_arrive(&id_ready[s]);
@@ -823,9 +872,8 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 mma_commit(&s_full[b]);
                 return idx;
             };
-            // Phase 2 of tile k (O = P V and the level reads, kLvSlots per round) is issued
-            // after phase 1 of tile k+1, so S of the next tile is computed while this
-            // tile waits for its P; the inputs are staged well ahead by the producer.
+            // Phase 2 of tile k: O = P V into the tile's retired S buffer and the level reads,
+            // kLvSlots per round.
             int p2_p = 0, p2_rounds = 0;
             auto phase2 = [&](int k, int idx, bool first_round) -> bool {
                 int bh, j;
@@ -850,7 +898,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; kk++) {
                             const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                            mma_bf16(tmem + C::kColO, sdesc(pb + aoff, 16, 1024),
+                            mma_bf16(tmem + C::col_o(b), sdesc(pb + aoff, 16, 1024),
                                      sdesc(vb + kk * 2048, kPanelBytes, 1024), kIdO, kk > 0 ? 1u : 0u);
                         }
                     }
@@ -862,7 +910,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                         if (!wait(&node_full[slot], (gn / C::kNodeSlots) & 1)) return false;
                         tc_fence_after();
                         const uint32_t nb = smem_u32(smem + C::kNodeBase + slot * C::kNodeBytes);
-                        const uint32_t dcol = C::kColLv + sl * DV;
+                        const uint32_t dcol = C::col_lv(b, sl);
 #pragma unroll
                         for (int kk = 0; kk < kDk / 16; kk++) {
                             const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
@@ -877,31 +925,13 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 if (r_end == p2_rounds) mma_commit(&in_empty[s]);  // every MMA of the tile is issued
                 return true;
             };
-            int ids[2] = {-1, -1};
-            int count = 1 << 30;  // jobs of this CTA, known once phase 1 meets the end marker
-            bool ok = true;
-            for (int k = 0; k < C::kAhead && ok; k++) {
-                const int id = phase1(k);
-                if (id == -2) ok = false;
-                else if (id < 0) { count = k; break; }
-                else ids[k & 1] = id;
-            }
-            for (int k = 0; ok; k++) {
-                if (C::kAhead == 0) {
-                    const int id = phase1(k);
-                    if (id < 0) break;
-                    ids[k & 1] = id;
-                } else if (k >= count) {
-                    break;
-                }
-                if (C::kAhead > 0 && k + C::kAhead < count) {
-                    const int id = phase1(k + C::kAhead);
-                    if (id == -2) break;
-                    if (id < 0) count = k + C::kAhead;
-                    else ids[(k + C::kAhead) & 1] = id;
-                }
-                if (!phase2(k, ids[k & 1], true)) break;
-                if (p2_rounds > 1 && !phase2(k, ids[k & 1], false)) break;
+            // Order: phase 1 of tile 0; then per tile k: phase 2 of k (all rounds), phase 1
+            // of k+1. The next tile's S is computed while the epilogue finishes tile k.
+            int id_cur = phase1(0);
+            for (int k = 0; id_cur >= 0; k++) {
+                if (!phase2(k, id_cur, true)) break;
+                if (p2_rounds > 1 && !phase2(k, id_cur, false)) break;
+                id_cur = phase1(k + 1);
             }
             // every MMA issued by this CTA has completed before TMEM is released
             mma_commit(&drain);
@@ -1006,10 +1036,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&p_ready[b]);
-                mbar_arrive(&s_free[b]);
-            }
+            if (lane == 0) mbar_arrive(&p_ready[b]);
             return idx;
         };
 
@@ -1035,13 +1062,13 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 tc_fence_after();
                 if (r == 0) {
 #pragma unroll
-                    for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tmem + lane_base + C::kColO + half * DH + c0, acc + c0);
+                    for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tmem + lane_base + C::col_o(b) + half * DH + c0, acc + c0);
                 }
                 const int x_end = min(nl, (r + 1) * C::kLvSlots);
 #pragma unroll 1
                 for (int x = r * C::kLvSlots; x < x_end; x++) {
                     const float w = rr[x];
-                    const uint32_t col = C::kColLv + (x - r * C::kLvSlots) * DV + half * DH;
+                    const uint32_t col = C::col_lv(b, x - r * C::kLvSlots) + half * DH;
 #pragma unroll
                     for (int c0 = 0; c0 < DH; c0 += 32) {
                         float lvv[32];
@@ -1054,6 +1081,10 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&lv_free);
             }
+            // the tile's TMEM buffer may now take the S of the tile two jobs ahead
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);
             uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV + half * DH);
 #pragma unroll
             for (int c = 0; c < DH / 8; c++)
@@ -1061,28 +1092,11 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                                     pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
         };
 
-        int ids[2] = {-1, -1};
-        int count = 1 << 30;
-        for (int k = 0; k < C::kAhead; k++) {
-            const int id = epi1(k);
-            if (id < 0) { count = k; break; }
-            ids[k & 1] = id;
-        }
         for (int k = 0;; k++) {
-            if (C::kAhead == 0) {
-                const int id = epi1(k);
-                if (id < 0) break;
-                ids[k & 1] = id;
-            } else if (k >= count) {
-                break;
-            }
-            prefetch2(ids[k & 1]);
-            if (C::kAhead > 0 && k + C::kAhead < count) {
-                const int id = epi1(k + C::kAhead);
-                if (id < 0) count = k + C::kAhead;
-                else ids[(k + C::kAhead) & 1] = id;
-            }
-            epi2(k, ids[k & 1]);
+            const int id = epi1(k);
+            if (id < 0) break;
+            prefetch2(id);
+            epi2(k, id);
         }
     }
 
