@@ -344,6 +344,129 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const T* __restrict__ 
     }
 }
 
+// The decode step for dk = DK known at compile time: each thread owns column group
+// col4 and rows i = tid / DV4 + r * (256 / DV4), r < RPT. Levels are the outer loop
+// and a thread's RPT rows are unrolled inside it, so every level issues RPT
+// independent 128-bit loads per thread. The state stream bypasses L2 retention
+// (evict-first loads and stores): it is read once and written once per step.
+template <typename T, int DV4, int DK>
+__global__ void __launch_bounds__(kThreads) decode_kernel_fixed(const T* __restrict__ q, const T* __restrict__ k,
+                                                                const T* __restrict__ v, const float* __restrict__ log_a,
+                                                                const float* __restrict__ lambda,
+                                                                float* __restrict__ states,
+                                                                const int64_t* __restrict__ tpos, T* __restrict__ out,
+                                                                int H, int Lmax, int* err) {
+    constexpr int DV = DV4 * 4;
+    constexpr int ROWS_PER_PASS = kThreads / DV4;
+    constexpr int RPT = DK / ROWS_PER_PASS;
+    static_assert(DK % ROWS_PER_PASS == 0, "rows must divide evenly");
+    __shared__ float qsh[DK], ksh[DK];
+    __shared__ float vsh[DV];
+    __shared__ float lam[40];
+    __shared__ float red[kThreads / 32][DV];
+    const int tid = threadIdx.x;
+    const int bh = blockIdx.x;
+    const int b = bh / H;
+    const int64_t tb = tpos[b];
+    if (tb < 0 || tb >= ((int64_t)1 << (Lmax - 1))) {
+        if (tid == 0) record_error(err, kDevBadInput);
+        return;
+    }
+    for (int x = tid; x < DK; x += kThreads) {
+        qsh[x] = load_f(q + (size_t)bh * DK + x);
+        ksh[x] = load_f(k + (size_t)bh * DK + x);
+    }
+    for (int x = tid; x < DV; x += kThreads) vsh[x] = load_f(v + (size_t)bh * DV + x);
+    for (int x = tid; x < Lmax; x += kThreads) lam[x] = lambda[(size_t)bh * Lmax + x];
+    __syncthreads();
+
+    const float a = expf(log_a[bh]);
+    const int c = tb > 0 ? __ffsll((long long)tb) - 1 : -1;  // trailing zeros of t
+    const int top = tb > 0 ? 64 - __clzll((long long)tb) : 0;  // bitlength(t): highest nonempty level
+    const int col4 = tid % DV4;
+    const int row0 = tid / DV4;
+    constexpr size_t msz4 = (size_t)DK * DV4;
+    float4* S = reinterpret_cast<float4*>(states) + (size_t)bh * Lmax * msz4 + (size_t)row0 * DV4 + col4;
+    constexpr size_t rstep = (size_t)ROWS_PER_PASS * DV4;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    if (tb > 0) {
+        // levels 0..c (all held for t-1) merge into level c+1, decayed by a_t
+        float4 mrg[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; r++) mrg[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int l = 0; l <= c; l++) {
+            float4 x[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; r++) x[r] = __ldcs(S + l * msz4 + r * rstep);
+#pragma unroll
+            for (int r = 0; r < RPT; r++) {
+                mrg[r].x += x[r].x; mrg[r].y += x[r].y; mrg[r].z += x[r].z; mrg[r].w += x[r].w;
+            }
+        }
+        const float lc = lam[c + 1];
+#pragma unroll
+        for (int r = 0; r < RPT; r++) {
+            float4 m = mrg[r];
+            m.x *= a; m.y *= a; m.z *= a; m.w *= a;
+            __stcs(S + (c + 1) * msz4 + r * rstep, m);
+            const float wq = lc * qsh[row0 + r * ROWS_PER_PASS];
+            o.x += wq * m.x; o.y += wq * m.y; o.z += wq * m.z; o.w += wq * m.w;
+        }
+        // coarser levels held for both t-1 and t: decay in place
+        for (int l = c + 2; l <= top; l++) {
+            if (((tb >> (l - 1)) & 1) == 0) continue;
+            float4 x[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; r++) x[r] = __ldcs(S + l * msz4 + r * rstep);
+            const float ll = lam[l];
+#pragma unroll
+            for (int r = 0; r < RPT; r++) {
+                x[r].x *= a; x[r].y *= a; x[r].z *= a; x[r].w *= a;
+                __stcs(S + l * msz4 + r * rstep, x[r]);
+                const float w = ll * qsh[row0 + r * ROWS_PER_PASS];
+                o.x += w * x[r].x; o.y += w * x[r].y; o.z += w * x[r].z; o.w += w * x[r].w;
+            }
+        }
+    }
+    // level 0: the new token
+    {
+        const float4 v4 = make_float4(vsh[col4 * 4], vsh[col4 * 4 + 1], vsh[col4 * 4 + 2], vsh[col4 * 4 + 3]);
+        const float l0 = lam[0];
+#pragma unroll
+        for (int r = 0; r < RPT; r++) {
+            const int i = row0 + r * ROWS_PER_PASS;
+            const float ki = ksh[i];
+            const float4 x0 = make_float4(ki * v4.x, ki * v4.y, ki * v4.z, ki * v4.w);
+            __stcs(S + r * rstep, x0);
+            const float w0 = l0 * qsh[i];
+            o.x += w0 * x0.x; o.y += w0 * x0.y; o.z += w0 * x0.z; o.w += w0 * x0.w;
+        }
+    }
+
+#pragma unroll
+    for (int off = DV4; off < 32; off <<= 1) {
+        o.x += __shfl_xor_sync(0xffffffffu, o.x, off);
+        o.y += __shfl_xor_sync(0xffffffffu, o.y, off);
+        o.z += __shfl_xor_sync(0xffffffffu, o.z, off);
+        o.w += __shfl_xor_sync(0xffffffffu, o.w, off);
+    }
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane < DV4) {
+        red[warp][lane * 4 + 0] = o.x;
+        red[warp][lane * 4 + 1] = o.y;
+        red[warp][lane * 4 + 2] = o.z;
+        red[warp][lane * 4 + 3] = o.w;
+    }
+    __syncthreads();
+    if (tid < DV) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; w++) sum += red[w][tid];
+        store_f(out + (size_t)bh * DV + tid, sum);
+    }
+}
+
 template <typename T>
 cudaError_t simt_forward_t(const SimtPlan& pl, const T* q, const T* k, const T* v, const float* log_a,
                            const float* lambda, T* out, void* workspace, cudaStream_t stream) {
@@ -376,6 +499,13 @@ template <typename T, int DV4>
 void launch_decode(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
                    float* states, const int64_t* t, void* out, int B, int H, int dk, int Lmax, int* err,
                    cudaStream_t stream) {
+    if (dk == 128) {
+        decode_kernel_fixed<T, DV4, 128><<<B * H, kThreads, 0, stream>>>(
+            static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), log_a, lambda, states, t,
+            static_cast<T*>(out), H, Lmax, err);
+        note_launch(stream, "decode_step");
+        return;
+    }
     decode_kernel<T, DV4><<<B * H, kThreads, 0, stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), log_a, lambda, states, t,
         static_cast<T*>(out), H, dk, Lmax, err);
