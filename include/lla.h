@@ -160,6 +160,25 @@ int lla_decode_step(const void* q, const void* k, const void* v, const float* lo
                     int B, int H, int dk, int dv, int Lmax, int dtype);
 
 /*
+ * Prefill -> decode hand-off: the Fenwick state set after a prompt of T tokens,
+ * i.e. what lla_decode_step expects on entry for the next position t = T.
+ *
+ *   k      [B,H,T,dk]  dtype   keys of the prompt
+ *   v      [B,H,T,dv]  dtype   values
+ *   log_a  [B,H,T]     fp32    log decays
+ *   fenwick_states [B,H,Lmax,dk,dv] fp32, written for every sequence: slot 0 =
+ *          k_{T-1} v_{T-1}^T, and each slot l >= 1 with bit l-1 of T-1 set = its
+ *          Fenwick bucket of T-1's prefix, sum_s prod_{r=s+1..T-1} a_r k_s v_s^T.
+ *          Slots empty at T-1 are left untouched. Needs Lmax >= bitlength(T-1) + 1.
+ *   dk, dv 1..128.
+ * Takes T fp32 values per (b, h) of scratch from the library's stream-ordered pool.
+ * Bucket pieces are added with fp32 atomics, so the summation order (and the last
+ * bits of the result) may vary between runs.
+ */
+int lla_prefill_state(const void* k, const void* v, const float* log_a, float* fenwick_states, int B, int H, int T,
+                      int dk, int dv, int Lmax, void* stream, int dtype);
+
+/*
  * Reads and clears the device error word of the current device after
  * synchronising `stream`: LLA_OK if no kernel recorded a fault since the last
  * read, LLA_ERR_DEVICE for rejected device-side input, LLA_ERR_TIMEOUT for a

@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
             lib.lla_forward_profile.restype = i
             lib.lla_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, vp, vp] + [i] * 6
             lib.lla_decode_step.restype = i
+            lib.lla_prefill_state.argtypes = [vp, vp, fp, fp] + [i] * 6 + [vp, i]
+            lib.lla_prefill_state.restype = i
             lib.lla_device_error.argtypes = [vp]
             lib.lla_device_error.restype = i
             _lib = lib
@@ -217,6 +219,22 @@ def decode_step(q, k, v, log_a, lam, states, t, out=None, stream=None):
                                  states.data_ptr(), t.data_ptr(), out.data_ptr(), _stream_handle(stream),
                                  B, H, dk, dv, Lmax, _dtype_code(q)), "lla_decode_step")
     return out
+
+
+def prefill_state(k, v, log_a, states, stream=None):
+    """lla_prefill_state: write into ``states`` [B,H,Lmax,dk,dv] fp32 the Fenwick state set after
+    the prompt (k [B,H,T,dk], v [B,H,T,dv], log_a [B,H,T]); the next decode position is t = T."""
+    torch = _torch()
+    B, H, T, dk = k.shape
+    dv = v.shape[-1]
+    Lmax = states.shape[2]
+    for t_, n in ((k, "k"), (v, "v"), (log_a, "log_a"), (states, "states")):
+        _check(t_, n, k.device)
+    if states.dtype != torch.float32 or states.shape != (B, H, Lmax, dk, dv):
+        raise ValueError("states must be float32 [B,H,Lmax,dk,dv]")
+    _call(load().lla_prefill_state(k.data_ptr(), v.data_ptr(), log_a.data_ptr(), states.data_ptr(), B, H, T, dk, dv,
+                                   Lmax, _stream_handle(stream), _dtype_code(k)), "lla_prefill_state")
+    return states
 
 
 def device_error(stream=None) -> int:

@@ -236,6 +236,31 @@ int lla_decode_step(const void* q, const void* k, const void* v, const float* lo
     return e == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
 }
 
+int lla_prefill_state(const void* k, const void* v, const float* log_a, float* fenwick_states, int B, int H, int T,
+                      int dk, int dv, int Lmax, void* stream, int dtype) {
+    if (!k || !v || !log_a || !fenwick_states) return LLA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(log_a) || !aligned16(fenwick_states)) return LLA_ERR_INVALID_ARG;
+    if (dtype != LLA_BF16 && dtype != LLA_F32) return LLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || T < 1 || dk < 1 || dv < 1 || Lmax < 1 || Lmax > 40) return LLA_ERR_INVALID_ARG;
+    if (lla::bitlength((int64_t)T - 1) + 1 > Lmax) return LLA_ERR_INVALID_ARG;
+    if (dk > 128 || dv > 128) return LLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 65535 || (int64_t)B * H * T * (dk > dv ? dk : dv) > ((int64_t)1 << 40)) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)B * H * T * sizeof(float);
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return LLA_ERR_CUDA;
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LLA_ERR_NOMEM;
+    }
+    cudaError_t e = lla::prefill_state(dtype, k, v, log_a, fenwick_states, B, H, T, dk, dv, Lmax, ws, s);
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
+}
+
 int lla_device_error(void* stream) {
     const int dev = current_device();
     if (dev < 0) return LLA_ERR_CUDA;

@@ -88,6 +88,8 @@ cudaError_t tc_forward(const TcPlan& plan, const void* q, const void* k, const v
 cudaError_t simt_forward(const SimtPlan& plan, int dtype, const void* q, const void* k, const void* v,
                          const float* log_a, const float* lambda, void* out, void* workspace, int* err,
                          cudaStream_t stream);
+cudaError_t prefill_state(int dtype, const void* k, const void* v, const float* log_a, float* states, int B, int H,
+                          int T, int dk, int dv, int Lmax, void* workspace, cudaStream_t stream);
 cudaError_t decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
                         const float* lambda, float* states, const int64_t* t, void* out, int B, int H,
                         int dk, int dv, int Lmax, int* err, cudaStream_t stream);

@@ -467,6 +467,139 @@ __global__ void __launch_bounds__(kThreads) decode_kernel_fixed(const T* __restr
     }
 }
 
+// ---- state set after a prefill (hand-off to the decode step)
+
+// Per head: the decay exponent from each token s to the last token pos = T-1,
+// suf[s] = sum_{r=s+1..pos} log_a_r, accumulated from pos downwards (so the
+// values near pos, the ones that matter, carry the least rounding); also writes
+// slot 0 (k_pos v_pos^T) and zeroes the other slots the pieces add into.
+// grid (BH), 256 threads.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) state_scan_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                                              const float* __restrict__ log_a, float* __restrict__ suf,
+                                                              float* __restrict__ states, int Tlen, int dk, int dv,
+                                                              int Lmax) {
+    __shared__ float carry_sh;
+    __shared__ float tile[kThreads];
+    const int bh = blockIdx.x, tid = threadIdx.x;
+    const float* a = log_a + (size_t)bh * Tlen;
+    float* sf = suf + (size_t)bh * Tlen;
+    const int pos = Tlen - 1;
+    if (tid == 0) carry_sh = 0.f;
+    __syncthreads();
+    // blocks of 256 tokens from the end: suf[s] = carry + sum_{r in (s, block end]} log_a_r
+    for (int end = pos; end >= 0; end -= kThreads) {
+        const int s = end - tid;
+        // inclusive suffix within the block of a[s+1 .. end]: x_s = a[s+1] (0 for s = pos)
+        tile[tid] = (s >= 0 && s + 1 <= pos) ? a[s + 1] : 0.f;
+        __syncthreads();
+        // Hillis-Steele inclusive scan over tid (tid 0 = the block's last token)
+        for (int off = 1; off < kThreads; off <<= 1) {
+            const float y = tid >= off ? tile[tid - off] : 0.f;
+            __syncthreads();
+            tile[tid] += y;
+            __syncthreads();
+        }
+        const float carry = carry_sh;
+        if (s >= 0) sf[s] = carry + tile[tid];
+        __syncthreads();
+        if (tid == kThreads - 1) carry_sh = carry + tile[tid];
+        __syncthreads();
+    }
+    const size_t msz = (size_t)dk * dv;
+    float* st = states + (size_t)bh * Lmax * msz;
+    for (int l = 1; l < Lmax; l++) {
+        if (((pos >> (l - 1)) & 1) == 0) continue;
+        for (size_t e = tid; e < msz; e += kThreads) st[l * msz + e] = 0.f;
+    }
+    const size_t r = (size_t)bh * Tlen + pos;
+    for (size_t e = tid; e < msz; e += kThreads)
+        st[e] = load_f(k + r * dk + e / dv) * load_f(v + r * dv + e % dv);
+}
+
+struct StatePieces {
+    static constexpr int kMax = 512;
+    int n;
+    int level[kMax], start[kMax], end[kMax];
+};
+
+// One piece [start, end) of a Fenwick bucket of pos = T-1: adds
+// sum_s exp(suf[s]) k_s v_s^T into its slot. grid (npieces, BH, ceil(dk*dv / 2048)).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) state_piece_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                                               const float* __restrict__ suf, float* __restrict__ states,
+                                                               int Tlen, int dk, int dv, int Lmax, StatePieces pc) {
+    __shared__ float ks[32][129];
+    __shared__ float vs[32][128];
+    const int tid = threadIdx.x;
+    const int piece = blockIdx.x, bh = blockIdx.y;
+    const int l = pc.level[piece], s0 = pc.start[piece], s1 = pc.end[piece];
+    const int msz = dk * dv;
+    float acc[8];
+    int ei[8], en[8];
+#pragma unroll
+    for (int r = 0; r < 8; r++) {
+        const int e = blockIdx.z * 2048 + tid + r * kThreads;
+        acc[r] = 0.f;
+        ei[r] = (e < msz) ? e / dv : 0;
+        en[r] = (e < msz) ? e % dv : 0;
+    }
+    const size_t row0 = (size_t)bh * Tlen;
+    for (int st = s0; st < s1; st += 32) {
+        const int ns = min(32, s1 - st);
+        for (int x = tid; x < ns * dk; x += kThreads) {
+            const int sl = x / dk, d = x % dk;
+            ks[sl][d] = expf(suf[row0 + st + sl]) * load_f(k + (row0 + st + sl) * dk + d);
+        }
+        for (int x = tid; x < ns * dv; x += kThreads) vs[x / dv][x % dv] = load_f(v + (row0 + st + x / dv) * dv + x % dv);
+        __syncthreads();
+        for (int sl = 0; sl < ns; sl++) {
+#pragma unroll
+            for (int r = 0; r < 8; r++) acc[r] += ks[sl][ei[r]] * vs[sl][en[r]];
+        }
+        __syncthreads();
+    }
+    float* dst = states + ((size_t)bh * Lmax + l) * msz;
+#pragma unroll
+    for (int r = 0; r < 8; r++) {
+        const int e = blockIdx.z * 2048 + tid + r * kThreads;
+        if (e < msz) atomicAdd(dst + e, acc[r]);
+    }
+}
+
+template <typename T>
+cudaError_t prefill_state_t(const void* k, const void* v, const float* log_a, float* states, int B, int H, int T_,
+                            int dk, int dv, int Lmax, void* workspace, cudaStream_t stream) {
+    const int BH = B * H;
+    float* suf = static_cast<float*>(workspace);
+    const int pos = T_ - 1;
+    // pieces of the buckets of pos's Fenwick walk, each at most `plen` tokens
+    StatePieces pc;
+    pc.n = 0;
+    int plen = 512;
+    while ((pos + plen - 1) / plen + 40 > StatePieces::kMax) plen *= 2;
+    for (int b = pos; b > 0; b -= b & (-b)) {
+        const int low = b & (-b);
+        int level = 1;
+        for (int w = low; w > 1; w >>= 1) level++;
+        for (int st = b - low; st < b; st += plen) {
+            pc.level[pc.n] = level;
+            pc.start[pc.n] = st;
+            pc.end[pc.n] = st + plen < b ? st + plen : b;
+            pc.n++;
+        }
+    }
+    state_scan_kernel<T><<<BH, kThreads, 0, stream>>>(static_cast<const T*>(k), static_cast<const T*>(v), log_a, suf,
+                                                       states, T_, dk, dv, Lmax);
+    note_launch(stream, "state_scan");
+    if (pc.n > 0) {
+        state_piece_kernel<T><<<dim3(pc.n, BH, (dk * dv + 2047) / 2048), kThreads, 0, stream>>>(
+            static_cast<const T*>(k), static_cast<const T*>(v), suf, states, T_, dk, dv, Lmax, pc);
+        note_launch(stream, "state_pieces");
+    }
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t simt_forward_t(const SimtPlan& pl, const T* q, const T* k, const T* v, const float* log_a,
                            const float* lambda, T* out, void* workspace, cudaStream_t stream) {
@@ -559,6 +692,12 @@ cudaError_t simt_forward(const SimtPlan& pl, int dtype, const void* q, const voi
     return simt_forward_t<__nv_bfloat16>(pl, static_cast<const __nv_bfloat16*>(q),
                                          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
                                          log_a, lambda, static_cast<__nv_bfloat16*>(out), workspace, stream);
+}
+
+cudaError_t prefill_state(int dtype, const void* k, const void* v, const float* log_a, float* states, int B, int H,
+                          int T, int dk, int dv, int Lmax, void* workspace, cudaStream_t stream) {
+    if (dtype == 1) return prefill_state_t<float>(k, v, log_a, states, B, H, T, dk, dv, Lmax, workspace, stream);
+    return prefill_state_t<__nv_bfloat16>(k, v, log_a, states, B, H, T, dk, dv, Lmax, workspace, stream);
 }
 
 cudaError_t decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,

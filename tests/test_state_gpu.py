@@ -1,0 +1,103 @@
+"""GPU checks of lla_prefill_state, the prefill -> decode hand-off.
+
+The state set after a prompt of T tokens is compared with the fp64 oracle's
+recurrent state (stepping its decode step from empty states over the prompt),
+slot by slot for the slots held at position T-1; then the hand-off itself:
+decode steps started from that state reproduce lla_forward's rows of the
+longer sequence.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from log_linear_attention_gb300 import inputs
+from tests._util import rel_err_per_head, to_device
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from log_linear_attention_gb300 import binding
+    binding.load()
+
+
+def oracle_state(inp, Lmax):
+    """fp64 state set after all T tokens, by stepping the oracle's decode step."""
+    q, k, v, log_a = inp.q, inp.k, inp.v, inp.log_a
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    states = np.zeros((B, H, Lmax, dk, dv))
+    lam = np.ones((B, H, Lmax))
+    for t in range(T):
+        oracle.decode_step(q[:, :, t], k[:, :, t], v[:, :, t], log_a[:, :, t], lam, states, np.full(B, t))
+    return states
+
+
+def held_levels(pos, Lmax):
+    return [0] + [l for l in range(1, Lmax) if (pos >> (l - 1)) & 1]
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,dtype", [
+    (1, 1, 1, 16, 16, "f32"),
+    (2, 1, 7, 8, 4, "f32"),
+    (1, 2, 64, 16, 16, "f32"),
+    (1, 1, 300, 24, 40, "f32"),
+    (2, 2, 1024, 128, 64, "bf16"),
+    (1, 1, 1537, 64, 128, "bf16"),
+])
+def test_prefill_state_matches_recurrence(B, H, T, dk, dv, dtype):
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.PrefillConfig("st", B, H, T, dk, dv, 16, dtype)
+    inp = inputs.make_prefill(cfg, seed=T + dk)
+    Lmax = inputs.num_levels(T) + 1
+    _, k, v, log_a, _ = to_device(inp)
+    states = torch.full((B, H, Lmax, dk, dv), float("nan"), dtype=torch.float32, device="cuda")
+    binding.prefill_state(k, v, log_a, states)
+    torch.cuda.synchronize()
+    got = states.cpu().numpy()
+    ref = oracle_state(inp, Lmax)
+    for l in held_levels(T - 1, Lmax):
+        d = np.abs(got[:, :, l] - ref[:, :, l]).max() / max(np.abs(ref[:, :, l]).max(), 1e-30)
+        assert d <= 1e-4, (l, d)
+    # slots empty at T-1 are left untouched
+    for l in range(Lmax):
+        if l not in held_levels(T - 1, Lmax):
+            assert np.isnan(got[:, :, l]).all()
+
+
+@pytest.mark.parametrize("T,extra,dk,dv,dtype,tol", [(256, 16, 32, 16, "f32", 1e-4), (1000, 8, 128, 64, "bf16", 2e-2),
+                                                      (1023, 129, 128, 64, "bf16", 2e-2)])
+def test_handoff_continues_the_forward(T, extra, dk, dv, dtype, tol):
+    """prefill_state(prompt of T) + decode steps t = T .. T+extra-1 == lla_forward rows of
+    the T+extra sequence."""
+    from log_linear_attention_gb300 import binding
+    full = T + extra
+    cfg = inputs.PrefillConfig("ho", 1, 2, full, dk, dv, 16, dtype)
+    inp = inputs.make_prefill(cfg, seed=full)
+    q, k, v, log_a, lam = to_device(inp)
+    chunk = 16 if full % 16 == 0 else None
+    ref = oracle.explicit(inp.q, inp.k, inp.v, inp.log_a, inp.lam) if full <= 300 else None
+    Lmax = inputs.num_levels(full)
+    states = torch.zeros((1, 2, Lmax, dk, dv), dtype=torch.float32, device="cuda")
+    binding.prefill_state(k[:, :, :T].contiguous(), v[:, :, :T].contiguous(), log_a[:, :, :T].contiguous(), states)
+    outs = []
+    for t in range(T, full):
+        tt = torch.full((1,), t, dtype=torch.int64, device="cuda")
+        o = binding.decode_step(q[:, :, t].contiguous(), k[:, :, t].contiguous(), v[:, :, t].contiguous(),
+                                log_a[:, :, t].contiguous(), lam[:, :, t, :Lmax].contiguous(), states, tt)
+        outs.append(o)
+    dec = torch.stack(outs, dim=2).float().cpu().numpy()
+    assert binding.device_error() == 0
+    if chunk is not None:
+        fwd = binding.forward(q, k, v, log_a, lam, chunk).float().cpu().numpy()[:, :, T:]
+        assert rel_err_per_head(dec, fwd) <= tol
+    rows = oracle.explicit_rows(inp.q, inp.k, inp.v, inp.log_a, inp.lam, 0, 1, list(range(T, full)))
+    err = np.abs(dec[0, 1] - rows).max() / np.abs(rows).max()
+    assert err <= tol
+    if ref is not None:
+        assert rel_err_per_head(dec, ref[:, :, T:]) <= tol
