@@ -223,14 +223,22 @@ def dist_env():
     return ws, rank, local
 
 
-def max_over_ranks(x: float, ws: int) -> float:
+def max_over_ranks(x: float, ws: int, device: str = "cuda") -> float:
+    """The slowest rank's time: every rank's timing scalar reduced with MAX (the only
+    collective of the benchmark; the workload itself has no data-path exchange)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tokens_per_s(tokens_per_rank: int, ms_max: float, ws: int) -> float:
+    """Whole-job throughput under weak scaling: every rank processes its own full
+    workload, so the job moves ws * tokens_per_rank tokens in the slowest rank's time."""
+    return ws * tokens_per_rank / (ms_max / 1e3)
 
 
 def barrier(ws: int):
@@ -408,7 +416,7 @@ def run_lla(args, cfg):
     clk = clocks.stop()
     ms_total = max_over_ranks(ms_total, ws)
     ms = ms_total / args.steps
-    tokens_per_s = ws * cfg.tokens / (ms / 1e3)
+    tokens_per_s = aggregate_tokens_per_s(cfg.tokens, ms, ws)
     tflops = work["flops"] / (ms / 1e3) / 1e12
 
     # ---- per-kernel device times (CUDA events recorded by the library between its launches)
@@ -456,6 +464,20 @@ def run_lla(args, cfg):
     d_ms_total, dbytes, dsteps = bench_decode(args, dev, stream, rank, ws)
     d_gbs = ws * dbytes / (d_ms_total / 1e3) / 1e9
 
+    # ---- prefill -> decode hand-off: the state set after the whole prompt
+    hL = inputs.num_levels(cfg.T + 1)
+    hstates = torch.empty((cfg.B, cfg.H, hL, cfg.dk, cfg.dv), dtype=torch.float32, device=dev)
+
+    def hstep():
+        binding.prefill_state(dk_, dv_, da, hstates)
+
+    for _ in range(3):
+        hstep()
+    n_h = max(3, min(args.steps, 20))
+    h_ms = cuda_time(hstep, n_h, stream) / n_h
+    held = 1 + bin(cfg.T - 1).count("1")
+    h_bytes = (cfg.B * cfg.H * cfg.T * ((cfg.dk + cfg.dv) * 2 + 4) + cfg.B * cfg.H * held * cfg.dk * cfg.dv * 4)
+
     line = None
     if rank == 0:
         # CPU baseline: the oracle as it stands, on the host cores, bounded sample
@@ -478,6 +500,10 @@ def run_lla(args, cfg):
                        "gbs": d_gbs, "frac_of_hbm": d_gbs / peaks["hbm_gbs"],
                        "bytes_per_step": dbytes / dsteps, "convention": "eager: nonempty levels read once, "
                                                                          "held levels written once"},
+            "handoff": {"workload": f"state set after the {cfg.T}-token prompt of every (b, h) (lla_prefill_state)",
+                        "ms": h_ms, "gbs": h_bytes / (h_ms / 1e3) / 1e9,
+                        "frac_of_hbm": h_bytes / (h_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                        "bytes": h_bytes, "convention": "k, v, log_a read once; held state slots written once"},
             "e2e": {"value": ws * cfg.tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": {"value": cpu_val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
