@@ -248,7 +248,10 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
     const int dev = current_device();
     if (dev < 0) return LLA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bytes = (size_t)B * H * T * sizeof(float);
+    const bool tc = lla::tc_state_supported(dtype, dk, dv, B, H, T);
+    const size_t bytes = tc ? lla::tc_state_workspace_bytes(B, H, T) : (size_t)B * H * T * sizeof(float);
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
     cudaMemPool_t pool = workspace_pool(dev);
     if (!pool) return LLA_ERR_CUDA;
     void* ws = nullptr;
@@ -256,7 +259,8 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
         cudaGetLastError();
         return LLA_ERR_NOMEM;
     }
-    cudaError_t e = lla::prefill_state(dtype, k, v, log_a, fenwick_states, B, H, T, dk, dv, Lmax, ws, s);
+    cudaError_t e = tc ? lla::tc_prefill_state(k, v, log_a, fenwick_states, B, H, T, dv, Lmax, ws, err, s)
+                       : lla::prefill_state(dtype, k, v, log_a, fenwick_states, B, H, T, dk, dv, Lmax, ws, s);
     const cudaError_t f = cudaFreeAsync(ws, s);
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }

@@ -84,6 +84,12 @@ bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* plan);
 cudaError_t tc_forward(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
                        const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream);
 
+// Tensor-core state set after a prefill (lla_tc_state.cu): bf16, dk = 128, dv in {64, 128}.
+bool tc_state_supported(int dtype, int dk, int dv, int B, int H, int T);
+size_t tc_state_workspace_bytes(int B, int H, int T);
+cudaError_t tc_prefill_state(const void* k, const void* v, const float* log_a, float* states, int B, int H, int T,
+                             int dv, int Lmax, void* workspace, int* err, cudaStream_t stream);
+
 // SIMT launchers (lla_simt.cu).
 cudaError_t simt_forward(const SimtPlan& plan, int dtype, const void* q, const void* k, const void* v,
                          const float* log_a, const float* lambda, void* out, void* workspace, int* err,

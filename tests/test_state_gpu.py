@@ -6,6 +6,8 @@ slot by slot for the slots held at position T-1; then the hand-off itself:
 decode steps started from that state reproduce lla_forward's rows of the
 longer sequence.
 """
+import types
+
 import numpy as np
 import pytest
 
@@ -38,6 +40,15 @@ def oracle_state(inp, Lmax):
     return states
 
 
+def oracle_state_heads(inp, Lmax, heads):
+    """fp64 state set after all T tokens for the chosen (b, h) heads only."""
+    out = {}
+    for b, h in heads:
+        one = types.SimpleNamespace(**{n: getattr(inp, n)[b:b + 1, h:h + 1] for n in ("q", "k", "v", "log_a")})
+        out[(b, h)] = oracle_state(one, Lmax)[0, 0]
+    return out
+
+
 def held_levels(pos, Lmax):
     return [0] + [l for l in range(1, Lmax) if (pos >> (l - 1)) & 1]
 
@@ -47,8 +58,14 @@ def held_levels(pos, Lmax):
     (2, 1, 7, 8, 4, "f32"),
     (1, 2, 64, 16, 16, "f32"),
     (1, 1, 300, 24, 40, "f32"),
+    (1, 1, 1537, 64, 128, "bf16"),   # dk != 128: SIMT kernels
+    # bf16, dk = 128: tensor-core kernels (full tiles) + the last tile's levels 0..7
+    (1, 1, 1, 128, 64, "bf16"),
+    (1, 2, 129, 128, 64, "bf16"),
     (2, 2, 1024, 128, 64, "bf16"),
-    (1, 1, 1537, 64, 128, "bf16"),
+    (2, 1, 1000, 128, 128, "bf16"),
+    (1, 2, 4097, 128, 64, "bf16"),
+    (1, 1, 8192, 128, 128, "bf16"),
 ])
 def test_prefill_state_matches_recurrence(B, H, T, dk, dv, dtype):
     from log_linear_attention_gb300 import binding
@@ -101,3 +118,47 @@ def test_handoff_continues_the_forward(T, extra, dk, dv, dtype, tol):
     assert err <= tol
     if ref is not None:
         assert rel_err_per_head(dec, ref[:, :, T:]) <= tol
+
+
+@pytest.mark.parametrize("B,H,T,dv", [(4, 16, 2048, 64), (3, 8, 3001, 128)])
+def test_prefill_state_many_heads_sampled(B, H, T, dv):
+    """More (head, tile) pairs than SMs: a slot's tiles are split over several CTAs that
+    add into it; checked on sampled heads, every held slot."""
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.PrefillConfig("stm", B, H, T, 128, dv, 16, "bf16")
+    inp = inputs.make_prefill(cfg, seed=7 + T)
+    Lmax = inputs.num_levels(T) + 2
+    _, k, v, log_a, _ = to_device(inp)
+    states = torch.full((B, H, Lmax, 128, dv), float("nan"), dtype=torch.float32, device="cuda")
+    binding.prefill_state(k, v, log_a, states)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    got = states.cpu().numpy()
+    heads = [(0, 0), (B - 1, H - 1), (B // 2, H // 3)]
+    ref = oracle_state_heads(inp, Lmax, heads)
+    for (b, h), r in ref.items():
+        for l in held_levels(T - 1, Lmax):
+            d = np.abs(got[b, h, l] - r[l]).max() / max(np.abs(r[l]).max(), 1e-30)
+            assert d <= 1e-4, ((b, h), l, d)
+        for l in range(Lmax):
+            if l not in held_levels(T - 1, Lmax):
+                assert np.isnan(got[b, h, l]).all()
+
+
+def test_prefill_state_headline_sampled():
+    """The 4 x 16 heads x 8192-token bf16 prompt (dk 128, dv 64): two sampled heads."""
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.PREFILL_CONFIGS["headline"]
+    inp = inputs.make_prefill(cfg, seed=0)
+    Lmax = inputs.num_levels(cfg.T)
+    _, k, v, log_a, _ = to_device(inp)
+    states = torch.zeros((cfg.B, cfg.H, Lmax, cfg.dk, cfg.dv), dtype=torch.float32, device="cuda")
+    binding.prefill_state(k, v, log_a, states)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    got = states.cpu().numpy()
+    ref = oracle_state_heads(inp, Lmax, [(0, 5), (3, 15)])
+    for (b, h), r in ref.items():
+        for l in held_levels(cfg.T - 1, Lmax):
+            d = np.abs(got[b, h, l] - r[l]).max() / max(np.abs(r[l]).max(), 1e-30)
+            assert d <= 1e-4, ((b, h), l, d)
