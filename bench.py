@@ -390,6 +390,17 @@ def run_lla(args, cfg):
     host = [h.pin_memory() for h in host]
     dq, dk_, dv_, da, dl = (h.to(dev) for h in host)
     out = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.bfloat16, device=dev)
+    if args.mode == "handoff":
+        # prefill -> decode hand-off launches only (a short target for profilers)
+        hstates = torch.empty((cfg.B, cfg.H, inputs.num_levels(cfg.T + 1), cfg.dk, cfg.dv), dtype=torch.float32,
+                              device=dev)
+        for _ in range(max(args.warmup, 3)):
+            binding.prefill_state(dk_, dv_, da, hstates)
+        h_ms = cuda_time(lambda: binding.prefill_state(dk_, dv_, da, hstates), args.steps, stream) / args.steps
+        assert binding.device_error() == 0
+        if rank == 0:
+            print(json.dumps({"mode": "handoff", "config": cfg.name, "ms": h_ms, "steps": args.steps}))
+        return 0
     work = prefill_work(cfg)
 
     def step():
@@ -530,8 +541,8 @@ def main():
     ap.add_argument("--config", default="headline", choices=sorted(inputs.PREFILL_CONFIGS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--mode", choices=["all", "prefill", "decode"], default="all",
-                    help="prefill / decode: run only that workload's launches (profiling targets)")
+    ap.add_argument("--mode", choices=["all", "prefill", "decode", "handoff"], default="all",
+                    help="prefill / decode / handoff: run only that workload's launches (profiling targets)")
     args = ap.parse_args()
     cfg = inputs.PREFILL_CONFIGS[args.config]
     if args.impl == "reference":

@@ -14,19 +14,22 @@
 //   * every key of a full tile u < Pt sits at level 8 + floor(log2(u xor Pt)),
 //     so a full tile adds K_u^T diag(w) V_u to a single slot; the tiles of one
 //     slot are consecutive;
-//   * the keys of tile Pt (tokens 128 Pt .. pos) have levels 0..7.
+//   * the keys of tile Pt (tokens 128 Pt .. pos) have levels 0..7: that tile
+//     is visited once per level held at pos (at most 8 "virtual" tiles), each
+//     time with the weights of the other levels (and of tokens past pos) zero.
 // Kernels (one stream, in order):
 //   state_tile_totals : g_u = sum of log_a over full tile u.
-//   state_prep        : per head, (y = 0) tail_u = sum of log_a from the end of
-//                       tile u to pos (reverse scan, newest first) and zeroes
-//                       the slots >= 8 the next kernel adds into; (y = 1) the
-//                       slots 0..7 from tile Pt, fp32 FMA.
+//   state_prep        : per head, tail_u = sum of log_a from the end of tile u
+//                       to pos (reverse scan, newest first); other blocks
+//                       zero the slots held at pos.
 //   tc_state          : persistent; each CTA takes an equal share of the
-//                       flattened (head, full tile) list. Per tile,
+//                       flattened (head, tile) list. Per tile,
 //                       w_s = exp(tail_u + decay from s to the tile end), and
 //                       w o V is split into bf16 hi + lo (so the product keeps
-//                       ~16 mantissa bits); two tcgen05 MMAs per 16-token step
-//                       accumulate K^T (w o V) in TMEM. A run of tiles of one
+//                       ~16 mantissa bits); one tcgen05 MMA per 16-token step
+//                       (N = 2 dv: both parts side by side) accumulates
+//                       K^T [hi | lo] in TMEM, and the two halves are summed
+//                       when the accumulator is drained. A run of tiles of one
 //                       slot ends with the accumulator added (fp32 vector
 //                       atomics) into the slot.
 // Every mbarrier wait is bounded; on overrun the kernel records LLA_ERR_TIMEOUT
@@ -69,116 +72,61 @@ __device__ __forceinline__ float block_excl_scan256(float x, float* warp_tot) {
     return base + incl - x;
 }
 
-// grid (BH, 2), 256 threads, dynamic shared memory (see prep_smem_bytes).
-template <int DV>
+// Slot l is held at position pos: level 0 always, level l >= 1 when bit l - 1 of pos is set.
+__device__ __forceinline__ bool slot_held(int pos, int l) { return l == 0 || (l - 1 < 31 && ((pos >> (l - 1)) & 1)); }
+
+// grid (BH, 1 + Lmax), 256 threads, dynamic shared memory: Pt floats. Block y = 0 scans
+// the head's tile totals; block y = 1 + l zeroes slot l if it is held at pos (the MMA
+// kernel adds into it).
 __global__ void __launch_bounds__(kPrepThreads)
-    state_prep_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-                      const float* __restrict__ log_a, const float* __restrict__ g, float* __restrict__ tail,
-                      float* __restrict__ states, int T, int Pt, int Lmax) {
-    extern __shared__ float psm[];
+    state_prep_kernel(const float* __restrict__ log_a, const float* __restrict__ g, float* __restrict__ tail,
+                      float* __restrict__ states, int T, int Pt, int Lmax, int msz) {
+    extern __shared__ float g_sh[];
     __shared__ float warp_tot[8];
-    __shared__ float la_sh[kTile];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bh = blockIdx.x;
     const int pos = T - 1;
+    if (blockIdx.y > 0) {
+        const int l = blockIdx.y - 1;
+        if (!slot_held(pos, l)) return;
+        float4* st4 = reinterpret_cast<float4*>(states + (static_cast<size_t>(bh) * Lmax + l) * msz);
+        for (int e = tid; e < msz / 4; e += kPrepThreads) st4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
     const int base = Pt * kTile;     // first token of the tile of pos
     const int n = pos - base + 1;    // its tokens, 1..128
     const float* a = log_a + static_cast<size_t>(bh) * T;
-    constexpr size_t msz = static_cast<size_t>(kDk) * DV;
 
-    if (blockIdx.y == 0) {
-        // tail_u for every full tile, summed from pos backwards
-        float ts = (tid < n) ? a[base + tid] : 0.f;
+    // tail_u for every full tile, summed from pos backwards
+    float ts = (tid < n) ? a[base + tid] : 0.f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, off);
-        if (lane == 0) warp_tot[warp] = ts;
-        __syncthreads();
-        float tail_tot = 0.f;
-        for (int w = 0; w < 8; w++) tail_tot += warp_tot[w];
-        __syncthreads();
-        float* g_sh = psm;
-        for (int u = tid; u < Pt; u += kPrepThreads) g_sh[u] = g[static_cast<size_t>(bh) * Pt + u];
-        __syncthreads();
-        // thread t owns the tiles [hi - C, hi), hi = Pt - t C: thread 0 the newest
-        const int C = (Pt + kPrepThreads - 1) / kPrepThreads;
-        const int hi = Pt - tid * C;
-        const int lo = hi - C > 0 ? hi - C : 0;
-        float csum = 0.f;
-        for (int u = hi - 1; u >= lo; u--) csum += g_sh[u];
-        float run = tail_tot + block_excl_scan256(csum, warp_tot);
-        for (int u = hi - 1; u >= lo; u--) {
-            tail[static_cast<size_t>(bh) * Pt + u] = run;
-            run += g_sh[u];
-        }
-        // zero the slots >= 8 held at pos (bit l - 8 of Pt): the MMA kernel adds into them
-        float4* st4 = reinterpret_cast<float4*>(states + static_cast<size_t>(bh) * Lmax * msz);
-        for (int l = 8; l < Lmax; l++) {
-            if (((Pt >> (l - 8)) & 1) == 0) continue;
-            for (size_t e = tid; e < msz / 4; e += kPrepThreads) st4[l * (msz / 4) + e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        return;
-    }
-
-    // slots 0..7 from the tokens base .. pos: w_s = exp(sum_{r=s+1..pos} log_a_r)
-    float* kw_sh = psm;                 // [128][kDk] fp32, w_s k_s
-    float* v_sh = psm + kTile * kDk;    // [128][DV] fp32
-    if (tid < kTile) la_sh[tid] = (tid < n) ? a[base + tid] : 0.f;
+    for (int off = 16; off > 0; off >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, off);
+    if (lane == 0) warp_tot[warp] = ts;
     __syncthreads();
-    float suf = 0.f;  // summed from pos downwards
-    if (tid < kTile)
-        for (int r = n - 1; r > tid; r--) suf += la_sh[r];
+    float tail_tot = 0.f;
+    for (int w = 0; w < 8; w++) tail_tot += warp_tot[w];
     __syncthreads();
-    if (tid < kTile) la_sh[tid] = suf;
+    for (int u = tid; u < Pt; u += kPrepThreads) g_sh[u] = g[static_cast<size_t>(bh) * Pt + u];
     __syncthreads();
-    const size_t row0 = static_cast<size_t>(bh) * T + base;
-    for (int x = tid; x < n * kDk; x += kPrepThreads) {
-        const int i = x / kDk, d = x % kDk;
-        kw_sh[i * kDk + d] = expf(la_sh[i]) * __bfloat162float(k[(row0 + i) * kDk + d]);
+    // thread t owns the tiles [hi - C, hi), hi = Pt - t C: thread 0 the newest
+    const int C = (Pt + kPrepThreads - 1) / kPrepThreads;
+    const int hi = Pt - tid * C;
+    const int lo = hi - C > 0 ? hi - C : 0;
+    float csum = 0.f;
+    for (int u = hi - 1; u >= lo; u--) csum += g_sh[u];
+    float run = tail_tot + block_excl_scan256(csum, warp_tot);
+    for (int u = hi - 1; u >= lo; u--) {
+        tail[static_cast<size_t>(bh) * Pt + u] = run;
+        run += g_sh[u];
     }
-    for (int x = tid; x < n * DV; x += kPrepThreads) {
-        const int i = x / DV, e = x % DV;
-        v_sh[i * DV + e] = __bfloat162float(v[(row0 + i) * DV + e]);
-    }
-    __syncthreads();
-    constexpr int EH = DV / 2;
-    const int d = tid >> 1, e0 = (tid & 1) * EH;
-    float acc[EH];
-#pragma unroll
-    for (int j = 0; j < EH; j++) acc[j] = 0.f;
-    float* st = states + static_cast<size_t>(bh) * Lmax * msz + static_cast<size_t>(d) * DV + e0;
-    int cur = fenwick_level(pos, base);
-    for (int i = 0; i < n; i++) {
-        const int l = fenwick_level(pos, base + i);
-        if (l != cur) {
-            float4* dst = reinterpret_cast<float4*>(st + cur * msz);
-#pragma unroll
-            for (int j = 0; j < EH / 4; j++) dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
-#pragma unroll
-            for (int j = 0; j < EH; j++) acc[j] = 0.f;
-            cur = l;
-        }
-        const float kd = kw_sh[i * kDk + d];
-        const float4* vr = reinterpret_cast<const float4*>(v_sh + i * DV + e0);
-#pragma unroll
-        for (int j = 0; j < EH / 4; j++) {
-            const float4 x = vr[j];
-            acc[4 * j] = fmaf(kd, x.x, acc[4 * j]);
-            acc[4 * j + 1] = fmaf(kd, x.y, acc[4 * j + 1]);
-            acc[4 * j + 2] = fmaf(kd, x.z, acc[4 * j + 2]);
-            acc[4 * j + 3] = fmaf(kd, x.w, acc[4 * j + 3]);
-        }
-    }
-    float4* dst = reinterpret_cast<float4*>(st + cur * msz);
-#pragma unroll
-    for (int j = 0; j < EH / 4; j++) dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
 }
 
-template <int DV>
-size_t prep_smem_bytes(int Pt) {
-    const size_t tiles = static_cast<size_t>(kTile) * (kDk + DV) * sizeof(float);
-    const size_t scan = static_cast<size_t>(Pt) * sizeof(float);
-    return tiles > scan ? tiles : scan;
-}
+// Levels of the m virtual tiles over the tile of pos: 0, then the held levels 1..7,
+// four bits each (tile j at bits 4j..4j+3).
+struct TailLevels {
+    int m;
+    uint32_t packed;
+};
 
 template <int DV>
 struct StateCfg {
@@ -188,31 +136,40 @@ struct StateCfg {
     static constexpr int kStageBytes = kKBytes + 2 * kVBytes;
     static constexpr uint32_t kTxBytes = kKBytes + kVBytes;
     static constexpr int kBytes = kStages * kStageBytes + 1024;  // + alignment slack
-    static constexpr int kThreads = 384;
-    static constexpr uint32_t kTmemCols = 2 * DV;              // two accumulators
+    static constexpr int kThreads = 512;
+    static constexpr uint32_t kAccCols = 2 * DV;               // [hi part | lo part] of one accumulator
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;        // two accumulators
 };
 
-// Level of full tile u (< Pt) for the last token pos (Pt = pos >> 7).
-__device__ __forceinline__ int tile_level(int u, int Pt) { return 8 + 31 - __clz(u ^ Pt); }
+// Slot of tile u of a head: a full tile (u < Pt) sits at level 8 + floor(log2(u xor Pt));
+// tile Pt + j is the j-th virtual tile over the tile of pos.
+__device__ __forceinline__ int tile_level(int u, int Pt, uint32_t tail_lev) {
+    return u < Pt ? 8 + 31 - __clz(u ^ Pt) : static_cast<int>((tail_lev >> (4 * (u - Pt))) & 15u);
+}
 
-// 384 threads: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4..7
-// scale V (one token row per thread), warps 8..11 drain accumulators (TMEM lane
-// quadrant = warp % 4, one dk row per thread).
+// 512 threads: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4..11
+// scale V (two threads per token row, four 16-byte chunks of each 128-byte panel
+// row each; every warp derives the tile's decay prefix on its own, so the scaler
+// warps never wait for one another), warps 12..15 drain accumulators (TMEM lane quadrant = warp % 4, one
+// dk row per thread). Each head contributes NTe = Pt + tl.m tiles to the
+// flattened list.
 template <int DV>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, const float* __restrict__ tail, float* __restrict__ states,
-                    int T, int Pt, int Lmax, int total, int* err) {
+                    int T, int Pt, int Lmax, int total, const TailLevels tl, int* err) {
     using C = StateCfg<DV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t full_bar[S], scaled_bar[S], empty_bar[S], acc_full[2], acc_empty[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
-    __shared__ float wt_sh[2][4];
     __shared__ int fail_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NTe = Pt + tl.m;
+    const int pos = T - 1;
+    const int base = Pt * kTile;  // first token of the tile of pos
     const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
     const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
     volatile int* fail = &fail_sh;
@@ -220,7 +177,7 @@ __global__ void __launch_bounds__(384, 1)
     if (tid == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&scaled_bar[s], 4);
+            mbar_init(&scaled_bar[s], 8);
             mbar_init(&empty_bar[s], 1);
         }
         for (int b = 0; b < 2; b++) {
@@ -240,23 +197,46 @@ __global__ void __launch_bounds__(384, 1)
     auto fail_now = [&]() {
         if (atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
     };
-    // same slot for flattened tiles f and f + 1
-    auto same_run = [&](int f) {
-        const int b0 = f / Pt, b1 = (f + 1) / Pt;
-        return b0 == b1 && tile_level(f % Pt, Pt) == tile_level((f + 1) % Pt, Pt);
+    // Walk of this CTA's tiles without divisions: (bh, u) of tile f, its slot, and
+    // whether the next tile (f + 1 < t1) continues the same run.
+    struct Cursor {
+        int bh, u, lvl;
+        bool last_of_run;
+    };
+    auto cursor_at = [&](int f) {
+        Cursor c;
+        c.bh = f / NTe;
+        c.u = f % NTe;
+        c.lvl = tile_level(c.u, Pt, tl.packed);
+        c.last_of_run = true;
+        return c;
+    };
+    // advances c from tile f to f + 1 and fills c.last_of_run for tile f
+    auto step = [&](Cursor& c, int f) {
+        int nbh = c.bh, nu = c.u + 1;
+        if (nu == NTe) {
+            nu = 0;
+            nbh++;
+        }
+        const int nlvl = tile_level(nu, Pt, tl.packed);
+        c.last_of_run = (f + 1 >= t1) || nbh != c.bh || nlvl != c.lvl;
+        return Cursor{nbh, nu, nlvl, true};
     };
 
     int issued = 0;  // producer: tiles whose copies were issued
     if (warp == 0) {
         if (lane == 0) {
+            Cursor c = cursor_at(t0);
+            int s = 0;
+            uint32_t ph = 0;
             for (int f = t0; f < t1 && !*fail; f++, issued++) {
-                const int i = f - t0, s = i % S;
-                if (i >= S && !mbar_wait(&empty_bar[s], ((i / S) - 1) & 1)) {
+                if (f - t0 >= S && !mbar_wait(&empty_bar[s], ph ^ 1u)) {
                     fail_now();
                     break;
                 }
-                const int bh = f / Pt, u = f % Pt;
-                const int r0 = bh * T + u * kTile;
+                // rows of the tile of pos past the head's end are another head's (weight 0)
+                // or past the tensor (filled with zeros)
+                const int r0 = c.bh * T + (c.u < Pt ? c.u : Pt) * kTile;
                 uint8_t* st = smem + s * C::kStageBytes;
                 mbar_expect_tx(&full_bar[s], C::kTxBytes);
                 tma_load_2d(st, &tm_k, &full_bar[s], 0, r0);
@@ -264,100 +244,147 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int p = 0; p < DV / 64; p++)
                     tma_load_2d(st + C::kKBytes + p * kPanelBytes, &tm_v, &full_bar[s], 64 * p, r0);
+                c = step(c, f);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t kIdesc = idesc_bf16(kDk, DV, 1, 1);  // A = K^T (MN-major), B = w o V (MN-major)
-            int run = 0;
+            // A = K^T (MN-major); B = [hi | lo] of w o V (MN-major, N = 2 DV: the lo panels follow the
+            // hi panels at the same 16 KB panel stride), so one MMA per 16-token step covers both parts
+            constexpr uint32_t kIdesc = idesc_bf16(kDk, 2 * DV, 1, 1);
+            // a K step of 16 tokens moves every operand by 2048 B: +128 in the descriptor's address field
+            const uint64_t kdesc0 = sdesc(smem_u32(smem), kPanelBytes, 1024);
+            const uint64_t vdesc0 = sdesc(smem_u32(smem + C::kKBytes), kPanelBytes, 1024);
+            constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+            Cursor c = cursor_at(t0);
+            bool starting = true;
+            int run = 0, s = 0;
+            uint32_t ph = 0;
             for (int f = t0; f < t1 && !*fail; f++) {
-                const int i = f - t0, s = i % S;
-                const bool starting = (f == t0) || !same_run(f - 1);
-                const bool ending = (f == t1 - 1) || !same_run(f);
+                const Cursor nc = step(c, f);
+                const bool ending = c.last_of_run;
                 const int buf = run & 1;
                 if (starting && run >= 2 && !mbar_wait(&acc_empty[buf], ((run >> 1) - 1) & 1)) {
                     fail_now();
                     break;
                 }
-                if (!mbar_wait(&scaled_bar[s], (i / S) & 1)) {
+                if (!mbar_wait(&scaled_bar[s], ph)) {
                     fail_now();
                     break;
                 }
                 tc_fence_after();
-                const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
-                const uint32_t vb = kb + C::kKBytes, lb = vb + C::kVBytes;
-                const uint32_t d = tmem + buf * DV;
+                const uint64_t so = kStageStep * s;
+                const uint32_t d = tmem + buf * C::kAccCols;
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; kk++) {
-                    const uint64_t ad = sdesc(kb + kk * 2048, kPanelBytes, 1024);
-                    mma_bf16(d, ad, sdesc(vb + kk * 2048, kPanelBytes, 1024), kIdesc, (starting && kk == 0) ? 0u : 1u);
-                    mma_bf16(d, ad, sdesc(lb + kk * 2048, kPanelBytes, 1024), kIdesc, 1u);
+                    const uint64_t ko = so + 128u * kk;
+                    mma_bf16(d, kdesc0 + ko, vdesc0 + ko, kIdesc, (starting && kk == 0) ? 0u : 1u);
                 }
                 mma_commit(&empty_bar[s]);
                 if (ending) {
                     mma_commit(&acc_full[buf]);
                     run++;
                 }
+                starting = ending;
+                c = nc;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             // every MMA issued above has completed before TMEM and shared memory go away
             mma_commit(&drain_bar);
             if (!mbar_wait(&drain_bar, 0)) fail_now();
         }
-    } else if (warp >= 4 && warp < 8) {
-        const int row = tid - 128, w4 = warp - 4;
-        float la_next = 0.f, tail_next = 0.f;
-        if (t0 < t1) {
-            la_next = log_a[static_cast<size_t>(t0 / Pt) * T + (t0 % Pt) * kTile + row];
-            tail_next = tail[t0];
-        }
-        for (int f = t0; f < t1; f++) {
-            const int i = f - t0, s = i % S;
-            const float la = la_next, tl = tail_next;
-            if (f + 1 < t1) {
-                la_next = log_a[static_cast<size_t>((f + 1) / Pt) * T + ((f + 1) % Pt) * kTile + row];
-                tail_next = tail[f + 1];
+    } else if (warp >= 4 && warp < 12) {
+        const int sidx = tid - 128;
+        const int row = sidx & 127, half = sidx >> 7, w4 = (warp - 4) & 3;
+        const int n_last = pos - base + 1;  // tokens of the tile of pos
+        // log_a of the tile's tokens 32 j + lane (0 past pos), j = 0..3, and the tile's tail decay
+        auto tile_inputs = [&](const Cursor& c, float* la, float& tlv) {
+            const size_t hb = static_cast<size_t>(c.bh) * T;
+            if (c.u < Pt) {
+#pragma unroll
+                for (int j = 0; j < 4; j++) la[j] = log_a[hb + static_cast<size_t>(c.u) * kTile + 32 * j + lane];
+                tlv = tail[static_cast<size_t>(c.bh) * Pt + c.u];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; j++) la[j] = 32 * j + lane < n_last ? log_a[hb + base + 32 * j + lane] : 0.f;
+                tlv = 0.f;
             }
-            // decay from token row to the tile end: total - inclusive prefix
-            float incl = la;
+        };
+        // inputs are fetched two tiles ahead
+        Cursor c0 = cursor_at(t0);
+        Cursor c1 = step(c0, t0);
+        float la0[4], la1[4], tl0 = 0.f, tl1 = 0.f;
+        tile_inputs(c0, la0, tl0);
+        if (t0 + 1 < t1) tile_inputs(c1, la1, tl1);
+        int s = 0;
+        uint32_t ph = 0;
+        for (int f = t0; f < t1; f++) {
+            if (__any_sync(0xffffffffu, *fail != 0)) break;
+            const int u = c0.u;
+            float x[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) x[j] = la0[j];
+            const float tlv = tl0;
+            // advance the queue: c0 <- c1, c1 <- tile f + 2
+            c0 = c1;
+#pragma unroll
+            for (int j = 0; j < 4; j++) la0[j] = la1[j];
+            tl0 = tl1;
+            if (f + 1 < t1) {
+                c1 = step(c1, f + 1);
+                if (f + 2 < t1) tile_inputs(c1, la1, tl1);
+            }
+            // in-tile inclusive prefix of log_a: four 32-token warp scans
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += y;
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float y = __shfl_up_sync(0xffffffffu, x[j], off);
+                    if (lane >= off) x[j] += y;
+                }
             }
-            if (lane == 31) wt_sh[i & 1][w4] = incl;
-            // the four scaler warps meet here each tile and leave together on a failure
-            uint32_t stop;
-            asm volatile(
-                "{\n\t.reg .pred p, q;\n\t"
-                "setp.ne.b32 q, %1, 0;\n\t"
-                "bar.red.or.pred p, 1, 128, q;\n\t"
-                "selp.u32 %0, 1, 0, p;\n\t}"
-                : "=r"(stop)
-                : "r"(*fail)
-                : "memory");
-            if (stop) break;
             float before = 0.f, tot = 0.f;
 #pragma unroll
-            for (int w = 0; w < 4; w++) {
-                const float x = wt_sh[i & 1][w];
-                before += (w < w4) ? x : 0.f;
-                tot += x;
+            for (int j = 0; j < 4; j++) {
+                const float cj = __shfl_sync(0xffffffffu, x[j], 31);
+                before += (j < w4) ? cj : 0.f;
+                tot += cj;
             }
-            const float w = exp2f((tl + tot - (before + incl)) * kLog2e);
-            if (!warp_wait(&full_bar[s], (i / S) & 1)) {
+            const float incl = before + (w4 == 0 ? x[0] : w4 == 1 ? x[1] : w4 == 2 ? x[2] : x[3]);
+            // decay from token row to pos: the rest of the tile, then the tail
+            float w = exp2f((tlv + tot - incl) * kLog2e);
+            if (u >= Pt) {
+                // virtual tile: only the keys of its level, none past pos
+                const bool keep = row < n_last && fenwick_level(pos, base + row) == tile_level(u, Pt, tl.packed);
+                w = keep ? w : 0.f;
+            }
+            const int cs = s;
+            const uint32_t cph = ph;
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (!warp_wait(&full_bar[cs], cph)) {
                 if (lane == 0) fail_now();
-                continue;  // the next meeting sees the failure
+                break;
             }
-            uint8_t* vrow = smem + s * C::kStageBytes + C::kKBytes + row * 128;
+            uint8_t* vrow = smem + cs * C::kStageBytes + C::kKBytes + row * 128;
 #pragma unroll
             for (int p = 0; p < DV / 64; p++) {
 #pragma unroll
-                for (int c = 0; c < 8; c++) {
+                for (int c = half * 4; c < half * 4 + 4; c++) {
                     const uint32_t off = p * kPanelBytes + ((c ^ (row & 7)) << 4);
                     uint4* hp = reinterpret_cast<uint4*>(vrow + off);
                     uint4* lp = reinterpret_cast<uint4*>(vrow + C::kVBytes + off);
-                    const uint4 x = *hp;
-                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                    const uint4 xv = *hp;
+                    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
                     uint32_t hs[4], ls[4];
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
@@ -373,15 +400,19 @@ __global__ void __launch_bounds__(384, 1)
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&scaled_bar[s]);
+            if (lane == 0) mbar_arrive(&scaled_bar[cs]);
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 12) {
         const int quad = warp & 3;
         const int d = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         int run = 0;
+        Cursor c = cursor_at(t0);
         for (int f = t0; f < t1; f++) {
-            if (!((f == t1 - 1) || !same_run(f))) continue;
+            const Cursor nc = step(c, f);
+            const Cursor cur = c;
+            c = nc;
+            if (!cur.last_of_run) continue;
             const int buf = run & 1;
             if (*fail) break;
             if (!warp_wait(&acc_full[buf], (run >> 1) & 1)) {
@@ -389,15 +420,17 @@ __global__ void __launch_bounds__(384, 1)
                 break;
             }
             tc_fence_after();
-            const int bh = f / Pt, l = tile_level(f % Pt, Pt);
+            const int bh = cur.bh, l = cur.lvl;
             float4* dst = reinterpret_cast<float4*>(states + ((static_cast<size_t>(bh) * Lmax + l) * kDk + d) * DV);
 #pragma unroll
             for (int c0 = 0; c0 < DV; c0 += 32) {
-                float x[32];
-                tmem_ld32(tmem + lane_base + buf * DV + c0, x);
+                float x[32], y[32];
+                tmem_ld32(tmem + lane_base + buf * C::kAccCols + c0, x);
+                tmem_ld32(tmem + lane_base + buf * C::kAccCols + DV + c0, y);
 #pragma unroll
                 for (int j = 0; j < 8; j++)
-                    atomicAdd(dst + c0 / 4 + j, make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]));
+                    atomicAdd(dst + c0 / 4 + j, make_float4(x[4 * j] + y[4 * j], x[4 * j + 1] + y[4 * j + 1],
+                                                            x[4 * j + 2] + y[4 * j + 2], x[4 * j + 3] + y[4 * j + 3]));
             }
             tc_fence_before();
             __syncwarp();
@@ -424,21 +457,25 @@ cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a
     const int Pt = pos >> 7;
     float* g = static_cast<float*>(workspace);
     float* tail = g + static_cast<size_t>(BH) * Pt;
+    TailLevels tl;
+    tl.m = 1;  // level 0 at bits 0..3
+    tl.packed = 0;
+    for (int l = 1; l <= 7; l++)
+        if ((pos >> (l - 1)) & 1) tl.packed |= static_cast<uint32_t>(l) << (4 * tl.m++);
     if (Pt > 0) {
         state_tile_totals_kernel<<<dim3((Pt + 7) / 8, BH), 256, 0, stream>>>(log_a, g, T, Pt);
         note_launch(stream, "state_tile_totals");
     }
     {
-        const size_t smem = prep_smem_bytes<DV>(Pt);
-        cudaError_t e = cudaFuncSetAttribute(state_prep_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const size_t smem = static_cast<size_t>(Pt) * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(state_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        state_prep_kernel<DV><<<dim3(BH, 2), kPrepThreads, smem, stream>>>(
-            static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), log_a, g, tail, states, T,
-            Pt, Lmax);
+        state_prep_kernel<<<dim3(BH, 1 + Lmax), kPrepThreads, smem, stream>>>(log_a, g, tail, states, T, Pt, Lmax,
+                                                                             kDk * DV);
         note_launch(stream, "state_prep");
     }
-    if (Pt > 0) {
+    {
         CUtensorMap tk, tv;
         const uint64_t rows = static_cast<uint64_t>(BH) * T;
         if (!make_map(&tk, k, rows, kDk) || !make_map(&tv, v, rows, DV)) return cudaErrorInvalidValue;
@@ -451,10 +488,10 @@ cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a
             cudaGetLastError();
             sms = 152;
         }
-        const int total = BH * Pt;
+        const int total = BH * (Pt + tl.m);
         const int grid = total < sms ? total : sms;
         tc_state_kernel<DV><<<grid, C::kThreads, C::kBytes, stream>>>(tk, tv, log_a, tail, states, T, Pt, Lmax,
-                                                                       total, err);
+                                                                       total, tl, err);
         note_launch(stream, "tc_state");
     }
     return cudaGetLastError();
@@ -464,7 +501,10 @@ cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a
 
 bool tc_state_supported(int dtype, int dk, int dv, int B, int H, int T) {
     const int64_t Pt = (static_cast<int64_t>(T) - 1) >> 7;
+    // (the tensor maps want at least one 128-row box of rows)
     return dtype == 0 && dk == kDk && (dv == 64 || dv == 128) && Pt <= kMaxStateTiles &&
+           static_cast<int64_t>(B) * H * T >= kTile &&
+           static_cast<int64_t>(B) * H * (Pt + 8) < (int64_t(1) << 31) &&
            static_cast<int64_t>(B) * H * T < (int64_t(1) << 31);
 }
 

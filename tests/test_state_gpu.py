@@ -60,7 +60,9 @@ def held_levels(pos, Lmax):
     (1, 1, 300, 24, 40, "f32"),
     (1, 1, 1537, 64, 128, "bf16"),   # dk != 128: SIMT kernels
     # bf16, dk = 128: tensor-core kernels (full tiles) + the last tile's levels 0..7
-    (1, 1, 1, 128, 64, "bf16"),
+    (1, 1, 1, 128, 64, "bf16"),      # fewer than 128 rows in all: SIMT kernels
+    (2, 1, 64, 128, 64, "bf16"),     # only the tile of the last token
+    (1, 2, 100, 128, 128, "bf16"),
     (1, 2, 129, 128, 64, "bf16"),
     (2, 2, 1024, 128, 64, "bf16"),
     (2, 1, 1000, 128, 128, "bf16"),
