@@ -55,6 +55,8 @@ def _load():
             lib.lla_oracle_explicit_rows.restype = None
             lib.lla_oracle_decode_step.argtypes = [dp] * 6 + [i64p, dp] + [ctypes.c_int] * 5
             lib.lla_oracle_decode_step.restype = ctypes.c_int
+            lib.lla_oracle_backward.argtypes = [dp] * 11 + [ctypes.c_int] * 6
+            lib.lla_oracle_backward.restype = None
             _lib = lib
     return _lib
 
@@ -107,6 +109,22 @@ def explicit_rows(q, k, v, log_a, lam, b: int, h: int, rows) -> np.ndarray:
                                      0, T, dk, dv, L,
                                      rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), int(rows.size))
     return out
+
+
+def backward(q, k, v, log_a, lam, dout):
+    """Gradients of L = sum(dout * O) for the explicit form, fp64:
+    returns (dq, dk, dv, dlog_a, dlambda) with the shapes of (q, k, v, log_a, lambda)."""
+    q, k, v, log_a, lam, (B, H, T, dk, dv, L) = _check_forward(q, k, v, log_a, lam)
+    dout = _f64(dout)
+    assert dout.shape == (B, H, T, dv)
+    dq = np.zeros_like(q)
+    dk_ = np.zeros_like(k)
+    dv_ = np.zeros_like(v)
+    dla = np.zeros_like(log_a)
+    dlam = np.zeros_like(lam)
+    _load().lla_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(dout),
+                                _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dla), _ptr(dlam), B, H, T, dk, dv, L)
+    return dq, dk_, dv_, dla, dlam
 
 
 def recurrent(q, k, v, log_a, lam) -> np.ndarray:

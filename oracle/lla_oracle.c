@@ -133,6 +133,70 @@ void lla_oracle_explicit_rows(const double* q, const double* k, const double* v,
     }
 }
 
+/* Gradients of the explicit form for an upstream gradient dout = dL/dO, with
+ * the loss L = sum_t dout_t . o_t. For every pair s <= t write
+ *   D_ts = exp(sum_{r=s+1..t} log_a_r), l = l(t,s), lam = lambda_t^(l),
+ *   qk = q_t . k_s,  gv = dout_t . v_s;
+ * the pair adds lam * D_ts * qk * (dout_t . v_s) to L, so
+ *   dq_t += lam D gv k_s,   dk_s += lam D gv q_t,   dv_s += lam D qk dout_t,
+ *   dlambda_t^(l) += D qk gv,
+ * and every log_a_r with s < r <= t (the factors of D_ts) gets lam D qk gv.
+ * That last sum over pairs is accumulated as +E at r = s+1 and -E at r = t+1
+ * followed by a running sum over r, which adds E exactly to r in (s, t].
+ * Outputs are overwritten. */
+void lla_oracle_backward(const double* q, const double* k, const double* v,
+                         const double* log_a, const double* lambda, const double* dout,
+                         double* dq, double* dk, double* dv, double* dlog_a, double* dlambda,
+                         int B, int H, int T, int dkk, int dvv, int L)
+{
+    double* diff = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+    for (int bh = 0; bh < B * H; bh++) {
+        const double* qh = q + (size_t)bh * T * dkk;
+        const double* kh = k + (size_t)bh * T * dkk;
+        const double* vh = v + (size_t)bh * T * dvv;
+        const double* ah = log_a + (size_t)bh * T;
+        const double* lh = lambda + (size_t)bh * T * L;
+        const double* gh = dout + (size_t)bh * T * dvv;
+        double* dqh = dq + (size_t)bh * T * dkk;
+        double* dkh = dk + (size_t)bh * T * dkk;
+        double* dvh = dv + (size_t)bh * T * dvv;
+        double* dah = dlog_a + (size_t)bh * T;
+        double* dlh = dlambda + (size_t)bh * T * L;
+        memset(dqh, 0, sizeof(double) * (size_t)T * dkk);
+        memset(dkh, 0, sizeof(double) * (size_t)T * dkk);
+        memset(dvh, 0, sizeof(double) * (size_t)T * dvv);
+        memset(dlh, 0, sizeof(double) * (size_t)T * L);
+        for (int r = 0; r <= T; r++) diff[r] = 0.0;
+        for (int t = 0; t < T; t++) {
+            double decay_exp = 0.0; /* sum of log_a over (s, t] */
+            for (int s = t; s >= 0; s--) {
+                int l = lla_oracle_level(t, s);
+                double qk = 0.0, gv = 0.0;
+                for (int i = 0; i < dkk; i++) qk += qh[(size_t)t * dkk + i] * kh[(size_t)s * dkk + i];
+                for (int j = 0; j < dvv; j++) gv += gh[(size_t)t * dvv + j] * vh[(size_t)s * dvv + j];
+                double D = exp(decay_exp);
+                double lam = lh[(size_t)t * L + l];
+                for (int i = 0; i < dkk; i++) {
+                    dqh[(size_t)t * dkk + i] += lam * D * gv * kh[(size_t)s * dkk + i];
+                    dkh[(size_t)s * dkk + i] += lam * D * gv * qh[(size_t)t * dkk + i];
+                }
+                for (int j = 0; j < dvv; j++) dvh[(size_t)s * dvv + j] += lam * D * qk * gh[(size_t)t * dvv + j];
+                dlh[(size_t)t * L + l] += D * qk * gv;
+                double E = lam * D * qk * gv;
+                diff[s + 1] += E;
+                diff[t + 1] -= E;
+                decay_exp += ah[s];
+            }
+        }
+        double run = 0.0;
+        for (int r = 0; r < T; r++) {
+            run += diff[r];
+            dah[r] = run;
+        }
+    }
+    free(diff);
+}
+
 /* Lowest set bit position of t > 0. */
 static int trailing_zeros(int64_t t)
 {
