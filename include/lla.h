@@ -179,6 +179,31 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
                       int dk, int dv, int Lmax, void* stream, int dtype);
 
 /*
+ * Backward of lla_forward: gradients of L = sum over all elements of dout * out.
+ * ("Log-Linear Attention", pt §2 "Mascara Hierarquica" / fr §2 "Matrice de
+ * Masque Hierarchique" define the operator differentiated here; the pages name
+ * the backward through lambda as needing its own kernels.)
+ *
+ *   q, k, v, log_a, lambda   the forward's inputs (same shapes, dtype, chunk rules)
+ *   dout     [B,H,T,dv]  dtype   upstream gradient dL/dout
+ *   dq, dk   [B,H,T,dk]  dtype   written
+ *   dv       [B,H,T,dv]  dtype   written
+ *   dlog_a   [B,H,T]     fp32    written
+ *   dlambda  [B,H,T,L]   fp32    written (0 for levels with no key at that query)
+ * The outputs must not overlap any input or each other. The forward's
+ * intermediate states are recomputed, so no forward workspace is kept between
+ * the calls. The chunk argument follows lla_forward; chunks above 64 are run as
+ * 64 (same operator, different rounding order). Arithmetic is fp32 on CUDA
+ * cores. Workspace comes from the same library-owned stream-ordered pool as
+ * lla_forward. Errors: LLA_ERR_INVALID_ARG / LLA_ERR_UNSUPPORTED before any
+ * launch, LLA_ERR_NOMEM if the pool cannot grow, LLA_ERR_CUDA on launch
+ * failure.
+ */
+int lla_backward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                 const void* dout, void* dq, void* dk, void* dv, float* dlog_a, float* dlambda, int B, int H,
+                 int T, int dk_, int dv_, int chunk, void* stream, int dtype);
+
+/*
  * Reads and clears the device error word of the current device after
  * synchronising `stream`: LLA_OK if no kernel recorded a fault since the last
  * read, LLA_ERR_DEVICE for rejected device-side input, LLA_ERR_TIMEOUT for a

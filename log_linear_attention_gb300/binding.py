@@ -63,6 +63,8 @@ def load() -> ctypes.CDLL:
             lib.lla_prefill_state.restype = i
             lib.lla_device_error.argtypes = [vp]
             lib.lla_device_error.restype = i
+            lib.lla_backward.argtypes = [vp, vp, vp, fp, fp, vp, vp, vp, vp, fp, fp] + [i] * 6 + [vp, i]
+            lib.lla_backward.restype = i
             _lib = lib
     return _lib
 
@@ -235,6 +237,37 @@ def prefill_state(k, v, log_a, states, stream=None):
     _call(load().lla_prefill_state(k.data_ptr(), v.data_ptr(), log_a.data_ptr(), states.data_ptr(), B, H, T, dk, dv,
                                    Lmax, _stream_handle(stream), _dtype_code(k)), "lla_prefill_state")
     return states
+
+
+def backward(q, k, v, log_a, lam, dout, chunk: int, stream=None):
+    """lla_backward: gradients of sum(dout * forward(q, k, v, log_a, lam)).
+
+    Device tensors with the shapes and dtypes of lla_forward's inputs; dout like the output.
+    Returns (dq, dk, dv, dlog_a, dlambda): dq/dk/dv in q's dtype, dlog_a/dlambda fp32."""
+    torch = _torch()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda"), (dout, "dout")):
+        _check(t_, n, q.device)
+    if k.dtype != q.dtype or v.dtype != q.dtype or dout.dtype != q.dtype:
+        raise TypeError("q, k, v and dout must share one dtype")
+    if log_a.dtype != torch.float32 or lam.dtype != torch.float32:
+        raise TypeError("log_a and lambda must be float32")
+    if (k.shape != q.shape or v.shape[:3] != (B, H, T) or dout.shape != v.shape or log_a.shape != (B, H, T)
+            or lam.shape[:3] != (B, H, T)):
+        raise ValueError("shape mismatch between q, k, v, dout, log_a and lambda")
+    if lam.shape[3] != num_levels(T):
+        raise ValueError(f"lambda needs {num_levels(T)} levels for T={T}, got {lam.shape[3]}")
+    dq = torch.empty_like(q)
+    dk_ = torch.empty_like(k)
+    dv_ = torch.empty_like(v)
+    dla = torch.empty_like(log_a)
+    dlam = torch.empty_like(lam)
+    _call(load().lla_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(),
+                              dout.data_ptr(), dq.data_ptr(), dk_.data_ptr(), dv_.data_ptr(), dla.data_ptr(),
+                              dlam.data_ptr(), B, H, T, dk, dv, chunk, _stream_handle(stream), _dtype_code(q)),
+          "lla_backward")
+    return dq, dk_, dv_, dla, dlam
 
 
 def device_error(stream=None) -> int:

@@ -265,6 +265,31 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }
 
+int lla_backward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                 const void* dout, void* dq, void* dk, void* dv, float* dlog_a, float* dlambda, int B, int H, int T,
+                 int dk_, int dv_, int chunk, void* stream, int dtype) {
+    int st = validate_forward(q, k, v, log_a, lambda, dout, B, H, T, dk_, dv_, chunk, dtype);
+    if (st != LLA_OK) return st;
+    if (!dq || !dk || !dv || !dlog_a || !dlambda) return LLA_ERR_INVALID_ARG;
+    if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dlog_a) || !aligned16(dlambda))
+        return LLA_ERR_INVALID_ARG;
+    lla::BwdPlan bp;
+    if (!lla::make_bwd_plan(B, H, T, dk_, dv_, chunk, &bp)) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return LLA_ERR_CUDA;
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bp.total_bytes, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LLA_ERR_NOMEM;
+    }
+    cudaError_t e = lla::simt_backward(bp, dtype, q, k, v, log_a, lambda, dout, dq, dk, dv, dlog_a, dlambda, ws, s);
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
+}
+
 int lla_device_error(void* stream) {
     const int dev = current_device();
     if (dev < 0) return LLA_ERR_CUDA;

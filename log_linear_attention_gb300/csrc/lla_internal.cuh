@@ -96,6 +96,23 @@ cudaError_t simt_forward(const SimtPlan& plan, int dtype, const void* q, const v
                          cudaStream_t stream);
 cudaError_t prefill_state(int dtype, const void* k, const void* v, const float* log_a, float* states, int B, int H,
                           int T, int dk, int dv, int Lmax, void* workspace, cudaStream_t stream);
+// The first half of the SIMT forward: chunk totals g and every fp32 pyramid node, laid out as
+// SimtPlan describes at the start of `workspace`.
+cudaError_t simt_nodes(const SimtPlan& plan, int dtype, const void* k, const void* v, const float* log_a,
+                       void* workspace, cudaStream_t stream);
+
+// Backward (lla_bwd.cu): plan and launcher.
+struct BwdPlan {
+    SimtPlan fw;             // forward nodes recomputed with the backward's chunk
+    int n_read;              // read nodes (p, m even, (m + 1) 2^p < N), all levels
+    int read_off[32];        // first read node of level p
+    int max_pieces;          // token pieces of the largest query block
+    size_t dnodes_bytes, dcum_bytes, total_bytes;
+};
+bool make_bwd_plan(int B, int H, int T, int dk, int dv, int chunk, BwdPlan* plan);
+cudaError_t simt_backward(const BwdPlan& plan, int dtype, const void* q, const void* k, const void* v,
+                          const float* log_a, const float* lambda, const void* dout, void* dq, void* dk, void* dv,
+                          float* dlog_a, float* dlambda, void* workspace, cudaStream_t stream);
 cudaError_t decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
                         const float* lambda, float* states, const int64_t* t, void* out, int B, int H,
                         int dk, int dv, int Lmax, int* err, cudaStream_t stream);

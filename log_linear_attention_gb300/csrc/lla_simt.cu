@@ -600,6 +600,27 @@ cudaError_t prefill_state_t(const void* k, const void* v, const float* log_a, fl
     return cudaGetLastError();
 }
 
+// Chunk totals g and the fp32 Fenwick pyramid of forward nodes (the first half of the forward).
+template <typename T>
+cudaError_t simt_nodes_t(const SimtPlan& pl, const T* k, const T* v, const float* log_a, void* workspace,
+                         cudaStream_t stream) {
+    const int BH = pl.B * pl.H;
+    float* g = reinterpret_cast<float*>(workspace);
+    float* nodes = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + pl.g_bytes);
+    LevelOffsets lo;
+    for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
+    chunk_totals_kernel<<<dim3((pl.N + 7) / 8, BH), kThreads, 0, stream>>>(log_a, g, pl.T, pl.chunk, pl.N);
+    const int msz = pl.dk * pl.dv;
+    if (pl.P > 0)
+        chunk_state_kernel<T><<<dim3(pl.N, BH, (msz + 2047) / 2048), kThreads, 0, stream>>>(k, v, log_a, nodes, pl.T,
+                                                                                           pl.dk, pl.dv, pl.chunk,
+                                                                                           pl.node_count);
+    if (pl.P > 1)
+        pyramid_kernel<<<dim3((msz + kThreads - 1) / kThreads, BH), kThreads, pl.node_count * sizeof(float), stream>>>(
+            nodes, g, pl.N, pl.P, pl.node_count, msz, lo);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t simt_forward_t(const SimtPlan& pl, const T* q, const T* k, const T* v, const float* log_a,
                            const float* lambda, T* out, void* workspace, cudaStream_t stream) {
@@ -692,6 +713,15 @@ cudaError_t simt_forward(const SimtPlan& pl, int dtype, const void* q, const voi
     return simt_forward_t<__nv_bfloat16>(pl, static_cast<const __nv_bfloat16*>(q),
                                          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
                                          log_a, lambda, static_cast<__nv_bfloat16*>(out), workspace, stream);
+}
+
+cudaError_t simt_nodes(const SimtPlan& pl, int dtype, const void* k, const void* v, const float* log_a,
+                       void* workspace, cudaStream_t stream) {
+    if (dtype == 1)
+        return simt_nodes_t<float>(pl, static_cast<const float*>(k), static_cast<const float*>(v), log_a, workspace,
+                                   stream);
+    return simt_nodes_t<__nv_bfloat16>(pl, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+                                       log_a, workspace, stream);
 }
 
 cudaError_t prefill_state(int dtype, const void* k, const void* v, const float* log_a, float* states, int B, int H,

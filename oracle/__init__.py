@@ -57,6 +57,8 @@ def _load():
             lib.lla_oracle_decode_step.restype = ctypes.c_int
             lib.lla_oracle_backward.argtypes = [dp] * 11 + [ctypes.c_int] * 6
             lib.lla_oracle_backward.restype = None
+            lib.lla_oracle_backward_rows.argtypes = [dp] * 6 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int] + [dp] * 5
+            lib.lla_oracle_backward_rows.restype = None
             _lib = lib
     return _lib
 
@@ -125,6 +127,22 @@ def backward(q, k, v, log_a, lam, dout):
     _load().lla_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(dout),
                                 _ptr(dq), _ptr(dk_), _ptr(dv_), _ptr(dla), _ptr(dlam), B, H, T, dk, dv, L)
     return dq, dk_, dv_, dla, dlam
+
+
+def backward_rows(q, k, v, log_a, lam, dout, b: int, h: int, rows):
+    """Backward at chosen positions x of head (b, h): returns (dq [n,dk], dk [n,dk], dv [n,dv],
+    dlambda [n,L], dcum [n]) where dcum_x = dlog_a_x - dlog_a_{x+1} (dlog_a_T = 0)."""
+    sl = (slice(b, b + 1), slice(h, h + 1))
+    q, k, v, log_a, lam, (_, _, T, dk, dv, L) = _check_forward(q[sl], k[sl], v[sl], log_a[sl], lam[sl])
+    dout = _f64(dout[sl])
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    assert rows.ndim == 1 and (rows >= 0).all() and (rows < T).all()
+    n = rows.size
+    out = [np.zeros((n, dk)), np.zeros((n, dk)), np.zeros((n, dv)), np.zeros((n, L)), np.zeros(n)]
+    _load().lla_oracle_backward_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(dout), 0, T, dk, dv, L,
+                                     rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), int(n),
+                                     *[_ptr(o) for o in out])
+    return tuple(out)
 
 
 def recurrent(q, k, v, log_a, lam) -> np.ndarray:

@@ -197,6 +197,68 @@ void lla_oracle_backward(const double* q, const double* k, const double* v,
     free(diff);
 }
 
+/* The backward restricted to chosen positions x of one head (bh), for spot
+ * checks of long sequences. For each x in rows[0..nrows):
+ *   dq_x, dlambda_x  from the pairs (x, s), s <= x   (x as the query),
+ *   dk_x, dv_x       from the pairs (t, x), t >= x   (x as the key),
+ *   dcum_x = sum_s E_xs - sum_t E_tx, the derivative with respect to
+ *            cum_x = sum_{r<=x} log_a_r, so that dlog_a_x - dlog_a_{x+1} = dcum_x,
+ * with the same per-pair terms as lla_oracle_backward. Outputs are overwritten:
+ * dq [nrows][dk], dk [nrows][dk], dv [nrows][dv], dlambda [nrows][L], dcum [nrows]. */
+void lla_oracle_backward_rows(const double* q, const double* k, const double* v,
+                              const double* log_a, const double* lambda, const double* dout,
+                              int bh, int T, int dkk, int dvv, int L, const int64_t* rows, int nrows,
+                              double* dq, double* dk, double* dv, double* dlambda, double* dcum)
+{
+    const double* qh = q + (size_t)bh * T * dkk;
+    const double* kh = k + (size_t)bh * T * dkk;
+    const double* vh = v + (size_t)bh * T * dvv;
+    const double* ah = log_a + (size_t)bh * T;
+    const double* lh = lambda + (size_t)bh * T * L;
+    const double* gh = dout + (size_t)bh * T * dvv;
+    for (int r = 0; r < nrows; r++) {
+        int64_t x = rows[r];
+        double* dqr = dq + (size_t)r * dkk;
+        double* dkr = dk + (size_t)r * dkk;
+        double* dvr = dv + (size_t)r * dvv;
+        double* dlr = dlambda + (size_t)r * L;
+        memset(dqr, 0, sizeof(double) * dkk);
+        memset(dkr, 0, sizeof(double) * dkk);
+        memset(dvr, 0, sizeof(double) * dvv);
+        memset(dlr, 0, sizeof(double) * L);
+        double dc = 0.0;
+        /* x as the query: pairs (x, s) */
+        double decay_exp = 0.0;
+        for (int64_t s = x; s >= 0; s--) {
+            int l = lla_oracle_level(x, s);
+            double qk = 0.0, gv = 0.0;
+            for (int i = 0; i < dkk; i++) qk += qh[(size_t)x * dkk + i] * kh[(size_t)s * dkk + i];
+            for (int j = 0; j < dvv; j++) gv += gh[(size_t)x * dvv + j] * vh[(size_t)s * dvv + j];
+            double D = exp(decay_exp);
+            double lam = lh[(size_t)x * L + l];
+            for (int i = 0; i < dkk; i++) dqr[i] += lam * D * gv * kh[(size_t)s * dkk + i];
+            dlr[l] += D * qk * gv;
+            dc += lam * D * qk * gv;
+            decay_exp += ah[s];
+        }
+        /* x as the key: pairs (t, x) */
+        decay_exp = 0.0; /* sum of log_a over (x, t] */
+        for (int64_t t = x; t < T; t++) {
+            if (t > x) decay_exp += ah[t];
+            int l = lla_oracle_level(t, x);
+            double qk = 0.0, gv = 0.0;
+            for (int i = 0; i < dkk; i++) qk += qh[(size_t)t * dkk + i] * kh[(size_t)x * dkk + i];
+            for (int j = 0; j < dvv; j++) gv += gh[(size_t)t * dvv + j] * vh[(size_t)x * dvv + j];
+            double D = exp(decay_exp);
+            double lam = lh[(size_t)t * L + l];
+            for (int i = 0; i < dkk; i++) dkr[i] += lam * D * gv * qh[(size_t)t * dkk + i];
+            for (int j = 0; j < dvv; j++) dvr[j] += lam * D * qk * gh[(size_t)t * dvv + j];
+            dc -= lam * D * qk * gv;
+        }
+        dcum[r] = dc;
+    }
+}
+
 /* Lowest set bit position of t > 0. */
 static int trailing_zeros(int64_t t)
 {

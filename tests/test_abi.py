@@ -94,6 +94,22 @@ def test_decode_rejects_bad_arguments(lib, args, expect):
     assert st == expect
 
 
+@pytest.mark.parametrize("args,expect", [
+    (dict(dq=None), binding.LLA_ERR_INVALID_ARG),
+    (dict(dlam=A + 4), binding.LLA_ERR_INVALID_ARG),
+    (dict(dout=None), binding.LLA_ERR_INVALID_ARG),
+    (dict(chunk=24), binding.LLA_ERR_INVALID_ARG),
+    (dict(T=80, chunk=64), binding.LLA_ERR_INVALID_ARG),
+    (dict(dv=129), binding.LLA_ERR_UNSUPPORTED),
+])
+def test_backward_rejects_bad_arguments(lib, args, expect):
+    a = dict(dq=A, dlam=A, dout=A, T=64, dk=16, dv=16, chunk=16)
+    a.update(args)
+    st = lib.lla_backward(A, A, A, A, A, a["dout"], a["dq"], A, A, A, a["dlam"], 1, 1, a["T"], a["dk"], a["dv"],
+                          a["chunk"], None, 1)
+    assert st == expect
+
+
 def test_product_package_never_imports_the_oracle():
     pkg = os.path.join(ROOT, "log_linear_attention_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -98,3 +98,21 @@ def test_backward_linear_in_dout():
     g2 = oracle.backward(q, k, v, log_a, lam, -2.5 * dout)
     for a, b in zip(g1, g2):
         np.testing.assert_allclose(b, -2.5 * a, rtol=1e-12, atol=1e-14)
+
+
+def test_backward_rows_match_full_backward():
+    """The per-position backward (used for spot checks of long sequences) against the
+    full backward: dq/dk/dv/dlambda rows, and dcum_x = dlog_a_x - dlog_a_{x+1}."""
+    rng = np.random.default_rng(6)
+    B, H, T, dk, dv = 2, 2, 70, 5, 4
+    q, k, v, log_a, lam, dout = _problem(rng, B, H, T, dk, dv)
+    dq, dk_, dv_, dla, dlam = oracle.backward(q, k, v, log_a, lam, dout)
+    rows = [0, 1, 31, 32, 63, 69]
+    for b, h in ((0, 1), (1, 0)):
+        rq, rk, rv, rl, rc = oracle.backward_rows(q, k, v, log_a, lam, dout, b, h, rows)
+        np.testing.assert_allclose(rq, dq[b, h, rows], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(rk, dk_[b, h, rows], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(rv, dv_[b, h, rows], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(rl, dlam[b, h, rows], rtol=1e-11, atol=1e-12)
+        nxt = np.append(dla[b, h], 0.0)
+        np.testing.assert_allclose(rc, nxt[rows] - nxt[np.array(rows) + 1], rtol=1e-9, atol=1e-10)
