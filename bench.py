@@ -85,6 +85,25 @@ def kernel_work(name: str, cfg: inputs.PrefillConfig) -> dict:
     return dict(bound="hbm", flops=0, bytes=a_b)
 
 
+def backward_work(cfg: inputs.PrefillConfig) -> dict:
+    """Algorithmic work of one lla_backward call (causal pairs and nonempty levels only):
+    in-chunk pairs need q.k, dO.v, and the dq, dk, dv products (3 dk + 2 dv multiply-adds);
+    the forward nodes are rebuilt (state); every level read appears twice (B dO for dq and
+    the node gradient q dO^T); the key side applies C_i twice (dk and dv)."""
+    w = prefill_work(cfg)
+    BH = cfg.B * cfg.H
+    C = min(cfg.chunk, 64)
+    N = cfg.T // C
+    intra = BH * N * C * (C + 1) // 2 * 2 * (3 * cfg.dk + 2 * cfg.dv)
+    state = BH * N * 2 * C * cfg.dk * cfg.dv
+    level = BH * sum(bin(j).count("1") for j in range(N)) * 2 * C * cfg.dk * cfg.dv
+    keyside = 2 * state
+    esz = 2 if cfg.dtype == "bf16" else 4
+    nbytes = (w["in_bytes"] + BH * cfg.T * cfg.dv * esz  # inputs + dout
+              + BH * cfg.T * (2 * cfg.dk + cfg.dv) * esz + BH * cfg.T * 4 * (1 + cfg.L))  # gradients
+    return dict(flops=intra + state + 2 * level + keyside, bytes=nbytes)
+
+
 def decode_bytes(t: np.ndarray, H: int, dk: int, dv: int, Lmax: int, esz: int = 2) -> int:
     """Bytes one decode step must move: every nonempty state level read once
     (popcount(t-1) + 1 of them) and every level held after the step written once
@@ -390,6 +409,16 @@ def run_lla(args, cfg):
     host = [h.pin_memory() for h in host]
     dq, dk_, dv_, da, dl = (h.to(dev) for h in host)
     out = torch.empty((cfg.B, cfg.H, cfg.T, cfg.dv), dtype=torch.bfloat16, device=dev)
+    if args.mode == "backward":
+        # backward launches only (a short target for profilers)
+        gout = torch.randn((cfg.B, cfg.H, cfg.T, cfg.dv), device=dev).to(torch.bfloat16)
+        for _ in range(max(args.warmup, 3)):
+            binding.backward(dq, dk_, dv_, da, dl, gout, cfg.chunk)
+        b_ms = cuda_time(lambda: binding.backward(dq, dk_, dv_, da, dl, gout, cfg.chunk), args.steps, stream) / args.steps
+        assert binding.device_error() == 0
+        if rank == 0:
+            print(json.dumps({"mode": "backward", "config": cfg.name, "ms": b_ms, "steps": args.steps}))
+        return 0
     if args.mode == "handoff":
         # prefill -> decode hand-off launches only (a short target for profilers)
         hstates = torch.empty((cfg.B, cfg.H, inputs.num_levels(cfg.T + 1), cfg.dk, cfg.dv), dtype=torch.float32,
@@ -487,6 +516,19 @@ def run_lla(args, cfg):
     n_h = max(3, min(args.steps, 20))
     h_ms = cuda_time(hstep, n_h, stream) / n_h
     held = 1 + bin(cfg.T - 1).count("1")
+
+    # ---- backward: gradients of sum(dout * out) for the same problem
+    gout = torch.randn((cfg.B, cfg.H, cfg.T, cfg.dv), device=dev).to(torch.bfloat16)
+
+    def bstep():
+        binding.backward(dq, dk_, dv_, da, dl, gout, cfg.chunk)
+
+    for _ in range(3):
+        bstep()
+    n_b = max(3, min(args.steps, 10))
+    b_ms = cuda_time(bstep, n_b, stream) / n_b
+    assert binding.device_error() == 0
+    bw = backward_work(cfg)
     h_bytes = (cfg.B * cfg.H * cfg.T * ((cfg.dk + cfg.dv) * 2 + 4) + cfg.B * cfg.H * held * cfg.dk * cfg.dv * 4)
 
     line = None
@@ -515,6 +557,12 @@ def run_lla(args, cfg):
                         "ms": h_ms, "gbs": h_bytes / (h_ms / 1e3) / 1e9,
                         "frac_of_hbm": h_bytes / (h_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                         "bytes": h_bytes, "convention": "k, v, log_a read once; held state slots written once"},
+            "backward": {"workload": f"lla_backward of the same {cfg.name} problem (dq, dk, dv, dlog_a, dlambda)",
+                         "ms": b_ms, "tokens_per_s": cfg.tokens / (b_ms / 1e3),
+                         "tflops": bw["flops"] / (b_ms / 1e3) / 1e12,
+                         "algorithmic_gflop": bw["flops"] / 1e9, "bound": "alu",
+                         "frac_of_alu_peak": bw["flops"] / (b_ms / 1e3) / 1e12 / ALU_F32_TFLOPS,
+                         "peak_source": "derived: 152 SM x 128 FMA x 2.07 GHz"},
             "e2e": {"value": ws * cfg.tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": {"value": cpu_val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -541,8 +589,8 @@ def main():
     ap.add_argument("--config", default="headline", choices=sorted(inputs.PREFILL_CONFIGS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--mode", choices=["all", "prefill", "decode", "handoff"], default="all",
-                    help="prefill / decode / handoff: run only that workload's launches (profiling targets)")
+    ap.add_argument("--mode", choices=["all", "prefill", "decode", "handoff", "backward"], default="all",
+                    help="prefill / decode / handoff / backward: run only that workload's launches (profiling targets)")
     args = ap.parse_args()
     cfg = inputs.PREFILL_CONFIGS[args.config]
     if args.impl == "reference":
