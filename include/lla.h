@@ -192,10 +192,13 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
  *   dlambda  [B,H,T,L]   fp32    written (0 for levels with no key at that query)
  * The outputs must not overlap any input or each other. The forward's
  * intermediate states are recomputed, so no forward workspace is kept between
- * the calls. The chunk argument follows lla_forward; chunks above 64 are run as
- * 64 (same operator, different rounding order). Arithmetic is fp32 on CUDA
- * cores. Workspace comes from the same library-owned stream-ordered pool as
- * lla_forward. Errors: LLA_ERR_INVALID_ARG / LLA_ERR_UNSUPPORTED before any
+ * the calls. The chunk argument follows lla_forward. bf16 inputs with dk = 128,
+ * dv = 64 and T % 128 == 0 run on tensor cores (128-token tiles, fp32
+ * accumulation, bf16 operands); every other shape runs fp32 arithmetic on CUDA
+ * cores with chunks of at most 64 (chunk 128 runs as 64: same operator,
+ * different rounding order). Workspace comes from the same library-owned
+ * stream-ordered pool as lla_forward. A kernel's bounded wait that runs out is
+ * reported by lla_device_error as LLA_ERR_TIMEOUT. Errors: LLA_ERR_INVALID_ARG / LLA_ERR_UNSUPPORTED before any
  * launch, LLA_ERR_NOMEM if the pool cannot grow, LLA_ERR_CUDA on launch
  * failure.
  */

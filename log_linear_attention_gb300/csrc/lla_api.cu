@@ -273,19 +273,26 @@ int lla_backward(const void* q, const void* k, const void* v, const float* log_a
     if (!dq || !dk || !dv || !dlog_a || !dlambda) return LLA_ERR_INVALID_ARG;
     if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dlog_a) || !aligned16(dlambda))
         return LLA_ERR_INVALID_ARG;
+    lla::TcPlan tp;
     lla::BwdPlan bp;
-    if (!lla::make_bwd_plan(B, H, T, dk_, dv_, chunk, &bp)) return LLA_ERR_UNSUPPORTED;
+    const bool tc = lla::tc_bwd_supported(dtype, dk_, dv_, T) && lla::make_tc_plan(B, H, T, dk_, dv_, &tp);
+    if (!tc && !lla::make_bwd_plan(B, H, T, dk_, dv_, chunk, &bp)) return LLA_ERR_UNSUPPORTED;
     const int dev = current_device();
     if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaMemPool_t pool = workspace_pool(dev);
     if (!pool) return LLA_ERR_CUDA;
     void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, bp.total_bytes, pool, s) != cudaSuccess) {
+    const size_t bytes = tc ? lla::tc_bwd_workspace_bytes(tp) : bp.total_bytes;
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, s) != cudaSuccess) {
         cudaGetLastError();
         return LLA_ERR_NOMEM;
     }
-    cudaError_t e = lla::simt_backward(bp, dtype, q, k, v, log_a, lambda, dout, dq, dk, dv, dlog_a, dlambda, ws, s);
+    cudaError_t e = tc ? lla::tc_backward(tp, q, k, v, log_a, lambda, dout, dq, dk, dv, dlog_a, dlambda, ws, err, s)
+                       : lla::simt_backward(bp, dtype, q, k, v, log_a, lambda, dout, dq, dk, dv, dlog_a, dlambda, ws,
+                                            s);
     const cudaError_t f = cudaFreeAsync(ws, s);
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }

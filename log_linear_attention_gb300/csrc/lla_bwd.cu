@@ -636,6 +636,12 @@ cudaError_t backward_t(const BwdPlan& pl, const T* q, const T* k, const T* v, co
 
 }  // namespace
 
+cudaError_t bwd_dloga(const float* dcum, float* dlog_a, int BH, int T, cudaStream_t stream) {
+    bwd_dloga_kernel<<<BH, kThreads, 0, stream>>>(dcum, dlog_a, T);
+    note_launch(stream, "bwd_dloga");
+    return cudaGetLastError();
+}
+
 bool make_bwd_plan(int B, int H, int T, int dk, int dv, int chunk, BwdPlan* pl) {
     const int C = chunk < kMaxChunk ? chunk : kMaxChunk;
     if (T % C != 0) return false;

@@ -83,6 +83,9 @@ bool tc_supported(int dtype, int dk, int dv, int T);
 bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* plan);
 cudaError_t tc_forward(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
                        const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream);
+// The node stage of tc_forward only (tc_nodes + tc_merge), for the backward.
+cudaError_t tc_nodes_only(const TcPlan& plan, const void* k, const void* v, const float* log_a, void* workspace,
+                          int* err, cudaStream_t stream);
 
 // Tensor-core state set after a prefill (lla_tc_state.cu): bf16, dk = 128, dv in {64, 128}.
 bool tc_state_supported(int dtype, int dk, int dv, int B, int H, int T);
@@ -113,6 +116,15 @@ bool make_bwd_plan(int B, int H, int T, int dk, int dv, int chunk, BwdPlan* plan
 cudaError_t simt_backward(const BwdPlan& plan, int dtype, const void* q, const void* k, const void* v,
                           const float* log_a, const float* lambda, const void* dout, void* dq, void* dk, void* dv,
                           float* dlog_a, float* dlambda, void* workspace, cudaStream_t stream);
+// dlog_a_r = sum_{t >= r} dcum_t per head (lla_bwd.cu).
+cudaError_t bwd_dloga(const float* dcum, float* dlog_a, int BH, int T, cudaStream_t stream);
+
+// Tensor-core backward (lla_tc_bwd.cu): bf16, dk = 128, dv = 64, T % 128 == 0.
+bool tc_bwd_supported(int dtype, int dk, int dv, int T);
+size_t tc_bwd_workspace_bytes(const TcPlan& plan);
+cudaError_t tc_backward(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
+                        const float* lambda, const void* dout, void* dq, void* dk, void* dv, float* dlog_a,
+                        float* dlambda, void* workspace, int* err, cudaStream_t stream);
 cudaError_t decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
                         const float* lambda, float* states, const int64_t* t, void* out, int B, int H,
                         int dk, int dv, int Lmax, int* err, cudaStream_t stream);

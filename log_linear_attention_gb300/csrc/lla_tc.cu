@@ -385,7 +385,6 @@ __global__ void __launch_bounds__(256)
 template <int DV>
 struct OutCfg {
     static constexpr int kStages = DV == 64 ? 2 : 1;
-    static constexpr int kAhead = kStages - 1;
     static constexpr int kQ = 0;
     static constexpr int kK = 2 * kPanelBytes;  // K tile, then P of the same tile
     static constexpr int kV = 4 * kPanelBytes;
@@ -910,9 +909,11 @@ int choose_q(int BH, int NT, int dv) {
 }
 
 
+// tc_nodes + tc_merge: tile decays, the Fenwick nodes that are read (bf16), the per-token
+// decay tables and the per-tile level decay table.
 template <int DV>
-cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
-                          const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream) {
+cudaError_t tc_node_stage(const TcPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv, const float* log_a,
+                          void* workspace, int* err, cudaStream_t stream) {
     const int BH = pl.B * pl.H;
     const int qlog = pl.q;
     const int seg_tiles = 1 << qlog;
@@ -927,17 +928,6 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
     int* tile_counter = reinterpret_cast<int*>(ws + pl.total_bytes - pl.ctr_bytes);
     LevelOffsets lo;
     for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
-    const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
-
-    CUtensorMap tq, tk, tv, tn;
-    if (!make_map(&tq, q, rows, kDk) || !make_map(&tk, k, rows, kDk) || !make_map(&tv, v, rows, DV))
-        return cudaErrorInvalidValue;
-    const bool have_nodes = pl.node_count > 0;
-    if (have_nodes && !make_map(&tn, nodes, static_cast<uint64_t>(BH) * pl.node_count * kDk, DV))
-        return cudaErrorInvalidValue;
-    if (!have_nodes) tn = tv;  // never read when no tile has an earlier tile
-
-    // nodes and tile decays
     {
         const int smem = NodesSmem<DV>::kBytes;
         auto launch = [&](auto kern) -> cudaError_t {
@@ -963,6 +953,36 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
         tc_merge_kernel<<<dim3(msz / 1024 + 1, n_above > 0 ? n_above : 1, BH), 256, pl.NT * sizeof(float), stream>>>(
             seg_tot, g_tiles, nodes, dtab, tile_counter, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
         note_launch(stream, "tc_merge");
+    }
+    return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
+                          const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream,
+                          bool nodes_only = false) {
+    const int BH = pl.B * pl.H;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    __nv_bfloat16* nodes = reinterpret_cast<__nv_bfloat16*>(ws + pl.g_bytes);
+    float* dtab = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes + pl.seg_bytes);
+    float* tok_cl2 = reinterpret_cast<float*>(ws + pl.g_bytes + pl.nodes_bytes + pl.seg_bytes + pl.dtab_bytes);
+    float* tok_colw = tok_cl2 + static_cast<size_t>(BH) * pl.T;
+    int* tile_counter = reinterpret_cast<int*>(ws + pl.total_bytes - pl.ctr_bytes);
+    LevelOffsets lo;
+    for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
+    const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
+
+    CUtensorMap tq, tk, tv, tn;
+    if (!make_map(&tq, q, rows, kDk) || !make_map(&tk, k, rows, kDk) || !make_map(&tv, v, rows, DV))
+        return cudaErrorInvalidValue;
+    const bool have_nodes = pl.node_count > 0;
+    if (have_nodes && !make_map(&tn, nodes, static_cast<uint64_t>(BH) * pl.node_count * kDk, DV))
+        return cudaErrorInvalidValue;
+    if (!have_nodes) tn = tv;  // never read when no tile has an earlier tile
+
+    {
+        cudaError_t e = tc_node_stage<DV>(pl, tk, tv, log_a, workspace, err, stream);
+        if (e != cudaSuccess || nodes_only) return e;
     }
     {
         const int smem = OutCfg<DV>::kBytes;
@@ -1028,6 +1048,12 @@ cudaError_t tc_forward(const TcPlan& pl, const void* q, const void* k, const voi
                        const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream) {
     if (pl.dv == 64) return tc_forward_dv<64>(pl, q, k, v, log_a, lambda, out, workspace, err, stream);
     return tc_forward_dv<128>(pl, q, k, v, log_a, lambda, out, workspace, err, stream);
+}
+
+cudaError_t tc_nodes_only(const TcPlan& pl, const void* k, const void* v, const float* log_a, void* workspace,
+                          int* err, cudaStream_t stream) {
+    if (pl.dv == 64) return tc_forward_dv<64>(pl, k, k, v, log_a, nullptr, nullptr, workspace, err, stream, true);
+    return tc_forward_dv<128>(pl, k, k, v, log_a, nullptr, nullptr, workspace, err, stream, true);
 }
 
 }  // namespace lla

@@ -1,0 +1,897 @@
+// Tensor-core (tcgen05 / TMEM / TMA) backward of log-linear Mamba-2 attention
+// for bf16 q/k/v/dO with dk = 128, dv = 64 and T % 128 == 0.
+//
+// The gradients of L = sum_t dO_t . o_t follow the forward's structure on
+// 128-token tiles ("Log-Linear Attention", pt §2 "Forma Recorrente e Paralela"
+// / fr §2 "Algorithmes Efficaces": dense work inside a block, Fenwick nodes
+// across blocks). Tile j reads node (p, m = (j >> p) - 1) for each set bit p of
+// j with per-query weight r_{t,p} = lambda_t^(8+p) exp(cum_t - cum_e), e the
+// node's last token; inside a tile the key levels are 0..7.
+//
+// Kernels (one stream, in order):
+//   tc_nodes, tc_merge : the forward's node stage (bf16 nodes that are read,
+//                        tile decays, per-token and per-level decay tables).
+//   tc_dnode           : node gradients dB_{p,m} = sum over the tiles j of the
+//                        reading block of Q_j^T diag(r_p) dO_j, on tcgen05 with
+//                        r_p o dO scaled in shared memory; runs of tiles of one
+//                        node accumulate in TMEM and are added (fp32 vector
+//                        atomics) into the node.
+//   tc_cmat            : per key tile i, C_i = sum over its read ancestor
+//                        nodes of exp(decay from tile i's end to the node's
+//                        end) dB (bf16, an MMA operand of the next kernel).
+//   tc_bwd_tile        : one CTA per tile: S = Q K^T and dP = dO V^T (TMEM);
+//                        A = lambda D S and G = lambda D dP (bf16, smem) with
+//                        dlambda levels 0..7 and the decay derivatives; then
+//                        dV = A^T dO, dQ = G K, dK = G^T Q; per set bit p,
+//                        Y_p = Q B_p (for dlambda_t^(8+p) and dcum) and
+//                        dQ += (r_p o dO) B_p^T; per key tile, dK += (w o V)
+//                        C_i^T, dV += (w o K) C_i and Z = K C_i (for dcum).
+//   bwd_dloga          : dlog_a_r = sum_{t >= r} dcum_t.
+// Every mbarrier wait is bounded; on overrun a kernel records LLA_ERR_TIMEOUT,
+// lets its own copies and MMAs land and returns.
+#include "lla_tc_ptx.cuh"
+
+namespace lla {
+namespace {
+
+constexpr int kDV = 64;
+constexpr int kMsz = kDk * kDV;
+
+struct Offsets { int off[32]; };
+
+// ------------------------------------------------------------------ tc_dnode
+
+// Items of one head, in order: level p, then the tiles j with bit p set (each
+// read block's tiles are consecutive). ofs[p] = first item of level p, ofs[P] =
+// items per head.
+struct DnodeLevels {
+    int P;
+    int ofs[17];
+};
+
+// The k-th integer with bit p set: k's bits with a 1 inserted at position p.
+__device__ __forceinline__ int insert_bit(int k, int p) {
+    return ((k >> p) << (p + 1)) | (1 << p) | (k & ((1 << p) - 1));
+}
+
+struct DnodeCfg {
+    static constexpr int kStages = 4;
+    static constexpr int kQBytes = 2 * kPanelBytes;  // Q tile: 128 tokens x 128
+    static constexpr int kDBytes = kPanelBytes;      // dO tile: 128 tokens x 64 (scaled in place)
+    static constexpr int kStageBytes = kQBytes + kDBytes;
+    static constexpr uint32_t kTxBytes = kStageBytes;
+    static constexpr int kBytes = kStages * kStageBytes + 1024;
+    static constexpr int kThreads = 384;
+    static constexpr uint32_t kTmemCols = 2 * kDV;  // two accumulators
+};
+
+// 384 threads: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4..7 scale
+// dO (one token row per thread), warps 8..11 drain accumulators (dk row per thread).
+__global__ void __launch_bounds__(384, 1)
+    tc_dnode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                    const float* __restrict__ lambda, const float* __restrict__ tok_cl2,
+                    const float* __restrict__ dtab, float* __restrict__ dnodes, int T, int NT, int L,
+                    int node_count, Offsets lo, const DnodeLevels lv, int total, int* err) {
+    using C = DnodeCfg;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t full_bar[S], scaled_bar[S], empty_bar[S], acc_full[2], acc_empty[2], drain_bar;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int fail_sh;
+    __shared__ int ofs[17];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per_head = lv.ofs[lv.P];
+    const int P = lv.P;
+    if (tid < 17) ofs[tid] = lv.ofs[tid];
+    const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
+    const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
+    volatile int* fail = &fail_sh;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&scaled_bar[s], 4);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(&drain_bar, 1);
+        fence_mbar_init();
+        fail_sh = 0;
+    }
+    if (warp == 1) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    auto fail_now = [&]() {
+        if (atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
+    };
+    // Walk of this CTA's items without divisions: head, level p, index k within the level,
+    // tile j; an item ends its run when the next one reads another node.
+    struct Cursor {
+        int bh, p, k, j;
+        bool last_of_run;
+    };
+    auto make_cursor = [&](int f) {
+        Cursor c;
+        c.bh = f / per_head;
+        const int w = f - c.bh * per_head;
+        c.p = 0;
+        while (c.p + 1 < P && ofs[c.p + 1] <= w) c.p++;
+        c.k = w - ofs[c.p];
+        c.j = insert_bit(c.k, c.p);
+        c.last_of_run = true;
+        return c;
+    };
+    // advances c from item f to f + 1 and fills c.last_of_run for item f
+    auto step = [&](Cursor& c, int f) {
+        Cursor n = c;
+        n.k++;
+        // skip to the next level that still has items (levels may be empty)
+        while (n.p < P && ofs[n.p] + n.k >= ofs[n.p + 1]) {
+            n.k = 0;
+            n.p++;
+        }
+        if (n.p >= P) {  // next head, first nonempty level
+            n.bh++;
+            n.p = 0;
+            n.k = 0;
+            while (n.p < P && ofs[n.p] >= ofs[n.p + 1]) n.p++;
+        }
+        n.j = insert_bit(n.k, n.p);
+        c.last_of_run = (f + 1 >= t1) || n.bh != c.bh || n.p != c.p || (n.j >> (n.p + 1)) != (c.j >> (c.p + 1));
+        n.last_of_run = true;
+        return n;
+    };
+
+    int issued = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            Cursor c = make_cursor(t0);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int f = t0; f < t1 && !*fail; f++, issued++) {
+                if (f - t0 >= S && !mbar_wait(&empty_bar[s], ph ^ 1u)) {
+                    fail_now();
+                    break;
+                }
+                const int r0 = c.bh * T + c.j * kTile;
+                uint8_t* st = smem + s * C::kStageBytes;
+                mbar_expect_tx(&full_bar[s], C::kTxBytes);
+                tma_load_2d(st, &tm_q, &full_bar[s], 0, r0);
+                tma_load_2d(st + kPanelBytes, &tm_q, &full_bar[s], 64, r0);
+                tma_load_2d(st + C::kQBytes, &tm_do, &full_bar[s], 0, r0);
+                c = step(c, f);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t kIdesc = idesc_bf16(kDk, kDV, 1, 1);  // A = Q^T, B = r o dO, both MN-major
+            const uint64_t qdesc0 = sdesc(smem_u32(smem), kPanelBytes, 1024);
+            const uint64_t ddesc0 = sdesc(smem_u32(smem + C::kQBytes), kPanelBytes, 1024);
+            constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+            Cursor c = make_cursor(t0);
+            bool starting = true;
+            int run = 0, s = 0;
+            uint32_t ph = 0;
+            for (int f = t0; f < t1 && !*fail; f++) {
+                const Cursor nc = step(c, f);
+                const bool ending = c.last_of_run;
+                const int buf = run & 1;
+                if (starting && run >= 2 && !mbar_wait(&acc_empty[buf], ((run >> 1) - 1) & 1)) {
+                    fail_now();
+                    break;
+                }
+                if (!mbar_wait(&scaled_bar[s], ph)) {
+                    fail_now();
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t so = kStageStep * s;
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; kk++) {
+                    const uint64_t ko = so + 128u * kk;
+                    mma_bf16(tmem + buf * kDV, qdesc0 + ko, ddesc0 + ko, kIdesc, (starting && kk == 0) ? 0u : 1u);
+                }
+                mma_commit(&empty_bar[s]);
+                if (ending) {
+                    mma_commit(&acc_full[buf]);
+                    run++;
+                }
+                starting = ending;
+                c = nc;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            mma_commit(&drain_bar);
+            if (!mbar_wait(&drain_bar, 0)) fail_now();
+        }
+    } else if (warp >= 4 && warp < 8) {
+        const int row = tid - 128;
+        // r_{t,p} = lambda_t^(8+p) exp2(cl2_t + dtab[j][p]) for this thread's token row
+        auto weight = [&](const Cursor& c) {
+            const size_t r = static_cast<size_t>(c.bh) * T + static_cast<size_t>(c.j) * kTile + row;
+            return lambda[r * L + 8 + c.p] *
+                   exp2f(tok_cl2[r] + dtab[(static_cast<size_t>(c.bh) * NT + c.j) * 16 + c.p]);
+        };
+        Cursor c = make_cursor(t0);
+        float w_next = weight(c);
+        int s = 0;
+        uint32_t ph = 0;
+        for (int f = t0; f < t1; f++) {
+            if (__any_sync(0xffffffffu, *fail != 0)) break;
+            const float w = w_next;
+            c = step(c, f);
+            if (f + 1 < t1) w_next = weight(c);
+            const int cs = s;
+            const uint32_t cph = ph;
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (!warp_wait(&full_bar[cs], cph)) {
+                if (lane == 0) fail_now();
+                break;
+            }
+            uint8_t* drow = smem + cs * C::kStageBytes + C::kQBytes + row * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ch++) {
+                uint4* hp = reinterpret_cast<uint4*>(drow + (((ch ^ (row & 7))) << 4));
+                const uint4 x = *hp;
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                *hp = make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
+                                 pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&scaled_bar[cs]);
+        }
+    } else if (warp >= 8) {
+        const int quad = warp & 3;
+        const int d = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        int run = 0;
+        Cursor c = make_cursor(t0);
+        for (int f = t0; f < t1; f++) {
+            const Cursor nc = step(c, f);
+            const Cursor cur = c;
+            c = nc;
+            if (!cur.last_of_run) continue;
+            const int buf = run & 1;
+            if (__any_sync(0xffffffffu, *fail != 0)) break;
+            if (!warp_wait(&acc_full[buf], (run >> 1) & 1)) {
+                if (lane == 0) fail_now();
+                break;
+            }
+            tc_fence_after();
+            const int m = (cur.j >> cur.p) - 1;
+            float4* dst = reinterpret_cast<float4*>(
+                dnodes + ((static_cast<size_t>(cur.bh) * node_count + lo.off[cur.p] + (m >> 1)) * kDk + d) * kDV);
+#pragma unroll
+            for (int c0 = 0; c0 < kDV; c0 += 32) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + buf * kDV + c0, x);
+#pragma unroll
+                for (int q = 0; q < 8; q++)
+                    atomicAdd(dst + c0 / 4 + q, make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            run++;
+        }
+    }
+
+    __syncthreads();
+    if (*fail && warp == 0 && lane == 0) {
+        for (int i = issued - S > 0 ? issued - S : 0; i < issued; i++) mbar_wait(&full_bar[i % S], (i / S) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ tc_cmat
+
+// C_i = sum over the read ancestors (p, i >> p) of key tile i of
+// exp(sum of the tile decays after i up to the node's last tile) dB_{p, i>>p},
+// bf16 [BH][NT][dk][dv]. grid (NT, BH, dk*dv / 1024), 256 threads, 4 elements each.
+__global__ void __launch_bounds__(256) tc_cmat_kernel(const float* __restrict__ dnodes, const float* __restrict__ g,
+                                                      __nv_bfloat16* __restrict__ cmat, int NT, int P, int node_count,
+                                                      Offsets lo) {
+    __shared__ float wsh[32];
+    __shared__ int rsh[32];
+    const int i = blockIdx.x, bh = blockIdx.y;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        for (int p = 0; p < P; p++) {
+            const int m = i >> p;
+            const bool read = (m & 1) == 0 && ((m + 1) << p) < NT;
+            const int end = (m + 1) << p;  // one past the node's last tile
+            float sacc = 0.f;
+            if (read)
+                for (int u = i + 1 + lane; u < end; u += 32) sacc += g[static_cast<size_t>(bh) * NT + u];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, off);
+            if (lane == 0) {
+                wsh[p] = read ? expf(sacc) : 0.f;
+                rsh[p] = read ? 1 : 0;
+            }
+        }
+    }
+    __syncthreads();
+    const int e = blockIdx.z * 1024 + threadIdx.x;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int p = 0; p < P; p++) {
+        if (!rsh[p]) continue;
+        const float w = wsh[p];
+        const float* node = dnodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + ((i >> p) >> 1)) * kMsz + e;
+#pragma unroll
+        for (int r = 0; r < 4; r++) acc[r] = fmaf(w, node[256 * r], acc[r]);
+    }
+    __nv_bfloat16* dst = cmat + (static_cast<size_t>(bh) * NT + i) * kMsz + e;
+#pragma unroll
+    for (int r = 0; r < 4; r++) dst[256 * r] = __float2bfloat16_rn(acc[r]);
+}
+
+// ------------------------------------------------------------------ tc_bwd_tile
+
+struct TileCfg {
+    static constexpr int kQ = 0;                     // Q tile  [t][d], 2 panels
+    static constexpr int kK = 2 * kPanelBytes;       // K tile  [s][d], 2 panels
+    static constexpr int kV = 4 * kPanelBytes;       // V tile  [s][e], 1 panel
+    static constexpr int kDO = 5 * kPanelBytes;      // dO tile [t][e], 1 panel
+    static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; later w o K [s][d]
+    static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels
+    static constexpr int kR = 10 * kPanelBytes;      // r_p o dO [t][e]; later w o V [s][e]
+    static constexpr int kN = 11 * kPanelBytes;      // node B_p [d][e]; later C_i [d][e]
+    static constexpr int kBytes = 12 * kPanelBytes + 1024;
+    static constexpr uint32_t kTxIn = 6 * kPanelBytes;
+    // TMEM columns
+    static constexpr uint32_t kS = 0, kDP = 128;                       // S, dP (phase 1)
+    static constexpr uint32_t kDQ = 0, kDK = 128, kDVc = 256, kY = 320, kZ = 384;
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+// Reduce-scatter of 32 values per lane over the warp: lane l ends with the sum over all
+// lanes of v[l] (31 shuffles).
+__device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; i++) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[0];
+}
+
+// One CTA per (head, tile); 256 threads: thread (quad = warp % 4, lane) owns row
+// t = 32 quad + lane (= TMEM lane), half = warp / 4 picks half of the columns. Thread 0
+// issues the TMA copies and the MMAs between block-wide phases.
+__global__ void __launch_bounds__(256, 1)
+    tc_bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_nodes, const __grid_constant__ CUtensorMap tm_cmat,
+                       const float* __restrict__ lambda, const float* __restrict__ tok_cl2,
+                       const float* __restrict__ dtab, __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
+                       __nv_bfloat16* __restrict__ dv, float* __restrict__ dlambda, float* __restrict__ dcum, int T,
+                       int NT, int L, int P, int node_count, Offsets lo, int* err) {
+    using C = TileCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar_in, bar_s, bar_m1, bar_node, bar_lv, bar_c, bar_k, bar_d;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ float cl2_sh[kTile];
+    __shared__ float lam8[kTile][8];
+    __shared__ float lamp[kTile][16];
+    __shared__ float dlam8[kTile][8];
+    __shared__ float dlamp[kTile][16];
+    __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile];
+    __shared__ float dtab_sh[16];
+    __shared__ int fail_sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int t = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int j = blockIdx.x, bh = blockIdx.y;
+    const int r0 = bh * T + j * kTile;
+    const unsigned lvbits = static_cast<unsigned>(j) & ((1u << P) - 1u);
+
+    if (tid == 0) {
+        mbar_init(&bar_in, 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_m1, 1);
+        mbar_init(&bar_node, 1);
+        mbar_init(&bar_lv, 1);
+        mbar_init(&bar_c, 1);
+        mbar_init(&bar_k, 1);
+        mbar_init(&bar_d, 1);
+        fence_mbar_init();
+        fail_sh = 0;
+    }
+    if (warp == 0) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    // every wait is warp-uniform and bounded; a failure is shared through fail_sh
+    auto ok_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (warp_wait(bar, parity)) return true;
+        if (lane == 0 && atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
+        return false;
+    };
+    auto node_row = [&](int p) { return (bh * node_count + lo.off[p] + (((j >> p) - 1) >> 1)) * kDk; };
+
+    int node_issued = 0;  // thread 0: node copies issued
+    bool c_issued = false;
+    if (tid == 0) {
+        uint8_t* st = smem;
+        mbar_expect_tx(&bar_in, C::kTxIn);
+        tma_load_2d(st + C::kQ, &tm_q, &bar_in, 0, r0);
+        tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &bar_in, 64, r0);
+        tma_load_2d(st + C::kK, &tm_k, &bar_in, 0, r0);
+        tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &bar_in, 64, r0);
+        tma_load_2d(st + C::kV, &tm_v, &bar_in, 0, r0);
+        tma_load_2d(st + C::kDO, &tm_do, &bar_in, 0, r0);
+        if (lvbits) {
+            const int p0 = __ffs(lvbits) - 1;
+            mbar_expect_tx(&bar_node, kPanelBytes);
+            tma_load_2d(st + C::kN, &tm_nodes, &bar_node, 0, node_row(p0));
+            node_issued = 1;
+        }
+    }
+    // per-row inputs: decay prefix, lambda levels, the tile's level decay row
+    if (tid < kTile) cl2_sh[tid] = tok_cl2[r0 + tid];
+    for (int x = tid; x < kTile * L; x += blockDim.x) {
+        const int row = x / L, l = x - row * L;
+        const float val = lambda[static_cast<size_t>(r0) * L + x];
+        if (l < 8) lam8[row][l] = val;
+        else if (l < 24) lamp[row][l - 8] = val;
+    }
+    if (tid < 16) dtab_sh[tid] = dtab[(static_cast<size_t>(bh) * NT + j) * 16 + tid];
+    for (int x = tid; x < kTile * 8; x += blockDim.x) (&dlam8[0][0])[x] = 0.f;
+    for (int x = tid; x < kTile * 16; x += blockDim.x) (&dlamp[0][0])[x] = 0.f;
+    if (tid < kTile) {
+        colE[tid] = 0.f;
+        dcs[tid] = 0.f;
+        zsh[tid] = 0.f;
+    }
+    __syncthreads();
+
+    // ok stays block-uniform: every change goes through a barrier reduction
+    bool ok = __syncthreads_and(ok_wait(&bar_in, 0));
+    // ---- S = Q K^T, dP = dO V^T
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        constexpr uint32_t kIdSS = idesc_bf16(kTile, kTile, 0, 0);
+        const uint32_t qb = smem_u32(smem + C::kQ), kb = smem_u32(smem + C::kK);
+        const uint32_t vb = smem_u32(smem + C::kV), ob = smem_u32(smem + C::kDO);
+#pragma unroll
+        for (int kk = 0; kk < kDk / 16; kk++) {
+            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+            mma_bf16(tmem + C::kS, sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kDV / 16; kk++) {
+            mma_bf16(tmem + C::kDP, sdesc(ob + kk * 32, 16, 1024), sdesc(vb + kk * 32, 16, 1024), kIdSS,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_s);
+    }
+    ok = __syncthreads_and(ok && ok_wait(&bar_s, 0));
+    tc_fence_after();
+
+    // ---- E1: A, G (bf16), dlambda levels 0..7, decay derivatives
+    if (ok) {
+        const float cl2_t = cl2_sh[t];
+        float dl[8];
+#pragma unroll
+        for (int l = 0; l < 8; l++) dl[l] = 0.f;
+        float rowE = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 2; c++) {
+            const int cb = 64 * half + 32 * c;  // first key of this chunk
+            float ev[32];
+            uint32_t pa[16], pg[16];
+            if (cb > quad * 32 + 31) {
+#pragma unroll
+                for (int e = 0; e < 32; e++) ev[e] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; e++) pa[e] = pg[e] = 0u;
+            } else {
+                float sv[32], dpv[32];
+                tmem_ld32(tmem + lane_base + C::kS + cb, sv);
+                tmem_ld32(tmem + lane_base + C::kDP + cb, dpv);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float av[2], gv[2];
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int s = cb + e + h;
+                        const int l = 32 - __clz(t ^ s);
+                        float lm = lam8[t][0];
+#pragma unroll
+                        for (int ll = 1; ll < 8; ll++) lm = (l == ll) ? lam8[t][ll] : lm;
+                        const float D = exp2f(fminf(cl2_t - cl2_sh[s], 0.f));
+                        const bool causal = s <= t;
+                        const float dq_ = causal ? D * sv[e + h] * dpv[e + h] : 0.f;
+#pragma unroll
+                        for (int ll = 0; ll < 8; ll++) dl[ll] += (l == ll) ? dq_ : 0.f;
+                        ev[e + h] = lm * dq_;
+                        av[h] = causal ? lm * D * sv[e + h] : 0.f;
+                        gv[h] = causal ? lm * D * dpv[e + h] : 0.f;
+                    }
+                    pa[e >> 1] = pack_bf16(av[0], av[1]);
+                    pg[e >> 1] = pack_bf16(gv[0], gv[1]);
+                    rowE += ev[e] + ev[e + 1];
+                }
+            }
+            uint8_t* pA = smem + C::kA + (cb >> 6) * kPanelBytes;
+            uint8_t* pG = smem + C::kG + (cb >> 6) * kPanelBytes;
+            const int ch0 = (cb & 63) >> 3;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                *reinterpret_cast<uint4*>(pA + sw128_off(t, ch0 + q)) =
+                    make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                *reinterpret_cast<uint4*>(pG + sw128_off(t, ch0 + q)) =
+                    make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
+            }
+            const float cs = warp_colsum32(ev);
+            atomicAdd(&colE[cb + lane], cs);
+        }
+#pragma unroll
+        for (int l = 0; l < 8; l++)
+            if (dl[l] != 0.f) atomicAdd(&dlam8[t][l], dl[l]);
+        atomicAdd(&dcs[t], rowE);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- dV = A^T dO, dQ = G K, dK = G^T Q
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t ab = smem_u32(smem + C::kA), gb = smem_u32(smem + C::kG);
+        const uint32_t qb = smem_u32(smem + C::kQ), kb = smem_u32(smem + C::kK), ob = smem_u32(smem + C::kDO);
+        constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 1, 1);
+        constexpr uint32_t kIdQ = idesc_bf16(kTile, kDk, 0, 1);
+        constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 1, 1);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; kk++) {
+            const uint32_t koff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+            mma_bf16(tmem + C::kDVc, sdesc(ab + kk * 2048, kPanelBytes, 1024), sdesc(ob + kk * 2048, kPanelBytes, 1024),
+                     kIdV, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + C::kDQ, sdesc(gb + koff, 16, 1024), sdesc(kb + kk * 2048, kPanelBytes, 1024), kIdQ,
+                     kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + C::kDK, sdesc(gb + kk * 2048, kPanelBytes, 1024), sdesc(qb + kk * 2048, kPanelBytes, 1024),
+                     kIdK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_m1);
+    }
+
+    // ---- query side: one round per set bit p of j
+    int li = 0;
+    for (int p = 0; p < P && ok; p++) {
+        if (((j >> p) & 1) == 0) continue;
+        const float cl2_t = cl2_sh[t];
+        const float rho = exp2f(cl2_t + dtab_sh[p]);
+        const float r = lamp[t][p] * rho;
+        // r_p o dO, row t, this half's 32 columns (chunks 4 half .. 4 half + 3)
+        {
+            const uint8_t* src = smem + C::kDO;
+            uint8_t* dst = smem + C::kR;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t off = sw128_off(t, 4 * half + q);
+                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                *reinterpret_cast<uint4*>(dst + off) =
+                    make_uint4(pack_bf16(a0.x * r, a0.y * r), pack_bf16(a1.x * r, a1.y * r),
+                               pack_bf16(a2.x * r, a2.y * r), pack_bf16(a3.x * r, a3.y * r));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            if (mbar_wait(&bar_node, li & 1)) {
+                tc_fence_after();
+                const uint32_t qb = smem_u32(smem + C::kQ), nb = smem_u32(smem + C::kN), rb = smem_u32(smem + C::kR);
+                constexpr uint32_t kIdY = idesc_bf16(kTile, kDV, 0, 1);
+                constexpr uint32_t kIdX = idesc_bf16(kTile, kDk, 0, 0);
+#pragma unroll
+                for (int kk = 0; kk < kDk / 16; kk++) {
+                    const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                    mma_bf16(tmem + C::kY, sdesc(qb + off, 16, 1024), sdesc(nb + kk * 2048, kPanelBytes, 1024), kIdY,
+                             kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kDV / 16; kk++)
+                    mma_bf16(tmem + C::kDQ, sdesc(rb + kk * 32, 16, 1024), sdesc(nb + kk * 32, 16, 1024), kIdX, 1u);
+                mma_commit(&bar_lv);
+            } else if (atomicExch(&fail_sh, 1) == 0) {
+                record_error(err, kDevTimeout);
+            }
+        }
+        ok = __syncthreads_and(ok_wait(&bar_lv, li & 1));
+        tc_fence_after();
+        if (ok) {
+            // the node slot is free: fetch the next level's node
+            if (tid == 0) {
+                const unsigned rest = lvbits & ~((2u << p) - 1u);
+                if (rest) {
+                    const int pn = __ffs(rest) - 1;
+                    mbar_expect_tx(&bar_node, kPanelBytes);
+                    tma_load_2d(smem + C::kN, &tm_nodes, &bar_node, 0, node_row(pn));
+                    node_issued++;
+                }
+            }
+            float yv[32];
+            tmem_ld32(tmem + lane_base + C::kY + 32 * half, yv);
+            const uint8_t* src = smem + C::kDO;
+            float z = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                z = fmaf(yv[8 * q], a0.x, z); z = fmaf(yv[8 * q + 1], a0.y, z);
+                z = fmaf(yv[8 * q + 2], a1.x, z); z = fmaf(yv[8 * q + 3], a1.y, z);
+                z = fmaf(yv[8 * q + 4], a2.x, z); z = fmaf(yv[8 * q + 5], a2.y, z);
+                z = fmaf(yv[8 * q + 6], a3.x, z); z = fmaf(yv[8 * q + 7], a3.y, z);
+            }
+            atomicAdd(&zsh[t], z);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (ok && half == 0) {
+            const float zt = zsh[t];
+            dlamp[t][p] = rho * zt;
+            dcs[t] += r * zt;
+            zsh[t] = 0.f;
+        }
+        __syncthreads();
+        li++;
+    }
+
+    // ---- key side: dK += (w o V) C_i^T, dV += (w o K) C_i, Z = K C_i
+    ok = __syncthreads_and(ok && ok_wait(&bar_m1, 0));  // A and G are consumed: their space takes w o K
+    if (tid == 0 && ok) {
+        mbar_expect_tx(&bar_c, kPanelBytes);
+        tma_load_2d(smem + C::kN, &tm_cmat, &bar_c, 0, (bh * NT + j) * kDk);
+        c_issued = true;
+    }
+    if (ok) {
+        const float w = exp2f(cl2_sh[kTile - 1] - cl2_sh[t]);
+        if (half == 0) wts[t] = w;
+        // w o V: row t (= key s), this half's 32 columns
+        {
+            const uint8_t* src = smem + C::kV;
+            uint8_t* dst = smem + C::kR;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t off = sw128_off(t, 4 * half + q);
+                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                *reinterpret_cast<uint4*>(dst + off) =
+                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
+                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
+            }
+        }
+        // w o K: row t, panel `half` (64 columns)
+        {
+            const uint8_t* src = smem + C::kK + half * kPanelBytes;
+            uint8_t* dst = smem + C::kA + half * kPanelBytes;
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const uint32_t off = sw128_off(t, q);
+                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                *reinterpret_cast<uint4*>(dst + off) =
+                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
+                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        if (mbar_wait(&bar_c, 0)) {
+            tc_fence_after();
+            const uint32_t rb = smem_u32(smem + C::kR), cb = smem_u32(smem + C::kN);
+            const uint32_t ab = smem_u32(smem + C::kA), kb = smem_u32(smem + C::kK);
+            constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 0, 0);
+            constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < kDV / 16; kk++)
+                mma_bf16(tmem + C::kDK, sdesc(rb + kk * 32, 16, 1024), sdesc(cb + kk * 32, 16, 1024), kIdK, 1u);
+#pragma unroll
+            for (int kk = 0; kk < kDk / 16; kk++) {
+                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                mma_bf16(tmem + C::kDVc, sdesc(ab + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV, 1u);
+                mma_bf16(tmem + C::kZ, sdesc(kb + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV,
+                         kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar_k);
+        } else if (atomicExch(&fail_sh, 1) == 0) {
+            record_error(err, kDevTimeout);
+        }
+    }
+    ok = __syncthreads_and(ok && ok_wait(&bar_k, 0));
+    tc_fence_after();
+    if (ok) {
+        float zv[32];
+        tmem_ld32(tmem + lane_base + C::kZ + 32 * half, zv);
+        const uint8_t* src = smem + C::kV;
+        float y = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
+            const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+            y = fmaf(zv[8 * q], a0.x, y); y = fmaf(zv[8 * q + 1], a0.y, y);
+            y = fmaf(zv[8 * q + 2], a1.x, y); y = fmaf(zv[8 * q + 3], a1.y, y);
+            y = fmaf(zv[8 * q + 4], a2.x, y); y = fmaf(zv[8 * q + 5], a2.y, y);
+            y = fmaf(zv[8 * q + 6], a3.x, y); y = fmaf(zv[8 * q + 7], a3.y, y);
+        }
+        atomicAdd(&zsh[t], y);
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- outputs
+    if (ok) {
+        const size_t row = static_cast<size_t>(r0) + t;
+        float x[32];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            tmem_ld32(tmem + lane_base + C::kDQ + 64 * half + c0, x);
+            uint4* d4 = reinterpret_cast<uint4*>(dq + row * kDk + 64 * half + c0);
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
+                                   pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+            tmem_ld32(tmem + lane_base + C::kDK + 64 * half + c0, x);
+            d4 = reinterpret_cast<uint4*>(dk + row * kDk + 64 * half + c0);
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
+                                   pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+        }
+        tmem_ld32(tmem + lane_base + C::kDVc + 32 * half, x);
+        uint4* d4 = reinterpret_cast<uint4*>(dv + row * kDV + 32 * half);
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
+                               pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+        if (half == 0) dcum[row] = dcs[t] - colE[t] - wts[t] * zsh[t];
+    }
+    for (int x = tid; x < kTile * L; x += blockDim.x) {
+        const int row = x / L, l = x - row * L;
+        dlambda[static_cast<size_t>(r0) * L + x] = l < 8 ? dlam8[row][l] : (l < 24 ? dlamp[row][l - 8] : 0.f);
+    }
+
+    __syncthreads();
+    if (tid == 0 && fail_sh) {
+        // let this CTA's copies land before its shared memory goes away
+        mbar_wait(&bar_in, 0);
+        if (node_issued > 0) mbar_wait(&bar_node, (node_issued - 1) & 1);
+        if (c_issued) mbar_wait(&bar_c, 0);
+    }
+    if (tid == 0) {
+        // every MMA issued above has completed before TMEM is released
+        mma_commit(&bar_d);
+        mbar_wait(&bar_d, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+}  // namespace
+
+bool tc_bwd_supported(int dtype, int dk, int dv, int T) {
+    return dtype == 0 && dk == kDk && dv == kDV && T % kTile == 0;
+}
+
+size_t tc_bwd_workspace_bytes(const TcPlan& pl) {
+    const size_t BH = static_cast<size_t>(pl.B) * pl.H;
+    const size_t dnodes = (BH * pl.node_count * kMsz * sizeof(float) + 1023) / 1024 * 1024;
+    const size_t cmat = (BH * pl.NT * kMsz * 2 + 1023) / 1024 * 1024;
+    const size_t dcum = (BH * pl.T * sizeof(float) + 255) / 256 * 256;
+    return pl.total_bytes + dnodes + cmat + dcum;
+}
+
+cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
+                        const float* lambda, const void* dout, void* dq, void* dk, void* dv, float* dlog_a,
+                        float* dlambda, void* workspace, int* err, cudaStream_t stream) {
+    const int BH = pl.B * pl.H;
+    const int L = bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const float* g_tiles = reinterpret_cast<const float*>(ws);
+    const __nv_bfloat16* nodes = reinterpret_cast<const __nv_bfloat16*>(ws + pl.g_bytes);
+    const float* dtab = reinterpret_cast<const float*>(ws + pl.g_bytes + pl.nodes_bytes + pl.seg_bytes);
+    const float* tok_cl2 =
+        reinterpret_cast<const float*>(ws + pl.g_bytes + pl.nodes_bytes + pl.seg_bytes + pl.dtab_bytes);
+    const size_t dnodes_bytes = (static_cast<size_t>(BH) * pl.node_count * kMsz * sizeof(float) + 1023) / 1024 * 1024;
+    const size_t cmat_bytes = (static_cast<size_t>(BH) * pl.NT * kMsz * 2 + 1023) / 1024 * 1024;
+    float* dnodes = reinterpret_cast<float*>(ws + pl.total_bytes);
+    __nv_bfloat16* cmat = reinterpret_cast<__nv_bfloat16*>(ws + pl.total_bytes + dnodes_bytes);
+    float* dcum = reinterpret_cast<float*>(ws + pl.total_bytes + dnodes_bytes + cmat_bytes);
+    Offsets lo;
+    for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
+
+    cudaError_t e = tc_nodes_only(pl, k, v, log_a, workspace, err, stream);
+    if (e != cudaSuccess) return e;
+
+    const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
+    CUtensorMap tq, tk, tv, tdo, tn, tc;
+    if (!make_map(&tq, q, rows, kDk) || !make_map(&tk, k, rows, kDk) || !make_map(&tv, v, rows, kDV) ||
+        !make_map(&tdo, dout, rows, kDV) ||
+        !make_map(&tc, cmat, static_cast<uint64_t>(BH) * pl.NT * kDk, kDV))
+        return cudaErrorInvalidValue;
+    if (pl.node_count > 0) {
+        if (!make_map(&tn, nodes, static_cast<uint64_t>(BH) * pl.node_count * kDk, kDV)) return cudaErrorInvalidValue;
+    } else {
+        tn = tc;  // never read: no tile has an earlier block
+    }
+
+    if (pl.node_count > 0) {
+        e = cudaMemsetAsync(dnodes, 0, dnodes_bytes, stream);
+        if (e != cudaSuccess) return e;
+        DnodeLevels lv;
+        lv.P = pl.P;
+        int n = 0;
+        for (int p = 0; p <= 16; p++) {
+            lv.ofs[p] = n;
+            if (p < pl.P) n += pl.NT / (2 << p) * (1 << p) + (pl.NT % (2 << p) > (1 << p) ? pl.NT % (2 << p) - (1 << p) : 0);
+        }
+        const int total = BH * n;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+            cudaGetLastError();
+            sms = 152;
+        }
+        const int grid = total < sms ? total : sms;
+        e = cudaFuncSetAttribute(tc_dnode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DnodeCfg::kBytes);
+        if (e != cudaSuccess) return e;
+        tc_dnode_kernel<<<grid, DnodeCfg::kThreads, DnodeCfg::kBytes, stream>>>(
+            tq, tdo, lambda, tok_cl2, dtab, dnodes, pl.T, pl.NT, L, pl.node_count, lo, lv, total, err);
+        note_launch(stream, "tc_dnode");
+    }
+    tc_cmat_kernel<<<dim3(pl.NT, BH, kMsz / 1024), 256, 0, stream>>>(dnodes, g_tiles, cmat, pl.NT, pl.P, pl.node_count,
+                                                                     lo);
+    note_launch(stream, "tc_cmat");
+    e = cudaFuncSetAttribute(tc_bwd_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg::kBytes);
+    if (e != cudaSuccess) return e;
+    tc_bwd_tile_kernel<<<dim3(pl.NT, BH), 256, TileCfg::kBytes, stream>>>(
+        tq, tk, tv, tdo, tn, tc, lambda, tok_cl2, dtab, static_cast<__nv_bfloat16*>(dq),
+        static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), dlambda, dcum, pl.T, pl.NT, L, pl.P,
+        pl.node_count, lo, err);
+    note_launch(stream, "tc_bwd_tile");
+    return bwd_dloga(dcum, dlog_a, BH, pl.T, stream);
+}
+
+}  // namespace lla

@@ -51,9 +51,14 @@ def _run(cfg, seed, chunk):
     (1, 2, 96, 24, 40, 32, "f32"),
     (1, 1, 256, 16, 16, 64, "f32"),
     (2, 1, 384, 64, 32, 128, "f32"),
-    (1, 2, 256, 64, 64, 64, "bf16"),
+    (1, 2, 256, 64, 64, 64, "bf16"),      # dk != 128: CUDA-core kernels
+    (1, 1, 640, 128, 128, 128, "bf16"),   # dv = 128: CUDA-core kernels
+    # bf16, dk = 128, dv = 64, T % 128 == 0: tensor-core kernels
+    (1, 1, 128, 128, 64, 64, "bf16"),     # one tile, no node
+    (1, 2, 384, 128, 64, 64, "bf16"),
     (2, 2, 512, 128, 64, 64, "bf16"),
-    (1, 1, 640, 128, 128, 128, "bf16"),
+    (2, 1, 1024, 128, 64, 128, "bf16"),
+    (1, 1, 2304, 128, 64, 64, "bf16"),    # 18 tiles
 ])
 def test_backward_matches_oracle(B, H, T, dk, dv, chunk, dtype):
     cfg = inputs.PrefillConfig("bw", B, H, T, dk, dv, chunk, dtype)
