@@ -560,9 +560,12 @@ def run_lla(args, cfg):
             "backward": {"workload": f"lla_backward of the same {cfg.name} problem (dq, dk, dv, dlog_a, dlambda)",
                          "ms": b_ms, "tokens_per_s": cfg.tokens / (b_ms / 1e3),
                          "tflops": bw["flops"] / (b_ms / 1e3) / 1e12,
-                         "algorithmic_gflop": bw["flops"] / 1e9, "bound": "alu",
-                         "frac_of_alu_peak": bw["flops"] / (b_ms / 1e3) / 1e12 / ALU_F32_TFLOPS,
-                         "peak_source": "derived: 152 SM x 128 FMA x 2.07 GHz"},
+                         "algorithmic_gflop": bw["flops"] / 1e9,
+                         "frac_of_bf16_peak": bw["flops"] / (b_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "bound": "hbm", "algorithmic_bytes": bw["bytes"],
+                         "gbs": bw["bytes"] / (b_ms / 1e3) / 1e9,
+                         "frac_of_hbm": bw["bytes"] / (b_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "peak_source": peaks["source"]},
             "e2e": {"value": ws * cfg.tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": {"value": cpu_val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
