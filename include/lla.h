@@ -202,6 +202,37 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
  * launch, LLA_ERR_NOMEM if the pool cannot grow, LLA_ERR_CUDA on launch
  * failure.
  */
+/*
+ * Packed variable-length sequences (no counterpart on the pages: a serving
+ * layout for many prompts of different lengths in one call).
+ *
+ * Layout: every tensor is packed per head, [H, total_T, W] row-major; sequence
+ * b owns rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of every head, and its token
+ * positions (hence its Fenwick levels) start at 0. cu_seqlens is DEVICE int32
+ * [n_seq + 1], non-decreasing, cu_seqlens[0] >= 0, cu_seqlens[n_seq] <= total_T,
+ * every length <= max_T. Lengths that break these rules are caught on the
+ * device: that sequence is skipped and lla_device_error reports LLA_ERR_DEVICE.
+ *
+ * lla_forward_varlen: the prefill of every sequence.
+ *   q, k [H,total_T,dk], v [H,total_T,dv] (dtype); log_a [H,total_T] fp32;
+ *   lambda [H,total_T,L] fp32 with L = lla_num_levels(max_T); out [H,total_T,dv].
+ *   The sequences are copied into a zero-padded [n_seq, H, Tpad] layout
+ *   (Tpad = max_T rounded up to 128) in pool workspace, run through the dense
+ *   prefill kernels and copied back; rows past a sequence's end cannot reach
+ *   its causal outputs. chunk as in lla_forward.
+ *
+ * lla_prefill_state_varlen: the decode state set after every sequence, as
+ * lla_prefill_state: fenwick_states [n_seq, H, Lmax, dk, dv] fp32 with
+ * Lmax >= lla_num_levels(max_T); slots empty at a sequence's last position are
+ * left untouched (an empty sequence touches none). CUDA-core kernels.
+ */
+int lla_forward_varlen(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                       void* out, const int32_t* cu_seqlens, int n_seq, int H, int total_T, int max_T, int dk, int dv,
+                       int chunk, void* stream, int dtype);
+int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, const int32_t* cu_seqlens,
+                             float* fenwick_states, int n_seq, int H, int total_T, int max_T, int dk, int dv, int Lmax,
+                             void* stream, int dtype);
+
 int lla_backward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
                  const void* dout, void* dq, void* dk, void* dv, float* dlog_a, float* dlambda, int B, int H,
                  int T, int dk_, int dv_, int chunk, void* stream, int dtype);

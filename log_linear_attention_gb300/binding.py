@@ -65,6 +65,10 @@ def load() -> ctypes.CDLL:
             lib.lla_device_error.restype = i
             lib.lla_backward.argtypes = [vp, vp, vp, fp, fp, vp, vp, vp, vp, fp, fp] + [i] * 6 + [vp, i]
             lib.lla_backward.restype = i
+            lib.lla_forward_varlen.argtypes = [vp, vp, vp, fp, fp, vp, vp] + [i] * 7 + [vp, i]
+            lib.lla_forward_varlen.restype = i
+            lib.lla_prefill_state_varlen.argtypes = [vp, vp, fp, vp, fp] + [i] * 7 + [vp, i]
+            lib.lla_prefill_state_varlen.restype = i
             _lib = lib
     return _lib
 
@@ -268,6 +272,47 @@ def backward(q, k, v, log_a, lam, dout, chunk: int, stream=None):
                               dlam.data_ptr(), B, H, T, dk, dv, chunk, _stream_handle(stream), _dtype_code(q)),
           "lla_backward")
     return dq, dk_, dv_, dla, dlam
+
+
+def forward_varlen(q, k, v, log_a, lam, cu_seqlens, max_T: int, chunk: int, out=None, stream=None):
+    """lla_forward_varlen: packed sequences. q, k [H,total,dk]; v [H,total,dv]; log_a [H,total];
+    lam [H,total,num_levels(max_T)]; cu_seqlens int32 [n+1] on the device."""
+    torch = _torch()
+    H, total, dk = q.shape
+    dv = v.shape[-1]
+    n = cu_seqlens.numel() - 1
+    for t_, nm in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda"), (cu_seqlens, "cu_seqlens")):
+        _check(t_, nm, q.device)
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if k.shape != q.shape or v.shape[:2] != (H, total) or log_a.shape != (H, total) or lam.shape[:2] != (H, total):
+        raise ValueError("shape mismatch between packed q, k, v, log_a and lambda")
+    if lam.shape[2] != num_levels(max_T):
+        raise ValueError(f"lambda needs {num_levels(max_T)} levels for max_T={max_T}")
+    if out is None:
+        out = torch.empty((H, total, dv), dtype=q.dtype, device=q.device)
+    _check(out, "out", q.device)
+    _call(load().lla_forward_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(),
+                                    out.data_ptr(), cu_seqlens.data_ptr(), n, H, total, max_T, dk, dv, chunk,
+                                    _stream_handle(stream), _dtype_code(q)), "lla_forward_varlen")
+    return out
+
+
+def prefill_state_varlen(k, v, log_a, cu_seqlens, max_T: int, states, stream=None):
+    """lla_prefill_state_varlen: states [n,H,Lmax,dk,dv] fp32 after each packed sequence."""
+    torch = _torch()
+    H, total, dk = k.shape
+    dv = v.shape[-1]
+    n = cu_seqlens.numel() - 1
+    Lmax = states.shape[2]
+    for t_, nm in ((k, "k"), (v, "v"), (log_a, "log_a"), (cu_seqlens, "cu_seqlens"), (states, "states")):
+        _check(t_, nm, k.device)
+    if cu_seqlens.dtype != torch.int32 or states.dtype != torch.float32 or states.shape != (n, H, Lmax, dk, dv):
+        raise ValueError("cu_seqlens must be int32 and states float32 [n,H,Lmax,dk,dv]")
+    _call(load().lla_prefill_state_varlen(k.data_ptr(), v.data_ptr(), log_a.data_ptr(), cu_seqlens.data_ptr(),
+                                          states.data_ptr(), n, H, total, max_T, dk, dv, Lmax,
+                                          _stream_handle(stream), _dtype_code(k)), "lla_prefill_state_varlen")
+    return states
 
 
 def device_error(stream=None) -> int:

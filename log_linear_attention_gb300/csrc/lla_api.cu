@@ -260,7 +260,7 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
         return LLA_ERR_NOMEM;
     }
     cudaError_t e = tc ? lla::tc_prefill_state(k, v, log_a, fenwick_states, B, H, T, dv, Lmax, ws, err, s)
-                       : lla::prefill_state(dtype, k, v, log_a, fenwick_states, B, H, T, dk, dv, Lmax, ws, s);
+                       : lla::prefill_state(dtype, k, v, log_a, fenwick_states, B, H, T, dk, dv, Lmax, ws, err, s);
     const cudaError_t f = cudaFreeAsync(ws, s);
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }
@@ -293,6 +293,90 @@ int lla_backward(const void* q, const void* k, const void* v, const float* log_a
     cudaError_t e = tc ? lla::tc_backward(tp, q, k, v, log_a, lambda, dout, dq, dk, dv, dlog_a, dlambda, ws, err, s)
                        : lla::simt_backward(bp, dtype, q, k, v, log_a, lambda, dout, dq, dk, dv, dlog_a, dlambda, ws,
                                             s);
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
+}
+
+int lla_forward_varlen(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                       void* out, const int32_t* cu_seqlens, int n_seq, int H, int total_T, int max_T, int dk, int dv,
+                       int chunk, void* stream, int dtype) {
+    if (!cu_seqlens || !aligned16(cu_seqlens)) return LLA_ERR_INVALID_ARG;
+    if (n_seq < 1 || max_T < 1 || total_T < 1) return LLA_ERR_INVALID_ARG;
+    if ((int64_t)n_seq * max_T < total_T) return LLA_ERR_INVALID_ARG;
+    const int Tpad = (max_T + 127) / 128 * 128;
+    int st = validate_forward(q, k, v, log_a, lambda, out, n_seq, H, Tpad, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    if ((int64_t)H * total_T * (dk > dv ? dk : dv) > ((int64_t)1 << 40)) return LLA_ERR_UNSUPPORTED;
+    ForwardPlan fp;
+    if (!plan_forward(n_seq, H, Tpad, dk, dv, chunk, dtype, &fp)) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return LLA_ERR_CUDA;
+    const int esz = dtype == LLA_BF16 ? 2 : 4;
+    const int L_in = lla_num_levels(max_T), L_pad = lla_num_levels(Tpad);
+    const size_t rows = (size_t)n_seq * H * Tpad;
+    auto up = [](size_t x) { return (x + 1023) / 1024 * 1024; };
+    const size_t bq = up(rows * dk * esz), bv = up(rows * dv * esz), ba = up(rows * 4), bl = up(rows * L_pad * 4);
+    const size_t bytes = 2 * bq + 2 * bv + ba + bl + fp.bytes;
+    char* ws = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), bytes, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LLA_ERR_NOMEM;
+    }
+    char* pq = ws;
+    char* pk = pq + bq;
+    char* pv = pk + bq;
+    char* po = pv + bv;
+    float* pa = reinterpret_cast<float*>(po + bv);
+    float* pl = reinterpret_cast<float*>(po + bv + ba);
+    char* fws = po + bv + ba + bl;
+    cudaError_t e = cudaSuccess;
+    auto chain = [&](cudaError_t x) {
+        if (e == cudaSuccess) e = x;
+    };
+    chain(lla::varlen_pack(esz, q, pq, cu_seqlens, n_seq, H, total_T, Tpad, dk, dk, max_T, err, s));
+    chain(lla::varlen_pack(esz, k, pk, cu_seqlens, n_seq, H, total_T, Tpad, dk, dk, max_T, err, s));
+    chain(lla::varlen_pack(esz, v, pv, cu_seqlens, n_seq, H, total_T, Tpad, dv, dv, max_T, err, s));
+    chain(lla::varlen_pack(4, log_a, pa, cu_seqlens, n_seq, H, total_T, Tpad, 1, 1, max_T, err, s));
+    chain(lla::varlen_pack(4, lambda, pl, cu_seqlens, n_seq, H, total_T, Tpad, L_in, L_pad, max_T, err, s));
+    if (e == cudaSuccess && run_forward(fp, pq, pk, pv, pa, pl, po, dtype, fws, err, s) != LLA_OK) e = cudaErrorUnknown;
+    chain(lla::varlen_unpack(esz, po, out, cu_seqlens, n_seq, H, total_T, Tpad, dv, max_T, err, s));
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
+}
+
+int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, const int32_t* cu_seqlens,
+                             float* fenwick_states, int n_seq, int H, int total_T, int max_T, int dk, int dv, int Lmax,
+                             void* stream, int dtype) {
+    if (!k || !v || !log_a || !cu_seqlens || !fenwick_states) return LLA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(log_a) || !aligned16(cu_seqlens) || !aligned16(fenwick_states))
+        return LLA_ERR_INVALID_ARG;
+    if (dtype != LLA_BF16 && dtype != LLA_F32) return LLA_ERR_INVALID_ARG;
+    if (n_seq < 1 || H < 1 || total_T < 1 || max_T < 1 || dk < 1 || dv < 1 || Lmax < 1 || Lmax > 40)
+        return LLA_ERR_INVALID_ARG;
+    if ((int64_t)n_seq * max_T < total_T) return LLA_ERR_INVALID_ARG;
+    if (lla::bitlength((int64_t)max_T - 1) + 1 > Lmax) return LLA_ERR_INVALID_ARG;
+    if (dk > 128 || dv > 128) return LLA_ERR_UNSUPPORTED;
+    if ((int64_t)n_seq * H > 65535 || (int64_t)H * total_T * (dk > dv ? dk : dv) > ((int64_t)1 << 40))
+        return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return LLA_ERR_CUDA;
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, (size_t)H * total_T * sizeof(float), pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LLA_ERR_NOMEM;
+    }
+    cudaError_t e = lla::prefill_state(dtype, k, v, log_a, fenwick_states, n_seq, H, max_T, dk, dv, Lmax, ws, err, s,
+                                       cu_seqlens, total_T);
     const cudaError_t f = cudaFreeAsync(ws, s);
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }

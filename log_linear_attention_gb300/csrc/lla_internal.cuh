@@ -97,8 +97,12 @@ cudaError_t tc_prefill_state(const void* k, const void* v, const float* log_a, f
 cudaError_t simt_forward(const SimtPlan& plan, int dtype, const void* q, const void* k, const void* v,
                          const float* log_a, const float* lambda, void* out, void* workspace, int* err,
                          cudaStream_t stream);
+// CUDA-core state set after a prefill. Dense: B sequences of T rows each. Packed (cu_seqlens
+// non-null, device int32 [B+1]): sequence b of head h has cu[b+1] - cu[b] <= T rows starting
+// at row h * total + cu[b]. Workspace: one float per row.
 cudaError_t prefill_state(int dtype, const void* k, const void* v, const float* log_a, float* states, int B, int H,
-                          int T, int dk, int dv, int Lmax, void* workspace, cudaStream_t stream);
+                          int T, int dk, int dv, int Lmax, void* workspace, int* err, cudaStream_t stream,
+                          const int32_t* cu_seqlens = nullptr, int total = 0);
 // The first half of the SIMT forward: chunk totals g and every fp32 pyramid node, laid out as
 // SimtPlan describes at the start of `workspace`.
 cudaError_t simt_nodes(const SimtPlan& plan, int dtype, const void* k, const void* v, const float* log_a,
@@ -116,6 +120,12 @@ bool make_bwd_plan(int B, int H, int T, int dk, int dv, int chunk, BwdPlan* plan
 cudaError_t simt_backward(const BwdPlan& plan, int dtype, const void* q, const void* k, const void* v,
                           const float* log_a, const float* lambda, const void* dout, void* dq, void* dk, void* dv,
                           float* dlog_a, float* dlambda, void* workspace, cudaStream_t stream);
+// Packed <-> padded copies for variable-length sequences (lla_varlen.cu); elem_bytes 2 = bf16, 4 = fp32.
+cudaError_t varlen_pack(int elem_bytes, const void* src, void* dst, const int32_t* cu, int n_seq, int H, int total,
+                        int Tpad, int W, int Wp, int max_len, int* err, cudaStream_t stream);
+cudaError_t varlen_unpack(int elem_bytes, const void* src, void* dst, const int32_t* cu, int n_seq, int H, int total,
+                          int Tpad, int W, int max_len, int* err, cudaStream_t stream);
+
 // dlog_a_r = sum_{t >= r} dcum_t per head (lla_bwd.cu).
 cudaError_t bwd_dloga(const float* dcum, float* dlog_a, int BH, int T, cudaStream_t stream);
 

@@ -469,22 +469,53 @@ __global__ void __launch_bounds__(kThreads) decode_kernel_fixed(const T* __restr
 
 // ---- state set after a prefill (hand-off to the decode step)
 
-// Per head: the decay exponent from each token s to the last token pos = T-1,
-// suf[s] = sum_{r=s+1..pos} log_a_r, accumulated from pos downwards (so the
+// Where the rows of sequence bh start and how many there are: every sequence has T rows
+// at bh * T (dense), or, with cu_seqlens, sequence b of head h has cu[b+1] - cu[b] rows
+// starting at h * total + cu[b] (packed). A packed length outside [0, T] or past
+// `total` is reported as bad input and treated as empty.
+struct SeqRows {
+    const int32_t* cu;
+    int T, H, total;
+    __device__ bool get(int bh, size_t& base, int& len, int* err) const {
+        if (!cu) {
+            base = static_cast<size_t>(bh) * T;
+            len = T;
+            return true;
+        }
+        const int b = bh / H, h = bh - b * H;
+        const int c0 = cu[b], c1 = cu[b + 1];
+        if (c0 < 0 || c1 < c0 || c1 > total || c1 - c0 > T) {
+            if (threadIdx.x == 0) record_error(err, kDevBadInput);
+            base = 0;
+            len = 0;
+            return false;
+        }
+        base = static_cast<size_t>(h) * total + c0;
+        len = c1 - c0;
+        return true;
+    }
+};
+
+// Per sequence: the decay exponent from each token s to the last token pos = len-1,
+// suf[base + s] = sum_{r=s+1..pos} log_a_r, accumulated from pos downwards (so the
 // values near pos, the ones that matter, carry the least rounding); also writes
 // slot 0 (k_pos v_pos^T) and zeroes the other slots the pieces add into.
-// grid (BH), 256 threads.
+// grid (sequences x heads), 256 threads.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) state_scan_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                                               const float* __restrict__ log_a, float* __restrict__ suf,
-                                                              float* __restrict__ states, int Tlen, int dk, int dv,
-                                                              int Lmax) {
+                                                              float* __restrict__ states, SeqRows rows, int dk, int dv,
+                                                              int Lmax, int* err) {
     __shared__ float carry_sh;
     __shared__ float tile[kThreads];
     const int bh = blockIdx.x, tid = threadIdx.x;
-    const float* a = log_a + (size_t)bh * Tlen;
-    float* sf = suf + (size_t)bh * Tlen;
-    const int pos = Tlen - 1;
+    size_t base;
+    int len;
+    rows.get(bh, base, len, err);
+    if (len == 0) return;  // an empty sequence holds no slot
+    const float* a = log_a + base;
+    float* sf = suf + base;
+    const int pos = len - 1;
     if (tid == 0) carry_sh = 0.f;
     __syncthreads();
     // blocks of 256 tokens from the end: suf[s] = carry + sum_{r in (s, block end]} log_a_r
@@ -509,31 +540,49 @@ __global__ void __launch_bounds__(kThreads) state_scan_kernel(const T* __restric
     const size_t msz = (size_t)dk * dv;
     float* st = states + (size_t)bh * Lmax * msz;
     for (int l = 1; l < Lmax; l++) {
-        if (((pos >> (l - 1)) & 1) == 0) continue;
+        if (l - 1 >= 31 || ((pos >> (l - 1)) & 1) == 0) continue;
         for (size_t e = tid; e < msz; e += kThreads) st[l * msz + e] = 0.f;
     }
-    const size_t r = (size_t)bh * Tlen + pos;
+    const size_t r = base + pos;
     for (size_t e = tid; e < msz; e += kThreads)
         st[e] = load_f(k + r * dk + e / dv) * load_f(v + r * dv + e % dv);
 }
 
-struct StatePieces {
-    static constexpr int kMax = 512;
-    int n;
-    int level[kMax], start[kMax], end[kMax];
-};
+constexpr int kPieceLen = 512;
 
-// One piece [start, end) of a Fenwick bucket of pos = T-1: adds
-// sum_s exp(suf[s]) k_s v_s^T into its slot. grid (npieces, BH, ceil(dk*dv / 2048)).
+// Piece idx of pos's Fenwick walk: buckets [b - lowbit(b), b) from b = pos down, each cut
+// into pieces of at most kPieceLen keys. Returns false when idx is past the last piece.
+__device__ bool fenwick_piece(int pos, int idx, int& level, int& s0, int& s1) {
+    int n = 0;
+    for (int b = pos; b > 0; b -= b & (-b)) {
+        const int low = b & (-b);
+        const int np = (low + kPieceLen - 1) / kPieceLen;
+        if (idx < n + np) {
+            level = 32 - __clz(low);  // log2(low) + 1
+            s0 = b - low + (idx - n) * kPieceLen;
+            s1 = min(s0 + kPieceLen, b);
+            return true;
+        }
+        n += np;
+    }
+    return false;
+}
+
+// One piece [start, end) of a Fenwick bucket of pos = len-1: adds
+// sum_s exp(suf[s]) k_s v_s^T into its slot. grid (pieces, sequences x heads, ceil(dk*dv / 2048)).
 template <typename T>
 __global__ void __launch_bounds__(kThreads) state_piece_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                                                const float* __restrict__ suf, float* __restrict__ states,
-                                                               int Tlen, int dk, int dv, int Lmax, StatePieces pc) {
+                                                               SeqRows rows, int dk, int dv, int Lmax, int* err) {
     __shared__ float ks[32][129];
     __shared__ float vs[32][128];
     const int tid = threadIdx.x;
-    const int piece = blockIdx.x, bh = blockIdx.y;
-    const int l = pc.level[piece], s0 = pc.start[piece], s1 = pc.end[piece];
+    const int bh = blockIdx.y;
+    size_t row0;
+    int len;
+    rows.get(bh, row0, len, err);
+    int l, s0, s1;
+    if (len < 2 || !fenwick_piece(len - 1, blockIdx.x, l, s0, s1)) return;
     const int msz = dk * dv;
     float acc[8];
     int ei[8], en[8];
@@ -544,7 +593,6 @@ __global__ void __launch_bounds__(kThreads) state_piece_kernel(const T* __restri
         ei[r] = (e < msz) ? e / dv : 0;
         en[r] = (e < msz) ? e % dv : 0;
     }
-    const size_t row0 = (size_t)bh * Tlen;
     for (int st = s0; st < s1; st += 32) {
         const int ns = min(32, s1 - st);
         for (int x = tid; x < ns * dk; x += kThreads) {
@@ -568,39 +616,21 @@ __global__ void __launch_bounds__(kThreads) state_piece_kernel(const T* __restri
 }
 
 template <typename T>
-cudaError_t prefill_state_t(const void* k, const void* v, const float* log_a, float* states, int B, int H, int T_,
-                            int dk, int dv, int Lmax, void* workspace, cudaStream_t stream) {
-    const int BH = B * H;
+cudaError_t prefill_state_t(const void* k, const void* v, const float* log_a, float* states, int n_seq, int H,
+                            SeqRows rows, int dk, int dv, int Lmax, void* workspace, int* err, cudaStream_t stream) {
+    const int BH = n_seq * H;
     float* suf = static_cast<float*>(workspace);
-    const int pos = T_ - 1;
-    // pieces of the buckets of pos's Fenwick walk, each at most `plen` tokens
-    StatePieces pc;
-    pc.n = 0;
-    int plen = 512;
-    while ((pos + plen - 1) / plen + 40 > StatePieces::kMax) plen *= 2;
-    for (int b = pos; b > 0; b -= b & (-b)) {
-        const int low = b & (-b);
-        int level = 1;
-        for (int w = low; w > 1; w >>= 1) level++;
-        for (int st = b - low; st < b; st += plen) {
-            pc.level[pc.n] = level;
-            pc.start[pc.n] = st;
-            pc.end[pc.n] = st + plen < b ? st + plen : b;
-            pc.n++;
-        }
-    }
+    // pieces of the longest walk: at most T / kPieceLen whole pieces plus one per bucket
+    const int max_pieces = rows.T / kPieceLen + 32;
     state_scan_kernel<T><<<BH, kThreads, 0, stream>>>(static_cast<const T*>(k), static_cast<const T*>(v), log_a, suf,
-                                                       states, T_, dk, dv, Lmax);
+                                                       states, rows, dk, dv, Lmax, err);
     note_launch(stream, "state_scan");
-    if (pc.n > 0) {
-        state_piece_kernel<T><<<dim3(pc.n, BH, (dk * dv + 2047) / 2048), kThreads, 0, stream>>>(
-            static_cast<const T*>(k), static_cast<const T*>(v), suf, states, T_, dk, dv, Lmax, pc);
-        note_launch(stream, "state_pieces");
-    }
+    state_piece_kernel<T><<<dim3(max_pieces, BH, (dk * dv + 2047) / 2048), kThreads, 0, stream>>>(
+        static_cast<const T*>(k), static_cast<const T*>(v), suf, states, rows, dk, dv, Lmax, err);
+    note_launch(stream, "state_pieces");
     return cudaGetLastError();
 }
 
-// Chunk totals g and the fp32 Fenwick pyramid of forward nodes (the first half of the forward).
 template <typename T>
 cudaError_t simt_nodes_t(const SimtPlan& pl, const T* k, const T* v, const float* log_a, void* workspace,
                          cudaStream_t stream) {
@@ -725,9 +755,12 @@ cudaError_t simt_nodes(const SimtPlan& pl, int dtype, const void* k, const void*
 }
 
 cudaError_t prefill_state(int dtype, const void* k, const void* v, const float* log_a, float* states, int B, int H,
-                          int T, int dk, int dv, int Lmax, void* workspace, cudaStream_t stream) {
-    if (dtype == 1) return prefill_state_t<float>(k, v, log_a, states, B, H, T, dk, dv, Lmax, workspace, stream);
-    return prefill_state_t<__nv_bfloat16>(k, v, log_a, states, B, H, T, dk, dv, Lmax, workspace, stream);
+                          int T, int dk, int dv, int Lmax, void* workspace, int* err, cudaStream_t stream,
+                          const int32_t* cu_seqlens, int total) {
+    SeqRows rows{cu_seqlens, T, H, total};
+    if (dtype == 1)
+        return prefill_state_t<float>(k, v, log_a, states, B, H, rows, dk, dv, Lmax, workspace, err, stream);
+    return prefill_state_t<__nv_bfloat16>(k, v, log_a, states, B, H, rows, dk, dv, Lmax, workspace, err, stream);
 }
 
 cudaError_t decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
