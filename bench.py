@@ -337,6 +337,52 @@ def cuda_time(fn, steps, stream):
     return start.elapsed_time(end)
 
 
+VARLEN = dict(n_seq=32, H=16, dk=128, dv=64, min_len=256, max_len=8192, chunk=64)
+
+
+def bench_varlen(args, dev, stream, rank):
+    """Packed prefill and hand-off of a serving-like mix: VARLEN["n_seq"] sequences with lengths
+    uniform in [min_len, max_len] (seeded), headline distributions, drawn on the device."""
+    import torch
+    from log_linear_attention_gb300 import binding
+    c = VARLEN
+    lengths = np.random.default_rng(1234 + rank).integers(c["min_len"], c["max_len"] + 1, size=c["n_seq"])
+    total, max_T = int(lengths.sum()), int(lengths.max())
+    H, dk, dv = c["H"], c["dk"], c["dv"]
+    L = inputs.num_levels(max_T)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321 + rank)
+    q = torch.randn((H, total, dk), device=dev, generator=g)
+    q = (q / q.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    k = torch.randn((H, total, dk), device=dev, generator=g)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn((H, total, dv), device=dev, generator=g).to(torch.bfloat16)
+    la = -torch.nn.functional.softplus(torch.randn((H, total), device=dev, generator=g) - 2.0)
+    lam = torch.nn.functional.softplus(torch.randn((H, total, L), device=dev, generator=g))
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)).to(dev)
+    out = torch.empty((H, total, dv), dtype=torch.bfloat16, device=dev)
+    states = torch.empty((c["n_seq"], H, L, dk, dv), dtype=torch.float32, device=dev)
+
+    def fstep():
+        binding.forward_varlen(q, k, v, la, lam, cu, max_T, c["chunk"], out=out)
+
+    def hstep():
+        binding.prefill_state_varlen(k, v, la, cu, max_T, states)
+
+    for _ in range(3):
+        fstep()
+        hstep()
+    n = max(3, min(args.steps, 10))
+    f_ms = cuda_time(fstep, n, stream) / n
+    h_ms = cuda_time(hstep, n, stream) / n
+    assert binding.device_error() == 0
+    return dict(workload=f"{c['n_seq']} packed sequences x {H} heads, lengths U[{c['min_len']},{c['max_len']}] "
+                         f"(total {total}, max {max_T}), dk={dk} dv={dv} bf16",
+                prefill_ms=f_ms, prefill_tokens_per_s=total / (f_ms / 1e3),
+                handoff_ms=h_ms, handoff_tokens_per_s=total / (h_ms / 1e3),
+                padding_overhead=c["n_seq"] * ((max_T + 127) // 128 * 128) / total)
+
+
 def bench_decode(args, dev, stream, rank, ws):
     """Time args.decode_steps one-token decode steps of the decode workload; returns
     (total ms, algorithmic bytes moved, steps)."""
@@ -418,6 +464,11 @@ def run_lla(args, cfg):
         assert binding.device_error() == 0
         if rank == 0:
             print(json.dumps({"mode": "backward", "config": cfg.name, "ms": b_ms, "steps": args.steps}))
+        return 0
+    if args.mode == "varlen":
+        vl = bench_varlen(args, dev, stream, rank)
+        if rank == 0:
+            print(json.dumps({"mode": "varlen", **vl}))
         return 0
     if args.mode == "handoff":
         # prefill -> decode hand-off launches only (a short target for profilers)
@@ -529,6 +580,7 @@ def run_lla(args, cfg):
     b_ms = cuda_time(bstep, n_b, stream) / n_b
     assert binding.device_error() == 0
     bw = backward_work(cfg)
+    vl = bench_varlen(args, dev, stream, rank)
     h_bytes = (cfg.B * cfg.H * cfg.T * ((cfg.dk + cfg.dv) * 2 + 4) + cfg.B * cfg.H * held * cfg.dk * cfg.dv * 4)
 
     line = None
@@ -566,6 +618,7 @@ def run_lla(args, cfg):
                          "gbs": bw["bytes"] / (b_ms / 1e3) / 1e9,
                          "frac_of_hbm": bw["bytes"] / (b_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                          "peak_source": peaks["source"]},
+            "varlen": vl,
             "e2e": {"value": ws * cfg.tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": {"value": cpu_val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -592,8 +645,8 @@ def main():
     ap.add_argument("--config", default="headline", choices=sorted(inputs.PREFILL_CONFIGS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--mode", choices=["all", "prefill", "decode", "handoff", "backward"], default="all",
-                    help="prefill / decode / handoff / backward: run only that workload's launches (profiling targets)")
+    ap.add_argument("--mode", choices=["all", "prefill", "decode", "handoff", "backward", "varlen"], default="all",
+                    help="prefill / decode / handoff / backward / varlen: run only that workload's launches (profiling targets)")
     args = ap.parse_args()
     cfg = inputs.PREFILL_CONFIGS[args.config]
     if args.impl == "reference":
