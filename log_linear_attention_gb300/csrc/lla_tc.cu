@@ -697,10 +697,33 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                         if (p2_p >= P) break;
                         p2_p++;
                         const int slot = gn % C::kNodeSlots;
+                        // Two levels in one MMA chain (N = 128, Q read once) when the next level's
+                        // node sits in the next ring slot (16 KB further: the B operand's panel
+                        // stride) and its TMEM level slot follows this one (slots 1.. are contiguous).
+                        int p_next = p2_p;
+                        while (p_next < P && ((j >> p_next) & 1) == 0) p_next++;
+                        const bool pair = DV == 64 && sl >= 1 && sl + 1 < C::kLvSlots && p_next < P &&
+                                          slot + 1 < C::kNodeSlots;
                         if (!wait(&node_full[slot], (gn / C::kNodeSlots) & 1)) return false;
+                        if (pair && !wait(&node_full[slot + 1], ((gn + 1) / C::kNodeSlots) & 1)) return false;
                         tc_fence_after();
                         const uint32_t nb = smem_u32(smem + C::kNodeBase + slot * C::kNodeBytes);
                         const uint32_t dcol = C::col_lv(b, sl);
+                        if (pair) {
+                            constexpr uint32_t kIdO2 = idesc_bf16(kTile, 2 * DV, 0, 1);
+#pragma unroll
+                            for (int kk = 0; kk < kDk / 16; kk++) {
+                                const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                                mma_bf16(tmem + dcol, sdesc(qb + aoff, 16, 1024),
+                                         sdesc(nb + kk * 2048, kPanelBytes, 1024), kIdO2, kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(&node_empty[slot]);
+                            mma_commit(&node_empty[slot + 1]);
+                            gn += 2;
+                            p2_p = p_next + 1;
+                            sl++;
+                            continue;
+                        }
 #pragma unroll
                         for (int kk = 0; kk < kDk / 16; kk++) {
                             const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
