@@ -224,7 +224,9 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
  * lla_prefill_state_varlen: the decode state set after every sequence, as
  * lla_prefill_state: fenwick_states [n_seq, H, Lmax, dk, dv] fp32 with
  * Lmax >= lla_num_levels(max_T); slots empty at a sequence's last position are
- * left untouched (an empty sequence touches none). CUDA-core kernels.
+ * left untouched (an empty sequence touches none). bf16 with dk = 128 and
+ * dv in {64, 128} runs the tensor-core hand-off over every sequence's own tile
+ * range; other shapes run CUDA-core kernels.
  */
 int lla_forward_varlen(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
                        void* out, const int32_t* cu_seqlens, int n_seq, int H, int total_T, int max_T, int dk, int dv,

@@ -370,13 +370,17 @@ int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaMemPool_t pool = workspace_pool(dev);
     if (!pool) return LLA_ERR_CUDA;
+    const bool tc = lla::tc_state_supported_packed(dtype, dk, dv, n_seq, H, total_T, max_T);
+    const size_t bytes = tc ? lla::tc_state_workspace_bytes(n_seq, H, max_T) : (size_t)H * total_T * sizeof(float);
     void* ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, (size_t)H * total_T * sizeof(float), pool, s) != cudaSuccess) {
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, s) != cudaSuccess) {
         cudaGetLastError();
         return LLA_ERR_NOMEM;
     }
-    cudaError_t e = lla::prefill_state(dtype, k, v, log_a, fenwick_states, n_seq, H, max_T, dk, dv, Lmax, ws, err, s,
-                                       cu_seqlens, total_T);
+    cudaError_t e = tc ? lla::tc_prefill_state(k, v, log_a, fenwick_states, n_seq, H, max_T, dv, Lmax, ws, err, s,
+                                               cu_seqlens, total_T)
+                       : lla::prefill_state(dtype, k, v, log_a, fenwick_states, n_seq, H, max_T, dk, dv, Lmax, ws,
+                                            err, s, cu_seqlens, total_T);
     const cudaError_t f = cudaFreeAsync(ws, s);
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }

@@ -88,10 +88,14 @@ cudaError_t tc_nodes_only(const TcPlan& plan, const void* k, const void* v, cons
                           int* err, cudaStream_t stream);
 
 // Tensor-core state set after a prefill (lla_tc_state.cu): bf16, dk = 128, dv in {64, 128}.
+// Dense: B sequences of T rows. Packed (cu non-null, device int32 [B+1]): sequence b of head h
+// has cu[b+1] - cu[b] <= T rows starting at row h * total + cu[b].
 bool tc_state_supported(int dtype, int dk, int dv, int B, int H, int T);
+bool tc_state_supported_packed(int dtype, int dk, int dv, int n_seq, int H, int total, int max_T);
 size_t tc_state_workspace_bytes(int B, int H, int T);
 cudaError_t tc_prefill_state(const void* k, const void* v, const float* log_a, float* states, int B, int H, int T,
-                             int dv, int Lmax, void* workspace, int* err, cudaStream_t stream);
+                             int dv, int Lmax, void* workspace, int* err, cudaStream_t stream,
+                             const int32_t* cu = nullptr, int total = 0);
 
 // SIMT launchers (lla_simt.cu).
 cudaError_t simt_forward(const SimtPlan& plan, int dtype, const void* q, const void* k, const void* v,

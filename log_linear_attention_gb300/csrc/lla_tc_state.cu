@@ -19,6 +19,8 @@
 //     time with the weights of the other levels (and of tokens past pos) zero.
 // Kernels (one stream, in order):
 //   state_tile_totals : g_u = sum of log_a over full tile u.
+//   state_offsets     : each sequence's first item in the flattened tile list
+//                       (sequences may have different lengths: packed input).
 //   state_prep        : per head, tail_u = sum of log_a from the end of tile u
 //                       to pos (reverse scan, newest first); other blocks
 //                       zero the slots held at pos.
@@ -42,17 +44,107 @@ namespace {
 constexpr int kPrepThreads = 256;
 constexpr int kMaxStateTiles = 8192;  // a head's tile totals staged in shared memory
 
-// grid (ceil(Pt / 8), BH), 256 threads: one warp per full tile.
+// The sequences whose state sets are built: dense (cu == nullptr: sequence bh has T rows
+// starting at row bh * T) or packed (sequence b of head h, bh = b * H + h, has
+// cu[b+1] - cu[b] <= T rows starting at row h * total + cu[b]; a length outside those
+// bounds is recorded as bad input and the sequence treated as empty). item_off[bh] is
+// the first item of sequence bh in the flattened tile list (state_offsets_kernel).
+struct StateSeqs {
+    const int32_t* cu;
+    int T, H, total;
+    const int* item_off;  // packed only
+    int nte;              // dense only: items of every sequence
+};
+
+// One sequence: first row, length, last position, full tiles before the tile of pos, and
+// the levels of the m virtual tiles over the tile of pos (0, then the held levels 1..7,
+// four bits each).
+struct SeqInfo {
+    int base, len, pos, Pt, m;
+    uint32_t packed;
+};
+
+// First item of sequence bh in the flattened list (bh = BH: all items).
+__device__ __forceinline__ int first_item(const StateSeqs& sq, int bh) {
+    return sq.cu ? sq.item_off[bh] : bh * sq.nte;
+}
+
+__device__ __forceinline__ SeqInfo seq_info(const StateSeqs& sq, int bh, int* err) {
+    SeqInfo si;
+    if (!sq.cu) {
+        si.base = bh * sq.T;
+        si.len = sq.T;
+    } else {
+        const int b = bh / sq.H, h = bh - b * sq.H;
+        const int c0 = sq.cu[b], c1 = sq.cu[b + 1];
+        if (c0 < 0 || c1 < c0 || c1 > sq.total || c1 - c0 > sq.T) {
+            if (err) record_error(err, kDevBadInput);
+            si.base = 0;
+            si.len = 0;
+        } else {
+            si.base = h * sq.total + c0;
+            si.len = c1 - c0;
+        }
+    }
+    si.pos = si.len - 1;
+    si.Pt = si.len > 0 ? si.pos >> 7 : 0;
+    si.m = 0;
+    si.packed = 0;
+    if (si.len > 0) {
+        si.m = 1;  // level 0 at bits 0..3
+        for (int l = 1; l <= 7; l++)
+            if ((si.pos >> (l - 1)) & 1) si.packed |= static_cast<uint32_t>(l) << (4 * si.m++);
+    }
+    return si;
+}
+
+// item_off[bh] = sum over earlier sequences of their items (full tiles + virtual tiles),
+// item_off[BH] = all items. One block of 1024 threads.
+__global__ void __launch_bounds__(1024) state_offsets_kernel(StateSeqs sq, int* __restrict__ item_off, int BH,
+                                                             int* err) {
+    __shared__ int warp_tot[32];
+    __shared__ int carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int b0 = 0; b0 < BH; b0 += 1024) {
+        const int bh = b0 + tid;
+        int n = 0;
+        if (bh < BH) {
+            const SeqInfo si = seq_info(sq, bh, err);
+            n = si.len > 0 ? si.Pt + si.m : 0;
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int before = carry;
+        for (int w = 0; w < warp; w++) before += warp_tot[w];
+        if (bh < BH) item_off[bh] = before + incl - n;
+        __syncthreads();
+        if (tid == 1023) carry = before + incl;
+        __syncthreads();
+    }
+    if (tid == 0) item_off[BH] = carry;
+}
+
+// g[item_off[bh] + u] = sum of log_a over full tile u of sequence bh.
+// grid (ceil(max Pt / 8), BH), 256 threads: one warp per full tile.
 __global__ void __launch_bounds__(256) state_tile_totals_kernel(const float* __restrict__ log_a,
-                                                                float* __restrict__ g, int T, int Pt) {
+                                                                float* __restrict__ g, StateSeqs sq) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u = blockIdx.x * 8 + warp, bh = blockIdx.y;
-    if (u >= Pt) return;
-    const float* a = log_a + static_cast<size_t>(bh) * T + static_cast<size_t>(u) * kTile;
+    const SeqInfo si = seq_info(sq, bh, nullptr);
+    if (u >= si.Pt) return;
+    const float* a = log_a + static_cast<size_t>(si.base) + static_cast<size_t>(u) * kTile;
     float s = a[lane] + a[lane + 32] + a[lane + 64] + a[lane + 96];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) g[static_cast<size_t>(bh) * Pt + u] = s;
+    if (lane == 0) g[first_item(sq, bh) + u] = s;
 }
 
 // Exclusive prefix sum over the 256 threads of the block.
@@ -75,17 +167,20 @@ __device__ __forceinline__ float block_excl_scan256(float x, float* warp_tot) {
 // Slot l is held at position pos: level 0 always, level l >= 1 when bit l - 1 of pos is set.
 __device__ __forceinline__ bool slot_held(int pos, int l) { return l == 0 || (l - 1 < 31 && ((pos >> (l - 1)) & 1)); }
 
-// grid (BH, 1 + Lmax), 256 threads, dynamic shared memory: Pt floats. Block y = 0 scans
-// the head's tile totals; block y = 1 + l zeroes slot l if it is held at pos (the MMA
-// kernel adds into it).
+// grid (BH, 1 + Lmax), 256 threads, dynamic shared memory: max Pt floats. Block y = 0
+// scans the sequence's tile totals into tail[item_off[bh] + u]; block y = 1 + l zeroes
+// slot l if it is held at pos (the MMA kernel adds into it).
 __global__ void __launch_bounds__(kPrepThreads)
     state_prep_kernel(const float* __restrict__ log_a, const float* __restrict__ g, float* __restrict__ tail,
-                      float* __restrict__ states, int T, int Pt, int Lmax, int msz) {
+                      float* __restrict__ states, StateSeqs sq, int Lmax, int msz) {
     extern __shared__ float g_sh[];
     __shared__ float warp_tot[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bh = blockIdx.x;
-    const int pos = T - 1;
+    const SeqInfo si = seq_info(sq, bh, nullptr);
+    if (si.len == 0) return;  // an empty sequence holds no slot
+    const int pos = si.pos, Pt = si.Pt;
+    const size_t off = first_item(sq, bh);
     if (blockIdx.y > 0) {
         const int l = blockIdx.y - 1;
         if (!slot_held(pos, l)) return;
@@ -95,7 +190,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
     const int base = Pt * kTile;     // first token of the tile of pos
     const int n = pos - base + 1;    // its tokens, 1..128
-    const float* a = log_a + static_cast<size_t>(bh) * T;
+    const float* a = log_a + static_cast<size_t>(si.base);
 
     // tail_u for every full tile, summed from pos backwards
     float ts = (tid < n) ? a[base + tid] : 0.f;
@@ -106,7 +201,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     float tail_tot = 0.f;
     for (int w = 0; w < 8; w++) tail_tot += warp_tot[w];
     __syncthreads();
-    for (int u = tid; u < Pt; u += kPrepThreads) g_sh[u] = g[static_cast<size_t>(bh) * Pt + u];
+    for (int u = tid; u < Pt; u += kPrepThreads) g_sh[u] = g[off + u];
     __syncthreads();
     // thread t owns the tiles [hi - C, hi), hi = Pt - t C: thread 0 the newest
     const int C = (Pt + kPrepThreads - 1) / kPrepThreads;
@@ -116,17 +211,10 @@ __global__ void __launch_bounds__(kPrepThreads)
     for (int u = hi - 1; u >= lo; u--) csum += g_sh[u];
     float run = tail_tot + block_excl_scan256(csum, warp_tot);
     for (int u = hi - 1; u >= lo; u--) {
-        tail[static_cast<size_t>(bh) * Pt + u] = run;
+        tail[off + u] = run;
         run += g_sh[u];
     }
 }
-
-// Levels of the m virtual tiles over the tile of pos: 0, then the held levels 1..7,
-// four bits each (tile j at bits 4j..4j+3).
-struct TailLevels {
-    int m;
-    uint32_t packed;
-};
 
 template <int DV>
 struct StateCfg {
@@ -151,13 +239,13 @@ __device__ __forceinline__ int tile_level(int u, int Pt, uint32_t tail_lev) {
 // scale V (two threads per token row, four 16-byte chunks of each 128-byte panel
 // row each; every warp derives the tile's decay prefix on its own, so the scaler
 // warps never wait for one another), warps 12..15 drain accumulators (TMEM lane quadrant = warp % 4, one
-// dk row per thread). Each head contributes NTe = Pt + tl.m tiles to the
-// flattened list.
+// dk row per thread). Sequence bh contributes Pt + m tiles to the flattened list,
+// starting at item_off[bh]; the CTAs take equal shares of item_off[BH] items.
 template <int DV>
 __global__ void __launch_bounds__(512, 1)
     tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, const float* __restrict__ tail, float* __restrict__ states,
-                    int T, int Pt, int Lmax, int total, const TailLevels tl, int* err) {
+                    StateSeqs sq, int BH, int Lmax, int* err) {
     using C = StateCfg<DV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -167,9 +255,7 @@ __global__ void __launch_bounds__(512, 1)
     __shared__ int fail_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int NTe = Pt + tl.m;
-    const int pos = T - 1;
-    const int base = Pt * kTile;  // first token of the tile of pos
+    const int total = first_item(sq, BH);
     const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
     const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
     volatile int* fail = &fail_sh;
@@ -197,30 +283,48 @@ __global__ void __launch_bounds__(512, 1)
     auto fail_now = [&]() {
         if (atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
     };
-    // Walk of this CTA's tiles without divisions: (bh, u) of tile f, its slot, and
-    // whether the next tile (f + 1 < t1) continues the same run.
+    // Walk of this CTA's tiles without divisions: sequence bh (and its SeqInfo), tile u of
+    // it, its slot, and whether the next tile (f + 1 < t1) continues the same run.
     struct Cursor {
         int bh, u, lvl;
+        SeqInfo si;
         bool last_of_run;
     };
     auto cursor_at = [&](int f) {
         Cursor c;
-        c.bh = f / NTe;
-        c.u = f % NTe;
-        c.lvl = tile_level(c.u, Pt, tl.packed);
+        // the sequence whose item range holds f: the last bh with first_item(bh) <= f
+        int lo = 0, hi = BH;
+        if (!sq.cu) {
+            lo = f / sq.nte < BH ? f / sq.nte : BH - 1;
+        } else {
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (sq.item_off[mid] <= f) lo = mid; else hi = mid;
+            }
+        }
+        c.bh = lo;
+        c.si = seq_info(sq, lo, nullptr);
+        c.u = f - first_item(sq, lo);
+        c.lvl = tile_level(c.u, c.si.Pt, c.si.packed);
         c.last_of_run = true;
         return c;
     };
     // advances c from tile f to f + 1 and fills c.last_of_run for tile f
     auto step = [&](Cursor& c, int f) {
-        int nbh = c.bh, nu = c.u + 1;
-        if (nu == NTe) {
-            nu = 0;
-            nbh++;
+        Cursor n = c;
+        n.u++;
+        if (n.u >= n.si.Pt + n.si.m) {
+            // next sequence with tiles (empty ones have none); stays in range while f + 1 < t1
+            n.u = 0;
+            do {
+                n.bh++;
+                n.si = seq_info(sq, n.bh < BH ? n.bh : BH - 1, nullptr);
+            } while (n.bh < BH - 1 && n.si.len == 0);
         }
-        const int nlvl = tile_level(nu, Pt, tl.packed);
-        c.last_of_run = (f + 1 >= t1) || nbh != c.bh || nlvl != c.lvl;
-        return Cursor{nbh, nu, nlvl, true};
+        n.lvl = tile_level(n.u, n.si.Pt, n.si.packed);
+        c.last_of_run = (f + 1 >= t1) || n.bh != c.bh || n.lvl != c.lvl;
+        n.last_of_run = true;
+        return n;
     };
 
     int issued = 0;  // producer: tiles whose copies were issued
@@ -234,9 +338,9 @@ __global__ void __launch_bounds__(512, 1)
                     fail_now();
                     break;
                 }
-                // rows of the tile of pos past the head's end are another head's (weight 0)
-                // or past the tensor (filled with zeros)
-                const int r0 = c.bh * T + (c.u < Pt ? c.u : Pt) * kTile;
+                // rows of the tile of pos past the sequence's end are another sequence's
+                // (weight 0) or past the tensor (filled with zeros)
+                const int r0 = c.si.base + (c.u < c.si.Pt ? c.u : c.si.Pt) * kTile;
                 uint8_t* st = smem + s * C::kStageBytes;
                 mbar_expect_tx(&full_bar[s], C::kTxBytes);
                 tma_load_2d(st, &tm_k, &full_bar[s], 0, r0);
@@ -303,31 +407,32 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp >= 4 && warp < 12) {
         const int sidx = tid - 128;
         const int row = sidx & 127, half = sidx >> 7, w4 = (warp - 4) & 3;
-        const int n_last = pos - base + 1;  // tokens of the tile of pos
         // log_a of the tile's tokens 32 j + lane (0 past pos), j = 0..3, and the tile's tail decay
         auto tile_inputs = [&](const Cursor& c, float* la, float& tlv) {
-            const size_t hb = static_cast<size_t>(c.bh) * T;
-            if (c.u < Pt) {
+            const size_t hb = static_cast<size_t>(c.si.base);
+            if (c.u < c.si.Pt) {
 #pragma unroll
                 for (int j = 0; j < 4; j++) la[j] = log_a[hb + static_cast<size_t>(c.u) * kTile + 32 * j + lane];
-                tlv = tail[static_cast<size_t>(c.bh) * Pt + c.u];
+                tlv = tail[first_item(sq, c.bh) + c.u];
             } else {
+                const int first = c.si.Pt * kTile, n_last = c.si.pos - first + 1;  // the tile of pos
 #pragma unroll
-                for (int j = 0; j < 4; j++) la[j] = 32 * j + lane < n_last ? log_a[hb + base + 32 * j + lane] : 0.f;
+                for (int j = 0; j < 4; j++) la[j] = 32 * j + lane < n_last ? log_a[hb + first + 32 * j + lane] : 0.f;
                 tlv = 0.f;
             }
         };
         // inputs are fetched two tiles ahead
         Cursor c0 = cursor_at(t0);
         Cursor c1 = step(c0, t0);
-        float la0[4], la1[4], tl0 = 0.f, tl1 = 0.f;
-        tile_inputs(c0, la0, tl0);
+        float la0[4] = {0.f, 0.f, 0.f, 0.f}, la1[4], tl0 = 0.f, tl1 = 0.f;
+        if (t0 < t1) tile_inputs(c0, la0, tl0);
         if (t0 + 1 < t1) tile_inputs(c1, la1, tl1);
         int s = 0;
         uint32_t ph = 0;
         for (int f = t0; f < t1; f++) {
             if (__any_sync(0xffffffffu, *fail != 0)) break;
             const int u = c0.u;
+            const SeqInfo si = c0.si;
             float x[4];
 #pragma unroll
             for (int j = 0; j < 4; j++) x[j] = la0[j];
@@ -360,9 +465,11 @@ __global__ void __launch_bounds__(512, 1)
             const float incl = before + (w4 == 0 ? x[0] : w4 == 1 ? x[1] : w4 == 2 ? x[2] : x[3]);
             // decay from token row to pos: the rest of the tile, then the tail
             float w = exp2f((tlv + tot - incl) * kLog2e);
-            if (u >= Pt) {
+            if (u >= si.Pt) {
                 // virtual tile: only the keys of its level, none past pos
-                const bool keep = row < n_last && fenwick_level(pos, base + row) == tile_level(u, Pt, tl.packed);
+                const int first = si.Pt * kTile;
+                const bool keep = row < si.pos - first + 1 &&
+                                  fenwick_level(si.pos, first + row) == tile_level(u, si.Pt, si.packed);
                 w = keep ? w : 0.f;
             }
             const int cs = s;
@@ -451,33 +558,38 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 template <int DV>
-cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a, float* states, int BH, int T,
-                                int Lmax, void* workspace, int* err, cudaStream_t stream) {
-    const int pos = T - 1;
-    const int Pt = pos >> 7;
-    float* g = static_cast<float*>(workspace);
-    float* tail = g + static_cast<size_t>(BH) * Pt;
-    TailLevels tl;
-    tl.m = 1;  // level 0 at bits 0..3
-    tl.packed = 0;
-    for (int l = 1; l <= 7; l++)
-        if ((pos >> (l - 1)) & 1) tl.packed |= static_cast<uint32_t>(l) << (4 * tl.m++);
-    if (Pt > 0) {
-        state_tile_totals_kernel<<<dim3((Pt + 7) / 8, BH), 256, 0, stream>>>(log_a, g, T, Pt);
+cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a, float* states, int BH, int H,
+                                int T, int Lmax, void* workspace, int* err, cudaStream_t stream, const int32_t* cu,
+                                int total) {
+    const int maxPt = (T - 1) >> 7;
+    const size_t off_bytes = (static_cast<size_t>(BH + 1) * sizeof(int) + 255) / 256 * 256;
+    int* item_off = static_cast<int*>(workspace);
+    float* g = reinterpret_cast<float*>(static_cast<char*>(workspace) + off_bytes);
+    float* tail = g + static_cast<size_t>(BH) * (maxPt + 8);
+    int nte = 0;  // dense: every sequence has the same items
+    if (!cu) {
+        const int pos = T - 1;
+        nte = (pos >> 7) + 1;
+        for (int l = 1; l <= 7; l++) nte += (pos >> (l - 1)) & 1;
+    }
+    const StateSeqs sq{cu, T, H, total, item_off, nte};
+    if (cu) state_offsets_kernel<<<1, 1024, 0, stream>>>(sq, item_off, BH, err);
+    if (maxPt > 0) {
+        state_tile_totals_kernel<<<dim3((maxPt + 7) / 8, BH), 256, 0, stream>>>(log_a, g, sq);
         note_launch(stream, "state_tile_totals");
     }
     {
-        const size_t smem = static_cast<size_t>(Pt) * sizeof(float);
+        const size_t smem = static_cast<size_t>(maxPt) * sizeof(float);
         cudaError_t e = cudaFuncSetAttribute(state_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        state_prep_kernel<<<dim3(BH, 1 + Lmax), kPrepThreads, smem, stream>>>(log_a, g, tail, states, T, Pt, Lmax,
+        state_prep_kernel<<<dim3(BH, 1 + Lmax), kPrepThreads, smem, stream>>>(log_a, g, tail, states, sq, Lmax,
                                                                              kDk * DV);
         note_launch(stream, "state_prep");
     }
     {
         CUtensorMap tk, tv;
-        const uint64_t rows = static_cast<uint64_t>(BH) * T;
+        const uint64_t rows = cu ? static_cast<uint64_t>(H) * total : static_cast<uint64_t>(BH) * T;
         if (!make_map(&tk, k, rows, kDk) || !make_map(&tv, v, rows, DV)) return cudaErrorInvalidValue;
         using C = StateCfg<DV>;
         cudaError_t e = cudaFuncSetAttribute(tc_state_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
@@ -488,10 +600,8 @@ cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a
             cudaGetLastError();
             sms = 152;
         }
-        const int total = BH * (Pt + tl.m);
-        const int grid = total < sms ? total : sms;
-        tc_state_kernel<DV><<<grid, C::kThreads, C::kBytes, stream>>>(tk, tv, log_a, tail, states, T, Pt, Lmax,
-                                                                       total, tl, err);
+        // the item count is only known on the device: one CTA per SM, each takes its share
+        tc_state_kernel<DV><<<sms, C::kThreads, C::kBytes, stream>>>(tk, tv, log_a, tail, states, sq, BH, Lmax, err);
         note_launch(stream, "tc_state");
     }
     return cudaGetLastError();
@@ -508,14 +618,25 @@ bool tc_state_supported(int dtype, int dk, int dv, int B, int H, int T) {
            static_cast<int64_t>(B) * H * T < (int64_t(1) << 31);
 }
 
+bool tc_state_supported_packed(int dtype, int dk, int dv, int n_seq, int H, int total, int max_T) {
+    const int64_t Pt = (static_cast<int64_t>(max_T) - 1) >> 7;
+    return dtype == 0 && dk == kDk && (dv == 64 || dv == 128) && Pt <= kMaxStateTiles &&
+           static_cast<int64_t>(H) * total >= kTile && static_cast<int64_t>(H) * total < (int64_t(1) << 31) &&
+           static_cast<int64_t>(n_seq) * H * (Pt + 8) < (int64_t(1) << 31);
+}
+
 size_t tc_state_workspace_bytes(int B, int H, int T) {
-    return 2 * static_cast<size_t>(B) * H * (static_cast<size_t>(T - 1) >> 7) * sizeof(float) + 256;
+    const size_t BH = static_cast<size_t>(B) * H;
+    return (static_cast<size_t>(BH + 1) * sizeof(int) + 255) / 256 * 256 +
+           2 * BH * ((static_cast<size_t>(T - 1) >> 7) + 8) * sizeof(float) + 256;
 }
 
 cudaError_t tc_prefill_state(const void* k, const void* v, const float* log_a, float* states, int B, int H, int T,
-                             int dv, int Lmax, void* workspace, int* err, cudaStream_t stream) {
-    if (dv == 64) return tc_prefill_state_dv<64>(k, v, log_a, states, B * H, T, Lmax, workspace, err, stream);
-    return tc_prefill_state_dv<128>(k, v, log_a, states, B * H, T, Lmax, workspace, err, stream);
+                             int dv, int Lmax, void* workspace, int* err, cudaStream_t stream, const int32_t* cu,
+                             int total) {
+    if (dv == 64)
+        return tc_prefill_state_dv<64>(k, v, log_a, states, B * H, H, T, Lmax, workspace, err, stream, cu, total);
+    return tc_prefill_state_dv<128>(k, v, log_a, states, B * H, H, T, Lmax, workspace, err, stream, cu, total);
 }
 
 }  // namespace lla
