@@ -16,7 +16,6 @@ namespace lla {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPerThread = 4;
 
 __device__ __forceinline__ bool seq_range(const int32_t* cu, int b, int total, int max_len, int& c0, int& len,
                                           int* err) {
@@ -31,52 +30,59 @@ __device__ __forceinline__ bool seq_range(const int32_t* cu, int b, int total, i
     return true;
 }
 
-// grid (ceil(Tpad * Wp / 1024), n * H), 256 threads, 4 elements each.
+// One warp per padded row: grid (ceil(Tpad / 8), n * H), 256 threads. Rows whose width
+// is a multiple of 16 bytes (and no column padding) move as 16-byte vectors; others
+// element by element.
 template <typename E>
 __global__ void __launch_bounds__(kThreads) pack_rows_kernel(const E* __restrict__ src, E* __restrict__ dst,
                                                              const int32_t* __restrict__ cu, int H, int total,
                                                              int Tpad, int W, int Wp, int max_len, int* err) {
     const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     int c0, len;
     seq_range(cu, b, total, max_len, c0, len, err);
-    const int64_t n = static_cast<int64_t>(Tpad) * Wp;
-    E* d = dst + static_cast<size_t>(bh) * n;
-    const E* s = src + (static_cast<size_t>(h) * total + c0) * W;
-#pragma unroll
-    for (int r = 0; r < kPerThread; r++) {
-        const int64_t e = (static_cast<int64_t>(blockIdx.x) * kPerThread + r) * kThreads + threadIdx.x;
-        if (e >= n) break;
-        const int t = static_cast<int>(e / Wp), w = static_cast<int>(e - static_cast<int64_t>(t) * Wp);
-        d[e] = (t < len && w < W) ? s[static_cast<size_t>(t) * W + w] : E(0.f);
+    if (t >= Tpad) return;
+    E* d = dst + (static_cast<size_t>(bh) * Tpad + t) * Wp;
+    const E* s = src + (static_cast<size_t>(h) * total + c0 + t) * W;
+    const bool live = t < len;
+    if (W == Wp && (W * sizeof(E)) % 16 == 0) {
+        const int nv = W * static_cast<int>(sizeof(E)) / 16;
+        uint4* d4 = reinterpret_cast<uint4*>(d);
+        const uint4* s4 = reinterpret_cast<const uint4*>(s);
+        for (int c = lane; c < nv; c += 32) d4[c] = live ? s4[c] : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+        for (int w = lane; w < Wp; w += 32) d[w] = (live && w < W) ? s[w] : E(0.f);
     }
 }
 
-// The inverse for the outputs: packed row cu[b] + t of head h <- padded row t of (b, h), t < len_b.
+// The inverse for the outputs: packed row cu[b] + t of head h <- padded row t of (b, h),
+// t < len_b; same grid and vector rule.
 template <typename E>
 __global__ void __launch_bounds__(kThreads) unpack_rows_kernel(const E* __restrict__ src, E* __restrict__ dst,
                                                                const int32_t* __restrict__ cu, int H, int total,
                                                                int Tpad, int W, int max_len, int* err) {
     const int bh = blockIdx.y, b = bh / H, h = bh - b * H;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     int c0, len;
     seq_range(cu, b, total, max_len, c0, len, err);
-    const int64_t n = static_cast<int64_t>(len) * W;
-    const E* s = src + static_cast<size_t>(bh) * Tpad * W;
-    E* d = dst + (static_cast<size_t>(h) * total + c0) * W;
-#pragma unroll
-    for (int r = 0; r < kPerThread; r++) {
-        const int64_t e = (static_cast<int64_t>(blockIdx.x) * kPerThread + r) * kThreads + threadIdx.x;
-        if (e >= n) break;
-        d[e] = s[e];
+    if (t >= len) return;
+    const E* s = src + (static_cast<size_t>(bh) * Tpad + t) * W;
+    E* d = dst + (static_cast<size_t>(h) * total + c0 + t) * W;
+    if ((W * sizeof(E)) % 16 == 0) {
+        const int nv = W * static_cast<int>(sizeof(E)) / 16;
+        for (int c = lane; c < nv; c += 32) reinterpret_cast<uint4*>(d)[c] = reinterpret_cast<const uint4*>(s)[c];
+    } else {
+        for (int w = lane; w < W; w += 32) d[w] = s[w];
     }
 }
 
 template <typename E>
 cudaError_t pack_t(const void* src, void* dst, const int32_t* cu, int n_seq, int H, int total, int Tpad, int W,
                    int Wp, int max_len, int* err, cudaStream_t stream) {
-    const int64_t per = static_cast<int64_t>(Tpad) * Wp;
-    const int64_t blocks = (per + kThreads * kPerThread - 1) / (kThreads * kPerThread);
-    if (blocks > 0x7fffffff || n_seq * H > 65535) return cudaErrorInvalidValue;
-    pack_rows_kernel<E><<<dim3(static_cast<unsigned>(blocks), n_seq * H), kThreads, 0, stream>>>(
+    if (n_seq * H > 65535) return cudaErrorInvalidValue;
+    pack_rows_kernel<E><<<dim3((Tpad + 7) / 8, n_seq * H), kThreads, 0, stream>>>(
         static_cast<const E*>(src), static_cast<E*>(dst), cu, H, total, Tpad, W, Wp, max_len, err);
     return cudaGetLastError();
 }
@@ -84,10 +90,8 @@ cudaError_t pack_t(const void* src, void* dst, const int32_t* cu, int n_seq, int
 template <typename E>
 cudaError_t unpack_t(const void* src, void* dst, const int32_t* cu, int n_seq, int H, int total, int Tpad, int W,
                      int max_len, int* err, cudaStream_t stream) {
-    const int64_t per = static_cast<int64_t>(max_len) * W;
-    const int64_t blocks = (per + kThreads * kPerThread - 1) / (kThreads * kPerThread);
-    if (blocks > 0x7fffffff || n_seq * H > 65535) return cudaErrorInvalidValue;
-    unpack_rows_kernel<E><<<dim3(static_cast<unsigned>(blocks), n_seq * H), kThreads, 0, stream>>>(
+    if (n_seq * H > 65535) return cudaErrorInvalidValue;
+    unpack_rows_kernel<E><<<dim3((max_len + 7) / 8, n_seq * H), kThreads, 0, stream>>>(
         static_cast<const E*>(src), static_cast<E*>(dst), cu, H, total, Tpad, W, max_len, err);
     return cudaGetLastError();
 }
