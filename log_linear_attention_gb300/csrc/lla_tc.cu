@@ -585,14 +585,13 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                 bulk_load(st + C::kCl2, tok_cl2 + row0, 512, &in_full[s]);
                 bulk_load(st + C::kColw, tok_colw + row0, 512, &in_full[s]);
             }
-            // lambda_t^(0..7) of the tile's 128 rows (rows are L floats apart, not 16-byte aligned)
+            // lambda_t^(0..7) of the tile's 128 rows (rows are L floats apart, not 16-byte aligned);
+            // consecutive lanes fill consecutive words of lam8[t][l] (no bank conflicts)
             float* lam8 = reinterpret_cast<float*>(st + C::kLam8);
-#pragma unroll
-            for (int rr = 0; rr < 4; rr++) {
-                const int t = lane * 4 + rr;
-                const float* src = lambda + static_cast<size_t>(row0 + t) * L;
-#pragma unroll
-                for (int l = 0; l < 8; l++) cp_async4(lam8 + t * 8 + l, src + l);
+#pragma unroll 8
+            for (int i = 0; i < 32; i++) {
+                const int x = lane + 32 * i, t = x >> 3, l = x & 7;
+                cp_async4(lam8 + x, lambda + static_cast<size_t>(row0 + t) * L + l);
             }
             cp_async_arrive(&in_full[s]);
             __syncwarp();
