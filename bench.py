@@ -154,8 +154,11 @@ def traffic_record(name: str):
             parts = line.split()
             if not parts or parts[0].startswith("#") or parts[0] != name or len(parts) != 4:
                 continue
-            src = os.path.join(ROOT, parts[1])
-            if hashlib.sha256(open(src, "rb").read()).hexdigest() != parts[2]:
+            # the kernel's source files, '+'-joined: their concatenation is what was hashed
+            h = hashlib.sha256()
+            for src in parts[1].split("+"):
+                h.update(open(os.path.join(ROOT, src), "rb").read())
+            if h.hexdigest() != parts[2]:
                 return None
             return float(parts[3])
     except OSError:
