@@ -129,8 +129,10 @@ def forward(q, k, v, log_a, lam, chunk: int, out=None, stream=None, workspace=No
     torch = _torch()
     host = not q.is_cuda
     if host:
+        # inputs copied on the stream the kernels run on (asynchronous from pinned memory)
         dev = torch.device("cuda", torch.cuda.current_device())
-        q, k, v, log_a, lam = (x.to(dev, non_blocking=True) for x in (q, k, v, log_a, lam))
+        with torch.cuda.stream(torch.cuda.current_stream() if stream is None else stream):
+            q, k, v, log_a, lam = (x.to(dev, non_blocking=True) for x in (q, k, v, log_a, lam))
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda")):
@@ -158,7 +160,14 @@ def forward(q, k, v, log_a, lam, chunk: int, out=None, stream=None, workspace=No
         _call(lib.lla_forward_ws(*args, workspace.data_ptr(), workspace.numel() * workspace.element_size()),
               "lla_forward_ws")
     if host:
-        return out.to("cpu")
+        # pinned host output (torch's caching host allocator reuses the block), copied on
+        # the call's stream and complete on return
+        res = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        cs = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(cs):
+            res.copy_(out, non_blocking=True)
+        cs.synchronize()
+        return res
     return out
 
 
