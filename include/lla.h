@@ -85,6 +85,20 @@ int lla_num_levels(int64_t T);
 int lla_forward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
                 void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype);
 
+/*
+ * lla_forward with HOST buffers (pinned for full copy bandwidth; pageable works,
+ * slower): same arguments and layouts as lla_forward, but q, k, v, log_a, lambda
+ * and out live in host memory (device or managed pointers: LLA_ERR_INVALID_ARG).
+ * The B*H heads are split into up to eight groups; each group's inputs are copied
+ * to the device on a library copy stream, its prefill runs on `stream`, and its
+ * output is copied back on a second library stream, so copies of one group
+ * overlap the kernels of the next. Device buffers come from the library pool.
+ * The call returns after `out` is written (it synchronizes `stream`). Calls on
+ * one device are serialized.
+ */
+int lla_forward_host(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                     void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype);
+
 /* Workspace bytes lla_forward_ws needs for these sizes (0 on invalid sizes). */
 size_t lla_forward_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype);
 

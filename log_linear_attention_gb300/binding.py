@@ -51,6 +51,8 @@ def load() -> ctypes.CDLL:
             lib.lla_forward.restype = i
             lib.lla_forward_workspace_size.argtypes = [i] * 7
             lib.lla_forward_workspace_size.restype = sz
+            lib.lla_forward_host.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i]
+            lib.lla_forward_host.restype = i
             lib.lla_forward_ws.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i, vp, sz]
             lib.lla_forward_ws.restype = i
             lib.lla_forward_noalloc.argtypes = [vp, vp, vp, fp, fp, vp] + [i] * 6 + [vp, i]
@@ -122,17 +124,13 @@ def forward(q, k, v, log_a, lam, chunk: int, out=None, stream=None, workspace=No
     """Chunk-parallel prefill, lla_forward / lla_forward_ws.
 
     q, k [B,H,T,dk]; v [B,H,T,dv] (bf16 or fp32, same dtype); log_a [B,H,T] fp32;
-    lam [B,H,T,L] fp32 with L = num_levels(T). Host (CPU) inputs are copied to the
-    current device first and the result is copied back (the end-to-end path).
+    lam [B,H,T,L] fp32 with L = num_levels(T). Host (CPU) inputs go through
+    lla_forward_host (pipelined copies in and out) and the result comes back in host memory.
     ``workspace``: optional uint8 CUDA tensor of at least workspace_size(...) bytes.
     """
     torch = _torch()
-    host = not q.is_cuda
-    if host:
-        # inputs copied on the stream the kernels run on (asynchronous from pinned memory)
-        dev = torch.device("cuda", torch.cuda.current_device())
-        with torch.cuda.stream(torch.cuda.current_stream() if stream is None else stream):
-            q, k, v, log_a, lam = (x.to(dev, non_blocking=True) for x in (q, k, v, log_a, lam))
+    if not q.is_cuda:
+        return _forward_host(q, k, v, log_a, lam, chunk, out, stream)
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda")):
@@ -159,15 +157,30 @@ def forward(q, k, v, log_a, lam, chunk: int, out=None, stream=None, workspace=No
         _check(workspace, "workspace", q.device)
         _call(lib.lla_forward_ws(*args, workspace.data_ptr(), workspace.numel() * workspace.element_size()),
               "lla_forward_ws")
-    if host:
-        # pinned host output (torch's caching host allocator reuses the block), copied on
-        # the call's stream and complete on return
-        res = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        cs = torch.cuda.current_stream() if stream is None else stream
-        with torch.cuda.stream(cs):
-            res.copy_(out, non_blocking=True)
-        cs.synchronize()
-        return res
+    return out
+
+
+def _forward_host(q, k, v, log_a, lam, chunk, out=None, stream=None):
+    """lla_forward_host: every tensor in host memory (pinned for full copy bandwidth). The
+    library copies head groups in, runs them and copies them out with the copies of one group
+    overlapping the kernels of the next; returns the host output (pinned unless given)."""
+    torch = _torch()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (lam, "lambda")):
+        if t_.is_cuda or not t_.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host tensor")
+    if k.dtype != q.dtype or v.dtype != q.dtype or log_a.dtype != torch.float32 or lam.dtype != torch.float32:
+        raise TypeError("q, k, v share one dtype; log_a and lambda are float32")
+    if k.shape != q.shape or v.shape[:3] != (B, H, T) or log_a.shape != (B, H, T) or lam.shape != (B, H, T, num_levels(T)):
+        raise ValueError("shape mismatch between q, k, v, log_a and lambda")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, pin_memory=True)
+    if out.is_cuda or not out.is_contiguous() or out.shape != (B, H, T, dv) or out.dtype != q.dtype:
+        raise ValueError("out must be a contiguous host tensor [B,H,T,dv] of q's dtype")
+    _call(load().lla_forward_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(),
+                                  out.data_ptr(), B, H, T, dk, dv, int(chunk), _stream_handle(stream),
+                                  _dtype_code(q)), "lla_forward_host")
     return out
 
 

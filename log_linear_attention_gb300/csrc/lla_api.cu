@@ -55,6 +55,30 @@ cudaMemPool_t workspace_pool(int dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// lla_forward_host: per device, one copy-in and one copy-out stream and the events that
+// order a chunk's copies and kernels; one call at a time per device.
+std::mutex g_host_mutex[kMaxDevices];
+cudaStream_t g_copy_in[kMaxDevices], g_copy_out[kMaxDevices];
+cudaEvent_t g_host_events[kMaxDevices][7];
+bool g_host_ready[kMaxDevices];
+
+bool host_streams_ready(int dev) {
+    if (g_host_ready[dev]) return true;
+    if (cudaStreamCreateWithFlags(&g_copy_in[dev], cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&g_copy_out[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    for (int i = 0; i < 7; i++) {
+        if (cudaEventCreateWithFlags(&g_host_events[dev][i], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+    }
+    g_host_ready[dev] = true;
+    return true;
+}
+
 struct ForwardPlan {
     bool tc;
     lla::TcPlan tcp;
@@ -174,6 +198,109 @@ int lla_forward(const void* q, const void* k, const void* v, const float* log_a,
     st = run_forward(fp, q, k, v, log_a, lambda, out, dtype, ws, err, s);
     if (ws && cudaFreeAsync(ws, s) != cudaSuccess && st == LLA_OK) st = LLA_ERR_CUDA;
     return st;
+}
+
+int lla_forward_host(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                     void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype) {
+    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    // the buffers must be host memory (pinned or pageable)
+    for (const void* p : {q, k, v, static_cast<const void*>(log_a), static_cast<const void*>(lambda),
+                          static_cast<const void*>(out)}) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            cudaGetLastError();
+            return LLA_ERR_INVALID_ARG;
+        }
+        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return LLA_ERR_INVALID_ARG;
+    }
+    const int BH = B * H;
+    // head groups of G consecutive (b, h) heads: [BH, T, .] rows, contiguous per group
+    const int nchunks = BH < 8 ? BH : 8;
+    const int G = (BH + nchunks - 1) / nchunks;
+    ForwardPlan fp;
+    if (!plan_forward(1, G, T, dk, dv, chunk, dtype, &fp)) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_host_mutex[dev]);
+    if (!host_streams_ready(dev)) return LLA_ERR_CUDA;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t in_s = g_copy_in[dev], out_s = g_copy_out[dev];
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return LLA_ERR_CUDA;
+    const size_t esz = dtype == LLA_BF16 ? 2 : 4;
+    const int L = lla_num_levels(T);
+    const size_t rq = (size_t)T * dk * esz, rv = (size_t)T * dv * esz, ra = (size_t)T * 4, rl = (size_t)T * L * 4;
+    auto up = [](size_t x) { return (x + 1023) / 1024 * 1024; };
+    const size_t slot_bytes = 2 * up(G * rq) + 2 * up(G * rv) + up(G * ra) + up(G * rl);
+    char* buf = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), 2 * slot_bytes + fp.bytes, pool, cs) != cudaSuccess) {
+        cudaGetLastError();
+        return LLA_ERR_NOMEM;
+    }
+    cudaEvent_t* ev = g_host_events[dev];
+    cudaError_t e = cudaEventRecord(ev[6], cs);  // the buffers exist from here on
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(in_s, ev[6], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(out_s, ev[6], 0);
+    char* ws = buf + 2 * slot_bytes;
+    const char* hq = static_cast<const char*>(q);
+    const char* hk = static_cast<const char*>(k);
+    const char* hv = static_cast<const char*>(v);
+    const char* ha = reinterpret_cast<const char*>(log_a);
+    const char* hl = reinterpret_cast<const char*>(lambda);
+    char* ho = static_cast<char*>(out);
+    for (int c = 0; c < nchunks && e == cudaSuccess; c++) {
+        const int h0 = c * G, g = (BH - h0) < G ? (BH - h0) : G;
+        if (g <= 0) break;
+        const int slot = c & 1;
+        char* sb = buf + slot * slot_bytes;
+        char* dq = sb;
+        char* dk_ = dq + up(G * rq);
+        char* dv_ = dk_ + up(G * rq);
+        char* dout = dv_ + up(G * rv);
+        char* da = dout + up(G * rv);
+        char* dl = da + up(G * ra);
+        // the slot's previous chunk has been copied out (and so computed) before it is refilled
+        if (c >= 2) e = cudaStreamWaitEvent(in_s, ev[4 + slot], 0);
+        auto h2d = [&](char* d, const char* h, size_t row) {
+            if (e == cudaSuccess) e = cudaMemcpyAsync(d, h + (size_t)h0 * row, (size_t)g * row, cudaMemcpyHostToDevice, in_s);
+        };
+        h2d(dq, hq, rq);
+        h2d(dk_, hk, rq);
+        h2d(dv_, hv, rv);
+        h2d(da, ha, ra);
+        h2d(dl, hl, rl);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[slot], in_s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev[slot], 0);
+        if (e != cudaSuccess) break;
+        ForwardPlan fg = fp;
+        if (g != G && !plan_forward(1, g, T, dk, dv, chunk, dtype, &fg)) {
+            e = cudaErrorInvalidValue;
+            break;
+        }
+        if (run_forward(fg, dq, dk_, dv_, reinterpret_cast<float*>(da), reinterpret_cast<float*>(dl), dout, dtype, ws,
+                        err, cs) != LLA_OK) {
+            e = cudaErrorLaunchFailure;
+            break;
+        }
+        e = cudaEventRecord(ev[2 + slot], cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(out_s, ev[2 + slot], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(ho + (size_t)h0 * rv, dout, (size_t)g * rv, cudaMemcpyDeviceToHost, out_s);
+        if (e == cudaSuccess) e = cudaEventRecord(ev[4 + slot], out_s);
+    }
+    // everything has landed in host memory before the buffers go back to the pool
+    const cudaError_t s1 = cudaStreamSynchronize(out_s);
+    const cudaError_t s2 = cudaStreamSynchronize(in_s);
+    const cudaError_t f = cudaFreeAsync(buf, cs);
+    const cudaError_t s3 = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess || s1 != cudaSuccess || s2 != cudaSuccess || f != cudaSuccess || s3 != cudaSuccess) {
+        cudaGetLastError();
+        return LLA_ERR_CUDA;
+    }
+    return LLA_OK;
 }
 
 int lla_forward_profile(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,

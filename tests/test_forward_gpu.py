@@ -154,3 +154,25 @@ def test_full_size_sampled_rows(name):
         ref = oracle.explicit_rows(inp.q, inp.k, inp.v, inp.log_a, inp.lam, b, h, rows)
         err = np.abs(got[b, h, rows] - ref).max() / np.abs(ref).max()
         assert err <= TOL_BF16, (b, h, err)
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,dtype,chunk", [(1, 5, 256, 128, 64, "bf16", 64), (2, 3, 96, 16, 24, "f32", 32)])
+def test_host_buffers_match_device_path(B, H, T, dk, dv, dtype, chunk):
+    """lla_forward_host (head groups copied in, run and copied out on separate streams) gives
+    the device path's result exactly, from pageable inputs into a pinned output."""
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.PrefillConfig("host", B, H, T, dk, dv, chunk, dtype)
+    inp = inputs.make_prefill(cfg, seed=5)
+    dev = to_device(inp)
+    ref = binding.forward(*dev, chunk).cpu()
+    host = [x.cpu() for x in dev]
+    out = torch.empty(ref.shape, dtype=ref.dtype, pin_memory=True)
+    got = binding.forward(*host, chunk, out=out)
+    assert got.data_ptr() == out.data_ptr()
+    assert torch.equal(got, ref)
+    with pytest.raises(binding.LLAError):
+        binding.load()
+        st = binding.load().lla_forward_host(dev[0].data_ptr(), host[1].data_ptr(), host[2].data_ptr(),
+                                             host[3].data_ptr(), host[4].data_ptr(), out.data_ptr(), B, H, T, dk, dv,
+                                             chunk, None, binding.LLA_BF16 if dtype == "bf16" else binding.LLA_F32)
+        binding._call(st, "lla_forward_host")
