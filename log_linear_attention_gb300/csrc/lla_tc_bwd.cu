@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(256, 1)
     __shared__ float lamp[kTile][16];
     __shared__ float dlam8[kTile][8];
     __shared__ float dlamp[kTile][16];
-    __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile];
+    __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile], colw_sh[kTile];
     __shared__ float dtab_sh[16];
     __shared__ int fail_sh;
 
@@ -460,15 +460,32 @@ __global__ void __launch_bounds__(256, 1)
             node_issued = 1;
         }
     }
-    // per-row inputs: decay prefix, lambda levels, the tile's level decay row
-    if (tid < kTile) cl2_sh[tid] = tok_cl2[r0 + tid];
-    for (int x = tid; x < kTile * L; x += blockDim.x) {
-        const int row = x / L, l = x - row * L;
-        const float val = lambda[static_cast<size_t>(r0) * L + x];
-        if (l < 8) lam8[row][l] = val;
-        else if (l < 24) lamp[row][l - 8] = val;
+    // per-row inputs: decay prefix, lambda levels, the tile's level decay row. The tile's
+    // lambda rows are one contiguous block of 128 L floats (L <= 32): every load is issued
+    // before any is used.
+    {
+        const float* lsrc = lambda + static_cast<size_t>(r0) * L;
+        const int n = kTile * L;
+        float lv[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const int x = tid + i * 256;
+            lv[i] = x < n ? lsrc[x] : 0.f;
+        }
+        const float c2 = tid < kTile ? tok_cl2[r0 + tid] : 0.f;
+        const float dt = tid < 16 ? dtab[(static_cast<size_t>(bh) * NT + j) * 16 + tid] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const int x = tid + i * 256;
+            if (x < n) {
+                const int row = x / L, l = x - row * L;
+                if (l < 8) lam8[row][l] = lv[i];
+                else if (l < 24) lamp[row][l - 8] = lv[i];
+            }
+        }
+        if (tid < kTile) cl2_sh[tid] = c2;
+        if (tid < 16) dtab_sh[tid] = dt;
     }
-    if (tid < 16) dtab_sh[tid] = dtab[(static_cast<size_t>(bh) * NT + j) * 16 + tid];
     for (int x = tid; x < kTile * 8; x += blockDim.x) (&dlam8[0][0])[x] = 0.f;
     for (int x = tid; x < kTile * 16; x += blockDim.x) (&dlamp[0][0])[x] = 0.f;
     if (tid < kTile) {
@@ -478,6 +495,8 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();
 
+    // decay from each key to the end of its 32-key block (the factorised decay of E1)
+    if (tid < kTile) colw_sh[tid] = exp2f(cl2_sh[tid | 31] - cl2_sh[tid]);
     // ok stays block-uniform: every change goes through a barrier reduction
     bool ok = __syncthreads_and(ok_wait(&bar_in, 0));
     // ---- S = Q K^T, dP = dO V^T
@@ -518,6 +537,32 @@ __global__ void __launch_bounds__(256, 1)
                 for (int e = 0; e < 32; e++) ev[e] = 0.f;
 #pragma unroll
                 for (int e = 0; e < 16; e++) pa[e] = pg[e] = 0u;
+            } else if (cb < quad * 32) {
+                // every key of the chunk precedes every row of this warp: one level per row
+                // (t and s differ first in bit 5 or 6) and decay exp2(cl_t - cl_end) colw[s]
+                float sv[32], dpv[32];
+                tmem_ld32(tmem + lane_base + C::kS + cb, sv);
+                tmem_ld32(tmem + lane_base + C::kDP + cb, dpv);
+                const int l = 32 - __clz(t ^ cb);
+                float lm = lam8[t][0];
+#pragma unroll
+                for (int ll = 1; ll < 8; ll++) lm = (l == ll) ? lam8[t][ll] : lm;
+                const float rowf = exp2f(cl2_t - cl2_sh[cb + 31]);
+                float dsum = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float D0 = rowf * colw_sh[cb + e], D1 = rowf * colw_sh[cb + e + 1];
+                    const float s0 = D0 * sv[e], s1 = D1 * sv[e + 1];
+                    const float q0 = s0 * dpv[e], q1 = s1 * dpv[e + 1];
+                    dsum += q0 + q1;
+                    ev[e] = lm * q0;
+                    ev[e + 1] = lm * q1;
+                    pa[e >> 1] = pack_bf16(lm * s0, lm * s1);
+                    pg[e >> 1] = pack_bf16(lm * D0 * dpv[e], lm * D1 * dpv[e + 1]);
+                }
+                rowE += lm * dsum;
+#pragma unroll
+                for (int ll = 0; ll < 8; ll++) dl[ll] += (l == ll) ? dsum : 0.f;
             } else {
                 float sv[32], dpv[32];
                 tmem_ld32(tmem + lane_base + C::kS + cb, sv);
