@@ -390,6 +390,8 @@ __global__ void __launch_bounds__(256, 1)
     tc_bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_nodes, const __grid_constant__ CUtensorMap tm_cmat,
+                       const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                       const __grid_constant__ CUtensorMap tm_dv,
                        const float* __restrict__ lambda, const float* __restrict__ tok_cl2,
                        const float* __restrict__ dtab, __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
                        __nv_bfloat16* __restrict__ dv, float* __restrict__ dlambda, float* __restrict__ dcum, int T,
@@ -805,38 +807,48 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- outputs
+    // ---- outputs: dQ, dK, dV (bf16) into the now free A, G and r o dO areas in the TMA
+    // layout, then written by tensor stores; the decay derivative per row
     if (ok) {
         const size_t row = static_cast<size_t>(r0) + t;
         float x[32];
+        auto put = [&](uint8_t* panel, int ch0) {
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                *reinterpret_cast<uint4*>(panel + sw128_off(t, ch0 + q)) =
+                    make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
+                               pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+        };
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
             tmem_ld32(tmem + lane_base + C::kDQ + 64 * half + c0, x);
-            uint4* d4 = reinterpret_cast<uint4*>(dq + row * kDk + 64 * half + c0);
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
-                                   pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+            put(smem + C::kA + half * kPanelBytes, c0 >> 3);
             tmem_ld32(tmem + lane_base + C::kDK + 64 * half + c0, x);
-            d4 = reinterpret_cast<uint4*>(dk + row * kDk + 64 * half + c0);
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
-                                   pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+            put(smem + C::kG + half * kPanelBytes, c0 >> 3);
         }
         tmem_ld32(tmem + lane_base + C::kDVc + 32 * half, x);
-        uint4* d4 = reinterpret_cast<uint4*>(dv + row * kDV + 32 * half);
-#pragma unroll
-        for (int q = 0; q < 4; q++)
-            d4[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
-                               pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+        put(smem + C::kR, 4 * half);
         if (half == 0) dcum[row] = dcs[t] - colE[t] - wts[t] * zsh[t];
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tma_store_2d(&tm_dq, smem + C::kA, 0, r0);
+        tma_store_2d(&tm_dq, smem + C::kA + kPanelBytes, 64, r0);
+        tma_store_2d(&tm_dk, smem + C::kG, 0, r0);
+        tma_store_2d(&tm_dk, smem + C::kG + kPanelBytes, 64, r0);
+        tma_store_2d(&tm_dv, smem + C::kR, 0, r0);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
     for (int x = tid; x < kTile * L; x += blockDim.x) {
         const int row = x / L, l = x - row * L;
         dlambda[static_cast<size_t>(r0) * L + x] = l < 8 ? dlam8[row][l] : (l < 24 ? dlamp[row][l - 8] : 0.f);
     }
 
+    if (tid == 0 && ok) {
+        // the tensor stores are complete before the shared memory goes away
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
     __syncthreads();
     if (tid == 0 && fail_sh) {
         // let this CTA's copies land before its shared memory goes away
@@ -931,8 +943,11 @@ cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const vo
     note_launch(stream, "tc_cmat");
     e = cudaFuncSetAttribute(tc_bwd_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg::kBytes);
     if (e != cudaSuccess) return e;
+    CUtensorMap tdq, tdk, tdv;
+    if (!make_map(&tdq, dq, rows, kDk) || !make_map(&tdk, dk, rows, kDk) || !make_map(&tdv, dv, rows, kDV))
+        return cudaErrorInvalidValue;
     tc_bwd_tile_kernel<<<dim3(pl.NT, BH), 256, TileCfg::kBytes, stream>>>(
-        tq, tk, tv, tdo, tn, tc, lambda, tok_cl2, dtab, static_cast<__nv_bfloat16*>(dq),
+        tq, tk, tv, tdo, tn, tc, tdq, tdk, tdv, lambda, tok_cl2, dtab, static_cast<__nv_bfloat16*>(dq),
         static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), dlambda, dcum, pl.T, pl.NT, L, pl.P,
         pl.node_count, lo, err);
     note_launch(stream, "tc_bwd_tile");
