@@ -566,9 +566,13 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int ll = 0; ll < 8; ll++) dl[ll] += (l == ll) ? dsum : 0.f;
             } else {
+                // the diagonal 32-key block: t and s share bits 5 and 6, so the levels are 0..5
                 float sv[32], dpv[32];
                 tmem_ld32(tmem + lane_base + C::kS + cb, sv);
                 tmem_ld32(tmem + lane_base + C::kDP + cb, dpv);
+                float lr[6];
+#pragma unroll
+                for (int ll = 0; ll < 6; ll++) lr[ll] = lam8[t][ll];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float av[2], gv[2];
@@ -576,17 +580,18 @@ __global__ void __launch_bounds__(256, 1)
                     for (int h = 0; h < 2; h++) {
                         const int s = cb + e + h;
                         const int l = 32 - __clz(t ^ s);
-                        float lm = lam8[t][0];
+                        float lm = lr[0];
 #pragma unroll
-                        for (int ll = 1; ll < 8; ll++) lm = (l == ll) ? lam8[t][ll] : lm;
-                        const float D = exp2f(fminf(cl2_t - cl2_sh[s], 0.f));
-                        const bool causal = s <= t;
-                        const float dq_ = causal ? D * sv[e + h] * dpv[e + h] : 0.f;
+                        for (int ll = 1; ll < 6; ll++) lm = (l == ll) ? lr[ll] : lm;
+                        // decay, zero for keys after t (masked)
+                        const float D = s <= t ? exp2f(fminf(cl2_t - cl2_sh[s], 0.f)) : 0.f;
+                        const float ds = D * sv[e + h];
+                        const float dq_ = ds * dpv[e + h];
 #pragma unroll
-                        for (int ll = 0; ll < 8; ll++) dl[ll] += (l == ll) ? dq_ : 0.f;
+                        for (int ll = 0; ll < 6; ll++) dl[ll] += (l == ll) ? dq_ : 0.f;
                         ev[e + h] = lm * dq_;
-                        av[h] = causal ? lm * D * sv[e + h] : 0.f;
-                        gv[h] = causal ? lm * D * dpv[e + h] : 0.f;
+                        av[h] = lm * ds;
+                        gv[h] = lm * D * dpv[e + h];
                     }
                     pa[e >> 1] = pack_bf16(av[0], av[1]);
                     pg[e >> 1] = pack_bf16(gv[0], gv[1]);
