@@ -24,8 +24,9 @@
 //                        dlambda levels 0..7 and the decay derivatives; then
 //                        dV = A^T dO, dQ = G K, dK = G^T Q; per set bit p,
 //                        Y_p = Q B_p (for dlambda_t^(8+p) and dcum) and
-//                        dQ += (r_p o dO) B_p^T; per key tile, dK += (w o V)
-//                        C_i^T, dV += (w o K) C_i and Z = K C_i (for dcum).
+//                        dQ += (r_p o dO) B_p^T; per key tile (issued before
+//                        the levels), dK += (w o V) C_i^T, dV += (w o K) C_i and
+//                        Z = K C_i (for dcum); dQ, dK, dV leave by TMA stores.
 //   bwd_dloga          : dlog_a_r = sum_{t >= r} dcum_t.
 // Every mbarrier wait is bounded; on overrun a kernel records LLA_ERR_TIMEOUT,
 // lets its own copies and MMAs land and returns.
@@ -354,10 +355,10 @@ struct TileCfg {
     static constexpr int kK = 2 * kPanelBytes;       // K tile  [s][d], 2 panels
     static constexpr int kV = 4 * kPanelBytes;       // V tile  [s][e], 1 panel
     static constexpr int kDO = 5 * kPanelBytes;      // dO tile [t][e], 1 panel
-    static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; later w o K [s][d]
-    static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels
-    static constexpr int kR = 10 * kPanelBytes;      // r_p o dO [t][e]; later w o V [s][e]
-    static constexpr int kN = 11 * kPanelBytes;      // node B_p [d][e]; later C_i [d][e]
+    static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; then w o K [s][d]; then dQ out
+    static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels; then w o V, C_i; then dK out
+    static constexpr int kR = 10 * kPanelBytes;      // r_p o dO [t][e]; then dV out
+    static constexpr int kN = 11 * kPanelBytes;      // node B_p [d][e]
     static constexpr int kBytes = 12 * kPanelBytes + 1024;
     static constexpr uint32_t kTxIn = 6 * kPanelBytes;
     // TMEM columns
@@ -641,6 +642,73 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&bar_m1);
     }
 
+    // ---- key side, issued before the query side so that its copy and MMAs overlap the
+    // level rounds: dK += (w o V) C_i^T, dV += (w o K) C_i, Z = K C_i. A and G are consumed:
+    // w o K takes A's space, w o V and C_i the two panels of G's.
+    ok = __syncthreads_and(ok && ok_wait(&bar_m1, 0));
+    if (tid == 0 && ok) {
+        mbar_expect_tx(&bar_c, kPanelBytes);
+        tma_load_2d(smem + C::kG + kPanelBytes, &tm_cmat, &bar_c, 0, (bh * NT + j) * kDk);
+        c_issued = true;
+    }
+    if (ok) {
+        const float w = exp2f(cl2_sh[kTile - 1] - cl2_sh[t]);
+        if (half == 0) wts[t] = w;
+        // w o V: row t (= key s), this half's 32 columns
+        {
+            const uint8_t* src = smem + C::kV;
+            uint8_t* dst = smem + C::kG;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t off = sw128_off(t, 4 * half + q);
+                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                *reinterpret_cast<uint4*>(dst + off) =
+                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
+                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
+            }
+        }
+        // w o K: row t, panel `half` (64 columns)
+        {
+            const uint8_t* src = smem + C::kK + half * kPanelBytes;
+            uint8_t* dst = smem + C::kA + half * kPanelBytes;
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const uint32_t off = sw128_off(t, q);
+                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                *reinterpret_cast<uint4*>(dst + off) =
+                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
+                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        if (mbar_wait(&bar_c, 0)) {
+            tc_fence_after();
+            const uint32_t rb = smem_u32(smem + C::kG), cb = smem_u32(smem + C::kG + kPanelBytes);
+            const uint32_t ab = smem_u32(smem + C::kA), kb = smem_u32(smem + C::kK);
+            constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 0, 0);
+            constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < kDV / 16; kk++)
+                mma_bf16(tmem + C::kDK, sdesc(rb + kk * 32, 16, 1024), sdesc(cb + kk * 32, 16, 1024), kIdK, 1u);
+#pragma unroll
+            for (int kk = 0; kk < kDk / 16; kk++) {
+                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                mma_bf16(tmem + C::kDVc, sdesc(ab + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV, 1u);
+                mma_bf16(tmem + C::kZ, sdesc(kb + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV,
+                         kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar_k);
+        } else if (atomicExch(&fail_sh, 1) == 0) {
+            record_error(err, kDevTimeout);
+        }
+    }
     // ---- query side: one round per set bit p of j
     int li = 0;
     for (int p = 0; p < P && ok; p++) {
@@ -726,71 +794,6 @@ __global__ void __launch_bounds__(256, 1)
         li++;
     }
 
-    // ---- key side: dK += (w o V) C_i^T, dV += (w o K) C_i, Z = K C_i
-    ok = __syncthreads_and(ok && ok_wait(&bar_m1, 0));  // A and G are consumed: their space takes w o K
-    if (tid == 0 && ok) {
-        mbar_expect_tx(&bar_c, kPanelBytes);
-        tma_load_2d(smem + C::kN, &tm_cmat, &bar_c, 0, (bh * NT + j) * kDk);
-        c_issued = true;
-    }
-    if (ok) {
-        const float w = exp2f(cl2_sh[kTile - 1] - cl2_sh[t]);
-        if (half == 0) wts[t] = w;
-        // w o V: row t (= key s), this half's 32 columns
-        {
-            const uint8_t* src = smem + C::kV;
-            uint8_t* dst = smem + C::kR;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const uint32_t off = sw128_off(t, 4 * half + q);
-                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
-                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-                *reinterpret_cast<uint4*>(dst + off) =
-                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
-                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
-            }
-        }
-        // w o K: row t, panel `half` (64 columns)
-        {
-            const uint8_t* src = smem + C::kK + half * kPanelBytes;
-            uint8_t* dst = smem + C::kA + half * kPanelBytes;
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const uint32_t off = sw128_off(t, q);
-                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
-                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-                *reinterpret_cast<uint4*>(dst + off) =
-                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
-                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
-            }
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        if (mbar_wait(&bar_c, 0)) {
-            tc_fence_after();
-            const uint32_t rb = smem_u32(smem + C::kR), cb = smem_u32(smem + C::kN);
-            const uint32_t ab = smem_u32(smem + C::kA), kb = smem_u32(smem + C::kK);
-            constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 0, 0);
-            constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 0, 1);
-#pragma unroll
-            for (int kk = 0; kk < kDV / 16; kk++)
-                mma_bf16(tmem + C::kDK, sdesc(rb + kk * 32, 16, 1024), sdesc(cb + kk * 32, 16, 1024), kIdK, 1u);
-#pragma unroll
-            for (int kk = 0; kk < kDk / 16; kk++) {
-                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                mma_bf16(tmem + C::kDVc, sdesc(ab + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV, 1u);
-                mma_bf16(tmem + C::kZ, sdesc(kb + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV,
-                         kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bar_k);
-        } else if (atomicExch(&fail_sh, 1) == 0) {
-            record_error(err, kDevTimeout);
-        }
-    }
     ok = __syncthreads_and(ok && ok_wait(&bar_k, 0));
     tc_fence_after();
     if (ok) {
