@@ -309,43 +309,45 @@ __global__ void __launch_bounds__(384, 1)
 
 // C_i = sum over the read ancestors (p, i >> p) of key tile i of
 // exp(sum of the tile decays after i up to the node's last tile) dB_{p, i>>p},
-// bf16 [BH][NT][dk][dv]. grid (NT, BH, dk*dv / 1024), 256 threads, 4 elements each.
+// bf16 [BH][NT][dk][dv]. grid (NT, BH), 256 threads: warp w finds the weights of levels
+// w, w + 8 (a warp-wide sum each), then every thread forms 32 elements.
 __global__ void __launch_bounds__(256) tc_cmat_kernel(const float* __restrict__ dnodes, const float* __restrict__ g,
                                                       __nv_bfloat16* __restrict__ cmat, int NT, int P, int node_count,
                                                       Offsets lo) {
     __shared__ float wsh[32];
     __shared__ int rsh[32];
     const int i = blockIdx.x, bh = blockIdx.y;
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        for (int p = 0; p < P; p++) {
-            const int m = i >> p;
-            const bool read = (m & 1) == 0 && ((m + 1) << p) < NT;
-            const int end = (m + 1) << p;  // one past the node's last tile
-            float sacc = 0.f;
-            if (read)
-                for (int u = i + 1 + lane; u < end; u += 32) sacc += g[static_cast<size_t>(bh) * NT + u];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int p = warp; p < P; p += 8) {
+        const int m = i >> p;
+        const bool read = (m & 1) == 0 && ((m + 1) << p) < NT;
+        const int end = (m + 1) << p;  // one past the node's last tile
+        float sacc = 0.f;
+        if (read)
+            for (int u = i + 1 + lane; u < end; u += 32) sacc += g[static_cast<size_t>(bh) * NT + u];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, off);
-            if (lane == 0) {
-                wsh[p] = read ? expf(sacc) : 0.f;
-                rsh[p] = read ? 1 : 0;
-            }
+        for (int off = 16; off > 0; off >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, off);
+        if (lane == 0) {
+            wsh[p] = read ? expf(sacc) : 0.f;
+            rsh[p] = read ? 1 : 0;
         }
     }
     __syncthreads();
-    const int e = blockIdx.z * 1024 + threadIdx.x;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int p = 0; p < P; p++) {
-        if (!rsh[p]) continue;
-        const float w = wsh[p];
-        const float* node = dnodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + ((i >> p) >> 1)) * kMsz + e;
-#pragma unroll
-        for (int r = 0; r < 4; r++) acc[r] = fmaf(w, node[256 * r], acc[r]);
+    __nv_bfloat16* dst = cmat + (static_cast<size_t>(bh) * NT + i) * kMsz;
+    for (int e0 = threadIdx.x * 4; e0 < kMsz; e0 += 256 * 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p = 0; p < P; p++) {
+            if (!rsh[p]) continue;
+            const float w = wsh[p];
+            const float4 x = *reinterpret_cast<const float4*>(
+                dnodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + ((i >> p) >> 1)) * kMsz + e0);
+            acc.x = fmaf(w, x.x, acc.x);
+            acc.y = fmaf(w, x.y, acc.y);
+            acc.z = fmaf(w, x.z, acc.z);
+            acc.w = fmaf(w, x.w, acc.w);
+        }
+        *reinterpret_cast<uint2*>(dst + e0) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
     }
-    __nv_bfloat16* dst = cmat + (static_cast<size_t>(bh) * NT + i) * kMsz + e;
-#pragma unroll
-    for (int r = 0; r < 4; r++) dst[256 * r] = __float2bfloat16_rn(acc[r]);
 }
 
 // ------------------------------------------------------------------ tc_bwd_tile
@@ -946,8 +948,7 @@ cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const vo
             tq, tdo, lambda, tok_cl2, dtab, dnodes, pl.T, pl.NT, L, pl.node_count, lo, lv, total, err);
         note_launch(stream, "tc_dnode");
     }
-    tc_cmat_kernel<<<dim3(pl.NT, BH, kMsz / 1024), 256, 0, stream>>>(dnodes, g_tiles, cmat, pl.NT, pl.P, pl.node_count,
-                                                                     lo);
+    tc_cmat_kernel<<<dim3(pl.NT, BH), 256, 0, stream>>>(dnodes, g_tiles, cmat, pl.NT, pl.P, pl.node_count, lo);
     note_launch(stream, "tc_cmat");
     e = cudaFuncSetAttribute(tc_bwd_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg::kBytes);
     if (e != cudaSuccess) return e;
