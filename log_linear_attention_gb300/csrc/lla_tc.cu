@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(256, 2)
     tc_nodes_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
                     float* __restrict__ seg_tot, float* __restrict__ tok_cl2, float* __restrict__ tok_colw, int T,
-                    int NT, int node_count, LevelOffsets lo, int* err) {
+                    int NT, int node_count, const __grid_constant__ LevelOffsets lo, int* err) {
     constexpr int DH = DV / 2;  // columns per thread
     constexpr int kSegTiles = 1 << Q;
     using S = NodesSmem<DV>;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(256, 2)
 __global__ void __launch_bounds__(256)
     tc_merge_kernel(const float* __restrict__ seg_tot, const float* __restrict__ g_tiles,
                     __nv_bfloat16* __restrict__ nodes, float* __restrict__ dtab, int* __restrict__ tile_counter,
-                    int NT, int q, int P, int nseg, int node_count, int msz, LevelOffsets lo) {
+                    int NT, int q, int P, int nseg, int node_count, int msz, const __grid_constant__ LevelOffsets lo) {
     __shared__ float wsg[1024];      // per-segment totals, then weights, of this block's node
     extern __shared__ float g_sh[];  // the head's tile totals (decay-table block only)
     const int bh = blockIdx.z;
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_nodes,
                      const float* __restrict__ tok_cl2, const float* __restrict__ tok_colw,
                      const float* __restrict__ lambda, const float* __restrict__ dtab,
-                     __nv_bfloat16* __restrict__ out, int T, int NT, int L, int P, int node_count, LevelOffsets lo,
+                     __nv_bfloat16* __restrict__ out, int T, int NT, int L, int P, int node_count, const __grid_constant__ LevelOffsets lo,
                      int total_tiles, int* __restrict__ tile_counter, int* err) {
     using C = OutCfg<DV>;
     constexpr int NS = C::kStages;

@@ -42,69 +42,94 @@ struct Offsets { int off[32]; };
 
 // ------------------------------------------------------------------ tc_dnode
 
-// Items of one head, in order: level p, then the tiles j with bit p set (each
-// read block's tiles are consecutive). ofs[p] = first item of level p, ofs[P] =
-// items per head.
-struct DnodeLevels {
-    int P;
-    int ofs[17];
-};
-
-// The k-th integer with bit p set: k's bits with a 1 inserted at position p.
-__device__ __forceinline__ int insert_bit(int k, int p) {
-    return ((k >> p) << (p + 1)) | (1 << p) | (k & ((1 << p) - 1));
-}
-
+// Tile-major: the CTA walks an equal share of the (head, tile) list; each tile's Q and dO
+// are loaded once, and for every set bit p of the tile index in the pass's level window
+// [p_lo, p_lo + np) the scaler warps write r_p o dO into a slot of the scaled ring. Level
+// p accumulates in TMEM columns 64 (p - p_lo) over the tiles of its reading block (a run)
+// and is drained into its node when the run ends: at the block's last tile, at the
+// head's last tile or at the end of the CTA's share. A drain warp stages its 32 rows in
+// shared memory and adds them to the fp32 node with TMA reduce-adds in L2 (partial runs of
+// neighbouring CTAs meet there).
 struct DnodeCfg {
-    static constexpr int kStages = 4;
-    static constexpr int kQBytes = 2 * kPanelBytes;  // Q tile: 128 tokens x 128
-    static constexpr int kDBytes = kPanelBytes;      // dO tile: 128 tokens x 64 (scaled in place)
-    static constexpr int kStageBytes = kQBytes + kDBytes;
-    static constexpr uint32_t kTxBytes = kStageBytes;
-    static constexpr int kBytes = kStages * kStageBytes + 1024;
+    static constexpr int kRaw = 2;                               // Q + dO stages
+    static constexpr int kScaled = 4;                            // r_p o dO slots
+    static constexpr int kQBytes = 2 * kPanelBytes;              // Q tile: 128 tokens x 128
+    static constexpr int kRawBytes = kQBytes + kPanelBytes;      // + dO tile: 128 tokens x 64
+    static constexpr int kDrainBytes = 2 * 4096;                 // per drain warp: 32 rows x 64 fp32
+    static constexpr int kBytes = kRaw * kRawBytes + kScaled * kPanelBytes + 4 * kDrainBytes + 1024;
     static constexpr int kThreads = 384;
-    static constexpr uint32_t kTmemCols = 2 * kDV;  // two accumulators
+    static constexpr int kMaxLevels = 8;                         // 8 x 64 TMEM columns
+    // dynamic + the kernel's static arrays (w_sh, barriers) within the 227 KB a CTA may hold
+    static_assert(kBytes + kMaxLevels * kTile * 4 + 512 <= 227 * 1024, "tc_dnode shared memory");
 };
+
+// Level window of one tile: bit q of `bits` = level p_lo + q is read by the tile; `start` /
+// `end` mark the levels whose run this CTA begins / finishes at the tile.
+struct DnodeTile {
+    int bh, j;
+    uint32_t bits, start, end;
+};
+
+__device__ __forceinline__ DnodeTile dnode_tile(int f, int NT, int p_lo, int np, int t0, int t1) {
+    DnodeTile d;
+    d.bh = f / NT;
+    d.j = f - d.bh * NT;
+    d.bits = (static_cast<uint32_t>(d.j) >> p_lo) & ((1u << np) - 1u);
+    d.start = d.end = 0;
+#pragma unroll
+    for (int q = 0; q < DnodeCfg::kMaxLevels; q++) {
+        if (!((d.bits >> q) & 1u)) continue;
+        const int full = (1 << (p_lo + q)) - 1, low = d.j & full;
+        if (f == t0 || low == 0) d.start |= 1u << q;
+        if (low == full || d.j + 1 == NT || f + 1 == t1) d.end |= 1u << q;
+    }
+    return d;
+}
 
 // 384 threads: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4..7 scale
 // dO (one token row per thread), warps 8..11 drain accumulators (dk row per thread).
 __global__ void __launch_bounds__(384, 1)
     tc_dnode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                    const float* __restrict__ lambda, const float* __restrict__ tok_cl2,
-                    const float* __restrict__ dtab, float* __restrict__ dnodes, int T, int NT, int L,
-                    int node_count, Offsets lo, const DnodeLevels lv, int total, int* err) {
+                    const __grid_constant__ CUtensorMap tm_dn, const float* __restrict__ lambda, const float* __restrict__ tok_cl2,
+                    const float* __restrict__ dtab, int T, int NT, int L, int node_count,
+                    const __grid_constant__ Offsets lo, int p_lo, int np, int total, int* err) {
     using C = DnodeCfg;
-    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t full_bar[S], scaled_bar[S], empty_bar[S], acc_full[2], acc_empty[2], drain_bar;
+    uint8_t* scaled = smem + C::kRaw * C::kRawBytes;
+    uint8_t* drain_stage = scaled + C::kScaled * kPanelBytes;
+    __shared__ uint64_t raw_full[C::kRaw], raw_empty[C::kRaw], sc_full[C::kScaled], sc_empty[C::kScaled];
+    __shared__ uint64_t acc_full[C::kMaxLevels], acc_empty[C::kMaxLevels], drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int fail_sh;
-    __shared__ int ofs[17];
+    __shared__ int lo_sh[32];
+    __shared__ float w_sh[DnodeCfg::kMaxLevels][kTile];  // this tile's r_{t, p_lo + q}, row t written by its scaler
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int per_head = lv.ofs[lv.P];
-    const int P = lv.P;
-    if (tid < 17) ofs[tid] = lv.ofs[tid];
     const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
     const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x);
+    const uint32_t tmem_cols = np <= 2 ? 128u : (np <= 4 ? 256u : 512u);
     volatile int* fail = &fail_sh;
+    if (tid < 32) lo_sh[tid] = lo.off[tid];
 
     if (tid == 0) {
-        for (int s = 0; s < S; s++) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&scaled_bar[s], 4);
-            mbar_init(&empty_bar[s], 1);
+        for (int s = 0; s < C::kRaw; s++) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], 1);
         }
-        for (int b = 0; b < 2; b++) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+        for (int s = 0; s < C::kScaled; s++) {
+            mbar_init(&sc_full[s], 4);
+            mbar_init(&sc_empty[s], 1);
+        }
+        for (int q = 0; q < C::kMaxLevels; q++) {
+            mbar_init(&acc_full[q], 1);
+            mbar_init(&acc_empty[q], 4);
         }
         mbar_init(&drain_bar, 1);
         fence_mbar_init();
         fail_sh = 0;
     }
-    if (warp == 1) tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    if (warp == 1) tmem_alloc(&tmem_base_sh, tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -113,63 +138,30 @@ __global__ void __launch_bounds__(384, 1)
     auto fail_now = [&]() {
         if (atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
     };
-    // Walk of this CTA's items without divisions: head, level p, index k within the level,
-    // tile j; an item ends its run when the next one reads another node.
-    struct Cursor {
-        int bh, p, k, j;
-        bool last_of_run;
-    };
-    auto make_cursor = [&](int f) {
-        Cursor c;
-        c.bh = f / per_head;
-        const int w = f - c.bh * per_head;
-        c.p = 0;
-        while (c.p + 1 < P && ofs[c.p + 1] <= w) c.p++;
-        c.k = w - ofs[c.p];
-        c.j = insert_bit(c.k, c.p);
-        c.last_of_run = true;
-        return c;
-    };
-    // advances c from item f to f + 1 and fills c.last_of_run for item f
-    auto step = [&](Cursor& c, int f) {
-        Cursor n = c;
-        n.k++;
-        // skip to the next level that still has items (levels may be empty)
-        while (n.p < P && ofs[n.p] + n.k >= ofs[n.p + 1]) {
-            n.k = 0;
-            n.p++;
-        }
-        if (n.p >= P) {  // next head, first nonempty level
-            n.bh++;
-            n.p = 0;
-            n.k = 0;
-            while (n.p < P && ofs[n.p] >= ofs[n.p + 1]) n.p++;
-        }
-        n.j = insert_bit(n.k, n.p);
-        c.last_of_run = (f + 1 >= t1) || n.bh != c.bh || n.p != c.p || (n.j >> (n.p + 1)) != (c.j >> (c.p + 1));
-        n.last_of_run = true;
-        return n;
+    auto level_bits = [&](int f) {
+        const int j = f % NT;
+        return (static_cast<uint32_t>(j) >> p_lo) & ((1u << np) - 1u);
     };
 
     int issued = 0;
     if (warp == 0) {
         if (lane == 0) {
-            Cursor c = make_cursor(t0);
             int s = 0;
             uint32_t ph = 0;
-            for (int f = t0; f < t1 && !*fail; f++, issued++) {
-                if (f - t0 >= S && !mbar_wait(&empty_bar[s], ph ^ 1u)) {
+            for (int f = t0; f < t1 && !*fail; f++) {
+                if (level_bits(f) == 0) continue;
+                if (issued >= C::kRaw && !mbar_wait(&raw_empty[s], ph ^ 1u)) {
                     fail_now();
                     break;
                 }
-                const int r0 = c.bh * T + c.j * kTile;
-                uint8_t* st = smem + s * C::kStageBytes;
-                mbar_expect_tx(&full_bar[s], C::kTxBytes);
-                tma_load_2d(st, &tm_q, &full_bar[s], 0, r0);
-                tma_load_2d(st + kPanelBytes, &tm_q, &full_bar[s], 64, r0);
-                tma_load_2d(st + C::kQBytes, &tm_do, &full_bar[s], 0, r0);
-                c = step(c, f);
-                if (++s == S) {
+                const int r0 = f * kTile;  // (bh * NT + j) * 128 = bh * T + 128 j
+                uint8_t* st = smem + s * C::kRawBytes;
+                mbar_expect_tx(&raw_full[s], C::kRawBytes);
+                tma_load_2d(st, &tm_q, &raw_full[s], 0, r0);
+                tma_load_2d(st + kPanelBytes, &tm_q, &raw_full[s], 64, r0);
+                tma_load_2d(st + C::kQBytes, &tm_do, &raw_full[s], 0, r0);
+                issued++;
+                if (++s == C::kRaw) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -179,130 +171,204 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
             constexpr uint32_t kIdesc = idesc_bf16(kDk, kDV, 1, 1);  // A = Q^T, B = r o dO, both MN-major
             const uint64_t qdesc0 = sdesc(smem_u32(smem), kPanelBytes, 1024);
-            const uint64_t ddesc0 = sdesc(smem_u32(smem + C::kQBytes), kPanelBytes, 1024);
-            constexpr uint64_t kStageStep = C::kStageBytes >> 4;
-            Cursor c = make_cursor(t0);
-            bool starting = true;
-            int run = 0, s = 0;
-            uint32_t ph = 0;
+            const uint64_t ddesc0 = sdesc(smem_u32(scaled), kPanelBytes, 1024);
+            constexpr uint64_t kRawStep = C::kRawBytes >> 4, kScStep = kPanelBytes >> 4;
+            int rs = 0, ss = 0;
+            uint32_t sph = 0, run_par = 0, used = 0;
             for (int f = t0; f < t1 && !*fail; f++) {
-                const Cursor nc = step(c, f);
-                const bool ending = c.last_of_run;
-                const int buf = run & 1;
-                if (starting && run >= 2 && !mbar_wait(&acc_empty[buf], ((run >> 1) - 1) & 1)) {
-                    fail_now();
-                    break;
-                }
-                if (!mbar_wait(&scaled_bar[s], ph)) {
-                    fail_now();
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t so = kStageStep * s;
+                const DnodeTile d = dnode_tile(f, NT, p_lo, np, t0, t1);
+                if (d.bits == 0) continue;
+                bool ok = true;
+#pragma unroll 1
+                for (uint32_t b = d.bits; b != 0; b &= b - 1) {
+                    const int q = __ffs(b) - 1;
+                    const bool st = (d.start >> q) & 1u;
+                    if (st) {
+                        if (((used >> q) & 1u) && !mbar_wait(&acc_empty[q], ((run_par >> q) & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        used |= 1u << q;
+                        run_par ^= 1u << q;
+                    }
+                    if (!mbar_wait(&sc_full[ss], sph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; kk++) {
-                    const uint64_t ko = so + 128u * kk;
-                    mma_bf16(tmem + buf * kDV, qdesc0 + ko, ddesc0 + ko, kIdesc, (starting && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < kTile / 16; kk++) {
+                        const uint64_t ko = 128u * kk;
+                        mma_bf16(tmem + q * kDV, qdesc0 + kRawStep * rs + ko, ddesc0 + kScStep * ss + ko, kIdesc,
+                                 (st && kk == 0) ? 0u : 1u);
+                    }
+                    mma_commit(&sc_empty[ss]);
+                    if ((d.end >> q) & 1u) mma_commit(&acc_full[q]);
+                    if (++ss == C::kScaled) {
+                        ss = 0;
+                        sph ^= 1u;
+                    }
                 }
-                mma_commit(&empty_bar[s]);
-                if (ending) {
-                    mma_commit(&acc_full[buf]);
-                    run++;
+                if (!ok) {
+                    fail_now();
+                    break;
                 }
-                starting = ending;
-                c = nc;
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                mma_commit(&raw_empty[rs]);
+                if (++rs == C::kRaw) rs = 0;
             }
             mma_commit(&drain_bar);
             if (!mbar_wait(&drain_bar, 0)) fail_now();
         }
     } else if (warp >= 4 && warp < 8) {
         const int row = tid - 128;
-        // r_{t,p} = lambda_t^(8+p) exp2(cl2_t + dtab[j][p]) for this thread's token row
-        auto weight = [&](const Cursor& c) {
-            const size_t r = static_cast<size_t>(c.bh) * T + static_cast<size_t>(c.j) * kTile + row;
-            return lambda[r * L + 8 + c.p] *
-                   exp2f(tok_cl2[r] + dtab[(static_cast<size_t>(c.bh) * NT + c.j) * 16 + c.p]);
+        // r_{t,p} = lambda_t^(8+p) exp2(cl2_t + dtab[j][p]) for this thread's token row; the
+        // factors of the next tile are fetched while the current one is scaled.
+        float lam[C::kMaxLevels], dt[C::kMaxLevels], cl2 = 0.f;
+        float nlam[C::kMaxLevels], ndt[C::kMaxLevels], ncl2 = 0.f;
+        auto next_tile = [&](int f) {
+            while (f < t1 && level_bits(f) == 0) f++;
+            return f;
         };
-        Cursor c = make_cursor(t0);
-        float w_next = weight(c);
-        int s = 0;
-        uint32_t ph = 0;
-        for (int f = t0; f < t1; f++) {
+        // factors of tile fn (level bits nb) into nlam / ndt / ncl2
+#define LLA_DNODE_FETCH(fn, nb)                                                   \
+    do {                                                                          \
+        const size_t r_ = static_cast<size_t>(fn) * kTile + row;                  \
+        ncl2 = tok_cl2[r_];                                                       \
+        _Pragma("unroll") for (int q = 0; q < C::kMaxLevels; q++) {               \
+            const bool on_ = ((nb) >> q) & 1u;                                    \
+            nlam[q] = on_ ? lambda[r_ * L + 8 + p_lo + q] : 0.f;                  \
+            ndt[q] = on_ ? dtab[static_cast<size_t>(fn) * 16 + p_lo + q] : 0.f;   \
+        }                                                                         \
+    } while (0)
+        int f = next_tile(t0);
+        if (f < t1) LLA_DNODE_FETCH(f, level_bits(f));
+        int rs = 0, ss = 0;
+        uint32_t rph = 0, sph = 0;
+        int n_sc = 0;
+        while (f < t1) {
             if (__any_sync(0xffffffffu, *fail != 0)) break;
-            const float w = w_next;
-            c = step(c, f);
-            if (f + 1 < t1) w_next = weight(c);
-            const int cs = s;
-            const uint32_t cph = ph;
-            if (++s == S) {
-                s = 0;
-                ph ^= 1u;
+            const uint32_t bits = level_bits(f);
+            cl2 = ncl2;
+#pragma unroll
+            for (int q = 0; q < C::kMaxLevels; q++) {
+                lam[q] = nlam[q];
+                dt[q] = ndt[q];
             }
-            if (!warp_wait(&full_bar[cs], cph)) {
+            const int fn = next_tile(f + 1);
+            if (fn < t1) LLA_DNODE_FETCH(fn, level_bits(fn));
+            if (!warp_wait(&raw_full[rs], rph)) {
                 if (lane == 0) fail_now();
                 break;
             }
-            uint8_t* drow = smem + cs * C::kStageBytes + C::kQBytes + row * 128;
 #pragma unroll
-            for (int ch = 0; ch < 8; ch++) {
-                uint4* hp = reinterpret_cast<uint4*>(drow + (((ch ^ (row & 7))) << 4));
-                const uint4 x = *hp;
-                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-                *hp = make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
-                                 pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
+            for (int q = 0; q < C::kMaxLevels; q++)
+                if ((bits >> q) & 1u) w_sh[q][row] = lam[q] * exp2f(cl2 + dt[q]);
+            const uint8_t* drow = smem + rs * C::kRawBytes + C::kQBytes + row * 128;
+            uint4 x[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ch++) x[ch] = *reinterpret_cast<const uint4*>(drow + ((ch ^ (row & 7)) << 4));
+            bool ok = true;
+#pragma unroll 1
+            for (uint32_t b = bits; b != 0; b &= b - 1) {
+                const float w = w_sh[__ffs(b) - 1][row];
+                if (n_sc >= C::kScaled && !warp_wait(&sc_empty[ss], sph ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* srow = scaled + ss * kPanelBytes + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ch++) {
+                    const float2 a0 = unpack_bf16(x[ch].x), a1 = unpack_bf16(x[ch].y), a2 = unpack_bf16(x[ch].z),
+                                 a3 = unpack_bf16(x[ch].w);
+                    *reinterpret_cast<uint4*>(srow + ((ch ^ (row & 7)) << 4)) =
+                        make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
+                                   pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sc_full[ss]);
+                n_sc++;
+                if (++ss == C::kScaled) {
+                    ss = 0;
+                    sph ^= 1u;
+                }
             }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&scaled_bar[cs]);
+            if (!ok) {
+                if (lane == 0) fail_now();
+                break;
+            }
+            if (++rs == C::kRaw) {
+                rs = 0;
+                rph ^= 1u;
+            }
+            f = fn;
         }
+#undef LLA_DNODE_FETCH
     } else if (warp >= 8) {
         const int quad = warp & 3;
-        const int d = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        int run = 0;
-        Cursor c = make_cursor(t0);
+        uint8_t* stage = drain_stage + quad * C::kDrainBytes;
+        uint32_t par = 0;
         for (int f = t0; f < t1; f++) {
-            const Cursor nc = step(c, f);
-            const Cursor cur = c;
-            c = nc;
-            if (!cur.last_of_run) continue;
-            const int buf = run & 1;
+            const DnodeTile dt = dnode_tile(f, NT, p_lo, np, t0, t1);
+            if (dt.end == 0) continue;
             if (__any_sync(0xffffffffu, *fail != 0)) break;
-            if (!warp_wait(&acc_full[buf], (run >> 1) & 1)) {
+            bool ok = true;
+#pragma unroll 1
+            for (uint32_t b = dt.end; b != 0; b &= b - 1) {
+                const int q = __ffs(b) - 1;
+                if (!warp_wait(&acc_full[q], (par >> q) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                par ^= 1u << q;
+                tc_fence_after();
+                float x[64];
+                tmem_ld32(tmem + lane_base + q * kDV, x);
+                tmem_ld32(tmem + lane_base + q * kDV + 32, x + 32);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[q]);
+                    bulk_wait_read0();  // the previous reduce has read the staging box
+                }
+                __syncwarp();
+                // row `lane` of this warp's 32: columns 32h + 4c .. + 3 at box h, chunk c ^ (lane & 7)
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+#pragma unroll
+                    for (int c = 0; c < 8; c++)
+                        *reinterpret_cast<float4*>(stage + h * 4096 + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            make_float4(x[32 * h + 4 * c], x[32 * h + 4 * c + 1], x[32 * h + 4 * c + 2],
+                                        x[32 * h + 4 * c + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int p = p_lo + q;
+                    const int m = (dt.j >> p) - 1;
+                    const int row0 = (dt.bh * node_count + lo_sh[p] + (m >> 1)) * kDk + quad * 32;
+                    tma_reduce_add_2d(&tm_dn, stage, 0, row0);
+                    tma_reduce_add_2d(&tm_dn, stage + 4096, 32, row0);
+                    bulk_commit();
+                }
+            }
+            if (!ok) {
                 if (lane == 0) fail_now();
                 break;
             }
-            tc_fence_after();
-            const int m = (cur.j >> cur.p) - 1;
-            float4* dst = reinterpret_cast<float4*>(
-                dnodes + ((static_cast<size_t>(cur.bh) * node_count + lo.off[cur.p] + (m >> 1)) * kDk + d) * kDV);
-#pragma unroll
-            for (int c0 = 0; c0 < kDV; c0 += 32) {
-                float x[32];
-                tmem_ld32(tmem + lane_base + buf * kDV + c0, x);
-#pragma unroll
-                for (int q = 0; q < 8; q++)
-                    atomicAdd(dst + c0 / 4 + q, make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]));
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            run++;
         }
+        if (lane == 0) bulk_wait0();
     }
 
     __syncthreads();
     if (*fail && warp == 0 && lane == 0) {
-        for (int i = issued - S > 0 ? issued - S : 0; i < issued; i++) mbar_wait(&full_bar[i % S], (i / S) & 1);
+        for (int i = issued - C::kRaw > 0 ? issued - C::kRaw : 0; i < issued; i++)
+            mbar_wait(&raw_full[i % C::kRaw], (i / C::kRaw) & 1);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, tmem_cols);
 }
 
 // ------------------------------------------------------------------ tc_cmat
@@ -313,7 +379,7 @@ __global__ void __launch_bounds__(384, 1)
 // w, w + 8 (a warp-wide sum each), then every thread forms 32 elements.
 __global__ void __launch_bounds__(256) tc_cmat_kernel(const float* __restrict__ dnodes, const float* __restrict__ g,
                                                       __nv_bfloat16* __restrict__ cmat, int NT, int P, int node_count,
-                                                      Offsets lo) {
+                                                      const __grid_constant__ Offsets lo) {
     __shared__ float wsh[32];
     __shared__ int rsh[32];
     const int i = blockIdx.x, bh = blockIdx.y;
@@ -398,7 +464,7 @@ __global__ void __launch_bounds__(256, 1)
                        const float* __restrict__ lambda, const float* __restrict__ tok_cl2,
                        const float* __restrict__ dtab, __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
                        __nv_bfloat16* __restrict__ dv, float* __restrict__ dlambda, float* __restrict__ dcum, int T,
-                       int NT, int L, int P, int node_count, Offsets lo, int* err) {
+                       int NT, int L, int P, int node_count, const __grid_constant__ Offsets lo, int* err) {
     using C = TileCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -927,14 +993,10 @@ cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const vo
     if (pl.node_count > 0) {
         e = cudaMemsetAsync(dnodes, 0, dnodes_bytes, stream);
         if (e != cudaSuccess) return e;
-        DnodeLevels lv;
-        lv.P = pl.P;
-        int n = 0;
-        for (int p = 0; p <= 16; p++) {
-            lv.ofs[p] = n;
-            if (p < pl.P) n += pl.NT / (2 << p) * (1 << p) + (pl.NT % (2 << p) > (1 << p) ? pl.NT % (2 << p) - (1 << p) : 0);
-        }
-        const int total = BH * n;
+        CUtensorMap tdn;
+        if (!make_map_f32_32x32(&tdn, dnodes, static_cast<uint64_t>(BH) * pl.node_count * kDk, kDV))
+            return cudaErrorInvalidValue;
+        const int total = BH * pl.NT;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
@@ -944,9 +1006,13 @@ cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const vo
         const int grid = total < sms ? total : sms;
         e = cudaFuncSetAttribute(tc_dnode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DnodeCfg::kBytes);
         if (e != cudaSuccess) return e;
-        tc_dnode_kernel<<<grid, DnodeCfg::kThreads, DnodeCfg::kBytes, stream>>>(
-            tq, tdo, lambda, tok_cl2, dtab, dnodes, pl.T, pl.NT, L, pl.node_count, lo, lv, total, err);
-        note_launch(stream, "tc_dnode");
+        // levels in windows of at most eight (one TMEM accumulator of 64 columns each)
+        for (int p_lo = 0; p_lo < pl.P; p_lo += DnodeCfg::kMaxLevels) {
+            const int np = pl.P - p_lo < DnodeCfg::kMaxLevels ? pl.P - p_lo : DnodeCfg::kMaxLevels;
+            tc_dnode_kernel<<<grid, DnodeCfg::kThreads, DnodeCfg::kBytes, stream>>>(
+                tq, tdo, tdn, lambda, tok_cl2, dtab, pl.T, pl.NT, L, pl.node_count, lo, p_lo, np, total, err);
+            note_launch(stream, "tc_dnode");
+        }
     }
     tc_cmat_kernel<<<dim3(pl.NT, BH), 256, 0, stream>>>(dnodes, g_tiles, cmat, pl.NT, pl.P, pl.node_count, lo);
     note_launch(stream, "tc_cmat");
