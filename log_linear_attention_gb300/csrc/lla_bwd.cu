@@ -533,33 +533,52 @@ size_t chunk_smem_floats(int C, int dk, int dv, int L) {
     return static_cast<size_t>(C) * (2 * (dk + 1) + 2 * (dv + 1) + 2 * (C + 1) + 2 * L) + 128 * 33 + 3 * kMaxChunk;
 }
 
-// dlog_a_r = sum_{t >= r} dcum_t, per head. grid (BH), 256 threads.
-__global__ void __launch_bounds__(kThreads) bwd_dloga_kernel(const float* __restrict__ dcum,
-                                                             float* __restrict__ dlog_a, int Tlen) {
-    __shared__ float warp_tot[8];
-    __shared__ float carry_sh;
+// dlog_a_r = sum_{t >= r} dcum_t, per head. grid (BH), 1024 threads. The head is taken in
+// pieces of 8192 tokens from its end: a coalesced copy into shared memory, suffix sums over
+// 8 consecutive tokens per thread, a block-wide suffix scan of those sums, a coalesced store.
+constexpr int kDlogaThreads = 1024;
+constexpr int kDlogaPiece = 8 * kDlogaThreads;
+
+__global__ void __launch_bounds__(kDlogaThreads) bwd_dloga_kernel(const float* __restrict__ dcum,
+                                                                 float* __restrict__ dlog_a, int Tlen) {
+    __shared__ float buf[kDlogaPiece];
+    __shared__ float warp_tot[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* src = dcum + static_cast<size_t>(blockIdx.x) * Tlen;
     float* dst = dlog_a + static_cast<size_t>(blockIdx.x) * Tlen;
-    if (tid == 0) carry_sh = 0.f;
-    __syncthreads();
-    // blocks of 256 tokens from the end; thread tid takes token end - tid
-    for (int end = Tlen - 1; end >= 0; end -= kThreads) {
-        const int r = end - tid;
-        const float x = r >= 0 ? src[r] : 0.f;
-        float incl = x;
+    float carry = 0.f;  // sum of the tokens after this piece
+    for (int end = Tlen; end > 0; end -= kDlogaPiece) {
+        const int beg = end > kDlogaPiece ? end - kDlogaPiece : 0, n = end - beg;
+        for (int i = tid; i < n; i += kDlogaThreads) buf[i] = src[beg + i];
+        __syncthreads();
+        float v[8], tot = 0.f;
+#pragma unroll
+        for (int e = 7; e >= 0; e--) {
+            const int i = 8 * tid + e;
+            tot += i < n ? buf[i] : 0.f;
+            v[e] = tot;
+        }
+        // suffix scan of the thread totals: lanes after this one, then warps after this one
+        float incl = tot;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += y;
+            const float y = __shfl_down_sync(0xffffffffu, incl, off);
+            if (lane + off < 32) incl += y;
         }
-        if (lane == 31) warp_tot[warp] = incl;
+        if (lane == 0) warp_tot[warp] = incl;
         __syncthreads();
-        float base = carry_sh;
-        for (int w = 0; w < warp; w++) base += warp_tot[w];
-        if (r >= 0) dst[r] = base + incl;
+        float after = carry + incl - tot;
+        for (int w = warp + 1; w < 32; w++) after += warp_tot[w];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const int i = 8 * tid + e;
+            if (i < n) buf[i] = v[e] + after;
+        }
+        float piece = 0.f;
+        for (int w = 0; w < 32; w++) piece += warp_tot[w];
         __syncthreads();
-        if (tid == kThreads - 1) carry_sh = base + incl;
+        for (int i = tid; i < n; i += kDlogaThreads) dst[beg + i] = buf[i];
+        carry += piece;
         __syncthreads();
     }
 }
@@ -629,7 +648,7 @@ cudaError_t backward_t(const BwdPlan& pl, const T* q, const T* k, const T* v, co
             fw.c, fw.N, fw.P, L, fw.node_count, lo);
         note_launch(stream, "bwd_chunk");
     }
-    bwd_dloga_kernel<<<BH, kThreads, 0, stream>>>(dcum, dlog_a, fw.T);
+    bwd_dloga_kernel<<<BH, kDlogaThreads, 0, stream>>>(dcum, dlog_a, fw.T);
     note_launch(stream, "bwd_dloga");
     return cudaGetLastError();
 }
@@ -637,7 +656,7 @@ cudaError_t backward_t(const BwdPlan& pl, const T* q, const T* k, const T* v, co
 }  // namespace
 
 cudaError_t bwd_dloga(const float* dcum, float* dlog_a, int BH, int T, cudaStream_t stream) {
-    bwd_dloga_kernel<<<BH, kThreads, 0, stream>>>(dcum, dlog_a, T);
+    bwd_dloga_kernel<<<BH, kDlogaThreads, 0, stream>>>(dcum, dlog_a, T);
     note_launch(stream, "bwd_dloga");
     return cudaGetLastError();
 }
