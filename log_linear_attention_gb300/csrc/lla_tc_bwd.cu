@@ -64,10 +64,12 @@ struct DnodeCfg {
 };
 
 // Level window of one tile: bit q of `bits` = level p_lo + q is read by the tile; `start` /
-// `end` mark the levels whose run this CTA begins / finishes at the tile.
+// `end` mark the levels whose run this CTA begins / finishes at the tile; `start_cut` /
+// `end_cut` the subset where that is only because the CTA's share begins / ends there (the
+// run continues in a neighbouring CTA).
 struct DnodeTile {
     int bh, j;
-    uint32_t bits, start, end;
+    uint32_t bits, start, end, start_cut, end_cut;
 };
 
 __device__ __forceinline__ DnodeTile dnode_tile(int f, int NT, int p_lo, int np, int t0, int t1) {
@@ -75,13 +77,16 @@ __device__ __forceinline__ DnodeTile dnode_tile(int f, int NT, int p_lo, int np,
     d.bh = f / NT;
     d.j = f - d.bh * NT;
     d.bits = (static_cast<uint32_t>(d.j) >> p_lo) & ((1u << np) - 1u);
-    d.start = d.end = 0;
+    d.start = d.end = d.start_cut = d.end_cut = 0;
 #pragma unroll
     for (int q = 0; q < DnodeCfg::kMaxLevels; q++) {
         if (!((d.bits >> q) & 1u)) continue;
         const int full = (1 << (p_lo + q)) - 1, low = d.j & full;
+        const bool natural_end = low == full || d.j + 1 == NT;
         if (f == t0 || low == 0) d.start |= 1u << q;
-        if (low == full || d.j + 1 == NT || f + 1 == t1) d.end |= 1u << q;
+        if (natural_end || f + 1 == t1) d.end |= 1u << q;
+        if (low != 0 && f == t0) d.start_cut |= 1u << q;
+        if (!natural_end && f + 1 == t1) d.end_cut |= 1u << q;
     }
     return d;
 }
@@ -308,9 +313,10 @@ __global__ void __launch_bounds__(384, 1)
         const int quad = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         uint8_t* stage = drain_stage + quad * C::kDrainBytes;
-        uint32_t par = 0;
+        uint32_t par = 0, cut = 0;  // cut: the slot's current run began in another CTA
         for (int f = t0; f < t1; f++) {
             const DnodeTile dt = dnode_tile(f, NT, p_lo, np, t0, t1);
+            cut = (cut & ~dt.start) | dt.start_cut;
             if (dt.end == 0) continue;
             if (__any_sync(0xffffffffu, *fail != 0)) break;
             bool ok = true;
@@ -347,8 +353,13 @@ __global__ void __launch_bounds__(384, 1)
                     const int p = p_lo + q;
                     const int m = (dt.j >> p) - 1;
                     const int row0 = (dt.bh * node_count + lo_sh[p] + (m >> 1)) * kDk + quad * 32;
-                    tma_reduce_add_2d(&tm_dn, stage, 0, row0);
-                    tma_reduce_add_2d(&tm_dn, stage + 4096, 32, row0);
+                    if (((cut | dt.end_cut) >> q) & 1u) {  // shared with a neighbour: add into the zeroed node
+                        tma_reduce_add_2d(&tm_dn, stage, 0, row0);
+                        tma_reduce_add_2d(&tm_dn, stage + 4096, 32, row0);
+                    } else {  // the whole reading block: this CTA is the node's only writer
+                        tma_store_2d(&tm_dn, stage, 0, row0);
+                        tma_store_2d(&tm_dn, stage + 4096, 32, row0);
+                    }
                     bulk_commit();
                 }
             }
@@ -369,6 +380,21 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+}
+
+// Zero the nodes whose reading block a CTA boundary of tc_dnode cuts (the only ones written by
+// reduce-adds). grid (CTAs - 1, P), 256 threads: boundary b starts CTA b's share at tile f; for
+// each set bit p of its tile index j with nonzero bits below p, the node (p, (j >> p) - 1) is cut.
+__global__ void __launch_bounds__(256) tc_dnode_zero_cut_kernel(float* __restrict__ dnodes, int NT, int total,
+                                                                int ctas, int node_count,
+                                                                const __grid_constant__ Offsets lo) {
+    const int b = blockIdx.x + 1, p = blockIdx.y;
+    const int f = static_cast<int>(static_cast<int64_t>(b) * total / ctas);
+    const int bh = f / NT, j = f - bh * NT;
+    if (!((j >> p) & 1) || (j & ((1 << p) - 1)) == 0) return;
+    float4* dst = reinterpret_cast<float4*>(
+        dnodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + (((j >> p) - 1) >> 1)) * kMsz);
+    for (int i = threadIdx.x; i < kMsz / 4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ tc_cmat
@@ -991,8 +1017,6 @@ cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const vo
     }
 
     if (pl.node_count > 0) {
-        e = cudaMemsetAsync(dnodes, 0, dnodes_bytes, stream);
-        if (e != cudaSuccess) return e;
         CUtensorMap tdn;
         if (!make_map_f32_32x32(&tdn, dnodes, static_cast<uint64_t>(BH) * pl.node_count * kDk, kDV))
             return cudaErrorInvalidValue;
@@ -1004,6 +1028,11 @@ cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const vo
             sms = 152;
         }
         const int grid = total < sms ? total : sms;
+        if (grid > 1) {
+            tc_dnode_zero_cut_kernel<<<dim3(grid - 1, pl.P), 256, 0, stream>>>(dnodes, pl.NT, total, grid,
+                                                                                pl.node_count, lo);
+            note_launch(stream, "tc_dnode_zero_cut");
+        }
         e = cudaFuncSetAttribute(tc_dnode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DnodeCfg::kBytes);
         if (e != cudaSuccess) return e;
         // levels in windows of at most eight (one TMEM accumulator of 64 columns each)
