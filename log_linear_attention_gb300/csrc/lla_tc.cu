@@ -411,14 +411,6 @@ struct OutCfg {
     static constexpr int kThreads = (3 + kEpiWarps) * 32;
 };
 
-// Contiguous global -> shared copy through the async proxy (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // Pull a 128-row x 64-column box of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -450,11 +450,12 @@ struct TileCfg {
     static constexpr int kV = 4 * kPanelBytes;       // V tile  [s][e], 1 panel
     static constexpr int kDO = 5 * kPanelBytes;      // dO tile [t][e], 1 panel
     static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; then w o K [s][d]; then dQ out
-    static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels; then w o V, C_i; then dK out
-    static constexpr int kR = 10 * kPanelBytes;      // r_p o dO [t][e]; then dV out
+    static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels; then w o V and r_p o dO; then dK out
+    static constexpr int kC = 10 * kPanelBytes;      // C_i [d][e] (copied with the inputs); then dV out
     static constexpr int kN = 11 * kPanelBytes;      // node B_p [d][e]
+    static constexpr int kR = kG + kPanelBytes;      // r_p o dO [t][e]: G's second panel once G is consumed
     static constexpr int kBytes = 12 * kPanelBytes + 1024;
-    static constexpr uint32_t kTxIn = 6 * kPanelBytes;
+    static constexpr uint32_t kTxIn = 7 * kPanelBytes;
     // TMEM columns
     static constexpr uint32_t kS = 0, kDP = 128;                       // S, dP (phase 1)
     static constexpr uint32_t kDQ = 0, kDK = 128, kDVc = 256, kY = 320, kZ = 384;
@@ -494,15 +495,14 @@ __global__ void __launch_bounds__(256, 1)
     using C = TileCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_in, bar_s, bar_m1, bar_node, bar_lv, bar_c, bar_k, bar_d;
+    __shared__ uint64_t bar_in, bar_s, bar_m1, bar_node, bar_lv, bar_k, bar_d;
     __shared__ uint32_t tmem_base_sh;
-    __shared__ float cl2_sh[kTile];
-    __shared__ float lam8[kTile][8];
-    __shared__ float lamp[kTile][16];
+    __shared__ __align__(16) float cl2_sh[kTile];
+    __shared__ __align__(16) float lam_sh[kTile * 32];  // the tile's lambda rows [t][L], L <= 32
     __shared__ float dlam8[kTile][8];
     __shared__ float dlamp[kTile][16];
     __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile], colw_sh[kTile];
-    __shared__ float dtab_sh[16];
+    __shared__ __align__(16) float dtab_sh[16];
     __shared__ int fail_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -519,7 +519,6 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(&bar_m1, 1);
         mbar_init(&bar_node, 1);
         mbar_init(&bar_lv, 1);
-        mbar_init(&bar_c, 1);
         mbar_init(&bar_k, 1);
         mbar_init(&bar_d, 1);
         fence_mbar_init();
@@ -540,48 +539,27 @@ __global__ void __launch_bounds__(256, 1)
     auto node_row = [&](int p) { return (bh * node_count + lo.off[p] + (((j >> p) - 1) >> 1)) * kDk; };
 
     int node_issued = 0;  // thread 0: node copies issued
-    bool c_issued = false;
     if (tid == 0) {
         uint8_t* st = smem;
-        mbar_expect_tx(&bar_in, C::kTxIn);
+        // inputs, C_i, and the per-row scalars: lambda rows (one contiguous block of 128 L
+        // floats), the in-tile log2 decay prefix and the tile's level decay row
+        mbar_expect_tx(&bar_in, C::kTxIn + kTile * L * 4 + kTile * 4 + 16 * 4);
+        bulk_load(lam_sh, lambda + static_cast<size_t>(r0) * L, kTile * L * 4, &bar_in);
+        bulk_load(cl2_sh, tok_cl2 + r0, kTile * 4, &bar_in);
+        bulk_load(dtab_sh, dtab + (static_cast<size_t>(bh) * NT + j) * 16, 16 * 4, &bar_in);
         tma_load_2d(st + C::kQ, &tm_q, &bar_in, 0, r0);
         tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &bar_in, 64, r0);
         tma_load_2d(st + C::kK, &tm_k, &bar_in, 0, r0);
         tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &bar_in, 64, r0);
         tma_load_2d(st + C::kV, &tm_v, &bar_in, 0, r0);
         tma_load_2d(st + C::kDO, &tm_do, &bar_in, 0, r0);
+        tma_load_2d(st + C::kC, &tm_cmat, &bar_in, 0, (bh * NT + j) * kDk);
         if (lvbits) {
             const int p0 = __ffs(lvbits) - 1;
             mbar_expect_tx(&bar_node, kPanelBytes);
             tma_load_2d(st + C::kN, &tm_nodes, &bar_node, 0, node_row(p0));
             node_issued = 1;
         }
-    }
-    // per-row inputs: decay prefix, lambda levels, the tile's level decay row. The tile's
-    // lambda rows are one contiguous block of 128 L floats (L <= 32): every load is issued
-    // before any is used.
-    {
-        const float* lsrc = lambda + static_cast<size_t>(r0) * L;
-        const int n = kTile * L;
-        float lv[16];
-#pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const int x = tid + i * 256;
-            lv[i] = x < n ? lsrc[x] : 0.f;
-        }
-        const float c2 = tid < kTile ? tok_cl2[r0 + tid] : 0.f;
-        const float dt = tid < 16 ? dtab[(static_cast<size_t>(bh) * NT + j) * 16 + tid] : 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const int x = tid + i * 256;
-            if (x < n) {
-                const int row = x / L, l = x - row * L;
-                if (l < 8) lam8[row][l] = lv[i];
-                else if (l < 24) lamp[row][l - 8] = lv[i];
-            }
-        }
-        if (tid < kTile) cl2_sh[tid] = c2;
-        if (tid < 16) dtab_sh[tid] = dt;
     }
     for (int x = tid; x < kTile * 8; x += blockDim.x) (&dlam8[0][0])[x] = 0.f;
     for (int x = tid; x < kTile * 16; x += blockDim.x) (&dlamp[0][0])[x] = 0.f;
@@ -590,12 +568,11 @@ __global__ void __launch_bounds__(256, 1)
         dcs[tid] = 0.f;
         zsh[tid] = 0.f;
     }
-    __syncthreads();
-
-    // decay from each key to the end of its 32-key block (the factorised decay of E1)
-    if (tid < kTile) colw_sh[tid] = exp2f(cl2_sh[tid | 31] - cl2_sh[tid]);
     // ok stays block-uniform: every change goes through a barrier reduction
     bool ok = __syncthreads_and(ok_wait(&bar_in, 0));
+    // decay from each key to the end of its 32-key block (the factorised decay of E1); read
+    // after the barrier that follows the S and dP MMAs
+    if (tid < kTile) colw_sh[tid] = exp2f(cl2_sh[tid | 31] - cl2_sh[tid]);
     // ---- S = Q K^T, dP = dO V^T
     if (tid == 0 && ok) {
         tc_fence_after();
@@ -641,9 +618,9 @@ __global__ void __launch_bounds__(256, 1)
                 tmem_ld32(tmem + lane_base + C::kS + cb, sv);
                 tmem_ld32(tmem + lane_base + C::kDP + cb, dpv);
                 const int l = 32 - __clz(t ^ cb);
-                float lm = lam8[t][0];
+                float lm = lam_sh[t * L];
 #pragma unroll
-                for (int ll = 1; ll < 8; ll++) lm = (l == ll) ? lam8[t][ll] : lm;
+                for (int ll = 1; ll < 8; ll++) lm = (l == ll) ? lam_sh[t * L + ll] : lm;
                 const float rowf = exp2f(cl2_t - cl2_sh[cb + 31]);
                 float dsum = 0.f;
 #pragma unroll
@@ -667,7 +644,7 @@ __global__ void __launch_bounds__(256, 1)
                 tmem_ld32(tmem + lane_base + C::kDP + cb, dpv);
                 float lr[6];
 #pragma unroll
-                for (int ll = 0; ll < 6; ll++) lr[ll] = lam8[t][ll];
+                for (int ll = 0; ll < 6; ll++) lr[ll] = lam_sh[t * L + ll];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float av[2], gv[2];
@@ -736,15 +713,11 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&bar_m1);
     }
 
-    // ---- key side, issued before the query side so that its copy and MMAs overlap the
-    // level rounds: dK += (w o V) C_i^T, dV += (w o K) C_i, Z = K C_i. A and G are consumed:
-    // w o K takes A's space, w o V and C_i the two panels of G's.
+    // ---- key side, issued before the query side so that its MMAs overlap the level rounds:
+    // dK += (w o V) C_i^T, dV += (w o K) C_i, Z = K C_i (C_i came with the inputs). A and G
+    // are consumed: w o K takes A's space, w o V G's first panel; the level rounds use the
+    // second for r_p o dO.
     ok = __syncthreads_and(ok && ok_wait(&bar_m1, 0));
-    if (tid == 0 && ok) {
-        mbar_expect_tx(&bar_c, kPanelBytes);
-        tma_load_2d(smem + C::kG + kPanelBytes, &tm_cmat, &bar_c, 0, (bh * NT + j) * kDk);
-        c_issued = true;
-    }
     if (ok) {
         const float w = exp2f(cl2_sh[kTile - 1] - cl2_sh[t]);
         if (half == 0) wts[t] = w;
@@ -782,9 +755,8 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     if (tid == 0 && ok) {
         tc_fence_after();
-        if (mbar_wait(&bar_c, 0)) {
-            tc_fence_after();
-            const uint32_t rb = smem_u32(smem + C::kG), cb = smem_u32(smem + C::kG + kPanelBytes);
+        {
+            const uint32_t rb = smem_u32(smem + C::kG), cb = smem_u32(smem + C::kC);
             const uint32_t ab = smem_u32(smem + C::kA), kb = smem_u32(smem + C::kK);
             constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 0, 0);
             constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 0, 1);
@@ -799,8 +771,6 @@ __global__ void __launch_bounds__(256, 1)
                          kk > 0 ? 1u : 0u);
             }
             mma_commit(&bar_k);
-        } else if (atomicExch(&fail_sh, 1) == 0) {
-            record_error(err, kDevTimeout);
         }
     }
     // ---- query side: one round per set bit p of j
@@ -809,7 +779,7 @@ __global__ void __launch_bounds__(256, 1)
         if (((j >> p) & 1) == 0) continue;
         const float cl2_t = cl2_sh[t];
         const float rho = exp2f(cl2_t + dtab_sh[p]);
-        const float r = lamp[t][p] * rho;
+        const float r = lam_sh[t * L + 8 + p] * rho;
         // r_p o dO, row t, this half's 32 columns (chunks 4 half .. 4 half + 3)
         {
             const uint8_t* src = smem + C::kDO;
@@ -929,7 +899,7 @@ __global__ void __launch_bounds__(256, 1)
             put(smem + C::kG + half * kPanelBytes, c0 >> 3);
         }
         tmem_ld32(tmem + lane_base + C::kDVc + 32 * half, x);
-        put(smem + C::kR, 4 * half);
+        put(smem + C::kC, 4 * half);
         if (half == 0) dcum[row] = dcs[t] - colE[t] - wts[t] * zsh[t];
     }
     fence_async_smem();
@@ -939,7 +909,7 @@ __global__ void __launch_bounds__(256, 1)
         tma_store_2d(&tm_dq, smem + C::kA + kPanelBytes, 64, r0);
         tma_store_2d(&tm_dk, smem + C::kG, 0, r0);
         tma_store_2d(&tm_dk, smem + C::kG + kPanelBytes, 64, r0);
-        tma_store_2d(&tm_dv, smem + C::kR, 0, r0);
+        tma_store_2d(&tm_dv, smem + C::kC, 0, r0);
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
     for (int x = tid; x < kTile * L; x += blockDim.x) {
@@ -948,15 +918,14 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     if (tid == 0 && ok) {
-        // the tensor stores are complete before the shared memory goes away
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        // the tensor stores have read their shared-memory sources before it goes away
+        bulk_wait_read0();
     }
     __syncthreads();
     if (tid == 0 && fail_sh) {
         // let this CTA's copies land before its shared memory goes away
         mbar_wait(&bar_in, 0);
         if (node_issued > 0) mbar_wait(&bar_node, (node_issued - 1) & 1);
-        if (c_issued) mbar_wait(&bar_c, 0);
     }
     if (tid == 0) {
         // every MMA issued above has completed before TMEM is released
