@@ -99,3 +99,22 @@ def test_backward_headline_sampled():
         # dcum from differences of a running sum: compare against the scale of dlog_a itself
         err = np.abs(gc - rc).max() / max(np.abs(rc).max(), 1e-30)
         assert err <= 2e-2, ("dcum", (b, h), err)
+
+
+def test_backward_long_sampled():
+    """1 x 2 heads x 65536 tokens, bf16, dk 128, dv 64: 512 tiles, nine node levels, so the
+    node-gradient kernel runs a second level window (level 8). Sampled positions of both heads,
+    including the block boundaries of the top levels."""
+    cfg = inputs.PrefillConfig("bwlong", 1, 2, 65536, 128, 64, 128, "bf16", qk_unit_rows=True, log_a_mu=-2.0)
+    inp, g, (dq, dk, dv, dla, dlam) = _run(cfg, seed=5, chunk=cfg.chunk)
+    rows = [0, 127, 128, 255, 256, 32767, 32768, 32895, 40000, 49152, 65407, 65535]
+    for b, h in ((0, 0), (0, 1)):
+        rq, rk, rv, rl, rc = oracle.backward_rows(inp.q, inp.k, inp.v, inp.log_a, inp.lam, g, b, h, rows)
+        nxt = np.append(dla[b, h], 0.0)
+        gc = nxt[rows] - nxt[np.array(rows) + 1]
+        for name, a, r in (("dq", dq[b, h, rows], rq), ("dk", dk[b, h, rows], rk), ("dv", dv[b, h, rows], rv),
+                           ("dlambda", dlam[b, h, rows], rl)):
+            err = np.abs(a - r).max() / np.abs(r).max()
+            assert err <= 2e-2, (name, (b, h), err)
+        err = np.abs(gc - rc).max() / max(np.abs(rc).max(), 1e-30)
+        assert err <= 2e-2, ("dcum", (b, h), err)
