@@ -113,9 +113,9 @@ int lla_forward_ws(const void* q, const void* k, const void* v, const float* log
 /*
  * lla_forward without any allocation, for callers that cannot call cudaMalloc
  * (a host that pre-sizes and owns every device allocation, or code that must
- * not grow the process's GPU footprint after start-up). The paper has no
- * counterpart: this is a deployment variant of lla_forward with identical
- * arguments, results and kernels.
+ * not grow the process's GPU footprint after start-up). "Log-Linear Attention"
+ * describes no counterpart: this is a deployment variant of lla_forward with
+ * identical arguments, results and kernels.
  *
  * Its scratch is a fixed, file-scope device array of LLA_NOALLOC_SCRATCH_BYTES
  * (32 MiB) that every GPU loading this library holds until the process exits.
