@@ -462,12 +462,12 @@ struct TileCfg {
     static constexpr uint32_t kTmemCols = 512;
 };
 
-// Reduce-scatter of 32 values per lane over the warp: lane l ends with the sum over all
-// lanes of v[l] (31 shuffles).
-__device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
+// Reduce-scatter of 16 values per lane over each half-warp: lane l ends with the sum of
+// v[l & 15] over the 16 lanes that share bit 4 of l (15 shuffles).
+__device__ __forceinline__ float warp_colsum16(float (&v)[16]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
+    for (int off = 8; off >= 1; off >>= 1) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int i = 0; i < off; i++) {
@@ -594,7 +594,9 @@ __global__ void __launch_bounds__(256, 1)
     ok = __syncthreads_and(ok && ok_wait(&bar_s, 0));
     tc_fence_after();
 
-    // ---- E1: A, G (bf16), dlambda levels 0..7, decay derivatives
+    // ---- E1: A, G (bf16), dlambda levels 0..7, decay derivatives. The two warps of a lane
+    // quadrant take alternate 16-key halves of every 32-key block, so the masked diagonal
+    // block of the quadrant is shared evenly between them.
     if (ok) {
         const float cl2_t = cl2_sh[t];
         float dl[8];
@@ -602,29 +604,29 @@ __global__ void __launch_bounds__(256, 1)
         for (int l = 0; l < 8; l++) dl[l] = 0.f;
         float rowE = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 2; c++) {
-            const int cb = 64 * half + 32 * c;  // first key of this chunk
-            float ev[32];
-            uint32_t pa[16], pg[16];
-            if (cb > quad * 32 + 31) {
+        for (int c = 0; c < 4; c++) {
+            const int cb32 = 32 * c;             // the 32-key block
+            const int cb = cb32 + 16 * half;     // this warp's 16 keys of it
+            float ev[16];
+            uint32_t pa[8], pg[8];
+            const bool zero = cb32 > quad * 32;  // every key after every row of this warp
+            if (zero) {
 #pragma unroll
-                for (int e = 0; e < 32; e++) ev[e] = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; e++) pa[e] = pg[e] = 0u;
-            } else if (cb < quad * 32) {
-                // every key of the chunk precedes every row of this warp: one level per row
+                for (int e = 0; e < 8; e++) pa[e] = pg[e] = 0u;
+            } else if (cb32 < quad * 32) {
+                // every key of the block precedes every row of this warp: one level per row
                 // (t and s differ first in bit 5 or 6) and decay exp2(cl_t - cl_end) colw[s]
-                float sv[32], dpv[32];
-                tmem_ld32(tmem + lane_base + C::kS + cb, sv);
-                tmem_ld32(tmem + lane_base + C::kDP + cb, dpv);
-                const int l = 32 - __clz(t ^ cb);
+                float sv[16], dpv[16];
+                tmem_ld16(tmem + lane_base + C::kS + cb, sv);
+                tmem_ld16(tmem + lane_base + C::kDP + cb, dpv);
+                const int l = 32 - __clz(t ^ cb32);
                 float lm = lam_sh[t * L];
 #pragma unroll
                 for (int ll = 1; ll < 8; ll++) lm = (l == ll) ? lam_sh[t * L + ll] : lm;
-                const float rowf = exp2f(cl2_t - cl2_sh[cb + 31]);
+                const float rowf = exp2f(cl2_t - cl2_sh[cb32 + 31]);
                 float dsum = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < 16; e += 2) {
                     const float D0 = rowf * colw_sh[cb + e], D1 = rowf * colw_sh[cb + e + 1];
                     const float s0 = D0 * sv[e], s1 = D1 * sv[e + 1];
                     const float q0 = s0 * dpv[e], q1 = s1 * dpv[e + 1];
@@ -639,14 +641,14 @@ __global__ void __launch_bounds__(256, 1)
                 for (int ll = 0; ll < 8; ll++) dl[ll] += (l == ll) ? dsum : 0.f;
             } else {
                 // the diagonal 32-key block: t and s share bits 5 and 6, so the levels are 0..5
-                float sv[32], dpv[32];
-                tmem_ld32(tmem + lane_base + C::kS + cb, sv);
-                tmem_ld32(tmem + lane_base + C::kDP + cb, dpv);
+                float sv[16], dpv[16];
+                tmem_ld16(tmem + lane_base + C::kS + cb, sv);
+                tmem_ld16(tmem + lane_base + C::kDP + cb, dpv);
                 float lr[6];
 #pragma unroll
                 for (int ll = 0; ll < 6; ll++) lr[ll] = lam_sh[t * L + ll];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < 16; e += 2) {
                     float av[2], gv[2];
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
@@ -674,14 +676,16 @@ __global__ void __launch_bounds__(256, 1)
             uint8_t* pG = smem + C::kG + (cb >> 6) * kPanelBytes;
             const int ch0 = (cb & 63) >> 3;
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
+            for (int q = 0; q < 2; q++) {
                 *reinterpret_cast<uint4*>(pA + sw128_off(t, ch0 + q)) =
                     make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
                 *reinterpret_cast<uint4*>(pG + sw128_off(t, ch0 + q)) =
                     make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
             }
-            const float cs = warp_colsum32(ev);
-            atomicAdd(&colE[cb + lane], cs);
+            if (!zero) {  // warp-uniform
+                const float cs = warp_colsum16(ev);  // key cb + (lane & 15), this lane's half-warp of rows
+                atomicAdd(&colE[cb + (lane & 15)], cs);
+            }
         }
 #pragma unroll
         for (int l = 0; l < 8; l++)
