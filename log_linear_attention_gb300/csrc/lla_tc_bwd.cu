@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(256) tc_dnode_zero_cut_kernel(float* __restric
 // C_i = sum over the read ancestors (p, i >> p) of key tile i of
 // exp(sum of the tile decays after i up to the node's last tile) dB_{p, i>>p},
 // bf16 [BH][NT][dk][dv]. grid (NT, BH), 256 threads: warp w finds the weights of levels
-// w, w + 8 (a warp-wide sum each), then every thread forms 32 elements.
+// w, w + 8 (a warp-wide sum each), then every thread forms 32 elements (8 float4s).
 __global__ void __launch_bounds__(256) tc_cmat_kernel(const float* __restrict__ dnodes, const float* __restrict__ g,
                                                       __nv_bfloat16* __restrict__ cmat, int NT, int P, int node_count,
                                                       const __grid_constant__ Offsets lo) {
@@ -425,21 +425,33 @@ __global__ void __launch_bounds__(256) tc_cmat_kernel(const float* __restrict__ 
         }
     }
     __syncthreads();
-    __nv_bfloat16* dst = cmat + (static_cast<size_t>(bh) * NT + i) * kMsz;
-    for (int e0 = threadIdx.x * 4; e0 < kMsz; e0 += 256 * 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int p = 0; p < P; p++) {
-            if (!rsh[p]) continue;
-            const float w = wsh[p];
-            const float4 x = *reinterpret_cast<const float4*>(
-                dnodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + ((i >> p) >> 1)) * kMsz + e0);
-            acc.x = fmaf(w, x.x, acc.x);
-            acc.y = fmaf(w, x.y, acc.y);
-            acc.z = fmaf(w, x.z, acc.z);
-            acc.w = fmaf(w, x.w, acc.w);
+    // thread x accumulates the float4s x + 256 k, k < 8, of the node: eight independent loads
+    // in flight per level
+    constexpr int kVec = kMsz / 4 / 256;
+    float4 acc[kVec];
+#pragma unroll
+    for (int k = 0; k < kVec; k++) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < P; p++) {
+        if (!rsh[p]) continue;
+        const float w = wsh[p];
+        const float4* src = reinterpret_cast<const float4*>(
+                                dnodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + ((i >> p) >> 1)) * kMsz) +
+                            threadIdx.x;
+        float4 x[kVec];
+#pragma unroll
+        for (int k = 0; k < kVec; k++) x[k] = src[256 * k];
+#pragma unroll
+        for (int k = 0; k < kVec; k++) {
+            acc[k].x = fmaf(w, x[k].x, acc[k].x);
+            acc[k].y = fmaf(w, x[k].y, acc[k].y);
+            acc[k].z = fmaf(w, x[k].z, acc[k].z);
+            acc[k].w = fmaf(w, x[k].w, acc[k].w);
         }
-        *reinterpret_cast<uint2*>(dst + e0) = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
     }
+    uint2* dst = reinterpret_cast<uint2*>(cmat + (static_cast<size_t>(bh) * NT + i) * kMsz) + threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < kVec; k++)
+        dst[256 * k] = make_uint2(pack_bf16(acc[k].x, acc[k].y), pack_bf16(acc[k].z, acc[k].w));
 }
 
 // ------------------------------------------------------------------ tc_bwd_tile
