@@ -11,11 +11,14 @@
 // Kernels (one stream, in order):
 //   tc_nodes, tc_merge : the forward's node stage (bf16 nodes that are read,
 //                        tile decays, per-token and per-level decay tables).
+//   tc_dnode_zero_cut  : zeroes the nodes whose reading block a CTA boundary of
+//                        tc_dnode cuts.
 //   tc_dnode           : node gradients dB_{p,m} = sum over the tiles j of the
 //                        reading block of Q_j^T diag(r_p) dO_j, on tcgen05 with
-//                        r_p o dO scaled in shared memory; runs of tiles of one
-//                        node accumulate in TMEM and are added (fp32 vector
-//                        atomics) into the node.
+//                        r_p o dO scaled in shared memory; tile-major (Q, dO
+//                        read once per tile), each level's run accumulates in
+//                        its TMEM slot and leaves by a TMA store (a whole run)
+//                        or TMA reduce-adds (a run cut by a CTA boundary).
 //   tc_cmat            : per key tile i, C_i = sum over its read ancestor
 //                        nodes of exp(decay from tile i's end to the node's
 //                        end) dB (bf16, an MMA operand of the next kernel).
