@@ -216,6 +216,10 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
  * launch, LLA_ERR_NOMEM if the pool cannot grow, LLA_ERR_CUDA on launch
  * failure.
  */
+int lla_backward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                 const void* dout, void* dq, void* dk, void* dv, float* dlog_a, float* dlambda, int B, int H,
+                 int T, int dk_, int dv_, int chunk, void* stream, int dtype);
+
 /*
  * Packed variable-length sequences (no counterpart on the pages: a serving
  * layout for many prompts of different lengths in one call).
@@ -248,10 +252,6 @@ int lla_forward_varlen(const void* q, const void* k, const void* v, const float*
 int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, const int32_t* cu_seqlens,
                              float* fenwick_states, int n_seq, int H, int total_T, int max_T, int dk, int dv, int Lmax,
                              void* stream, int dtype);
-
-int lla_backward(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
-                 const void* dout, void* dq, void* dk, void* dv, float* dlog_a, float* dlambda, int B, int H,
-                 int T, int dk_, int dv_, int chunk, void* stream, int dtype);
 
 /*
  * Reads and clears the device error word of the current device after
