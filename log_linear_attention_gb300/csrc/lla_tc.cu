@@ -909,6 +909,419 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// ------------------------------------------------------------------ tc_output_pp (dv = 64)
+
+// Ping-pong output kernel for dv = 64: two independent tile pipelines share one CTA.
+// Epilogue group g (eight warps, two per TMEM lane quadrant; thread = query row)
+// owns input stage g and TMEM columns [256 g, 256 g + 256) and takes every other
+// tile the CTA claims, so one group builds its tile's P while the other group's
+// level and PV products run on the tensor pipe. Roles (20 warps):
+//   warps 0, 1  producers of groups 0 and 1 (one lane each): claim the group's next
+//               tile from the dynamic counter and pull it into L2; once the group's
+//               stage is free, TMA of Q, K, V and a bulk copy of the tile's decay
+//               prefix into it, then the Fenwick nodes the tile reads, in level
+//               order, into the group's two-slot node ring.
+//   warps 2, 3  MMA issuers of groups 0 and 1 (one lane each).
+//   warps 4-11  epilogue of group 0; warps 12-19 epilogue of group 1. The two warps
+//               of a lane quadrant split every 32-key block of P (16 keys each) and
+//               the dv columns of the result (32 each).
+// TMEM of a group, per tile:
+//   round 0: S = Q K^T in [0, 128); the first two level reads L_p = Q B_p in
+//            [128, 192) and [192, 256) (they overlap the build of P);
+//   round 1: O = P V in [0, 64) once P is in shared memory (over K), and up to
+//            three more level reads in [64, 128), [128, 192), [192, 256);
+//   round r >= 2: three more level reads each in [64, 256).
+// The epilogue reads every round back into fp32 accumulators,
+// acc = O + sum_p lambda_t^(8+p) exp(cl_t + D_p) L_p, and stores them as bf16.
+struct PpCfg {
+    static constexpr int kQ = 0;
+    static constexpr int kK = 2 * kPanelBytes;  // K tile, then P of the same tile
+    static constexpr int kV = 4 * kPanelBytes;
+    static constexpr int kQkvBytes = 5 * kPanelBytes;
+    static constexpr int kStageBytes = kQkvBytes;
+    static constexpr int kNodeSlots = 2;  // per group
+    static constexpr int kNodeBytes = kPanelBytes;
+    static constexpr int kNodeBase = 2 * kStageBytes;
+    // 128 floats per group after the node slots: the tile's in-tile log2 decay prefix
+    static constexpr int kCl2Base = kNodeBase + 2 * kNodeSlots * kNodeBytes;
+    static constexpr int kScalarTx = 512;
+    static constexpr int kBytes = kCl2Base + 2 * 512 + 1024;
+    static constexpr int kEpiWarps = 8;  // per group
+    static constexpr int kFirstEpi = 4;  // first epilogue warp
+    static constexpr int kThreads = (kFirstEpi + 2 * kEpiWarps) * 32;
+    static constexpr int kR0 = 2;  // level reads in round 0
+    static constexpr int kRn = 3;  // level reads in each later round
+    __host__ __device__ static constexpr int rounds(int n_lv) {
+        return n_lv <= kR0 + kRn ? 2 : 2 + (n_lv - kR0 - kRn + kRn - 1) / kRn;
+    }
+    // first level (index into the tile's list of set bits) of round r, and the TMEM column of its i-th read
+    __host__ __device__ static constexpr int round_begin(int r) { return r == 0 ? 0 : kR0 + (r - 1) * kRn; }
+    __host__ __device__ static constexpr int round_size(int r) { return r == 0 ? kR0 : kRn; }
+    __device__ static constexpr uint32_t lv_col(int r, int i) { return r == 0 ? 128u + 64u * i : 64u + 64u * i; }
+};
+static_assert(PpCfg::kBytes <= 232448 - 512, "ping-pong output kernel exceeds shared memory");
+
+__global__ void __launch_bounds__(PpCfg::kThreads, 1)
+    tc_output_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_nodes,
+                        const float* __restrict__ tok_cl2, const float* __restrict__ tok_colw,
+                        const float* __restrict__ lambda, const float* __restrict__ dtab,
+                        __nv_bfloat16* __restrict__ out, int T, int NT, int L, int P, int node_count,
+                        const __grid_constant__ LevelOffsets lo, int total_tiles, int* __restrict__ tile_counter,
+                        int* err) {
+    constexpr int DV = 64;
+    constexpr int DH = DV / 2;  // result columns per epilogue warp
+    using C = PpCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t in_full[2], in_empty[2], s_full[2], p_ready[2], lv_full[2], lv_free[2], drain[2];
+    __shared__ uint64_t node_full[2][C::kNodeSlots], node_empty[2][C::kNodeSlots];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int tile_id_sh[2];  // tile of the job in each stage, -1 = no more tiles
+    __shared__ volatile int fail_sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int g = 0; g < 2; g++) {
+            mbar_init(&in_full[g], 1);  // the producer's expect_tx arrive + the bytes
+            mbar_init(&in_empty[g], 1);
+            mbar_init(&s_full[g], 1);
+            mbar_init(&p_ready[g], C::kEpiWarps);
+            mbar_init(&lv_full[g], 1);
+            mbar_init(&lv_free[g], C::kEpiWarps);
+            mbar_init(&drain[g], 1);
+        }
+        for (int g = 0; g < 2; g++)
+            for (int s = 0; s < C::kNodeSlots; s++) {
+                mbar_init(&node_full[g][s], 1);
+                mbar_init(&node_empty[g][s], 1);
+            }
+        fence_mbar_init();
+        fail_sh = 0;
+    }
+    if (warp == 2) tmem_alloc(&tmem_base_sh, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    // head-major; within a head from the last tile down (most Fenwick levels first)
+    auto tile_of = [&](int idx, int& bh, int& j) {
+        bh = idx / NT;
+        j = NT - 1 - (idx - bh * NT);
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (fail_sh) return false;
+        if (mbar_wait(bar, parity)) return true;
+        fail_sh = 1;
+        record_error(err, kDevTimeout);
+        return false;
+    };
+    auto ewait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (__any_sync(0xffffffffu, fail_sh != 0)) return false;
+        if (warp_wait(bar, parity)) return true;
+        if (lane == 0) {
+            fail_sh = 1;
+            record_error(err, kDevTimeout);
+        }
+        return false;
+    };
+
+    if (warp < 2) {
+        // ---------------------------------------------------------------- producer of group g
+        const int g = warp;
+        if (lane == 0) {
+            // a claimed tile's inputs are pulled into L2 at once; the stage copies come later
+            auto claimed = [&](int idx) -> int {
+                if (idx >= total_tiles) return -1;
+                int pbh, pj;
+                tile_of(idx, pbh, pj);
+                const int r0 = pbh * T + pj * kTile;
+                tma_prefetch_l2(&tm_q, 0, r0);
+                tma_prefetch_l2(&tm_q, 64, r0);
+                tma_prefetch_l2(&tm_k, 0, r0);
+                tma_prefetch_l2(&tm_k, 64, r0);
+                tma_prefetch_l2(&tm_v, 0, r0);
+                prefetch_l2(tok_cl2 + r0, 512);
+                const uintptr_t lb = reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r0) * L) & ~uintptr_t(15);
+                const uintptr_t le = (reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r0 + kTile) * L) + 15) &
+                                     ~uintptr_t(15);
+                prefetch_l2(reinterpret_cast<const void*>(lb), static_cast<uint32_t>(le - lb));
+                return idx;
+            };
+            uint8_t* st = smem + g * C::kStageBytes;
+            uint8_t* ring = smem + C::kNodeBase + g * C::kNodeSlots * C::kNodeBytes;
+            int next = claimed(atomicAdd(tile_counter, 1));
+            int gn = 0, n_in = 0;
+            for (int c = 0;; c++) {
+                if (c > 0 && !wait(&in_empty[g], (c - 1) & 1)) break;
+                const int idx = next;
+                tile_id_sh[g] = idx;
+                if (idx < 0) {
+                    mbar_arrive(&in_full[g]);  // end marker
+                    break;
+                }
+                int bh, j;
+                tile_of(idx, bh, j);
+                const int row0 = bh * T + j * kTile;
+                mbar_expect_tx(&in_full[g], C::kQkvBytes + C::kScalarTx);
+                tma_load_2d(st + C::kQ, &tm_q, &in_full[g], 0, row0);
+                tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[g], 64, row0);
+                tma_load_2d(st + C::kK, &tm_k, &in_full[g], 0, row0);
+                tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &in_full[g], 64, row0);
+                tma_load_2d(st + C::kV, &tm_v, &in_full[g], 0, row0);
+                bulk_load(smem + C::kCl2Base + g * 512, tok_cl2 + row0, 512, &in_full[g]);
+                n_in = c + 1;
+                // claim the group's next tile; its index is used once this tile's node copies are issued
+                const int next_idx = atomicAdd(tile_counter, 1);
+                // the tile's Fenwick nodes, in level order, into the group's ring
+                bool ok = true;
+                for (int p = 0; p < P && ok; p++) {
+                    if (((j >> p) & 1) == 0) continue;
+                    const int slot = gn % C::kNodeSlots;
+                    if (gn >= C::kNodeSlots && !wait(&node_empty[g][slot], ((gn / C::kNodeSlots) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const int m = (j >> p) - 1;
+                    const int nrow = (bh * node_count + lo.off[p] + (m >> 1)) * kDk;
+                    mbar_expect_tx(&node_full[g][slot], C::kNodeBytes);
+                    tma_load_2d(ring + slot * C::kNodeBytes, &tm_nodes, &node_full[g][slot], 0, nrow);
+                    gn++;
+                }
+                if (!ok) break;
+                next = claimed(next_idx);
+            }
+            if (fail_sh) {
+                // let this group's copies land before the shared memory is released
+                if (n_in > 0) mbar_wait(&in_full[g], (n_in - 1) & 1);
+                for (int x = gn - C::kNodeSlots; x < gn; x++)
+                    if (x >= 0) mbar_wait(&node_full[g][x % C::kNodeSlots], (x / C::kNodeSlots) & 1);
+            }
+        }
+    } else if (warp < 4) {
+        // ---------------------------------------------------------------- MMA issuer of group g
+        const int g = warp - 2;
+        if (lane == 0) {
+            const uint32_t tb = tmem + 256u * g;
+            constexpr uint32_t kIdS = idesc_bf16(kTile, kTile, 0, 0);
+            constexpr uint32_t kIdO = idesc_bf16(kTile, DV, 0, 1);
+            const uint32_t st = smem_u32(smem + g * C::kStageBytes);
+            const uint32_t qb = st + C::kQ, kb = st + C::kK, vb = st + C::kV;
+            int lvf = 0;  // lv_free phases of this group waited so far
+            int gn = 0;   // nodes of this group's ring consumed so far
+            const uint32_t ring = smem_u32(smem + C::kNodeBase + g * C::kNodeSlots * C::kNodeBytes);
+            // level reads [x0, x1) of the tile, into round r's slots
+            auto levels = [&](int x0, int x1, int r) -> bool {
+                for (int x = x0; x < x1; x++) {
+                    const int slot = gn % C::kNodeSlots;
+                    if (!wait(&node_full[g][slot], (gn / C::kNodeSlots) & 1)) return false;
+                    tc_fence_after();
+                    const uint32_t nb = ring + slot * C::kNodeBytes;
+                    const uint32_t dcol = tb + C::lv_col(r, x - x0);
+#pragma unroll
+                    for (int kk = 0; kk < kDk / 16; kk++) {
+                        const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                        mma_bf16(dcol, sdesc(qb + aoff, 16, 1024), sdesc(nb + kk * 2048, kPanelBytes, 1024), kIdO,
+                                 kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&node_empty[g][slot]);
+                    gn++;
+                }
+                return true;
+            };
+            for (int c = 0;; c++) {
+                if (!wait(&in_full[g], c & 1)) break;
+                const int idx = tile_id_sh[g];
+                if (idx < 0) break;
+                const int n_lv = __popc(static_cast<unsigned>(NT - 1 - idx % NT));
+                const int R = C::rounds(n_lv);
+                // the previous tile of this group is read back: its TMEM columns are free
+                if (c > 0 && !wait(&lv_free[g], (lvf++) & 1)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kDk / 16; kk++) {
+                    const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                    mma_bf16(tb, sdesc(qb + off, 16, 1024), sdesc(kb + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[g]);
+                bool ok = levels(0, min(n_lv, C::kR0), 0);
+                if (!ok) break;
+                mma_commit(&lv_full[g]);
+                // round 1: O = P V once P has replaced K, then the next level reads
+                if (!wait(&p_ready[g], c & 1)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; kk++) {
+                    const uint32_t aoff = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                    mma_bf16(tb, sdesc(kb + aoff, 16, 1024), sdesc(vb + kk * 2048, kPanelBytes, 1024), kIdO,
+                             kk > 0 ? 1u : 0u);
+                }
+                for (int r = 1; r < R && ok; r++) {
+                    if (!wait(&lv_free[g], (lvf++) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int x0 = C::round_begin(r);
+                    ok = levels(min(n_lv, x0), min(n_lv, x0 + C::round_size(r)), r);
+                    if (ok) mma_commit(&lv_full[g]);
+                }
+                if (!ok) break;
+                mma_commit(&in_empty[g]);  // every MMA reading this stage has been issued
+            }
+            mma_commit(&drain[g]);
+            mbar_wait(&drain[g], 0);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue of group g
+        const int ew = warp - C::kFirstEpi;
+        const int g = ew >> 3;
+        const int half = (ew >> 2) & 1;
+        const int quad = warp & 3;
+        const int t = quad * 32 + lane;  // query row = TMEM lane
+        const int q32 = quad * 32;
+        const uint32_t tb = tmem + 256u * g + (static_cast<uint32_t>(q32) << 16);
+        const float* cl2 = reinterpret_cast<const float*>(smem + C::kCl2Base + g * 512);
+        int rnd = 0;  // lv_full phases of this group consumed so far
+        for (int c = 0;; c++) {
+            if (!ewait(&in_full[g], c & 1)) break;
+            const int idx = tile_id_sh[g];
+            if (idx < 0) break;
+            int bh, j;
+            tile_of(idx, bh, j);
+            const int row0 = bh * T + j * kTile;
+            const float cl2_t = cl2[t];
+            // this row's lambda (levels 0..7 for P; 8 + p for the level reads) and the tile's
+            // decay-table row, loaded while S is computed; rr[p] = lambda_t^(8+p) exp(cl_t + D_p)
+            // is the weight of level read p (0 where bit p of j is clear)
+            float lam_in[8];
+            float rr[16];
+            {
+                const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
+#pragma unroll
+                for (int l = 0; l < 8; l++) lam_in[l] = l < L ? lam_row[l] : 0.f;
+                const float4* drow = reinterpret_cast<const float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; c4++) {
+                    const float4 x = drow[c4];
+                    rr[4 * c4] = x.x; rr[4 * c4 + 1] = x.y; rr[4 * c4 + 2] = x.z; rr[4 * c4 + 3] = x.w;
+                }
+#pragma unroll
+                for (int p = 0; p < 16; p++)
+                    rr[p] = (p < P && ((j >> p) & 1)) ? lam_row[8 + p] * exp2f(cl2_t + rr[p]) : 0.f;
+            }
+            // ---- P = (S masked, decayed, lambda-weighted) -> bf16 over K in shared memory
+            if (!ewait(&s_full[g], c & 1)) break;
+            tc_fence_after();
+            uint8_t* pbase = smem + g * C::kStageBytes + C::kK;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kTile; c0 += 32) {
+                const int cb = c0 + half * 16;  // first key of this warp's 16
+                uint32_t pk[8];
+                if (c0 > q32) {
+#pragma unroll
+                    for (int e = 0; e < 8; e++) pk[e] = 0u;
+                } else {
+                    float sv[16];
+                    tmem_ld16(tb + cb, sv);
+                    if (c0 < q32) {
+                        // keys before every row of this warp: one level per row, factorised decay
+                        // exp2(cl_t - cl_s) = exp2(cl_t - cl_{c0+31}) * exp2(cl_{c0+31} - cl_s), both <= 1;
+                        // lane e computes the column factor of key cb + (e & 15)
+                        const int lvl = 32 - __clz(t ^ c0);
+                        float lw = lam_in[0];
+#pragma unroll
+                        for (int l = 1; l < 8; l++) lw = (lvl == l) ? lam_in[l] : lw;
+                        const float cend = cl2[c0 + 31];
+                        const float rowf = exp2f(cl2_t - cend) * lw;
+                        const float cw = exp2f(cend - cl2[cb + (lane & 15)]);
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const float w0 = __shfl_sync(0xffffffffu, cw, e), w1 = __shfl_sync(0xffffffffu, cw, e + 1);
+                            pk[e >> 1] = pack_bf16(sv[e] * rowf * w0, sv[e + 1] * rowf * w1);
+                        }
+                    } else {
+                        // diagonal block: causal mask and per-key levels 0..5
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            float v2[2];
+#pragma unroll
+                            for (int h = 0; h < 2; h++) {
+                                const int sidx = cb + e + h;
+                                const int lvl = 32 - __clz(t ^ sidx);
+                                float lw = lam_in[0];
+#pragma unroll
+                                for (int l = 1; l < 6; l++) lw = (lvl == l) ? lam_in[l] : lw;
+                                const float x = sv[e + h] * exp2f(fminf(cl2_t - cl2[sidx], 0.f)) * lw;
+                                v2[h] = sidx <= t ? x : 0.f;
+                            }
+                            pk[e >> 1] = pack_bf16(v2[0], v2[1]);
+                        }
+                    }
+                }
+                uint8_t* panel = pbase + (c0 >> 6) * kPanelBytes;
+                const int chunk0 = (cb & 63) >> 3;
+                *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(panel + sw128_off(t, chunk0 + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_ready[g]);
+
+            // ---- read back every round: acc = O + sum_p r_p L_p (this warp's half of the columns)
+            const int n_lv = __popc(static_cast<unsigned>(j));
+            const int R = C::rounds(n_lv);
+            float acc[DH];
+#pragma unroll
+            for (int e = 0; e < DH; e++) acc[e] = 0.f;
+            bool ok = true;
+            int p_cur = 0;  // level of the next read
+            for (int r = 0; r < R; r++) {
+                if (!ewait(&lv_full[g], (rnd++) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (r == 1) {
+                    float o[DH];
+                    tmem_ld32(tb + half * DH, o);
+#pragma unroll
+                    for (int e = 0; e < DH; e++) acc[e] += o[e];
+                }
+                const int x0 = min(n_lv, C::round_begin(r)), x1 = min(n_lv, C::round_begin(r) + C::round_size(r));
+#pragma unroll 1
+                for (int x = x0; x < x1; x++) {
+                    while (((j >> p_cur) & 1) == 0) p_cur++;
+                    float w = rr[0];
+#pragma unroll
+                    for (int i = 1; i < 16; i++) w = (p_cur == i) ? rr[i] : w;
+                    p_cur++;
+                    float lv[DH];
+                    tmem_ld32(tb + C::lv_col(r, x - x0) + half * DH, lv);
+#pragma unroll
+                    for (int e = 0; e < DH; e++) acc[e] = fmaf(w, lv[e], acc[e]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&lv_free[g]);
+            }
+            if (!ok) break;
+            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV + half * DH);
+#pragma unroll
+            for (int c8 = 0; c8 < DH / 8; c8++)
+                dst[c8] = make_uint4(pack_bf16(acc[8 * c8], acc[8 * c8 + 1]), pack_bf16(acc[8 * c8 + 2], acc[8 * c8 + 3]),
+                                     pack_bf16(acc[8 * c8 + 4], acc[8 * c8 + 5]),
+                                     pack_bf16(acc[8 * c8 + 6], acc[8 * c8 + 7]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) tmem_dealloc(tmem, 512);
+}
+
 // ------------------------------------------------------------------ host side
 
 // Segment size 2^q: the node kernel keeps q level accumulators of dv/2 floats per
@@ -999,16 +1412,26 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
         if (e != cudaSuccess || nodes_only) return e;
     }
     {
-        const int smem = OutCfg<DV>::kBytes;
-        cudaError_t e = cudaFuncSetAttribute(tc_output_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
         const int L = bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
         const int total = BH * pl.NT;
         const int grid = total < pl.num_sms ? total : pl.num_sms;
-        tc_output_kernel<DV><<<grid, OutCfg<DV>::kThreads, smem, stream>>>(tq, tk, tv, tn, tok_cl2, tok_colw, lambda, dtab,
-                                                                            static_cast<__nv_bfloat16*>(out), pl.T,
-                                                                            pl.NT, L, pl.P, pl.node_count, lo, total,
-                                                                            tile_counter, err);
+        if constexpr (DV == 64) {
+            const int smem = PpCfg::kBytes;
+            cudaError_t e =
+                cudaFuncSetAttribute(tc_output_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            tc_output_pp_kernel<<<grid, PpCfg::kThreads, smem, stream>>>(
+                tq, tk, tv, tn, tok_cl2, tok_colw, lambda, dtab, static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L,
+                pl.P, pl.node_count, lo, total, tile_counter, err);
+        } else {
+            const int smem = OutCfg<DV>::kBytes;
+            cudaError_t e =
+                cudaFuncSetAttribute(tc_output_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            tc_output_kernel<DV><<<grid, OutCfg<DV>::kThreads, smem, stream>>>(
+                tq, tk, tv, tn, tok_cl2, tok_colw, lambda, dtab, static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L,
+                pl.P, pl.node_count, lo, total, tile_counter, err);
+        }
         note_launch(stream, "tc_output");
     }
     return cudaGetLastError();
