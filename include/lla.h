@@ -31,6 +31,11 @@
  *    Faults found by a kernel (an out-of-range decode position, a bounded wait
  *    that ran out) are recorded in a per-device error word and reported by
  *    lla_device_error(). No kernel traps and the library never exits.
+ *  - The library keeps per-device state for the life of the process: the device
+ *    address of its error word and of the lla_forward_noalloc scratch, looked up
+ *    once, and a memory pool. Do not call it on a device after cudaDeviceReset()
+ *    (or any teardown of that device's primary context) in the same process: the
+ *    cached addresses would no longer be valid.
  */
 #ifndef LLA_H
 #define LLA_H
@@ -75,7 +80,7 @@ int lla_num_levels(int64_t T);
  *   chunk  chunk length of the scan: 16, 32, 64 or 128, with T % chunk == 0.
  *          It sets how keys are grouped into inter-chunk states; the result is
  *          the same operator for every valid chunk (up to rounding order).
- *   dk, dv 1..128; the bf16 tensor-core path runs for dk == 128, dv in {64,128},
+ *   dk, dv 1..128; the bf16 tensor-core path runs for dk in {64,128}, dv in {64,128},
  *          T % 128 == 0; other shapes run the fp32 SIMT path.
  *
  * Scratch: the call takes its workspace (inter-chunk states) from a
@@ -123,7 +128,8 @@ int lla_forward_ws(const void* q, const void* k, const void* v, const float* log
  * with LLA_ERR_NOMEM before anything is enqueued. No cudaMalloc, cudaFree or
  * allocating library routine is called.
  *  - The first call on a device looks up that device's copy of the array; make
- *    that first call before capturing a stream into a CUDA graph.
+ *    that first call before capturing a stream into a CUDA graph. The address is
+ *    kept for the life of the process (see the cudaDeviceReset note above).
  *  - Every call on a device shares the one array and leaves its contents
  *    behind; no part of it needs to start at zero (each call writes every
  *    scratch value before reading it). Calls whose work overlaps on the GPU
@@ -252,6 +258,20 @@ int lla_forward_varlen(const void* q, const void* k, const void* v, const float*
 int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, const int32_t* cu_seqlens,
                              float* fenwick_states, int n_seq, int H, int total_T, int max_T, int dk, int dv, int Lmax,
                              void* stream, int dtype);
+
+/*
+ * Test hook for the failure path of the bounded waits (no counterpart on the
+ * pages; not for production use). On the current device, for the tensor-core
+ * prefill output kernel of dv = 64: limit_cycles > 0 bounds each of its pipeline
+ * waits to that many SM cycles (<= 0 restores the default, about 2 s at the
+ * maximum clock); hold != 0 makes its epilogue first wait on a barrier that
+ * nothing arrives at, so that wait runs out. The kernel then records
+ * LLA_ERR_TIMEOUT in the device error word, lets its own in-flight copies and
+ * MMAs land (those drain waits keep the full bound), frees its tensor memory and
+ * returns; the call's output is then undefined. Synchronous with the host; takes
+ * effect for kernels launched afterwards. Returns LLA_OK or LLA_ERR_CUDA.
+ */
+int lla_debug_set_waits(int64_t limit_cycles, int hold);
 
 /*
  * Reads and clears the device error word of the current device after

@@ -1,6 +1,10 @@
 // Tensor-core (tcgen05 / TMEM / TMA) path of log-linear Mamba-2 attention
-// prefill, bf16 q/k/v with fp32 accumulation, dk = 128, dv in {64, 128},
-// T % 128 == 0.
+// prefill, bf16 q/k/v with fp32 accumulation, dk in {64, 128}, dv in {64, 128},
+// T % 128 == 0. dk = 64 runs the dk = 128 kernels on zero-padded operands: the
+// tensor maps of q and k have the real 64 columns, so the second 64-column panel
+// of every Q and K tile lies wholly outside the tensor and TMA fills it with
+// zeros; every product over dk is then the 64-column one, and the Fenwick nodes
+// (128 x dv) carry zero rows 64..127.
 //
 // Chunkwise algorithm ("Log-Linear Attention", pt §2 "Forma Recorrente e
 // Paralela" / fr §2 "Algorithmes Efficaces": dense intra-block work,
@@ -34,6 +38,14 @@
 #include "lla_tc_ptx.cuh"
 
 namespace lla {
+
+// Failure-path test hooks of tc_output_pp (set from the host by tc_set_debug_waits):
+// the bound, in SM cycles, on the kernel's pipeline waits (its drain waits, which let
+// in-flight copies and MMAs land, always keep the full bound), and a switch that makes
+// the epilogue first wait on a barrier nothing arrives at, so that wait runs out.
+__device__ long long tc_pipe_wait_limit = 4000000000LL;
+__device__ int tc_debug_hold = 0;
+
 namespace {
 
 struct LevelOffsets { int off[32]; };
@@ -976,6 +988,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t in_full[2], in_empty[2], s_full[2], p_ready[2], lv_full[2], lv_free[2], drain[2];
     __shared__ uint64_t node_full[2][C::kNodeSlots], node_empty[2][C::kNodeSlots];
+    __shared__ uint64_t never;  // nothing arrives at it (failure-path test hook)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int tile_id_sh[2];  // tile of the job in each stage, -1 = no more tiles
     __shared__ volatile int fail_sh;
@@ -996,6 +1009,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 mbar_init(&node_full[g][s], 1);
                 mbar_init(&node_empty[g][s], 1);
             }
+        mbar_init(&never, 1);
         fence_mbar_init();
         fail_sh = 0;
     }
@@ -1010,16 +1024,17 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
         bh = idx / NT;
         j = NT - 1 - (idx - bh * NT);
     };
+    const long long lim = tc_pipe_wait_limit;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         if (fail_sh) return false;
-        if (mbar_wait(bar, parity)) return true;
+        if (mbar_wait(bar, parity, lim)) return true;
         fail_sh = 1;
         record_error(err, kDevTimeout);
         return false;
     };
     auto ewait = [&](uint64_t* bar, uint32_t parity) -> bool {
         if (__any_sync(0xffffffffu, fail_sh != 0)) return false;
-        if (warp_wait(bar, parity)) return true;
+        if (warp_wait(bar, parity, lim)) return true;
         if (lane == 0) {
             fail_sh = 1;
             record_error(err, kDevTimeout);
@@ -1184,7 +1199,9 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
         const uint32_t tb = tmem + 256u * g + (static_cast<uint32_t>(q32) << 16);
         const float* cl2 = reinterpret_cast<const float*>(smem + C::kCl2Base + g * 512);
         int rnd = 0;  // lv_full phases of this group consumed so far
-        for (int c = 0;; c++) {
+        // test hook: a wait that runs out (records the timeout; every role then leaves)
+        const bool held = tc_debug_hold != 0 && !ewait(&never, 0);
+        for (int c = 0; !held; c++) {
             if (!ewait(&in_full[g], c & 1)) break;
             const int idx = tile_id_sh[g];
             if (idx < 0) break;
@@ -1400,7 +1417,7 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
     const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
 
     CUtensorMap tq, tk, tv, tn;
-    if (!make_map(&tq, q, rows, kDk) || !make_map(&tk, k, rows, kDk) || !make_map(&tv, v, rows, DV))
+    if (!make_map(&tq, q, rows, pl.dk) || !make_map(&tk, k, rows, pl.dk) || !make_map(&tv, v, rows, DV))
         return cudaErrorInvalidValue;
     const bool have_nodes = pl.node_count > 0;
     if (have_nodes && !make_map(&tn, nodes, static_cast<uint64_t>(BH) * pl.node_count * kDk, DV))
@@ -1439,8 +1456,16 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
 
 }  // namespace
 
+cudaError_t tc_set_debug_waits(long long limit_cycles, int hold) {
+    const long long lim = limit_cycles > 0 ? limit_cycles : kWaitCycles;
+    const int h = hold != 0;
+    cudaError_t e = cudaMemcpyToSymbol(tc_pipe_wait_limit, &lim, sizeof(lim));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(tc_debug_hold, &h, sizeof(h));
+    return e;
+}
+
 bool tc_supported(int dtype, int dk, int dv, int T) {
-    return dtype == 0 && dk == kDk && (dv == 64 || dv == 128) && T % kTile == 0;
+    return dtype == 0 && (dk == 64 || dk == kDk) && (dv == 64 || dv == 128) && T % kTile == 0;
 }
 
 bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* pl) {
@@ -1470,7 +1495,7 @@ bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* pl) {
     if (pl->P - 1 - pl->q > 10) return false;  // the merge kernel weighs at most 1024 segments per node
     if (pl->NT > 8192) return false;            // and holds a head's tile totals in shared memory
     if (static_cast<int64_t>(BH) * pl->node_count * kDk >= (int64_t(1) << 31)) return false;
-    const size_t msz = static_cast<size_t>(dk) * dv;
+    const size_t msz = static_cast<size_t>(kDk) * dv;  // nodes are 128 x dv (dk = 64 pads rows 64..127)
     pl->g_bytes = (static_cast<size_t>(BH) * pl->NT * sizeof(float) + 1023) / 1024 * 1024;
     pl->nodes_bytes = (static_cast<size_t>(BH) * pl->node_count * msz * 2 + 1023) / 1024 * 1024;
     pl->seg_bytes = (static_cast<size_t>(BH) * nseg * msz * sizeof(float) + 1023) / 1024 * 1024;

@@ -78,6 +78,27 @@ def test_small_bf16():
     assert rel_err_per_head(got, oracle_full(inp)) <= TOL_BF16
 
 
+def test_small_bf16_runs_on_tensor_cores():
+    """dk = dv = 64 in bf16 takes the tcgen05 kernels (q and k zero-padded to 128 columns by
+    TMA), not the fp32 CUDA-core kernels."""
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.PREFILL_CONFIGS["small"]
+    inp = inputs.make_prefill(cfg, seed=2)
+    q, k, v, log_a, lam = to_device(inp)
+    names = [n for n, _ in binding.forward_profile(q, k, v, log_a, lam, cfg.chunk, torch.empty_like(v))]
+    assert names == ["tc_nodes", "tc_merge", "tc_output"], names
+
+
+@pytest.mark.parametrize("T,dv", [(256, 64), (1152, 128)])
+def test_bf16_dk64_shapes(T, dv):
+    """dk = 64 on the tensor-core path at dv = 64 and 128, several tiles and a tile count
+    that is not a power of two."""
+    cfg = cfg_like("small", B=2, H=1, T=T, dv=dv, chunk=64)
+    inp = inputs.make_prefill(cfg, seed=T + 17)
+    got = run(inp, 64)
+    assert rel_err_per_head(got, oracle_full(inp)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("T,dv,chunk", [(128, 64, 64), (1024, 64, 64), (640, 64, 128), (2048, 128, 128),
                                         (384, 64, 32)])
 def test_bf16_dk128_shapes(T, dv, chunk):
