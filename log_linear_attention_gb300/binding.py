@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
             lib.lla_prefill_state.restype = i
             lib.lla_device_error.argtypes = [vp]
             lib.lla_device_error.restype = i
+            lib.lla_debug_set_waits.argtypes = [ctypes.c_int64, i]
+            lib.lla_debug_set_waits.restype = i
             lib.lla_backward.argtypes = [vp, vp, vp, fp, fp, vp, vp, vp, vp, fp, fp] + [i] * 6 + [vp, i]
             lib.lla_backward.restype = i
             lib.lla_forward_varlen.argtypes = [vp, vp, vp, fp, fp, vp, vp] + [i] * 7 + [vp, i]
@@ -216,6 +218,11 @@ def forward_profile(q, k, v, log_a, lam, chunk: int, out, stream=None):
     if n < 0:
         raise LLAError(n, "lla_forward_profile")
     return [(names[i].decode(), float(ms[i])) for i in range(min(n, cap))]
+
+
+def debug_set_waits(limit_cycles: int, hold: bool) -> None:
+    """lla_debug_set_waits: test hook of the bounded waits (see include/lla.h)."""
+    _call(load().lla_debug_set_waits(int(limit_cycles), 1 if hold else 0), "lla_debug_set_waits")
 
 
 def workspace_size(B: int, H: int, T: int, dk: int, dv: int, chunk: int, dtype) -> int:

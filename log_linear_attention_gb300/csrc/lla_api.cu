@@ -512,6 +512,11 @@ int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, c
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }
 
+int lla_debug_set_waits(int64_t limit_cycles, int hold) {
+    if (current_device() < 0) return LLA_ERR_CUDA;
+    return lla::tc_set_debug_waits(static_cast<long long>(limit_cycles), hold) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
 int lla_device_error(void* stream) {
     const int dev = current_device();
     if (dev < 0) return LLA_ERR_CUDA;

@@ -83,6 +83,10 @@ bool tc_supported(int dtype, int dk, int dv, int T);
 bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* plan);
 cudaError_t tc_forward(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
                        const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream);
+// Failure-path test hooks of the dv = 64 output kernel on the current device: the bound
+// on its pipeline waits (limit_cycles <= 0: the default of about 2 s) and a wait that
+// nothing completes (hold != 0).
+cudaError_t tc_set_debug_waits(long long limit_cycles, int hold);
 // The node stage of tc_forward only (tc_nodes + tc_merge), for the backward.
 cudaError_t tc_nodes_only(const TcPlan& plan, const void* k, const void* v, const float* log_a, void* workspace,
                           int* err, cudaStream_t stream);

@@ -54,11 +54,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity to complete (limit in SM cycles).
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit = kWaitCycles) {
     const long long start = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - start > kWaitCycles) return false;
+        if (clock64() - start > limit) return false;
     }
     return true;
 }
@@ -241,12 +241,12 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
 
 
 // Bounded wait taken by a whole warp: every lane polls, the warp leaves together.
-__device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+__device__ __noinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long long limit = kWaitCycles) {
     const long long start = clock64();
     while (true) {
         const bool done = mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, done)) return true;
-        const bool late = clock64() - start > kWaitCycles;
+        const bool late = clock64() - start > limit;
         if (__any_sync(0xffffffffu, late)) return false;
     }
 }
