@@ -66,3 +66,33 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     st = lib.lla_forward_noalloc(*(x.data_ptr() for x in big), cfg.B, cfg.H, cfg.T, cfg.dk, cfg.dv, cfg.chunk,
                                  None, binding.LLA_BF16)
     assert st == binding.LLA_ERR_NOMEM
+
+
+@pytest.mark.parametrize("name,tol", [("headline", 2e-2), ("oracle-scale", 1e-4)])
+def test_noalloc_second_call_ignores_poisoned_scratch(name, tol):
+    """The first call of each pair runs on a value tensor holding NaN and infinity, so the
+    inter-chunk states it leaves in the shared scratch are not finite. The next call, on
+    clean inputs of the same shape, must not read any of them: its output is finite and
+    matches the regular entry point."""
+    from log_linear_attention_gb300 import binding
+    over = dict(B=1, H=4, T=2048) if name == "headline" else dict(B=2, H=3, T=192, dk=24, dv=40, chunk=64)
+    cfg = _cfg(name, **over)
+    inp = inputs.make_prefill(cfg, seed=300)
+    q, k, v, log_a, lam = to_device(inp)
+    poisoned = v.clone()
+    poisoned.view(-1)[:: 97] = float("nan")
+    poisoned.view(-1)[5:: 131] = float("inf")
+    sink = torch.empty_like(v)
+    for _ in range(2):
+        binding.forward_noalloc(q, k, poisoned, log_a, lam, cfg.chunk, sink)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        assert not torch.isfinite(sink.float()).all()  # the poison reached the scratch
+        got = torch.full_like(v, float("nan"))
+        binding.forward_noalloc(q, k, v, log_a, lam, cfg.chunk, got)
+        want = binding.forward(q, k, v, log_a, lam, cfg.chunk)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        g = got.float().cpu().numpy()
+        assert np.isfinite(g).all()
+        assert rel_err_per_head(g, want.float().cpu().numpy()) <= tol
