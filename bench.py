@@ -291,6 +291,57 @@ def oracle_tokens_per_s(cfg: inputs.PrefillConfig, inp: inputs.PrefillInputs, bu
     return tokens / dt, f"{heads} of {cfg.B * cfg.H} heads x {T} tokens (recurrent form), scaled by 1/H", dt
 
 
+def cpu_info() -> dict:
+    """Host CPU model and core count (the CPU baseline runs on these cores)."""
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "cpu model", "hardware"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or "unknown"}
+
+
+def oracle_tokens_per_s_all_cores(cfg: inputs.PrefillConfig, inp: inputs.PrefillInputs, budget_s: float):
+    """The same oracle (single-threaded C, unchanged) on every host core at once: a thread
+    pool over independent (b, h) heads (the ctypes calls release the GIL). Returns
+    (tokens/s in whole-token units, threads used, sample text)."""
+    import concurrent.futures
+    import oracle
+    n = os.cpu_count() or 1
+    T = cfg.T
+    L = inputs.num_levels(T)
+
+    def one(bh):
+        b, h = divmod(bh, cfg.H)
+        sl = (slice(b, b + 1), slice(h, h + 1), slice(0, T))
+        oracle.recurrent(inp.q[sl], inp.k[sl], inp.v[sl], inp.log_a[sl], inp.lam[sl][..., :L])
+        return 1
+
+    heads = 0
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+        nxt = 0
+        while nxt < cfg.B * cfg.H and time.perf_counter() - t0 < budget_s:
+            batch = list(range(nxt, min(nxt + n, cfg.B * cfg.H)))
+            nxt += len(batch)
+            heads += sum(ex.map(one, batch))
+    dt = time.perf_counter() - t0
+    return heads * T / cfg.H / dt, n, f"{heads} of {cfg.B * cfg.H} heads x {T} tokens (recurrent form) on {n} threads"
+
+
 def run_reference(args, cfg):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -426,6 +477,59 @@ def bench_decode(args, dev, stream, rank, ws):
     return d_ms_total, dbytes, dsteps
 
 
+def bench_prefill_config(args, dev, stream, name, peaks) -> dict:
+    """One more prefill workload of the stated configs (inputs drawn on the device with that
+    config's distributions): time per call, throughput, and the roofline of its dominant
+    kernel, measured the same way as the headline."""
+    import torch
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.PREFILL_CONFIGS[name]
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    shp = (cfg.B, cfg.H, cfg.T)
+
+    def qk():
+        x = torch.randn(shp + (cfg.dk,), device=dev, generator=g)
+        x = x / x.norm(dim=-1, keepdim=True) if cfg.qk_unit_rows else x * cfg.dk ** -0.5
+        return x.to(torch.bfloat16)
+
+    q, k = qk(), qk()
+    v = torch.randn(shp + (cfg.dv,), device=dev, generator=g).to(torch.bfloat16)
+    la = -torch.nn.functional.softplus(torch.randn(shp, device=dev, generator=g) + cfg.log_a_mu)
+    lam = torch.nn.functional.softplus(torch.randn(shp + (cfg.L,), device=dev, generator=g))
+    out = torch.empty(shp + (cfg.dv,), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        binding.forward(q, k, v, la, lam, cfg.chunk, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    n = max(5, min(args.steps, 30))
+    ms = cuda_time(step, n, stream) / n
+    per = {}
+    for _ in range(max(3, min(args.steps, 10))):
+        for kname, kms in binding.forward_profile(q, k, v, la, lam, cfg.chunk, out):
+            per.setdefault(kname, []).append(kms)
+    assert binding.device_error() == 0
+    kavg = {kn: sum(x) / len(x) for kn, x in per.items()}
+    top = max(kavg, key=kavg.get)
+    kw = kernel_work(top, cfg)
+    work = prefill_work(cfg)
+    if kw["bound"] == "hbm":
+        achieved, peak, unit = kw["bytes"] / (kavg[top] / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = kw["flops"] / (kavg[top] / 1e3) / 1e12, ALU_F32_TFLOPS, "TFLOP/s"
+    return {"workload": f"{cfg.name} prefill: B={cfg.B} H={cfg.H} T={cfg.T} dk={cfg.dk} dv={cfg.dv} "
+                        f"chunk={cfg.chunk}, bf16 q/k/v ({cfg.L} levels), inputs drawn on the device",
+            "ms": ms, "tokens_per_s": cfg.tokens / (ms / 1e3),
+            "tflops": work["flops"] / (ms / 1e3) / 1e12, "algorithmic_gflop": work["flops"] / 1e9,
+            "frac_of_bf16_peak": work["flops"] / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+            "hbm_frac_of_call": work["bytes"] / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "roofline": {"kernel": top, "bound": kw["bound"], "achieved": achieved, "peak": peak, "unit": unit,
+                         "frac": achieved / peak, "kernel_ms": kavg[top]},
+            "kernels_ms": kavg}
+
+
 def run_lla(args, cfg):
     import torch
     from log_linear_attention_gb300 import binding
@@ -555,8 +659,19 @@ def run_lla(args, cfg):
     h2d = sum(h.numel() * h.element_size() for h in host)
     d2h = out.numel() * out.element_size()
 
+    # pinned host <-> device copy rates on this machine: the ceiling of the e2e number
+    cbuf_h = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    cbuf_d = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        cbuf_d.copy_(cbuf_h, non_blocking=True)
+        cbuf_h.copy_(cbuf_d, non_blocking=True)
+    h2d_ms = cuda_time(lambda: cbuf_d.copy_(cbuf_h, non_blocking=True), 5, stream) / 5
+    d2h_ms = cuda_time(lambda: cbuf_h.copy_(cbuf_d, non_blocking=True), 5, stream) / 5
+    del cbuf_h, cbuf_d
+
     d_ms_total, dbytes, dsteps = bench_decode(args, dev, stream, rank, ws)
     d_gbs = ws * dbytes / (d_ms_total / 1e3) / 1e9
+    sub = {name: bench_prefill_config(args, dev, stream, name, peaks) for name in ("small", "long")}
 
     # ---- prefill -> decode hand-off: the state set after the whole prompt
     hL = inputs.num_levels(cfg.T + 1)
@@ -590,6 +705,8 @@ def run_lla(args, cfg):
     if rank == 0:
         # CPU baseline: the oracle as it stands, on the host cores, bounded sample
         cpu_val, cpu_sample, _ = oracle_tokens_per_s(cfg, inp, args.cpu_budget)
+        cpu_all, cpu_threads, cpu_all_sample = oracle_tokens_per_s_all_cores(cfg, inp, args.cpu_budget)
+        cpu = cpu_info()
         line = {
             "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -622,10 +739,17 @@ def run_lla(args, cfg):
                          "frac_of_hbm": bw["bytes"] / (b_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                          "peak_source": peaks["source"]},
             "varlen": vl,
+            "small": sub["small"],
+            "long": sub["long"],
             "e2e": {"value": ws * cfg.tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                    "pinned_copy_gbs": {"h2d": (256 << 20) / (h2d_ms / 1e3) / 1e9,
+                                        "d2h": (256 << 20) / (d2h_ms / 1e3) / 1e9},
+                    "copy_bound_ms": h2d / ((256 << 20) / (h2d_ms / 1e3)) * 1e3},
             "cpu_baseline": {"value": cpu_val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": cpu_sample},
+                             "sample": cpu_sample, **cpu,
+                             "all_cores": {"value": cpu_all, "unit": "tokens/s", "cores": cpu_threads,
+                                           "sample": cpu_all_sample}},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "peaks": {k_: peaks[k_] for k_ in ("hbm_gbs", "bf16_tflops", "source")},
