@@ -7,7 +7,10 @@ patterns, the oracle gets the same values widened to fp64.
 
 Distributions follow the workload shapes of the benchmark configurations:
 q, k ~ N(0, 1/dk) (or unit-norm rows), v ~ N(0, 1), log_a = -softplus(N(mu, 1)),
-lambda = softplus(N(0, 1)) for every Fenwick level.
+lambda = softplus(N(0, 1)) for every Fenwick level. The Gated DeltaNet variant
+adds the delta-rule strength beta = sigmoid(N(0, 1)) per token and always uses
+unit-norm key rows (the delta rule's transition I - beta k k^T is then a
+contraction for beta in [0, 1]).
 """
 from __future__ import annotations
 
@@ -80,6 +83,21 @@ PREFILL_CONFIGS = {
 }
 
 DECODE_CONFIG = DecodeConfig("decode", batch=64, H=16, dk=128, dv=64, t_max=65536, steps=1000)
+
+# Log-linear Gated DeltaNet workloads: the Mamba-2 prefill shapes with unit-norm q and k rows.
+GDN_CONFIGS = {
+    "gdn-oracle-scale": PrefillConfig("gdn-oracle-scale", 1, 1, 64, 16, 16, 16, "f32", qk_unit_rows=True),
+    "gdn-small": PrefillConfig("gdn-small", 2, 4, 2048, 64, 64, 64, "bf16", qk_unit_rows=True),
+    "gdn-headline": PrefillConfig("gdn-headline", 4, 16, 8192, 128, 64, 64, "bf16", qk_unit_rows=True,
+                                  log_a_mu=-2.0),
+}
+
+
+def make_beta(seed: int, shape) -> np.ndarray:
+    """Delta-rule strengths beta = sigmoid(N(0, 1)), float32, for the given shape."""
+    shape = tuple(int(x) for x in shape)
+    rng = np.random.default_rng(np.random.SeedSequence([0xBE7A, seed, *shape]))
+    return (1.0 / (1.0 + np.exp(-rng.standard_normal(shape)))).astype(np.float32)
 
 
 @dataclass

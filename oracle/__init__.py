@@ -1,4 +1,5 @@
-"""Plain fp64 CPU oracle for causal log-linear Mamba-2 attention.
+"""Plain fp64 CPU oracle for causal log-linear Mamba-2 attention and for the
+log-linear Gated DeltaNet.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package; the product path
@@ -59,6 +60,12 @@ def _load():
             lib.lla_oracle_backward.restype = None
             lib.lla_oracle_backward_rows.argtypes = [dp] * 6 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int] + [dp] * 5
             lib.lla_oracle_backward_rows.restype = None
+            lib.lla_oracle_gdn_explicit.argtypes = [dp] * 7 + [ctypes.c_int] * 6
+            lib.lla_oracle_gdn_explicit.restype = None
+            lib.lla_oracle_gdn_recurrent.argtypes = [dp] * 7 + [ctypes.c_int] * 6
+            lib.lla_oracle_gdn_recurrent.restype = ctypes.c_int
+            lib.lla_oracle_gdn_decode_step.argtypes = [dp] * 7 + [i64p, dp] + [ctypes.c_int] * 5
+            lib.lla_oracle_gdn_decode_step.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -172,6 +179,57 @@ def decode_step(q, k, v, log_a, lam, states, t):
     rc = _load().lla_oracle_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(lam), _ptr(states),
                                         t.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _ptr(out),
                                         B, H, dk, dv, Lmax)
+    if rc != 0:
+        raise ValueError("decode position needs more levels than the state set holds")
+    return out
+
+
+# ----------------------------------------------------------------------------- Gated DeltaNet
+
+def _check_gdn(q, k, v, log_a, beta, lam):
+    q, k, v, log_a, lam, dims = _check_forward(q, k, v, log_a, lam)
+    beta = _f64(beta)
+    assert beta.shape == log_a.shape
+    return q, k, v, log_a, beta, lam, dims
+
+
+def gdn_explicit(q, k, v, log_a, beta, lam) -> np.ndarray:
+    """Log-linear Gated DeltaNet, explicit O(T^2) form: o_t = sum_{s<=t} lambda_t^(l(t,s)) A[t,s] v_s with
+    A[t,s] = beta_s k_s^T A_{s+1} ... A_t q_t and A_r = exp(log_a_r) (I - beta_r k_r k_r^T); fp64."""
+    q, k, v, log_a, beta, lam, (B, H, T, dk, dv, L) = _check_gdn(q, k, v, log_a, beta, lam)
+    out = np.zeros((B, H, T, dv), dtype=np.float64)
+    _load().lla_oracle_gdn_explicit(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(beta), _ptr(lam), _ptr(out),
+                                    B, H, T, dk, dv, L)
+    return out
+
+
+def gdn_recurrent(q, k, v, log_a, beta, lam) -> np.ndarray:
+    """Log-linear Gated DeltaNet, token-by-token Fenwick recurrence (every held bucket evolves under
+    the gated delta-rule transition, lowbit-carry merges); fp64."""
+    q, k, v, log_a, beta, lam, (B, H, T, dk, dv, L) = _check_gdn(q, k, v, log_a, beta, lam)
+    out = np.zeros((B, H, T, dv), dtype=np.float64)
+    rc = _load().lla_oracle_gdn_recurrent(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(beta), _ptr(lam),
+                                          _ptr(out), B, H, T, dk, dv, L)
+    if rc != 0:
+        raise MemoryError("oracle state allocation failed")
+    return out
+
+
+def gdn_decode_step(q, k, v, log_a, beta, lam, states, t):
+    """One log-linear Gated DeltaNet decode step for a batch, fp64; ``states`` [B,H,Lmax,dk,dv]
+    (C-contiguous float64) is updated in place; returns ``out`` [B,H,dv]."""
+    q, k, v, log_a, beta, lam = (_f64(x) for x in (q, k, v, log_a, beta, lam))
+    assert isinstance(states, np.ndarray) and states.dtype == np.float64 and states.flags.c_contiguous
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.int64))
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    Lmax = states.shape[2]
+    assert states.shape == (B, H, Lmax, dk, dv) and lam.shape == (B, H, Lmax) and t.shape == (B,)
+    assert beta.shape == (B, H) and log_a.shape == (B, H)
+    out = np.zeros((B, H, dv), dtype=np.float64)
+    rc = _load().lla_oracle_gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(beta), _ptr(lam),
+                                            _ptr(states), t.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                            _ptr(out), B, H, dk, dv, Lmax)
     if rc != 0:
         raise ValueError("decode position needs more levels than the state set holds")
     return out

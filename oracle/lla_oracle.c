@@ -1,5 +1,6 @@
 /*
- * Plain CPU oracle for the causal log-linear Mamba-2 attention operator.
+ * Plain CPU oracle for the causal log-linear Mamba-2 attention operator and
+ * for its Gated DeltaNet counterpart (end of the file).
  *
  * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
  * call this file; only the tests, the smoke check and the CPU-baseline leg of
@@ -364,6 +365,162 @@ int lla_oracle_decode_step(const double* q, const double* k, const double* v,
             size_t bh = (size_t)b * H + h;
             recurrent_step(states + bh * Lmax * msz, q + bh * dk, k + bh * dk, v + bh * dv,
                            log_a[bh], lambda + bh * Lmax, tb, dk, dv, Lmax, out + bh * dv);
+        }
+    }
+    return 0;
+}
+
+/* ======================================================================
+ * Log-Linear Gated DeltaNet.
+ *
+ * Sources: pt §2 "Generalizacao" and pt §4, fr §3 "Cadre General" and
+ * "Etudes de Cas" ("Log-Linear Attention"): the log-linear framework is
+ * applied on top of an existing linear-attention model by replacing its
+ * temporal mask with the hierarchical one, P = A (.) M_H (pt §2 "Mascara
+ * Hierarquica"); Gated DeltaNet is the second model it is applied to. The
+ * recurrent form keeps the same O(log T) Fenwick bucket states: the new token
+ * updates the finest level and levels merge along the tree (pt §2 "Forma
+ * Recorrente e Paralela", fr §2 "Algorithmes Efficaces").
+ *
+ * Readings (the pages do not define Gated DeltaNet itself; its published
+ * recurrence is taken as the base model):
+ *   - base recurrence, states dk x dv: S_t = A_t S_{t-1} + beta_t k_t v_t^T with
+ *     the gated delta-rule transition A_t = alpha_t (I - beta_t k_t k_t^T),
+ *     alpha_t = exp(log_a_t), beta_t in [0,1] a per-token input; o_t = S_t^T q_t;
+ *   - its attention matrix (the coefficient of v_s in o_t) is
+ *     A[t,s] = beta_s k_s^T A_{s+1} A_{s+2} ... A_t q_t (s <= t);
+ *   - log-linear: o_t = sum_{s<=t} lambda_t^(l(t,s)) A[t,s] v_s, with the Fenwick
+ *     level l(t,s) and query-indexed lambda of the Mamba-2 variant above;
+ *   - recurrently: every held bucket state evolves under A_t, buckets merge on
+ *     the lowbit carry, and the new token's beta_t k_t v_t^T is level 0.
+ * Layouts as above, plus beta [B,H,T] (decode: [B,H]).
+ * ====================================================================== */
+
+/* x <- A_t x = alpha (x - beta k (k . x)) for one dk-vector x. */
+static void gdn_transition_vec(double* x, const double* kt, double alpha, double beta, int dk)
+{
+    double kx = 0.0;
+    for (int i = 0; i < dk; i++) kx += kt[i] * x[i];
+    for (int i = 0; i < dk; i++) x[i] = alpha * (x[i] - beta * kt[i] * kx);
+}
+
+/* Explicit form: o_t = sum_{s<=t} lambda_t^(l(t,s)) A[t,s] v_s. For each query
+ * the vector u = A_{s+1} ... A_t q_t is carried while s walks down from t:
+ * u starts at q_t; key s contributes A[t,s] = beta_s (k_s . u); then u <- A_s u. */
+void lla_oracle_gdn_explicit(const double* q, const double* k, const double* v,
+                             const double* log_a, const double* beta, const double* lambda,
+                             double* out, int B, int H, int T, int dk, int dv, int L)
+{
+    double* u = (double*)malloc((size_t)(dk > 0 ? dk : 1) * sizeof(double));
+    if (!u) return;
+    for (int bh = 0; bh < B * H; bh++) {
+        const double* qh = q + (size_t)bh * T * dk;
+        const double* kh = k + (size_t)bh * T * dk;
+        const double* vh = v + (size_t)bh * T * dv;
+        const double* ah = log_a + (size_t)bh * T;
+        const double* bth = beta + (size_t)bh * T;
+        const double* lh = lambda + (size_t)bh * T * L;
+        double* oh = out + (size_t)bh * T * dv;
+        for (int t = 0; t < T; t++) {
+            double* o = oh + (size_t)t * dv;
+            for (int j = 0; j < dv; j++) o[j] = 0.0;
+            for (int i = 0; i < dk; i++) u[i] = qh[(size_t)t * dk + i];
+            for (int s = t; s >= 0; s--) {
+                const double* ks = kh + (size_t)s * dk;
+                double ku = 0.0;
+                for (int i = 0; i < dk; i++) ku += ks[i] * u[i];
+                double w = lh[(size_t)t * L + lla_oracle_level(t, s)] * bth[s] * ku;
+                for (int j = 0; j < dv; j++) o[j] += w * vh[(size_t)s * dv + j];
+                gdn_transition_vec(u, ks, exp(ah[s]), bth[s], dk);
+            }
+        }
+    }
+    free(u);
+}
+
+/* One recurrent step of the log-linear Gated DeltaNet on one head's state set,
+ * in place: as recurrent_step, with the scalar decay of every held bucket
+ * replaced by the transition A_t (S <- alpha (S - beta k (k^T S)), column by
+ * column) and the new level 0 = beta_t k_t v_t^T. */
+static void gdn_step(double* S, const double* qt, const double* kt, const double* vt,
+                     double log_a_t, double beta_t, const double* lam, int64_t t,
+                     int dk, int dv, int Lmax, double* o)
+{
+    size_t msz = (size_t)dk * dv;
+    if (t > 0) {
+        int c = trailing_zeros(t);
+        double alpha = exp(log_a_t);
+        for (int l = 0; l < Lmax; l++) {
+            if (!level_nonempty(t - 1, l)) continue;
+            double* Sl = S + (size_t)l * msz;
+            for (int j = 0; j < dv; j++) {
+                double kS = 0.0;
+                for (int i = 0; i < dk; i++) kS += kt[i] * Sl[(size_t)i * dv + j];
+                for (int i = 0; i < dk; i++)
+                    Sl[(size_t)i * dv + j] = alpha * (Sl[(size_t)i * dv + j] - beta_t * kt[i] * kS);
+            }
+        }
+        double* dst = S + (size_t)(c + 1) * msz;
+        for (size_t e = 0; e < msz; e++) dst[e] = 0.0;
+        for (int l = 0; l <= c; l++) {
+            for (size_t e = 0; e < msz; e++) dst[e] += S[l * msz + e];
+            if (l > 0)
+                for (size_t e = 0; e < msz; e++) S[l * msz + e] = 0.0;
+        }
+    }
+    for (int i = 0; i < dk; i++)
+        for (int j = 0; j < dv; j++) S[(size_t)i * dv + j] = beta_t * kt[i] * vt[j];
+    for (int j = 0; j < dv; j++) o[j] = 0.0;
+    for (int l = 0; l < Lmax; l++) {
+        if (!level_nonempty(t, l)) continue;
+        const double* Sl = S + (size_t)l * msz;
+        for (int j = 0; j < dv; j++) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; i++) acc += qt[i] * Sl[(size_t)i * dv + j];
+            o[j] += lam[l] * acc;
+        }
+    }
+}
+
+/* Recurrent form of the log-linear Gated DeltaNet over whole sequences. It never
+ * evaluates l(t,s) or a pairwise attention coefficient. */
+int lla_oracle_gdn_recurrent(const double* q, const double* k, const double* v,
+                             const double* log_a, const double* beta, const double* lambda,
+                             double* out, int B, int H, int T, int dk, int dv, int L)
+{
+    size_t msz = (size_t)dk * dv;
+    double* S = (double*)calloc((size_t)L * msz, sizeof(double));
+    if (!S) return -1;
+    for (int bh = 0; bh < B * H; bh++) {
+        memset(S, 0, (size_t)L * msz * sizeof(double));
+        for (int t = 0; t < T; t++) {
+            size_t r = (size_t)bh * T + t;
+            gdn_step(S, q + r * dk, k + r * dk, v + r * dv, log_a[r], beta[r], lambda + r * L, t, dk, dv, L,
+                     out + r * dv);
+        }
+    }
+    free(S);
+    return 0;
+}
+
+/* One decode step of the log-linear Gated DeltaNet for a batch (states as in
+ * lla_oracle_decode_step). */
+int lla_oracle_gdn_decode_step(const double* q, const double* k, const double* v,
+                               const double* log_a, const double* beta, const double* lambda,
+                               double* states, const int64_t* t, double* out,
+                               int B, int H, int dk, int dv, int Lmax)
+{
+    size_t msz = (size_t)dk * dv;
+    for (int b = 0; b < B; b++) {
+        int64_t tb = t[b];
+        if (tb < 0) return -1;
+        int need = 1;
+        for (int64_t x = tb; x > 0; x >>= 1) need++;
+        if (need > Lmax) return -1;
+        for (int h = 0; h < H; h++) {
+            size_t bh = (size_t)b * H + h;
+            gdn_step(states + bh * Lmax * msz, q + bh * dk, k + bh * dk, v + bh * dv, log_a[bh], beta[bh],
+                     lambda + bh * Lmax, tb, dk, dv, Lmax, out + bh * dv);
         }
     }
     return 0;
