@@ -260,6 +260,42 @@ int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, c
                              void* stream, int dtype);
 
 /*
+ * Log-linear Gated DeltaNet ("Log-Linear Attention", pt §2 "Generalizacao" and
+ * fr §3 "Etudes de Cas": the hierarchical mask applied to Gated DeltaNet; the
+ * base model is Gated DeltaNet's published gated delta rule):
+ *
+ *     o_t = sum_{s<=t} lambda_t^(l(t,s)) A[t,s] v_s,
+ *     A[t,s] = beta_s k_s^T A_{s+1} A_{s+2} ... A_t q_t,
+ *     A_r = exp(log_a_r) (I - beta_r k_r k_r^T),
+ *
+ * i.e. Gated DeltaNet's own attention matrix under the Fenwick mask M^H. In
+ * recurrent form every held Fenwick bucket state S (dk x dv) evolves as
+ * S <- A_t S, buckets merge on the lowbit carry as in lla_decode_step, and the
+ * new token writes beta_t k_t v_t^T at level 0. Keys are expected L2-normalised
+ * and beta in [0, 1] (the transition is then a contraction); other values are
+ * computed as given.
+ *
+ * lla_gdn_forward: chunkwise prefill. Arguments as lla_forward, plus
+ *   beta   [B,H,T]  fp32   delta-rule strength of every token.
+ *   chunk  16, 32, 64 or 128 (128 runs as 64: same operator, different rounding
+ *          order), T % chunk == 0; dk 1..128; dv a multiple of 16 up to 128.
+ * All arithmetic is fp32 on CUDA cores. Workspace comes from the library's
+ * stream-ordered pool: per head about (2 dk T + 2 (T / C) dk dv + dv T) floats.
+ *
+ * lla_gdn_decode_step: one recurrent step; arguments as lla_decode_step, plus
+ *   beta   [B,H]    fp32   the new token's delta-rule strength.
+ *   fenwick_states holds each bucket's state under the transitions above (the
+ *   layout, emptiness and position rules of lla_decode_step apply unchanged).
+ *   dk and dv in {16, 32, 64, 128}.
+ */
+int lla_gdn_forward(const void* q, const void* k, const void* v, const float* log_a, const float* beta,
+                    const float* lambda, void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream,
+                    int dtype);
+int lla_gdn_decode_step(const void* q, const void* k, const void* v, const float* log_a, const float* beta,
+                        const float* lambda, float* fenwick_states, const int64_t* t, void* out, void* stream, int B,
+                        int H, int dk, int dv, int Lmax, int dtype);
+
+/*
  * Test hook for the failure path of the bounded waits (no counterpart on the
  * pages; not for production use). On the current device, for the tensor-core
  * prefill output kernel of dv = 64: limit_cycles > 0 bounds each of its pipeline

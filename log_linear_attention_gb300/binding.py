@@ -65,6 +65,10 @@ def load() -> ctypes.CDLL:
             lib.lla_prefill_state.restype = i
             lib.lla_device_error.argtypes = [vp]
             lib.lla_device_error.restype = i
+            lib.lla_gdn_forward.argtypes = [vp, vp, vp, fp, fp, fp, vp] + [i] * 6 + [vp, i]
+            lib.lla_gdn_forward.restype = i
+            lib.lla_gdn_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, fp, vp, vp, vp] + [i] * 6
+            lib.lla_gdn_decode_step.restype = i
             lib.lla_debug_set_waits.argtypes = [ctypes.c_int64, i]
             lib.lla_debug_set_waits.restype = i
             lib.lla_backward.argtypes = [vp, vp, vp, fp, fp, vp, vp, vp, vp, fp, fp] + [i] * 6 + [vp, i]
@@ -218,6 +222,39 @@ def forward_profile(q, k, v, log_a, lam, chunk: int, out, stream=None):
     if n < 0:
         raise LLAError(n, "lla_forward_profile")
     return [(names[i].decode(), float(ms[i])) for i in range(min(n, cap))]
+
+
+def gdn_forward(q, k, v, log_a, beta, lam, chunk: int, out=None, stream=None):
+    """Log-linear Gated DeltaNet prefill, lla_gdn_forward: as ``forward`` plus ``beta`` [B,H,T] fp32."""
+    torch = _torch()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (beta, "beta"), (lam, "lambda"), (out, "out")):
+        _check(t_, n, q.device)
+    _call(load().lla_gdn_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), beta.data_ptr(),
+                                 lam.data_ptr(), out.data_ptr(), B, H, T, dk, dv, int(chunk), _stream_handle(stream),
+                                 _dtype_code(q)), "lla_gdn_forward")
+    return out
+
+
+def gdn_decode_step(q, k, v, log_a, beta, lam, states, t, out=None, stream=None):
+    """One log-linear Gated DeltaNet decode step, lla_gdn_decode_step (states updated in place)."""
+    torch = _torch()
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    Lmax = states.shape[2]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q.dtype, device=q.device)
+    for t_, n in ((q, "q"), (k, "k"), (v, "v"), (log_a, "log_a"), (beta, "beta"), (lam, "lambda"),
+                  (states, "states"), (t, "t"), (out, "out")):
+        _check(t_, n, q.device)
+    _call(load().lla_gdn_decode_step(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), beta.data_ptr(),
+                                     lam.data_ptr(), states.data_ptr(), t.data_ptr(), out.data_ptr(),
+                                     _stream_handle(stream), B, H, dk, dv, Lmax, _dtype_code(q)),
+          "lla_gdn_decode_step")
+    return out
 
 
 def debug_set_waits(limit_cycles: int, hold: bool) -> None:

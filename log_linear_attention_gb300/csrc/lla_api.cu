@@ -512,6 +512,50 @@ int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, c
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }
 
+int lla_gdn_forward(const void* q, const void* k, const void* v, const float* log_a, const float* beta,
+                    const float* lambda, void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream,
+                    int dtype) {
+    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    if (!beta || !aligned16(beta)) return LLA_ERR_INVALID_ARG;
+    lla::GdnPlan pl;
+    if (dv % 16 != 0 || !lla::make_gdn_plan(B, H, T, dk, dv, chunk, &pl)) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool = workspace_pool(dev);
+    if (!pool) return LLA_ERR_CUDA;
+    void* ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, pl.total_bytes, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LLA_ERR_NOMEM;
+    }
+    const cudaError_t e = lla::gdn_forward(pl, dtype, q, k, v, log_a, beta, lambda, out, ws, s);
+    const cudaError_t f = cudaFreeAsync(ws, s);
+    return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
+}
+
+int lla_gdn_decode_step(const void* q, const void* k, const void* v, const float* log_a, const float* beta,
+                        const float* lambda, float* fenwick_states, const int64_t* t, void* out, void* stream, int B,
+                        int H, int dk, int dv, int Lmax, int dtype) {
+    if (!q || !k || !v || !log_a || !beta || !lambda || !fenwick_states || !t || !out) return LLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_a) || !aligned16(beta) ||
+        !aligned16(lambda) || !aligned16(fenwick_states) || !aligned16(t) || !aligned16(out))
+        return LLA_ERR_INVALID_ARG;
+    if (dtype != LLA_BF16 && dtype != LLA_F32) return LLA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || dk < 1 || dv < 1 || Lmax < 1 || Lmax > 40) return LLA_ERR_INVALID_ARG;
+    if ((dk != 16 && dk != 32 && dk != 64 && dk != 128) || (dv != 16 && dv != 32 && dv != 64 && dv != 128))
+        return LLA_ERR_UNSUPPORTED;
+    if ((int64_t)B * H > 0x7fffffff) return LLA_ERR_UNSUPPORTED;
+    const int dev = current_device();
+    if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
+    cudaError_t e = lla::gdn_decode_step(dtype, q, k, v, log_a, beta, lambda, fenwick_states, t, out, B, H, dk, dv,
+                                         Lmax, err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;
+}
+
 int lla_debug_set_waits(int64_t limit_cycles, int hold) {
     if (current_device() < 0) return LLA_ERR_CUDA;
     return lla::tc_set_debug_waits(static_cast<long long>(limit_cycles), hold) == cudaSuccess ? LLA_OK : LLA_ERR_CUDA;

@@ -143,6 +143,24 @@ size_t tc_bwd_workspace_bytes(const TcPlan& plan);
 cudaError_t tc_backward(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
                         const float* lambda, const void* dout, void* dq, void* dk, void* dv, float* dlog_a,
                         float* dlambda, void* workspace, int* err, cudaStream_t stream);
+// Log-linear Gated DeltaNet (lla_gdn.cu): chunkwise prefill on CUDA cores and the decode step.
+struct GdnPlan {
+    int B, H, T, dk, dv;
+    int C;                   // chunk of the scan (the API chunk, at most 64)
+    int N;                   // chunks per sequence
+    int P;                   // node levels read: bitlength(N - 1)
+    int node_count;          // complete nodes per head, all levels <= P
+    int level_off[32];       // first node of level p
+    size_t w_off, qt_off, node_off, gam_off, oacc_off, total_bytes;
+};
+bool make_gdn_plan(int B, int H, int T, int dk, int dv, int chunk, GdnPlan* plan);
+cudaError_t gdn_forward(const GdnPlan& plan, int dtype, const void* q, const void* k, const void* v,
+                        const float* log_a, const float* beta, const float* lambda, void* out, void* workspace,
+                        cudaStream_t stream);
+cudaError_t gdn_decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
+                            const float* beta, const float* lambda, float* states, const int64_t* t, void* out, int B,
+                            int H, int dk, int dv, int Lmax, int* err, cudaStream_t stream);
+
 cudaError_t decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
                         const float* lambda, float* states, const int64_t* t, void* out, int B, int H,
                         int dk, int dv, int Lmax, int* err, cudaStream_t stream);

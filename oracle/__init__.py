@@ -66,6 +66,8 @@ def _load():
             lib.lla_oracle_gdn_recurrent.restype = ctypes.c_int
             lib.lla_oracle_gdn_decode_step.argtypes = [dp] * 7 + [i64p, dp] + [ctypes.c_int] * 5
             lib.lla_oracle_gdn_decode_step.restype = ctypes.c_int
+            lib.lla_oracle_gdn_explicit_rows.argtypes = [dp] * 7 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int]
+            lib.lla_oracle_gdn_explicit_rows.restype = None
             _lib = lib
     return _lib
 
@@ -232,4 +234,17 @@ def gdn_decode_step(q, k, v, log_a, beta, lam, states, t):
                                             _ptr(out), B, H, dk, dv, Lmax)
     if rc != 0:
         raise ValueError("decode position needs more levels than the state set holds")
+    return out
+
+
+def gdn_explicit_rows(q, k, v, log_a, beta, lam, b: int, h: int, rows) -> np.ndarray:
+    """gdn_explicit for chosen query rows of head (b, h) only: returns [len(rows), dv]."""
+    sl = (slice(b, b + 1), slice(h, h + 1))
+    q, k, v, log_a, beta, lam, (_, _, T, dk, dv, L) = _check_gdn(q[sl], k[sl], v[sl], log_a[sl], beta[sl], lam[sl])
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    assert rows.ndim == 1 and (rows >= 0).all() and (rows < T).all()
+    out = np.zeros((rows.size, dv), dtype=np.float64)
+    _load().lla_oracle_gdn_explicit_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(log_a), _ptr(beta), _ptr(lam), _ptr(out),
+                                         0, T, dk, dv, L,
+                                         rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), int(rows.size))
     return out

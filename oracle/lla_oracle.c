@@ -525,3 +525,36 @@ int lla_oracle_gdn_decode_step(const double* q, const double* k, const double* v
     }
     return 0;
 }
+
+/* lla_oracle_gdn_explicit restricted to chosen query rows of one head (bh), for spot
+ * checks of long sequences: o_t for each t in rows[0..nrows), written to out[r * dv ...].
+ * Same definition and summation order. */
+void lla_oracle_gdn_explicit_rows(const double* q, const double* k, const double* v,
+                                  const double* log_a, const double* beta, const double* lambda,
+                                  double* out, int bh, int T, int dk, int dv, int L,
+                                  const int64_t* rows, int nrows)
+{
+    double* u = (double*)malloc((size_t)(dk > 0 ? dk : 1) * sizeof(double));
+    if (!u) return;
+    const double* qh = q + (size_t)bh * T * dk;
+    const double* kh = k + (size_t)bh * T * dk;
+    const double* vh = v + (size_t)bh * T * dv;
+    const double* ah = log_a + (size_t)bh * T;
+    const double* bth = beta + (size_t)bh * T;
+    const double* lh = lambda + (size_t)bh * T * L;
+    for (int rr = 0; rr < nrows; rr++) {
+        int64_t t = rows[rr];
+        double* o = out + (size_t)rr * dv;
+        for (int j = 0; j < dv; j++) o[j] = 0.0;
+        for (int i = 0; i < dk; i++) u[i] = qh[(size_t)t * dk + i];
+        for (int64_t s = t; s >= 0; s--) {
+            const double* ks = kh + (size_t)s * dk;
+            double ku = 0.0;
+            for (int i = 0; i < dk; i++) ku += ks[i] * u[i];
+            double w = lh[(size_t)t * L + lla_oracle_level(t, s)] * bth[s] * ku;
+            for (int j = 0; j < dv; j++) o[j] += w * vh[(size_t)s * dv + j];
+            gdn_transition_vec(u, ks, exp(ah[s]), bth[s], dk);
+        }
+    }
+    free(u);
+}

@@ -173,3 +173,12 @@ def test_gdn_decode_steps_reproduce_recurrent_rows():
         o = oracle.gdn_decode_step(q[:, :, t], k[:, :, t], v[:, :, t], log_a[:, :, t], beta[:, :, t],
                                    lam[:, :, t], states, np.full(B, t))
         assert _rel(o, ref[:, :, t]) <= 1e-12
+
+
+def test_gdn_rows_form_equals_full_explicit():
+    rng = np.random.default_rng(14)
+    q, k, v, log_a, beta, lam = _problem(rng, 2, 2, 77, 5, 3)
+    full = oracle.gdn_explicit(q, k, v, log_a, beta, lam)
+    rows = [0, 1, 31, 32, 63, 76]
+    got = oracle.gdn_explicit_rows(q, k, v, log_a, beta, lam, 1, 0, rows)
+    assert np.max(np.abs(got - full[1, 0, rows])) == 0.0
