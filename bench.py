@@ -477,6 +477,99 @@ def bench_decode(args, dev, stream, rank, ws):
     return d_ms_total, dbytes, dsteps
 
 
+def gdn_work(cfg: inputs.PrefillConfig) -> dict:
+    """Algorithmic flops of one log-linear Gated DeltaNet prefill (the chunkwise algorithm, chunk
+    C = min(chunk, 64)): per chunk the causal halves of Q K^T and K K^T, the two unit-triangular
+    inverses (C^3/6 multiply-adds each), W, Q~ and the pseudo-values, the in-chunk attention
+    matrix and its product with V, the chunk state; per Fenwick level read the node read
+    (2 C dk dv) and its carry through the chunk (4 C dk dv)."""
+    BH = cfg.B * cfg.H
+    C = min(cfg.chunk, 64)
+    N = cfg.T // C
+    dk, dv = cfg.dk, cfg.dv
+    tri = C * (C + 1) // 2
+    chunk = (2 * tri * 2 * dk + 2 * C ** 3 // 3 + tri * 2 * (2 * dk + dv) + C ** 3 // 3 + tri * 2 * dv
+             + 2 * C * dk * dv)
+    reads = popcount_sum(N)
+    flops = BH * (N * chunk + reads * 6 * C * dk * dv)
+    esz = 2 if cfg.dtype == "bf16" else 4
+    nbytes = BH * cfg.T * ((2 * dk + 2 * dv) * esz + 8 + cfg.L * 4)
+    return dict(flops=flops, bytes=nbytes)
+
+
+def bench_gdn(args, dev, stream, peaks) -> dict:
+    """The log-linear Gated DeltaNet: prefill of the headline-shaped workload (B4 H16 T8192 dk128
+    dv64, unit-norm q/k, beta = sigmoid(N(0,1))) and the decode step of the decode workload."""
+    import torch
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.GDN_CONFIGS["gdn-headline"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(99)
+    shp = (cfg.B, cfg.H, cfg.T)
+
+    def unit(x):
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    q = unit(torch.randn(shp + (cfg.dk,), device=dev, generator=g))
+    k = unit(torch.randn(shp + (cfg.dk,), device=dev, generator=g))
+    v = torch.randn(shp + (cfg.dv,), device=dev, generator=g).to(torch.bfloat16)
+    la = -torch.nn.functional.softplus(torch.randn(shp, device=dev, generator=g) + cfg.log_a_mu)
+    bt = torch.sigmoid(torch.randn(shp, device=dev, generator=g))
+    lam = torch.nn.functional.softplus(torch.randn(shp + (cfg.L,), device=dev, generator=g))
+    out = torch.empty(shp + (cfg.dv,), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        binding.gdn_forward(q, k, v, la, bt, lam, cfg.chunk, out=out)
+
+    step()
+    n = 3
+    ms = cuda_time(step, n, stream) / n
+    per = {}
+    for kname, kms in binding.gdn_forward_profile(q, k, v, la, bt, lam, cfg.chunk, out):
+        per[kname] = per.get(kname, 0.0) + kms
+    work = gdn_work(cfg)
+    tfl = work["flops"] / (ms / 1e3) / 1e12
+    # decode: the decode workload's shapes and positions, random states
+    dcfg = inputs.DECODE_CONFIG
+    pos = torch.from_numpy(inputs.make_positions(dcfg, 0)).to(dev)
+    states = torch.randn((dcfg.batch, dcfg.H, dcfg.Lmax, dcfg.dk, dcfg.dv), device=dev, generator=g) * dcfg.dk ** -0.5
+    dq = torch.randn((dcfg.batch, dcfg.H, dcfg.dk), device=dev, generator=g).to(torch.bfloat16)
+    dk_ = unit(torch.randn((dcfg.batch, dcfg.H, dcfg.dk), device=dev, generator=g))
+    dv_ = torch.randn((dcfg.batch, dcfg.H, dcfg.dv), device=dev, generator=g).to(torch.bfloat16)
+    dla = -torch.nn.functional.softplus(torch.randn((dcfg.batch, dcfg.H), device=dev, generator=g))
+    dbt = torch.sigmoid(torch.randn((dcfg.batch, dcfg.H), device=dev, generator=g))
+    dlam = torch.nn.functional.softplus(torch.randn((dcfg.batch, dcfg.H, dcfg.Lmax), device=dev, generator=g))
+    dout = torch.empty((dcfg.batch, dcfg.H, dcfg.dv), dtype=torch.bfloat16, device=dev)
+    t_np = pos.cpu().numpy()
+    nsteps = 200
+    ts = [pos + i for i in range(nsteps + 3)]
+
+    counter = [0]
+
+    def dstep():
+        binding.gdn_decode_step(dq, dk_, dv_, dla, dbt, dlam, states, ts[counter[0]], out=dout)
+        counter[0] += 1
+
+    for _ in range(3):
+        dstep()
+    d_ms = cuda_time(dstep, nsteps, stream)
+    dbytes = sum(decode_bytes(t_np + i, dcfg.H, dcfg.dk, dcfg.dv, dcfg.Lmax) + len(t_np) * dcfg.H * 4
+                 for i in range(3, 3 + nsteps))
+    assert binding.device_error() == 0
+    d_gbs = dbytes / (d_ms / 1e3) / 1e9
+    return {"prefill": {"workload": f"{cfg.name}: B={cfg.B} H={cfg.H} T={cfg.T} dk={cfg.dk} dv={cfg.dv} "
+                                    f"chunk={cfg.chunk}, bf16 q/k/v (unit-norm q, k), fp32 log_a/beta/lambda",
+                        "ms": ms, "tokens_per_s": cfg.tokens / (ms / 1e3), "algorithmic_gflop": work["flops"] / 1e9,
+                        "kernels_ms": per,
+                        "roofline": {"bound": "alu", "achieved": tfl, "peak": ALU_F32_TFLOPS, "unit": "TFLOP/s",
+                                     "frac": tfl / ALU_F32_TFLOPS,
+                                     "peak_source": "derived: 152 SM x 128 FMA x 2.07 GHz (fp32 CUDA cores)"}},
+            "decode": {"workload": "64 sequences x 16 heads, dk=128 dv=64, t ~ U[1,65536), fp32 states (18 slots)",
+                       "steps": nsteps, "us_per_step": 1e3 * d_ms / nsteps, "gbs": d_gbs,
+                       "frac_of_hbm": d_gbs / peaks["hbm_gbs"],
+                       "convention": "eager: nonempty levels read once, held levels written once"}}
+
+
 def bench_prefill_config(args, dev, stream, name, peaks) -> dict:
     """One more prefill workload of the stated configs (inputs drawn on the device with that
     config's distributions): time per call, throughput, and the roofline of its dominant
@@ -672,6 +765,7 @@ def run_lla(args, cfg):
     d_ms_total, dbytes, dsteps = bench_decode(args, dev, stream, rank, ws)
     d_gbs = ws * dbytes / (d_ms_total / 1e3) / 1e9
     sub = {name: bench_prefill_config(args, dev, stream, name, peaks) for name in ("small", "long")}
+    gdn = bench_gdn(args, dev, stream, peaks)
 
     # ---- prefill -> decode hand-off: the state set after the whole prompt
     hL = inputs.num_levels(cfg.T + 1)
@@ -741,6 +835,7 @@ def run_lla(args, cfg):
             "varlen": vl,
             "small": sub["small"],
             "long": sub["long"],
+            "gdn": gdn,
             "e2e": {"value": ws * cfg.tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                     "pinned_copy_gbs": {"h2d": (256 << 20) / (h2d_ms / 1e3) / 1e9,

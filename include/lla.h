@@ -294,6 +294,10 @@ int lla_gdn_forward(const void* q, const void* k, const void* v, const float* lo
 int lla_gdn_decode_step(const void* q, const void* k, const void* v, const float* log_a, const float* beta,
                         const float* lambda, float* fenwick_states, const int64_t* t, void* out, void* stream, int B,
                         int H, int dk, int dv, int Lmax, int dtype);
+/* Measurement aid for lla_gdn_forward, as lla_forward_profile is for lla_forward. */
+int lla_gdn_forward_profile(const void* q, const void* k, const void* v, const float* log_a, const float* beta,
+                            const float* lambda, void* out, int B, int H, int T, int dk, int dv, int chunk,
+                            void* stream, int dtype, float* kernel_ms, const char** kernel_names, int cap);
 
 /*
  * Test hook for the failure path of the bounded waits (no counterpart on the

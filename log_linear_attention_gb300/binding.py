@@ -69,6 +69,8 @@ def load() -> ctypes.CDLL:
             lib.lla_gdn_forward.restype = i
             lib.lla_gdn_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, fp, vp, vp, vp] + [i] * 6
             lib.lla_gdn_decode_step.restype = i
+            lib.lla_gdn_forward_profile.argtypes = [vp, vp, vp, fp, fp, fp, vp] + [i] * 6 + [vp, i, vp, vp, i]
+            lib.lla_gdn_forward_profile.restype = i
             lib.lla_debug_set_waits.argtypes = [ctypes.c_int64, i]
             lib.lla_debug_set_waits.restype = i
             lib.lla_backward.argtypes = [vp, vp, vp, fp, fp, vp, vp, vp, vp, fp, fp] + [i] * 6 + [vp, i]
@@ -212,7 +214,7 @@ def forward_profile(q, k, v, log_a, lam, chunk: int, out, stream=None):
     in launch order, timed with CUDA events on the launch stream."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
-    cap = 16
+    cap = 32
     ms = (ctypes.c_float * cap)()
     names = (ctypes.c_char_p * cap)()
     n = load().lla_forward_profile(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), lam.data_ptr(),
@@ -237,6 +239,22 @@ def gdn_forward(q, k, v, log_a, beta, lam, chunk: int, out=None, stream=None):
                                  lam.data_ptr(), out.data_ptr(), B, H, T, dk, dv, int(chunk), _stream_handle(stream),
                                  _dtype_code(q)), "lla_gdn_forward")
     return out
+
+
+def gdn_forward_profile(q, k, v, log_a, beta, lam, chunk: int, out, stream=None):
+    """lla_gdn_forward_profile: one synchronous call; returns [(kernel_name, ms), ...] in launch order."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    cap = 32
+    ms = (ctypes.c_float * cap)()
+    names = (ctypes.c_char_p * cap)()
+    n = load().lla_gdn_forward_profile(q.data_ptr(), k.data_ptr(), v.data_ptr(), log_a.data_ptr(), beta.data_ptr(),
+                                       lam.data_ptr(), out.data_ptr(), B, H, T, dk, dv, int(chunk),
+                                       _stream_handle(stream), _dtype_code(q), ctypes.cast(ms, ctypes.c_void_p),
+                                       ctypes.cast(names, ctypes.c_void_p), cap)
+    if n < 0:
+        raise LLAError(n, "lla_gdn_forward_profile")
+    return [(names[i].decode(), float(ms[i])) for i in range(min(n, cap))]
 
 
 def gdn_decode_step(q, k, v, log_a, beta, lam, states, t, out=None, stream=None):

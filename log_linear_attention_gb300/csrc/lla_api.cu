@@ -303,13 +303,17 @@ int lla_forward_host(const void* q, const void* k, const void* v, const float* l
     return LLA_OK;
 }
 
-int lla_forward_profile(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
-                        void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype,
-                        float* kernel_ms, const char** kernel_names, int cap) {
+}  // extern "C"
+
+namespace {
+
+// Runs `call` (which enqueues one library call on `stream`) with the launch log active:
+// a CUDA event before the first kernel and after each launch; writes each kernel's device
+// time (ms) and name, in launch order, for i < cap. Returns the number of kernels launched
+// or a negative lla_status.
+template <typename Fn>
+int profile_call(cudaStream_t s, float* kernel_ms, const char** kernel_names, int cap, Fn call) {
     if (cap < 0 || (cap > 0 && (!kernel_ms || !kernel_names))) return LLA_ERR_INVALID_ARG;
-    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
-    if (st != LLA_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     lla::LaunchLog log;
     log.count = 0;
     cudaEvent_t start;
@@ -324,7 +328,7 @@ int lla_forward_profile(const void* q, const void* k, const void* v, const float
     }
     cudaEventRecord(start, s);
     lla::active_launch_log() = &log;
-    st = lla_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, stream, dtype);
+    int st = call();
     lla::active_launch_log() = nullptr;
     int n = log.count < lla::LaunchLog::kMax ? log.count : lla::LaunchLog::kMax;
     if (st == LLA_OK && n > 0 && cudaEventSynchronize(log.events[n - 1]) != cudaSuccess) st = LLA_ERR_CUDA;
@@ -341,6 +345,30 @@ int lla_forward_profile(const void* q, const void* k, const void* v, const float
     for (int i = 0; i < lla::LaunchLog::kMax; i++) cudaEventDestroy(log.events[i]);
     cudaEventDestroy(start);
     return st == LLA_OK ? log.count : st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lla_forward_profile(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,
+                        void* out, int B, int H, int T, int dk, int dv, int chunk, void* stream, int dtype,
+                        float* kernel_ms, const char** kernel_names, int cap) {
+    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    return profile_call(static_cast<cudaStream_t>(stream), kernel_ms, kernel_names, cap, [&] {
+        return lla_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, stream, dtype);
+    });
+}
+
+int lla_gdn_forward_profile(const void* q, const void* k, const void* v, const float* log_a, const float* beta,
+                            const float* lambda, void* out, int B, int H, int T, int dk, int dv, int chunk,
+                            void* stream, int dtype, float* kernel_ms, const char** kernel_names, int cap) {
+    int st = validate_forward(q, k, v, log_a, lambda, out, B, H, T, dk, dv, chunk, dtype);
+    if (st != LLA_OK) return st;
+    return profile_call(static_cast<cudaStream_t>(stream), kernel_ms, kernel_names, cap, [&] {
+        return lla_gdn_forward(q, k, v, log_a, beta, lambda, out, B, H, T, dk, dv, chunk, stream, dtype);
+    });
 }
 
 int lla_decode_step(const void* q, const void* k, const void* v, const float* log_a, const float* lambda,

@@ -231,82 +231,104 @@ cudaError_t gdn_decode_t(int dk, int dv, const void* q, const void* k, const voi
 
 // ------------------------------------------------------------------ prefill: one chunk
 
-// Shared-memory layout of gdn_chunk_kernel (fp32): Q, K [C][dk]; V [C][dv]; W/U [C][max(dk, dv)];
-// G, QK, Lk, Lg [C][C].
+constexpr int kGdnChunkThreads = 512;
+
+// Shared-memory layout of gdn_chunk_kernel (fp32): Q, K [C][dk + 1] (rows padded so that a
+// warp reading one element of 32 different rows meets 32 different banks); V [C][dv];
+// W/U [C][max(dk, dv)]; G = K K^T, Gg = Gamma (.) G, QK = Q K^T (later Gamma (.) Q K^T),
+// Lk, Lg [C][C]; cl, beta, the decays to the chunk end [C].
 struct GdnChunkSmem {
-    int C, dk, dv, wcols;
-    size_t q, k, v, w, g, qk, lk, lg, cl, bt, total;
+    int C, dk, dv, ldk, wcols;
+    size_t q, k, v, w, g, gg, qk, lk, lg, cl, bt, ce, total;
     __host__ __device__ GdnChunkSmem(int C_, int dk_, int dv_) : C(C_), dk(dk_), dv(dv_) {
+        ldk = dk + 1;
         wcols = dk > dv ? dk : dv;
         q = 0;
-        k = q + (size_t)C * dk;
-        v = k + (size_t)C * dk;
+        k = q + (size_t)C * ldk;
+        v = k + (size_t)C * ldk;
         w = v + (size_t)C * dv;
         g = w + (size_t)C * wcols;
-        qk = g + (size_t)C * C;
+        gg = g + (size_t)C * C;
+        qk = gg + (size_t)C * C;
         lk = qk + (size_t)C * C;
         lg = lk + (size_t)C * C;
         cl = lg + (size_t)C * C;
         bt = cl + C;
-        total = (bt + C) * sizeof(float);
+        ce = bt + C;
+        total = (ce + C) * sizeof(float);
     }
 };
 
-// grid (N, BH), 256 threads; see the file header. Writes, per chunk: W and Q~ (fp32
+// grid (N, BH), 512 threads; see the file header. Writes, per chunk: W and Q~ (fp32
 // [BH][N][C][dk]), the chunk state (fp32 [BH][node][dk][dv], level 0 of the node
 // pyramid), the chunk's total decay gamma (fp32 [BH][N]), and its in-chunk output
 // (fp32 accumulator [BH][T][dv], or straight to `out` when the sequence is one chunk).
 template <typename T>
-__global__ void __launch_bounds__(kGdnThreads) gdn_chunk_kernel(
+__global__ void __launch_bounds__(kGdnChunkThreads) gdn_chunk_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const float* __restrict__ log_a,
     const float* __restrict__ beta, const float* __restrict__ lambda, float* __restrict__ Wg, float* __restrict__ Qt,
     float* __restrict__ nodes, float* __restrict__ gam, float* __restrict__ oacc, T* __restrict__ out, int T_, int C,
     int dk, int dv, int L, int node_count) {
+    constexpr int NT = kGdnChunkThreads;
     extern __shared__ float sm[];
     const GdnChunkSmem lay(C, dk, dv);
+    const int ldk = lay.ldk, ldw = lay.wcols;
     float* Qs = sm + lay.q;
     float* Ks = sm + lay.k;
     float* Vs = sm + lay.v;
     float* Ws = sm + lay.w;
     float* G = sm + lay.g;
+    float* Gg = sm + lay.gg;
     float* QK = sm + lay.qk;
     float* Lk = sm + lay.lk;
     float* Lg = sm + lay.lg;
     float* cl = sm + lay.cl;
     float* bt = sm + lay.bt;
+    float* ce = sm + lay.ce;
     const int tid = threadIdx.x;
     const int j = blockIdx.x, bh = blockIdx.y;
     const int N = T_ / C;
     const size_t row0 = (size_t)bh * T_ + (size_t)j * C;
 
-    for (int x = tid; x < C * dk; x += kGdnThreads) {
-        Qs[x] = load_f(q + row0 * dk + x);
-        Ks[x] = load_f(k + row0 * dk + x);
+    for (int x = tid; x < C * dk; x += NT) {
+        const int t = x / dk, i = x % dk;
+        Qs[t * ldk + i] = load_f(q + row0 * dk + x);
+        Ks[t * ldk + i] = load_f(k + row0 * dk + x);
     }
-    for (int x = tid; x < C * dv; x += kGdnThreads) Vs[x] = load_f(v + row0 * dv + x);
+    for (int x = tid; x < C * dv; x += NT) Vs[x] = load_f(v + row0 * dv + x);
     if (tid < C) bt[tid] = beta[row0 + tid];
-    if (tid == 0) {
-        float s = 0.f;
-        for (int t = 0; t < C; t++) {
-            s += log_a[row0 + t];
-            cl[t] = s;
+    if (tid < 32) {
+        // in-chunk inclusive prefix of log a, 32 lanes over C <= 64 tokens
+        float carry = 0.f;
+        for (int base = 0; base < C; base += 32) {
+            float x = base + tid < C ? log_a[row0 + base + tid] : 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (tid >= off) x += y;
+            }
+            if (base + tid < C) cl[base + tid] = carry + x;
+            carry += __shfl_sync(0xffffffffu, x, 31);
         }
     }
     __syncthreads();
-    // G = K K^T, QK = Q K^T (lower triangles, diagonal included)
-    for (int x = tid; x < C * C; x += kGdnThreads) {
+    if (tid < C) ce[tid] = expf(cl[C - 1] - cl[tid]);
+    // G = K K^T, Gg = Gamma (.) G (strictly lower), QK = Q K^T (lower, diagonal included);
+    // Gamma_sr = e^{cl_s - cl_r}
+    for (int x = tid; x < C * C; x += NT) {
         const int t = x / C, r = x % C;
         float g = 0.f, a = 0.f;
         if (r <= t) {
-            const float* kt = Ks + (size_t)t * dk;
-            const float* kr = Ks + (size_t)r * dk;
-            const float* qt = Qs + (size_t)t * dk;
+            const float* kt = Ks + (size_t)t * ldk;
+            const float* kr = Ks + (size_t)r * ldk;
+            const float* qt = Qs + (size_t)t * ldk;
             for (int i = 0; i < dk; i++) {
                 g += kt[i] * kr[i];
                 a += qt[i] * kr[i];
             }
         }
         G[x] = g;
+        Gg[x] = r < t ? g * expf(cl[t] - cl[r]) : 0.f;
         QK[x] = a;
     }
     __syncthreads();
@@ -317,6 +339,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_chunk_kernel(
             const bool gated = tid >= C;
             const int col = gated ? tid - C : tid;
             float* M = gated ? Lg : Lk;
+            const float* A = (gated ? Gg : G) + (size_t)s * C;
             float val;
             if (col > s) {
                 val = 0.f;
@@ -324,11 +347,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_chunk_kernel(
                 val = 1.f;
             } else {
                 float acc = 0.f;
-                for (int r = col; r < s; r++) {
-                    float gsr = G[(size_t)s * C + r];
-                    if (gated) gsr *= expf(cl[s] - cl[r]);
-                    acc += gsr * M[(size_t)r * C + col];
-                }
+                for (int r = col; r < s; r++) acc += A[r] * M[(size_t)r * C + col];
                 val = -bt[s] * acc;
             }
             M[(size_t)s * C + col] = val;
@@ -336,39 +355,43 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_chunk_kernel(
         __syncthreads();
     }
     // W = Lk diag(beta) K
-    for (int x = tid; x < C * dk; x += kGdnThreads) {
+    for (int x = tid; x < C * dk; x += NT) {
         const int t = x / dk, i = x % dk;
         float acc = 0.f;
-        for (int r = 0; r <= t; r++) acc += Lk[(size_t)t * C + r] * bt[r] * Ks[(size_t)r * dk + i];
-        Ws[(size_t)t * lay.wcols + i] = acc;
+        for (int r = 0; r <= t; r++) acc += Lk[(size_t)t * C + r] * bt[r] * Ks[(size_t)r * ldk + i];
+        Ws[(size_t)t * ldw + i] = acc;
     }
     __syncthreads();
     const size_t cbase = ((size_t)bh * N + j) * C * dk;
-    for (int x = tid; x < C * dk; x += kGdnThreads) {
+    for (int x = tid; x < C * dk; x += NT) {
         const int t = x / dk, i = x % dk;
-        Wg[cbase + x] = Ws[(size_t)t * lay.wcols + i];
+        Wg[cbase + x] = Ws[(size_t)t * ldw + i];
         // Q~_t = e^{cl_t} (q_t - sum_{r<=t} (q_t . k_r) w_r)
-        float acc = Qs[x];
-        for (int r = 0; r <= t; r++) acc -= QK[(size_t)t * C + r] * Ws[(size_t)r * lay.wcols + i];
+        float acc = Qs[(size_t)t * ldk + i];
+        for (int r = 0; r <= t; r++) acc -= QK[(size_t)t * C + r] * Ws[(size_t)r * ldw + i];
         Qt[cbase + x] = expf(cl[t]) * acc;
     }
     __syncthreads();
-    // pseudo-values U = Lg diag(beta) V (over the W buffer)
-    for (int x = tid; x < C * dv; x += kGdnThreads) {
+    // pseudo-values U = Lg diag(beta) V (over the W buffer); QK <- Gamma (.) QK (diagonal: 1)
+    for (int x = tid; x < C * dv; x += NT) {
         const int t = x / dv, jj = x % dv;
         float acc = 0.f;
         for (int r = 0; r <= t; r++) acc += Lg[(size_t)t * C + r] * bt[r] * Vs[(size_t)r * dv + jj];
-        Ws[(size_t)t * lay.wcols + jj] = acc;
+        Ws[(size_t)t * ldw + jj] = acc;
     }
+    for (int x = tid; x < C * C; x += NT) {
+        const int t = x / C, r = x % C;
+        if (r < t) QK[x] *= expf(cl[t] - cl[r]);
+    }
+    __syncthreads();
     // attention matrix inside the chunk, lambda-weighted: P[t][s] = lambda_t^(l(t,s)) *
-    // beta_s sum_{r=s..t} e^{cl_t - cl_r} (q_t . k_r) Lg[r][s]  (over G, which is no longer needed)
-    for (int x = tid; x < C * C; x += kGdnThreads) {
+    // beta_s sum_{r=s..t} Gamma_tr (q_t . k_r) Lg[r][s]  (over G, which is no longer needed)
+    for (int x = tid; x < C * C; x += NT) {
         const int t = x / C, s = x % C;
         float acc = 0.f;
         if (s <= t) {
-            for (int r = s; r <= t; r++) acc += expf(cl[t] - cl[r]) * QK[(size_t)t * C + r] * Lg[(size_t)r * C + s];
-            const int gt = j * C + t, gs = j * C + s;
-            const int lvl = fenwick_level(gt, gs);
+            for (int r = s; r <= t; r++) acc += QK[(size_t)t * C + r] * Lg[(size_t)r * C + s];
+            const int lvl = fenwick_level(j * C + t, j * C + s);
             acc *= bt[s] * lambda[(row0 + t) * L + lvl];
         }
         G[x] = acc;
@@ -376,19 +399,17 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_chunk_kernel(
     __syncthreads();
     // the chunk's state at its end: K^T diag(e^{cl_end - cl}) U
     if (N > 1) {
-        const float cend = cl[C - 1];
         float* node = nodes + ((size_t)bh * node_count + j) * dk * dv;
-        for (int x = tid; x < dk * dv; x += kGdnThreads) {
+        for (int x = tid; x < dk * dv; x += NT) {
             const int i = x / dv, jj = x % dv;
             float acc = 0.f;
-            for (int s = 0; s < C; s++)
-                acc += Ks[(size_t)s * dk + i] * expf(cend - cl[s]) * Ws[(size_t)s * lay.wcols + jj];
+            for (int s = 0; s < C; s++) acc += Ks[(size_t)s * ldk + i] * ce[s] * Ws[(size_t)s * ldw + jj];
             node[x] = acc;
         }
-        if (tid == 0) gam[(size_t)bh * N + j] = expf(cend);
+        if (tid == 0) gam[(size_t)bh * N + j] = expf(cl[C - 1]);
     }
     // in-chunk output P V
-    for (int x = tid; x < C * dv; x += kGdnThreads) {
+    for (int x = tid; x < C * dv; x += NT) {
         const int t = x / dv, jj = x % dv;
         float acc = 0.f;
         for (int s = 0; s <= t; s++) acc += G[(size_t)t * C + s] * Vs[(size_t)s * dv + jj];
@@ -407,7 +428,7 @@ constexpr int kGdnDS = 16;  // dv columns per level-kernel CTA
 // (p, m = 2x) of head bh, columns [16 slice, 16 slice + 16): it reads node m at every chunk
 // of block m + 1 and carries it through them; when block m + 1 is complete it writes node
 // (p + 1, x) = carried node + node (p, m + 1) if level p + 1 is read.
-// Shared memory (fp32): X [dk][16], Y [C][16], and the chunk's Q~, W, K [C][dk].
+// Shared memory (fp32): X [dk][16], Y [C][16], and the chunk's Q~, W, K [C][dk + 1] (padded rows).
 template <typename T>
 __global__ void __launch_bounds__(kGdnThreads) gdn_level_kernel(
     const T* __restrict__ k, const float* __restrict__ Wg, const float* __restrict__ Qt, float* __restrict__ nodes,
@@ -416,9 +437,10 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_level_kernel(
     extern __shared__ float sm[];
     float* X = sm;                        // [dk][16]
     float* Y = X + (size_t)dk * kGdnDS;   // [C][16]
-    float* Qs = Y + (size_t)C * kGdnDS;   // [C][dk]
-    float* Wsh = Qs + (size_t)C * dk;     // [C][dk]
-    float* Ksh = Wsh + (size_t)C * dk;    // [C][dk]
+    const int ldk = dk + 1;
+    float* Qs = Y + (size_t)C * kGdnDS;   // [C][ldk]
+    float* Wsh = Qs + (size_t)C * ldk;    // [C][ldk]
+    float* Ksh = Wsh + (size_t)C * ldk;   // [C][ldk]
     const int tid = threadIdx.x;
     const int bh = blockIdx.x / n_even, xi = blockIdx.x % n_even;
     const int j0 = blockIdx.y * kGdnDS;
@@ -441,9 +463,10 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_level_kernel(
         const size_t cbase = ((size_t)bh * N + jc) * C * dk;
         const size_t row0 = (size_t)bh * T_ + (size_t)jc * C;
         for (int x = tid; x < C * dk; x += kGdnThreads) {
-            Qs[x] = Qt[cbase + x];
-            Wsh[x] = Wg[cbase + x];
-            Ksh[x] = load_f(k + row0 * dk + x);
+            const int pos = (x / dk) * ldk + x % dk;
+            Qs[pos] = Qt[cbase + x];
+            Wsh[pos] = Wg[cbase + x];
+            Ksh[pos] = load_f(k + row0 * dk + x);
         }
         __syncthreads();
         // read: O[t][j0 + d] += lambda_t^(lev) sum_i Q~[t][i] X[i][d]; and Y = W X for the carry
@@ -452,8 +475,8 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_level_kernel(
             float a = 0.f, yw = 0.f;
             for (int i = 0; i < dk; i++) {
                 const float xv = X[i * kGdnDS + d];
-                a += Qs[(size_t)t * dk + i] * xv;
-                yw += Wsh[(size_t)t * dk + i] * xv;
+                a += Qs[(size_t)t * ldk + i] * xv;
+                yw += Wsh[(size_t)t * ldk + i] * xv;
             }
             oacc[(row0 + t) * dv + j0 + d] += lambda[(row0 + t) * L + lev] * a;
             Y[x] = yw;
@@ -465,7 +488,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_level_kernel(
             for (int x = tid; x < dk * kGdnDS; x += kGdnThreads) {
                 const int i = x / kGdnDS, d = x % kGdnDS;
                 float acc = 0.f;
-                for (int t = 0; t < C; t++) acc += Ksh[(size_t)t * dk + i] * Y[t * kGdnDS + d];
+                for (int t = 0; t < C; t++) acc += Ksh[(size_t)t * ldk + i] * Y[t * kGdnDS + d];
                 X[x] = gj * (X[x] - acc);
             }
         }
@@ -505,13 +528,13 @@ cudaError_t gdn_forward_t(const GdnPlan& pl, const void* q, const void* k, const
         cudaError_t e = cudaFuncSetAttribute(gdn_chunk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(lay.total));
         if (e != cudaSuccess) return e;
-        gdn_chunk_kernel<T><<<dim3(N, BH), kGdnThreads, lay.total, stream>>>(
+        gdn_chunk_kernel<T><<<dim3(N, BH), kGdnChunkThreads, lay.total, stream>>>(
             static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), log_a, beta, lambda, Wg, Qt,
             nodes, gam, oacc, static_cast<T*>(out), pl.T, C, pl.dk, pl.dv, L, pl.node_count);
         note_launch(stream, "gdn_chunk");
     }
     if (N == 1) return cudaGetLastError();
-    const size_t smem = ((size_t)pl.dk * kGdnDS + (size_t)C * kGdnDS + 3 * (size_t)C * pl.dk) * sizeof(float);
+    const size_t smem = ((size_t)pl.dk * kGdnDS + (size_t)C * kGdnDS + 3 * (size_t)C * (pl.dk + 1)) * sizeof(float);
     {
         cudaError_t e = cudaFuncSetAttribute(gdn_level_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));

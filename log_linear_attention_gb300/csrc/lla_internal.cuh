@@ -29,7 +29,7 @@ __device__ __forceinline__ int fenwick_level(int t, int s) { return 32 - __clz(t
 // this host thread, every launcher calls note_launch() right after enqueueing a
 // kernel, which records a CUDA event on the launch stream.
 struct LaunchLog {
-    static constexpr int kMax = 16;
+    static constexpr int kMax = 32;
     cudaEvent_t events[kMax];
     const char* names[kMax];
     int count;
