@@ -1232,46 +1232,54 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             if (!ewait(&s_full[g], c & 1)) break;
             tc_fence_after();
             uint8_t* pbase = smem + g * C::kStageBytes + C::kK;
+            // key chunk ci (32 keys, this warp's 16 of them) is live for the warp's rows when 32 ci <= q32
 #pragma unroll 1
-            for (int c0 = 0; c0 < kTile; c0 += 32) {
+            for (int ci = 0; ci < kTile / 32; ci++) {
+                const int c0 = ci * 32;
                 const int cb = c0 + half * 16;  // first key of this warp's 16
+                uint32_t sv[16];
                 uint32_t pk[8];
                 if (c0 > q32) {
 #pragma unroll
                     for (int e = 0; e < 8; e++) pk[e] = 0u;
                 } else {
-                    float sv[16];
-                    tmem_ld16(tb + cb, sv);
+                    tmem_ld16_issue(tb + cb, sv);
+                    tmem_ld16_wait(sv);
                     if (c0 < q32) {
                         // keys before every row of this warp: one level per row, factorised decay
-                        // exp2(cl_t - cl_s) = exp2(cl_t - cl_{c0+31}) * exp2(cl_{c0+31} - cl_s), both <= 1;
+                        // 2^(cl_t - cl_s) = 2^(cl_t - cl_{c0+31}) * 2^(cl_{c0+31} - cl_s), both <= 1;
                         // lane e computes the column factor of key cb + (e & 15)
                         const int lvl = 32 - __clz(t ^ c0);
                         float lw = lam_in[0];
 #pragma unroll
                         for (int l = 1; l < 8; l++) lw = (lvl == l) ? lam_in[l] : lw;
                         const float cend = cl2[c0 + 31];
-                        const float rowf = exp2f(cl2_t - cend) * lw;
-                        const float cw = exp2f(cend - cl2[cb + (lane & 15)]);
+                        const float rowf = ex2_ftz(cl2_t - cend) * lw;
+                        const float cw = ex2_ftz(cend - cl2[cb + (lane & 15)]);
 #pragma unroll
                         for (int e = 0; e < 16; e += 2) {
                             const float w0 = __shfl_sync(0xffffffffu, cw, e), w1 = __shfl_sync(0xffffffffu, cw, e + 1);
-                            pk[e >> 1] = pack_bf16(sv[e] * rowf * w0, sv[e + 1] * rowf * w1);
+                            pk[e >> 1] = pack_bf16(__uint_as_float(sv[e]) * rowf * w0,
+                                                   __uint_as_float(sv[e + 1]) * rowf * w1);
                         }
                     } else {
-                        // diagonal block: causal mask and per-key levels 0..5
+                        // diagonal block: causal mask, per-key level 1 + floor(log2(t ^ s)) (0 at
+                        // s = t, at most 5) and the exact per-key decay. A masked key (s > t) may
+                        // give an infinite decay factor; the select drops it.
 #pragma unroll
                         for (int e = 0; e < 16; e += 2) {
                             float v2[2];
 #pragma unroll
                             for (int h = 0; h < 2; h++) {
                                 const int sidx = cb + e + h;
-                                const int lvl = 32 - __clz(t ^ sidx);
-                                float lw = lam_in[0];
-#pragma unroll
-                                for (int l = 1; l < 6; l++) lw = (lvl == l) ? lam_in[l] : lw;
-                                const float x = sv[e + h] * exp2f(fminf(cl2_t - cl2[sidx], 0.f)) * lw;
-                                v2[h] = sidx <= t ? x : 0.f;
+                                const int x = t ^ sidx;
+                                float lw = x >= 16 ? lam_in[5] : lam_in[4];
+                                lw = x < 8 ? lam_in[3] : lw;
+                                lw = x < 4 ? lam_in[2] : lw;
+                                lw = x < 2 ? lam_in[1] : lw;
+                                lw = x == 0 ? lam_in[0] : lw;
+                                const float val = __uint_as_float(sv[e + h]) * ex2_ftz(cl2_t - cl2[sidx]) * lw;
+                                v2[h] = sidx <= t ? val : 0.f;
                             }
                             pk[e >> 1] = pack_bf16(v2[0], v2[1]);
                         }
