@@ -550,6 +550,8 @@ int lla_gdn_forward(const void* q, const void* k, const void* v, const float* lo
     if (dv % 16 != 0 || !lla::make_gdn_plan(B, H, T, dk, dv, chunk, &pl)) return LLA_ERR_UNSUPPORTED;
     const int dev = current_device();
     if (dev < 0) return LLA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return LLA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaMemPool_t pool = workspace_pool(dev);
     if (!pool) return LLA_ERR_CUDA;
@@ -558,7 +560,7 @@ int lla_gdn_forward(const void* q, const void* k, const void* v, const float* lo
         cudaGetLastError();
         return LLA_ERR_NOMEM;
     }
-    const cudaError_t e = lla::gdn_forward(pl, dtype, q, k, v, log_a, beta, lambda, out, ws, s);
+    const cudaError_t e = lla::gdn_forward(pl, dtype, q, k, v, log_a, beta, lambda, out, ws, err, s);
     const cudaError_t f = cudaFreeAsync(ws, s);
     return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
 }

@@ -511,8 +511,9 @@ __global__ void gdn_finalize_kernel(const float* __restrict__ oacc, T* __restric
 }
 
 template <typename T>
-cudaError_t gdn_forward_t(const GdnPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
-                          const float* beta, const float* lambda, void* out, void* workspace, cudaStream_t stream) {
+cudaError_t gdn_forward_t(const GdnPlan& pl, int dtype, const void* q, const void* k, const void* v,
+                          const float* log_a, const float* beta, const float* lambda, void* out, void* workspace,
+                          int* err, cudaStream_t stream) {
     const int BH = pl.B * pl.H, C = pl.C, N = pl.N;
     char* ws = static_cast<char*>(workspace);
     float* Wg = reinterpret_cast<float*>(ws + pl.w_off);
@@ -534,21 +535,25 @@ cudaError_t gdn_forward_t(const GdnPlan& pl, const void* q, const void* k, const
         note_launch(stream, "gdn_chunk");
     }
     if (N == 1) return cudaGetLastError();
-    const size_t smem = ((size_t)pl.dk * kGdnDS + (size_t)C * kGdnDS + 3 * (size_t)C * (pl.dk + 1)) * sizeof(float);
-    {
+    int c_log2 = 0;
+    while ((1 << c_log2) < C) c_log2++;
+    if (gdn_level_tc_supported(pl, dtype)) {
+        const cudaError_t e = gdn_levels_tc(pl, k, Wg, Qt, nodes, gam, lambda, oacc, L, c_log2, err, stream);
+        if (e != cudaSuccess) return e;
+    } else {
+        const size_t smem =
+            ((size_t)pl.dk * kGdnDS + (size_t)C * kGdnDS + 3 * (size_t)C * (pl.dk + 1)) * sizeof(float);
         cudaError_t e = cudaFuncSetAttribute(gdn_level_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-    }
-    int c_log2 = 0;
-    while ((1 << c_log2) < C) c_log2++;
-    for (int p = 0; p < pl.P; p++) {
-        const int n_even = (((N - 1) >> p) + 1) / 2;
-        if (n_even <= 0) continue;
-        gdn_level_kernel<T><<<dim3(BH * n_even, pl.dv / kGdnDS), kGdnThreads, smem, stream>>>(
-            static_cast<const T*>(k), Wg, Qt, nodes, gam, lambda, oacc, pl.T, C, pl.dk, pl.dv, L, c_log2, p, pl.P,
-            n_even, pl.node_count, lo);
-        note_launch(stream, "gdn_level");
+        for (int p = 0; p < pl.P; p++) {
+            const int n_even = (((N - 1) >> p) + 1) / 2;
+            if (n_even <= 0) continue;
+            gdn_level_kernel<T><<<dim3(BH * n_even, pl.dv / kGdnDS), kGdnThreads, smem, stream>>>(
+                static_cast<const T*>(k), Wg, Qt, nodes, gam, lambda, oacc, pl.T, C, pl.dk, pl.dv, L, c_log2, p,
+                pl.P, n_even, pl.node_count, lo);
+            note_launch(stream, "gdn_level");
+        }
     }
     const size_t n = (size_t)BH * pl.T * pl.dv;
     const size_t blocks = (n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16;
@@ -587,9 +592,10 @@ bool make_gdn_plan(int B, int H, int T, int dk, int dv, int chunk, GdnPlan* pl) 
 
 cudaError_t gdn_forward(const GdnPlan& pl, int dtype, const void* q, const void* k, const void* v,
                         const float* log_a, const float* beta, const float* lambda, void* out, void* workspace,
-                        cudaStream_t stream) {
-    return dtype == 0 ? gdn_forward_t<__nv_bfloat16>(pl, q, k, v, log_a, beta, lambda, out, workspace, stream)
-                      : gdn_forward_t<float>(pl, q, k, v, log_a, beta, lambda, out, workspace, stream);
+                        int* err, cudaStream_t stream) {
+    return dtype == 0 ? gdn_forward_t<__nv_bfloat16>(pl, dtype, q, k, v, log_a, beta, lambda, out, workspace, err,
+                                                     stream)
+                      : gdn_forward_t<float>(pl, dtype, q, k, v, log_a, beta, lambda, out, workspace, err, stream);
 }
 
 cudaError_t gdn_decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,

@@ -156,7 +156,12 @@ struct GdnPlan {
 bool make_gdn_plan(int B, int H, int T, int dk, int dv, int chunk, GdnPlan* plan);
 cudaError_t gdn_forward(const GdnPlan& plan, int dtype, const void* q, const void* k, const void* v,
                         const float* log_a, const float* beta, const float* lambda, void* out, void* workspace,
-                        cudaStream_t stream);
+                        int* err, cudaStream_t stream);
+// Tensor-core level pass (bf16, C = 64, dv = 64, dk in {64, 128}); csrc/lla_gdn_tc.cu.
+bool gdn_level_tc_supported(const GdnPlan& plan, int dtype);
+cudaError_t gdn_levels_tc(const GdnPlan& plan, const void* k, const float* Wg, const float* Qt, float* nodes,
+                          const float* gam, const float* lambda, float* oacc, int L, int c_log2, int* err,
+                          cudaStream_t stream);
 cudaError_t gdn_decode_step(int dtype, const void* q, const void* k, const void* v, const float* log_a,
                             const float* beta, const float* lambda, float* states, const int64_t* t, void* out, int B,
                             int H, int dk, int dv, int Lmax, int* err, cudaStream_t stream);

@@ -127,6 +127,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], tf32 inputs (fp32 data in shared memory, read as tf32),
+// fp32 accumulate, issued by one thread. One instruction covers K = 8.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -236,6 +248,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, 
            | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor, kind::tf32: tf32 A and B (both K-major), fp32 D, dense.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4)                                // D format: f32
+           | (2u << 7)                              // A format: tf32
+           | (2u << 10)                             // B format: tf32
+           | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+
 // Byte offset of element (row r, col c) of a 128-row x 64-col bf16 panel in SWIZZLE_128B layout.
 __device__ __forceinline__ uint32_t sw128_off(int r, int chunk16) {
     return static_cast<uint32_t>(r * 128 + ((chunk16 ^ (r & 7)) << 4));
@@ -327,6 +348,23 @@ bool make_map_f32_32x32(CUtensorMap* m, const void* base, uint64_t rows, uint64_
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2D row-major [rows, cols] tensor of 2- or 4-byte elements, box = box_cols x box_rows
+// (box_cols * element size = 128 bytes), 128-byte swizzle. Columns past `cols` read as zero.
+bool make_map_box(CUtensorMap* m, const void* base, bool f32, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t esz = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * esz};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
