@@ -524,7 +524,11 @@ cudaError_t gdn_forward_t(const GdnPlan& pl, int dtype, const void* q, const voi
     GdnLevels lo;
     for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
     const int L = bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
-    {
+    if (gdn_chunk_tc_supported(pl, dtype)) {
+        const cudaError_t e =
+            gdn_chunk_tc(pl, q, k, v, log_a, beta, lambda, Wg, Qt, nodes, gam, oacc, out, L, err, stream);
+        if (e != cudaSuccess) return e;
+    } else {
         const GdnChunkSmem lay(C, pl.dk, pl.dv);
         cudaError_t e = cudaFuncSetAttribute(gdn_chunk_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(lay.total));

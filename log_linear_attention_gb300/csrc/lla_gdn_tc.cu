@@ -276,10 +276,405 @@ __global__ void __launch_bounds__(128, 2)
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// ------------------------------------------------------------------ chunk pass
+
+struct CkCfg {
+    static constexpr int kC = 64;                   // chunk tokens
+    static constexpr int kDV = 64;
+    static constexpr int kKQPanel = 16384;          // 128 rows x 64 dk (bf16): rows 0..63 K, 64..127 Q
+    static constexpr int kKQ = 0;                   // 2 panels (dk 0..127)
+    static constexpr int kV = kKQ + 2 * kKQPanel;   // V: 64 rows x 64 dv (bf16), 8 KB
+    static constexpr int kA2 = kV + 8192;           // A2 hi, lo: 128 rows x 64 tokens (bf16), 16 KB each
+    static constexpr int kR = kA2 + 32768;          // Bk, Bg (fp32 [64][kLd]); later A1 hi, lo; later U hi, lo
+    static constexpr int kLd = 68;                  // row stride of Bk, Bg in floats (16-byte rows, no bank conflicts)
+    static constexpr int kBBytes = 64 * kLd * 4;
+    static constexpr int kRBytes = 2 * kBBytes > 32768 ? 2 * kBBytes : 32768;
+    static constexpr int kScal = kR + kRBytes;      // cl, beta, ce: 64 floats each
+    static constexpr int kBar = kScal + 3 * 64 * 4;
+    static constexpr int kBytes = kBar + 64;
+    static constexpr int kSlack = 1024 - 128;
+    static constexpr uint32_t kInBytes = 2 * kKQPanel + 8192;
+};
+
+// y (I + B) = y0 for the row vector y, B strictly lower triangular (fp32 [64][kLd] in shared
+// memory): from the last column down, y[s] is final once every later column has been
+// subtracted, y[r] -= y[s] B[s][r] for r < s (rows of B, read as broadcast float4).
+__device__ __forceinline__ void gdn_row_solve(const float* __restrict__ B, float* y) {
+#pragma unroll
+    for (int s = 63; s > 0; s--) {
+        const float ys = y[s];
+        const float4* brow = reinterpret_cast<const float4*>(B + s * CkCfg::kLd);
+#pragma unroll
+        for (int r4 = 0; r4 < (s + 3) / 4; r4++) {
+            const float4 b = brow[r4];
+            if (4 * r4 + 0 < s) y[4 * r4 + 0] = fmaf(-ys, b.x, y[4 * r4 + 0]);
+            if (4 * r4 + 1 < s) y[4 * r4 + 1] = fmaf(-ys, b.y, y[4 * r4 + 1]);
+            if (4 * r4 + 2 < s) y[4 * r4 + 2] = fmaf(-ys, b.z, y[4 * r4 + 2]);
+            if (4 * r4 + 3 < s) y[4 * r4 + 3] = fmaf(-ys, b.w, y[4 * r4 + 3]);
+        }
+    }
+}
+
+// grid (N chunks, B*H), 256 threads (warp w reads TMEM lanes 32 (w % 4) ..), two CTAs per SM.
+// Per chunk of 64 tokens:
+//   MMA-a: [K; Q] K^T -> G = K K^T, QK = Q K^T (bf16 operands, exact products)
+//   Bk = diag(beta) strictlower(G), Bg = diag(beta) strictlower(Gamma (.) G), Gamma_tr = e^{cl_t - cl_r}
+//   four row solves (fp32, one 64-thread group each, the row in registers):
+//     row t of Lk = (I + Bk)^-1 and of Lg = (I + Bg)^-1 (right-hand side e_t),
+//     row t of M = tril(QK) Lk and of Z Lg, Z = tril(Gamma (.) QK)
+//   MMA-b: [Lk diag(beta); M diag(beta)] K -> W = Lk diag(beta) K and M diag(beta) K, from which
+//          Q~ = diag(e^{cl}) (Q - tril(QK) W)
+//   MMA-c: [Lg diag(beta); P] V -> U = Lg diag(beta) V and the in-chunk output P V, with
+//          P[t][s] = lambda_t^(level(t,s)) (Z Lg)[t][s] beta_s for s <= t
+//   MMA-d: K^T diag(e^{cl_end - cl}) U -> the chunk's state, node (0, j)
+// The A operands of MMA-b/c and the B operand of MMA-d are fp32 values split into bf16 hi + lo
+// (two MMAs each); K and V are exact in bf16.
+__global__ void __launch_bounds__(256, 2)
+    gdn_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
+                        const float* __restrict__ log_a, const float* __restrict__ beta,
+                        const float* __restrict__ lambda, float* __restrict__ Wg, float* __restrict__ Qt,
+                        float* __restrict__ nodes, float* __restrict__ gam, float* __restrict__ oacc,
+                        __nv_bfloat16* __restrict__ out, int T, int N, int dk, int L, int node_count, int* err) {
+    using C = CkCfg;
+    constexpr int DV = C::kDV;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    float* Bk = reinterpret_cast<float*>(smem + C::kR);
+    float* Bg = Bk + 64 * C::kLd;
+    float* cl = reinterpret_cast<float*>(smem + C::kScal);
+    float* bt = cl + 64;
+    float* ce = bt + 64;
+    uint64_t* in_full = reinterpret_cast<uint64_t*>(smem + C::kBar);
+    uint64_t* mma_a = in_full + 1;
+    uint64_t* mma_bc = in_full + 2;
+    uint64_t* mma_d = in_full + 3;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_full + 4);
+    volatile int* fail = reinterpret_cast<volatile int*>(in_full + 5);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (pad > static_cast<uint32_t>(C::kSlack)) {
+        if (tid == 0) record_error(err, kDevBadInput);
+        return;
+    }
+    const int j = blockIdx.x, bh = blockIdx.y;
+    const size_t row0 = static_cast<size_t>(bh) * T + static_cast<size_t>(j) * C::kC;
+    const int grp = warp >> 1;  // 0: Lk, 1: M, 2: Lg, 3: Z Lg (row t = tid % 64 of each)
+    const int t = tid & 63;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+
+    if (tid == 0) {
+        mbar_init(in_full, 1);
+        mbar_init(mma_a, 1);
+        mbar_init(mma_bc, 1);
+        mbar_init(mma_d, 1);
+        fence_mbar_init();
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int n_in = 0, n_a = 0, n_bc = 0, n_d = 0;
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_wait(bar, parity)) return true;
+        *fail = 1;
+        record_error(err, kDevTimeout);
+        return false;
+    };
+    auto block_sync = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+
+    if (tid == 0) {
+        mbar_expect_tx(in_full, C::kInBytes);
+        for (int pnl = 0; pnl < 2; pnl++) {
+            tma_load_2d(smem + C::kKQ + pnl * C::kKQPanel, &tm_k, in_full, 64 * pnl, static_cast<int>(row0));
+            tma_load_2d(smem + C::kKQ + pnl * C::kKQPanel + C::kKQPanel / 2, &tm_q, in_full, 64 * pnl,
+                        static_cast<int>(row0));
+        }
+        tma_load_2d(smem + C::kV, &tm_v, in_full, 0, static_cast<int>(row0));
+        n_in = 1;
+    }
+    if (warp == 1) {
+        // in-chunk inclusive prefix of log a (natural log units)
+        float a0 = log_a[row0 + lane], a1 = log_a[row0 + 32 + lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y0 = __shfl_up_sync(0xffffffffu, a0, off), y1 = __shfl_up_sync(0xffffffffu, a1, off);
+            if (lane >= off) {
+                a0 += y0;
+                a1 += y1;
+            }
+        }
+        const float tot0 = __shfl_sync(0xffffffffu, a0, 31);
+        cl[lane] = a0;
+        cl[32 + lane] = a1 + tot0;
+    }
+    if (warp == 2) {
+        bt[lane] = beta[row0 + lane];
+        bt[32 + lane] = beta[row0 + 32 + lane];
+    }
+    __syncthreads();
+    if (tid < 64) ce[tid] = expf(cl[63] - cl[tid]);
+    do {
+        if (tid == 0 && wait(in_full, 0)) {
+            tc_fence_after();
+            const uint32_t kq = smem_u32(smem + C::kKQ);
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {
+                const uint32_t off = (kk >> 2) * C::kKQPanel + (kk & 3) * 32;
+                mma_bf16(tmem, sdesc(kq + off, 16, 1024), sdesc(kq + off, 16, 1024), idesc_bf16(128, 64, 0, 0),
+                         kk > 0 ? 1u : 0u);
+            }
+            mma_commit(mma_a);
+            n_a = 1;
+            wait(mma_a, 0);
+        }
+        block_sync();
+        if (*fail) break;
+
+        // ---- G, QK out of TMEM; Bk, Bg into shared memory; right-hand sides in registers
+        float x[64];
+        if (grp != 2) {
+            tmem_ld32(tmem + lane_base, x);
+            tmem_ld32(tmem + lane_base + 32, x + 32);
+        }
+        const float clt = cl[t];
+        if (grp == 0) {
+            const float b = bt[t];
+            float4* bk = reinterpret_cast<float4*>(Bk + t * C::kLd);
+            float4* bg = reinterpret_cast<float4*>(Bg + t * C::kLd);
+#pragma unroll
+            for (int r4 = 0; r4 < 16; r4++) {
+                float vk[4], vg[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int r = 4 * r4 + e;
+                    vk[e] = r < t ? b * x[r] : 0.f;
+                    vg[e] = r < t ? b * expf(clt - cl[r]) * x[r] : 0.f;
+                }
+                bk[r4] = make_float4(vk[0], vk[1], vk[2], vk[3]);
+                bg[r4] = make_float4(vg[0], vg[1], vg[2], vg[3]);
+            }
+        }
+        // right-hand sides: e_t (Lk, Lg), tril(QK)_t (M), tril(Gamma (.) QK)_t (Z Lg)
+#pragma unroll
+        for (int r = 0; r < 64; r++) {
+            if (grp == 0 || grp == 2)
+                x[r] = r == t ? 1.f : 0.f;
+            else if (grp == 1)
+                x[r] = r <= t ? x[r] : 0.f;
+            else
+                x[r] = r <= t ? expf(clt - cl[r]) * x[r] : 0.f;
+        }
+        __syncthreads();
+        gdn_row_solve(grp < 2 ? Bk : Bg, x);
+        __syncthreads();  // Bk, Bg are read; A1 goes over them
+
+        // ---- A operands, bf16 hi + lo, K-major rows of 64 tokens: A1 = [Lk; M] diag(beta),
+        //      A2 = [Lg diag(beta); P]
+        {
+            float lam[7];
+            if (grp == 3) {
+#pragma unroll
+                for (int l = 0; l < 7; l++) lam[l] = lambda[(row0 + t) * L + l];
+            }
+            uint8_t* dst = smem + ((grp == 0 || grp == 1) ? C::kR : C::kA2);
+            const int row = (grp & 1) ? 64 + t : t;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; c8++) {
+                uint32_t h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    float w2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; u++) {
+                        const int sidx = 8 * c8 + 2 * e + u;
+                        float w = x[sidx] * bt[sidx];
+                        if (grp == 3) {
+                            const int xo = t ^ sidx;
+                            float lw = xo >= 32 ? lam[6] : lam[5];
+                            lw = xo < 16 ? lam[4] : lw;
+                            lw = xo < 8 ? lam[3] : lw;
+                            lw = xo < 4 ? lam[2] : lw;
+                            lw = xo < 2 ? lam[1] : lw;
+                            lw = xo == 0 ? lam[0] : lw;
+                            w = sidx <= t ? w * lw : 0.f;
+                        }
+                        w2[u] = w;
+                    }
+                    h[e] = pack_bf16(w2[0], w2[1]);
+                    const float2 hf = unpack_bf16(h[e]);
+                    l[e] = pack_bf16(w2[0] - hf.x, w2[1] - hf.y);
+                }
+                *reinterpret_cast<uint4*>(dst + sw128_off(row, c8)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(dst + 16384 + sw128_off(row, c8)) = make_uint4(l[0], l[1], l[2], l[3]);
+            }
+        }
+        fence_async_smem();
+        block_sync();
+        if (tid == 0) {
+            const uint32_t kq = smem_u32(smem + C::kKQ), a1 = smem_u32(smem + C::kR), a2 = smem_u32(smem + C::kA2),
+                           vb = smem_u32(smem + C::kV);
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++)
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const uint32_t acc = (kk > 0 || h > 0) ? 1u : 0u;
+                    mma_bf16(tmem + 64, sdesc(a1 + h * 16384 + kk * 32, 16, 1024),
+                             sdesc(kq + kk * 2048, C::kKQPanel, 1024), idesc_bf16(128, 128, 0, 1), acc);
+                    mma_bf16(tmem + 192, sdesc(a2 + h * 16384 + kk * 32, 16, 1024), sdesc(vb + kk * 2048, 8192, 1024),
+                             idesc_bf16(128, 64, 0, 1), acc);
+                }
+            mma_commit(mma_bc);
+            n_bc = 1;
+            wait(mma_bc, 0);
+        }
+        block_sync();
+        if (*fail) break;
+
+        // ---- W, Q~ (fp32, the level pass reads them), U (into shared memory), in-chunk output
+        {
+            const int half = warp >> 2;  // which 64 of the 128 columns of MMA-b, 32 of the 64 of MMA-c
+            const bool top = (warp & 3) < 2;  // TMEM lanes 0..63 (W, U rows) or 64..127 (Q~, output rows)
+            float v[64];
+            tmem_ld32(tmem + lane_base + 64 + 64 * half, v);
+            tmem_ld32(tmem + lane_base + 96 + 64 * half, v + 32);
+            const size_t wrow = (static_cast<size_t>(bh) * N + j) * C::kC + t;
+            if (64 * half < dk) {
+                if (top) {
+                    float4* dst = reinterpret_cast<float4*>(Wg + wrow * dk + 64 * half);
+#pragma unroll
+                    for (int c4 = 0; c4 < 16; c4++)
+                        dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                } else {
+                    const float e = expf(clt);
+                    const uint4* qrow = reinterpret_cast<const uint4*>(q + (row0 + t) * dk + 64 * half);
+                    float4* dst = reinterpret_cast<float4*>(Qt + wrow * dk + 64 * half);
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; c8++) {
+                        const uint4 u = qrow[c8];
+                        const float2 f0 = unpack_bf16(u.x), f1 = unpack_bf16(u.y), f2 = unpack_bf16(u.z),
+                                     f3 = unpack_bf16(u.w);
+                        dst[2 * c8] = make_float4(e * (f0.x - v[8 * c8]), e * (f0.y - v[8 * c8 + 1]),
+                                                  e * (f1.x - v[8 * c8 + 2]), e * (f1.y - v[8 * c8 + 3]));
+                        dst[2 * c8 + 1] = make_float4(e * (f2.x - v[8 * c8 + 4]), e * (f2.y - v[8 * c8 + 5]),
+                                                      e * (f3.x - v[8 * c8 + 6]), e * (f3.y - v[8 * c8 + 7]));
+                    }
+                }
+            }
+            tmem_ld32(tmem + lane_base + 192 + 32 * half, v);
+            if (top) {
+                // U row t scaled by its decay to the chunk end, bf16 hi + lo, MN-major rows of 64 dv
+                const float w = ce[t];
+                uint8_t* uh = smem + C::kR;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; c8++) {
+                    uint32_t h[4], l[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const float a = w * v[8 * c8 + 2 * e], b = w * v[8 * c8 + 2 * e + 1];
+                        h[e] = pack_bf16(a, b);
+                        const float2 hf = unpack_bf16(h[e]);
+                        l[e] = pack_bf16(a - hf.x, b - hf.y);
+                    }
+                    *reinterpret_cast<uint4*>(uh + sw128_off(t, 4 * half + c8)) = make_uint4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<uint4*>(uh + 8192 + sw128_off(t, 4 * half + c8)) =
+                        make_uint4(l[0], l[1], l[2], l[3]);
+                }
+            } else if (N > 1) {
+                float4* dst = reinterpret_cast<float4*>(oacc + (row0 + t) * DV + 32 * half);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; c4++)
+                    dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(out + (row0 + t) * DV + 32 * half);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; c8++)
+                    dst[c8] = make_uint4(pack_bf16(v[8 * c8], v[8 * c8 + 1]), pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]),
+                                         pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]),
+                                         pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
+            }
+        }
+        if (N == 1) break;
+        fence_async_smem();
+        block_sync();
+        if (tid == 0) {
+            const uint32_t kq = smem_u32(smem + C::kKQ), ub = smem_u32(smem + C::kR);
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++)
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+                    mma_bf16(tmem, sdesc(kq + kk * 2048, C::kKQPanel, 1024), sdesc(ub + h * 8192 + kk * 2048, 8192, 1024),
+                             idesc_bf16(128, 64, 1, 1), (kk > 0 || h > 0) ? 1u : 0u);
+            mma_commit(mma_d);
+            n_d = 1;
+            wait(mma_d, 0);
+            gam[static_cast<size_t>(bh) * N + j] = expf(cl[63]);
+        }
+        block_sync();
+        if (*fail) break;
+        {
+            // the chunk's state: TMEM lane i = dk row i; warps 0..3 columns 0..31, warps 4..7 32..63
+            const int i = (warp & 3) * 32 + lane;
+            const int c0 = 32 * (warp >> 2);
+            float v[32];
+            tmem_ld32(tmem + lane_base + c0, v);
+            if (i < dk) {
+                float4* dst = reinterpret_cast<float4*>(
+                    nodes + (static_cast<size_t>(bh) * node_count + j) * static_cast<size_t>(dk) * DV +
+                    static_cast<size_t>(i) * DV + c0);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; c4++)
+                    dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+            }
+        }
+    } while (false);
+
+    if (tid == 0 && *fail) {
+        if (n_in) mbar_wait(in_full, 0);
+        if (n_a) mbar_wait(mma_a, 0);
+        if (n_bc) mbar_wait(mma_bc, 0);
+        if (n_d) mbar_wait(mma_d, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 }  // namespace
 
 bool gdn_level_tc_supported(const GdnPlan& pl, int dtype) {
     return dtype == 0 && pl.C == LvCfg::kC && pl.dv == LvCfg::kDV && (pl.dk == 64 || pl.dk == 128);
+}
+
+bool gdn_chunk_tc_supported(const GdnPlan& pl, int dtype) {
+    return dtype == 0 && pl.C == CkCfg::kC && pl.dv == CkCfg::kDV && (pl.dk == 64 || pl.dk == 128);
+}
+
+// The chunk pass on tensor cores: W, Q~, node (0, j), gamma_j and the in-chunk output (into
+// oacc, or straight into out when the sequence is one chunk).
+cudaError_t gdn_chunk_tc(const GdnPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
+                         const float* beta, const float* lambda, float* Wg, float* Qt, float* nodes, float* gam,
+                         float* oacc, void* out, int L, int* err, cudaStream_t stream) {
+    const uint64_t rows = static_cast<uint64_t>(pl.B) * pl.H * pl.T;
+    CUtensorMap tq, tk, tv;
+    if (!make_map_box(&tq, q, false, rows, pl.dk, 64, CkCfg::kC) || !make_map_box(&tk, k, false, rows, pl.dk, 64, CkCfg::kC) ||
+        !make_map_box(&tv, v, false, rows, pl.dv, 64, CkCfg::kC))
+        return cudaErrorInvalidValue;
+    const int smem = CkCfg::kBytes + CkCfg::kSlack;
+    cudaError_t e = cudaFuncSetAttribute(gdn_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    gdn_chunk_tc_kernel<<<dim3(pl.N, pl.B * pl.H), 256, smem, stream>>>(
+        tq, tk, tv, static_cast<const __nv_bfloat16*>(q), log_a, beta, lambda, Wg, Qt, nodes, gam, oacc,
+        static_cast<__nv_bfloat16*>(out), pl.T, pl.N, pl.dk, L, pl.node_count, err);
+    note_launch(stream, "gdn_chunk_tc");
+    return cudaGetLastError();
 }
 
 // All Fenwick levels of the prefill on tensor cores (one launch per level, in order).

@@ -157,7 +157,11 @@ bool make_gdn_plan(int B, int H, int T, int dk, int dv, int chunk, GdnPlan* plan
 cudaError_t gdn_forward(const GdnPlan& plan, int dtype, const void* q, const void* k, const void* v,
                         const float* log_a, const float* beta, const float* lambda, void* out, void* workspace,
                         int* err, cudaStream_t stream);
-// Tensor-core level pass (bf16, C = 64, dv = 64, dk in {64, 128}); csrc/lla_gdn_tc.cu.
+// Tensor-core chunk and level passes (bf16, C = 64, dv = 64, dk in {64, 128}); csrc/lla_gdn_tc.cu.
+bool gdn_chunk_tc_supported(const GdnPlan& plan, int dtype);
+cudaError_t gdn_chunk_tc(const GdnPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
+                         const float* beta, const float* lambda, float* Wg, float* Qt, float* nodes, float* gam,
+                         float* oacc, void* out, int L, int* err, cudaStream_t stream);
 bool gdn_level_tc_supported(const GdnPlan& plan, int dtype);
 cudaError_t gdn_levels_tc(const GdnPlan& plan, const void* k, const float* Wg, const float* Qt, float* nodes,
                           const float* gam, const float* lambda, float* oacc, int L, int c_log2, int* err,

@@ -86,8 +86,9 @@ def test_gdn_bf16_shapes(T, dk, dv, chunk):
 
 @pytest.mark.parametrize("dk", [128, 64])
 def test_gdn_bf16_levels_run_on_tensor_cores(dk):
-    """bf16 with chunk 64 and dv = 64 carries the Fenwick nodes on tcgen05 (gdn_level_tc), at
-    dk = 128 and at dk = 64 (zero-padded operands); the result matches the oracle."""
+    """bf16 with chunk 64 and dv = 64 runs the chunk pass and the Fenwick level carries on
+    tcgen05 (gdn_chunk_tc, gdn_level_tc), at dk = 128 and at dk = 64 (zero-padded operands);
+    the result matches the oracle."""
     from log_linear_attention_gb300 import binding
     cfg = _cfg("gdn-headline", B=1, H=2, T=1024, dk=dk)
     inp, beta = _problem(cfg, 40 + dk)
@@ -95,7 +96,7 @@ def test_gdn_bf16_levels_run_on_tensor_cores(dk):
     out = torch.empty_like(v)
     names = [n for n, _ in binding.gdn_forward_profile(q, k, v, log_a, torch.from_numpy(beta).cuda(), lam, 64, out)]
     assert binding.device_error() == 0
-    assert "gdn_level_tc" in names and "gdn_level" not in names, names
+    assert names[0] == "gdn_chunk_tc" and "gdn_level_tc" in names and "gdn_level" not in names, names
     assert rel_err_per_head(out.float().cpu().numpy(), _ref(inp, beta)) <= TOL_BF16
 
 
