@@ -52,13 +52,17 @@ struct LvCfg {
     static constexpr uint32_t kKBytes = 2 * kKPanel;
 };
 
-// grid (number of read nodes of level p per head, B*H), 128 threads (thread = TMEM lane),
-// two CTAs per SM.
+// Persistent: grid min(chains, 2 per SM), 128 threads (thread = TMEM lane), two CTAs per SM.
+// A CTA walks the read nodes c = blockIdx.x, blockIdx.x + gridDim.x, ... of level p (chain c:
+// head c / n_even, read node m = 2 (c % n_even)), step by step through each chain's chunks. The
+// copies of the next step in that walk (the next chunk of the chain, else the first chunk of
+// the CTA's next chain) are issued as soon as their buffers are free: [W; Q~] once MMA1 has
+// read the stage, K once MMA2 has (or once the step is over, when it needs no MMA2).
 __global__ void __launch_bounds__(128, 2)
     gdn_level_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_qt,
                         const __grid_constant__ CUtensorMap tm_k, float* __restrict__ nodes,
                         const float* __restrict__ gam, const float* __restrict__ lambda, float* __restrict__ oacc,
-                        int T, int N, int dk, int L, int lev, int p, int P, int node_count,
+                        int T, int N, int dk, int L, int lev, int p, int P, int node_count, int n_even, int n_chains,
                         const __grid_constant__ GdnTcLevels lo, int* err) {
     using C = LvCfg;
     constexpr int DV = C::kDV;
@@ -77,11 +81,17 @@ __global__ void __launch_bounds__(128, 2)
         if (tid == 0) record_error(err, kDevBadInput);
         return;
     }
-    const int xi = blockIdx.x, bh = blockIdx.y;
-    const int m = 2 * xi, span = 1 << p;
-    const int b0 = (m + 1) * span, b1 = min((m + 2) * span, N);
-    const bool want_parent = (m + 2) * span <= N && p + 1 < P;
+    const int span = 1 << p;
     const size_t msz = static_cast<size_t>(dk) * DV;
+    auto chain_range = [&](int c, int& bh, int& xi, int& b0, int& b1) {
+        bh = c / n_even;
+        xi = c - bh * n_even;
+        b0 = (2 * xi + 1) * span;
+        b1 = min((2 * xi + 2) * span, N);
+    };
+    auto node_ptr = [&](int bh, int lvl, int idx) {
+        return nodes + (static_cast<size_t>(bh) * node_count + lo.off[lvl] + idx) * msz;
+    };
 
     if (tid == 0) {
         mbar_init(full_a, 1);
@@ -103,8 +113,8 @@ __global__ void __launch_bounds__(128, 2)
     constexpr uint32_t kIdB = idesc_bf16(128, DV, 1, 1);  // K^T (MN-major) x Y (MN-major)
 
     int n_a = 0, n_k = 0, n_m1 = 0, n_m2 = 0;  // copies and MMA groups issued (thread 0)
-    auto load_a = [&](int jc) {
-        const int r = (bh * N + jc) * C::kC;
+    auto load_a = [&](int c, int jc) {
+        const int r = ((c / n_even) * N + jc) * C::kC;
         mbar_expect_tx(full_a, C::kABytes);
 #pragma unroll
         for (int q = 0; q < 4; q++) {
@@ -113,12 +123,27 @@ __global__ void __launch_bounds__(128, 2)
         }
         n_a++;
     };
-    auto load_k = [&](int jc) {
-        const int r = bh * T + jc * C::kC;
+    auto load_k = [&](int c, int jc) {
+        const int r = (c / n_even) * T + jc * C::kC;
         mbar_expect_tx(full_k, C::kKBytes);
         tma_load_2d(smem + C::kK, &tm_k, full_k, 0, r);
         tma_load_2d(smem + C::kK + C::kKPanel, &tm_k, full_k, 64, r);
         n_k++;
+    };
+    // the step after (chain c, chunk jc) in this CTA's walk; false at the end of the walk
+    auto next_step = [&](int c, int jc, int& nc, int& njc) -> bool {
+        int bh, xi, b0, b1;
+        chain_range(c, bh, xi, b0, b1);
+        if (jc + 1 < b1) {
+            nc = c;
+            njc = jc + 1;
+            return true;
+        }
+        nc = c + gridDim.x;
+        if (nc >= n_chains) return false;
+        chain_range(nc, bh, xi, b0, b1);
+        njc = b0;
+        return true;
     };
     // thread 0 waits; the block learns the outcome from `fail` after its next barrier
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -136,132 +161,160 @@ __global__ void __launch_bounds__(128, 2)
         for (int d = 0; d < DV; d++) *reinterpret_cast<float*>(base + d * 128 + ((c ^ (d & 7)) << 4)) = x[d];
     };
 
-    if (tid == 0) {
-        load_a(b0);
-        load_k(b0);
+    if (tid == 0 && static_cast<int>(blockIdx.x) < n_chains) {
+        int bh, xi, b0, b1;
+        chain_range(blockIdx.x, bh, xi, b0, b1);
+        load_a(blockIdx.x, b0);
+        load_k(blockIdx.x, b0);
     }
-    {
-        // X = node (p, m); rows dk..127 are zero
-        float x[DV];
-        const float4* src = reinterpret_cast<const float4*>(
-            nodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + m) * msz + static_cast<size_t>(tid) * DV);
-#pragma unroll
-        for (int c4 = 0; c4 < DV / 4; c4++) {
-            const float4 f = tid < dk ? src[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
-            x[4 * c4] = f.x; x[4 * c4 + 1] = f.y; x[4 * c4 + 2] = f.z; x[4 * c4 + 3] = f.w;
+    int gs = 0;  // steps taken: the phase of full_a, full_k and mma1
+    for (int c = blockIdx.x; c < n_chains; c += gridDim.x) {
+        int bh, xi, b0, b1;
+        chain_range(c, bh, xi, b0, b1);
+        const int m = 2 * xi;
+        const bool want_parent = (m + 2) * span <= N && p + 1 < P;
+        if (tid == 0 && c + static_cast<int>(gridDim.x) < n_chains) {
+            // the next chain's node and sibling into L2 while this chain runs
+            int nbh, nxi, nb0, nb1;
+            chain_range(c + gridDim.x, nbh, nxi, nb0, nb1);
+            prefetch_l2(node_ptr(nbh, p, 2 * nxi), static_cast<uint32_t>(msz * 4));
+            if ((2 * nxi + 2) * span <= N && p + 1 < P)
+                prefetch_l2(node_ptr(nbh, p, 2 * nxi + 1), static_cast<uint32_t>(msz * 4));
         }
-        tmem_st32(tX, x);
-        tmem_st32(tX + 32, x + 32);
-        stage_xt(x);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    float Gam = 1.f;  // product of gamma over the chunks passed
-    for (int jc = b0, s = 0; jc < b1; jc++, s++) {
-        const uint32_t ph = s & 1;
-        const bool last = jc + 1 == b1;
-        const bool carry = !last || want_parent;
-        if (tid == 0 && wait(full_a, ph)) {
-            tc_fence_after();
-            const uint32_t ab = smem_u32(smem + C::kA), xb = smem_u32(smem + C::kX);
+        {
+            // X = node (p, m); rows dk..127 are zero
+            float x[DV];
+            const float4* src = reinterpret_cast<const float4*>(node_ptr(bh, p, m) + static_cast<size_t>(tid) * DV);
 #pragma unroll
-            for (int kk = 0; kk < 16; kk++) {
-                const uint32_t oa = (kk >> 2) * C::kAPanel + (kk & 3) * 32;
-                const uint32_t ob = (kk >> 2) * C::kXPanel + (kk & 3) * 32;
-                mma_tf32(tmem, sdesc(ab + oa, 16, 1024), sdesc(xb + ob, 16, 1024), kIdA, kk > 0 ? 1u : 0u);
+            for (int c4 = 0; c4 < DV / 4; c4++) {
+                const float4 f = tid < dk ? src[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                x[4 * c4] = f.x; x[4 * c4 + 1] = f.y; x[4 * c4 + 2] = f.z; x[4 * c4 + 3] = f.w;
             }
-            mma_commit(mma1);
-            n_m1++;
-            if (wait(mma1, ph) && !last) load_a(jc + 1);  // MMA1 has read the stage
+            tmem_st32(tX, x);
+            tmem_st32(tX + 32, x + 32);
+            stage_xt(x);
         }
+        fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (*fail) break;
-        const size_t row0 = static_cast<size_t>(bh) * T + static_cast<size_t>(jc) * C::kC;
-        float v[DV];
-        tmem_ld32(tD, v);
-        tmem_ld32(tD + 32, v + 32);
-        if (tid < C::kC) {
-            if (carry) {
-                // -Y row tid as bf16 hi + lo, MN-major rows of 64 dv (one 128-byte row per token)
-                uint8_t* hi = smem + C::kX;
-                uint8_t* lo_ = smem + C::kX + C::kXPanel;
+
+        float Gam = 1.f;  // product of gamma over the chunks passed
+        for (int jc = b0; jc < b1; jc++, gs++) {
+            const uint32_t ph = gs & 1;
+            const bool last = jc + 1 == b1;
+            const bool carry = !last || want_parent;
+            int nc = 0, njc = 0;
+            const bool more = next_step(c, jc, nc, njc);
+            const size_t row0 = static_cast<size_t>(bh) * T + static_cast<size_t>(jc) * C::kC;
+            // the read's lambda and accumulator row, loaded while MMA1 runs
+            float lw = 0.f;
+            float4 oa[DV / 4];
+            if (tid >= C::kC) {
+                const size_t t = row0 + (tid - C::kC);
+                lw = lambda[t * L + lev] * Gam;
+                const float4* o = reinterpret_cast<const float4*>(oacc + t * DV);
 #pragma unroll
-                for (int c8 = 0; c8 < DV / 8; c8++) {
-                    uint32_t h[4], l[4];
+                for (int c4 = 0; c4 < DV / 4; c4++) oa[c4] = o[c4];
+            }
+            if (tid == 0 && wait(full_a, ph)) {
+                tc_fence_after();
+                const uint32_t ab = smem_u32(smem + C::kA), xb = smem_u32(smem + C::kX);
 #pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const float a = -v[8 * c8 + 2 * e], b = -v[8 * c8 + 2 * e + 1];
-                        h[e] = pack_bf16(a, b);
-                        const float2 hf = unpack_bf16(h[e]);
-                        l[e] = pack_bf16(a - hf.x, b - hf.y);
+                for (int kk = 0; kk < 16; kk++) {
+                    const uint32_t oa_ = (kk >> 2) * C::kAPanel + (kk & 3) * 32;
+                    const uint32_t ob = (kk >> 2) * C::kXPanel + (kk & 3) * 32;
+                    mma_tf32(tmem, sdesc(ab + oa_, 16, 1024), sdesc(xb + ob, 16, 1024), kIdA, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(mma1);
+                n_m1++;
+                if (wait(mma1, ph) && more) load_a(nc, njc);  // MMA1 has read the stage
+            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (*fail) break;
+            float v[DV];
+            tmem_ld32(tD, v);
+            tmem_ld32(tD + 32, v + 32);
+            if (tid < C::kC) {
+                if (carry) {
+                    // -Y row tid as bf16 hi + lo, MN-major rows of 64 dv (one 128-byte row per token)
+                    uint8_t* hi = smem + C::kX;
+                    uint8_t* lo_ = smem + C::kX + C::kXPanel;
+#pragma unroll
+                    for (int c8 = 0; c8 < DV / 8; c8++) {
+                        uint32_t h[4], l[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const float a = -v[8 * c8 + 2 * e], b = -v[8 * c8 + 2 * e + 1];
+                            h[e] = pack_bf16(a, b);
+                            const float2 hf = unpack_bf16(h[e]);
+                            l[e] = pack_bf16(a - hf.x, b - hf.y);
+                        }
+                        *reinterpret_cast<uint4*>(hi + sw128_off(tid, c8)) = make_uint4(h[0], h[1], h[2], h[3]);
+                        *reinterpret_cast<uint4*>(lo_ + sw128_off(tid, c8)) = make_uint4(l[0], l[1], l[2], l[3]);
                     }
-                    *reinterpret_cast<uint4*>(hi + sw128_off(tid, c8)) = make_uint4(h[0], h[1], h[2], h[3]);
-                    *reinterpret_cast<uint4*>(lo_ + sw128_off(tid, c8)) = make_uint4(l[0], l[1], l[2], l[3]);
+                }
+            } else {
+                float4* o = reinterpret_cast<float4*>(oacc + (row0 + (tid - C::kC)) * DV);
+#pragma unroll
+                for (int c4 = 0; c4 < DV / 4; c4++)
+                    o[c4] = make_float4(fmaf(lw, v[4 * c4], oa[c4].x), fmaf(lw, v[4 * c4 + 1], oa[c4].y),
+                                        fmaf(lw, v[4 * c4 + 2], oa[c4].z), fmaf(lw, v[4 * c4 + 3], oa[c4].w));
+            }
+            if (!carry) {
+                // no MMA2: K of this step arrived unused; the next step's K may take its buffer
+                if (tid == 0 && wait(full_k, ph) && more) load_k(nc, njc);
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+                gs++;
+                break;
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (tid == 0 && wait(full_k, ph)) {
+                tc_fence_after();
+                const uint32_t kb = smem_u32(smem + C::kK), yb = smem_u32(smem + C::kX);
+#pragma unroll
+                for (int kk = 0; kk < C::kC / 16; kk++)
+#pragma unroll
+                    for (int h = 0; h < 2; h++)
+                        mma_bf16(tmem + 64, sdesc(kb + kk * 2048, C::kKPanel, 1024),
+                                 sdesc(yb + h * C::kXPanel + kk * 2048, C::kXPanel, 1024), kIdB, 1u);
+                mma_commit(mma2);
+                n_m2++;
+                if (wait(mma2, (n_m2 - 1) & 1) && more) load_k(nc, njc);  // MMA2 has read K
+            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (*fail) break;
+            Gam *= gam[static_cast<size_t>(bh) * N + jc];
+            tmem_ld32(tX, v);
+            tmem_ld32(tX + 32, v + 32);
+            if (!last) {
+                stage_xt(v);
+            } else if (tid < dk) {
+                // node (p + 1, m / 2) = Gamma X^ + node (p, m + 1)
+                const float4* sib = reinterpret_cast<const float4*>(node_ptr(bh, p, m + 1) + static_cast<size_t>(tid) * DV);
+                float4* dst = reinterpret_cast<float4*>(node_ptr(bh, p + 1, xi) + static_cast<size_t>(tid) * DV);
+#pragma unroll
+                for (int c4 = 0; c4 < DV / 4; c4++) {
+                    const float4 b = sib[c4];
+                    dst[c4] = make_float4(fmaf(Gam, v[4 * c4], b.x), fmaf(Gam, v[4 * c4 + 1], b.y),
+                                          fmaf(Gam, v[4 * c4 + 2], b.z), fmaf(Gam, v[4 * c4 + 3], b.w));
                 }
             }
-        } else {
-            const size_t t = row0 + (tid - C::kC);
-            const float w = lambda[t * L + lev] * Gam;
-            float4* o = reinterpret_cast<float4*>(oacc + t * DV);
-#pragma unroll
-            for (int c4 = 0; c4 < DV / 4; c4++) {
-                float4 a = o[c4];
-                a.x = fmaf(w, v[4 * c4], a.x);
-                a.y = fmaf(w, v[4 * c4 + 1], a.y);
-                a.z = fmaf(w, v[4 * c4 + 2], a.z);
-                a.w = fmaf(w, v[4 * c4 + 3], a.w);
-                o[c4] = a;
-            }
-        }
-        if (!carry) break;
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0 && wait(full_k, ph)) {
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
             tc_fence_after();
-            const uint32_t kb = smem_u32(smem + C::kK), yb = smem_u32(smem + C::kX);
-#pragma unroll
-            for (int kk = 0; kk < C::kC / 16; kk++)
-#pragma unroll
-                for (int h = 0; h < 2; h++)
-                    mma_bf16(tmem + 64, sdesc(kb + kk * 2048, C::kKPanel, 1024),
-                             sdesc(yb + h * C::kXPanel + kk * 2048, C::kXPanel, 1024), kIdB, 1u);
-            mma_commit(mma2);
-            n_m2++;
-            if (wait(mma2, ph) && !last) load_k(jc + 1);  // MMA2 has read K
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
         if (*fail) break;
-        Gam *= gam[static_cast<size_t>(bh) * N + jc];
-        tmem_ld32(tX, v);
-        tmem_ld32(tX + 32, v + 32);
-        if (!last) {
-            stage_xt(v);
-        } else if (tid < dk) {
-            // node (p + 1, m / 2) = Gamma X^ + node (p, m + 1)
-            const float4* sib = reinterpret_cast<const float4*>(
-                nodes + (static_cast<size_t>(bh) * node_count + lo.off[p] + m + 1) * msz + static_cast<size_t>(tid) * DV);
-            float4* dst = reinterpret_cast<float4*>(
-                nodes + (static_cast<size_t>(bh) * node_count + lo.off[p + 1] + xi) * msz + static_cast<size_t>(tid) * DV);
-#pragma unroll
-            for (int c4 = 0; c4 < DV / 4; c4++) {
-                const float4 b = sib[c4];
-                dst[c4] = make_float4(fmaf(Gam, v[4 * c4], b.x), fmaf(Gam, v[4 * c4 + 1], b.y),
-                                      fmaf(Gam, v[4 * c4 + 2], b.z), fmaf(Gam, v[4 * c4 + 3], b.w));
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
     }
 
     if (tid == 0 && *fail) {
@@ -690,14 +743,19 @@ cudaError_t gdn_levels_tc(const GdnPlan& pl, const void* k, const float* Wg, con
     const int smem = LvCfg::kBytes + LvCfg::kSlack;
     cudaError_t e = cudaFuncSetAttribute(gdn_level_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidValue;
     GdnTcLevels lo;
     for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
     for (int p = 0; p < pl.P; p++) {
         const int n_even = (((pl.N - 1) >> p) + 1) / 2;
         if (n_even <= 0) continue;
-        gdn_level_tc_kernel<<<dim3(n_even, static_cast<unsigned>(BH)), 128, smem, stream>>>(
-            tw, tq, tk, nodes, gam, lambda, oacc, pl.T, pl.N, pl.dk, L, c_log2 + 1 + p, p, pl.P, pl.node_count, lo,
-            err);
+        const int n_chains = static_cast<int>(BH) * n_even;
+        const int grid = n_chains < 2 * sms ? n_chains : 2 * sms;
+        gdn_level_tc_kernel<<<grid, 128, smem, stream>>>(tw, tq, tk, nodes, gam, lambda, oacc, pl.T, pl.N, pl.dk, L,
+                                                         c_log2 + 1 + p, p, pl.P, pl.node_count, n_even, n_chains,
+                                                         lo, err);
         note_launch(stream, "gdn_level_tc");
     }
     return cudaGetLastError();

@@ -423,19 +423,6 @@ struct OutCfg {
     static constexpr int kThreads = (3 + kEpiWarps) * 32;
 };
 
-// Pull a 128-row x 64-column box of a tensor map into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-// Pull a contiguous range (16-byte aligned, size % 16 == 0) into L2.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // 4-byte asynchronous global -> shared copy (no alignment beyond 4 bytes needed).
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
