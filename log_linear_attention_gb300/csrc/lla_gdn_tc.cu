@@ -491,25 +491,29 @@ __global__ void __launch_bounds__(256, 2)
         block_sync();
         if (*fail) break;
 
-        // ---- G, QK out of TMEM; Bk, Bg into shared memory; right-hand sides in registers
+        // ---- G, QK out of TMEM; Bk, Bg into shared memory (row t: warps 0, 1 build columns
+        //      0..31, warps 4, 5 columns 32..63); right-hand sides in registers. Decay factors
+        //      2^((cl_t - cl_r) log2 e) have non-positive exponents (r <= t).
         float x[64];
-        if (grp != 2) {
+        {
             tmem_ld32(tmem + lane_base, x);
             tmem_ld32(tmem + lane_base + 32, x + 32);
         }
-        const float clt = cl[t];
-        if (grp == 0) {
+        const float clt = cl[t] * kLog2e;
+        if (grp == 0 || grp == 2) {
             const float b = bt[t];
-            float4* bk = reinterpret_cast<float4*>(Bk + t * C::kLd);
-            float4* bg = reinterpret_cast<float4*>(Bg + t * C::kLd);
+            const int h = grp >> 1;  // column half
+            float4* bk = reinterpret_cast<float4*>(Bk + t * C::kLd + 32 * h);
+            float4* bg = reinterpret_cast<float4*>(Bg + t * C::kLd + 32 * h);
 #pragma unroll
-            for (int r4 = 0; r4 < 16; r4++) {
+            for (int r4 = 0; r4 < 8; r4++) {
                 float vk[4], vg[4];
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
-                    const int r = 4 * r4 + e;
-                    vk[e] = r < t ? b * x[r] : 0.f;
-                    vg[e] = r < t ? b * expf(clt - cl[r]) * x[r] : 0.f;
+                    const int r = 32 * h + 4 * r4 + e;
+                    const float g = h ? x[32 + 4 * r4 + e] : x[4 * r4 + e];
+                    vk[e] = r < t ? b * g : 0.f;
+                    vg[e] = r < t ? b * ex2_ftz(clt - cl[r] * kLog2e) * g : 0.f;
                 }
                 bk[r4] = make_float4(vk[0], vk[1], vk[2], vk[3]);
                 bg[r4] = make_float4(vg[0], vg[1], vg[2], vg[3]);
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__(256, 2)
             else if (grp == 1)
                 x[r] = r <= t ? x[r] : 0.f;
             else
-                x[r] = r <= t ? expf(clt - cl[r]) * x[r] : 0.f;
+                x[r] = r <= t ? ex2_ftz(clt - cl[r] * kLog2e) * x[r] : 0.f;
         }
         __syncthreads();
         gdn_row_solve(grp < 2 ? Bk : Bg, x);
@@ -606,7 +610,7 @@ __global__ void __launch_bounds__(256, 2)
                     for (int c4 = 0; c4 < 16; c4++)
                         dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
                 } else {
-                    const float e = expf(clt);
+                    const float e = ex2_ftz(clt);  // e^{cl_t}, clt in log2 units
                     const uint4* qrow = reinterpret_cast<const uint4*>(q + (row0 + t) * dk + 64 * half);
                     float4* dst = reinterpret_cast<float4*>(Qt + wrow * dk + 64 * half);
 #pragma unroll
