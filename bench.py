@@ -529,6 +529,7 @@ def bench_gdn(args, dev, stream, peaks) -> dict:
         per[kname] = per.get(kname, 0.0) + kms
     work = gdn_work(cfg)
     tfl = work["flops"] / (ms / 1e3) / 1e12
+    tf32_peak = peaks["bf16_tflops"] / 2
     # decode: the decode workload's shapes and positions, random states
     dcfg = inputs.DECODE_CONFIG
     pos = torch.from_numpy(inputs.make_positions(dcfg, 0)).to(dev)
@@ -561,9 +562,11 @@ def bench_gdn(args, dev, stream, peaks) -> dict:
                                     f"chunk={cfg.chunk}, bf16 q/k/v (unit-norm q, k), fp32 log_a/beta/lambda",
                         "ms": ms, "tokens_per_s": cfg.tokens / (ms / 1e3), "algorithmic_gflop": work["flops"] / 1e9,
                         "kernels_ms": per,
-                        "roofline": {"bound": "alu", "achieved": tfl, "peak": ALU_F32_TFLOPS, "unit": "TFLOP/s",
-                                     "frac": tfl / ALU_F32_TFLOPS,
-                                     "peak_source": "derived: 152 SM x 128 FMA x 2.07 GHz (fp32 CUDA cores)"}},
+                        "roofline": {"bound": "tensor", "achieved": tfl, "peak": tf32_peak, "unit": "TFLOP/s",
+                                     "frac": tfl / tf32_peak,
+                                     "peak_source": f"{peaks['source']} bf16 x 1/2 (tf32, the dtype of the level "
+                                                    "pass's dominant MMA)",
+                                     "hbm_frac_of_call": work["bytes"] / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}},
             "decode": {"workload": "64 sequences x 16 heads, dk=128 dv=64, t ~ U[1,65536), fp32 states (18 slots)",
                        "steps": nsteps, "us_per_step": 1e3 * d_ms / nsteps, "gbs": d_gbs,
                        "frac_of_hbm": d_gbs / peaks["hbm_gbs"],

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(256, 2)
     __shared__ float g2_sh[kSegTiles];          // tile totals, log2 units
     __shared__ int fail_sh;
 
+    grid_dep_launch();  // the merge kernel may be launched while this grid drains
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, bh = blockIdx.y;
     const int tile0 = seg * kSegTiles;
@@ -301,6 +302,8 @@ __global__ void __launch_bounds__(256)
                     int NT, int q, int P, int nseg, int node_count, int msz, const __grid_constant__ LevelOffsets lo) {
     __shared__ float wsg[1024];      // per-segment totals, then weights, of this block's node
     extern __shared__ float g_sh[];  // the head's tile totals (decay-table block only)
+    grid_dep_wait();                 // the node kernel's totals (launched early, see launch_pdl)
+    grid_dep_launch();
     const int bh = blockIdx.z;
     const float* gh = g_tiles + static_cast<size_t>(bh) * NT;
     if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *tile_counter = 0;
@@ -481,6 +484,7 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    grid_dep_wait();  // the node and merge kernels' outputs (launched early, see launch_pdl)
 
     // Tiles are handed out by a global counter (zeroed by tc_merge), head by head and,
     // within a head, from the last tile down: the tiles with the most Fenwick levels
@@ -1005,6 +1009,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    grid_dep_wait();  // the node and merge kernels' outputs (launched early, see launch_pdl)
 
     // head-major; within a head from the last tile down (most Fenwick levels first)
     auto tile_of = [&](int idx, int& bh, int& j) {
@@ -1389,8 +1394,10 @@ cudaError_t tc_node_stage(const TcPlan& pl, const CUtensorMap& tk, const CUtenso
         const int msz = kDk * DV;
         int n_above = 0;
         for (int p = qlog + 1; p < pl.P; p++) n_above += (((pl.NT - 1) >> p) + 1) / 2;
-        tc_merge_kernel<<<dim3(msz / 1024 + 1, n_above > 0 ? n_above : 1, BH), 256, pl.NT * sizeof(float), stream>>>(
-            seg_tot, g_tiles, nodes, dtab, tile_counter, pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
+        const cudaError_t e = launch_pdl(tc_merge_kernel, dim3(msz / 1024 + 1, n_above > 0 ? n_above : 1, BH), dim3(256),
+                                         pl.NT * sizeof(float), stream, seg_tot, g_tiles, nodes, dtab, tile_counter,
+                                         pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
+        if (e != cudaSuccess) return e;
         note_launch(stream, "tc_merge");
     }
     return cudaGetLastError();
@@ -1432,17 +1439,19 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
             cudaError_t e =
                 cudaFuncSetAttribute(tc_output_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
-            tc_output_pp_kernel<<<grid, PpCfg::kThreads, smem, stream>>>(
-                tq, tk, tv, tn, tok_cl2, tok_colw, lambda, dtab, static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L,
-                pl.P, pl.node_count, lo, total, tile_counter, err);
+            e = launch_pdl(tc_output_pp_kernel, dim3(grid), dim3(PpCfg::kThreads), smem, stream, tq, tk, tv, tn,
+                           tok_cl2, tok_colw, lambda, dtab, static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L, pl.P,
+                           pl.node_count, lo, total, tile_counter, err);
+            if (e != cudaSuccess) return e;
         } else {
             const int smem = OutCfg<DV>::kBytes;
             cudaError_t e =
                 cudaFuncSetAttribute(tc_output_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
-            tc_output_kernel<DV><<<grid, OutCfg<DV>::kThreads, smem, stream>>>(
-                tq, tk, tv, tn, tok_cl2, tok_colw, lambda, dtab, static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L,
-                pl.P, pl.node_count, lo, total, tile_counter, err);
+            e = launch_pdl(tc_output_kernel<DV>, dim3(grid), dim3(OutCfg<DV>::kThreads), smem, stream, tq, tk, tv,
+                           tn, tok_cl2, tok_colw, lambda, dtab, static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L,
+                           pl.P, pl.node_count, lo, total, tile_counter, err);
+            if (e != cudaSuccess) return e;
         }
         note_launch(stream, "tc_output");
     }

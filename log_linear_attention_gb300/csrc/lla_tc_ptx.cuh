@@ -96,6 +96,13 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
                  "r"(smem_u32(src)), "r"(x), "r"(y)
                  : "memory");
 }
+// Programmatic dependent launch: a kernel launched with launch_pdl() may start while the
+// previous kernel of its stream drains; grid_dep_wait() blocks until that kernel has completed
+// and its writes are visible (a no-op without a prerequisite). grid_dep_launch() lets the next
+// kernel of the stream be launched early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Pull one box of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -332,6 +339,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     });
     return fn;
+}
+
+// Launch with the programmatic-stream-serialization attribute (see grid_dep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 // 2D bf16 row-major [rows, cols] tensor, box = 64 cols x 128 rows, 128-byte swizzle.
