@@ -15,6 +15,7 @@ has) on a bounded sample of the same workload, on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -497,14 +498,12 @@ def gdn_work(cfg: inputs.PrefillConfig) -> dict:
     return dict(flops=flops, bytes=nbytes)
 
 
-def bench_gdn(args, dev, stream, peaks) -> dict:
-    """The log-linear Gated DeltaNet: prefill of the headline-shaped workload (B4 H16 T8192 dk128
-    dv64, unit-norm q/k, beta = sigmoid(N(0,1))) and the decode step of the decode workload."""
+def gdn_device_inputs(cfg: inputs.PrefillConfig, dev, seed: int = 99):
+    """One Gated DeltaNet prefill problem drawn on the device with the config's distributions
+    (unit-norm q/k rows, beta = sigmoid(N(0,1))): q, k, v, log_a, beta, lambda, out."""
     import torch
-    from log_linear_attention_gb300 import binding
-    cfg = inputs.GDN_CONFIGS["gdn-headline"]
     g = torch.Generator(device=dev)
-    g.manual_seed(99)
+    g.manual_seed(seed)
     shp = (cfg.B, cfg.H, cfg.T)
 
     def unit(x):
@@ -517,6 +516,21 @@ def bench_gdn(args, dev, stream, peaks) -> dict:
     bt = torch.sigmoid(torch.randn(shp, device=dev, generator=g))
     lam = torch.nn.functional.softplus(torch.randn(shp + (cfg.L,), device=dev, generator=g))
     out = torch.empty(shp + (cfg.dv,), dtype=torch.bfloat16, device=dev)
+    return q, k, v, la, bt, lam, out
+
+
+def bench_gdn(args, dev, stream, peaks) -> dict:
+    """The log-linear Gated DeltaNet: prefill of the headline-shaped workload (B4 H16 T8192 dk128
+    dv64, unit-norm q/k, beta = sigmoid(N(0,1))) and the decode step of the decode workload."""
+    import torch
+    from log_linear_attention_gb300 import binding
+    cfg = inputs.GDN_CONFIGS["gdn-headline"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(98)
+    q, k, v, la, bt, lam, out = gdn_device_inputs(cfg, dev)
+
+    def unit(x):
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
 
     def step():
         binding.gdn_forward(q, k, v, la, bt, lam, cfg.chunk, out=out)
@@ -639,6 +653,20 @@ def run_lla(args, cfg):
     stream = torch.cuda.current_stream()
     peaks = load_peaks()
 
+    if args.mode == "gdn":
+        # Gated DeltaNet prefill launches only (a short target for profilers)
+        gcfg = inputs.GDN_CONFIGS["gdn-headline"]
+        if args.batch:
+            gcfg = dataclasses.replace(gcfg, B=args.batch)
+        q, k, v, la, bt, lam, gout = gdn_device_inputs(gcfg, dev)
+        gstep = lambda: binding.gdn_forward(q, k, v, la, bt, lam, gcfg.chunk, out=gout)  # noqa: E731
+        for _ in range(max(args.warmup, 3)):
+            gstep()
+        g_ms = cuda_time(gstep, args.steps, stream) / args.steps
+        assert binding.device_error() == 0
+        if rank == 0:
+            print(json.dumps({"mode": "gdn", "workload": f"{gcfg.name} B={gcfg.B}", "ms": g_ms, "steps": args.steps}))
+        return 0
     if args.mode == "decode":
         # decode launches only (a short target for profilers); not the benchmark line
         d_ms_total, dbytes, dsteps = bench_decode(args, dev, stream, rank, ws)
@@ -870,10 +898,18 @@ def main():
     ap.add_argument("--config", default="headline", choices=sorted(inputs.PREFILL_CONFIGS))
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
-    ap.add_argument("--mode", choices=["all", "prefill", "decode", "handoff", "backward", "varlen"], default="all",
-                    help="prefill / decode / handoff / backward / varlen: run only that workload's launches (profiling targets)")
+    ap.add_argument("--mode", choices=["all", "prefill", "decode", "handoff", "backward", "varlen", "gdn"],
+                    default="all",
+                    help="prefill / decode / handoff / backward / varlen / gdn: run only that workload's launches "
+                         "(profiling targets)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling modes only: the config's shapes with this many sequences (a smaller case)")
     args = ap.parse_args()
     cfg = inputs.PREFILL_CONFIGS[args.config]
+    if args.batch:
+        if args.mode == "all":
+            ap.error("--batch applies to the profiling modes only, not to the benchmark line")
+        cfg = dataclasses.replace(cfg, B=args.batch)
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_lla(args, cfg)
