@@ -435,7 +435,8 @@ def bench_varlen(args, dev, stream, rank):
                          f"(total {total}, max {max_T}), dk={dk} dv={dv} bf16",
                 prefill_ms=f_ms, prefill_tokens_per_s=total / (f_ms / 1e3),
                 handoff_ms=h_ms, handoff_tokens_per_s=total / (h_ms / 1e3),
-                padding_overhead=c["n_seq"] * ((max_T + 127) // 128 * 128) / total)
+                layout="packed: each sequence's own 128-token tiles (no padded copy) on the tensor-core path",
+                tile_overhead=float(sum((int(x) + 127) // 128 * 128 for x in lengths)) / total)
 
 
 def bench_decode(args, dev, stream, rank, ws):

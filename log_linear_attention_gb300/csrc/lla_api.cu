@@ -462,8 +462,6 @@ int lla_forward_varlen(const void* q, const void* k, const void* v, const float*
     int st = validate_forward(q, k, v, log_a, lambda, out, n_seq, H, Tpad, dk, dv, chunk, dtype);
     if (st != LLA_OK) return st;
     if ((int64_t)H * total_T * (dk > dv ? dk : dv) > ((int64_t)1 << 40)) return LLA_ERR_UNSUPPORTED;
-    ForwardPlan fp;
-    if (!plan_forward(n_seq, H, Tpad, dk, dv, chunk, dtype, &fp)) return LLA_ERR_UNSUPPORTED;
     const int dev = current_device();
     if (dev < 0) return LLA_ERR_CUDA;
     int* err = error_word(dev);
@@ -471,8 +469,25 @@ int lla_forward_varlen(const void* q, const void* k, const void* v, const float*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaMemPool_t pool = workspace_pool(dev);
     if (!pool) return LLA_ERR_CUDA;
-    const int esz = dtype == LLA_BF16 ? 2 : 4;
     const int L_in = lla_num_levels(max_T), L_pad = lla_num_levels(Tpad);
+    lla::TcPlan tp;
+    if (lla::tc_varlen_supported(dtype, dk, dv) && (int64_t)H * total_T < ((int64_t)1 << 31) &&
+        lla::make_tc_plan(n_seq, H, Tpad, dk, dv, &tp)) {
+        // tensor-core kernels over each sequence's own tiles of the packed layout: no padding
+        const size_t tbytes = lla::tc_varlen_table_bytes(n_seq);
+        char* ws = nullptr;
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), tp.total_bytes + tbytes, pool, s) != cudaSuccess) {
+            cudaGetLastError();
+            return LLA_ERR_NOMEM;
+        }
+        const cudaError_t e = lla::tc_forward_varlen(tp, q, k, v, log_a, lambda, out, cu_seqlens, total_T, max_T,
+                                                     L_in, ws, ws + tp.total_bytes, err, s);
+        const cudaError_t f = cudaFreeAsync(ws, s);
+        return (e == cudaSuccess && f == cudaSuccess) ? LLA_OK : LLA_ERR_CUDA;
+    }
+    ForwardPlan fp;
+    if (!plan_forward(n_seq, H, Tpad, dk, dv, chunk, dtype, &fp)) return LLA_ERR_UNSUPPORTED;
+    const int esz = dtype == LLA_BF16 ? 2 : 4;
     const size_t rows = (size_t)n_seq * H * Tpad;
     auto up = [](size_t x) { return (x + 1023) / 1024 * 1024; };
     const size_t bq = up(rows * dk * esz), bv = up(rows * dv * esz), ba = up(rows * 4), bl = up(rows * L_pad * 4);

@@ -83,6 +83,14 @@ bool tc_supported(int dtype, int dk, int dv, int T);
 bool make_tc_plan(int B, int H, int T, int dk, int dv, TcPlan* plan);
 cudaError_t tc_forward(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
                        const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream);
+// Packed variable-length sequences (bf16, dv = 64, dk in {64, 128}) on the tensor-core kernels:
+// plan = make_tc_plan(n_seq, H, Tpad = max_T rounded up to 128, dk, dv); tensors [H, total_T, .];
+// `table` holds tc_varlen_table_bytes(n_seq) of device scratch (the validated sequence table).
+bool tc_varlen_supported(int dtype, int dk, int dv);
+size_t tc_varlen_table_bytes(int n_seq);
+cudaError_t tc_forward_varlen(const TcPlan& plan, const void* q, const void* k, const void* v, const float* log_a,
+                              const float* lambda, void* out, const int32_t* cu_seqlens, int total_T, int max_T,
+                              int lam_levels, void* workspace, void* table, int* err, cudaStream_t stream);
 // Failure-path test hooks of the dv = 64 output kernel on the current device: the bound
 // on its pipeline waits (limit_cycles <= 0: the default of about 2 s) and a wait that
 // nothing completes (hold != 0).

@@ -50,6 +50,69 @@ namespace {
 
 struct LevelOffsets { int off[32]; };
 
+// Where a head's rows are. Dense layout (seq == nullptr): head bh = b * H + h is rows bh * T ..
+// of every [B*H*T, .] tensor. Packed variable-length sequences: the tensors are [H, total_T, .]
+// and sequence i owns rows seq[i].x .. seq[i].x + seq[i].y - 1 of every head (a validated copy of
+// cu_seqlens); the workspace keeps the dense layout with T = the longest sequence rounded up to
+// a tile, head bh = i * H + h.
+struct SeqMap {
+    const int2* seq;          // per sequence {first row, length}; null: dense
+    const int* tile_prefix;   // [n_seq + 1]: H x (tiles of the sequences before i)
+    int H, n_seq, total_T;
+};
+
+// First input row and length of head bh.
+__device__ __forceinline__ void seq_of(const SeqMap& sm, int bh, int T, int& rowbase, int& len) {
+    if (!sm.seq) {
+        rowbase = bh * T;
+        len = T;
+        return;
+    }
+    const int i = bh / sm.H, h = bh - i * sm.H;
+    const int2 s = sm.seq[i];
+    rowbase = h * sm.total_T + s.x;
+    len = s.y;
+}
+
+// One block: the validated sequence table and the tile prefix of the packed layout. A sequence
+// whose bounds are inconsistent (negative start, decreasing offsets, rows past total_T, longer
+// than max_T) is recorded as bad input and gets length 0 (no tiles, no output rows written).
+__global__ void __launch_bounds__(1024) seq_table_kernel(const int32_t* __restrict__ cu, int2* __restrict__ seq,
+                                                         int* __restrict__ tile_prefix, int n_seq, int H, int total_T,
+                                                         int max_T, int* err) {
+    __shared__ int part[1024];
+    const int tid = threadIdx.x;
+    const int per = (n_seq + 1023) / 1024;
+    const int i0 = tid * per, i1 = min(n_seq, i0 + per);
+    int sum = 0;
+    for (int i = i0; i < i1; i++) {
+        const int c0 = cu[i], c1 = cu[i + 1];
+        const bool ok = c0 >= 0 && c1 >= c0 && c1 <= total_T && c1 - c0 <= max_T;
+        if (!ok) record_error(err, kDevBadInput);
+        const int len = ok ? c1 - c0 : 0;
+        seq[i] = make_int2(ok ? c0 : 0, len);
+        sum += (len + kTile - 1) / kTile;
+    }
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int t = 0; t < 1024; t++) {
+            const int x = part[t];
+            part[t] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    int run = part[tid];
+    for (int i = i0; i < i1; i++) {
+        tile_prefix[i] = H * run;
+        run += (seq[i].y + kTile - 1) / kTile;
+    }
+    if (i1 == n_seq && i0 < i1) tile_prefix[n_seq] = H * run;
+    if (n_seq == 0 && tid == 0) tile_prefix[0] = 0;
+}
+
 // ------------------------------------------------------------------ tc_nodes
 
 template <int DV>
@@ -73,7 +136,7 @@ __global__ void __launch_bounds__(256, 2)
     tc_nodes_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
                     float* __restrict__ seg_tot, float* __restrict__ tok_cl2, float* __restrict__ tok_colw, int T,
-                    int NT, int node_count, const __grid_constant__ LevelOffsets lo, int* err) {
+                    int NT, int node_count, const __grid_constant__ LevelOffsets lo, const SeqMap sm, int* err) {
     constexpr int DH = DV / 2;  // columns per thread
     constexpr int kSegTiles = 1 << Q;
     using S = NodesSmem<DV>;
@@ -90,7 +153,11 @@ __global__ void __launch_bounds__(256, 2)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, bh = blockIdx.y;
     const int tile0 = seg * kSegTiles;
-    const int ntiles = min(kSegTiles, NT - tile0);
+    int rowbase, len;
+    seq_of(sm, bh, T, rowbase, len);
+    const int NTi = (len + kTile - 1) / kTile;  // this head's tiles (NT in the dense layout)
+    const int ntiles = min(kSegTiles, NTi - tile0);
+    if (ntiles <= 0) return;  // packed layout: past this sequence's last tile
     const int row = tid & 127;         // dk row in the epilogue, token row while scaling V
     const int half = tid >> 7;         // which half of the dv columns / of the V row
     const int quad = warp & 3;         // TMEM lane quadrant of this warp
@@ -116,7 +183,7 @@ __global__ void __launch_bounds__(256, 2)
     auto issue_tile = [&](int u) {
         const int s = u & 1;
         uint8_t* st = stage_ptr(s);
-        const int r0 = bh * T + (tile0 + u) * kTile;
+        const int r0 = rowbase + (tile0 + u) * kTile;
         mbar_expect_tx(&bar_full[s], kTxBytes);
         tma_load_2d(st, &tm_k, &bar_full[s], 0, r0);
         tma_load_2d(st + kPanelBytes, &tm_k, &bar_full[s], 64, r0);
@@ -135,8 +202,8 @@ __global__ void __launch_bounds__(256, 2)
     float la[kSegTiles];
 #pragma unroll
     for (int u = 0; u < kSegTiles; u++) {
-        const size_t tok = static_cast<size_t>(bh) * T + static_cast<size_t>(tile0 + u) * kTile + row;
-        la[u] = (half == 0 && u < ntiles) ? log_a[tok] : 0.f;
+        const int pos = (tile0 + u) * kTile + row;
+        la[u] = (half == 0 && u < ntiles && pos < len) ? log_a[static_cast<size_t>(rowbase) + pos] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kSegTiles; u++) {
@@ -253,7 +320,7 @@ __global__ void __launch_bounds__(256, 2)
             for (int c = 0; c < DH / 4; c++) d4[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         };
         // level 0: the tile itself
-        if ((tile & 1) == 0 && tile + 1 < NT) store_node(0, tile, sv);
+        if ((tile & 1) == 0 && tile + 1 < NTi) store_node(0, tile, sv);
         if (Q == 0 && ntiles == kSegTiles) store_seg(sv);
 #pragma unroll
         for (int l = 1; l <= Q; l++) {
@@ -264,7 +331,7 @@ __global__ void __launch_bounds__(256, 2)
             for (int e = 0; e < DH; e++) acc[l - 1][e] = first ? sv[e] : fmaf(acc[l - 1][e], ge, sv[e]);
             if (closes) {
                 const int m = tile >> l;
-                if ((m & 1) == 0 && ((m + 1) << l) < NT) store_node(l, m, acc[l - 1]);
+                if ((m & 1) == 0 && ((m + 1) << l) < NTi) store_node(l, m, acc[l - 1]);
                 if (l == Q && ntiles == kSegTiles) store_seg(acc[l - 1]);
             }
         }
@@ -299,19 +366,23 @@ __global__ void __launch_bounds__(256, 2)
 __global__ void __launch_bounds__(256)
     tc_merge_kernel(const float* __restrict__ seg_tot, const float* __restrict__ g_tiles,
                     __nv_bfloat16* __restrict__ nodes, float* __restrict__ dtab, int* __restrict__ tile_counter,
-                    int NT, int q, int P, int nseg, int node_count, int msz, const __grid_constant__ LevelOffsets lo) {
+                    int NT, int q, int P, int nseg, int node_count, int msz, const __grid_constant__ LevelOffsets lo,
+                    int T, const SeqMap sm) {
     __shared__ float wsg[1024];      // per-segment totals, then weights, of this block's node
     extern __shared__ float g_sh[];  // the head's tile totals (decay-table block only)
     grid_dep_wait();                 // the node kernel's totals (launched early, see launch_pdl)
     grid_dep_launch();
     const int bh = blockIdx.z;
     const float* gh = g_tiles + static_cast<size_t>(bh) * NT;
+    int rowbase, len;
+    seq_of(sm, bh, T, rowbase, len);
+    const int NTi = (len + kTile - 1) / kTile;  // this head's tiles (NT in the dense layout)
     if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *tile_counter = 0;
     if (blockIdx.x == 0) {
         if (blockIdx.y != 0) return;
-        for (int i = threadIdx.x; i < NT; i += blockDim.x) g_sh[i] = gh[i];
+        for (int i = threadIdx.x; i < NTi; i += blockDim.x) g_sh[i] = gh[i];
         __syncthreads();
-        for (int j = threadIdx.x; j < NT; j += blockDim.x) {
+        for (int j = threadIdx.x; j < NTi; j += blockDim.x) {
             float d[16];
 #pragma unroll
             for (int p = 0; p < 16; p++) d[p] = 0.f;
@@ -339,7 +410,7 @@ __global__ void __launch_bounds__(256)
         if (y < cnt) { m = 2 * y; break; }
         y -= cnt;
     }
-    if (m < 0) return;
+    if (m < 0 || ((m + 1) << p) >= NTi) return;  // no such node, or no tile of this head reads it
     const int nsg = 1 << (p - q);      // segments in the block
     const int sg0 = m * nsg;           // its first segment
     const int seg_tiles = 1 << q;
@@ -971,7 +1042,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                         const float* __restrict__ lambda, const float* __restrict__ dtab,
                         __nv_bfloat16* __restrict__ out, int T, int NT, int L, int P, int node_count,
                         const __grid_constant__ LevelOffsets lo, int total_tiles, int* __restrict__ tile_counter,
-                        int* err) {
+                        const SeqMap sm, int in_rows, int* err) {
     constexpr int DV = 64;
     constexpr int DH = DV / 2;  // result columns per epilogue warp
     using C = PpCfg;
@@ -1011,10 +1082,25 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
     const uint32_t tmem = tmem_base_sh;
     grid_dep_wait();  // the node and merge kernels' outputs (launched early, see launch_pdl)
 
-    // head-major; within a head from the last tile down (most Fenwick levels first)
+    // head-major; within a head from the last tile down (most Fenwick levels first). Packed
+    // sequences: sequence-major, then head; the sequence is found in the tile prefix.
+    if (sm.seq) total_tiles = sm.tile_prefix[sm.n_seq];
     auto tile_of = [&](int idx, int& bh, int& j) {
-        bh = idx / NT;
-        j = NT - 1 - (idx - bh * NT);
+        if (!sm.seq) {
+            bh = idx / NT;
+            j = NT - 1 - (idx - bh * NT);
+            return;
+        }
+        int lo_ = 0, hi_ = sm.n_seq - 1;  // the sequence i with prefix[i] <= idx < prefix[i + 1]
+        while (lo_ < hi_) {
+            const int mid = (lo_ + hi_ + 1) >> 1;
+            if (sm.tile_prefix[mid] <= idx) lo_ = mid; else hi_ = mid - 1;
+        }
+        const int p0 = sm.tile_prefix[lo_];
+        const int nti = (sm.tile_prefix[lo_ + 1] - p0) / sm.H;
+        const int r = idx - p0, h = r / nti;
+        bh = lo_ * sm.H + h;
+        j = nti - 1 - (r - h * nti);
     };
     const long long lim = tc_pipe_wait_limit;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -1041,19 +1127,21 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             // a claimed tile's inputs are pulled into L2 at once; the stage copies come later
             auto claimed = [&](int idx) -> int {
                 if (idx >= total_tiles) return -1;
-                int pbh, pj;
+                int pbh, pj, prb, plen;
                 tile_of(idx, pbh, pj);
-                const int r0 = pbh * T + pj * kTile;
+                seq_of(sm, pbh, T, prb, plen);
+                const int r0 = prb + pj * kTile;
                 tma_prefetch_l2(&tm_q, 0, r0);
                 tma_prefetch_l2(&tm_q, 64, r0);
                 tma_prefetch_l2(&tm_k, 0, r0);
                 tma_prefetch_l2(&tm_k, 64, r0);
                 tma_prefetch_l2(&tm_v, 0, r0);
-                prefetch_l2(tok_cl2 + r0, 512);
+                prefetch_l2(tok_cl2 + pbh * T + pj * kTile, 512);
+                // this tile's lambda rows, within the tensor (a packed tile may end past it)
+                const int r1 = min(r0 + kTile, in_rows);
                 const uintptr_t lb = reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r0) * L) & ~uintptr_t(15);
-                const uintptr_t le = (reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r0 + kTile) * L) + 15) &
-                                     ~uintptr_t(15);
-                prefetch_l2(reinterpret_cast<const void*>(lb), static_cast<uint32_t>(le - lb));
+                const uintptr_t le = reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r1) * L) & ~uintptr_t(15);
+                if (le > lb) prefetch_l2(reinterpret_cast<const void*>(lb), static_cast<uint32_t>(le - lb));
                 return idx;
             };
             uint8_t* st = smem + g * C::kStageBytes;
@@ -1068,16 +1156,17 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                     mbar_arrive(&in_full[g]);  // end marker
                     break;
                 }
-                int bh, j;
+                int bh, j, rb, len;
                 tile_of(idx, bh, j);
-                const int row0 = bh * T + j * kTile;
+                seq_of(sm, bh, T, rb, len);
+                const int row0 = rb + j * kTile;  // input rows
                 mbar_expect_tx(&in_full[g], C::kQkvBytes + C::kScalarTx);
                 tma_load_2d(st + C::kQ, &tm_q, &in_full[g], 0, row0);
                 tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[g], 64, row0);
                 tma_load_2d(st + C::kK, &tm_k, &in_full[g], 0, row0);
                 tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &in_full[g], 64, row0);
                 tma_load_2d(st + C::kV, &tm_v, &in_full[g], 0, row0);
-                bulk_load(smem + C::kCl2Base + g * 512, tok_cl2 + row0, 512, &in_full[g]);
+                bulk_load(smem + C::kCl2Base + g * 512, tok_cl2 + bh * T + j * kTile, 512, &in_full[g]);
                 n_in = c + 1;
                 // claim the group's next tile; its index is used once this tile's node copies are issued
                 const int next_idx = atomicAdd(tile_counter, 1);
@@ -1141,7 +1230,9 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 if (!wait(&in_full[g], c & 1)) break;
                 const int idx = tile_id_sh[g];
                 if (idx < 0) break;
-                const int n_lv = __popc(static_cast<unsigned>(NT - 1 - idx % NT));
+                int tbh, tj;
+                tile_of(idx, tbh, tj);
+                const int n_lv = __popc(static_cast<unsigned>(tj));
                 const int R = C::rounds(n_lv);
                 // the previous tile of this group is read back: its TMEM columns are free
                 if (c > 0 && !wait(&lv_free[g], (lvf++) & 1)) break;
@@ -1197,9 +1288,12 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             if (!ewait(&in_full[g], c & 1)) break;
             const int idx = tile_id_sh[g];
             if (idx < 0) break;
-            int bh, j;
+            int bh, j, rb, len;
             tile_of(idx, bh, j);
-            const int row0 = bh * T + j * kTile;
+            seq_of(sm, bh, T, rb, len);
+            const int row0 = rb + j * kTile;         // input rows
+            const int live = len - j * kTile;        // rows of this tile inside the sequence (>= 1)
+            const int tr = t < live ? t : live - 1;  // lambda row read for this lane
             const float cl2_t = cl2[t];
             // this row's lambda (levels 0..7 for P; 8 + p for the level reads) and the tile's
             // decay-table row, loaded while S is computed; rr[p] = lambda_t^(8+p) exp(cl_t + D_p)
@@ -1207,7 +1301,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             float lam_in[8];
             float rr[16];
             {
-                const float* lam_row = lambda + static_cast<size_t>(row0 + t) * L;
+                const float* lam_row = lambda + static_cast<size_t>(row0 + tr) * L;
 #pragma unroll
                 for (int l = 0; l < 8; l++) lam_in[l] = l < L ? lam_row[l] : 0.f;
                 const float4* drow = reinterpret_cast<const float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
@@ -1325,12 +1419,15 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 if (lane == 0) mbar_arrive(&lv_free[g]);
             }
             if (!ok) break;
-            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV + half * DH);
+            if (t < live) {  // a packed sequence's last tile ends inside the tile
+                uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV + half * DH);
 #pragma unroll
-            for (int c8 = 0; c8 < DH / 8; c8++)
-                dst[c8] = make_uint4(pack_bf16(acc[8 * c8], acc[8 * c8 + 1]), pack_bf16(acc[8 * c8 + 2], acc[8 * c8 + 3]),
-                                     pack_bf16(acc[8 * c8 + 4], acc[8 * c8 + 5]),
-                                     pack_bf16(acc[8 * c8 + 6], acc[8 * c8 + 7]));
+                for (int c8 = 0; c8 < DH / 8; c8++)
+                    dst[c8] = make_uint4(pack_bf16(acc[8 * c8], acc[8 * c8 + 1]),
+                                         pack_bf16(acc[8 * c8 + 2], acc[8 * c8 + 3]),
+                                         pack_bf16(acc[8 * c8 + 4], acc[8 * c8 + 5]),
+                                         pack_bf16(acc[8 * c8 + 6], acc[8 * c8 + 7]));
+            }
         }
     }
 
@@ -1357,7 +1454,7 @@ int choose_q(int BH, int NT, int dv) {
 // decay tables and the per-tile level decay table.
 template <int DV>
 cudaError_t tc_node_stage(const TcPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv, const float* log_a,
-                          void* workspace, int* err, cudaStream_t stream) {
+                          void* workspace, int* err, cudaStream_t stream, const SeqMap& sm) {
     const int BH = pl.B * pl.H;
     const int qlog = pl.q;
     const int seg_tiles = 1 << qlog;
@@ -1378,7 +1475,7 @@ cudaError_t tc_node_stage(const TcPlan& pl, const CUtensorMap& tk, const CUtenso
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
             kern<<<dim3(nseg, BH), 256, smem, stream>>>(tk, tv, log_a, g_tiles, nodes, seg_tot, tok_cl2, tok_colw, pl.T,
-                                                        pl.NT, pl.node_count, lo, err);
+                                                        pl.NT, pl.node_count, lo, sm, err);
             return cudaSuccess;
         };
         cudaError_t e;
@@ -1396,7 +1493,7 @@ cudaError_t tc_node_stage(const TcPlan& pl, const CUtensorMap& tk, const CUtenso
         for (int p = qlog + 1; p < pl.P; p++) n_above += (((pl.NT - 1) >> p) + 1) / 2;
         const cudaError_t e = launch_pdl(tc_merge_kernel, dim3(msz / 1024 + 1, n_above > 0 ? n_above : 1, BH), dim3(256),
                                          pl.NT * sizeof(float), stream, seg_tot, g_tiles, nodes, dtab, tile_counter,
-                                         pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo);
+                                         pl.NT, qlog, pl.P, nseg, pl.node_count, msz, lo, pl.T, sm);
         if (e != cudaSuccess) return e;
         note_launch(stream, "tc_merge");
     }
@@ -1406,7 +1503,7 @@ cudaError_t tc_node_stage(const TcPlan& pl, const CUtensorMap& tk, const CUtenso
 template <int DV>
 cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
                           const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream,
-                          bool nodes_only = false) {
+                          bool nodes_only = false, SeqMap sm = SeqMap{nullptr, nullptr, 1, 0, 0}, int lam_levels = 0) {
     const int BH = pl.B * pl.H;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     __nv_bfloat16* nodes = reinterpret_cast<__nv_bfloat16*>(ws + pl.g_bytes);
@@ -1416,7 +1513,9 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
     int* tile_counter = reinterpret_cast<int*>(ws + pl.total_bytes - pl.ctr_bytes);
     LevelOffsets lo;
     for (int p = 0; p < 32; p++) lo.off[p] = pl.level_off[p];
-    const uint64_t rows = static_cast<uint64_t>(BH) * pl.T;
+    if (!sm.seq) sm = SeqMap{nullptr, nullptr, pl.H, pl.B, 0};
+    // input rows: [B*H*T] dense, [H * total_T] packed
+    const uint64_t rows = sm.seq ? static_cast<uint64_t>(pl.H) * sm.total_T : static_cast<uint64_t>(BH) * pl.T;
 
     CUtensorMap tq, tk, tv, tn;
     if (!make_map(&tq, q, rows, pl.dk) || !make_map(&tk, k, rows, pl.dk) || !make_map(&tv, v, rows, DV))
@@ -1427,11 +1526,12 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
     if (!have_nodes) tn = tv;  // never read when no tile has an earlier tile
 
     {
-        cudaError_t e = tc_node_stage<DV>(pl, tk, tv, log_a, workspace, err, stream);
+        cudaError_t e = tc_node_stage<DV>(pl, tk, tv, log_a, workspace, err, stream, sm);
         if (e != cudaSuccess || nodes_only) return e;
     }
     {
-        const int L = bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
+        // lambda row length: num_levels(T) dense; packed, that of the longest sequence (given)
+        const int L = lam_levels > 0 ? lam_levels : bitlength(static_cast<int64_t>(pl.T) - 1) + 1;
         const int total = BH * pl.NT;
         const int grid = total < pl.num_sms ? total : pl.num_sms;
         if constexpr (DV == 64) {
@@ -1441,7 +1541,7 @@ cudaError_t tc_forward_dv(const TcPlan& pl, const void* q, const void* k, const 
             if (e != cudaSuccess) return e;
             e = launch_pdl(tc_output_pp_kernel, dim3(grid), dim3(PpCfg::kThreads), smem, stream, tq, tk, tv, tn,
                            tok_cl2, tok_colw, lambda, dtab, static_cast<__nv_bfloat16*>(out), pl.T, pl.NT, L, pl.P,
-                           pl.node_count, lo, total, tile_counter, err);
+                           pl.node_count, lo, total, tile_counter, sm, static_cast<int>(rows), err);
             if (e != cudaSuccess) return e;
         } else {
             const int smem = OutCfg<DV>::kBytes;
@@ -1514,6 +1614,26 @@ cudaError_t tc_forward(const TcPlan& pl, const void* q, const void* k, const voi
                        const float* lambda, void* out, void* workspace, int* err, cudaStream_t stream) {
     if (pl.dv == 64) return tc_forward_dv<64>(pl, q, k, v, log_a, lambda, out, workspace, err, stream);
     return tc_forward_dv<128>(pl, q, k, v, log_a, lambda, out, workspace, err, stream);
+}
+
+bool tc_varlen_supported(int dtype, int dk, int dv) { return dtype == 0 && (dk == 64 || dk == kDk) && dv == 64; }
+
+size_t tc_varlen_table_bytes(int n_seq) {
+    return (static_cast<size_t>(n_seq) * sizeof(int2) + (n_seq + 1) * sizeof(int) + 255) / 256 * 256;
+}
+
+cudaError_t tc_forward_varlen(const TcPlan& pl, const void* q, const void* k, const void* v, const float* log_a,
+                              const float* lambda, void* out, const int32_t* cu_seqlens, int total_T, int max_T,
+                              int lam_levels, void* workspace, void* table, int* err, cudaStream_t stream) {
+    if (pl.dv != 64) return cudaErrorInvalidValue;
+    int2* seq = static_cast<int2*>(table);
+    int* prefix = reinterpret_cast<int*>(seq + pl.B);
+    seq_table_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, seq, prefix, pl.B, pl.H, total_T, max_T, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    note_launch(stream, "seq_table");
+    return tc_forward_dv<64>(pl, q, k, v, log_a, lambda, out, workspace, err, stream, false,
+                             SeqMap{seq, prefix, pl.H, pl.B, total_T}, lam_levels);
 }
 
 cudaError_t tc_nodes_only(const TcPlan& pl, const void* k, const void* v, const float* log_a, void* workspace,

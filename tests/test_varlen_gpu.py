@@ -75,6 +75,39 @@ def test_forward_varlen_matches_each_sequence(lengths, H, dk, dv, chunk, dtype):
         assert rel_err_per_head(got[:, cu[b]:cu[b + 1]], ref) <= tol, b
 
 
+@pytest.mark.parametrize("lengths,H,dk", [([128, 1, 383, 2048, 129], 3, 64), ([3000, 130, 64, 255], 2, 128)])
+def test_forward_varlen_tensor_core_ragged(lengths, H, dk):
+    """bf16 with dv = 64 walks each sequence's own tiles of the packed layout on the tensor-core
+    kernels (no padded copy): ragged last tiles, sequences shorter than a tile, dk = 64 and 128."""
+    from log_linear_attention_gb300 import binding
+    seqs, packed, cu, max_T = packed_problem(lengths, H, dk, 64, "bf16", seed=3 * len(lengths) + dk)
+    q, k, v, la, lam = to_dev(packed, seqs, "bf16")
+    out = binding.forward_varlen(q, k, v, la, lam, torch.from_numpy(cu).cuda(), max_T, 64)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    got = out.float().cpu().numpy()
+    for b, x in enumerate(seqs):
+        fn = oracle.explicit if lengths[b] <= 512 else oracle.recurrent
+        ref = fn(x.q, x.k, x.v, x.log_a, x.lam)[0]
+        assert rel_err_per_head(got[:, cu[b]:cu[b + 1]], ref) <= 2e-2, b
+
+
+def test_forward_varlen_empty_sequences():
+    """Zero-length sequences in cu_seqlens own no rows and no tiles; the others are unaffected."""
+    from log_linear_attention_gb300 import binding
+    lengths = [300, 129]
+    seqs, packed, cu2, max_T = packed_problem(lengths, 2, 128, 64, "bf16", seed=41)
+    q, k, v, la, lam = to_dev(packed, seqs, "bf16")
+    cu = np.array([0, 0, 300, 300, 429, 429], dtype=np.int32)
+    out = binding.forward_varlen(q, k, v, la, lam, torch.from_numpy(cu).cuda(), max_T, 64)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    got = out.float().cpu().numpy()
+    for b, x in zip((1, 3), seqs):
+        ref = oracle.explicit(x.q, x.k, x.v, x.log_a, x.lam)[0]
+        assert rel_err_per_head(got[:, cu[b]:cu[b + 1]], ref) <= 2e-2, b
+
+
 def held_levels(pos, Lmax):
     return [0] + [l for l in range(1, Lmax) if (pos >> (l - 1)) & 1]
 
@@ -165,3 +198,24 @@ def test_varlen_bad_lengths_are_reported():
     binding.forward_varlen(q, q, q, la, lam, cu, 64, 16)
     assert binding.device_error() == binding.LLA_ERR_DEVICE
     assert binding.device_error() == 0
+
+
+def test_varlen_bad_lengths_tensor_core_path():
+    """The same check on the tensor-core walk (bf16, dk = 128, dv = 64): the over-long sequence is
+    skipped (its rows untouched), the error is reported, the valid sequence is correct."""
+    from log_linear_attention_gb300 import binding
+    seqs, packed, _, max_T = packed_problem([200], 1, 128, 64, "bf16", seed=77)
+    q, k, v, la, lam = to_dev(packed, seqs, "bf16")
+    # rows 0..199 hold sequence 0; sequence 1 claims rows 200..455, longer than max_T = 200
+    pad = lambda x: torch.cat([x, torch.zeros((1, 256) + tuple(x.shape[2:]), dtype=x.dtype, device="cuda")], 1)  # noqa: E731
+    q, k, v, la, lam = (pad(x) for x in (q, k, v, la, lam))
+    out = torch.full((1, 456, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 200, 456, 456], dtype=torch.int32, device="cuda")
+    binding.forward_varlen(q, k, v, la, lam, cu, max_T, 64, out=out)
+    torch.cuda.synchronize()
+    assert binding.device_error() == binding.LLA_ERR_DEVICE
+    assert binding.device_error() == 0
+    assert torch.all(out[:, 200:] == 7.0)
+    x = seqs[0]
+    ref = oracle.explicit(x.q, x.k, x.v, x.log_a, x.lam)[0]
+    assert rel_err_per_head(out[:, :200].float().cpu().numpy(), ref) <= 2e-2
