@@ -240,10 +240,14 @@ int lla_backward(const void* q, const void* k, const void* v, const float* log_a
  * lla_forward_varlen: the prefill of every sequence.
  *   q, k [H,total_T,dk], v [H,total_T,dv] (dtype); log_a [H,total_T] fp32;
  *   lambda [H,total_T,L] fp32 with L = lla_num_levels(max_T); out [H,total_T,dv].
- *   The sequences are copied into a zero-padded [n_seq, H, Tpad] layout
- *   (Tpad = max_T rounded up to 128) in pool workspace, run through the dense
- *   prefill kernels and copied back; rows past a sequence's end cannot reach
- *   its causal outputs. chunk as in lla_forward.
+ *   bf16 with dv = 64 and dk in {64, 128}: the tensor-core prefill kernels walk
+ *   every sequence's own 128-token tiles of the packed tensors (a sequence's
+ *   last tile may end inside it; its rows past the end are neither read into
+ *   the sequence's outputs nor written). Other shapes: the sequences are copied
+ *   into a zero-padded [n_seq, H, Tpad] layout (Tpad = max_T rounded up to
+ *   128) in pool workspace, run through the dense prefill kernels and copied
+ *   back. Requires H * total_T < 2^31 for the tensor-core walk. chunk as in
+ *   lla_forward.
  *
  * lla_prefill_state_varlen: the decode state set after every sequence, as
  * lla_prefill_state: fenwick_states [n_seq, H, Lmax, dk, dv] fp32 with
