@@ -192,8 +192,10 @@ int lla_decode_step(const void* q, const void* k, const void* v, const float* lo
  *          Slots empty at T-1 are left untouched. Needs Lmax >= bitlength(T-1) + 1.
  *   dk, dv 1..128.
  * Takes T fp32 values per (b, h) of scratch from the library's stream-ordered pool.
- * Bucket pieces are added with fp32 atomics, so the summation order (and the last
- * bits of the result) may vary between runs.
+ * Tensor-core path (bf16, dk = 128): every held slot is written exactly once, its
+ * pieces summed in a fixed order, so repeated calls give identical bits. The
+ * CUDA-core path adds bucket pieces of at most 512 keys with fp32 atomics, so for
+ * buckets of more than 1024 keys the last bits may vary between runs.
  */
 int lla_prefill_state(const void* k, const void* v, const float* log_a, float* fenwick_states, int B, int H, int T,
                       int dk, int dv, int Lmax, void* stream, int dtype);

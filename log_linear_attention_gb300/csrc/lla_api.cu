@@ -404,7 +404,7 @@ int lla_prefill_state(const void* k, const void* v, const float* log_a, float* f
     if (dev < 0) return LLA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool tc = lla::tc_state_supported(dtype, dk, dv, B, H, T);
-    const size_t bytes = tc ? lla::tc_state_workspace_bytes(B, H, T) : (size_t)B * H * T * sizeof(float);
+    const size_t bytes = tc ? lla::tc_state_workspace_bytes(B, H, T, dv) : (size_t)B * H * T * sizeof(float);
     int* err = error_word(dev);
     if (!err) return LLA_ERR_CUDA;
     cudaMemPool_t pool = workspace_pool(dev);
@@ -541,7 +541,7 @@ int lla_prefill_state_varlen(const void* k, const void* v, const float* log_a, c
     cudaMemPool_t pool = workspace_pool(dev);
     if (!pool) return LLA_ERR_CUDA;
     const bool tc = lla::tc_state_supported_packed(dtype, dk, dv, n_seq, H, total_T, max_T);
-    const size_t bytes = tc ? lla::tc_state_workspace_bytes(n_seq, H, max_T) : (size_t)H * total_T * sizeof(float);
+    const size_t bytes = tc ? lla::tc_state_workspace_bytes(n_seq, H, max_T, dv) : (size_t)H * total_T * sizeof(float);
     void* ws = nullptr;
     if (cudaMallocFromPoolAsync(&ws, bytes, pool, s) != cudaSuccess) {
         cudaGetLastError();

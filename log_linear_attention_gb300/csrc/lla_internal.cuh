@@ -104,7 +104,7 @@ cudaError_t tc_nodes_only(const TcPlan& plan, const void* k, const void* v, cons
 // has cu[b+1] - cu[b] <= T rows starting at row h * total + cu[b].
 bool tc_state_supported(int dtype, int dk, int dv, int B, int H, int T);
 bool tc_state_supported_packed(int dtype, int dk, int dv, int n_seq, int H, int total, int max_T);
-size_t tc_state_workspace_bytes(int B, int H, int T);
+size_t tc_state_workspace_bytes(int B, int H, int T, int dv);
 cudaError_t tc_prefill_state(const void* k, const void* v, const float* log_a, float* states, int B, int H, int T,
                              int dv, int Lmax, void* workspace, int* err, cudaStream_t stream,
                              const int32_t* cu = nullptr, int total = 0);

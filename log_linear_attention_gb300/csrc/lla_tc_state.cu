@@ -22,8 +22,9 @@
 //   state_offsets     : each sequence's first item in the flattened tile list
 //                       (sequences may have different lengths: packed input).
 //   state_prep        : per head, tail_u = sum of log_a from the end of tile u
-//                       to pos (reverse scan, newest first); other blocks
-//                       zero the slots held at pos.
+//                       to pos (reverse scan, newest first). The held slots need
+//                       no zeroing: each has at least one tile and is written
+//                       exactly once (by tc_state or state_fixup).
 //   tc_state          : persistent; each CTA takes an equal share of the
 //                       flattened (head, tile) list. Per tile,
 //                       w_s = exp(tail_u + decay from s to the tile end), and
@@ -32,8 +33,12 @@
 //                       (N = 2 dv: both parts side by side) accumulates
 //                       K^T [hi | lo] in TMEM, and the two halves are summed
 //                       when the accumulator is drained. A run of tiles of one
-//                       slot ends with the accumulator added (fp32 vector
-//                       atomics) into the slot.
+//                       slot that lies within one CTA's share is stored into the
+//                       slot; a run that a share boundary cuts leaves its partial
+//                       sum in a per-CTA piece buffer.
+//   state_fixup       : every cut run's pieces summed in CTA order into its slot,
+//                       so each slot has exactly one writer and one summation
+//                       order: the result does not depend on the schedule.
 // Every mbarrier wait is bounded; on overrun the kernel records LLA_ERR_TIMEOUT
 // in the device error word, lets its own copies and MMAs land and returns.
 #include "lla_tc_ptx.cuh"
@@ -165,7 +170,6 @@ __device__ __forceinline__ float block_excl_scan256(float x, float* warp_tot) {
 }
 
 // Slot l is held at position pos: level 0 always, level l >= 1 when bit l - 1 of pos is set.
-__device__ __forceinline__ bool slot_held(int pos, int l) { return l == 0 || (l - 1 < 31 && ((pos >> (l - 1)) & 1)); }
 
 // grid (BH, 1 + Lmax), 256 threads, dynamic shared memory: max Pt floats. Block y = 0
 // scans the sequence's tile totals into tail[item_off[bh] + u]; block y = 1 + l zeroes
@@ -181,13 +185,6 @@ __global__ void __launch_bounds__(kPrepThreads)
     if (si.len == 0) return;  // an empty sequence holds no slot
     const int pos = si.pos, Pt = si.Pt;
     const size_t off = first_item(sq, bh);
-    if (blockIdx.y > 0) {
-        const int l = blockIdx.y - 1;
-        if (!slot_held(pos, l)) return;
-        float4* st4 = reinterpret_cast<float4*>(states + (static_cast<size_t>(bh) * Lmax + l) * msz);
-        for (int e = tid; e < msz / 4; e += kPrepThreads) st4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        return;
-    }
     const int base = Pt * kTile;     // first token of the tile of pos
     const int n = pos - base + 1;    // its tokens, 1..128
     const float* a = log_a + static_cast<size_t>(si.base);
@@ -245,7 +242,8 @@ template <int DV>
 __global__ void __launch_bounds__(512, 1)
     tc_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, const float* __restrict__ tail, float* __restrict__ states,
-                    StateSeqs sq, int BH, int Lmax, int* err) {
+                    StateSeqs sq, int BH, int Lmax, float* __restrict__ pieces, int* __restrict__ piece_slot,
+                    int* __restrict__ piece_flags, int* err) {
     using C = StateCfg<DV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -254,6 +252,7 @@ __global__ void __launch_bounds__(512, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int fail_sh;
 
+    grid_dep_wait();  // the item offsets and tails (launched early, see launch_pdl)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int total = first_item(sq, BH);
     const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * total / gridDim.x);
@@ -273,6 +272,10 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(&drain_bar, 1);
         fence_mbar_init();
         fail_sh = 0;
+        // this share's pieces: none yet (bit 2 marks a share without items)
+        piece_slot[2 * blockIdx.x] = piece_slot[2 * blockIdx.x + 1] = -1;
+        piece_flags[2 * blockIdx.x] = t0 == t1 ? 4 : 0;
+        piece_flags[2 * blockIdx.x + 1] = 0;
     }
     if (warp == 1) tmem_alloc(&tmem_base_sh, C::kTmemCols);
     tc_fence_before();
@@ -515,6 +518,12 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         int run = 0;
         Cursor c = cursor_at(t0);
+        // whether this share's first run continues the previous share's last run
+        bool cut_start = false;
+        if (t0 > 0 && t0 < t1) {
+            const Cursor pc = cursor_at(t0 - 1);
+            cut_start = pc.bh == c.bh && pc.lvl == c.lvl;
+        }
         for (int f = t0; f < t1; f++) {
             const Cursor nc = step(c, f);
             const Cursor cur = c;
@@ -528,7 +537,20 @@ __global__ void __launch_bounds__(512, 1)
             }
             tc_fence_after();
             const int bh = cur.bh, l = cur.lvl;
-            float4* dst = reinterpret_cast<float4*>(states + ((static_cast<size_t>(bh) * Lmax + l) * kDk + d) * DV);
+            // a run held whole by this share is the slot's only writer; a cut one leaves a piece
+            const bool cs = run == 0 && cut_start;
+            const bool ce = f + 1 == t1 && t1 < total && nc.bh == cur.bh && nc.lvl == cur.lvl;
+            float4* dst;
+            if (!cs && !ce) {
+                dst = reinterpret_cast<float4*>(states + ((static_cast<size_t>(bh) * Lmax + l) * kDk + d) * DV);
+            } else {
+                const int kind = cs ? 0 : 1;
+                dst = reinterpret_cast<float4*>(pieces + (static_cast<size_t>(2 * blockIdx.x + kind) * kDk + d) * DV);
+                if (warp == 12 && lane == 0) {
+                    piece_slot[2 * blockIdx.x + kind] = bh * Lmax + l;
+                    piece_flags[2 * blockIdx.x + kind] = (cs ? 1 : 0) | (ce ? 2 : 0);
+                }
+            }
 #pragma unroll
             for (int c0 = 0; c0 < DV; c0 += 32) {
                 float x[32], y[32];
@@ -536,8 +558,8 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_ld32(tmem + lane_base + buf * C::kAccCols + DV + c0, y);
 #pragma unroll
                 for (int j = 0; j < 8; j++)
-                    atomicAdd(dst + c0 / 4 + j, make_float4(x[4 * j] + y[4 * j], x[4 * j + 1] + y[4 * j + 1],
-                                                            x[4 * j + 2] + y[4 * j + 2], x[4 * j + 3] + y[4 * j + 3]));
+                    dst[c0 / 4 + j] = make_float4(x[4 * j] + y[4 * j], x[4 * j + 1] + y[4 * j + 1],
+                                                  x[4 * j + 2] + y[4 * j + 2], x[4 * j + 3] + y[4 * j + 3]);
             }
             tc_fence_before();
             __syncwarp();
@@ -557,6 +579,52 @@ __global__ void __launch_bounds__(512, 1)
     if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// One block per tc_state share b: if b's last run continues into the next share and began in b
+// (b leads that run), the run's pieces are summed in share order -- b's piece, then the first
+// piece of each following share while the run continues (shares without items skipped) -- and
+// stored into the run's slot. 256 threads, float4 elements of the dk x dv slot.
+__global__ void __launch_bounds__(256) state_fixup_kernel(const float* __restrict__ pieces,
+                                                          const int* __restrict__ piece_slot,
+                                                          const int* __restrict__ piece_flags, float* __restrict__ states,
+                                                          int n_shares, int msz) {
+    grid_dep_wait();  // tc_state's pieces (launched early, see launch_pdl)
+    const int b = blockIdx.x;
+    int k = -1;
+    if (piece_flags[2 * b + 1] & 2) k = 1;
+    else if ((piece_flags[2 * b] & 6) == 2) k = 0;
+    if (k < 0 || (piece_flags[2 * b + k] & 1)) return;  // no run leaves b, or b only continues one
+    float4* dst = reinterpret_cast<float4*>(states + static_cast<size_t>(piece_slot[2 * b + k]) * msz);
+    const float4* first = reinterpret_cast<const float4*>(pieces + static_cast<size_t>(2 * b + k) * msz);
+    for (int e = threadIdx.x; e < msz / 4; e += blockDim.x) {
+        float4 acc = first[e];
+        for (int c = b + 1; c < n_shares; c++) {
+            const int fl = piece_flags[2 * c];
+            if (fl & 4) continue;  // a share without items
+            const float4 x = reinterpret_cast<const float4*>(pieces + static_cast<size_t>(2 * c) * msz)[e];
+            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+            if (!(fl & 2)) break;  // the run ends in share c
+        }
+        dst[e] = acc;
+    }
+}
+
+// CTAs of tc_state: one per SM (the item count is only known on the device).
+int state_shares() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        sms = 152;
+    }
+    return sms < 1024 ? sms : 1024;
+}
+
+// Workspace: item offsets | tile totals g | tails | pieces [shares][2][dk][dv] | piece slots, flags.
+size_t state_base_bytes(size_t BH, int T) {
+    return (static_cast<size_t>(BH + 1) * sizeof(int) + 255) / 256 * 256 +
+           (2 * BH * ((static_cast<size_t>(T - 1) >> 7) + 8) * sizeof(float) + 255) / 256 * 256;
+}
+
 template <int DV>
 cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a, float* states, int BH, int H,
                                 int T, int Lmax, void* workspace, int* err, cudaStream_t stream, const int32_t* cu,
@@ -566,6 +634,10 @@ cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a
     int* item_off = static_cast<int*>(workspace);
     float* g = reinterpret_cast<float*>(static_cast<char*>(workspace) + off_bytes);
     float* tail = g + static_cast<size_t>(BH) * (maxPt + 8);
+    const int sms = state_shares();
+    float* pieces = reinterpret_cast<float*>(static_cast<char*>(workspace) + state_base_bytes(BH, T));
+    int* piece_slot = reinterpret_cast<int*>(pieces + static_cast<size_t>(2) * sms * kDk * DV);
+    int* piece_flags = piece_slot + 2 * sms;
     int nte = 0;  // dense: every sequence has the same items
     if (!cu) {
         const int pos = T - 1;
@@ -583,8 +655,7 @@ cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a
         cudaError_t e = cudaFuncSetAttribute(state_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        state_prep_kernel<<<dim3(BH, 1 + Lmax), kPrepThreads, smem, stream>>>(log_a, g, tail, states, sq, Lmax,
-                                                                             kDk * DV);
+        state_prep_kernel<<<BH, kPrepThreads, smem, stream>>>(log_a, g, tail, states, sq, Lmax, kDk * DV);
         note_launch(stream, "state_prep");
     }
     {
@@ -594,15 +665,16 @@ cudaError_t tc_prefill_state_dv(const void* k, const void* v, const float* log_a
         using C = StateCfg<DV>;
         cudaError_t e = cudaFuncSetAttribute(tc_state_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
         if (e != cudaSuccess) return e;
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
-            cudaGetLastError();
-            sms = 152;
-        }
         // the item count is only known on the device: one CTA per SM, each takes its share
-        tc_state_kernel<DV><<<sms, C::kThreads, C::kBytes, stream>>>(tk, tv, log_a, tail, states, sq, BH, Lmax, err);
+        e = launch_pdl(tc_state_kernel<DV>, dim3(sms), dim3(C::kThreads), C::kBytes, stream, tk, tv, log_a,
+                       static_cast<const float*>(tail), states, sq, BH, Lmax, pieces, piece_slot, piece_flags, err);
+        if (e != cudaSuccess) return e;
         note_launch(stream, "tc_state");
+        e = launch_pdl(state_fixup_kernel, dim3(sms), dim3(256), 0, stream, static_cast<const float*>(pieces),
+                       static_cast<const int*>(piece_slot), static_cast<const int*>(piece_flags), states, sms,
+                       kDk * DV);
+        if (e != cudaSuccess) return e;
+        note_launch(stream, "state_fixup");
     }
     return cudaGetLastError();
 }
@@ -625,10 +697,10 @@ bool tc_state_supported_packed(int dtype, int dk, int dv, int n_seq, int H, int 
            static_cast<int64_t>(n_seq) * H * (Pt + 8) < (int64_t(1) << 31);
 }
 
-size_t tc_state_workspace_bytes(int B, int H, int T) {
-    const size_t BH = static_cast<size_t>(B) * H;
-    return (static_cast<size_t>(BH + 1) * sizeof(int) + 255) / 256 * 256 +
-           2 * BH * ((static_cast<size_t>(T - 1) >> 7) + 8) * sizeof(float) + 256;
+size_t tc_state_workspace_bytes(int B, int H, int T, int dv) {
+    const size_t sms = static_cast<size_t>(state_shares());
+    return state_base_bytes(static_cast<size_t>(B) * H, T) + 2 * sms * kDk * dv * sizeof(float) +
+           4 * sms * sizeof(int) + 256;
 }
 
 cudaError_t tc_prefill_state(const void* k, const void* v, const float* log_a, float* states, int B, int H, int T,
