@@ -1048,7 +1048,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
     using C = PpCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t in_full[2], in_empty[2], s_full[2], p_ready[2], lv_full[2], lv_free[2], drain[2];
+    __shared__ uint64_t in_full[2], in_empty[2], kv_empty[2], s_full[2], p_ready[2], lv_full[2], lv_free[2], drain[2];
     __shared__ uint64_t node_full[2][C::kNodeSlots], node_empty[2][C::kNodeSlots];
     __shared__ uint64_t never;  // nothing arrives at it (failure-path test hook)
     __shared__ uint32_t tmem_base_sh;
@@ -1060,6 +1060,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
         for (int g = 0; g < 2; g++) {
             mbar_init(&in_full[g], 1);  // the producer's expect_tx arrive + the bytes
             mbar_init(&in_empty[g], 1);
+            mbar_init(&kv_empty[g], 1);
             mbar_init(&s_full[g], 1);
             mbar_init(&p_ready[g], C::kEpiWarps);
             mbar_init(&lv_full[g], 1);
@@ -1149,7 +1150,9 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             int next = claimed(atomicAdd(tile_counter, 1));
             int gn = 0, n_in = 0;
             for (int c = 0;; c++) {
-                if (c > 0 && !wait(&in_empty[g], (c - 1) & 1)) break;
+                // K (P) and V of the previous tile are free once PV has read them; Q and the
+                // decay prefix once its last level read has
+                if (c > 0 && !wait(&kv_empty[g], (c - 1) & 1)) break;
                 const int idx = next;
                 tile_id_sh[g] = idx;
                 if (idx < 0) {
@@ -1161,13 +1164,17 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 seq_of(sm, bh, T, rb, len);
                 const int row0 = rb + j * kTile;  // input rows
                 mbar_expect_tx(&in_full[g], C::kQkvBytes + C::kScalarTx);
-                tma_load_2d(st + C::kQ, &tm_q, &in_full[g], 0, row0);
-                tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[g], 64, row0);
                 tma_load_2d(st + C::kK, &tm_k, &in_full[g], 0, row0);
                 tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &in_full[g], 64, row0);
                 tma_load_2d(st + C::kV, &tm_v, &in_full[g], 0, row0);
-                bulk_load(smem + C::kCl2Base + g * 512, tok_cl2 + bh * T + j * kTile, 512, &in_full[g]);
                 n_in = c + 1;
+                // (on a failed wait the rest is still copied, so that the phase completes and the
+                // clean-up below can wait for every copy of it to land)
+                const bool q_free = c == 0 || wait(&in_empty[g], (c - 1) & 1);
+                tma_load_2d(st + C::kQ, &tm_q, &in_full[g], 0, row0);
+                tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[g], 64, row0);
+                bulk_load(smem + C::kCl2Base + g * 512, tok_cl2 + bh * T + j * kTile, 512, &in_full[g]);
+                if (!q_free) break;
                 // claim the group's next tile; its index is used once this tile's node copies are issued
                 const int next_idx = atomicAdd(tile_counter, 1);
                 // the tile's Fenwick nodes, in level order, into the group's ring
@@ -1255,6 +1262,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                     mma_bf16(tb, sdesc(kb + aoff, 16, 1024), sdesc(vb + kk * 2048, kPanelBytes, 1024), kIdO,
                              kk > 0 ? 1u : 0u);
                 }
+                mma_commit(&kv_empty[g]);  // PV has been issued: K (P) and V are read once it completes
                 for (int r = 1; r < R && ok; r++) {
                     if (!wait(&lv_free[g], (lvf++) & 1)) {
                         ok = false;
