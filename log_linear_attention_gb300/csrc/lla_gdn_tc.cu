@@ -349,42 +349,25 @@ struct CkCfg {
     static constexpr uint32_t kInBytes = 2 * kKQPanel + 8192;
 };
 
-// y (I + B) = y0 for the row vector y, B strictly lower triangular (fp32 [64][kLd] in shared
-// memory): from the last column down, y[s] is final once every later column has been
-// subtracted, y[r] -= y[s] B[s][r] for r < s (rows of B, read as broadcast float4).
-__device__ __forceinline__ void gdn_row_solve(const float* __restrict__ B, float* y) {
-#pragma unroll
-    for (int s = 63; s > 0; s--) {
-        const float ys = y[s];
-        const float4* brow = reinterpret_cast<const float4*>(B + s * CkCfg::kLd);
-#pragma unroll
-        for (int r4 = 0; r4 < (s + 3) / 4; r4++) {
-            const float4 b = brow[r4];
-            if (4 * r4 + 0 < s) y[4 * r4 + 0] = fmaf(-ys, b.x, y[4 * r4 + 0]);
-            if (4 * r4 + 1 < s) y[4 * r4 + 1] = fmaf(-ys, b.y, y[4 * r4 + 1]);
-            if (4 * r4 + 2 < s) y[4 * r4 + 2] = fmaf(-ys, b.z, y[4 * r4 + 2]);
-            if (4 * r4 + 3 < s) y[4 * r4 + 3] = fmaf(-ys, b.w, y[4 * r4 + 3]);
-        }
-    }
-}
-
 // grid (N chunks, B*H), 256 threads (warp w reads TMEM lanes 32 (w % 4) ..), two CTAs per SM.
 // Per chunk of 64 tokens:
 //   MMA-a: [K; Q] K^T -> G = K K^T, QK = Q K^T (bf16 operands, exact products)
 //   Bk = diag(beta) strictlower(G), Bg = diag(beta) strictlower(Gamma (.) G), Gamma_tr = e^{cl_t - cl_r}
-//   four row solves (fp32, one 64-thread group each, the row in registers):
-//     row t of Lk = (I + Bk)^-1 and of Lg = (I + Bg)^-1 (right-hand side e_t),
-//     row t of M = tril(QK) Lk and of Z Lg, Z = tril(Gamma (.) QK)
-//   MMA-b: [Lk diag(beta); M diag(beta)] K -> W = Lk diag(beta) K and M diag(beta) K, from which
+//   Lk = (I + Bk)^-1, Lg = (I + Bg)^-1 in fp32, blockwise in place (16 x 16 diagonal blocks by row
+//   solves, then two merges in rolled loops: the kernel's code stays compact, which keeps its
+//   warps fed by the instruction cache)
+//   MMA-m: [tril(QK); Z] [Lk | Lg] -> tril(QK) Lk and Z Lg, Z = tril(Gamma (.) QK)
+//   MMA-b: [Lk diag(beta); tril(QK) Lk diag(beta)] K -> W = Lk diag(beta) K and the correction of
 //          Q~ = diag(e^{cl}) (Q - tril(QK) W)
 //   MMA-c: [Lg diag(beta); P] V -> U = Lg diag(beta) V and the in-chunk output P V, with
 //          P[t][s] = lambda_t^(level(t,s)) (Z Lg)[t][s] beta_s for s <= t
 //   MMA-d: K^T diag(e^{cl_end - cl}) U -> the chunk's state, node (0, j)
-// The A operands of MMA-b/c and the B operand of MMA-d are fp32 values split into bf16 hi + lo
-// (two MMAs each); K and V are exact in bf16.
+// Every fp32 operand of MMA-m/b/c/d is split into bf16 hi + lo (MMA-m: three passes, the others
+// two); K and V are exact in bf16.
 __global__ void __launch_bounds__(256, 2)
     gdn_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ q,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+                        const __grid_constant__ CUtensorMap tm_qt, const __nv_bfloat16* __restrict__ q,
                         const float* __restrict__ log_a, const float* __restrict__ beta,
                         const float* __restrict__ lambda, float* __restrict__ Wg, float* __restrict__ Qt,
                         float* __restrict__ nodes, float* __restrict__ gam, float* __restrict__ oacc,
@@ -405,6 +388,7 @@ __global__ void __launch_bounds__(256, 2)
     uint64_t* mma_d = in_full + 3;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(in_full + 4);
     volatile int* fail = reinterpret_cast<volatile int*>(in_full + 5);
+    uint64_t* mma_m = in_full + 6;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (pad > static_cast<uint32_t>(C::kSlack)) {
@@ -413,7 +397,6 @@ __global__ void __launch_bounds__(256, 2)
     }
     const int j = blockIdx.x, bh = blockIdx.y;
     const size_t row0 = static_cast<size_t>(bh) * T + static_cast<size_t>(j) * C::kC;
-    const int grp = warp >> 1;  // 0: Lk, 1: M, 2: Lg, 3: Z Lg (row t = tid % 64 of each)
     const int t = tid & 63;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
@@ -422,6 +405,7 @@ __global__ void __launch_bounds__(256, 2)
         mbar_init(mma_a, 1);
         mbar_init(mma_bc, 1);
         mbar_init(mma_d, 1);
+        mbar_init(mma_m, 1);
         fence_mbar_init();
         *fail = 0;
     }
@@ -430,7 +414,7 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    int n_in = 0, n_a = 0, n_bc = 0, n_d = 0;
+    int n_in = 0, n_a = 0, n_bc = 0, n_d = 0, n_m = 0, n_st = 0;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         if (mbar_wait(bar, parity)) return true;
         *fail = 1;
@@ -491,18 +475,19 @@ __global__ void __launch_bounds__(256, 2)
         block_sync();
         if (*fail) break;
 
-        // ---- G, QK out of TMEM; Bk, Bg into shared memory (row t: warps 0, 1 build columns
-        //      0..31, warps 4, 5 columns 32..63); right-hand sides in registers. Decay factors
-        //      2^((cl_t - cl_r) log2 e) have non-positive exponents (r <= t).
-        float x[64];
-        {
-            tmem_ld32(tmem + lane_base, x);
-            tmem_ld32(tmem + lane_base + 32, x + 32);
-        }
+        // ---- G, QK out of TMEM (decay factors 2^((cl_t - cl_r) log2 e) have non-positive
+        //      exponents, r <= t).
+        //      Lanes 0..63 (warps 0, 1: columns 0..31; warps 4, 5: 32..63): Bk = diag(beta)
+        //      strictlower(G) and Bg = diag(beta) strictlower(Gamma (.) G), fp32 in the R area.
+        //      Lanes 64..127: the A operand of MMA-m, [tril(QK); Z] with Z = tril(Gamma (.) QK),
+        //      as bf16 hi + lo K-major rows of 64 tokens in the A2 area (warps 2, 3: tril(QK)
+        //      rows; warps 6, 7: Z rows).
         const float clt = cl[t] * kLog2e;
-        if (grp == 0 || grp == 2) {
+        if ((warp & 3) < 2) {
+            const int h = warp >> 2;  // column half
+            float x[32];
+            tmem_ld32(tmem + lane_base + 32 * h, x);
             const float b = bt[t];
-            const int h = grp >> 1;  // column half
             float4* bk = reinterpret_cast<float4*>(Bk + t * C::kLd + 32 * h);
             float4* bg = reinterpret_cast<float4*>(Bg + t * C::kLd + 32 * h);
 #pragma unroll
@@ -511,67 +496,242 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int r = 32 * h + 4 * r4 + e;
-                    const float g = h ? x[32 + 4 * r4 + e] : x[4 * r4 + e];
+                    const float g = x[4 * r4 + e];
                     vk[e] = r < t ? b * g : 0.f;
                     vg[e] = r < t ? b * ex2_ftz(clt - cl[r] * kLog2e) * g : 0.f;
                 }
                 bk[r4] = make_float4(vk[0], vk[1], vk[2], vk[3]);
                 bg[r4] = make_float4(vg[0], vg[1], vg[2], vg[3]);
             }
-        }
-        // right-hand sides: e_t (Lk, Lg), tril(QK)_t (M), tril(Gamma (.) QK)_t (Z Lg)
+        } else {
+            const bool zrow = warp >= 4;
+            const int row = zrow ? 64 + t : t;
+            uint8_t* dst = smem + C::kA2;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; hh++) {
+                float x[32];
+                tmem_ld32(tmem + lane_base + 32 * hh, x);
 #pragma unroll
-        for (int r = 0; r < 64; r++) {
-            if (grp == 0 || grp == 2)
-                x[r] = r == t ? 1.f : 0.f;
-            else if (grp == 1)
-                x[r] = r <= t ? x[r] : 0.f;
-            else
-                x[r] = r <= t ? ex2_ftz(clt - cl[r] * kLog2e) * x[r] : 0.f;
+                for (int c8 = 0; c8 < 4; c8++) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        float w2[2];
+#pragma unroll
+                        for (int u = 0; u < 2; u++) {
+                            const int r = 32 * hh + 8 * c8 + 2 * e + u;
+                            const float q = x[8 * c8 + 2 * e + u];
+                            const float w = zrow ? q * ex2_ftz(clt - cl[r] * kLog2e) : q;
+                            w2[u] = r <= t ? w : 0.f;
+                        }
+                        hi[e] = pack_bf16(w2[0], w2[1]);
+                        const float2 hf = unpack_bf16(hi[e]);
+                        lo[e] = pack_bf16(w2[0] - hf.x, w2[1] - hf.y);
+                    }
+                    const int c = 4 * hh + c8;
+                    *reinterpret_cast<uint4*>(dst + sw128_off(row, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(dst + 16384 + sw128_off(row, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
         }
         __syncthreads();
-        gdn_row_solve(grp < 2 ? Bk : Bg, x);
-        __syncthreads();  // Bk, Bg are read; A1 goes over them
 
-        // ---- A operands, bf16 hi + lo, K-major rows of 64 tokens: A1 = [Lk; M] diag(beta),
-        //      A2 = [Lg diag(beta); P]
+        // ---- Lk = (I + Bk)^-1 (threads 0..127) and Lg = (I + Bg)^-1 (threads 128..255), in place,
+        //      by blocks: the 16 x 16 diagonal blocks by row solves, then pairs of blocks merged,
+        //      [[A, 0], [C, D]]^-1 = [[A^-1, 0], [-D^-1 C A^-1, D^-1]], into 32 x 32 and 64 x 64.
+        //      The merge products run in rolled loops; their C A^-1 goes to a scratch in the Q
+        //      half of the input tile (Q is not read after MMA-a). B is strictly lower, so every
+        //      block above the diagonal is zero throughout.
         {
+            const int mt = tid & 127;
+            float* Bm = tid < 128 ? Bk : Bg;
+            float* tsc = reinterpret_cast<float*>(smem + C::kKQ + (tid < 128 ? 0 : C::kKQPanel) + C::kKQPanel / 2);
+            if (mt < 64) {
+                // row i of the inverse of diagonal block b (its right-hand side e_i is zero past i)
+                const int b16 = (mt >> 4) * 16, i = mt & 15;
+                float y[16];
+#pragma unroll
+                for (int c = 0; c < 16; c++) y[c] = c == i ? 1.f : 0.f;
+#pragma unroll
+                for (int s = 15; s > 0; s--) {
+                    if (s > i) continue;
+                    const float ys = y[s];
+                    const float* brow = Bm + (b16 + s) * C::kLd + b16;
+#pragma unroll
+                    for (int c = 0; c < s; c++) y[c] = fmaf(-ys, brow[c], y[c]);
+                }
+                __syncwarp();  // the block's rows are read by the warp that holds them
+                float4* out = reinterpret_cast<float4*>(Bm + (b16 + i) * C::kLd + b16);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; c4++) out[c4] = make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
+            }
+            __syncthreads();
+            // 16 -> 32: blocks (2c, 2c + 1), rows r0 = 32 c ..; thread: row i, columns j0 .. j0 + 3
+            {
+                const int c = mt >> 6, i = (mt >> 2) & 15, j0 = (mt & 3) * 4, r0 = 32 * c;
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+                for (int k = 0; k < 16; k++) {
+                    const float bik = Bm[(r0 + 16 + i) * C::kLd + r0 + k];
+                    const float4 d = *reinterpret_cast<const float4*>(Bm + (r0 + k) * C::kLd + r0 + j0);
+                    a0 = fmaf(bik, d.x, a0); a1 = fmaf(bik, d.y, a1); a2 = fmaf(bik, d.z, a2); a3 = fmaf(bik, d.w, a3);
+                }
+                *reinterpret_cast<float4*>(tsc + (c * 16 + i) * 16 + j0) = make_float4(a0, a1, a2, a3);
+            }
+            __syncthreads();
+            {
+                const int c = mt >> 6, i = (mt >> 2) & 15, j0 = (mt & 3) * 4, r0 = 32 * c;
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+                for (int k = 0; k <= i; k++) {
+                    const float dik = Bm[(r0 + 16 + i) * C::kLd + r0 + 16 + k];
+                    const float4 v = *reinterpret_cast<const float4*>(tsc + (c * 16 + k) * 16 + j0);
+                    a0 = fmaf(-dik, v.x, a0); a1 = fmaf(-dik, v.y, a1); a2 = fmaf(-dik, v.z, a2); a3 = fmaf(-dik, v.w, a3);
+                }
+                *reinterpret_cast<float4*>(Bm + (r0 + 16 + i) * C::kLd + r0 + j0) = make_float4(a0, a1, a2, a3);
+            }
+            __syncthreads();
+            // 32 -> 64: thread: row i of the lower half, columns j0 .. j0 + 7
+            {
+                const int i = mt >> 2, j0 = (mt & 3) * 8;
+                float a[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) a[e] = 0.f;
+#pragma unroll 4
+                for (int k = 0; k < 32; k++) {
+                    const float bik = Bm[(32 + i) * C::kLd + k];
+                    const float4 d0 = *reinterpret_cast<const float4*>(Bm + k * C::kLd + j0);
+                    const float4 d1 = *reinterpret_cast<const float4*>(Bm + k * C::kLd + j0 + 4);
+                    a[0] = fmaf(bik, d0.x, a[0]); a[1] = fmaf(bik, d0.y, a[1]); a[2] = fmaf(bik, d0.z, a[2]);
+                    a[3] = fmaf(bik, d0.w, a[3]); a[4] = fmaf(bik, d1.x, a[4]); a[5] = fmaf(bik, d1.y, a[5]);
+                    a[6] = fmaf(bik, d1.z, a[6]); a[7] = fmaf(bik, d1.w, a[7]);
+                }
+                *reinterpret_cast<float4*>(tsc + i * 32 + j0) = make_float4(a[0], a[1], a[2], a[3]);
+                *reinterpret_cast<float4*>(tsc + i * 32 + j0 + 4) = make_float4(a[4], a[5], a[6], a[7]);
+            }
+            __syncthreads();
+            {
+                const int i = mt >> 2, j0 = (mt & 3) * 8;
+                float a[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) a[e] = 0.f;
+#pragma unroll 4
+                for (int k = 0; k <= i; k++) {
+                    const float dik = Bm[(32 + i) * C::kLd + 32 + k];
+                    const float4 v0 = *reinterpret_cast<const float4*>(tsc + k * 32 + j0);
+                    const float4 v1 = *reinterpret_cast<const float4*>(tsc + k * 32 + j0 + 4);
+                    a[0] = fmaf(-dik, v0.x, a[0]); a[1] = fmaf(-dik, v0.y, a[1]); a[2] = fmaf(-dik, v0.z, a[2]);
+                    a[3] = fmaf(-dik, v0.w, a[3]); a[4] = fmaf(-dik, v1.x, a[4]); a[5] = fmaf(-dik, v1.y, a[5]);
+                    a[6] = fmaf(-dik, v1.z, a[6]); a[7] = fmaf(-dik, v1.w, a[7]);
+                }
+                float4* out = reinterpret_cast<float4*>(Bm + (32 + i) * C::kLd + j0);
+                out[0] = make_float4(a[0], a[1], a[2], a[3]);
+                out[1] = make_float4(a[4], a[5], a[6], a[7]);
+            }
+            __syncthreads();
+        }
+
+        // ---- MMA-m: [tril(QK); Z] [Lk | Lg] -> tril(QK) Lk (rows 0..63, columns 0..63) and Z Lg
+        //      (rows 64..127, columns 64..127), 3 bf16 passes (hi hi, hi lo, lo hi). Thread
+        //      (m = tid / 128, row r, half hl) keeps L_m[r][32 hl ..] for the A operands; B =
+        //      [Lk | Lg] (MN-major, 64-column atoms: Lk, Lg) is written over the R area.
+        const int lm = tid >> 7, lr = (tid >> 1) & 63, hl = tid & 1;
+        float lv[32];
+        {
+            const float4* src = reinterpret_cast<const float4*>((lm ? Bg : Bk) + lr * C::kLd + 32 * hl);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; c4++) {
+                const float4 f = src[c4];
+                lv[4 * c4] = f.x; lv[4 * c4 + 1] = f.y; lv[4 * c4 + 2] = f.z; lv[4 * c4 + 3] = f.w;
+            }
+        }
+        __syncthreads();
+        {
+            uint8_t* dst = smem + C::kR + lm * 8192;
+#pragma unroll
+            for (int c8 = 0; c8 < 4; c8++) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const float a = lv[8 * c8 + 2 * e], b2 = lv[8 * c8 + 2 * e + 1];
+                    hi[e] = pack_bf16(a, b2);
+                    const float2 hf = unpack_bf16(hi[e]);
+                    lo[e] = pack_bf16(a - hf.x, b2 - hf.y);
+                }
+                *reinterpret_cast<uint4*>(dst + sw128_off(lr, 4 * hl + c8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(dst + 16384 + sw128_off(lr, 4 * hl + c8)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        fence_async_smem();
+        block_sync();
+        if (tid == 0) {
+            const uint32_t ab = smem_u32(smem + C::kA2), bb = smem_u32(smem + C::kR);
+#pragma unroll
+            for (int pass = 0; pass < 3; pass++) {
+                const uint32_t pa = pass == 2 ? 16384u : 0u, pb = pass == 1 ? 16384u : 0u;
+#pragma unroll
+                for (int kk = 0; kk < 4; kk++)
+                    mma_bf16(tmem + 64, sdesc(ab + pa + kk * 32, 16, 1024), sdesc(bb + pb + kk * 2048, 8192, 1024),
+                             idesc_bf16(128, 128, 0, 1), (pass > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(mma_m);
+            n_m = 1;
+            wait(mma_m, 0);
+        }
+        block_sync();
+        if (*fail) break;
+
+        // ---- A operands, bf16 hi + lo, K-major rows of 64 tokens: A1 = [Lk; tril(QK) Lk] diag(beta)
+        //      over the R area, A2 = [Lg diag(beta); P] over the A2 area, with
+        //      P[t][s] = lambda_t^(level(t,s)) (Z Lg)[t][s] beta_s for s <= t.
+        {
+            // product row t (lane), columns 32 hq ..: tril(QK) Lk (lanes 0..63) or Z Lg (lanes 64..127)
+            const int hq = warp >> 2;
+            const bool zq = (warp & 3) >= 2;
+            float pv[32];
+            tmem_ld32(tmem + lane_base + 64 + (zq ? 64 : 0) + 32 * hq, pv);
             float lam[7];
-            if (grp == 3) {
+            if (zq) {
 #pragma unroll
                 for (int l = 0; l < 7; l++) lam[l] = lambda[(row0 + t) * L + l];
             }
-            uint8_t* dst = smem + ((grp == 0 || grp == 1) ? C::kR : C::kA2);
-            const int row = (grp & 1) ? 64 + t : t;
+            // (tmask >= 0: the row is token tmask's row of P: lambda weights and the causal mask)
+            auto put = [&](uint8_t* dst, int row, int c0, const float* v, int tmask) {
 #pragma unroll
-            for (int c8 = 0; c8 < 8; c8++) {
-                uint32_t h[4], l[4];
+                for (int c8 = 0; c8 < 4; c8++) {
+                    uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    float w2[2];
+                    for (int e = 0; e < 4; e++) {
+                        float w2[2];
 #pragma unroll
-                    for (int u = 0; u < 2; u++) {
-                        const int sidx = 8 * c8 + 2 * e + u;
-                        float w = x[sidx] * bt[sidx];
-                        if (grp == 3) {
-                            const int xo = t ^ sidx;
-                            float lw = xo >= 32 ? lam[6] : lam[5];
-                            lw = xo < 16 ? lam[4] : lw;
-                            lw = xo < 8 ? lam[3] : lw;
-                            lw = xo < 4 ? lam[2] : lw;
-                            lw = xo < 2 ? lam[1] : lw;
-                            lw = xo == 0 ? lam[0] : lw;
-                            w = sidx <= t ? w * lw : 0.f;
+                        for (int u = 0; u < 2; u++) {
+                            const int s = c0 + 8 * c8 + 2 * e + u;
+                            float w = v[8 * c8 + 2 * e + u] * bt[s];
+                            if (tmask >= 0) {
+                                const int xo = tmask ^ s;
+                                float lw = xo >= 32 ? lam[6] : lam[5];
+                                lw = xo < 16 ? lam[4] : lw;
+                                lw = xo < 8 ? lam[3] : lw;
+                                lw = xo < 4 ? lam[2] : lw;
+                                lw = xo < 2 ? lam[1] : lw;
+                                lw = xo == 0 ? lam[0] : lw;
+                                w = s <= tmask ? w * lw : 0.f;
+                            }
+                            w2[u] = w;
                         }
-                        w2[u] = w;
+                        hi[e] = pack_bf16(w2[0], w2[1]);
+                        const float2 hf = unpack_bf16(hi[e]);
+                        lo[e] = pack_bf16(w2[0] - hf.x, w2[1] - hf.y);
                     }
-                    h[e] = pack_bf16(w2[0], w2[1]);
-                    const float2 hf = unpack_bf16(h[e]);
-                    l[e] = pack_bf16(w2[0] - hf.x, w2[1] - hf.y);
+                    const int cc = (c0 >> 3) + c8;
+                    *reinterpret_cast<uint4*>(dst + sw128_off(row, cc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(dst + 16384 + sw128_off(row, cc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
-                *reinterpret_cast<uint4*>(dst + sw128_off(row, c8)) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(dst + 16384 + sw128_off(row, c8)) = make_uint4(l[0], l[1], l[2], l[3]);
-            }
+            };
+            // (MMA-m has completed: its operands in the R and A2 areas are free)
+            put(smem + (lm ? C::kA2 : C::kR), lr, 32 * hl, lv, -1);
+            put(smem + (zq ? C::kA2 : C::kR), 64 + t, 32 * hq, pv, zq ? t : -1);
         }
         fence_async_smem();
         block_sync();
@@ -596,33 +756,46 @@ __global__ void __launch_bounds__(256, 2)
         if (*fail) break;
 
         // ---- W, Q~ (fp32, the level pass reads them), U (into shared memory), in-chunk output
+        auto qt_box = [&](int b) -> uint8_t* {
+            return b < 2 ? smem + C::kKQ + b * C::kKQPanel + C::kKQPanel / 2 : smem + C::kR + 16384 + (b - 2) * 8192;
+        };
         {
             const int half = warp >> 2;  // which 64 of the 128 columns of MMA-b, 32 of the 64 of MMA-c
             const bool top = (warp & 3) < 2;  // TMEM lanes 0..63 (W, U rows) or 64..127 (Q~, output rows)
             float v[64];
             tmem_ld32(tmem + lane_base + 64 + 64 * half, v);
             tmem_ld32(tmem + lane_base + 96 + 64 * half, v + 32);
-            const size_t wrow = (static_cast<size_t>(bh) * N + j) * C::kC + t;
-            if (64 * half < dk) {
-                if (top) {
-                    float4* dst = reinterpret_cast<float4*>(Wg + wrow * dk + 64 * half);
+            if (N > 1 && 64 * half < dk) {
+                // row t of W (top) or Q~ into two 32-column TMA boxes (64 rows x 128 B, SW128: the
+                // 16-byte chunk c of row t at c ^ (t % 8)); thread 0 stores the boxes after the
+                // next barrier. W's boxes go to the A2 area, Q~'s to the Q halves of the input
+                // tile and the upper R area (all read by no MMA any more).
+                uint8_t* bx[2];
 #pragma unroll
-                    for (int c4 = 0; c4 < 16; c4++)
-                        dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-                } else {
-                    const float e = ex2_ftz(clt);  // e^{cl_t}, clt in log2 units
-                    const uint4* qrow = reinterpret_cast<const uint4*>(q + (row0 + t) * dk + 64 * half);
-                    float4* dst = reinterpret_cast<float4*>(Qt + wrow * dk + 64 * half);
+                for (int u = 0; u < 2; u++) bx[u] = top ? smem + C::kA2 + (2 * half + u) * 8192 : qt_box(2 * half + u);
+                const float e = ex2_ftz(clt);  // e^{cl_t}, clt in log2 units
+                const uint4* qrow = reinterpret_cast<const uint4*>(q + (row0 + t) * dk + 64 * half);
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; c8++) {
+                for (int c8 = 0; c8 < 8; c8++) {
+                    float w[8];
+                    if (top) {
+#pragma unroll
+                        for (int e8 = 0; e8 < 8; e8++) w[e8] = v[8 * c8 + e8];
+                    } else {
                         const uint4 u = qrow[c8];
                         const float2 f0 = unpack_bf16(u.x), f1 = unpack_bf16(u.y), f2 = unpack_bf16(u.z),
                                      f3 = unpack_bf16(u.w);
-                        dst[2 * c8] = make_float4(e * (f0.x - v[8 * c8]), e * (f0.y - v[8 * c8 + 1]),
-                                                  e * (f1.x - v[8 * c8 + 2]), e * (f1.y - v[8 * c8 + 3]));
-                        dst[2 * c8 + 1] = make_float4(e * (f2.x - v[8 * c8 + 4]), e * (f2.y - v[8 * c8 + 5]),
-                                                      e * (f3.x - v[8 * c8 + 6]), e * (f3.y - v[8 * c8 + 7]));
+                        w[0] = e * (f0.x - v[8 * c8]); w[1] = e * (f0.y - v[8 * c8 + 1]);
+                        w[2] = e * (f1.x - v[8 * c8 + 2]); w[3] = e * (f1.y - v[8 * c8 + 3]);
+                        w[4] = e * (f2.x - v[8 * c8 + 4]); w[5] = e * (f2.y - v[8 * c8 + 5]);
+                        w[6] = e * (f3.x - v[8 * c8 + 6]); w[7] = e * (f3.y - v[8 * c8 + 7]);
                     }
+                    // floats 8 c8 .. 8 c8 + 7 of the row: box c8 / 4, chunks 2 (c8 % 4), 2 (c8 % 4) + 1
+                    uint8_t* b = bx[c8 >> 2];
+                    const int ch = 2 * (c8 & 3);
+                    *reinterpret_cast<float4*>(b + t * 128 + ((ch ^ (t & 7)) << 4)) = make_float4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<float4*>(b + t * 128 + (((ch + 1) ^ (t & 7)) << 4)) =
+                        make_float4(w[4], w[5], w[6], w[7]);
                 }
             }
             tmem_ld32(tmem + lane_base + 192 + 32 * half, v);
@@ -662,6 +835,16 @@ __global__ void __launch_bounds__(256, 2)
         fence_async_smem();
         block_sync();
         if (tid == 0) {
+            // W and Q~ of the chunk: (dk / 32) boxes each
+            const int wr = static_cast<int>((static_cast<size_t>(bh) * N + j) * C::kC);
+            for (int b = 0; b < dk / 32; b++) {
+                tma_store_2d(&tm_w, smem + C::kA2 + b * 8192, 32 * b, wr);
+                tma_store_2d(&tm_qt, qt_box(b), 32 * b, wr);
+            }
+            bulk_commit();
+            n_st = 1;
+        }
+        if (tid == 0) {
             const uint32_t kq = smem_u32(smem + C::kKQ), ub = smem_u32(smem + C::kR);
 #pragma unroll
             for (int kk = 0; kk < 4; kk++)
@@ -693,11 +876,13 @@ __global__ void __launch_bounds__(256, 2)
         }
     } while (false);
 
+    if (tid == 0 && n_st) bulk_wait0();  // the stores of W and Q~ have read their boxes
     if (tid == 0 && *fail) {
         if (n_in) mbar_wait(in_full, 0);
         if (n_a) mbar_wait(mma_a, 0);
         if (n_bc) mbar_wait(mma_bc, 0);
         if (n_d) mbar_wait(mma_d, 0);
+        if (n_m) mbar_wait(mma_m, 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -720,15 +905,18 @@ cudaError_t gdn_chunk_tc(const GdnPlan& pl, const void* q, const void* k, const 
                          const float* beta, const float* lambda, float* Wg, float* Qt, float* nodes, float* gam,
                          float* oacc, void* out, int L, int* err, cudaStream_t stream) {
     const uint64_t rows = static_cast<uint64_t>(pl.B) * pl.H * pl.T;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tw, tqt;
+    const uint64_t wrows = static_cast<uint64_t>(pl.B) * pl.H * pl.N * CkCfg::kC;
     if (!make_map_box(&tq, q, false, rows, pl.dk, 64, CkCfg::kC) || !make_map_box(&tk, k, false, rows, pl.dk, 64, CkCfg::kC) ||
-        !make_map_box(&tv, v, false, rows, pl.dv, 64, CkCfg::kC))
+        !make_map_box(&tv, v, false, rows, pl.dv, 64, CkCfg::kC) ||
+        !make_map_box(&tw, Wg, true, wrows, pl.dk, 32, CkCfg::kC) ||
+        !make_map_box(&tqt, Qt, true, wrows, pl.dk, 32, CkCfg::kC))
         return cudaErrorInvalidValue;
     const int smem = CkCfg::kBytes + CkCfg::kSlack;
     cudaError_t e = cudaFuncSetAttribute(gdn_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     gdn_chunk_tc_kernel<<<dim3(pl.N, pl.B * pl.H), 256, smem, stream>>>(
-        tq, tk, tv, static_cast<const __nv_bfloat16*>(q), log_a, beta, lambda, Wg, Qt, nodes, gam, oacc,
+        tq, tk, tv, tw, tqt, static_cast<const __nv_bfloat16*>(q), log_a, beta, lambda, Wg, Qt, nodes, gam, oacc,
         static_cast<__nv_bfloat16*>(out), pl.T, pl.N, pl.dk, L, pl.node_count, err);
     note_launch(stream, "gdn_chunk_tc");
     return cudaGetLastError();
