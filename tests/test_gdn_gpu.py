@@ -100,6 +100,21 @@ def test_gdn_bf16_levels_run_on_tensor_cores(dk):
     assert rel_err_per_head(out.float().cpu().numpy(), _ref(inp, beta)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("B,H,T,dk", [(2, 3, 64, 128), (1, 2, 64, 64), (3, 1, 128, 64)])
+def test_gdn_tensor_core_short_sequences(B, H, T, dk):
+    """The tensor-core chunk pass on one chunk (its output goes straight to `out`, no level pass)
+    and on two chunks (one level-0 read), at dk = 128 and 64."""
+    from log_linear_attention_gb300 import binding
+    cfg = _cfg("gdn-headline", B=B, H=H, T=T, dk=dk)
+    inp, beta = _problem(cfg, 60 + T + dk)
+    q, k, v, log_a, lam = to_device(inp)
+    out = torch.empty_like(v)
+    names = [n for n, _ in binding.gdn_forward_profile(q, k, v, log_a, torch.from_numpy(beta).cuda(), lam, 64, out)]
+    assert binding.device_error() == 0
+    assert names[0] == "gdn_chunk_tc", names
+    assert rel_err_per_head(out.float().cpu().numpy(), _ref(inp, beta)) <= TOL_BF16
+
+
 def test_gdn_slow_decay_long_range():
     """log_a near 0 keeps far keys alive, so the coarse Fenwick levels (and the carried
     transitions through many chunks) carry much of the output."""
