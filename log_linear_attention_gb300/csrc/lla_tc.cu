@@ -1007,6 +1007,37 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 //   round r >= 2: three more level reads each in [64, 256).
 // The epilogue reads every round back into fp32 accumulators,
 // acc = O + sum_p lambda_t^(8+p) exp(cl_t + D_p) L_p, and stores them as bf16.
+// Weights of the 16 keys s = 32 blk + 16 HALF + e (e = 0..15) of a diagonal 32 x 32 block for the
+// query in lane `lane` of the block: lx[l] for the level l = 1 + floor(log2(lane ^ s')) of the
+// pair (lx[0] at s' = lane; s' = s mod 32), 0 where s' > lane (the highest differing bit is set in
+// s'), times the key's column weight cw[e]. With s' fixed at compile time every bit test is a
+// per-lane predicate, so a weight is five selects.
+template <int HALF>
+__device__ __forceinline__ void diag_weights(int lane, const float* lx, const float* cw, float* w) {
+    bool lb[5];
+#pragma unroll
+    for (int b = 0; b < 5; b++) lb[b] = (lane >> b) & 1;
+    const float4* cw4 = reinterpret_cast<const float4*>(cw);
+    float c[16];
+#pragma unroll
+    for (int e4 = 0; e4 < 4; e4++) {
+        const float4 x = cw4[e4];
+        c[4 * e4] = x.x; c[4 * e4 + 1] = x.y; c[4 * e4 + 2] = x.z; c[4 * e4 + 3] = x.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; e++) {
+        constexpr int kHalf = HALF * 16;
+        const int sp = kHalf + e;
+        float v = lx[0];
+#pragma unroll
+        for (int b = 0; b < 5; b++) {
+            const bool sb = (sp >> b) & 1;
+            v = (lb[b] != sb) ? (sb ? 0.f : lx[b + 1]) : v;  // higher bits override lower ones
+        }
+        w[e] = v * c[e];
+    }
+}
+
 struct PpCfg {
     static constexpr int kQ = 0;
     static constexpr int kK = 2 * kPanelBytes;  // K tile, then P of the same tile
@@ -1016,10 +1047,11 @@ struct PpCfg {
     static constexpr int kNodeSlots = 2;  // per group
     static constexpr int kNodeBytes = kPanelBytes;
     static constexpr int kNodeBase = 2 * kStageBytes;
-    // 128 floats per group after the node slots: the tile's in-tile log2 decay prefix
-    static constexpr int kCl2Base = kNodeBase + 2 * kNodeSlots * kNodeBytes;
+    // 128 floats per group after the node slots: the tile's column decay weights
+    // 2^(cl_{s|31} - cl_s) (key s to the end of its 32-key block)
+    static constexpr int kColwBase = kNodeBase + 2 * kNodeSlots * kNodeBytes;
     static constexpr int kScalarTx = 512;
-    static constexpr int kBytes = kCl2Base + 2 * 512 + 1024;
+    static constexpr int kBytes = kColwBase + 2 * 512 + 1024;
     static constexpr int kEpiWarps = 8;  // per group
     static constexpr int kFirstEpi = 4;  // first epilogue warp
     static constexpr int kThreads = (kFirstEpi + 2 * kEpiWarps) * 32;
@@ -1138,6 +1170,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 tma_prefetch_l2(&tm_k, 64, r0);
                 tma_prefetch_l2(&tm_v, 0, r0);
                 prefetch_l2(tok_cl2 + pbh * T + pj * kTile, 512);
+                prefetch_l2(tok_colw + pbh * T + pj * kTile, 512);
                 // this tile's lambda rows, within the tensor (a packed tile may end past it)
                 const int r1 = min(r0 + kTile, in_rows);
                 const uintptr_t lb = reinterpret_cast<uintptr_t>(lambda + static_cast<size_t>(r0) * L) & ~uintptr_t(15);
@@ -1173,7 +1206,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 const bool q_free = c == 0 || wait(&in_empty[g], (c - 1) & 1);
                 tma_load_2d(st + C::kQ, &tm_q, &in_full[g], 0, row0);
                 tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[g], 64, row0);
-                bulk_load(smem + C::kCl2Base + g * 512, tok_cl2 + bh * T + j * kTile, 512, &in_full[g]);
+                bulk_load(smem + C::kColwBase + g * 512, tok_colw + bh * T + j * kTile, 512, &in_full[g]);
                 if (!q_free) break;
                 // claim the group's next tile; its index is used once this tile's node copies are issued
                 const int next_idx = atomicAdd(tile_counter, 1);
@@ -1288,7 +1321,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
         const int t = quad * 32 + lane;  // query row = TMEM lane
         const int q32 = quad * 32;
         const uint32_t tb = tmem + 256u * g + (static_cast<uint32_t>(q32) << 16);
-        const float* cl2 = reinterpret_cast<const float*>(smem + C::kCl2Base + g * 512);
+        const float* colw = reinterpret_cast<const float*>(smem + C::kColwBase + g * 512);
         int rnd = 0;  // lv_full phases of this group consumed so far
         // test hook: a wait that runs out (records the timeout; every role then leaves)
         const bool held = tc_debug_hold != 0 && !ewait(&never, 0);
@@ -1302,26 +1335,22 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             const int row0 = rb + j * kTile;         // input rows
             const int live = len - j * kTile;        // rows of this tile inside the sequence (>= 1)
             const int tr = t < live ? t : live - 1;  // lambda row read for this lane
+            // in-tile log2 decay prefix: this row's and the last of each 32-key block
+            const float* cl2 = tok_cl2 + bh * T + j * kTile;
             const float cl2_t = cl2[t];
-            // this row's lambda (levels 0..7 for P; 8 + p for the level reads) and the tile's
-            // decay-table row, loaded while S is computed; rr[p] = lambda_t^(8+p) exp(cl_t + D_p)
-            // is the weight of level read p (0 where bit p of j is clear)
+            float cend[4];
+#pragma unroll
+            for (int b = 0; b < 4; b++) cend[b] = cl2[32 * b + 31];
+            // this row's lambda for levels 0..7 (the weights of P), loaded while S is computed;
+            // the rest of the row (levels 8 + p, the weights of the level reads) and the tile's
+            // decay-table row are pulled into L1 for the read-back
             float lam_in[8];
-            float rr[16];
-            {
-                const float* lam_row = lambda + static_cast<size_t>(row0 + tr) * L;
+            const float* lam_row = lambda + static_cast<size_t>(row0 + tr) * L;
+            const float* drow = dtab + (static_cast<size_t>(bh) * NT + j) * 16;
 #pragma unroll
-                for (int l = 0; l < 8; l++) lam_in[l] = l < L ? lam_row[l] : 0.f;
-                const float4* drow = reinterpret_cast<const float4*>(dtab + (static_cast<size_t>(bh) * NT + j) * 16);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; c4++) {
-                    const float4 x = drow[c4];
-                    rr[4 * c4] = x.x; rr[4 * c4 + 1] = x.y; rr[4 * c4 + 2] = x.z; rr[4 * c4 + 3] = x.w;
-                }
-#pragma unroll
-                for (int p = 0; p < 16; p++)
-                    rr[p] = (p < P && ((j >> p) & 1)) ? lam_row[8 + p] * exp2f(cl2_t + rr[p]) : 0.f;
-            }
+            for (int l = 0; l < 8; l++) lam_in[l] = l < L ? lam_row[l] : 0.f;
+            if (L > 8) prefetch_l1(lam_row + L - 1);
+            if (lane == 0) prefetch_l1(drow);
             // ---- P = (S masked, decayed, lambda-weighted) -> bf16 over K in shared memory
             if (!ewait(&s_full[g], c & 1)) break;
             tc_fence_after();
@@ -1336,47 +1365,59 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 if (c0 > q32) {
 #pragma unroll
                     for (int e = 0; e < 8; e++) pk[e] = 0u;
-                } else {
+                } else if (c0 < q32) {
+                    // keys before every row of this warp: one level per row (7 if bit 6 of t ^ s
+                    // is set, else 6) and the decay factorised at the block end,
+                    // 2^(cl_t - cl_s) = 2^(cl_t - cl_{c0+31}) * 2^(cl_{c0+31} - cl_s), both <= 1
+                    // for non-positive log decays; the weights are formed while S is loaded
+                    const float rowf = ex2_ftz(cl2_t - cend[ci]) * (((t ^ c0) & 64) ? lam_in[7] : lam_in[6]);
                     tmem_ld16_issue(tb + cb, sv);
+                    float w[16];
+                    const float4* cw4 = reinterpret_cast<const float4*>(colw + cb);
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; e4++) {
+                        const float4 x = cw4[e4];
+                        w[4 * e4] = rowf * x.x; w[4 * e4 + 1] = rowf * x.y;
+                        w[4 * e4 + 2] = rowf * x.z; w[4 * e4 + 3] = rowf * x.w;
+                    }
                     tmem_ld16_wait(sv);
-                    if (c0 < q32) {
-                        // keys before every row of this warp: one level per row, factorised decay
-                        // 2^(cl_t - cl_s) = 2^(cl_t - cl_{c0+31}) * 2^(cl_{c0+31} - cl_s), both <= 1;
-                        // lane e computes the column factor of key cb + (e & 15)
-                        const int lvl = 32 - __clz(t ^ c0);
-                        float lw = lam_in[0];
 #pragma unroll
-                        for (int l = 1; l < 8; l++) lw = (lvl == l) ? lam_in[l] : lw;
-                        const float cend = cl2[c0 + 31];
-                        const float rowf = ex2_ftz(cl2_t - cend) * lw;
-                        const float cw = ex2_ftz(cend - cl2[cb + (lane & 15)]);
+                    for (int e = 0; e < 16; e += 2)
+                        pk[e >> 1] = pack_bf16(__uint_as_float(sv[e]) * w[e], __uint_as_float(sv[e + 1]) * w[e + 1]);
+                } else {
+                    // diagonal block: the causal mask and a per-key level 1 + floor(log2(t ^ s))
+                    // (0 at s = t). Where every column weight of the block lies in [2^-100, 2^100]
+                    // the decay is factorised at the block end as above (the row factor is then at
+                    // most 2^100, the product exact to a few ulp); else each key's factor is exact.
+                    const bool fact = __all_sync(0xffffffffu, colw[c0 + lane] >= 0x1p-100f && colw[c0 + lane] <= 0x1p100f);
+                    tmem_ld16_issue(tb + cb, sv);
+                    float w[16];
+                    if (fact) {
+                        const float rowf = ex2_ftz(cl2_t - cend[ci]);
+                        float lx[6];
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            const float w0 = __shfl_sync(0xffffffffu, cw, e), w1 = __shfl_sync(0xffffffffu, cw, e + 1);
-                            pk[e >> 1] = pack_bf16(__uint_as_float(sv[e]) * rowf * w0,
-                                                   __uint_as_float(sv[e + 1]) * rowf * w1);
-                        }
+                        for (int l = 0; l < 6; l++) lx[l] = lam_in[l] * rowf;
+                        if (half == 0) diag_weights<0>(lane, lx, colw + cb, w);
+                        else diag_weights<1>(lane, lx, colw + cb, w);
                     } else {
-                        // diagonal block: causal mask, per-key level 1 + floor(log2(t ^ s)) (0 at
-                        // s = t, at most 5) and the exact per-key decay. A masked key (s > t) may
-                        // give an infinite decay factor; the select drops it.
+                        // a masked key (s > t) may give an infinite factor; the select drops it
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            float v2[2];
-#pragma unroll
-                            for (int h = 0; h < 2; h++) {
-                                const int sidx = cb + e + h;
-                                const int x = t ^ sidx;
-                                float lw = x >= 16 ? lam_in[5] : lam_in[4];
-                                lw = x < 8 ? lam_in[3] : lw;
-                                lw = x < 4 ? lam_in[2] : lw;
-                                lw = x < 2 ? lam_in[1] : lw;
-                                lw = x == 0 ? lam_in[0] : lw;
-                                const float val = __uint_as_float(sv[e + h]) * ex2_ftz(cl2_t - cl2[sidx]) * lw;
-                                v2[h] = sidx <= t ? val : 0.f;
-                            }
-                            pk[e >> 1] = pack_bf16(v2[0], v2[1]);
+                        for (int e = 0; e < 16; e++) {
+                            const int sidx = cb + e;
+                            const int x = t ^ sidx;
+                            float lw = x >= 16 ? lam_in[5] : lam_in[4];
+                            lw = x < 8 ? lam_in[3] : lw;
+                            lw = x < 4 ? lam_in[2] : lw;
+                            lw = x < 2 ? lam_in[1] : lw;
+                            lw = x == 0 ? lam_in[0] : lw;
+                            w[e] = sidx <= t ? ex2_ftz(cl2_t - cl2[sidx]) * lw : 0.f;
                         }
+                    }
+                    tmem_ld16_wait(sv);
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        // 0 * S, not a select: S is finite
+                        pk[e >> 1] = pack_bf16(__uint_as_float(sv[e]) * w[e], __uint_as_float(sv[e + 1]) * w[e + 1]);
                     }
                 }
                 uint8_t* panel = pbase + (c0 >> 6) * kPanelBytes;
@@ -1413,9 +1454,9 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
 #pragma unroll 1
                 for (int x = x0; x < x1; x++) {
                     while (((j >> p_cur) & 1) == 0) p_cur++;
-                    float w = rr[0];
-#pragma unroll
-                    for (int i = 1; i < 16; i++) w = (p_cur == i) ? rr[i] : w;
+                    // lambda_t^(8+p) exp(cl_t + D_p), read where it is used (the row and the
+                    // decay-table row are in L1 from the tile's start)
+                    const float w = lam_row[8 + p_cur] * exp2f(cl2_t + drow[p_cur]);
                     p_cur++;
                     float lv[DH];
                     tmem_ld32(tb + C::lv_col(r, x - x0) + half * DH, lv);

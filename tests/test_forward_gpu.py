@@ -118,6 +118,17 @@ def test_bf16_slow_decay_long_range():
     assert rel_err_per_head(got, oracle_full(inp)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("mu", [2.0, 4.0])
+def test_bf16_fast_decay(mu):
+    """Strong decays: at mu = 4 every 32-token block decays by more than 100 bits, so the
+    diagonal blocks of the tensor-core output kernel take their exact per-key decay; at
+    mu = 2 (about 95 bits a block) most blocks take the factorised one and some do not."""
+    cfg = cfg_like("headline", B=1, H=2, T=512, log_a_mu=mu)
+    inp = inputs.make_prefill(cfg, seed=11)
+    got = run(inp, 64)
+    assert rel_err_per_head(got, oracle_full(inp)) <= TOL_BF16
+
+
 def test_chunk_invariance_bf16():
     cfg = cfg_like("small", B=1, H=2, T=1024)
     inp = inputs.make_prefill(cfg, seed=3)
