@@ -1007,16 +1007,17 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 //   round r >= 2: three more level reads each in [64, 256).
 // The epilogue reads every round back into fp32 accumulators,
 // acc = O + sum_p lambda_t^(8+p) exp(cl_t + D_p) L_p, and stores them as bf16.
-// Weights of the 16 keys s = 32 blk + 16 HALF + e (e = 0..15) of a diagonal 32 x 32 block for the
+// Weights of the 16 keys s = 32 blk + 16 half + e (e = 0..15) of a diagonal 32 x 32 block for the
 // query in lane `lane` of the block: lx[l] for the level l = 1 + floor(log2(lane ^ s')) of the
 // pair (lx[0] at s' = lane; s' = s mod 32), 0 where s' > lane (the highest differing bit is set in
-// s'), times the key's column weight cw[e]. With s' fixed at compile time every bit test is a
-// per-lane predicate, so a weight is five selects.
-template <int HALF>
-__device__ __forceinline__ void diag_weights(int lane, const float* lx, const float* cw, float* w) {
-    bool lb[5];
+// s'), times the key's column weight cw[e]. Bits 0..3 of s' are e, fixed at compile time, so each
+// of their tests is a per-lane predicate; bit 4 (the half) is decided once per lane.
+__device__ __forceinline__ void diag_weights(int lane, int half, const float* lx, const float* cw, float* w) {
+    bool lb[4];
 #pragma unroll
-    for (int b = 0; b < 5; b++) lb[b] = (lane >> b) & 1;
+    for (int b = 0; b < 4; b++) lb[b] = (lane >> b) & 1;
+    const bool diff4 = ((lane >> 4) & 1) != half;  // the key is in the other 16-key half
+    const float v4 = half ? 0.f : lx[5];           // key after every such row, or before it
     const float4* cw4 = reinterpret_cast<const float4*>(cw);
     float c[16];
 #pragma unroll
@@ -1026,14 +1027,13 @@ __device__ __forceinline__ void diag_weights(int lane, const float* lx, const fl
     }
 #pragma unroll
     for (int e = 0; e < 16; e++) {
-        constexpr int kHalf = HALF * 16;
-        const int sp = kHalf + e;
         float v = lx[0];
 #pragma unroll
-        for (int b = 0; b < 5; b++) {
-            const bool sb = (sp >> b) & 1;
+        for (int b = 0; b < 4; b++) {
+            const bool sb = (e >> b) & 1;
             v = (lb[b] != sb) ? (sb ? 0.f : lx[b + 1]) : v;  // higher bits override lower ones
         }
+        v = diff4 ? v4 : v;
         w[e] = v * c[e];
     }
 }
@@ -1360,6 +1360,9 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             for (int ci = 0; ci < kTile / 32; ci++) {
                 const int c0 = ci * 32;
                 const int cb = c0 + half * 16;  // first key of this warp's 16
+                // the block's last log decay, by selects (an indexed register array would be
+                // placed in local memory)
+                const float cen = ci == 0 ? cend[0] : ci == 1 ? cend[1] : ci == 2 ? cend[2] : cend[3];
                 uint32_t sv[16];
                 uint32_t pk[8];
                 if (c0 > q32) {
@@ -1370,7 +1373,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                     // is set, else 6) and the decay factorised at the block end,
                     // 2^(cl_t - cl_s) = 2^(cl_t - cl_{c0+31}) * 2^(cl_{c0+31} - cl_s), both <= 1
                     // for non-positive log decays; the weights are formed while S is loaded
-                    const float rowf = ex2_ftz(cl2_t - cend[ci]) * (((t ^ c0) & 64) ? lam_in[7] : lam_in[6]);
+                    const float rowf = ex2_ftz(cl2_t - cen) * (((t ^ c0) & 64) ? lam_in[7] : lam_in[6]);
                     tmem_ld16_issue(tb + cb, sv);
                     float w[16];
                     const float4* cw4 = reinterpret_cast<const float4*>(colw + cb);
@@ -1393,12 +1396,11 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                     tmem_ld16_issue(tb + cb, sv);
                     float w[16];
                     if (fact) {
-                        const float rowf = ex2_ftz(cl2_t - cend[ci]);
+                        const float rowf = ex2_ftz(cl2_t - cen);
                         float lx[6];
 #pragma unroll
                         for (int l = 0; l < 6; l++) lx[l] = lam_in[l] * rowf;
-                        if (half == 0) diag_weights<0>(lane, lx, colw + cb, w);
-                        else diag_weights<1>(lane, lx, colw + cb, w);
+                        diag_weights(lane, half, lx, colw + cb, w);
                     } else {
                         // a masked key (s > t) may give an infinite factor; the select drops it
 #pragma unroll
