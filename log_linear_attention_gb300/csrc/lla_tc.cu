@@ -303,21 +303,61 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 32) tmem_ld32(tmem + lane_base + s * DV + half * DH + c0, sv + c0);
         const float ge = exp2f(g2_sh[u]);
-        auto store_node = [&](int l, int m, const float* v) {
-            __nv_bfloat16* dst = nodes + (static_cast<size_t>(bh) * node_count + lo.off[l] + (m >> 1)) * msz +
-                                 static_cast<size_t>(row) * DV + half * DH;
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+        // A thread holds DH consecutive values of one row (its TMEM lane); stored as they are,
+        // every 16-byte store of a warp would touch 32 rows. The four lanes of a group swap
+        // their 16-byte chunks (a 4 x 4 transpose, two xor-shuffle stages), so that in store i
+        // the group writes row 4 g + i whole: 8 rows of 64 contiguous bytes per warp store.
+        auto store_rows = [&](uint8_t* base, size_t row_stride, uint4 (&x)[4]) {
+            const int c = lane & 3;
 #pragma unroll
-            for (int c = 0; c < DH / 8; c++)
-                d4[c] = make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
-                                   pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+            for (int st = 2; st >= 1; st >>= 1) {
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    if (j & st) continue;
+                    const bool hi = (c & st) != 0;
+                    uint4 snd = hi ? x[j] : x[j + st];
+                    uint4 rcv;
+                    rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, st);
+                    rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, st);
+                    rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, st);
+                    rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, st);
+                    if (hi) x[j] = rcv;
+                    else x[j + st] = rcv;
+                }
+            }
+            // lane 4 g + c now holds chunk c of rows 4 g + 0..3 (row r = this warp's rows)
+            const int r0 = (row & ~31) + (lane & ~3);
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                *reinterpret_cast<uint4*>(base + static_cast<size_t>(r0 + i) * row_stride + 16 * c) = x[i];
+        };
+        auto store_node = [&](int l, int m, const float* v) {
+            uint8_t* dst = reinterpret_cast<uint8_t*>(nodes + (static_cast<size_t>(bh) * node_count + lo.off[l] + (m >> 1)) * msz +
+                                                      half * DH);
+#pragma unroll
+            for (int b = 0; b < DH / 32; b++) {  // columns [32 b, 32 b + 32) of this thread's DH
+                uint4 x[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const float* w = v + 32 * b + 8 * c;
+                    x[c] = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]),
+                                      pack_bf16(w[6], w[7]));
+                }
+                store_rows(dst + 64 * b, DV * sizeof(__nv_bfloat16), x);
+            }
         };
         auto store_seg = [&](const float* v) {
-            float* dst = seg_tot + (static_cast<size_t>(bh) * ((NT + kSegTiles - 1) / kSegTiles) + seg) * msz +
-                         static_cast<size_t>(row) * DV + half * DH;
-            float4* d4 = reinterpret_cast<float4*>(dst);
+            uint8_t* dst = reinterpret_cast<uint8_t*>(seg_tot + (static_cast<size_t>(bh) * ((NT + kSegTiles - 1) / kSegTiles) + seg) * msz +
+                                                      half * DH);
 #pragma unroll
-            for (int c = 0; c < DH / 4; c++) d4[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            for (int hh = 0; hh < DH / 16; hh++) {  // columns [16 hh, 16 hh + 16) of this thread's DH
+                uint4 x[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+                    x[c] = make_uint4(__float_as_uint(v[16 * hh + 4 * c]), __float_as_uint(v[16 * hh + 4 * c + 1]),
+                                      __float_as_uint(v[16 * hh + 4 * c + 2]), __float_as_uint(v[16 * hh + 4 * c + 3]));
+                store_rows(dst + 64 * hh, DV * sizeof(float), x);
+            }
         };
         // level 0: the tile itself
         if ((tile & 1) == 0 && tile + 1 < NTi) store_node(0, tile, sv);
