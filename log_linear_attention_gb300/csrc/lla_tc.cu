@@ -113,6 +113,29 @@ __global__ void __launch_bounds__(1024) seq_table_kernel(const int32_t* __restri
     if (n_seq == 0 && tid == 0) tile_prefix[0] = 0;
 }
 
+// Four lanes 4 g + c (c = 0..3) each hold four 16-byte chunks x[0..3] of their own row. After
+// the call lane 4 g + c holds chunk c of the rows of lanes 4 g + 0..3, in that order: a 4 x 4
+// transpose in two xor-shuffle stages. A warp then stores whole 64-byte runs of 8 rows per
+// store instead of 16 bytes of 32 rows. Every lane of the warp takes part.
+__device__ __forceinline__ void lane_group_transpose(uint4 (&x)[4], int lane) {
+#pragma unroll
+    for (int st = 2; st >= 1; st >>= 1) {
+        const bool hi = (lane & st) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (j & st) continue;
+            const uint4 snd = hi ? x[j] : x[j + st];
+            uint4 rcv;
+            rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, st);
+            rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, st);
+            rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, st);
+            rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, st);
+            if (hi) x[j] = rcv;
+            else x[j + st] = rcv;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ tc_nodes
 
 template <int DV>
@@ -309,23 +332,7 @@ __global__ void __launch_bounds__(256, 2)
         // the group writes row 4 g + i whole: 8 rows of 64 contiguous bytes per warp store.
         auto store_rows = [&](uint8_t* base, size_t row_stride, uint4 (&x)[4]) {
             const int c = lane & 3;
-#pragma unroll
-            for (int st = 2; st >= 1; st >>= 1) {
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    if (j & st) continue;
-                    const bool hi = (c & st) != 0;
-                    uint4 snd = hi ? x[j] : x[j + st];
-                    uint4 rcv;
-                    rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, st);
-                    rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, st);
-                    rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, st);
-                    rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, st);
-                    if (hi) x[j] = rcv;
-                    else x[j + st] = rcv;
-                }
-            }
-            // lane 4 g + c now holds chunk c of rows 4 g + 0..3 (row r = this warp's rows)
+            lane_group_transpose(x, lane);
             const int r0 = (row & ~31) + (lane & ~3);
 #pragma unroll
             for (int i = 0; i < 4; i++)
@@ -1510,14 +1517,20 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 if (lane == 0) mbar_arrive(&lv_free[g]);
             }
             if (!ok) break;
-            if (t < live) {  // a packed sequence's last tile ends inside the tile
-                uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV + half * DH);
+            {
+                // rows 4 g + i of the lane group, chunk c = lane & 3 each (whole 64-byte runs);
+                // rows past a packed sequence's end are not stored
+                uint4 x[4];
 #pragma unroll
-                for (int c8 = 0; c8 < DH / 8; c8++)
-                    dst[c8] = make_uint4(pack_bf16(acc[8 * c8], acc[8 * c8 + 1]),
-                                         pack_bf16(acc[8 * c8 + 2], acc[8 * c8 + 3]),
-                                         pack_bf16(acc[8 * c8 + 4], acc[8 * c8 + 5]),
-                                         pack_bf16(acc[8 * c8 + 6], acc[8 * c8 + 7]));
+                for (int c8 = 0; c8 < 4; c8++)
+                    x[c8] = make_uint4(pack_bf16(acc[8 * c8], acc[8 * c8 + 1]), pack_bf16(acc[8 * c8 + 2], acc[8 * c8 + 3]),
+                                       pack_bf16(acc[8 * c8 + 4], acc[8 * c8 + 5]), pack_bf16(acc[8 * c8 + 6], acc[8 * c8 + 7]));
+                lane_group_transpose(x, lane);
+                const int tg = q32 + (lane & ~3);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    if (tg + i < live)
+                        *reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + tg + i) * DV + half * DH + 8 * (lane & 3)) = x[i];
             }
         }
     }
