@@ -113,29 +113,6 @@ __global__ void __launch_bounds__(1024) seq_table_kernel(const int32_t* __restri
     if (n_seq == 0 && tid == 0) tile_prefix[0] = 0;
 }
 
-// Four lanes 4 g + c (c = 0..3) each hold four 16-byte chunks x[0..3] of their own row. After
-// the call lane 4 g + c holds chunk c of the rows of lanes 4 g + 0..3, in that order: a 4 x 4
-// transpose in two xor-shuffle stages. A warp then stores whole 64-byte runs of 8 rows per
-// store instead of 16 bytes of 32 rows. Every lane of the warp takes part.
-__device__ __forceinline__ void lane_group_transpose(uint4 (&x)[4], int lane) {
-#pragma unroll
-    for (int st = 2; st >= 1; st >>= 1) {
-        const bool hi = (lane & st) != 0;
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            if (j & st) continue;
-            const uint4 snd = hi ? x[j] : x[j + st];
-            uint4 rcv;
-            rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, st);
-            rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, st);
-            rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, st);
-            rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, st);
-            if (hi) x[j] = rcv;
-            else x[j + st] = rcv;
-        }
-    }
-}
-
 // ------------------------------------------------------------------ tc_nodes
 
 template <int DV>
@@ -1010,11 +987,22 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[b]);
-            uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + t) * DV + half * DH);
+            // whole 64-byte runs of 8 rows per warp store (rows q32 + (lane & ~3) + i)
 #pragma unroll
-            for (int c = 0; c < DH / 8; c++)
-                dst[c] = make_uint4(pack_bf16(acc[8 * c], acc[8 * c + 1]), pack_bf16(acc[8 * c + 2], acc[8 * c + 3]),
-                                    pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
+            for (int cb = 0; cb < DH / 32; cb++) {
+                uint4 x[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const float* a = acc + 32 * cb + 8 * c;
+                    x[c] = make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
+                                      pack_bf16(a[6], a[7]));
+                }
+                lane_group_transpose(x, lane);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    *reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + q32 + (lane & ~3) + i) * DV + half * DH +
+                                              32 * cb + 8 * (lane & 3)) = x[i];
+            }
         };
 
         for (int k = 0;; k++) {

@@ -304,6 +304,29 @@ __device__ __forceinline__ float block_scan128(float x, float* warp_tot) {
     return incl + base;
 }
 
+// Four lanes 4 g + c (c = 0..3) each hold four 16-byte chunks x[0..3] of their own row. After
+// the call lane 4 g + c holds chunk c of the rows of lanes 4 g + 0..3, in that order: a 4 x 4
+// transpose in two xor-shuffle stages. A warp then stores whole 64-byte runs of 8 rows per
+// store instead of 16 bytes of 32 rows. Every lane of the warp takes part.
+__device__ __forceinline__ void lane_group_transpose(uint4 (&x)[4], int lane) {
+#pragma unroll
+    for (int st = 2; st >= 1; st >>= 1) {
+        const bool hi = (lane & st) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (j & st) continue;
+            const uint4 snd = hi ? x[j] : x[j + st];
+            uint4 rcv;
+            rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, st);
+            rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, st);
+            rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, st);
+            rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, st);
+            if (hi) x[j] = rcv;
+            else x[j + st] = rcv;
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);

@@ -540,12 +540,12 @@ __global__ void __launch_bounds__(512, 1)
             // a run held whole by this share is the slot's only writer; a cut one leaves a piece
             const bool cs = run == 0 && cut_start;
             const bool ce = f + 1 == t1 && t1 < total && nc.bh == cur.bh && nc.lvl == cur.lvl;
-            float4* dst;
+            float* slot;  // row 0 of the dk x DV slot (or piece) this run is drained into
             if (!cs && !ce) {
-                dst = reinterpret_cast<float4*>(states + ((static_cast<size_t>(bh) * Lmax + l) * kDk + d) * DV);
+                slot = states + (static_cast<size_t>(bh) * Lmax + l) * kDk * DV;
             } else {
                 const int kind = cs ? 0 : 1;
-                dst = reinterpret_cast<float4*>(pieces + (static_cast<size_t>(2 * blockIdx.x + kind) * kDk + d) * DV);
+                slot = pieces + static_cast<size_t>(2 * blockIdx.x + kind) * kDk * DV;
                 if (warp == 12 && lane == 0) {
                     piece_slot[2 * blockIdx.x + kind] = bh * Lmax + l;
                     piece_flags[2 * blockIdx.x + kind] = (cs ? 1 : 0) | (ce ? 2 : 0);
@@ -556,10 +556,24 @@ __global__ void __launch_bounds__(512, 1)
                 float x[32], y[32];
                 tmem_ld32(tmem + lane_base + buf * C::kAccCols + c0, x);
                 tmem_ld32(tmem + lane_base + buf * C::kAccCols + DV + c0, y);
+                // 16-byte chunks of this row, transposed within lane groups so that each store
+                // writes 64 contiguous bytes of 8 rows (row quad * 32 + (lane & ~3) + i)
 #pragma unroll
-                for (int j = 0; j < 8; j++)
-                    dst[c0 / 4 + j] = make_float4(x[4 * j] + y[4 * j], x[4 * j + 1] + y[4 * j + 1],
-                                                  x[4 * j + 2] + y[4 * j + 2], x[4 * j + 3] + y[4 * j + 3]);
+                for (int hh = 0; hh < 2; hh++) {
+                    uint4 ch[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const int e = 16 * hh + 4 * j;
+                        ch[j] = make_uint4(__float_as_uint(x[e] + y[e]), __float_as_uint(x[e + 1] + y[e + 1]),
+                                           __float_as_uint(x[e + 2] + y[e + 2]), __float_as_uint(x[e + 3] + y[e + 3]));
+                    }
+                    lane_group_transpose(ch, lane);
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int r = quad * 32 + (lane & ~3) + i;
+                        *reinterpret_cast<uint4*>(slot + static_cast<size_t>(r) * DV + c0 + 16 * hh + 4 * (lane & 3)) = ch[i];
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
