@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(128, 2)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full_a + 4);
     volatile int* fail = reinterpret_cast<volatile int*>(full_a + 5);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (pad > static_cast<uint32_t>(C::kSlack)) {  // base alignment below the assumed 128 bytes
         if (tid == 0) record_error(err, kDevBadInput);
         return;
@@ -161,6 +161,44 @@ __global__ void __launch_bounds__(128, 2)
         for (int d = 0; d < DV; d++) *reinterpret_cast<float*>(base + d * 128 + ((c ^ (d & 7)) << 4)) = x[d];
     };
 
+    // Row-major fp32 rows of DV values, one row per thread of a warp with consecutive rows
+    // (`rows` points at the warp's first row, `live` rows exist): loaded and stored in whole
+    // 64-byte runs of 8 rows per warp access, the chunks swapped within lane groups.
+    auto load_rows = [&](const float* rows, int live, float* x) {
+        const int g0 = lane & ~3, c = lane & 3;
+#pragma unroll
+        for (int q = 0; q < DV / 16; q++) {
+            uint4 y[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                y[i] = g0 + i < live ? *reinterpret_cast<const uint4*>(rows + (g0 + i) * DV + 16 * q + 4 * c)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            lane_group_transpose(y, lane);
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                x[16 * q + 4 * j] = __uint_as_float(y[j].x);
+                x[16 * q + 4 * j + 1] = __uint_as_float(y[j].y);
+                x[16 * q + 4 * j + 2] = __uint_as_float(y[j].z);
+                x[16 * q + 4 * j + 3] = __uint_as_float(y[j].w);
+            }
+        }
+    };
+    auto store_rows = [&](float* rows, int live, const float* x) {
+        const int g0 = lane & ~3, c = lane & 3;
+#pragma unroll
+        for (int q = 0; q < DV / 16; q++) {
+            uint4 y[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                y[j] = make_uint4(__float_as_uint(x[16 * q + 4 * j]), __float_as_uint(x[16 * q + 4 * j + 1]),
+                                  __float_as_uint(x[16 * q + 4 * j + 2]), __float_as_uint(x[16 * q + 4 * j + 3]));
+            lane_group_transpose(y, lane);
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                if (g0 + i < live) *reinterpret_cast<uint4*>(rows + (g0 + i) * DV + 16 * q + 4 * c) = y[i];
+        }
+    };
+
     if (tid == 0 && static_cast<int>(blockIdx.x) < n_chains) {
         int bh, xi, b0, b1;
         chain_range(blockIdx.x, bh, xi, b0, b1);
@@ -184,12 +222,7 @@ __global__ void __launch_bounds__(128, 2)
         {
             // X = node (p, m); rows dk..127 are zero
             float x[DV];
-            const float4* src = reinterpret_cast<const float4*>(node_ptr(bh, p, m) + static_cast<size_t>(tid) * DV);
-#pragma unroll
-            for (int c4 = 0; c4 < DV / 4; c4++) {
-                const float4 f = tid < dk ? src[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
-                x[4 * c4] = f.x; x[4 * c4 + 1] = f.y; x[4 * c4 + 2] = f.z; x[4 * c4 + 3] = f.w;
-            }
+            load_rows(node_ptr(bh, p, m) + static_cast<size_t>(32 * warp) * DV, dk - 32 * warp, x);
             tmem_st32(tX, x);
             tmem_st32(tX + 32, x + 32);
             stage_xt(x);
@@ -209,13 +242,11 @@ __global__ void __launch_bounds__(128, 2)
             const size_t row0 = static_cast<size_t>(bh) * T + static_cast<size_t>(jc) * C::kC;
             // the read's lambda and accumulator row, loaded while MMA1 runs
             float lw = 0.f;
-            float4 oa[DV / 4];
-            if (tid >= C::kC) {
+            float oa[DV];
+            if (tid >= C::kC) {  // warps 2 and 3 whole
                 const size_t t = row0 + (tid - C::kC);
                 lw = lambda[t * L + lev] * Gam;
-                const float4* o = reinterpret_cast<const float4*>(oacc + t * DV);
-#pragma unroll
-                for (int c4 = 0; c4 < DV / 4; c4++) oa[c4] = o[c4];
+                load_rows(oacc + (row0 + 32 * (warp - 2)) * DV, 32, oa);
             }
             if (tid == 0 && wait(full_a, ph)) {
                 tc_fence_after();
@@ -257,11 +288,9 @@ __global__ void __launch_bounds__(128, 2)
                     }
                 }
             } else {
-                float4* o = reinterpret_cast<float4*>(oacc + (row0 + (tid - C::kC)) * DV);
 #pragma unroll
-                for (int c4 = 0; c4 < DV / 4; c4++)
-                    o[c4] = make_float4(fmaf(lw, v[4 * c4], oa[c4].x), fmaf(lw, v[4 * c4 + 1], oa[c4].y),
-                                        fmaf(lw, v[4 * c4 + 2], oa[c4].z), fmaf(lw, v[4 * c4 + 3], oa[c4].w));
+                for (int e = 0; e < DV; e++) oa[e] = fmaf(lw, v[e], oa[e]);
+                store_rows(oacc + (row0 + 32 * (warp - 2)) * DV, 32, oa);
             }
             if (!carry) {
                 // no MMA2: K of this step arrived unused; the next step's K may take its buffer
@@ -298,16 +327,13 @@ __global__ void __launch_bounds__(128, 2)
             tmem_ld32(tX + 32, v + 32);
             if (!last) {
                 stage_xt(v);
-            } else if (tid < dk) {
-                // node (p + 1, m / 2) = Gamma X^ + node (p, m + 1)
-                const float4* sib = reinterpret_cast<const float4*>(node_ptr(bh, p, m + 1) + static_cast<size_t>(tid) * DV);
-                float4* dst = reinterpret_cast<float4*>(node_ptr(bh, p + 1, xi) + static_cast<size_t>(tid) * DV);
+            } else {
+                // node (p + 1, m / 2) = Gamma X^ + node (p, m + 1) (rows dk.. do not exist)
+                float sib[DV];
+                load_rows(node_ptr(bh, p, m + 1) + static_cast<size_t>(32 * warp) * DV, dk - 32 * warp, sib);
 #pragma unroll
-                for (int c4 = 0; c4 < DV / 4; c4++) {
-                    const float4 b = sib[c4];
-                    dst[c4] = make_float4(fmaf(Gam, v[4 * c4], b.x), fmaf(Gam, v[4 * c4 + 1], b.y),
-                                          fmaf(Gam, v[4 * c4 + 2], b.z), fmaf(Gam, v[4 * c4 + 3], b.w));
-                }
+                for (int e = 0; e < DV; e++) sib[e] = fmaf(Gam, v[e], sib[e]);
+                store_rows(node_ptr(bh, p + 1, xi) + static_cast<size_t>(32 * warp) * DV, dk - 32 * warp, sib);
             }
             fence_async_smem();
             tc_fence_before();
@@ -818,17 +844,31 @@ __global__ void __launch_bounds__(256, 2)
                         make_uint4(l[0], l[1], l[2], l[3]);
                 }
             } else if (N > 1) {
-                float4* dst = reinterpret_cast<float4*>(oacc + (row0 + t) * DV + 32 * half);
+                // whole 64-byte runs of 8 rows per warp store (rows (t & ~3) + i of the lane group)
+                float* dst = oacc + (row0 + (t & ~3)) * DV + 32 * half + 4 * (lane & 3);
 #pragma unroll
-                for (int c4 = 0; c4 < 8; c4++)
-                    dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                for (int hh = 0; hh < 2; hh++) {
+                    uint4 y[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const float* a = v + 16 * hh + 4 * j;
+                        y[j] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                          __float_as_uint(a[3]));
+                    }
+                    lane_group_transpose(y, lane);
+#pragma unroll
+                    for (int i = 0; i < 4; i++) *reinterpret_cast<uint4*>(dst + i * DV + 16 * hh) = y[i];
+                }
             } else {
-                uint4* dst = reinterpret_cast<uint4*>(out + (row0 + t) * DV + 32 * half);
+                uint4 y[4];
 #pragma unroll
                 for (int c8 = 0; c8 < 4; c8++)
-                    dst[c8] = make_uint4(pack_bf16(v[8 * c8], v[8 * c8 + 1]), pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]),
-                                         pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]),
-                                         pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
+                    y[c8] = make_uint4(pack_bf16(v[8 * c8], v[8 * c8 + 1]), pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]),
+                                       pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]), pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
+                lane_group_transpose(y, lane);
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    *reinterpret_cast<uint4*>(out + (row0 + (t & ~3) + i) * DV + 32 * half + 8 * (lane & 3)) = y[i];
             }
         }
         if (N == 1) break;
@@ -865,13 +905,25 @@ __global__ void __launch_bounds__(256, 2)
             const int c0 = 32 * (warp >> 2);
             float v[32];
             tmem_ld32(tmem + lane_base + c0, v);
-            if (i < dk) {
-                float4* dst = reinterpret_cast<float4*>(
-                    nodes + (static_cast<size_t>(bh) * node_count + j) * static_cast<size_t>(dk) * DV +
-                    static_cast<size_t>(i) * DV + c0);
+            {
+                // whole 64-byte runs of 8 rows per warp store; rows dk.. do not exist
+                const int i0 = (warp & 3) * 32 + (lane & ~3);
+                float* dst = nodes + (static_cast<size_t>(bh) * node_count + j) * static_cast<size_t>(dk) * DV +
+                             static_cast<size_t>(i0) * DV + c0 + 4 * (lane & 3);
 #pragma unroll
-                for (int c4 = 0; c4 < 8; c4++)
-                    dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                for (int hh = 0; hh < 2; hh++) {
+                    uint4 y[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const float* a = v + 16 * hh + 4 * e;
+                        y[e] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                          __float_as_uint(a[3]));
+                    }
+                    lane_group_transpose(y, lane);
+#pragma unroll
+                    for (int r = 0; r < 4; r++)
+                        if (i0 + r < dk) *reinterpret_cast<uint4*>(dst + r * DV + 16 * hh) = y[r];
+                }
             }
         }
     } while (false);
