@@ -506,8 +506,23 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_level_kernel(
 
 template <typename T>
 __global__ void gdn_finalize_kernel(const float* __restrict__ oacc, T* __restrict__ out, size_t n) {
-    for (size_t x = (size_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (size_t)gridDim.x * blockDim.x)
-        store_f(out + x, oacc[x]);
+    // four elements a thread and step (16-byte loads; 8- or 16-byte stores), then the tail
+    const size_t stride = (size_t)gridDim.x * blockDim.x, first = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t n4 = n / 4;
+    const float4* src = reinterpret_cast<const float4*>(oacc);
+    for (size_t x = first; x < n4; x += stride) {
+        const float4 a = src[x];
+        if constexpr (sizeof(T) == 2) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t*>(&lo);
+            w.y = *reinterpret_cast<const uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(out)[x] = w;
+        } else {
+            reinterpret_cast<float4*>(out)[x] = a;
+        }
+    }
+    for (size_t x = 4 * n4 + first; x < n; x += stride) store_f(out + x, oacc[x]);
 }
 
 template <typename T>
@@ -560,7 +575,7 @@ cudaError_t gdn_forward_t(const GdnPlan& pl, int dtype, const void* q, const voi
         }
     }
     const size_t n = (size_t)BH * pl.T * pl.dv;
-    const size_t blocks = (n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16;
+    const size_t blocks = (n / 4 + 255) / 256 < 152 * 8 ? (n / 4 + 255) / 256 + 1 : 152 * 8;
     gdn_finalize_kernel<T><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         oacc, static_cast<T*>(out), n);
     note_launch(stream, "gdn_finalize");
