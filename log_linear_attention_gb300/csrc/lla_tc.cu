@@ -185,11 +185,14 @@ __global__ void __launch_bounds__(256, 2)
         uint8_t* st = stage_ptr(s);
         const int r0 = rowbase + (tile0 + u) * kTile;
         mbar_expect_tx(&bar_full[s], kTxBytes);
-        tma_load_2d(st, &tm_k, &bar_full[s], 0, r0);
-        tma_load_2d(st + kPanelBytes, &tm_k, &bar_full[s], 64, r0);
+        // K and V are read again only by the output kernel, after every node kernel: keeping them
+        // in L2 would only push out the segment totals and nodes that are read back sooner
+        const uint64_t pol = l2_evict_first();
+        tma_load_2d_hint(st, &tm_k, &bar_full[s], 0, r0, pol);
+        tma_load_2d_hint(st + kPanelBytes, &tm_k, &bar_full[s], 64, r0, pol);
 #pragma unroll
         for (int p = 0; p < DV / 64; p++)
-            tma_load_2d(st + S::kKBytes + p * kPanelBytes, &tm_v, &bar_full[s], 64 * p, r0);
+            tma_load_2d_hint(st + S::kKBytes + p * kPanelBytes, &tm_v, &bar_full[s], 64 * p, r0, pol);
     };
     if (tid == 0) {
         issue_tile(0);
