@@ -52,13 +52,14 @@ struct LvCfg {
     static constexpr uint32_t kKBytes = 2 * kKPanel;
 };
 
-// Persistent: grid min(chains, 2 per SM), 128 threads (thread = TMEM lane), two CTAs per SM.
+// Persistent: grid min(chains, 2 per SM), 256 threads (two per TMEM lane, each with half of the
+// dv columns), two CTAs per SM.
 // A CTA walks the read nodes c = blockIdx.x, blockIdx.x + gridDim.x, ... of level p (chain c:
 // head c / n_even, read node m = 2 (c % n_even)), step by step through each chain's chunks. The
 // copies of the next step in that walk (the next chunk of the chain, else the first chunk of
 // the CTA's next chain) are issued as soon as their buffers are free: [W; Q~] once MMA1 has
 // read the stage, K once MMA2 has (or once the step is over, when it needs no MMA2).
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(256, 2)
     gdn_level_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_qt,
                         const __grid_constant__ CUtensorMap tm_k, float* __restrict__ nodes,
                         const float* __restrict__ gam, const float* __restrict__ lambda, float* __restrict__ oacc,
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(128, 2)
                         const __grid_constant__ GdnTcLevels lo, int* err) {
     using C = LvCfg;
     constexpr int DV = C::kDV;
+    constexpr int DH = DV / 2;  // columns of a thread: two threads per TMEM lane
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t* smem = smem_raw + pad;
@@ -77,6 +79,9 @@ __global__ void __launch_bounds__(128, 2)
     volatile int* fail = reinterpret_cast<volatile int*>(full_a + 5);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = tid & 127;   // TMEM lane: a dk row of X, a token row of Y (< 64) or of R
+    const int half = tid >> 7;   // which DH columns of the row
+    const int wq = warp & 3;     // lane quadrant of this warp
     if (pad > static_cast<uint32_t>(C::kSlack)) {  // base alignment below the assumed 128 bytes
         if (tid == 0) record_error(err, kDevBadInput);
         return;
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(128, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tD = tmem + lane_base;       // MMA1 result, columns [0, 64)
     const uint32_t tX = tmem + lane_base + 64;  // carried node, columns [64, 128)
     constexpr uint32_t kIdA = idesc_tf32(128, DV);        // [W; Q~] (K-major) x X (K-major)
@@ -152,27 +157,33 @@ __global__ void __launch_bounds__(128, 2)
         record_error(err, kDevTimeout);
         return false;
     };
-    // X row i (i = tid, a dk row) into the K-major fp32 staging of X^T: element (d, i) sits in
-    // panel i / 32, row d, 16-byte chunk ((i % 32) / 4) ^ (d % 8), word i % 4
+    // X row i (i = row, a dk row; this thread's DH columns d) into the K-major fp32 staging of
+    // X^T: element (d, i) sits in panel i / 32, row d, 16-byte chunk ((i % 32) / 4) ^ (d % 8),
+    // word i % 4
     auto stage_xt = [&](const float* x) {
-        uint8_t* base = smem + C::kX + (tid >> 5) * C::kXPanel + (tid & 3) * 4;
-        const int c = (tid & 31) >> 2;
+        uint8_t* base = smem + C::kX + (row >> 5) * C::kXPanel + (row & 3) * 4;
+        const int c = (row & 31) >> 2;
 #pragma unroll
-        for (int d = 0; d < DV; d++) *reinterpret_cast<float*>(base + d * 128 + ((c ^ (d & 7)) << 4)) = x[d];
+        for (int e = 0; e < DH; e++) {
+            const int d = DH * half + e;
+            *reinterpret_cast<float*>(base + d * 128 + ((c ^ (d & 7)) << 4)) = x[e];
+        }
     };
 
-    // Row-major fp32 rows of DV values, one row per thread of a warp with consecutive rows
-    // (`rows` points at the warp's first row, `live` rows exist): loaded and stored in whole
-    // 64-byte runs of 8 rows per warp access, the chunks swapped within lane groups.
+    // This thread's DH columns of row-major fp32 rows of DV values, one row per thread of a warp
+    // with consecutive rows (`rows` points at the warp's first row, `live` rows exist): loaded
+    // and stored in whole 64-byte runs of 8 rows per warp access, the chunks swapped within lane
+    // groups.
     auto load_rows = [&](const float* rows, int live, float* x) {
         const int g0 = lane & ~3, c = lane & 3;
 #pragma unroll
-        for (int q = 0; q < DV / 16; q++) {
+        for (int q = 0; q < DH / 16; q++) {
             uint4 y[4];
 #pragma unroll
             for (int i = 0; i < 4; i++)
-                y[i] = g0 + i < live ? *reinterpret_cast<const uint4*>(rows + (g0 + i) * DV + 16 * q + 4 * c)
-                                     : make_uint4(0u, 0u, 0u, 0u);
+                y[i] = g0 + i < live
+                           ? *reinterpret_cast<const uint4*>(rows + (g0 + i) * DV + DH * half + 16 * q + 4 * c)
+                           : make_uint4(0u, 0u, 0u, 0u);
             lane_group_transpose(y, lane);
 #pragma unroll
             for (int j = 0; j < 4; j++) {
@@ -186,7 +197,7 @@ __global__ void __launch_bounds__(128, 2)
     auto store_rows = [&](float* rows, int live, const float* x) {
         const int g0 = lane & ~3, c = lane & 3;
 #pragma unroll
-        for (int q = 0; q < DV / 16; q++) {
+        for (int q = 0; q < DH / 16; q++) {
             uint4 y[4];
 #pragma unroll
             for (int j = 0; j < 4; j++)
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(128, 2)
             lane_group_transpose(y, lane);
 #pragma unroll
             for (int i = 0; i < 4; i++)
-                if (g0 + i < live) *reinterpret_cast<uint4*>(rows + (g0 + i) * DV + 16 * q + 4 * c) = y[i];
+                if (g0 + i < live) *reinterpret_cast<uint4*>(rows + (g0 + i) * DV + DH * half + 16 * q + 4 * c) = y[i];
         }
     };
 
@@ -221,10 +232,9 @@ __global__ void __launch_bounds__(128, 2)
         }
         {
             // X = node (p, m); rows dk..127 are zero
-            float x[DV];
-            load_rows(node_ptr(bh, p, m) + static_cast<size_t>(32 * warp) * DV, dk - 32 * warp, x);
-            tmem_st32(tX, x);
-            tmem_st32(tX + 32, x + 32);
+            float x[DH];
+            load_rows(node_ptr(bh, p, m) + static_cast<size_t>(32 * wq) * DV, dk - 32 * wq, x);
+            tmem_st32(tX + DH * half, x);
             stage_xt(x);
         }
         fence_async_smem();
@@ -242,11 +252,11 @@ __global__ void __launch_bounds__(128, 2)
             const size_t row0 = static_cast<size_t>(bh) * T + static_cast<size_t>(jc) * C::kC;
             // the read's lambda and accumulator row, loaded while MMA1 runs
             float lw = 0.f;
-            float oa[DV];
-            if (tid >= C::kC) {  // warps 2 and 3 whole
-                const size_t t = row0 + (tid - C::kC);
+            float oa[DH];
+            if (row >= C::kC) {  // warps 2, 3, 6 and 7 whole
+                const size_t t = row0 + (row - C::kC);
                 lw = lambda[t * L + lev] * Gam;
-                load_rows(oacc + (row0 + 32 * (warp - 2)) * DV, 32, oa);
+                load_rows(oacc + (row0 + 32 * (wq - 2)) * DV, 32, oa);
             }
             if (tid == 0 && wait(full_a, ph)) {
                 tc_fence_after();
@@ -265,16 +275,16 @@ __global__ void __launch_bounds__(128, 2)
             __syncthreads();
             tc_fence_after();
             if (*fail) break;
-            float v[DV];
-            tmem_ld32(tD, v);
-            tmem_ld32(tD + 32, v + 32);
-            if (tid < C::kC) {
+            float v[DH];
+            tmem_ld32(tD + DH * half, v);
+            if (row < C::kC) {
                 if (carry) {
-                    // -Y row tid as bf16 hi + lo, MN-major rows of 64 dv (one 128-byte row per token)
+                    // -Y row `row` as bf16 hi + lo, MN-major rows of 64 dv (one 128-byte row per
+                    // token; this thread's DH columns are chunks 4 half .. 4 half + 3)
                     uint8_t* hi = smem + C::kX;
                     uint8_t* lo_ = smem + C::kX + C::kXPanel;
 #pragma unroll
-                    for (int c8 = 0; c8 < DV / 8; c8++) {
+                    for (int c8 = 0; c8 < DH / 8; c8++) {
                         uint32_t h[4], l[4];
 #pragma unroll
                         for (int e = 0; e < 4; e++) {
@@ -283,14 +293,15 @@ __global__ void __launch_bounds__(128, 2)
                             const float2 hf = unpack_bf16(h[e]);
                             l[e] = pack_bf16(a - hf.x, b - hf.y);
                         }
-                        *reinterpret_cast<uint4*>(hi + sw128_off(tid, c8)) = make_uint4(h[0], h[1], h[2], h[3]);
-                        *reinterpret_cast<uint4*>(lo_ + sw128_off(tid, c8)) = make_uint4(l[0], l[1], l[2], l[3]);
+                        const int ch = (DH / 8) * half + c8;
+                        *reinterpret_cast<uint4*>(hi + sw128_off(row, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+                        *reinterpret_cast<uint4*>(lo_ + sw128_off(row, ch)) = make_uint4(l[0], l[1], l[2], l[3]);
                     }
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < DV; e++) oa[e] = fmaf(lw, v[e], oa[e]);
-                store_rows(oacc + (row0 + 32 * (warp - 2)) * DV, 32, oa);
+                for (int e = 0; e < DH; e++) oa[e] = fmaf(lw, v[e], oa[e]);
+                store_rows(oacc + (row0 + 32 * (wq - 2)) * DV, 32, oa);
             }
             if (!carry) {
                 // no MMA2: K of this step arrived unused; the next step's K may take its buffer
@@ -323,17 +334,16 @@ __global__ void __launch_bounds__(128, 2)
             tc_fence_after();
             if (*fail) break;
             Gam *= gam[static_cast<size_t>(bh) * N + jc];
-            tmem_ld32(tX, v);
-            tmem_ld32(tX + 32, v + 32);
+            tmem_ld32(tX + DH * half, v);
             if (!last) {
                 stage_xt(v);
             } else {
                 // node (p + 1, m / 2) = Gamma X^ + node (p, m + 1) (rows dk.. do not exist)
-                float sib[DV];
-                load_rows(node_ptr(bh, p, m + 1) + static_cast<size_t>(32 * warp) * DV, dk - 32 * warp, sib);
+                float sib[DH];
+                load_rows(node_ptr(bh, p, m + 1) + static_cast<size_t>(32 * wq) * DV, dk - 32 * wq, sib);
 #pragma unroll
-                for (int e = 0; e < DV; e++) sib[e] = fmaf(Gam, v[e], sib[e]);
-                store_rows(node_ptr(bh, p + 1, xi) + static_cast<size_t>(32 * warp) * DV, dk - 32 * warp, sib);
+                for (int e = 0; e < DH; e++) sib[e] = fmaf(Gam, v[e], sib[e]);
+                store_rows(node_ptr(bh, p + 1, xi) + static_cast<size_t>(32 * wq) * DV, dk - 32 * wq, sib);
             }
             fence_async_smem();
             tc_fence_before();
@@ -997,7 +1007,7 @@ cudaError_t gdn_levels_tc(const GdnPlan& pl, const void* k, const float* Wg, con
         if (n_even <= 0) continue;
         const int n_chains = static_cast<int>(BH) * n_even;
         const int grid = n_chains < 2 * sms ? n_chains : 2 * sms;
-        gdn_level_tc_kernel<<<grid, 128, smem, stream>>>(tw, tq, tk, nodes, gam, lambda, oacc, pl.T, pl.N, pl.dk, L,
+        gdn_level_tc_kernel<<<grid, 256, smem, stream>>>(tw, tq, tk, nodes, gam, lambda, oacc, pl.T, pl.N, pl.dk, L,
                                                          c_log2 + 1 + p, p, pl.P, pl.node_count, n_even, n_chains,
                                                          lo, err);
         note_launch(stream, "gdn_level_tc");
