@@ -911,7 +911,6 @@ __global__ void __launch_bounds__(256, 2)
         if (*fail) break;
         {
             // the chunk's state: TMEM lane i = dk row i; warps 0..3 columns 0..31, warps 4..7 32..63
-            const int i = (warp & 3) * 32 + lane;
             const int c0 = 32 * (warp >> 2);
             float v[32];
             tmem_ld32(tmem + lane_base + c0, v);

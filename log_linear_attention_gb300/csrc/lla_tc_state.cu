@@ -514,7 +514,6 @@ __global__ void __launch_bounds__(512, 1)
         }
     } else if (warp >= 12) {
         const int quad = warp & 3;
-        const int d = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         int run = 0;
         Cursor c = cursor_at(t0);
