@@ -1023,28 +1023,6 @@ __global__ void __launch_bounds__(OutCfg<DV>::kThreads, 1)
 
 // ------------------------------------------------------------------ tc_output_pp (dv = 64)
 
-// Ping-pong output kernel for dv = 64: two independent tile pipelines share one CTA.
-// Epilogue group g (eight warps, two per TMEM lane quadrant; thread = query row)
-// owns input stage g and TMEM columns [256 g, 256 g + 256) and takes every other
-// tile the CTA claims, so one group builds its tile's P while the other group's
-// level and PV products run on the tensor pipe. Roles (20 warps):
-//   warps 0, 1  producers of groups 0 and 1 (one lane each): claim the group's next
-//               tile from the dynamic counter and pull it into L2; once the group's
-//               stage is free, TMA of Q, K, V and a bulk copy of the tile's decay
-//               prefix into it, then the Fenwick nodes the tile reads, in level
-//               order, into the group's two-slot node ring.
-//   warps 2, 3  MMA issuers of groups 0 and 1 (one lane each).
-//   warps 4-11  epilogue of group 0; warps 12-19 epilogue of group 1. The two warps
-//               of a lane quadrant split every 32-key block of P (16 keys each) and
-//               the dv columns of the result (32 each).
-// TMEM of a group, per tile:
-//   round 0: S = Q K^T in [0, 128); the first two level reads L_p = Q B_p in
-//            [128, 192) and [192, 256) (they overlap the build of P);
-//   round 1: O = P V in [0, 64) once P is in shared memory (over K), and up to
-//            three more level reads in [64, 128), [128, 192), [192, 256);
-//   round r >= 2: three more level reads each in [64, 256).
-// The epilogue reads every round back into fp32 accumulators,
-// acc = O + sum_p lambda_t^(8+p) exp(cl_t + D_p) L_p, and stores them as bf16.
 // Weights of the 16 keys s = 32 blk + 16 half + e (e = 0..15) of a diagonal 32 x 32 block for the
 // query in lane `lane` of the block: lx[l] for the level l = 1 + floor(log2(lane ^ s')) of the
 // pair (lx[0] at s' = lane; s' = s mod 32), 0 where s' > lane (the highest differing bit is set in
@@ -1076,6 +1054,29 @@ __device__ __forceinline__ void diag_weights(int lane, int half, const float* lx
     }
 }
 
+// Ping-pong output kernel for dv = 64: two independent tile pipelines share one CTA.
+// Epilogue group g (eight warps, two per TMEM lane quadrant; thread = query row)
+// owns input stage g and TMEM columns [256 g, 256 g + 256) and takes every other
+// tile the CTA claims, so one group builds its tile's P while the other group's
+// level and PV products run on the tensor pipe. Roles (20 warps):
+//   warps 0, 1  producers of groups 0 and 1 (one lane each): claim the group's next
+//               tile from the dynamic counter and pull it into L2; once the group's
+//               stage is free, TMA of Q, K, V and a bulk copy of the tile's column
+//               decay weights into it, then the Fenwick nodes the tile reads, in level
+//               order, into the group's two-slot node ring.
+//   warps 2, 3  MMA issuers of groups 0 and 1 (one lane each).
+//   warps 4-11  epilogue of group 0; warps 12-19 epilogue of group 1. The two warps
+//               of a lane quadrant split every 32-key block of P (16 keys each) and
+//               the dv columns of the result (32 each).
+// TMEM of a group, per tile:
+//   round 0: S = Q K^T in [0, 128); the first two level reads L_p = Q B_p in
+//            [128, 192) and [192, 256) (they overlap the build of P);
+//   round 1: O = P V in [0, 64) once P is in shared memory (over K), and up to
+//            three more level reads in [64, 128), [128, 192), [192, 256);
+//   round r >= 2: three more level reads each in [64, 256).
+// The epilogue reads every round back into fp32 accumulators,
+// acc = O + sum_p lambda_t^(8+p) exp(cl_t + D_p) L_p, and stores them as bf16 (whole
+// 64-byte runs of rows, through the lane-group transpose).
 struct PpCfg {
     static constexpr int kQ = 0;
     static constexpr int kK = 2 * kPanelBytes;  // K tile, then P of the same tile
