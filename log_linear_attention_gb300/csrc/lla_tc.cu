@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(256, 2)
     tc_nodes_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const float* __restrict__ log_a, float* __restrict__ g_tiles, __nv_bfloat16* __restrict__ nodes,
                     float* __restrict__ seg_tot, float* __restrict__ tok_cl2, float* __restrict__ tok_colw, int T,
-                    int NT, int node_count, const __grid_constant__ LevelOffsets lo, const SeqMap sm, int* err) {
+                    int NT, int node_count, const __grid_constant__ LevelOffsets lo, const SeqMap sm,
+                    int* __restrict__ tile_counter, int* err) {
     constexpr int DH = DV / 2;  // columns per thread
     constexpr int kSegTiles = 1 << Q;
     using S = NodesSmem<DV>;
@@ -151,6 +152,9 @@ __global__ void __launch_bounds__(256, 2)
 
     grid_dep_launch();  // the merge kernel may be launched while this grid drains
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the output kernel's tile counter: it starts claiming tiles only after this grid has
+    // completed (its launch waits on the merge kernel, which waits on this one)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *tile_counter = 0;
     const int seg = blockIdx.x, bh = blockIdx.y;
     const int tile0 = seg * kSegTiles;
     int rowbase, len;
@@ -389,7 +393,6 @@ __global__ void __launch_bounds__(256, 2)
 //  * block (0, 0): the per-tile decay table dtab[bh][j][p] (log2 units): sum of g over
 //    tiles [(j >> p) << p, j), the log-decay from the end of node (p, (j >> p) - 1) to
 //    the start of tile j, for each set bit p of j.
-// Block (0, 0) also resets the tile counter tc_output's CTAs take tiles from.
 __global__ void __launch_bounds__(256)
     tc_merge_kernel(const float* __restrict__ seg_tot, const float* __restrict__ g_tiles,
                     __nv_bfloat16* __restrict__ nodes, float* __restrict__ dtab, int* __restrict__ tile_counter,
@@ -404,7 +407,6 @@ __global__ void __launch_bounds__(256)
     int rowbase, len;
     seq_of(sm, bh, T, rowbase, len);
     const int NTi = (len + kTile - 1) / kTile;  // this head's tiles (NT in the dense layout)
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *tile_counter = 0;
     if (blockIdx.x == 0) {
         if (blockIdx.y != 0) return;
         for (int i = threadIdx.x; i < NTi; i += blockDim.x) g_sh[i] = gh[i];
@@ -1152,7 +1154,11 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    grid_dep_wait();  // the node and merge kernels' outputs (launched early, see launch_pdl)
+    // The node kernel's outputs (decay tables, level 0..q nodes, the tile counter's reset) are
+    // complete when this grid starts. The merge kernel's (nodes above level q, the level decay
+    // table) are waited for where they are first read: by a producer before its first node copy,
+    // by an epilogue thread before its first read-back; the first tiles' Q, K, V copies, S and P
+    // run while the merge kernel drains.
 
     // head-major; within a head from the last tile down (most Fenwick levels first). Packed
     // sequences: sequence-major, then head; the sequence is found in the tile prefix.
@@ -1247,6 +1253,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
                 tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &in_full[g], 64, row0);
                 bulk_load(smem + C::kColwBase + g * 512, tok_colw + bh * T + j * kTile, 512, &in_full[g]);
                 if (!q_free) break;
+                if (c == 0) grid_dep_wait();  // the merge kernel's nodes
                 // claim the group's next tile; its index is used once this tile's node copies are issued
                 const int next_idx = atomicAdd(tile_counter, 1);
                 // the tile's Fenwick nodes, in level order, into the group's ring
@@ -1471,6 +1478,7 @@ __global__ void __launch_bounds__(PpCfg::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_ready[g]);
 
+            if (c == 0) grid_dep_wait();  // the merge kernel's level decay table
             // ---- read back every round: acc = O + sum_p r_p L_p (this warp's half of the columns)
             const int n_lv = __popc(static_cast<unsigned>(j));
             const int R = C::rounds(n_lv);
@@ -1571,7 +1579,7 @@ cudaError_t tc_node_stage(const TcPlan& pl, const CUtensorMap& tk, const CUtenso
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
             kern<<<dim3(nseg, BH), 256, smem, stream>>>(tk, tv, log_a, g_tiles, nodes, seg_tot, tok_cl2, tok_colw, pl.T,
-                                                        pl.NT, pl.node_count, lo, sm, err);
+                                                        pl.NT, pl.node_count, lo, sm, tile_counter, err);
             return cudaSuccess;
         };
         cudaError_t e;
