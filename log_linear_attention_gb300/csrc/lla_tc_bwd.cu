@@ -22,14 +22,16 @@
 //   tc_cmat            : per key tile i, C_i = sum over its read ancestor
 //                        nodes of exp(decay from tile i's end to the node's
 //                        end) dB (bf16, an MMA operand of the next kernel).
-//   tc_bwd_tile        : one CTA per tile: S = Q K^T and dP = dO V^T (TMEM);
+//   tc_bwd_tile        : persistent, one CTA per SM and one (head, tile) item at
+//                        a time: S = Q K^T and dP = dO V^T (TMEM);
 //                        A = lambda D S and G = lambda D dP (bf16, smem) with
 //                        dlambda levels 0..7 and the decay derivatives; then
 //                        dV = A^T dO, dQ = G K, dK = G^T Q; per set bit p,
 //                        Y_p = Q B_p (for dlambda_t^(8+p) and dcum) and
 //                        dQ += (r_p o dO) B_p^T; per key tile (issued before
-//                        the levels), dK += (w o V) C_i^T, dV += (w o K) C_i and
-//                        Z = K C_i (for dcum); dQ, dK, dV leave by TMA stores.
+//                        the levels), dK += (w o V) C_i^T and Z = K C_i (for
+//                        dcum and dV += diag(w) Z); dQ, dK, dV leave by TMA
+//                        stores while the next item's inputs are copied in.
 //   bwd_dloga          : dlog_a_r = sum_{t >= r} dcum_t.
 // Every mbarrier wait is bounded; on overrun a kernel records LLA_ERR_TIMEOUT,
 // lets its own copies and MMAs land and returns.
@@ -408,10 +410,12 @@ __global__ void __launch_bounds__(256) tc_dnode_zero_cut_kernel(float* __restric
 // w, w + 8 (a warp-wide sum each), then every thread forms 32 elements (8 float4s).
 __global__ void __launch_bounds__(256) tc_cmat_kernel(const float* __restrict__ dnodes, const float* __restrict__ g,
                                                       __nv_bfloat16* __restrict__ cmat, int NT, int P, int node_count,
-                                                      const __grid_constant__ Offsets lo) {
+                                                      const __grid_constant__ Offsets lo, int* __restrict__ item_counter) {
     __shared__ float wsh[32];
     __shared__ int rsh[32];
     const int i = blockIdx.x, bh = blockIdx.y;
+    // the next kernel's item counter (this kernel runs before it on the same stream)
+    if (i == 0 && bh == 0 && threadIdx.x == 0) *item_counter = 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int p = warp; p < P; p += 8) {
         const int m = i >> p;
@@ -464,10 +468,10 @@ struct TileCfg {
     static constexpr int kK = 2 * kPanelBytes;       // K tile  [s][d], 2 panels
     static constexpr int kV = 4 * kPanelBytes;       // V tile  [s][e], 1 panel
     static constexpr int kDO = 5 * kPanelBytes;      // dO tile [t][e], 1 panel
-    static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; then w o K [s][d]; then dQ out
+    static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; then dQ out
     static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels; then w o V and r_p o dO; then dK out
-    static constexpr int kC = 10 * kPanelBytes;      // C_i [d][e] (copied with the inputs); then dV out
-    static constexpr int kN = 11 * kPanelBytes;      // node B_p [d][e]
+    static constexpr int kC = 10 * kPanelBytes;      // C_i [d][e] (copied with the inputs)
+    static constexpr int kN = 11 * kPanelBytes;      // node B_p [d][e]; then dV out
     static constexpr int kR = kG + kPanelBytes;      // r_p o dO [t][e]: G's second panel once G is consumed
     static constexpr int kBytes = 12 * kPanelBytes + 1024;
     static constexpr uint32_t kTxIn = 7 * kPanelBytes;
@@ -494,9 +498,12 @@ __device__ __forceinline__ float warp_colsum16(float (&v)[16]) {
     return v[0];
 }
 
-// One CTA per (head, tile); 256 threads: thread (quad = warp % 4, lane) owns row
+// Persistent, one CTA per SM; 256 threads: thread (quad = warp % 4, lane) owns row
 // t = 32 quad + lane (= TMEM lane), half = warp / 4 picks half of the columns. Thread 0
-// issues the TMA copies and the MMAs between block-wide phases.
+// issues the TMA copies and the MMAs between block-wide phases. A CTA takes its first
+// (head, tile) item by its index and the rest from item_counter (zero at launch). Once an
+// item's inputs are dead (its last MMA done and read back) the next item's inputs are
+// copied in, behind this item's output staging, stores and dlambda rows.
 __global__ void __launch_bounds__(256, 1)
     tc_bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -504,9 +511,9 @@ __global__ void __launch_bounds__(256, 1)
                        const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
                        const __grid_constant__ CUtensorMap tm_dv,
                        const float* __restrict__ lambda, const float* __restrict__ tok_cl2,
-                       const float* __restrict__ dtab, __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
-                       __nv_bfloat16* __restrict__ dv, float* __restrict__ dlambda, float* __restrict__ dcum, int T,
-                       int NT, int L, int P, int node_count, const __grid_constant__ Offsets lo, int* err) {
+                       const float* __restrict__ dtab, float* __restrict__ dlambda, float* __restrict__ dcum, int T,
+                       int NT, int L, int P, int node_count, const __grid_constant__ Offsets lo, int n_items,
+                       int* __restrict__ item_counter, int* err) {
     using C = TileCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -518,15 +525,12 @@ __global__ void __launch_bounds__(256, 1)
     __shared__ float dlamp[kTile][16];
     __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile], colw_sh[kTile];
     __shared__ __align__(16) float dtab_sh[16];
-    __shared__ int fail_sh;
+    __shared__ int fail_sh, next_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
     const int t = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int j = blockIdx.x, bh = blockIdx.y;
-    const int r0 = bh * T + j * kTile;
-    const unsigned lvbits = static_cast<unsigned>(j) & ((1u << P) - 1u);
 
     if (tid == 0) {
         mbar_init(&bar_in, 1);
@@ -551,40 +555,54 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0 && atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
         return false;
     };
-    auto node_row = [&](int p) { return (bh * node_count + lo.off[p] + (((j >> p) - 1) >> 1)) * kDk; };
-
-    int node_issued = 0;  // thread 0: node copies issued
-    if (tid == 0) {
+    // thread 0: item it's inputs, C_i, and the per-row scalars: lambda rows (one contiguous
+    // block of 128 L floats), the in-tile log2 decay prefix and the tile's level decay row
+    auto issue_inputs = [&](int it) {
+        const int ibh = it / NT, ij = it - ibh * NT;
+        const int ir0 = ibh * T + ij * kTile;
         uint8_t* st = smem;
-        // inputs, C_i, and the per-row scalars: lambda rows (one contiguous block of 128 L
-        // floats), the in-tile log2 decay prefix and the tile's level decay row
         mbar_expect_tx(&bar_in, C::kTxIn + kTile * L * 4 + kTile * 4 + 16 * 4);
-        bulk_load(lam_sh, lambda + static_cast<size_t>(r0) * L, kTile * L * 4, &bar_in);
-        bulk_load(cl2_sh, tok_cl2 + r0, kTile * 4, &bar_in);
-        bulk_load(dtab_sh, dtab + (static_cast<size_t>(bh) * NT + j) * 16, 16 * 4, &bar_in);
-        tma_load_2d(st + C::kQ, &tm_q, &bar_in, 0, r0);
-        tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &bar_in, 64, r0);
-        tma_load_2d(st + C::kK, &tm_k, &bar_in, 0, r0);
-        tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &bar_in, 64, r0);
-        tma_load_2d(st + C::kV, &tm_v, &bar_in, 0, r0);
-        tma_load_2d(st + C::kDO, &tm_do, &bar_in, 0, r0);
-        tma_load_2d(st + C::kC, &tm_cmat, &bar_in, 0, (bh * NT + j) * kDk);
-        if (lvbits) {
-            const int p0 = __ffs(lvbits) - 1;
-            mbar_expect_tx(&bar_node, kPanelBytes);
-            tma_load_2d(st + C::kN, &tm_nodes, &bar_node, 0, node_row(p0));
-            node_issued = 1;
+        bulk_load(lam_sh, lambda + static_cast<size_t>(ir0) * L, kTile * L * 4, &bar_in);
+        bulk_load(cl2_sh, tok_cl2 + ir0, kTile * 4, &bar_in);
+        bulk_load(dtab_sh, dtab + (static_cast<size_t>(ibh) * NT + ij) * 16, 16 * 4, &bar_in);
+        tma_load_2d(st + C::kQ, &tm_q, &bar_in, 0, ir0);
+        tma_load_2d(st + C::kQ + kPanelBytes, &tm_q, &bar_in, 64, ir0);
+        tma_load_2d(st + C::kK, &tm_k, &bar_in, 0, ir0);
+        tma_load_2d(st + C::kK + kPanelBytes, &tm_k, &bar_in, 64, ir0);
+        tma_load_2d(st + C::kV, &tm_v, &bar_in, 0, ir0);
+        tma_load_2d(st + C::kDO, &tm_do, &bar_in, 0, ir0);
+        tma_load_2d(st + C::kC, &tm_cmat, &bar_in, 0, (ibh * NT + ij) * kDk);
+    };
+    auto zero_sums = [&]() {
+        for (int x = tid; x < kTile * 8; x += blockDim.x) (&dlam8[0][0])[x] = 0.f;
+        for (int x = tid; x < kTile * 16; x += blockDim.x) (&dlamp[0][0])[x] = 0.f;
+        if (tid < kTile) {
+            colE[tid] = 0.f;
+            dcs[tid] = 0.f;
+            zsh[tid] = 0.f;
         }
+    };
+
+    // thread 0's copy bookkeeping, for the drain after a failed wait
+    int in_issued = 0, in_waited = 0, node_issued = 0, node_waited = 0;
+    int item = blockIdx.x;
+    if (tid == 0 && item < n_items) {
+        issue_inputs(item);
+        in_issued = 1;
     }
-    for (int x = tid; x < kTile * 8; x += blockDim.x) (&dlam8[0][0])[x] = 0.f;
-    for (int x = tid; x < kTile * 16; x += blockDim.x) (&dlamp[0][0])[x] = 0.f;
-    if (tid < kTile) {
-        colE[tid] = 0.f;
-        dcs[tid] = 0.f;
-        zsh[tid] = 0.f;
-    }
+    zero_sums();
+    bool ok = true;
+    uint32_t li = 0;  // level rounds so far: uses of bar_node and bar_lv
+    for (uint32_t ip = 0; item < n_items; ip++) {
+    const int bh = item / NT, j = item - bh * NT;
+    const int r0 = bh * T + j * kTile;
+    const unsigned lvbits = static_cast<unsigned>(j) & ((1u << P) - 1u);
+    const uint32_t par = ip & 1u;  // bar_in, bar_s, bar_m1, bar_k: one use per item
+    auto node_row = [&](int p) { return (bh * node_count + lo.off[p] + (((j >> p) - 1) >> 1)) * kDk; };
     // ok stays block-uniform: every change goes through a barrier reduction
-    bool ok = __syncthreads_and(ok_wait(&bar_in, 0));
+    ok = __syncthreads_and(ok && ok_wait(&bar_in, par));
+    if (!ok) break;
+    if (tid == 0) in_waited++;
     // decay from each key to the end of its 32-key block (the factorised decay of E1); read
     // after the barrier that follows the S and dP MMAs
     if (tid < kTile) colw_sh[tid] = exp2f(cl2_sh[tid | 31] - cl2_sh[tid]);
@@ -605,8 +623,17 @@ __global__ void __launch_bounds__(256, 1)
                      kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s);
+        // the previous item's tensor stores have read A, G and N before E1 and the first
+        // node copy write there
+        bulk_wait_read0();
+        if (lvbits) {
+            const int p0 = __ffs(lvbits) - 1;
+            mbar_expect_tx(&bar_node, kPanelBytes);
+            tma_load_2d(smem + C::kN, &tm_nodes, &bar_node, 0, node_row(p0));
+            node_issued++;
+        }
     }
-    ok = __syncthreads_and(ok && ok_wait(&bar_s, 0));
+    ok = __syncthreads_and(ok && ok_wait(&bar_s, par));
     tc_fence_after();
 
     // ---- E1: A, G (bf16), dlambda levels 0..7, decay derivatives. The two warps of a lane
@@ -733,10 +760,10 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     // ---- key side, issued before the query side so that its MMAs overlap the level rounds:
-    // dK += (w o V) C_i^T, dV += (w o K) C_i, Z = K C_i (C_i came with the inputs). A and G
-    // are consumed: w o K takes A's space, w o V G's first panel; the level rounds use the
-    // second for r_p o dO.
-    ok = __syncthreads_and(ok && ok_wait(&bar_m1, 0));
+    // dK += (w o V) C_i^T and Z = K C_i (C_i came with the inputs); the key side's dV term
+    // (w o K) C_i is diag(w) Z, added when dV is staged. G is consumed: w o V takes its
+    // first panel, the level rounds its second for r_p o dO.
+    ok = __syncthreads_and(ok && ok_wait(&bar_m1, par));
     if (ok) {
         const float w = exp2f(cl2_sh[kTile - 1] - cl2_sh[t]);
         if (half == 0) wts[t] = w;
@@ -754,20 +781,6 @@ __global__ void __launch_bounds__(256, 1)
                                pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
             }
         }
-        // w o K: row t, panel `half` (64 columns)
-        {
-            const uint8_t* src = smem + C::kK + half * kPanelBytes;
-            uint8_t* dst = smem + C::kA + half * kPanelBytes;
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const uint32_t off = sw128_off(t, q);
-                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
-                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-                *reinterpret_cast<uint4*>(dst + off) =
-                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
-                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
-            }
-        }
     }
     fence_async_smem();
     tc_fence_before();
@@ -776,7 +789,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         {
             const uint32_t rb = smem_u32(smem + C::kG), cb = smem_u32(smem + C::kC);
-            const uint32_t ab = smem_u32(smem + C::kA), kb = smem_u32(smem + C::kK);
+            const uint32_t kb = smem_u32(smem + C::kK);
             constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 0, 0);
             constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 0, 1);
 #pragma unroll
@@ -785,7 +798,6 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int kk = 0; kk < kDk / 16; kk++) {
                 const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                mma_bf16(tmem + C::kDVc, sdesc(ab + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV, 1u);
                 mma_bf16(tmem + C::kZ, sdesc(kb + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV,
                          kk > 0 ? 1u : 0u);
             }
@@ -793,7 +805,6 @@ __global__ void __launch_bounds__(256, 1)
         }
     }
     // ---- query side: one round per set bit p of j
-    int li = 0;
     for (int p = 0; p < P && ok; p++) {
         if (((j >> p) & 1) == 0) continue;
         const float cl2_t = cl2_sh[t];
@@ -819,6 +830,7 @@ __global__ void __launch_bounds__(256, 1)
         if (tid == 0) {
             tc_fence_after();
             if (mbar_wait(&bar_node, li & 1)) {
+                node_waited++;
                 tc_fence_after();
                 const uint32_t qb = smem_u32(smem + C::kQ), nb = smem_u32(smem + C::kN), rb = smem_u32(smem + C::kR);
                 constexpr uint32_t kIdY = idesc_bf16(kTile, kDV, 0, 1);
@@ -877,7 +889,7 @@ __global__ void __launch_bounds__(256, 1)
         li++;
     }
 
-    ok = __syncthreads_and(ok && ok_wait(&bar_k, 0));
+    ok = __syncthreads_and(ok && ok_wait(&bar_k, par));
     tc_fence_after();
     if (ok) {
         float zv[32];
@@ -897,9 +909,21 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // this item's inputs are dead: copy in the next item's
+    if (tid == 0) {
+        int next = n_items;
+        if (ok) {
+            next = static_cast<int>(gridDim.x) + atomicAdd(item_counter, 1);
+            if (next < n_items) {
+                issue_inputs(next);
+                in_issued++;
+            }
+        }
+        next_sh = next;
+    }
 
-    // ---- outputs: dQ, dK, dV (bf16) into the now free A, G and r o dO areas in the TMA
-    // layout, then written by tensor stores; the decay derivative per row
+    // ---- outputs: dQ, dK, dV (bf16) into the now free A, G and N areas in the TMA layout,
+    // then written by tensor stores; the decay derivative per row
     if (ok) {
         const size_t row = static_cast<size_t>(r0) + t;
         float x[32];
@@ -917,34 +941,49 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld32(tmem + lane_base + C::kDK + 64 * half + c0, x);
             put(smem + C::kG + half * kPanelBytes, c0 >> 3);
         }
+        // dV: A^T dO + diag(w) Z, w the key's decay to the tile end
         tmem_ld32(tmem + lane_base + C::kDVc + 32 * half, x);
-        put(smem + C::kC, 4 * half);
+        {
+            float zv[32];
+            tmem_ld32(tmem + lane_base + C::kZ + 32 * half, zv);
+            const float w = wts[t];
+#pragma unroll
+            for (int i = 0; i < 32; i++) x[i] = fmaf(w, zv[i], x[i]);
+        }
+        put(smem + C::kN, 4 * half);
         if (half == 0) dcum[row] = dcs[t] - colE[t] - wts[t] * zsh[t];
     }
     fence_async_smem();
+    tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
         tma_store_2d(&tm_dq, smem + C::kA, 0, r0);
         tma_store_2d(&tm_dq, smem + C::kA + kPanelBytes, 64, r0);
         tma_store_2d(&tm_dk, smem + C::kG, 0, r0);
         tma_store_2d(&tm_dk, smem + C::kG + kPanelBytes, 64, r0);
-        tma_store_2d(&tm_dv, smem + C::kC, 0, r0);
+        tma_store_2d(&tm_dv, smem + C::kN, 0, r0);
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
-    for (int x = tid; x < kTile * L; x += blockDim.x) {
-        const int row = x / L, l = x - row * L;
-        dlambda[static_cast<size_t>(r0) * L + x] = l < 8 ? dlam8[row][l] : (l < 24 ? dlamp[row][l - 8] : 0.f);
+    if (ok)
+        for (int x = tid; x < kTile * L; x += blockDim.x) {
+            const int row = x / L, l = x - row * L;
+            dlambda[static_cast<size_t>(r0) * L + x] = l < 8 ? dlam8[row][l] : (l < 24 ? dlamp[row][l - 8] : 0.f);
+        }
+    __syncthreads();
+    item = next_sh;
+    zero_sums();
+    if (!ok) break;
     }
 
-    if (tid == 0 && ok) {
+    if (tid == 0) {
         // the tensor stores have read their shared-memory sources before it goes away
         bulk_wait_read0();
     }
     __syncthreads();
     if (tid == 0 && fail_sh) {
         // let this CTA's copies land before its shared memory goes away
-        mbar_wait(&bar_in, 0);
-        if (node_issued > 0) mbar_wait(&bar_node, (node_issued - 1) & 1);
+        if (in_issued > in_waited) mbar_wait(&bar_in, (in_issued - 1) & 1);
+        if (node_issued > node_waited) mbar_wait(&bar_node, (node_issued - 1) & 1);
     }
     if (tid == 0) {
         // every MMA issued above has completed before TMEM is released
@@ -1031,17 +1070,26 @@ cudaError_t tc_backward(const TcPlan& pl, const void* q, const void* k, const vo
             note_launch(stream, "tc_dnode");
         }
     }
-    tc_cmat_kernel<<<dim3(pl.NT, BH), 256, 0, stream>>>(dnodes, g_tiles, cmat, pl.NT, pl.P, pl.node_count, lo);
+    int* item_counter = reinterpret_cast<int*>(ws + pl.total_bytes - pl.ctr_bytes);
+    tc_cmat_kernel<<<dim3(pl.NT, BH), 256, 0, stream>>>(dnodes, g_tiles, cmat, pl.NT, pl.P, pl.node_count, lo,
+                                                         item_counter);
     note_launch(stream, "tc_cmat");
     e = cudaFuncSetAttribute(tc_bwd_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg::kBytes);
     if (e != cudaSuccess) return e;
     CUtensorMap tdq, tdk, tdv;
     if (!make_map(&tdq, dq, rows, kDk) || !make_map(&tdk, dk, rows, kDk) || !make_map(&tdv, dv, rows, kDV))
         return cudaErrorInvalidValue;
-    tc_bwd_tile_kernel<<<dim3(pl.NT, BH), 256, TileCfg::kBytes, stream>>>(
-        tq, tk, tv, tdo, tn, tc, tdq, tdk, tdv, lambda, tok_cl2, dtab, static_cast<__nv_bfloat16*>(dq),
-        static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), dlambda, dcum, pl.T, pl.NT, L, pl.P,
-        pl.node_count, lo, err);
+    const int n_items = BH * pl.NT;
+    int tdev = 0, tsms = 0;
+    if (cudaGetDevice(&tdev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&tsms, cudaDevAttrMultiProcessorCount, tdev) != cudaSuccess || tsms <= 0) {
+        cudaGetLastError();
+        tsms = 152;
+    }
+    const int tile_grid = n_items < tsms ? n_items : tsms;
+    tc_bwd_tile_kernel<<<tile_grid, 256, TileCfg::kBytes, stream>>>(tq, tk, tv, tdo, tn, tc, tdq, tdk, tdv, lambda,
+                                                                    tok_cl2, dtab, dlambda, dcum, pl.T, pl.NT, L, pl.P,
+                                                                    pl.node_count, lo, n_items, item_counter, err);
     note_launch(stream, "tc_bwd_tile");
     return bwd_dloga(dcum, dlog_a, BH, pl.T, stream);
 }
