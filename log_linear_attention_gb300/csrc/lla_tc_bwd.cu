@@ -469,15 +469,16 @@ struct TileCfg {
     static constexpr int kV = 4 * kPanelBytes;       // V tile  [s][e], 1 panel
     static constexpr int kDO = 5 * kPanelBytes;      // dO tile [t][e], 1 panel
     static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; then dQ out
-    static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels; then w o V and r_p o dO; then dK out
-    static constexpr int kC = 10 * kPanelBytes;      // C_i [d][e] (copied with the inputs)
-    static constexpr int kN = 11 * kPanelBytes;      // node B_p [d][e]; then dV out
+    static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels; then r_p o dO; then dK out
+    static constexpr int kC = 10 * kPanelBytes;      // C_i [d][e] (copied with the inputs); then a node slot
+    static constexpr int kN = 11 * kPanelBytes;      // w o V [s][e]; then a node slot (B_p [d][e]); then dV out
     static constexpr int kR = kG + kPanelBytes;      // r_p o dO [t][e]: G's second panel once G is consumed
     static constexpr int kBytes = 12 * kPanelBytes + 1024;
     static constexpr uint32_t kTxIn = 7 * kPanelBytes;
-    // TMEM columns
-    static constexpr uint32_t kS = 0, kDP = 128;                       // S, dP (phase 1)
-    static constexpr uint32_t kDQ = 0, kDK = 128, kDVc = 256, kY = 320, kZ = 384;
+    // TMEM columns: S and dP until the A/G epilogue; dK and Z from the key side's MMAs, which
+    // run beside it; then dQ over S, Y over dP, and dV
+    static constexpr uint32_t kS = 0, kDP = 128;
+    static constexpr uint32_t kDQ = 0, kY = 128, kDK = 256, kDVc = 384, kZ = 448;
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -517,13 +518,14 @@ __global__ void __launch_bounds__(256, 1)
     using C = TileCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_in, bar_s, bar_m1, bar_node, bar_lv, bar_k, bar_d;
+    __shared__ uint64_t bar_in, bar_s, bar_m1, bar_node[2], bar_lv, bar_k, bar_d;
     __shared__ uint32_t tmem_base_sh;
     __shared__ __align__(16) float cl2_sh[kTile];
     __shared__ __align__(16) float lam_sh[kTile * 32];  // the tile's lambda rows [t][L], L <= 32
     __shared__ float dlam8[kTile][8];
     __shared__ float dlamp[kTile][16];
     __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile], colw_sh[kTile];
+    __shared__ float zpart[2][kTile];  // a level round's q_t^T B_p dO_t, per column half
     __shared__ __align__(16) float dtab_sh[16];
     __shared__ int fail_sh, next_sh;
 
@@ -536,7 +538,8 @@ __global__ void __launch_bounds__(256, 1)
         mbar_init(&bar_in, 1);
         mbar_init(&bar_s, 1);
         mbar_init(&bar_m1, 1);
-        mbar_init(&bar_node, 1);
+        mbar_init(&bar_node[0], 1);
+        mbar_init(&bar_node[1], 1);
         mbar_init(&bar_lv, 1);
         mbar_init(&bar_k, 1);
         mbar_init(&bar_d, 1);
@@ -584,7 +587,10 @@ __global__ void __launch_bounds__(256, 1)
     };
 
     // thread 0's copy bookkeeping, for the drain after a failed wait
-    int in_issued = 0, in_waited = 0, node_issued = 0, node_waited = 0;
+    int in_issued = 0, in_waited = 0;
+    int node_issued0 = 0, node_issued1 = 0, node_waited0 = 0, node_waited1 = 0;  // per node slot
+    int claimed = 0;     // thread 0: the item claimed to follow this one
+    bool k_bad = false;  // this thread saw a wait for the key side's MMAs run out
     int item = blockIdx.x;
     if (tid == 0 && item < n_items) {
         issue_inputs(item);
@@ -592,13 +598,29 @@ __global__ void __launch_bounds__(256, 1)
     }
     zero_sums();
     bool ok = true;
-    uint32_t li = 0;  // level rounds so far: uses of bar_node and bar_lv
+    uint32_t li = 0;  // level rounds so far: uses of bar_lv
     for (uint32_t ip = 0; item < n_items; ip++) {
     const int bh = item / NT, j = item - bh * NT;
     const int r0 = bh * T + j * kTile;
     const unsigned lvbits = static_cast<unsigned>(j) & ((1u << P) - 1u);
     const uint32_t par = ip & 1u;  // bar_in, bar_s, bar_m1, bar_k: one use per item
     auto node_row = [&](int p) { return (bh * node_count + lo.off[p] + (((j >> p) - 1) >> 1)) * kDk; };
+    const int nrounds = __popc(lvbits);
+    auto round_level = [&](int r) {  // the set bit of j that level round r reads
+        unsigned b = lvbits;
+        for (int k = 0; k < r; k++) b &= b - 1;
+        return __ffs(b) - 1;
+    };
+    // thread 0: round r's node into slot r & 1 (N or C: both free once the key side's MMAs
+    // are done)
+    auto issue_node = [&](int r) {
+        const int sl = r & 1;
+        mbar_expect_tx(&bar_node[sl], kPanelBytes);
+        tma_load_2d(smem + (sl ? C::kC : C::kN), &tm_nodes, &bar_node[sl], 0, node_row(round_level(r)));
+        if (sl) node_issued1++; else node_issued0++;
+    };
+    // the previous item's tensor stores have read A, G and N before this item writes there
+    if (tid == 0) bulk_wait_read0();
     // ok stays block-uniform: every change goes through a barrier reduction
     ok = __syncthreads_and(ok && ok_wait(&bar_in, par));
     if (!ok) break;
@@ -623,18 +645,49 @@ __global__ void __launch_bounds__(256, 1)
                      kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s);
-        // the previous item's tensor stores have read A, G and N before E1 and the first
-        // node copy write there
-        bulk_wait_read0();
-        if (lvbits) {
-            const int p0 = __ffs(lvbits) - 1;
-            mbar_expect_tx(&bar_node, kPanelBytes);
-            tma_load_2d(smem + C::kN, &tm_nodes, &bar_node, 0, node_row(p0));
-            node_issued++;
+    }
+    // ---- key side, beside S and dP: dK = (w o V) C_i^T and Z = K C_i (C_i came with the
+    // inputs); the key side's dV term (w o K) C_i is diag(w) Z, added when dV is staged.
+    // w o V (row t = key s, this half's 32 columns) goes to N while S and dP run.
+    {
+        const float w = exp2f(cl2_sh[kTile - 1] - cl2_sh[t]);
+        if (half == 0) wts[t] = w;
+        const uint8_t* src = smem + C::kV;
+        uint8_t* dst = smem + C::kN;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const uint32_t off = sw128_off(t, 4 * half + q);
+            const uint4 x = *reinterpret_cast<const uint4*>(src + off);
+            const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+            *reinterpret_cast<uint4*>(dst + off) =
+                make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
+                           pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
         }
     }
+    fence_async_smem();
     ok = __syncthreads_and(ok && ok_wait(&bar_s, par));
     tc_fence_after();
+    // thread 0 (lane quadrant 0, the lightest share of the epilogue below) issues the key
+    // side's MMAs; they run beside the epilogue
+    if (tid == 0 && ok) {
+        const uint32_t rb = smem_u32(smem + C::kN), cb = smem_u32(smem + C::kC);
+        const uint32_t kb = smem_u32(smem + C::kK);
+        constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 0, 0);
+        constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 0, 1);
+#pragma unroll
+        for (int kk = 0; kk < kDV / 16; kk++)
+            mma_bf16(tmem + C::kDK, sdesc(rb + kk * 32, 16, 1024), sdesc(cb + kk * 32, 16, 1024), kIdK,
+                     kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kDk / 16; kk++) {
+            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+            mma_bf16(tmem + C::kZ, sdesc(kb + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_k);
+        // the item to follow
+        claimed = static_cast<int>(gridDim.x) + atomicAdd(item_counter, 1);
+    }
 
     // ---- E1: A, G (bf16), dlambda levels 0..7, decay derivatives. The two warps of a lane
     // quadrant take alternate 16-key halves of every 32-key block, so the masked diagonal
@@ -754,144 +807,22 @@ __global__ void __launch_bounds__(256, 1)
             mma_bf16(tmem + C::kDQ, sdesc(gb + koff, 16, 1024), sdesc(kb + kk * 2048, kPanelBytes, 1024), kIdQ,
                      kk > 0 ? 1u : 0u);
             mma_bf16(tmem + C::kDK, sdesc(gb + kk * 2048, kPanelBytes, 1024), sdesc(qb + kk * 2048, kPanelBytes, 1024),
-                     kIdK, kk > 0 ? 1u : 0u);
+                     kIdK, 1u);
         }
         mma_commit(&bar_m1);
+        // N and C are free once the key side's MMAs are done: the first two rounds' nodes
+        if (mbar_wait(&bar_k, par)) {
+            if (nrounds > 0) issue_node(0);
+            if (nrounds > 1) issue_node(1);
+        } else {
+            k_bad = true;
+            if (atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
+        }
     }
 
-    // ---- key side, issued before the query side so that its MMAs overlap the level rounds:
-    // dK += (w o V) C_i^T and Z = K C_i (C_i came with the inputs); the key side's dV term
-    // (w o K) C_i is diag(w) Z, added when dV is staged. G is consumed: w o V takes its
-    // first panel, the level rounds its second for r_p o dO.
-    ok = __syncthreads_and(ok && ok_wait(&bar_m1, par));
-    if (ok) {
-        const float w = exp2f(cl2_sh[kTile - 1] - cl2_sh[t]);
-        if (half == 0) wts[t] = w;
-        // w o V: row t (= key s), this half's 32 columns
-        {
-            const uint8_t* src = smem + C::kV;
-            uint8_t* dst = smem + C::kG;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const uint32_t off = sw128_off(t, 4 * half + q);
-                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
-                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-                *reinterpret_cast<uint4*>(dst + off) =
-                    make_uint4(pack_bf16(a0.x * w, a0.y * w), pack_bf16(a1.x * w, a1.y * w),
-                               pack_bf16(a2.x * w, a2.y * w), pack_bf16(a3.x * w, a3.y * w));
-            }
-        }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && ok) {
+    // Z's row sums with V (for dcum) while the MMAs above run
+    if (ok && ok_wait(&bar_k, par)) {
         tc_fence_after();
-        {
-            const uint32_t rb = smem_u32(smem + C::kG), cb = smem_u32(smem + C::kC);
-            const uint32_t kb = smem_u32(smem + C::kK);
-            constexpr uint32_t kIdK = idesc_bf16(kTile, kDk, 0, 0);
-            constexpr uint32_t kIdV = idesc_bf16(kTile, kDV, 0, 1);
-#pragma unroll
-            for (int kk = 0; kk < kDV / 16; kk++)
-                mma_bf16(tmem + C::kDK, sdesc(rb + kk * 32, 16, 1024), sdesc(cb + kk * 32, 16, 1024), kIdK, 1u);
-#pragma unroll
-            for (int kk = 0; kk < kDk / 16; kk++) {
-                const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                mma_bf16(tmem + C::kZ, sdesc(kb + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024), kIdV,
-                         kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bar_k);
-        }
-    }
-    // ---- query side: one round per set bit p of j
-    for (int p = 0; p < P && ok; p++) {
-        if (((j >> p) & 1) == 0) continue;
-        const float cl2_t = cl2_sh[t];
-        const float rho = exp2f(cl2_t + dtab_sh[p]);
-        const float r = lam_sh[t * L + 8 + p] * rho;
-        // r_p o dO, row t, this half's 32 columns (chunks 4 half .. 4 half + 3)
-        {
-            const uint8_t* src = smem + C::kDO;
-            uint8_t* dst = smem + C::kR;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const uint32_t off = sw128_off(t, 4 * half + q);
-                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
-                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-                *reinterpret_cast<uint4*>(dst + off) =
-                    make_uint4(pack_bf16(a0.x * r, a0.y * r), pack_bf16(a1.x * r, a1.y * r),
-                               pack_bf16(a2.x * r, a2.y * r), pack_bf16(a3.x * r, a3.y * r));
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            if (mbar_wait(&bar_node, li & 1)) {
-                node_waited++;
-                tc_fence_after();
-                const uint32_t qb = smem_u32(smem + C::kQ), nb = smem_u32(smem + C::kN), rb = smem_u32(smem + C::kR);
-                constexpr uint32_t kIdY = idesc_bf16(kTile, kDV, 0, 1);
-                constexpr uint32_t kIdX = idesc_bf16(kTile, kDk, 0, 0);
-#pragma unroll
-                for (int kk = 0; kk < kDk / 16; kk++) {
-                    const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                    mma_bf16(tmem + C::kY, sdesc(qb + off, 16, 1024), sdesc(nb + kk * 2048, kPanelBytes, 1024), kIdY,
-                             kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < kDV / 16; kk++)
-                    mma_bf16(tmem + C::kDQ, sdesc(rb + kk * 32, 16, 1024), sdesc(nb + kk * 32, 16, 1024), kIdX, 1u);
-                mma_commit(&bar_lv);
-            } else if (atomicExch(&fail_sh, 1) == 0) {
-                record_error(err, kDevTimeout);
-            }
-        }
-        ok = __syncthreads_and(ok_wait(&bar_lv, li & 1));
-        tc_fence_after();
-        if (ok) {
-            // the node slot is free: fetch the next level's node
-            if (tid == 0) {
-                const unsigned rest = lvbits & ~((2u << p) - 1u);
-                if (rest) {
-                    const int pn = __ffs(rest) - 1;
-                    mbar_expect_tx(&bar_node, kPanelBytes);
-                    tma_load_2d(smem + C::kN, &tm_nodes, &bar_node, 0, node_row(pn));
-                    node_issued++;
-                }
-            }
-            float yv[32];
-            tmem_ld32(tmem + lane_base + C::kY + 32 * half, yv);
-            const uint8_t* src = smem + C::kDO;
-            float z = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
-                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-                z = fmaf(yv[8 * q], a0.x, z); z = fmaf(yv[8 * q + 1], a0.y, z);
-                z = fmaf(yv[8 * q + 2], a1.x, z); z = fmaf(yv[8 * q + 3], a1.y, z);
-                z = fmaf(yv[8 * q + 4], a2.x, z); z = fmaf(yv[8 * q + 5], a2.y, z);
-                z = fmaf(yv[8 * q + 6], a3.x, z); z = fmaf(yv[8 * q + 7], a3.y, z);
-            }
-            atomicAdd(&zsh[t], z);
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (ok && half == 0) {
-            const float zt = zsh[t];
-            dlamp[t][p] = rho * zt;
-            dcs[t] += r * zt;
-            zsh[t] = 0.f;
-        }
-        __syncthreads();
-        li++;
-    }
-
-    ok = __syncthreads_and(ok && ok_wait(&bar_k, par));
-    tc_fence_after();
-    if (ok) {
         float zv[32];
         tmem_ld32(tmem + lane_base + C::kZ + 32 * half, zv);
         const uint8_t* src = smem + C::kV;
@@ -906,14 +837,121 @@ __global__ void __launch_bounds__(256, 1)
             y = fmaf(zv[8 * q + 6], a3.x, y); y = fmaf(zv[8 * q + 7], a3.y, y);
         }
         atomicAdd(&zsh[t], y);
+    } else {
+        k_bad = true;
     }
     tc_fence_before();
-    __syncthreads();
-    // this item's inputs are dead: copy in the next item's
+    ok = __syncthreads_and(ok && ok_wait(&bar_m1, par) && !k_bad);
+    // ---- query side: one round per set bit p of j, lowest first. Round r's node is in slot
+    // r & 1: the copies for rounds 0 and 1 went out with the MMAs above, round r + 2's goes
+    // out when round r is done. The next round's r o dO is scaled while this round's Y is
+    // read back, and the row sums go through zpart: one block barrier per round.
+    {
+        const float cl2_t = cl2_sh[t];
+        // r o dO, row t, this half's 32 columns (chunks 4 half .. 4 half + 3)
+        auto scale_rdo = [&](float rr) {
+            const uint8_t* src = smem + C::kDO;
+            uint8_t* dst = smem + C::kR;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t off = sw128_off(t, 4 * half + q);
+                const uint4 x = *reinterpret_cast<const uint4*>(src + off);
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+                *reinterpret_cast<uint4*>(dst + off) =
+                    make_uint4(pack_bf16(a0.x * rr, a0.y * rr), pack_bf16(a1.x * rr, a1.y * rr),
+                               pack_bf16(a2.x * rr, a2.y * rr), pack_bf16(a3.x * rr, a3.y * rr));
+            }
+        };
+        float rho = 0.f, rr = 0.f;
+        int p = 0;
+        if (nrounds > 0 && ok) {
+            p = round_level(0);
+            rho = exp2f(cl2_t + dtab_sh[p]);
+            rr = lam_sh[t * L + 8 + p] * rho;
+            scale_rdo(rr);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        for (int r = 0; r < nrounds && ok; r++) {
+            const int sl = r & 1;
+            if (tid == 0) {
+                tc_fence_after();
+                if (mbar_wait(&bar_node[sl], (sl ? node_waited1 : node_waited0) & 1)) {
+                    if (sl) node_waited1++; else node_waited0++;
+                    tc_fence_after();
+                    const uint32_t qb = smem_u32(smem + C::kQ), rb = smem_u32(smem + C::kR);
+                    const uint32_t nb = smem_u32(smem + (sl ? C::kC : C::kN));
+                    constexpr uint32_t kIdY = idesc_bf16(kTile, kDV, 0, 1);
+                    constexpr uint32_t kIdX = idesc_bf16(kTile, kDk, 0, 0);
+#pragma unroll
+                    for (int kk = 0; kk < kDk / 16; kk++) {
+                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                        mma_bf16(tmem + C::kY, sdesc(qb + off, 16, 1024), sdesc(nb + kk * 2048, kPanelBytes, 1024),
+                                 kIdY, kk > 0 ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < kDV / 16; kk++)
+                        mma_bf16(tmem + C::kDQ, sdesc(rb + kk * 32, 16, 1024), sdesc(nb + kk * 32, 16, 1024), kIdX,
+                                 1u);
+                    mma_commit(&bar_lv);
+                } else if (atomicExch(&fail_sh, 1) == 0) {
+                    record_error(err, kDevTimeout);
+                }
+            }
+            ok = __syncthreads_and(ok_wait(&bar_lv, li & 1));
+            tc_fence_after();
+            float rho_n = 0.f, rr_n = 0.f;
+            int p_n = 0;
+            if (ok) {
+                if (tid == 0 && r + 2 < nrounds) issue_node(r + 2);
+                uint32_t y0[16], y1[16];
+                tmem_ld16_issue(tmem + lane_base + C::kY + 32 * half, y0);
+                tmem_ld16_issue(tmem + lane_base + C::kY + 32 * half + 16, y1);
+                if (r + 1 < nrounds) {
+                    p_n = round_level(r + 1);
+                    rho_n = exp2f(cl2_t + dtab_sh[p_n]);
+                    rr_n = lam_sh[t * L + 8 + p_n] * rho_n;
+                    scale_rdo(rr_n);
+                }
+                tmem_ld16_wait(y0);
+                tmem_ld16_wait(y1);
+                const uint8_t* src = smem + C::kDO;
+                float z = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const uint32_t* yv = q < 2 ? y0 + 8 * q : y1 + 8 * (q - 2);
+                    const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
+                    const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z),
+                                 a3 = unpack_bf16(x.w);
+                    z = fmaf(__uint_as_float(yv[0]), a0.x, z); z = fmaf(__uint_as_float(yv[1]), a0.y, z);
+                    z = fmaf(__uint_as_float(yv[2]), a1.x, z); z = fmaf(__uint_as_float(yv[3]), a1.y, z);
+                    z = fmaf(__uint_as_float(yv[4]), a2.x, z); z = fmaf(__uint_as_float(yv[5]), a2.y, z);
+                    z = fmaf(__uint_as_float(yv[6]), a3.x, z); z = fmaf(__uint_as_float(yv[7]), a3.y, z);
+                }
+                zpart[half][t] = z;
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (ok && half == 0) {
+                const float zt = zpart[0][t] + zpart[1][t];
+                dlamp[t][p] = rho * zt;
+                dcs[t] += rr * zt;
+            }
+            rho = rho_n;
+            rr = rr_n;
+            p = p_n;
+            li++;
+        }
+    }
+
+    // this item's inputs are dead (the last block barrier above follows their last reads and
+    // MMAs): copy in the next item's
     if (tid == 0) {
         int next = n_items;
         if (ok) {
-            next = static_cast<int>(gridDim.x) + atomicAdd(item_counter, 1);
+            next = claimed;
             if (next < n_items) {
                 issue_inputs(next);
                 in_issued++;
@@ -983,7 +1021,8 @@ __global__ void __launch_bounds__(256, 1)
     if (tid == 0 && fail_sh) {
         // let this CTA's copies land before its shared memory goes away
         if (in_issued > in_waited) mbar_wait(&bar_in, (in_issued - 1) & 1);
-        if (node_issued > node_waited) mbar_wait(&bar_node, (node_issued - 1) & 1);
+        if (node_issued0 > node_waited0) mbar_wait(&bar_node[0], (node_issued0 - 1) & 1);
+        if (node_issued1 > node_waited1) mbar_wait(&bar_node[1], (node_issued1 - 1) & 1);
     }
     if (tid == 0) {
         // every MMA issued above has completed before TMEM is released
