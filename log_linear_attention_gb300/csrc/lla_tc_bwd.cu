@@ -524,7 +524,8 @@ __global__ void __launch_bounds__(256, 1)
     __shared__ __align__(16) float lam_sh[kTile * 32];  // the tile's lambda rows [t][L], L <= 32
     __shared__ float dlam8[kTile][8];
     __shared__ float dlamp[kTile][16];
-    __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile], colw_sh[kTile];
+    __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile];
+    __shared__ __align__(16) float colw_sh[kTile];
     __shared__ float zpart[2][kTile];  // a level round's q_t^T B_p dO_t, per column half
     __shared__ __align__(16) float dtab_sh[16];
     __shared__ int fail_sh, next_sh;
@@ -734,8 +735,99 @@ __global__ void __launch_bounds__(256, 1)
                 rowE += lm * dsum;
 #pragma unroll
                 for (int ll = 0; ll < 8; ll++) dl[ll] += (l == ll) ? dsum : 0.f;
+            } else if (cl2_sh[cb32] - cl2_sh[cb32 + 31] < 100.f) {
+                // the diagonal 32-key block (t and s share bits 5 and 6, so the levels are 0..5)
+                // with the block's decay under 2^100: decay exp2(cl_t - cl_end) colw[s], both
+                // factors within 2^(+-100). With m = t mod 16, a lane whose 16-key group is
+                // this half's sees level bitlength(m ^ k) at key k and keeps keys k <= m; a
+                // lane of the other group sees level 5 everywhere and keeps every key (half 0)
+                // or none (half 1).
+                float sv[16], dpv[16];
+                tmem_ld16(tmem + lane_base + C::kS + cb, sv);
+                tmem_ld16(tmem + lane_base + C::kDP + cb, dpv);
+                const int m = lane & 15;
+                const bool same = ((lane >> 4) & 1) == half;
+                const int klim = same ? m : (half == 0 ? 15 : -1);
+                float w[6];
+#pragma unroll
+                for (int ll = 0; ll < 6; ll++) w[ll] = lam_sh[t * L + ll];
+#pragma unroll
+                for (int ll = 0; ll < 5; ll++) w[ll] = same ? w[ll] : w[5];
+                // lambda at each key by the bits of m ^ k, lowest bit first
+                const bool m0 = m & 1, m1 = (m >> 1) & 1, m2 = (m >> 2) & 1, m3 = (m >> 3) & 1;
+                float w1x[2], w2x[4], w3x[8], lmk[16];
+#pragma unroll
+                for (int b = 0; b < 2; b++) w1x[b] = (b != static_cast<int>(m0)) ? w[1] : w[0];
+#pragma unroll
+                for (int b = 0; b < 4; b++) w2x[b] = ((b >> 1) != static_cast<int>(m1)) ? w[2] : w1x[b & 1];
+#pragma unroll
+                for (int b = 0; b < 8; b++) w3x[b] = ((b >> 2) != static_cast<int>(m2)) ? w[3] : w2x[b & 3];
+#pragma unroll
+                for (int b = 0; b < 16; b++) lmk[b] = ((b >> 3) != static_cast<int>(m3)) ? w[4] : w3x[b & 7];
+                const float rowf = exp2f(cl2_t - cl2_sh[cb32 + 31]);
+                float cw[16];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(colw_sh + cb + 4 * q);
+                    cw[4 * q] = c4.x;
+                    cw[4 * q + 1] = c4.y;
+                    cw[4 * q + 2] = c4.z;
+                    cw[4 * q + 3] = c4.w;
+                }
+                float x[16];  // D S dP per key
+#pragma unroll
+                for (int k = 0; k < 16; k += 2) {
+                    float av[2], gv[2];
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const float D = k + h <= klim ? rowf * cw[k + h] : 0.f;
+                        const float ds = D * sv[k + h];
+                        x[k + h] = ds * dpv[k + h];
+                        av[h] = lmk[k + h] * ds;
+                        gv[h] = lmk[k + h] * D * dpv[k + h];
+                    }
+                    pa[k >> 1] = pack_bf16(av[0], av[1]);
+                    pg[k >> 1] = pack_bf16(gv[0], gv[1]);
+                }
+                // per-level sums: level l > 0 of the own group is the 2^(l-1) keys whose bits
+                // above l - 1 match m's and whose bit l - 1 does not
+                float g2[8], g4[4], g8[2];
+#pragma unroll
+                for (int b = 0; b < 8; b++) g2[b] = x[2 * b] + x[2 * b + 1];
+#pragma unroll
+                for (int b = 0; b < 4; b++) g4[b] = g2[2 * b] + g2[2 * b + 1];
+#pragma unroll
+                for (int b = 0; b < 2; b++) g8[b] = g4[2 * b] + g4[2 * b + 1];
+                const float tot = g8[0] + g8[1];
+                float y0[8], y1[8];  // pairs picked by bit 0: the key m's side, the other side
+#pragma unroll
+                for (int b = 0; b < 8; b++) {
+                    y0[b] = m0 ? x[2 * b + 1] : x[2 * b];
+                    y1[b] = m0 ? x[2 * b] : x[2 * b + 1];
+                }
+                auto pick8 = [&](const float (&v)[8], bool b0, bool b1, bool b2) {
+                    const float a0 = b0 ? v[1] : v[0], a1 = b0 ? v[3] : v[2];
+                    const float a2 = b0 ? v[5] : v[4], a3 = b0 ? v[7] : v[6];
+                    const float c0 = b1 ? a1 : a0, c1 = b1 ? a3 : a2;
+                    return b2 ? c1 : c0;
+                };
+                const float l0 = pick8(y0, m1, m2, m3);   // key m
+                const float l1 = pick8(y1, m1, m2, m3);   // key m ^ 1
+                const float l2 = pick8(g2, !m1, m2, m3);  // keys m ^ 2, m ^ 3
+                const float l3 = m2 ? (m3 ? g4[2] : g4[0]) : (m3 ? g4[3] : g4[1]);
+                const float l4 = m3 ? g8[0] : g8[1];
+                dl[0] += same ? l0 : 0.f;
+                dl[1] += same ? l1 : 0.f;
+                dl[2] += same ? l2 : 0.f;
+                dl[3] += same ? l3 : 0.f;
+                dl[4] += same ? l4 : 0.f;
+                dl[5] += same ? 0.f : tot;
+                rowE += same ? w[0] * l0 + w[1] * l1 + w[2] * l2 + w[3] * l3 + w[4] * l4 : w[5] * tot;
+                // column sums over the rows, below
+#pragma unroll
+                for (int k = 0; k < 16; k++) ev[k] = lmk[k] * x[k];
             } else {
-                // the diagonal 32-key block: t and s share bits 5 and 6, so the levels are 0..5
+                // the diagonal 32-key block with a decay over 2^100 across it: one exp2 per key
                 float sv[16], dpv[16];
                 tmem_ld16(tmem + lane_base + C::kS + cb, sv);
                 tmem_ld16(tmem + lane_base + C::kDP + cb, dpv);

@@ -73,6 +73,21 @@ def test_backward_matches_oracle(B, H, T, dk, dv, chunk, dtype):
         assert err <= tol, (name, err)
 
 
+@pytest.mark.parametrize("mu", [2.0, 4.0])
+def test_backward_fast_decay(mu):
+    """Strong decays on the tensor-core path: at mu = 4 every 32-token block decays by more
+    than 100 bits, so the diagonal blocks of the tile kernel take their exact per-key decay;
+    at mu = 2 most blocks take the factorised one and some do not."""
+    cfg = inputs.PrefillConfig("bwfast", 1, 2, 512, 128, 64, 64, "bf16", log_a_mu=mu)
+    inp, g, got = _run(cfg, seed=21, chunk=64)
+    ref = oracle.backward(inp.q, inp.k, inp.v, inp.log_a, inp.lam, g)
+    for name, a, r in zip(["dq", "dk", "dv", "dlog_a", "dlambda"], got, ref):
+        if name == "dlog_a":
+            a, r = a[..., None], r[..., None]
+        err = rel_err_per_head(a, r)
+        assert err <= 2e-2, (name, err)
+
+
 def test_backward_chunk_invariance():
     cfg = inputs.PrefillConfig("bwc", 1, 2, 512, 32, 32, 16, "f32")
     outs = [_run(cfg, seed=3, chunk=c)[2] for c in (16, 32, 64)]
