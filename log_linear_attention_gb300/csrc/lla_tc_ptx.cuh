@@ -129,12 +129,12 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, i
                  : "memory");
 }
 
-// Pull a contiguous range (16-byte aligned, size % 16 == 0) into L2.
 // Pull the line holding `p` into this SM's L1 (a hint; no fault on any address).
 __device__ __forceinline__ void prefetch_l1(const void* p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
+// Pull a contiguous range (16-byte aligned, size % 16 == 0) into L2.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
