@@ -470,9 +470,9 @@ struct TileCfg {
     static constexpr int kDO = 5 * kPanelBytes;      // dO tile [t][e], 1 panel
     static constexpr int kA = 6 * kPanelBytes;       // A [t][s] bf16, 2 panels; then dQ out
     static constexpr int kG = 8 * kPanelBytes;       // G [t][s] bf16, 2 panels; then r_p o dO; then dK out
-    static constexpr int kC = 10 * kPanelBytes;      // C_i [d][e] (copied with the inputs); then a node slot
-    static constexpr int kN = 11 * kPanelBytes;      // w o V [s][e]; then a node slot (B_p [d][e]); then dV out
-    static constexpr int kR = kG + kPanelBytes;      // r_p o dO [t][e]: G's second panel once G is consumed
+    static constexpr int kC = 10 * kPanelBytes;      // C_i [d][e] (copied with the inputs); then node slot 0
+    static constexpr int kN = 11 * kPanelBytes;      // w o V [s][e]; then node slot 1 (B_p [d][e]); then dV out
+    static constexpr int kR = kG + kPanelBytes;      // G's second panel; G's two hold a level pair's r_p o dO
     static constexpr int kBytes = 12 * kPanelBytes + 1024;
     static constexpr uint32_t kTxIn = 7 * kPanelBytes;
     // TMEM columns: S and dP until the A/G epilogue; dK and Z from the key side's MMAs, which
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(256, 1)
     __shared__ float dlamp[kTile][16];
     __shared__ float colE[kTile], dcs[kTile], zsh[kTile], wts[kTile];
     __shared__ __align__(16) float colw_sh[kTile];
-    __shared__ float zpart[2][kTile];  // a level round's q_t^T B_p dO_t, per column half
+    __shared__ float zpart[2][2][kTile];  // a level pair's q_t^T B_p dO_t, per round and column half
     __shared__ __align__(16) float dtab_sh[16];
     __shared__ int fail_sh, next_sh;
 
@@ -612,12 +612,12 @@ __global__ void __launch_bounds__(256, 1)
         for (int k = 0; k < r; k++) b &= b - 1;
         return __ffs(b) - 1;
     };
-    // thread 0: round r's node into slot r & 1 (N or C: both free once the key side's MMAs
-    // are done)
+    // thread 0: round r's node into slot r & 1 (C or N, adjacent panels, so a level pair's two
+    // nodes form one 128-column operand; both are free once the key side's MMAs are done)
     auto issue_node = [&](int r) {
         const int sl = r & 1;
         mbar_expect_tx(&bar_node[sl], kPanelBytes);
-        tma_load_2d(smem + (sl ? C::kC : C::kN), &tm_nodes, &bar_node[sl], 0, node_row(round_level(r)));
+        tma_load_2d(smem + (sl ? C::kN : C::kC), &tm_nodes, &bar_node[sl], 0, node_row(round_level(r)));
         if (sl) node_issued1++; else node_issued0++;
     };
     // the previous item's tensor stores have read A, G and N before this item writes there
@@ -934,16 +934,18 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc_fence_before();
     ok = __syncthreads_and(ok && ok_wait(&bar_m1, par) && !k_bad);
-    // ---- query side: one round per set bit p of j, lowest first. Round r's node is in slot
-    // r & 1: the copies for rounds 0 and 1 went out with the MMAs above, round r + 2's goes
-    // out when round r is done. The next round's r o dO is scaled while this round's Y is
-    // read back, and the row sums go through zpart: one block barrier per round.
+    // ---- query side: one round per set bit p of j, lowest first, in pairs. Rounds 2k and
+    // 2k + 1 read their nodes from slots C and N and their r o dO from G's two panels: one
+    // N = 128 chain gives both Y_p = Q B_p, one K = 128 chain adds both (r_p o dO) B_p^T to
+    // dQ. The first pair's copies went out with the MMAs above, the next pair's go out when a
+    // pair is done; its r o dO is scaled while this pair's Y is read back, and the row sums go
+    // through zpart: one block barrier per pair.
     {
         const float cl2_t = cl2_sh[t];
-        // r o dO, row t, this half's 32 columns (chunks 4 half .. 4 half + 3)
-        auto scale_rdo = [&](float rr) {
+        // r o dO, row t, this half's 32 columns (chunks 4 half .. 4 half + 3), into panel dst
+        auto scale_rdo = [&](int dst_off, float rr) {
             const uint8_t* src = smem + C::kDO;
-            uint8_t* dst = smem + C::kR;
+            uint8_t* dst = smem + dst_off;
 #pragma unroll
             for (int q = 0; q < 4; q++) {
                 const uint32_t off = sw128_off(t, 4 * half + q);
@@ -954,38 +956,73 @@ __global__ void __launch_bounds__(256, 1)
                                pack_bf16(a2.x * rr, a2.y * rr), pack_bf16(a3.x * rr, a3.y * rr));
             }
         };
-        float rho = 0.f, rr = 0.f;
-        int p = 0;
+        // round r's level, its decay rho and weight rr = lambda_t^(8+p) rho for row t
+        auto weights = [&](int r, int& pp, float& rho_, float& rr_) {
+            pp = round_level(r);
+            rho_ = exp2f(cl2_t + dtab_sh[pp]);
+            rr_ = lam_sh[t * L + 8 + pp] * rho_;
+        };
+        // this half's share of Y[t, col ..] . dO_t (32 columns)
+        auto y_dot_do = [&](const uint32_t (&y0)[16], const uint32_t (&y1)[16]) {
+            const uint8_t* src = smem + C::kDO;
+            float z = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t* yv = q < 2 ? y0 + 8 * q : y1 + 8 * (q - 2);
+                const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
+                const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z),
+                             a3 = unpack_bf16(x.w);
+                z = fmaf(__uint_as_float(yv[0]), a0.x, z); z = fmaf(__uint_as_float(yv[1]), a0.y, z);
+                z = fmaf(__uint_as_float(yv[2]), a1.x, z); z = fmaf(__uint_as_float(yv[3]), a1.y, z);
+                z = fmaf(__uint_as_float(yv[4]), a2.x, z); z = fmaf(__uint_as_float(yv[5]), a2.y, z);
+                z = fmaf(__uint_as_float(yv[6]), a3.x, z); z = fmaf(__uint_as_float(yv[7]), a3.y, z);
+            }
+            return z;
+        };
+        float rho_a = 0.f, rr_a = 0.f, rho_b = 0.f, rr_b = 0.f;
+        int p_a = 0, p_b = 0;
         if (nrounds > 0 && ok) {
-            p = round_level(0);
-            rho = exp2f(cl2_t + dtab_sh[p]);
-            rr = lam_sh[t * L + 8 + p] * rho;
-            scale_rdo(rr);
+            weights(0, p_a, rho_a, rr_a);
+            scale_rdo(C::kG, rr_a);
+            if (nrounds > 1) {
+                weights(1, p_b, rho_b, rr_b);
+                scale_rdo(C::kR, rr_b);
+            }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        for (int r = 0; r < nrounds && ok; r++) {
-            const int sl = r & 1;
+        for (int r = 0; r < nrounds && ok; r += 2) {
+            const bool two = r + 1 < nrounds;
             if (tid == 0) {
                 tc_fence_after();
-                if (mbar_wait(&bar_node[sl], (sl ? node_waited1 : node_waited0) & 1)) {
-                    if (sl) node_waited1++; else node_waited0++;
+                bool got = mbar_wait(&bar_node[0], node_waited0 & 1);
+                if (got) node_waited0++;
+                if (got && two) {
+                    got = mbar_wait(&bar_node[1], node_waited1 & 1);
+                    if (got) node_waited1++;
+                }
+                if (got) {
                     tc_fence_after();
-                    const uint32_t qb = smem_u32(smem + C::kQ), rb = smem_u32(smem + C::kR);
-                    const uint32_t nb = smem_u32(smem + (sl ? C::kC : C::kN));
-                    constexpr uint32_t kIdY = idesc_bf16(kTile, kDV, 0, 1);
+                    const uint32_t qb = smem_u32(smem + C::kQ), gb = smem_u32(smem + C::kG);
+                    const uint32_t cb = smem_u32(smem + C::kC);
+                    const uint32_t idy = two ? idesc_bf16(kTile, 2 * kDV, 0, 1) : idesc_bf16(kTile, kDV, 0, 1);
                     constexpr uint32_t kIdX = idesc_bf16(kTile, kDk, 0, 0);
 #pragma unroll
                     for (int kk = 0; kk < kDk / 16; kk++) {
                         const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                        mma_bf16(tmem + C::kY, sdesc(qb + off, 16, 1024), sdesc(nb + kk * 2048, kPanelBytes, 1024),
-                                 kIdY, kk > 0 ? 1u : 0u);
+                        mma_bf16(tmem + C::kY, sdesc(qb + off, 16, 1024), sdesc(cb + kk * 2048, kPanelBytes, 1024),
+                                 idy, kk > 0 ? 1u : 0u);
                     }
+                    // K = 64 per round: rows of r o dO (panel G or R) against the node's rows (C or N)
+                    const int nk = two ? 2 * kDV / 16 : kDV / 16;
 #pragma unroll
-                    for (int kk = 0; kk < kDV / 16; kk++)
-                        mma_bf16(tmem + C::kDQ, sdesc(rb + kk * 32, 16, 1024), sdesc(nb + kk * 32, 16, 1024), kIdX,
-                                 1u);
+                    for (int kk = 0; kk < 2 * kDV / 16; kk++) {
+                        if (kk < nk) {
+                            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                            mma_bf16(tmem + C::kDQ, sdesc(gb + off, 16, 1024), sdesc(cb + off, 16, 1024), kIdX, 1u);
+                        }
+                    }
                     mma_commit(&bar_lv);
                 } else if (atomicExch(&fail_sh, 1) == 0) {
                     record_error(err, kDevTimeout);
@@ -993,47 +1030,57 @@ __global__ void __launch_bounds__(256, 1)
             }
             ok = __syncthreads_and(ok_wait(&bar_lv, li & 1));
             tc_fence_after();
-            float rho_n = 0.f, rr_n = 0.f;
-            int p_n = 0;
+            float rho_na = 0.f, rr_na = 0.f, rho_nb = 0.f, rr_nb = 0.f;
+            int p_na = 0, p_nb = 0;
             if (ok) {
-                if (tid == 0 && r + 2 < nrounds) issue_node(r + 2);
-                uint32_t y0[16], y1[16];
-                tmem_ld16_issue(tmem + lane_base + C::kY + 32 * half, y0);
-                tmem_ld16_issue(tmem + lane_base + C::kY + 32 * half + 16, y1);
-                if (r + 1 < nrounds) {
-                    p_n = round_level(r + 1);
-                    rho_n = exp2f(cl2_t + dtab_sh[p_n]);
-                    rr_n = lam_sh[t * L + 8 + p_n] * rho_n;
-                    scale_rdo(rr_n);
+                if (tid == 0) {
+                    if (r + 2 < nrounds) issue_node(r + 2);
+                    if (r + 3 < nrounds) issue_node(r + 3);
                 }
-                tmem_ld16_wait(y0);
-                tmem_ld16_wait(y1);
-                const uint8_t* src = smem + C::kDO;
-                float z = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const uint32_t* yv = q < 2 ? y0 + 8 * q : y1 + 8 * (q - 2);
-                    const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
-                    const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z),
-                                 a3 = unpack_bf16(x.w);
-                    z = fmaf(__uint_as_float(yv[0]), a0.x, z); z = fmaf(__uint_as_float(yv[1]), a0.y, z);
-                    z = fmaf(__uint_as_float(yv[2]), a1.x, z); z = fmaf(__uint_as_float(yv[3]), a1.y, z);
-                    z = fmaf(__uint_as_float(yv[4]), a2.x, z); z = fmaf(__uint_as_float(yv[5]), a2.y, z);
-                    z = fmaf(__uint_as_float(yv[6]), a3.x, z); z = fmaf(__uint_as_float(yv[7]), a3.y, z);
+                uint32_t ya0[16], ya1[16], yb0[16], yb1[16];
+                tmem_ld16_issue(tmem + lane_base + C::kY + 32 * half, ya0);
+                tmem_ld16_issue(tmem + lane_base + C::kY + 32 * half + 16, ya1);
+                if (two) {
+                    tmem_ld16_issue(tmem + lane_base + C::kY + kDV + 32 * half, yb0);
+                    tmem_ld16_issue(tmem + lane_base + C::kY + kDV + 32 * half + 16, yb1);
                 }
-                zpart[half][t] = z;
+                if (r + 2 < nrounds) {
+                    weights(r + 2, p_na, rho_na, rr_na);
+                    scale_rdo(C::kG, rr_na);
+                    if (r + 3 < nrounds) {
+                        weights(r + 3, p_nb, rho_nb, rr_nb);
+                        scale_rdo(C::kR, rr_nb);
+                    }
+                }
+                tmem_ld16_wait(ya0);
+                tmem_ld16_wait(ya1);
+                zpart[0][half][t] = y_dot_do(ya0, ya1);
+                if (two) {
+                    tmem_ld16_wait(yb0);
+                    tmem_ld16_wait(yb1);
+                    zpart[1][half][t] = y_dot_do(yb0, yb1);
+                }
             }
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
             if (ok && half == 0) {
-                const float zt = zpart[0][t] + zpart[1][t];
-                dlamp[t][p] = rho * zt;
-                dcs[t] += rr * zt;
+                const float za = zpart[0][0][t] + zpart[0][1][t];
+                dlamp[t][p_a] = rho_a * za;
+                float d = rr_a * za;
+                if (two) {
+                    const float zb = zpart[1][0][t] + zpart[1][1][t];
+                    dlamp[t][p_b] = rho_b * zb;
+                    d += rr_b * zb;
+                }
+                dcs[t] += d;
             }
-            rho = rho_n;
-            rr = rr_n;
-            p = p_n;
+            rho_a = rho_na;
+            rr_a = rr_na;
+            p_a = p_na;
+            rho_b = rho_nb;
+            rr_b = rr_nb;
+            p_b = p_nb;
             li++;
         }
     }
