@@ -23,14 +23,14 @@
 //                        nodes of exp(decay from tile i's end to the node's
 //                        end) dB (bf16, an MMA operand of the next kernel).
 //   tc_bwd_tile        : persistent, one CTA per SM and one (head, tile) item at
-//                        a time: S = Q K^T and dP = dO V^T (TMEM);
+//                        a time: S = Q K^T and dP = dO V^T (TMEM), and beside
+//                        the epilogue the key side, dK = (w o V) C_i^T and
+//                        Z = K C_i (for dcum and dV's term diag(w) Z);
 //                        A = lambda D S and G = lambda D dP (bf16, smem) with
 //                        dlambda levels 0..7 and the decay derivatives; then
-//                        dV = A^T dO, dQ = G K, dK = G^T Q; per set bit p,
-//                        Y_p = Q B_p (for dlambda_t^(8+p) and dcum) and
-//                        dQ += (r_p o dO) B_p^T; per key tile (issued before
-//                        the levels), dK += (w o V) C_i^T and Z = K C_i (for
-//                        dcum and dV += diag(w) Z); dQ, dK, dV leave by TMA
+//                        dV = A^T dO, dQ = G K, dK += G^T Q; per set bit p (two
+//                        at a time), Y_p = Q B_p (for dlambda_t^(8+p) and dcum)
+//                        and dQ += (r_p o dO) B_p^T; dQ, dK, dV leave by TMA
 //                        stores while the next item's inputs are copied in.
 //   bwd_dloga          : dlog_a_r = sum_{t >= r} dcum_t.
 // Every mbarrier wait is bounded; on overrun a kernel records LLA_ERR_TIMEOUT,
