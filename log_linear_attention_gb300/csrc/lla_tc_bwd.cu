@@ -883,7 +883,7 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- dV = A^T dO, dQ = G K, dK = G^T Q
+    // ---- dV = A^T dO, dQ = G K, dK += G^T Q (onto the key side's term)
     if (tid == 0 && ok) {
         tc_fence_after();
         const uint32_t ab = smem_u32(smem + C::kA), gb = smem_u32(smem + C::kG);
