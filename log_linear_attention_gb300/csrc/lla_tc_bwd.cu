@@ -482,23 +482,6 @@ struct TileCfg {
     static constexpr uint32_t kTmemCols = 512;
 };
 
-// Reduce-scatter of 16 values per lane over each half-warp: lane l ends with the sum of
-// v[l & 15] over the 16 lanes that share bit 4 of l (15 shuffles).
-__device__ __forceinline__ float warp_colsum16(float (&v)[16]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < off; i++) {
-            const float send = upper ? v[i] : v[i + off];
-            const float keep = upper ? v[i + off] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-    }
-    return v[0];
-}
-
 // Persistent, one CTA per SM; 256 threads: thread (quad = warp % 4, lane) owns row
 // t = 32 quad + lane (= TMEM lane), half = warp / 4 picks half of the columns. Thread 0
 // issues the TMA copies and the MMAs between block-wide phases. A CTA takes its first
@@ -558,6 +541,24 @@ __global__ void __launch_bounds__(256, 1)
         if (warp_wait(bar, parity)) return true;
         if (lane == 0 && atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
         return false;
+    };
+    // row t of the 32 TMEM columns col + 32 half .. of this thread's lanes against the same
+    // columns of V's row t (this half's share of the dot product)
+    auto tmem_row_dot_v = [&](uint32_t col) -> float {
+        float zv[32];
+        tmem_ld32(tmem + lane_base + col + 32 * half, zv);
+        const uint8_t* src = smem + C::kV;
+        float y = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
+            const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
+            y = fmaf(zv[8 * q], a0.x, y); y = fmaf(zv[8 * q + 1], a0.y, y);
+            y = fmaf(zv[8 * q + 2], a1.x, y); y = fmaf(zv[8 * q + 3], a1.y, y);
+            y = fmaf(zv[8 * q + 4], a2.x, y); y = fmaf(zv[8 * q + 5], a2.y, y);
+            y = fmaf(zv[8 * q + 6], a3.x, y); y = fmaf(zv[8 * q + 7], a3.y, y);
+        }
+        return y;
     };
     // thread 0: item it's inputs, C_i, and the per-row scalars: lambda rows (one contiguous
     // block of 128 L floats), the in-tile log2 decay prefix and the tile's level decay row
@@ -690,9 +691,23 @@ __global__ void __launch_bounds__(256, 1)
         claimed = static_cast<int>(gridDim.x) + atomicAdd(item_counter, 1);
     }
 
-    // ---- E1: A, G (bf16), dlambda levels 0..7, decay derivatives. The two warps of a lane
-    // quadrant take alternate 16-key halves of every 32-key block, so the masked diagonal
-    // block of the quadrant is shared evenly between them.
+    // ---- E1: A, G (bf16), dlambda levels 0..7, the decay derivatives' row sums. The two
+    // warps of a lane quadrant take alternate 16-key halves of every 32-key block, so the
+    // masked diagonal block of the quadrant is shared evenly between them. The decay
+    // derivative of pair (t, s) is E = A (o) dP: its row sums (here) and column sums (from
+    // dV's accumulator, below) both take A as rounded to bf16 for the MMAs, so that the pairs
+    // the suffix sums of dlog_a cancel cancel exactly.
+    // row t's sum over this half's 16 keys of A[t][s] dP[t][s], A as packed in pa
+    auto rowsum_a = [&](const uint32_t (&pa)[8], const float (&dpv)[16]) {
+        float r = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            const float2 a = unpack_bf16(pa[e]);
+            r = fmaf(a.x, dpv[2 * e], r);
+            r = fmaf(a.y, dpv[2 * e + 1], r);
+        }
+        return r;
+    };
     if (ok) {
         const float cl2_t = cl2_sh[t];
         float dl[8];
@@ -703,7 +718,6 @@ __global__ void __launch_bounds__(256, 1)
         for (int c = 0; c < 4; c++) {
             const int cb32 = 32 * c;             // the 32-key block
             const int cb = cb32 + 16 * half;     // this warp's 16 keys of it
-            float ev[16];
             uint32_t pa[8], pg[8];
             const bool zero = cb32 > quad * 32;  // every key after every row of this warp
             if (zero) {
@@ -727,12 +741,10 @@ __global__ void __launch_bounds__(256, 1)
                     const float s0 = D0 * sv[e], s1 = D1 * sv[e + 1];
                     const float q0 = s0 * dpv[e], q1 = s1 * dpv[e + 1];
                     dsum += q0 + q1;
-                    ev[e] = lm * q0;
-                    ev[e + 1] = lm * q1;
                     pa[e >> 1] = pack_bf16(lm * s0, lm * s1);
                     pg[e >> 1] = pack_bf16(lm * D0 * dpv[e], lm * D1 * dpv[e + 1]);
                 }
-                rowE += lm * dsum;
+                rowE += rowsum_a(pa, dpv);
 #pragma unroll
                 for (int ll = 0; ll < 8; ll++) dl[ll] += (l == ll) ? dsum : 0.f;
             } else if (cl2_sh[cb32] - cl2_sh[cb32 + 31] < 100.f) {
@@ -822,10 +834,7 @@ __global__ void __launch_bounds__(256, 1)
                 dl[3] += same ? l3 : 0.f;
                 dl[4] += same ? l4 : 0.f;
                 dl[5] += same ? 0.f : tot;
-                rowE += same ? w[0] * l0 + w[1] * l1 + w[2] * l2 + w[3] * l3 + w[4] * l4 : w[5] * tot;
-                // column sums over the rows, below
-#pragma unroll
-                for (int k = 0; k < 16; k++) ev[k] = lmk[k] * x[k];
+                rowE += rowsum_a(pa, dpv);
             } else {
                 // the diagonal 32-key block with a decay over 2^100 across it: one exp2 per key
                 float sv[16], dpv[16];
@@ -850,14 +859,13 @@ __global__ void __launch_bounds__(256, 1)
                         const float dq_ = ds * dpv[e + h];
 #pragma unroll
                         for (int ll = 0; ll < 6; ll++) dl[ll] += (l == ll) ? dq_ : 0.f;
-                        ev[e + h] = lm * dq_;
                         av[h] = lm * ds;
                         gv[h] = lm * D * dpv[e + h];
                     }
                     pa[e >> 1] = pack_bf16(av[0], av[1]);
                     pg[e >> 1] = pack_bf16(gv[0], gv[1]);
-                    rowE += ev[e] + ev[e + 1];
                 }
+                rowE += rowsum_a(pa, dpv);
             }
             uint8_t* pA = smem + C::kA + (cb >> 6) * kPanelBytes;
             uint8_t* pG = smem + C::kG + (cb >> 6) * kPanelBytes;
@@ -868,10 +876,6 @@ __global__ void __launch_bounds__(256, 1)
                     make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
                 *reinterpret_cast<uint4*>(pG + sw128_off(t, ch0 + q)) =
                     make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
-            }
-            if (!zero) {  // warp-uniform
-                const float cs = warp_colsum16(ev);  // key cb + (lane & 15), this lane's half-warp of rows
-                atomicAdd(&colE[cb + (lane & 15)], cs);
             }
         }
 #pragma unroll
@@ -915,25 +919,16 @@ __global__ void __launch_bounds__(256, 1)
     // Z's row sums with V (for dcum) while the MMAs above run
     if (ok && ok_wait(&bar_k, par)) {
         tc_fence_after();
-        float zv[32];
-        tmem_ld32(tmem + lane_base + C::kZ + 32 * half, zv);
-        const uint8_t* src = smem + C::kV;
-        float y = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const uint4 x = *reinterpret_cast<const uint4*>(src + sw128_off(t, 4 * half + q));
-            const float2 a0 = unpack_bf16(x.x), a1 = unpack_bf16(x.y), a2 = unpack_bf16(x.z), a3 = unpack_bf16(x.w);
-            y = fmaf(zv[8 * q], a0.x, y); y = fmaf(zv[8 * q + 1], a0.y, y);
-            y = fmaf(zv[8 * q + 2], a1.x, y); y = fmaf(zv[8 * q + 3], a1.y, y);
-            y = fmaf(zv[8 * q + 4], a2.x, y); y = fmaf(zv[8 * q + 5], a2.y, y);
-            y = fmaf(zv[8 * q + 6], a3.x, y); y = fmaf(zv[8 * q + 7], a3.y, y);
-        }
-        atomicAdd(&zsh[t], y);
+        atomicAdd(&zsh[t], tmem_row_dot_v(C::kZ));
     } else {
         k_bad = true;
     }
     tc_fence_before();
     ok = __syncthreads_and(ok && ok_wait(&bar_m1, par) && !k_bad);
+    tc_fence_after();
+    // the column sums of E: for key s, sum_t A[t][s] (dO_t . V_s) = (A^T dO)[s,:] . V_s, dV's
+    // accumulator (before the key side's term, added when dV is staged) against V
+    if (ok) atomicAdd(&colE[t], tmem_row_dot_v(C::kDVc));
     // ---- query side: one round per set bit p of j, lowest first, in pairs. Rounds 2k and
     // 2k + 1 read their nodes from slots C and N and their r o dO from G's two panels: one
     // N = 128 chain gives both Y_p = Q B_p, one K = 128 chain adds both (r_p o dO) B_p^T to
