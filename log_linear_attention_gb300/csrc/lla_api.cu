@@ -35,7 +35,7 @@ int* error_word(int dev) {
 }
 
 // Library-private stream-ordered pool: freed workspace stays reserved for the
-// next call instead of going back to the driver.
+// next call instead of going back to the CUDA driver.
 cudaMemPool_t workspace_pool(int dev) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!g_pool_ready[dev]) {
