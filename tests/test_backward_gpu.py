@@ -59,6 +59,7 @@ def _run(cfg, seed, chunk):
     (2, 2, 512, 128, 64, 64, "bf16"),
     (2, 1, 1024, 128, 64, 128, "bf16"),
     (1, 1, 2304, 128, 64, 64, "bf16"),    # 18 tiles
+    (1, 9, 2176, 128, 64, 64, "bf16"),    # 153 (head, tile) items: one more than a GB300 has SMs
 ])
 def test_backward_matches_oracle(B, H, T, dk, dv, chunk, dtype):
     cfg = inputs.PrefillConfig("bw", B, H, T, dk, dv, chunk, dtype)
