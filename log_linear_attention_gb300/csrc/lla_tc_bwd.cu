@@ -77,10 +77,11 @@ struct DnodeTile {
     uint32_t bits, start, end, start_cut, end_cut;
 };
 
-__device__ __forceinline__ DnodeTile dnode_tile(int f, int NT, int p_lo, int np, int t0, int t1) {
+// Tile f of the flattened (head, tile) list is tile j of head bh (the callers step both along f).
+__device__ __forceinline__ DnodeTile dnode_tile(int f, int bh, int j, int NT, int p_lo, int np, int t0, int t1) {
     DnodeTile d;
-    d.bh = f / NT;
-    d.j = f - d.bh * NT;
+    d.bh = bh;
+    d.j = j;
     d.bits = (static_cast<uint32_t>(d.j) >> p_lo) & ((1u << np) - 1u);
     d.start = d.end = d.start_cut = d.end_cut = 0;
 #pragma unroll
@@ -148,18 +149,25 @@ __global__ void __launch_bounds__(384, 1)
     auto fail_now = [&]() {
         if (atomicExch(&fail_sh, 1) == 0) record_error(err, kDevTimeout);
     };
-    auto level_bits = [&](int f) {
-        const int j = f % NT;
-        return (static_cast<uint32_t>(j) >> p_lo) & ((1u << np) - 1u);
+    // the window's level bits of tile j of a head; the loops below step (head, j) along the
+    // flattened tile index f instead of dividing it
+    auto lbits = [&](int j) { return (static_cast<uint32_t>(j) >> p_lo) & ((1u << np) - 1u); };
+    auto step = [&](int& j, int& bh) {
+        if (++j == NT) {
+            j = 0;
+            bh++;
+        }
     };
+    const int bh0 = t0 / NT, j0 = t0 - (t0 / NT) * NT;
 
     int issued = 0;
     if (warp == 0) {
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            for (int f = t0; f < t1 && !*fail; f++) {
-                if (level_bits(f) == 0) continue;
+            int j = j0, bh = bh0;
+            for (int f = t0; f < t1 && !*fail; f++, step(j, bh)) {
+                if (lbits(j) == 0) continue;
                 if (issued >= C::kRaw && !mbar_wait(&raw_empty[s], ph ^ 1u)) {
                     fail_now();
                     break;
@@ -185,8 +193,9 @@ __global__ void __launch_bounds__(384, 1)
             constexpr uint64_t kRawStep = C::kRawBytes >> 4, kScStep = kPanelBytes >> 4;
             int rs = 0, ss = 0;
             uint32_t sph = 0, run_par = 0, used = 0;
-            for (int f = t0; f < t1 && !*fail; f++) {
-                const DnodeTile d = dnode_tile(f, NT, p_lo, np, t0, t1);
+            int j = j0, bh = bh0;
+            for (int f = t0; f < t1 && !*fail; f++, step(j, bh)) {
+                const DnodeTile d = dnode_tile(f, bh, j, NT, p_lo, np, t0, t1);
                 if (d.bits == 0) continue;
                 bool ok = true;
 #pragma unroll 1
@@ -235,8 +244,13 @@ __global__ void __launch_bounds__(384, 1)
         // factors of the next tile are fetched while the current one is scaled.
         float lam[C::kMaxLevels], dt[C::kMaxLevels], cl2 = 0.f;
         float nlam[C::kMaxLevels], ndt[C::kMaxLevels], ncl2 = 0.f;
-        auto next_tile = [&](int f) {
-            while (f < t1 && level_bits(f) == 0) f++;
+        // the first tile from f on (j: its index in its head) with level bits in the window
+        auto next_tile = [&](int f, int& j) {
+            int bh_ = 0;
+            while (f < t1 && lbits(j) == 0) {
+                f++;
+                step(j, bh_);
+            }
             return f;
         };
         // factors of tile fn (level bits nb) into nlam / ndt / ncl2
@@ -250,22 +264,25 @@ __global__ void __launch_bounds__(384, 1)
             ndt[q] = on_ ? dtab[static_cast<size_t>(fn) * 16 + p_lo + q] : 0.f;   \
         }                                                                         \
     } while (0)
-        int f = next_tile(t0);
-        if (f < t1) LLA_DNODE_FETCH(f, level_bits(f));
+        int jf = j0;
+        int f = next_tile(t0, jf);
+        if (f < t1) LLA_DNODE_FETCH(f, lbits(jf));
         int rs = 0, ss = 0;
         uint32_t rph = 0, sph = 0;
         int n_sc = 0;
         while (f < t1) {
             if (__any_sync(0xffffffffu, *fail != 0)) break;
-            const uint32_t bits = level_bits(f);
+            const uint32_t bits = lbits(jf);
             cl2 = ncl2;
 #pragma unroll
             for (int q = 0; q < C::kMaxLevels; q++) {
                 lam[q] = nlam[q];
                 dt[q] = ndt[q];
             }
-            const int fn = next_tile(f + 1);
-            if (fn < t1) LLA_DNODE_FETCH(fn, level_bits(fn));
+            int jn = jf, bh_n = 0;
+            step(jn, bh_n);
+            const int fn = next_tile(f + 1, jn);
+            if (fn < t1) LLA_DNODE_FETCH(fn, lbits(jn));
             if (!warp_wait(&raw_full[rs], rph)) {
                 if (lane == 0) fail_now();
                 break;
@@ -312,6 +329,7 @@ __global__ void __launch_bounds__(384, 1)
                 rph ^= 1u;
             }
             f = fn;
+            jf = jn;
         }
 #undef LLA_DNODE_FETCH
     } else if (warp >= 8) {
@@ -319,8 +337,9 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         uint8_t* stage = drain_stage + quad * C::kDrainBytes;
         uint32_t par = 0, cut = 0;  // cut: the slot's current run began in another CTA
-        for (int f = t0; f < t1; f++) {
-            const DnodeTile dt = dnode_tile(f, NT, p_lo, np, t0, t1);
+        int j = j0, bh = bh0;
+        for (int f = t0; f < t1; f++, step(j, bh)) {
+            const DnodeTile dt = dnode_tile(f, bh, j, NT, p_lo, np, t0, t1);
             cut = (cut & ~dt.start) | dt.start_cut;
             if (dt.end == 0) continue;
             if (__any_sync(0xffffffffu, *fail != 0)) break;
